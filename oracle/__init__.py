@@ -1,0 +1,252 @@
+"""CPU oracle for Lookahead Decoding -- TEST INFRASTRUCTURE.
+
+Only tests/, ``__graft_entry__.smoke()`` and bench.py's CPU-baseline leg may
+import this package.  It wraps ``oracle.c`` (plain fp32 C, no BLAS, built with
+``-O2 -fno-fast-math -ffp-contract=off``; OpenMP only over independent output
+elements, so results do not depend on the thread count) through ctypes.  It
+shares no code with the CUDA library.
+
+Functions and what pins them (the tests under tests/test_oracle_*.py):
+  greedy          plain greedy decoding -- pinned by an fp64 numpy/torch
+                  re-evaluation of the layer math, textbook special cases of
+                  RMSNorm/RoPE/softmax, and the library routine
+                  ``scaled_dot_product_attention``.
+  lookahead       the method -- pinned by losslessness (equal to greedy token
+                  for token, the summary's exactness claim), the step shape
+                  T = 1 + (W+G)(N-1) against the pages' 120x/80x/56x FLOPs
+                  figures, per-row equivalence of the masked forward with the
+                  plain causal forward, a brute-force LCP check of verification
+                  and a list-based replay of the pool.
+  Controller      the window/pool/verify state machine fed external argmaxes.
+  Parity unpinned: acceptance rate and the choice among the readings R1, R3,
+  R6, R7 (nothing on the pages fixes them).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SO = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (gcc, OpenMP)."""
+    src = os.path.join(_HERE, "oracle.c")
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(src):
+        tmp = _SO + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fopenmp",
+                               "-fPIC", "-shared", "-fvisibility=hidden", "-o", tmp, src, "-lm"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+class _Model(C.Structure):
+    _fields_ = [("n_layers", C.c_int), ("d_model", C.c_int), ("n_heads", C.c_int),
+                ("n_kv_heads", C.c_int), ("head_dim", C.c_int), ("ffn", C.c_int),
+                ("vocab", C.c_int), ("rms_eps", C.c_float), ("rope_theta", C.c_float),
+                ("emb", C.c_void_p), ("final_norm", C.c_void_p), ("lm_head", C.c_void_p),
+                ("attn_norm", C.c_void_p), ("wq", C.c_void_p), ("wk", C.c_void_p),
+                ("wv", C.c_void_p), ("wo", C.c_void_p), ("ffn_norm", C.c_void_p),
+                ("wg", C.c_void_p), ("wu", C.c_void_p), ("wd", C.c_void_p)]
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        L = C.CDLL(build())
+        vp, i32, u64 = C.c_void_p, C.c_int, C.c_uint64
+        sig = {
+            "om_seq_new": (vp, [vp, i32]), "om_seq_free": (None, [vp]),
+            "om_threads": (i32, []), "om_rope_table": (None, [vp, vp, vp]),
+            "om_rope": (None, [vp, vp, i32]),
+            "om_step_forward": (i32, [vp, i32, i32, vp, vp, vp, vp, vp]),
+            "om_commit": (i32, [vp, i32, i32, vp]), "om_prefill": (i32, [vp, i32, vp, i32]),
+            "om_greedy": (i32, [vp, vp, i32, i32, i32, vp, vp]),
+            "om_ctrl_new": (vp, [i32, i32, i32, i32]), "om_ctrl_free": (None, [vp]),
+            "om_splitmix64": (u64, [vp]), "om_pool_insert": (None, [vp, i32, vp]),
+            "om_ctrl_init": (i32, [vp, vp, i32, u64, i32]), "om_ctrl_rows_max": (i32, [vp]),
+            "om_ctrl_rows": (i32, [vp, i32, i32, vp, vp, vp]),
+            "om_ctrl_advance": (i32, [vp, vp, vp, vp, vp]), "om_ctrl_pool": (i32, [vp, i32, vp]),
+            "om_ctrl_window": (None, [vp, vp]),
+            "om_lookahead": (i32, [vp, vp, i32, i32, i32, i32, u64, i32, i32, i32, vp, vp, vp]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype, f.argtypes = res, args
+        _lib = L
+    return _lib
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(C.c_void_p)
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+class Model:
+    """fp32 host copy of a decoder's weights, in the oracle's struct."""
+
+    def __init__(self, cfg, weights):
+        self.cfg = cfg
+        f32 = lambda a: np.ascontiguousarray(a, dtype=np.float32)
+        self._keep = []
+
+        def arr(x):
+            x = f32(x)
+            self._keep.append(x)
+            return x.ctypes.data
+
+        def per_layer(name):
+            ptrs = (C.c_void_p * cfg.n_layers)(*[arr(w) for w in weights[name]])
+            self._keep.append(ptrs)
+            return C.cast(ptrs, C.c_void_p).value
+
+        self.s = _Model(cfg.n_layers, cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim,
+                        cfg.ffn, cfg.vocab, cfg.rms_eps, cfg.rope_theta,
+                        arr(weights["emb"]), arr(weights["final_norm"]), arr(weights["lm_head"]),
+                        *[per_layer(n) for n in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm",
+                                                 "wg", "wu", "wd")])
+
+    @property
+    def ptr(self):
+        return C.cast(C.pointer(self.s), C.c_void_p)
+
+
+class Seq:
+    """A KV cache plus the step forward of the oracle."""
+
+    def __init__(self, model: Model, max_seq: int):
+        self.model = model
+        self.max_seq = max_seq
+        self.h = lib().om_seq_new(model.ptr, max_seq)
+        if not self.h:
+            raise MemoryError("om_seq_new failed")
+
+    def __del__(self):
+        if getattr(self, "h", None):
+            lib().om_seq_free(self.h)
+            self.h = None
+
+    def prefill(self, toks, P0: int = 0):
+        t = _i32(toks)
+        if lib().om_prefill(self.h, P0, _p(t), len(t)):
+            raise ValueError("om_prefill failed")
+
+    def step(self, P: int, tok, pos, vis, want_logits: bool = True):
+        tok, pos = _i32(tok), _i32(pos)
+        T = len(tok)
+        vis = np.ascontiguousarray(np.asarray(vis, dtype=np.uint8).reshape(T, T))
+        logits = np.zeros((T, self.model.cfg.vocab), np.float32) if want_logits else None
+        amax = np.zeros(T, np.int32)
+        rc = lib().om_step_forward(self.h, P, T, _p(tok), _p(pos), _p(vis),
+                                   _p(logits) if want_logits else None, _p(amax))
+        if rc:
+            raise ValueError("om_step_forward failed")
+        return logits, amax
+
+    def commit(self, P: int, rows):
+        r = _i32(rows)
+        if lib().om_commit(self.h, P, len(r), _p(r)):
+            raise ValueError("om_commit failed")
+
+    def rope(self, v, pos: int):
+        x = np.ascontiguousarray(np.asarray(v, dtype=np.float32)).copy()
+        lib().om_rope(self.h, _p(x), pos)
+        return x
+
+    def rope_table(self):
+        half = self.model.cfg.head_dim // 2
+        c = np.zeros((self.max_seq, half), np.float32)
+        s = np.zeros((self.max_seq, half), np.float32)
+        lib().om_rope_table(self.h, _p(c), _p(s))
+        return c, s
+
+
+def greedy(model: Model, prompt, max_new: int, max_seq: int | None = None, logits: bool = False):
+    p = _i32(prompt)
+    max_seq = max_seq or (len(p) + max_new + 8)
+    out = np.zeros(max_new, np.int32)
+    lg = np.zeros((max_new, model.cfg.vocab), np.float32) if logits else None
+    if lib().om_greedy(model.ptr, _p(p), len(p), max_new, max_seq, _p(out), _p(lg) if logits else None):
+        raise ValueError("om_greedy failed")
+    return (out, lg) if logits else out
+
+
+def lookahead(model: Model, prompt, W: int, N: int, G: int, max_new: int, seed: int = 2,
+              preseed: bool = False, max_seq: int | None = None):
+    """Returns (tokens, steps, accept_hist[0..N])."""
+    p = _i32(prompt)
+    max_seq = max_seq or (len(p) + max_new + W + N + 8)
+    out = np.zeros(max_new, np.int32)
+    steps = np.zeros(1, np.int32)
+    hist = np.zeros(N + 1, np.int32)
+    rc = lib().om_lookahead(model.ptr, _p(p), len(p), W, N, G, seed, int(preseed), max_new, max_seq,
+                            _p(out), _p(steps), _p(hist))
+    if rc:
+        raise ValueError("om_lookahead failed")
+    return out, int(steps[0]), hist
+
+
+def splitmix64_stream(seed: int, n: int):
+    st = (C.c_uint64 * 1)(seed)
+    return [lib().om_splitmix64(C.cast(st, C.c_void_p)) for _ in range(n)]
+
+
+class Controller:
+    """Window / pool / verification state machine (R1-R9) fed external argmaxes."""
+
+    def __init__(self, W: int, N: int, G: int, V: int):
+        self.W, self.N, self.G, self.V = W, N, G, V
+        self.h = lib().om_ctrl_new(W, N, G, V)
+        if not self.h:
+            raise ValueError("bad controller arguments")
+        self.Tmax = lib().om_ctrl_rows_max(self.h)
+
+    def __del__(self):
+        if getattr(self, "h", None):
+            lib().om_ctrl_free(self.h)
+            self.h = None
+
+    def init(self, prompt, seed: int = 2, preseed: bool = False):
+        p = _i32(prompt)
+        lib().om_ctrl_init(self.h, _p(p), len(p), seed, int(preseed))
+
+    def insert(self, key: int, val):
+        v = _i32(val)
+        lib().om_pool_insert(self.h, key, _p(v))
+
+    def rows(self, c: int, P: int):
+        tok = np.zeros(self.Tmax, np.int32)
+        pos = np.zeros(self.Tmax, np.int32)
+        vis = np.zeros(self.Tmax * self.Tmax, np.uint8)
+        T = lib().om_ctrl_rows(self.h, c, P, _p(tok), _p(pos), _p(vis))
+        return tok[:T].copy(), pos[:T].copy(), vis[:T * T].reshape(T, T).copy()
+
+    def advance(self, amax):
+        a = _i32(amax)
+        emit = np.zeros(self.N + 1, np.int32)
+        rows = np.zeros(self.N + 1, np.int32)
+        g = (C.c_int * 1)()
+        n = lib().om_ctrl_advance(self.h, _p(a), _p(emit), _p(rows), C.cast(g, C.c_void_p))
+        return emit[:n].copy(), rows[:n].copy(), int(g[0])
+
+    def pool(self, key: int):
+        out = np.zeros(max(self.G, 1) * (self.N - 1), np.int32)
+        n = lib().om_ctrl_pool(self.h, key, _p(out))
+        return out[: n * (self.N - 1)].reshape(n, self.N - 1).copy()
+
+    def window(self):
+        out = np.zeros(max(self.W, 1) * (self.N - 1), np.int32)
+        lib().om_ctrl_window(self.h, _p(out))
+        return out[: self.W * (self.N - 1)].reshape(self.N - 1, self.W).copy()
+
+
+def threads() -> int:
+    return lib().om_threads()

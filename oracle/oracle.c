@@ -1,0 +1,592 @@
+/*
+ * oracle.c -- plain, slow, obviously-correct fp32 CPU oracle for Lookahead
+ * Decoding (Fu, Bailis, Stoica, Zhang 2024, "Break the Sequential Dependency
+ * of LLM Inference Using Lookahead Decoding").
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg load this library.  It shares no code, header, table or
+ * constant with the CUDA library: it is written from the method's definition.
+ *
+ * What it computes
+ *  - G-oracle: plain greedy decoding of a Llama-style decoder (the baseline
+ *    the summary's "Summary" paragraph says each step of which is bound by
+ *    memory bandwidth).  Its output is the definition of the right answer:
+ *    the summary states that lookahead decoding keeps the output exactly the
+ *    same.
+ *  - LA-oracle: lookahead decoding, step by step: a lookahead branch over a
+ *    2D window of W columns x (N-1) levels, an n-gram pool keyed on the first
+ *    token holding up to G (N-1)-grams per key, and a verification branch,
+ *    all evaluated in one forward pass per step under one attention mask
+ *    ("Summary" paragraph and "Key points", tuning knobs W, N, G).
+ *
+ * Readings where the pages are silent (each listed in the design notes):
+ *  R1 window init from a splitmix64 stream (Vigna's published definition);
+ *  R2 row order: row 0 = current token c at P; lookahead row (l,j) =
+ *     1 + l*W + j at P+1+j+l; verification row (g,i) = 1 + W(N-1) + g(N-1) + i
+ *     at P+1+i;
+ *  R3 mask: row 0 sees {0}; (l,j) sees {0} u {(0,j'): j'<=j} u {(l',j):
+ *     1<=l'<=l}; (g,i) sees {0} u {(g,i'): i'<=i}; every row also sees the
+ *     cache [0,P) and itself;
+ *  R5 verify: longest candidate prefix equal to the model's argmaxes, ties to
+ *     the lowest g, plus one bonus token;
+ *  R6 harvest: for j ascending, key win[0][j], value (win[1..N-2][j],
+ *     argmax of row (N-2,j)); present -> no-op, else append, evicting the
+ *     oldest when G entries are held (FIFO);
+ *  R7 window: drop level 0, shift up, new last level = argmaxes of the last
+ *     level's rows;
+ *  R8 commit KV of row 0 and of the accepted candidate rows;
+ *  R9 optional prompt pre-seed: insert (prompt[i], prompt[i+1..i+N-1]) for
+ *     i ascending ("Key points": prompt n-grams in the pool help).
+ *
+ * Model (M1-M3): h = x + Wo*Attn(RMSNorm(x)); y = h + Wd*(silu(Wg n) . Wu n),
+ * n = RMSNorm(h); RMSNorm(x) = x / sqrt(mean(x^2) + eps) * w (Zhang and
+ * Sennrich 2019, cited by the pages); rotate-half RoPE, angle
+ * pos * theta^(-2i/hd), table computed in double and rounded to float;
+ * softmax over visible keys in ascending position order; GQA head map
+ * h -> h / (H/Hkv); greedy argmax = lowest index of the maximum.
+ * All dot products accumulate in ascending index order in fp32.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define OM_EXPORT __attribute__((visibility("default")))
+
+typedef struct om_model {
+    int n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn, vocab;
+    float rms_eps, rope_theta;
+    const float* emb;        /* [vocab][d_model] */
+    const float* final_norm; /* [d_model] */
+    const float* lm_head;    /* [vocab][d_model] */
+    const float* const* attn_norm; /* per layer [d_model] */
+    const float* const* wq;        /* per layer [H*hd][d_model] */
+    const float* const* wk;        /* per layer [Hkv*hd][d_model] */
+    const float* const* wv;        /* per layer [Hkv*hd][d_model] */
+    const float* const* wo;        /* per layer [d_model][H*hd] */
+    const float* const* ffn_norm;  /* per layer [d_model] */
+    const float* const* wg;        /* per layer [ffn][d_model] */
+    const float* const* wu;        /* per layer [ffn][d_model] */
+    const float* const* wd;        /* per layer [d_model][ffn] */
+} om_model;
+
+/* ---------------------------------------------------------------- sequence */
+
+typedef struct om_seq {
+    const om_model* m;
+    int max_seq, d_kv;
+    float* kc;   /* [L][max_seq][d_kv] rotated keys */
+    float* vc;   /* [L][max_seq][d_kv] */
+    float* cosb; /* [max_seq][hd/2] */
+    float* sinb;
+    int cap_rows, last_T;
+    float* sk;   /* [L][cap_rows][d_kv] keys of the last step's rows */
+    float* sv;
+} om_seq;
+
+OM_EXPORT om_seq* om_seq_new(const om_model* m, int max_seq)
+{
+    om_seq* s = (om_seq*)calloc(1, sizeof(om_seq));
+    if (!s) return NULL;
+    s->m = m;
+    s->max_seq = max_seq;
+    s->d_kv = m->n_kv_heads * m->head_dim;
+    size_t n = (size_t)m->n_layers * max_seq * s->d_kv;
+    s->kc = (float*)calloc(n, sizeof(float));
+    s->vc = (float*)calloc(n, sizeof(float));
+    int half = m->head_dim / 2;
+    s->cosb = (float*)malloc(sizeof(float) * (size_t)max_seq * half);
+    s->sinb = (float*)malloc(sizeof(float) * (size_t)max_seq * half);
+    if (!s->kc || !s->vc || !s->cosb || !s->sinb) return NULL;
+    for (int p = 0; p < max_seq; p++)
+        for (int i = 0; i < half; i++) {
+            double ang = (double)p * pow((double)m->rope_theta, -2.0 * i / (double)m->head_dim);
+            s->cosb[(size_t)p * half + i] = (float)cos(ang);
+            s->sinb[(size_t)p * half + i] = (float)sin(ang);
+        }
+    return s;
+}
+
+OM_EXPORT void om_seq_free(om_seq* s)
+{
+    if (!s) return;
+    free(s->kc); free(s->vc); free(s->cosb); free(s->sinb); free(s->sk); free(s->sv);
+    free(s);
+}
+
+OM_EXPORT int om_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+OM_EXPORT void om_rope_table(const om_seq* s, float* cos_out, float* sin_out)
+{
+    size_t n = (size_t)s->max_seq * (s->m->head_dim / 2);
+    memcpy(cos_out, s->cosb, n * sizeof(float));
+    memcpy(sin_out, s->sinb, n * sizeof(float));
+}
+
+static float dot(const float* a, const float* b, int n)
+{
+    float acc = 0.0f;
+    for (int i = 0; i < n; i++) acc += a[i] * b[i];
+    return acc;
+}
+
+static void rmsnorm(const float* x, const float* w, int d, float eps, float* out)
+{
+    float ss = 0.0f;
+    for (int i = 0; i < d; i++) ss += x[i] * x[i];
+    float r = 1.0f / sqrtf(ss / (float)d + eps);
+    for (int i = 0; i < d; i++) out[i] = x[i] * r * w[i];
+}
+
+/* rotate-half RoPE of one head vector at position pos */
+static void rope(float* v, int hd, const float* cosb, const float* sinb, int pos)
+{
+    int half = hd / 2;
+    for (int i = 0; i < half; i++) {
+        float c = cosb[(size_t)pos * half + i], s = sinb[(size_t)pos * half + i];
+        float x1 = v[i], x2 = v[i + half];
+        v[i] = x1 * c - x2 * s;
+        v[i + half] = x2 * c + x1 * s;
+    }
+}
+
+/* rotate one head vector in place with the sequence's table (exported so the
+ * tests can check the rotation's relative-position property directly) */
+OM_EXPORT void om_rope(const om_seq* s, float* v, int pos)
+{
+    rope(v, s->m->head_dim, s->cosb, s->sinb, pos);
+}
+
+static float silu(float z) { return z / (1.0f + expf(-z)); }
+
+static int argmax_row(const float* x, int n)
+{
+    int best = 0;
+    for (int i = 1; i < n; i++)
+        if (x[i] > x[best]) best = i;
+    return best;
+}
+
+/*
+ * One forward pass over T rows (tokens tok[r] at positions pos[r]).  Row r
+ * attends to the cache [0,P) and to every in-step row s with
+ * vis[r*T+s] != 0, in ascending position order.  The step rows' keys and
+ * values are kept for om_commit.  logits (T x V) and argmax (T) may be NULL.
+ * Returns 0, or -1 on bad arguments / allocation failure.
+ */
+OM_EXPORT int om_step_forward(om_seq* s, int P, int T, const int* tok, const int* pos,
+                              const unsigned char* vis, float* logits, int* amax)
+{
+    const om_model* m = s->m;
+    const int L = m->n_layers, d = m->d_model, H = m->n_heads, Hkv = m->n_kv_heads;
+    const int hd = m->head_dim, F = m->ffn, V = m->vocab, dq = H * hd, dkv = s->d_kv;
+    const int grp = H / Hkv;
+    if (T <= 0 || P < 0) return -1;
+    for (int r = 0; r < T; r++)
+        if (pos[r] < 0 || pos[r] >= s->max_seq || tok[r] < 0 || tok[r] >= V) return -1;
+    if (T > s->cap_rows) {
+        free(s->sk); free(s->sv);
+        s->sk = (float*)malloc(sizeof(float) * (size_t)L * T * dkv);
+        s->sv = (float*)malloc(sizeof(float) * (size_t)L * T * dkv);
+        if (!s->sk || !s->sv) return -1;
+        s->cap_rows = T;
+    }
+    s->last_T = T;
+    float* x = (float*)malloc(sizeof(float) * (size_t)T * d);
+    float* xn = (float*)malloc(sizeof(float) * (size_t)T * d);
+    float* q = (float*)malloc(sizeof(float) * (size_t)T * dq);
+    float* att = (float*)malloc(sizeof(float) * (size_t)T * dq);
+    float* act = (float*)malloc(sizeof(float) * (size_t)T * F);
+    int* order = (int*)malloc(sizeof(int) * (size_t)T * T);
+    int* nvis = (int*)malloc(sizeof(int) * T);
+    if (!x || !xn || !q || !att || !act || !order || !nvis) return -1;
+
+    /* visible in-step rows of each row, sorted by (position, index) */
+    for (int r = 0; r < T; r++) {
+        int n = 0;
+        for (int c = 0; c < T; c++) {
+            if (!vis[(size_t)r * T + c]) continue;
+            int k = n++;
+            while (k > 0 && pos[order[(size_t)r * T + k - 1]] > pos[c]) {
+                order[(size_t)r * T + k] = order[(size_t)r * T + k - 1];
+                k--;
+            }
+            order[(size_t)r * T + k] = c;
+        }
+        nvis[r] = n;
+    }
+
+    for (int r = 0; r < T; r++)
+        memcpy(x + (size_t)r * d, m->emb + (size_t)tok[r] * d, sizeof(float) * d);
+
+    const float scale_div = sqrtf((float)hd);
+    for (int l = 0; l < L; l++) {
+        float* skl = s->sk + (size_t)l * s->cap_rows * dkv;
+        float* svl = s->sv + (size_t)l * s->cap_rows * dkv;
+        const float* kcl = s->kc + (size_t)l * s->max_seq * dkv;
+        const float* vcl = s->vc + (size_t)l * s->max_seq * dkv;
+
+        for (int r = 0; r < T; r++)
+            rmsnorm(x + (size_t)r * d, m->attn_norm[l], d, m->rms_eps, xn + (size_t)r * d);
+        #pragma omp parallel for collapse(2) schedule(static)
+        for (int r = 0; r < T; r++)
+            for (int o = 0; o < dq + 2 * dkv; o++) {
+                const float* xr = xn + (size_t)r * d;
+                if (o < dq) q[(size_t)r * dq + o] = dot(m->wq[l] + (size_t)o * d, xr, d);
+                else if (o < dq + dkv) skl[(size_t)r * dkv + (o - dq)] = dot(m->wk[l] + (size_t)(o - dq) * d, xr, d);
+                else svl[(size_t)r * dkv + (o - dq - dkv)] = dot(m->wv[l] + (size_t)(o - dq - dkv) * d, xr, d);
+            }
+        for (int r = 0; r < T; r++) {
+            for (int h = 0; h < H; h++) rope(q + (size_t)r * dq + h * hd, hd, s->cosb, s->sinb, pos[r]);
+            for (int h = 0; h < Hkv; h++) rope(skl + (size_t)r * dkv + h * hd, hd, s->cosb, s->sinb, pos[r]);
+        }
+
+        /* attention: row r, head h over cache [0,P) then visible step rows */
+        #pragma omp parallel for collapse(2) schedule(dynamic)
+        for (int r = 0; r < T; r++)
+            for (int h = 0; h < H; h++) {
+                int kvh = h / grp;
+                int nk = P + nvis[r];
+                float* sc = (float*)malloc(sizeof(float) * (size_t)(nk > 0 ? nk : 1));
+                const float* qh = q + (size_t)r * dq + h * hd;
+                for (int j = 0; j < P; j++)
+                    sc[j] = dot(qh, kcl + (size_t)j * dkv + kvh * hd, hd) / scale_div;
+                for (int t = 0; t < nvis[r]; t++) {
+                    int c = order[(size_t)r * T + t];
+                    sc[P + t] = dot(qh, skl + (size_t)c * dkv + kvh * hd, hd) / scale_div;
+                }
+                float mx = -INFINITY;
+                for (int j = 0; j < nk; j++) if (sc[j] > mx) mx = sc[j];
+                float sum = 0.0f;
+                for (int j = 0; j < nk; j++) { sc[j] = expf(sc[j] - mx); sum += sc[j]; }
+                float* out = att + (size_t)r * dq + h * hd;
+                for (int e = 0; e < hd; e++) {
+                    float acc = 0.0f;
+                    for (int j = 0; j < P; j++) acc += sc[j] * vcl[(size_t)j * dkv + kvh * hd + e];
+                    for (int t = 0; t < nvis[r]; t++) {
+                        int c = order[(size_t)r * T + t];
+                        acc += sc[P + t] * svl[(size_t)c * dkv + kvh * hd + e];
+                    }
+                    out[e] = acc / sum;
+                }
+                free(sc);
+            }
+
+        #pragma omp parallel for collapse(2) schedule(static)
+        for (int r = 0; r < T; r++)
+            for (int o = 0; o < d; o++)
+                x[(size_t)r * d + o] = x[(size_t)r * d + o] + dot(m->wo[l] + (size_t)o * dq, att + (size_t)r * dq, dq);
+
+        for (int r = 0; r < T; r++)
+            rmsnorm(x + (size_t)r * d, m->ffn_norm[l], d, m->rms_eps, xn + (size_t)r * d);
+        #pragma omp parallel for collapse(2) schedule(static)
+        for (int r = 0; r < T; r++)
+            for (int f = 0; f < F; f++) {
+                const float* xr = xn + (size_t)r * d;
+                float g = dot(m->wg[l] + (size_t)f * d, xr, d);
+                float u = dot(m->wu[l] + (size_t)f * d, xr, d);
+                act[(size_t)r * F + f] = silu(g) * u;
+            }
+        #pragma omp parallel for collapse(2) schedule(static)
+        for (int r = 0; r < T; r++)
+            for (int o = 0; o < d; o++)
+                x[(size_t)r * d + o] = x[(size_t)r * d + o] + dot(m->wd[l] + (size_t)o * F, act + (size_t)r * F, F);
+    }
+
+    if (logits || amax) {
+        for (int r = 0; r < T; r++)
+            rmsnorm(x + (size_t)r * d, m->final_norm, d, m->rms_eps, xn + (size_t)r * d);
+        float* lg = logits ? logits : (float*)malloc(sizeof(float) * (size_t)T * V);
+        #pragma omp parallel for collapse(2) schedule(static)
+        for (int r = 0; r < T; r++)
+            for (int v = 0; v < V; v++)
+                lg[(size_t)r * V + v] = dot(m->lm_head + (size_t)v * d, xn + (size_t)r * d, d);
+        if (amax)
+            for (int r = 0; r < T; r++) amax[r] = argmax_row(lg + (size_t)r * V, V);
+        if (!logits) free(lg);
+    }
+    free(x); free(xn); free(q); free(att); free(act); free(order); free(nvis);
+    return 0;
+}
+
+/* Copy the keys/values of the last step's rows rows[0..n-1] to cache
+ * positions P..P+n-1 of every layer. */
+OM_EXPORT int om_commit(om_seq* s, int P, int n, const int* rows)
+{
+    if (P < 0 || P + n > s->max_seq) return -1;
+    const int L = s->m->n_layers, dkv = s->d_kv;
+    for (int i = 0; i < n; i++)
+        if (rows[i] < 0 || rows[i] >= s->last_T) return -1;
+    for (int l = 0; l < L; l++)
+        for (int i = 0; i < n; i++) {
+            memcpy(s->kc + ((size_t)l * s->max_seq + P + i) * dkv, s->sk + ((size_t)l * s->cap_rows + rows[i]) * dkv,
+                   sizeof(float) * dkv);
+            memcpy(s->vc + ((size_t)l * s->max_seq + P + i) * dkv, s->sv + ((size_t)l * s->cap_rows + rows[i]) * dkv,
+                   sizeof(float) * dkv);
+        }
+    return 0;
+}
+
+/* Causal prefill of toks[0..n-1] at positions P0.. one token at a time. */
+OM_EXPORT int om_prefill(om_seq* s, int P0, const int* toks, int n)
+{
+    for (int t = 0; t < n; t++) {
+        int p = P0 + t;
+        unsigned char one = 1;
+        int row = 0;
+        if (om_step_forward(s, p, 1, toks + t, &p, &one, NULL, NULL)) return -1;
+        if (om_commit(s, p, 1, &row)) return -1;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ greedy */
+
+/* G-oracle: greedy decoding.  Prefills prompt[0..len-2], then emits max_new
+ * tokens, each the argmax of the forward of the current token at P.
+ * logits_out (max_new x V) may be NULL. */
+OM_EXPORT int om_greedy(const om_model* m, const int* prompt, int len, int max_new, int max_seq,
+                        int* out, float* logits_out)
+{
+    if (len < 1 || len - 1 + max_new > max_seq) return -1;
+    om_seq* s = om_seq_new(m, max_seq);
+    if (!s) return -1;
+    int rc = om_prefill(s, 0, prompt, len - 1);
+    int c = prompt[len - 1], P = len - 1;
+    for (int t = 0; t < max_new && !rc; t++) {
+        unsigned char one = 1;
+        int a, row = 0;
+        rc = om_step_forward(s, P, 1, &c, &P, &one, logits_out ? logits_out + (size_t)t * m->vocab : NULL, &a);
+        if (!rc) rc = om_commit(s, P, 1, &row);
+        out[t] = a;
+        c = a;
+        P++;
+    }
+    om_seq_free(s);
+    return rc;
+}
+
+/* -------------------------------------------------------------- controller */
+
+typedef struct om_ctrl {
+    int W, N, G, V;
+    int* win;      /* [N-1][W] */
+    int* pool_cnt; /* [V] */
+    int* pool;     /* [V][G][N-1], oldest first */
+    /* snapshot of the last om_ctrl_rows call */
+    int c, P, T, Gp;
+    int* cands;    /* [G][N-1] */
+} om_ctrl;
+
+OM_EXPORT om_ctrl* om_ctrl_new(int W, int N, int G, int V)
+{
+    if (W < 0 || N < 2 || G < 0 || V < 1) return NULL;
+    om_ctrl* k = (om_ctrl*)calloc(1, sizeof(om_ctrl));
+    k->W = W; k->N = N; k->G = G; k->V = V;
+    k->win = (int*)calloc((size_t)(N - 1) * (W > 0 ? W : 1), sizeof(int));
+    k->pool_cnt = (int*)calloc(V, sizeof(int));
+    k->pool = (int*)calloc((size_t)V * (G > 0 ? G : 1) * (N - 1), sizeof(int));
+    k->cands = (int*)calloc((size_t)(G > 0 ? G : 1) * (N - 1), sizeof(int));
+    return k;
+}
+
+OM_EXPORT void om_ctrl_free(om_ctrl* k)
+{
+    if (!k) return;
+    free(k->win); free(k->pool_cnt); free(k->pool); free(k->cands); free(k);
+}
+
+/* splitmix64 (S. Vigna): state += golden gamma, then two xor-shift-multiply
+ * mixing rounds and a final xor-shift. */
+OM_EXPORT uint64_t om_splitmix64(uint64_t* state)
+{
+    uint64_t z = (*state += 0x9E3779B97F4A7C15ull);
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+/* R6: insert an (N-1)-gram under key. */
+OM_EXPORT void om_pool_insert(om_ctrl* k, int key, const int* val)
+{
+    const int n1 = k->N - 1;
+    if (k->G == 0 || key < 0 || key >= k->V) return;
+    int* e = k->pool + (size_t)key * k->G * n1;
+    int cnt = k->pool_cnt[key];
+    for (int g = 0; g < cnt; g++)
+        if (memcmp(e + (size_t)g * n1, val, sizeof(int) * n1) == 0) return;
+    if (cnt == k->G) {
+        memmove(e, e + n1, sizeof(int) * (size_t)(k->G - 1) * n1);
+        cnt--;
+    }
+    memcpy(e + (size_t)cnt * n1, val, sizeof(int) * n1);
+    k->pool_cnt[key] = cnt + 1;
+}
+
+/* R1 window init and optional R9 prompt pre-seed; clears the pool. */
+OM_EXPORT int om_ctrl_init(om_ctrl* k, const int* prompt, int len, uint64_t seed, int preseed)
+{
+    if (len < 1) return -1;
+    memset(k->pool_cnt, 0, sizeof(int) * k->V);
+    uint64_t st = seed;
+    for (int l = 0; l < k->N - 1; l++)
+        for (int j = 0; j < k->W; j++)
+            k->win[(size_t)l * k->W + j] = prompt[om_splitmix64(&st) % (uint64_t)len];
+    if (preseed)
+        for (int i = 0; i + k->N - 1 < len; i++) om_pool_insert(k, prompt[i], prompt + i + 1);
+    return 0;
+}
+
+OM_EXPORT int om_ctrl_rows_max(const om_ctrl* k) { return 1 + (k->W + k->G) * (k->N - 1); }
+
+static int row_la(const om_ctrl* k, int l, int j) { return 1 + l * k->W + j; }
+static int row_vf(const om_ctrl* k, int g, int i) { return 1 + k->W * (k->N - 1) + g * (k->N - 1) + i; }
+
+/*
+ * R2 + R3: the rows of the step for current token c with P cached tokens.
+ * Candidates = pool[c] in insertion order (G' of them).  Writes tok, pos (T
+ * entries) and vis (T*T, vis[r*T+s]) and returns T = 1 + (W+G')(N-1).
+ * Buffers must hold om_ctrl_rows_max() rows.
+ */
+OM_EXPORT int om_ctrl_rows(om_ctrl* k, int c, int P, int* tok, int* pos, unsigned char* vis)
+{
+    const int W = k->W, n1 = k->N - 1;
+    int Gp = (c >= 0 && c < k->V && k->G > 0) ? k->pool_cnt[c] : 0;
+    k->c = c; k->P = P; k->Gp = Gp;
+    if (Gp) memcpy(k->cands, k->pool + (size_t)c * k->G * n1, sizeof(int) * (size_t)Gp * n1);
+    int T = 1 + (W + Gp) * n1;
+    k->T = T;
+    memset(vis, 0, (size_t)T * T);
+    tok[0] = c; pos[0] = P; vis[0] = 1;
+    for (int l = 0; l < n1; l++)
+        for (int j = 0; j < W; j++) {
+            int r = row_la(k, l, j);
+            tok[r] = k->win[(size_t)l * W + j];
+            pos[r] = P + 1 + j + l;
+            vis[(size_t)r * T + 0] = 1;
+            for (int jj = 0; jj <= j; jj++) vis[(size_t)r * T + row_la(k, 0, jj)] = 1;
+            for (int ll = 1; ll <= l; ll++) vis[(size_t)r * T + row_la(k, ll, j)] = 1;
+        }
+    for (int g = 0; g < Gp; g++)
+        for (int i = 0; i < n1; i++) {
+            int r = row_vf(k, g, i);
+            tok[r] = k->cands[(size_t)g * n1 + i];
+            pos[r] = P + 1 + i;
+            vis[(size_t)r * T + 0] = 1;
+            for (int ii = 0; ii <= i; ii++) vis[(size_t)r * T + row_vf(k, g, ii)] = 1;
+        }
+    return T;
+}
+
+/*
+ * R5-R7 after the forward of the rows built by the last om_ctrl_rows call.
+ * amax: argmax of every row.  Writes the emitted tokens (m+1 of them) to emit,
+ * the rows whose KV is committed (m+1, row 0 first) to rows, returns m + 1.
+ * *gstar receives the chosen candidate (-1 if none).
+ */
+OM_EXPORT int om_ctrl_advance(om_ctrl* k, const int* amax, int* emit, int* rows, int* gstar)
+{
+    const int W = k->W, n1 = k->N - 1;
+    int best_m = 0, best_g = -1;
+    for (int g = 0; g < k->Gp; g++) {
+        int m = 0;
+        while (m < n1) {
+            int expect = (m == 0) ? amax[0] : amax[row_vf(k, g, m - 1)];
+            if (k->cands[(size_t)g * n1 + m] != expect) break;
+            m++;
+        }
+        if (best_g < 0 || m > best_m) { best_m = m; best_g = g; }
+    }
+    emit[0] = amax[0];
+    rows[0] = 0;
+    for (int i = 0; i < best_m; i++) {
+        emit[i + 1] = amax[row_vf(k, best_g, i)];
+        rows[i + 1] = row_vf(k, best_g, i);
+    }
+    if (gstar) *gstar = best_g;
+
+    /* R6 harvest, j ascending, from the window before the shift */
+    int* val = (int*)malloc(sizeof(int) * n1);
+    for (int j = 0; j < W; j++) {
+        int key = k->win[j];
+        for (int l = 1; l < n1; l++) val[l - 1] = k->win[(size_t)l * W + j];
+        val[n1 - 1] = amax[row_la(k, n1 - 1, j)];
+        om_pool_insert(k, key, val);
+    }
+    free(val);
+    /* R7 window shift */
+    for (int l = 0; l + 1 < n1; l++)
+        memcpy(k->win + (size_t)l * W, k->win + (size_t)(l + 1) * W, sizeof(int) * W);
+    for (int j = 0; j < W; j++) k->win[(size_t)(n1 - 1) * W + j] = amax[row_la(k, n1 - 1, j)];
+    return best_m + 1;
+}
+
+OM_EXPORT int om_ctrl_pool(const om_ctrl* k, int key, int* out)
+{
+    if (key < 0 || key >= k->V || k->G == 0) return 0;
+    int cnt = k->pool_cnt[key];
+    memcpy(out, k->pool + (size_t)key * k->G * (k->N - 1), sizeof(int) * (size_t)cnt * (k->N - 1));
+    return cnt;
+}
+
+OM_EXPORT void om_ctrl_window(const om_ctrl* k, int* out)
+{
+    memcpy(out, k->win, sizeof(int) * (size_t)(k->N - 1) * k->W);
+}
+
+/* ---------------------------------------------------------------- lookahead */
+
+/*
+ * LA-oracle: lookahead decoding of max_new tokens.  steps_out receives the
+ * number of steps, accept_hist (N+1 entries, may be NULL) counts steps by the
+ * number of tokens they emitted.  Returns 0, or -1 on bad arguments.
+ */
+OM_EXPORT int om_lookahead(const om_model* m, const int* prompt, int len, int W, int N, int G,
+                           uint64_t seed, int preseed, int max_new, int max_seq, int* out,
+                           int* steps_out, int* accept_hist)
+{
+    if (len < 1 || max_new < 0) return -1;
+    /* the farthest position a step touches is P + W + N - 2 */
+    if (len - 1 + max_new + W + N > max_seq) return -1;
+    om_ctrl* k = om_ctrl_new(W, N, G, m->vocab);
+    om_seq* s = om_seq_new(m, max_seq);
+    if (!k || !s) return -1;
+    om_ctrl_init(k, prompt, len, seed, preseed);
+    int rc = om_prefill(s, 0, prompt, len - 1);
+    int Tmax = om_ctrl_rows_max(k);
+    int* tok = (int*)malloc(sizeof(int) * Tmax);
+    int* pos = (int*)malloc(sizeof(int) * Tmax);
+    int* amax = (int*)malloc(sizeof(int) * Tmax);
+    unsigned char* vis = (unsigned char*)malloc((size_t)Tmax * Tmax);
+    int emit[64], rows[64];
+    int c = prompt[len - 1], P = len - 1, n = 0, steps = 0;
+    if (accept_hist) memset(accept_hist, 0, sizeof(int) * (N + 1));
+    while (n < max_new && !rc) {
+        int T = om_ctrl_rows(k, c, P, tok, pos, vis);
+        rc = om_step_forward(s, P, T, tok, pos, vis, NULL, amax);
+        if (rc) break;
+        int ne = om_ctrl_advance(k, amax, emit, rows, NULL);
+        rc = om_commit(s, P, ne, rows);
+        for (int i = 0; i < ne && n < max_new; i++) out[n++] = emit[i];
+        if (accept_hist) accept_hist[ne]++;
+        P += ne;
+        c = emit[ne - 1];
+        steps++;
+    }
+    if (steps_out) *steps_out = steps;
+    free(tok); free(pos); free(amax); free(vis);
+    om_ctrl_free(k);
+    om_seq_free(s);
+    return rc;
+}

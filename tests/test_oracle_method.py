@@ -1,0 +1,239 @@
+"""Pins of the oracle's lookahead decoding against what the pages and the
+mathematics fix (not against the oracle itself):
+
+* losslessness: lookahead output == greedy output token for token (the
+  summary's claim that the output distribution stays exactly the same);
+* the step shape against the pages' printed FLOPs overheads (Key points);
+* gap-free causal visibility of every row of the combined mask, and per-row
+  equivalence of the masked forward with the plain causal forward;
+* verification: brute force over all candidate sets on a tiny vocabulary with
+  a bigram "model" whose greedy continuation is known in closed form;
+* the pool: replay against a list-of-tuples simulator;
+* reductions: W=G=0 is greedy, G=0 emits one token per step, W=0 with a
+  prompt-seeded pool only ever holds prompt n-grams;
+* splitmix64 known-answer outputs.
+"""
+import itertools
+import os
+
+import numpy as np
+import pytest
+
+import la_inputs as I
+import oracle as O
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+SMALL = I.ModelConfig("small-gqa", 2, 64, 4, 2, 16, 96, 50)
+MICRO = I.ModelConfig("micro", 1, 32, 2, 1, 16, 48, 24)
+
+
+def _golden(name):
+    rows = []
+    for line in open(os.path.join(GOLD, name)):
+        line = line.split("#")[0].split()
+        if line:
+            rows.append(line)
+    return rows
+
+
+def test_splitmix64_known_answers():
+    for row in _golden("splitmix64_kat.txt"):
+        seed, vals = int(row[0]), [int(v) for v in row[1:]]
+        assert O.splitmix64_stream(seed, len(vals)) == vals
+
+
+@pytest.mark.parametrize("row", _golden("page_settings.txt"), ids=lambda r: r[0])
+def test_step_rows_match_pages_flops_overhead(row):
+    """With a full pool, a step has 1 + (W+G)(N-1) rows; at G = W the extra
+    rows are 2W(N-1), the pages' 120x / 80x / 56x per-step FLOPs overhead."""
+    W, N, G, extra = map(int, row[1:])
+    V = 40
+    k = O.Controller(W, N, G, V)
+    k.init(np.arange(V, dtype=np.int32), seed=2)
+    for g in range(G):
+        k.insert(5, [g + 1] * (N - 1))
+    tok, pos, vis = k.rows(5, 100)
+    assert len(tok) - 1 == extra
+    assert len(tok) == k.Tmax
+
+
+def test_attention_microbench_row_count():
+    """The 1 + 60 + 60 = 121 query rows of the W=15 N=5 G=15 attention case."""
+    k = O.Controller(15, 5, 15, 64)
+    assert k.Tmax == 121
+
+
+def _check_visibility(tok, pos, vis, P, W, N, G):
+    T = len(tok)
+    for r in range(T):
+        seen = sorted(pos[s] for s in range(T) if vis[r, s])
+        assert seen == list(range(P, pos[r] + 1)), (r, seen)
+    # each lookahead column is a run of consecutive positions, level by level
+    for j in range(W):
+        ps = [pos[1 + l * W + j] for l in range(N - 1)]
+        assert ps == list(range(P + 1 + j, P + 1 + j + N - 1))
+
+
+def test_mask_brute_force_gap_free():
+    for W, N, G in itertools.product(range(5), range(2, 5), range(4)):
+        k = O.Controller(W, N, G, 32)
+        k.init(np.arange(32, dtype=np.int32), seed=W * 100 + N * 10 + G)
+        for g in range(G):
+            k.insert(3, [(g + 7 * i) % 32 for i in range(N - 1)])
+        tok, pos, vis = k.rows(3, 11)
+        assert len(tok) == 1 + (W + G) * (N - 1)
+        _check_visibility(tok, pos, vis, 11, W, N, G)
+
+
+@pytest.mark.parametrize("W,N,G", [(4, 3, 4), (2, 4, 3), (3, 2, 2), (0, 3, 2), (3, 3, 0)])
+def test_masked_rows_equal_plain_causal_forward(W, N, G):
+    """Row r of the combined step equals, bit for bit, the plain causal forward
+    of the token sequence row r sees (its visible positions in order)."""
+    cfg = SMALL
+    m = O.Model(cfg, I.make_weights(cfg, 0))
+    prompt = I.random_prompt(9, cfg.vocab, 11)
+    P = len(prompt) - 1
+    k = O.Controller(W, N, G, cfg.vocab)
+    k.init(prompt, seed=5)
+    c = int(prompt[-1])
+    g = np.random.default_rng(2)
+    for _ in range(G):
+        k.insert(c, g.integers(0, cfg.vocab, N - 1))
+    tok, pos, vis = k.rows(c, P)
+    s = O.Seq(m, 64)
+    s.prefill(prompt[:-1])
+    lg, amax = s.step(P, tok, pos, vis)
+    for r in range(len(tok)):
+        order = sorted((pos[t], t) for t in range(len(tok)) if vis[r, t])
+        seq = np.concatenate([prompt[:-1], [tok[t] for _, t in order]]).astype(np.int32)
+        ref = O.Seq(m, 64)
+        ref.prefill(seq[:-1])
+        lr, ar = ref.step(len(seq) - 1, seq[-1:], [len(seq) - 1], [[1]])
+        assert np.array_equal(lr[0], lg[r]), r
+        assert ar[0] == amax[r]
+
+
+def test_verify_brute_force_bigram():
+    """A bigram model f: every row's argmax is f(its token), so the greedy
+    continuation of c is s1 = f(c), s2 = f(s1), ...  For every ordered set of
+    candidate 2-grams the step must emit s1..s(m+1), m = the longest common
+    prefix of a candidate with (s1, s2), first such candidate chosen."""
+    V, N = 3, 3
+    grams = list(itertools.product(range(V), repeat=N - 1))
+    c = 0
+    for table in itertools.product(range(V), repeat=V):
+        f = lambda t: table[t]
+        greedy = [f(c)]
+        for _ in range(N - 1):
+            greedy.append(f(greedy[-1]))
+        for G in range(0, 4):
+            for cands in itertools.permutations(grams, G):
+                k = O.Controller(0, N, G, V)
+                k.init([c], seed=1)
+                for cand in cands:
+                    k.insert(c, cand)
+                tok, pos, vis = k.rows(c, 4)
+                emit, rows, gstar = k.advance([f(t) for t in tok])
+                lcp = [next((i for i in range(N - 1) if cand[i] != greedy[i]), N - 1) for cand in cands]
+                m = max(lcp) if lcp else 0
+                assert list(emit) == greedy[:m + 1]
+                assert gstar == (lcp.index(m) if lcp else -1)
+                assert 1 <= len(emit) <= N
+
+
+def _sim_insert(pool, key, val, G):
+    if G == 0:
+        return
+    lst = pool.setdefault(key, [])
+    if val in lst:
+        return
+    if len(lst) == G:
+        lst.pop(0)
+    lst.append(val)
+
+
+@pytest.mark.parametrize("W,N,G", [(4, 3, 4), (5, 4, 2), (3, 2, 3), (6, 5, 1), (2, 3, 0)])
+def test_pool_replay_against_list_simulator(W, N, G):
+    V = 12
+    g = np.random.default_rng(W * 31 + N * 7 + G)
+    prompt = g.integers(0, V, 20).astype(np.int32)
+    k = O.Controller(W, N, G, V)
+    k.init(prompt, seed=9, preseed=True)
+    pool = {}
+    for i in range(len(prompt) - N + 1):
+        _sim_insert(pool, int(prompt[i]), tuple(int(t) for t in prompt[i + 1:i + N]), G)
+    win = k.window().tolist()
+    c = int(prompt[-1])
+    for step in range(60):
+        tok, pos, vis = k.rows(c, 19 + step)
+        amax = g.integers(0, V, len(tok))
+        emit, rows, gstar = k.advance(amax)
+        last = [int(amax[1 + (N - 2) * W + j]) for j in range(W)]
+        for j in range(W):
+            _sim_insert(pool, win[0][j], tuple(win[l][j] for l in range(1, N - 1)) + (last[j],), G)
+        win = win[1:] + [last]
+        assert k.window().tolist() == win
+        for key in range(V):
+            got = [tuple(int(x) for x in r) for r in k.pool(key)]
+            assert got == pool.get(key, [])
+            assert len(got) <= G and len(set(got)) == len(got)
+        c = int(emit[-1])
+
+
+def _lossless(cfg, bf16, W, N, G, seed, n_new, prompt, preseed=False):
+    m = O.Model(cfg, I.make_weights(cfg, 0, bf16=bf16))
+    g = O.greedy(m, prompt, n_new)
+    la, steps, hist = O.lookahead(m, prompt, W, N, G, n_new, seed=seed, preseed=preseed)
+    assert np.array_equal(la, g), (W, N, G, seed)
+    assert hist.sum() == steps and hist[0] == 0
+    assert (hist[N + 1:] == 0).all() if len(hist) > N + 1 else True
+    return steps, hist
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_lossless_tiny_workload(bf16):
+    W, N, G = I.LOOKAHEAD["tiny"]
+    steps, hist = _lossless(I.MODELS["tiny"], bf16, W, N, G, 2, 64, I.make_prompt("tiny"))
+    assert steps < 64  # some candidate was accepted on the planted-span prompt
+
+
+def test_lossless_random_cases():
+    g = np.random.default_rng(123)
+    for case in range(40):
+        W, N, G = int(g.integers(0, 6)), int(g.integers(2, 6)), int(g.integers(0, 6))
+        prompt = g.integers(0, MICRO.vocab, int(g.integers(1, 12))).astype(np.int32)
+        _lossless(MICRO, bool(case % 2), W, N, G, int(g.integers(0, 1 << 30)), 24, prompt,
+                  preseed=bool(case % 3 == 0))
+
+
+def test_reduction_greedy_and_no_verification():
+    cfg = MICRO
+    prompt = I.random_prompt(6, cfg.vocab, 3)
+    steps, hist = _lossless(cfg, False, 0, 2, 0, 1, 20, prompt)
+    assert steps == 20 and hist[1] == 20
+    steps, hist = _lossless(cfg, False, 4, 4, 0, 1, 20, prompt)
+    assert steps == 20 and hist[1] == 20  # G = 0: no candidates, one token per step
+    k = O.Controller(0, 2, 0, 8)
+    tok, pos, vis = k.rows(3, 0)
+    assert len(tok) == 1 and pos[0] == 0 and vis.tolist() == [[1]]
+
+
+def test_reduction_prompt_lookup():
+    """W = 0 with a prompt-seeded pool: the pool only ever holds prompt
+    n-grams, and a prompt that already contains the greedy continuation lets
+    whole candidates be accepted."""
+    cfg = MICRO
+    m = O.Model(cfg, I.make_weights(cfg, 0))
+    head = I.random_prompt(5, cfg.vocab, 8)
+    cont = O.greedy(m, head, 16)
+    prompt = np.concatenate([head, cont, head]).astype(np.int32)
+    N, G = 4, 3
+    la, steps, hist = O.lookahead(m, prompt, 0, N, G, 16, preseed=True)
+    assert np.array_equal(la, O.greedy(m, prompt, 16))
+    assert steps < 16
+    k = O.Controller(0, N, G, cfg.vocab)
+    k.init(prompt, preseed=True)
+    grams = {(int(prompt[i]), tuple(int(t) for t in prompt[i + 1:i + N])) for i in range(len(prompt) - N + 1)}
+    for key in range(cfg.vocab):
+        for v in k.pool(key):
+            assert (key, tuple(int(t) for t in v)) in grams
