@@ -1,0 +1,163 @@
+/*
+ * lookahead.h -- C ABI of liblookahead.so: one combined Lookahead Decoding
+ * step on one GB300 (sm_103a).
+ *
+ * Method: Fu, Bailis, Stoica, Zhang 2024, "Break the Sequential Dependency of
+ * LLM Inference Using Lookahead Decoding" (summary page, "Summary" and "Key
+ * points").  Each decode step runs ONE forward pass of a Llama-style decoder
+ * over 1 + W(N-1) lookahead-branch rows plus G(N-1) verification-branch rows
+ * under a combined attention mask against the KV cache, then greedily
+ * verifies the candidate n-grams, harvests new n-grams from the 2D window into
+ * the n-gram pool, and commits the accepted tokens' keys/values.  The output
+ * equals plain greedy decoding token for token.
+ *
+ * Conventions (all entry points):
+ *  - Return LA_OK (0) or a negative LA_ERR_* code; no exception crosses the
+ *    ABI.  la_last_error() gives a message for the last failure on a context.
+ *  - A context is single-threaded; all device work is issued on desc.stream
+ *    (NULL = the legacy default stream).
+ *  - "host" pointers are caller-owned host memory; "device" pointers are
+ *    caller-owned device memory that must stay valid until la_destroy.
+ *  - Matrices are row-major [out][in] (PyTorch nn.Linear layout).
+ *  - Compiled limits: rows per step T = 1 + (W+G)(N-1) <= 128, N <= 8,
+ *    head_dim in {64, 128}, n_heads % n_kv_heads == 0, d_model % 64 == 0.
+ */
+#ifndef LOOKAHEAD_H
+#define LOOKAHEAD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LA_API __attribute__((visibility("default")))
+#else
+#define LA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LA_OK 0
+#define LA_ERR_ARG (-1)         /* invalid argument or unsupported shape        */
+#define LA_ERR_OOM (-2)         /* device or pinned-host allocation failed      */
+#define LA_ERR_CAPACITY (-3)    /* KV cache (max_seq) or pool capacity exceeded */
+#define LA_ERR_CUDA (-4)        /* a CUDA runtime call failed                   */
+#define LA_ERR_TIMEOUT (-5)     /* a bounded device-side wait gave up           */
+#define LA_ERR_STATE (-6)       /* call out of order (e.g. step before prefill) */
+
+#define LA_FP32 0 /* fp32 weights/activations: SIMT debug path               */
+#define LA_BF16 1 /* bf16 weights/activations: tcgen05 GEMMs, MMA attention  */
+
+#define LA_PRESEED_PROMPT 1 /* insert the prompt's n-grams into the pool at prefill */
+#define LA_DEBUG_LOGITS 2   /* keep the last step's fp32 logits for la_debug_logits */
+#define LA_NO_GRAPH 4       /* launch kernels directly instead of a CUDA graph      */
+#define LA_SIMT 8           /* bf16 model on the SIMT kernels (debug)               */
+
+typedef struct la_ctx la_ctx;
+
+/* Decoder description.  Weight pointers are DEVICE pointers of `dtype`
+ * elements, borrowed (not copied) until la_destroy.
+ *   emb        [vocab][d_model]
+ *   layer_w    n_layers*9 pointers, per layer in this order:
+ *              attn_norm [d_model], wq [H*hd][d_model], wk [Hkv*hd][d_model],
+ *              wv [Hkv*hd][d_model], wo [d_model][H*hd], ffn_norm [d_model],
+ *              wg [ffn][d_model], wu [ffn][d_model], wd [d_model][ffn]
+ *              (the array itself is host memory, copied by la_create)
+ *   final_norm [d_model]
+ *   lm_head    [vocab][d_model]  (untied)
+ * Model: h = x + Wo Attn(RMSNorm(x)); y = h + Wd(silu(Wg n) * Wu n),
+ * n = RMSNorm(h); rotate-half RoPE with angle pos*rope_theta^(-2i/hd). */
+typedef struct la_model_desc {
+    int n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn, vocab, max_seq;
+    float rms_eps;    /* e.g. 1e-5  */
+    float rope_theta; /* e.g. 1e4   */
+    int dtype;        /* LA_FP32 or LA_BF16 */
+    const void* emb;
+    const void* const* layer_w;
+    const void* final_norm;
+    const void* lm_head;
+    void* stream; /* cudaStream_t */
+} la_model_desc;
+
+typedef struct la_stats {
+    long long steps;          /* la_step calls since the last prefill        */
+    long long emitted;        /* tokens emitted since the last prefill       */
+    long long prefill_tokens; /* prompt tokens written to the cache          */
+    long long accept_hist[9]; /* steps by tokens emitted (1..N)              */
+    int P;                    /* tokens whose KV is cached                   */
+    int rows;                 /* T rows per step                             */
+    float last_step_ms;       /* device time of the last step (CUDA events)  */
+} la_stats;
+
+/* Bytes of device workspace la_create needs for this model and (W,N,G):
+ * KV cache, per-layer step K/V, activations, row tables, window and pool.
+ * Returns 0 for unsupported arguments. */
+LA_API size_t la_workspace_bytes(const la_model_desc* desc, int W, int N, int G);
+
+/* Create a decoding context.  W >= 0 lookahead columns, N >= 2 n-gram size,
+ * G >= 0 verification candidates per step; W = G = 0 is plain greedy.
+ * workspace: DEVICE buffer of ws_bytes >= la_workspace_bytes(), borrowed; or
+ * NULL, and the library allocates (and frees) its own.  seed initialises the
+ * lookahead window (splitmix64 stream).  flags: LA_PRESEED_PROMPT |
+ * LA_DEBUG_LOGITS | LA_NO_GRAPH | LA_SIMT.  On success *out owns the context. */
+LA_API int la_create(const la_model_desc* desc, int W, int N, int G, void* workspace, size_t ws_bytes,
+              uint64_t seed, int flags, la_ctx** out);
+
+/* Prefill: write the KV of prompt[0..len-2] into the cache, reset the window
+ * and the pool (optionally seed it with the prompt's n-grams) and make
+ * prompt[len-1] the current token.  prompt: HOST int32[len], len >= 1,
+ * len + W + N <= max_seq.  Blocks until done. */
+LA_API int la_prefill(la_ctx* ctx, const int32_t* prompt, int len);
+
+/* One combined lookahead decode step.  Writes the 1..N emitted tokens to the
+ * HOST buffer out (cap >= N entries) and their count to *n_out.  Blocks until
+ * the tokens are on the host.  LA_ERR_CAPACITY if the cache cannot hold the
+ * step (P + W + N > max_seq); LA_ERR_STATE before la_prefill. */
+LA_API int la_step(la_ctx* ctx, int32_t* out, int cap, int* n_out);
+
+/* la_prefill, then la_step until max_new tokens; out: HOST int32[max_new]
+ * receives exactly min(max_new, emitted) tokens, count in *n_out. */
+LA_API int la_generate(la_ctx* ctx, const int32_t* prompt, int len, int max_new, int32_t* out, int* n_out);
+
+LA_API int la_get_stats(la_ctx* ctx, la_stats* out);
+
+/* ---- debug accessors (host copies of device state, after a step) ---- */
+
+/* Last step's logits, fp32 [T][vocab]; needs LA_DEBUG_LOGITS; n >= T*vocab. */
+LA_API int la_debug_logits(la_ctx* ctx, float* host, size_t n);
+/* Last step's per-row argmax, int32[T]; *T_out = T. */
+LA_API int la_debug_argmax(la_ctx* ctx, int32_t* host, int cap, int* T_out);
+/* Last step's row table: tokens and positions int32[T]; *ncand = candidates
+ * found in the pool (rows of missing candidates are padding). */
+LA_API int la_debug_rows(la_ctx* ctx, int32_t* tok, int32_t* pos, int cap, int* T_out, int* ncand);
+/* Pool entries of key, oldest first: int32[count][N-1] into host (cap ints). */
+LA_API int la_debug_pool(la_ctx* ctx, int32_t key, int32_t* host, int cap, int* count);
+/* Lookahead window, int32[N-1][W] into host (cap ints). */
+LA_API int la_debug_window(la_ctx* ctx, int32_t* host, int cap);
+
+LA_API const char* la_last_error(la_ctx* ctx);
+LA_API void la_destroy(la_ctx* ctx);
+
+/* ---- standalone n-gram pool (the pool the step uses, exposed for bulk work) ----
+ * A GPU hash table keyed on a token, each key holding up to G (N-1)-grams in
+ * insertion order with first-in-first-out eviction; an insert of an n-gram
+ * already held is a no-op.  Open addressing with warp-cooperative probing.
+ * capacity: number of key slots (rounded up to a power of two, >= 64). */
+typedef struct la_pool la_pool;
+LA_API int la_pool_create(int capacity, int N, int G, void* stream, la_pool** out);
+/* Insert n (key, (N-1)-gram) pairs in index order (equal keys keep their
+ * order; distinct keys are inserted in parallel).  keys: DEVICE int32[n],
+ * grams: DEVICE int32[n][N-1].  LA_ERR_CAPACITY when the table is full. */
+LA_API int la_pool_insert(la_pool* pool, const int32_t* keys, const int32_t* grams, int n);
+/* Look up n keys.  out: DEVICE int32[n][G][N-1] (oldest first, unused slots
+ * -1), counts: DEVICE int32[n].  Asynchronous on the pool's stream. */
+LA_API int la_pool_lookup(la_pool* pool, const int32_t* keys, int n, int32_t* out, int32_t* counts);
+/* Number of keys held (synchronises the stream). */
+LA_API int la_pool_size(la_pool* pool, int* n_keys);
+LA_API void la_pool_destroy(la_pool* pool);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LOOKAHEAD_H */

@@ -199,3 +199,24 @@ def pool_bench_ngrams(n: int, vocab: int = 32000, n_minus_1: int = 4, s: float =
     """n (key, (N-1)-gram) pairs with Zipf(s) tokens for the pool micro-bench."""
     toks = zipf_tokens(n * (1 + n_minus_1), vocab, s, seed).reshape(n, 1 + n_minus_1)
     return toks[:, 0].copy(), toks[:, 1:].copy()
+
+
+def pool_bench_inserts(n_keys: int = 4096, per_key: int = 20, vocab: int = 32000, n_minus_1: int = 4,
+                       s: float = 1.1, seed: int = 5):
+    """Insert stream for the pool micro-benchmark: n_keys distinct Zipf(s) keys,
+    per_key Zipf(s) (N-1)-grams each, in a seeded interleaved order.
+    Returns keys int32[n], grams int32[n][N-1]."""
+    g = np.random.default_rng(seed)
+    keys, seen, draw = [], set(), 0
+    while len(keys) < n_keys:
+        for t in zipf_tokens(4 * n_keys, vocab, s, seed + 17 + draw).tolist():
+            if t not in seen:
+                seen.add(t)
+                keys.append(t)
+                if len(keys) == n_keys:
+                    break
+        draw += 1
+    k = np.repeat(np.array(keys, np.int32), per_key)
+    order = g.permutation(len(k))
+    grams = zipf_tokens(len(k) * n_minus_1, vocab, s, seed + 1).reshape(len(k), n_minus_1)
+    return k[order].copy(), grams.astype(np.int32)

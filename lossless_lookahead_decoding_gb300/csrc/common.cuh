@@ -1,0 +1,122 @@
+// common.cuh -- types shared by the kernels and the engine of liblookahead.so.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace la {
+
+constexpr int kRows = 128;   // rows of one forward pass (step rows or a prefill block)
+constexpr int kMaxN = 8;     // largest n-gram size N
+constexpr int kWarp = 32;
+
+// Device-side decode state: read and written by the step's kernels so that a
+// step is a fixed launch sequence (capturable in one CUDA graph).
+struct DState {
+    int P;         // tokens whose KV is in the cache
+    int c;         // current token (its KV is not cached yet)
+    int T;         // rows of the current step
+    int ncand;     // candidates found in the pool for c (G')
+    int n_emit;    // tokens emitted by the last step (m + 1)
+    int gstar;     // chosen candidate, -1 if none
+    int P_before;  // P at the start of the last step (commit base)
+    int status;    // 0 or a negative LA_ERR_* raised on the device
+    int emit[kMaxN];
+    int commit_rows[kMaxN];
+    long long steps;
+};
+
+// Static description of which in-step row provides the key at each position
+// offset for every row group.  A row r of group grp[r] at position
+// P + rel_pos[r] sees the cache [0,P) and, at offset o in [0, rel_pos[r]],
+// the step row grp_map[grp[r]*maxoff + o].
+struct RowSet {
+    const int* rel_pos;
+    const int* grp;
+    const int* grp_map;
+    int maxoff;
+    int ngrp;
+};
+
+// The n-gram pool: open-addressing hash table keyed on a token.  Each slot
+// holds up to G (N-1)-grams, oldest first.
+struct PoolView {
+    int* keys;    // [cap], -1 = empty
+    int* cnt;     // [cap]
+    int* ent;     // [cap][G][n1]
+    int* first;   // [cap] bulk-insert scratch (INT_MAX when idle)
+    int* slot_of; // [max_bulk] bulk-insert scratch
+    int* status;  // device int: set to LA_ERR_CAPACITY when full
+    int cap;      // power of two
+    int log2cap;
+    int G, n1;
+};
+
+__host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+template <typename T> __device__ __forceinline__ float to_f(T x);
+template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// ---- launchers (defined in the .cu files) ----
+struct Dims {
+    int L, d, H, Hkv, hd, F, V, max_seq;
+    float eps;
+};
+
+// control.cu
+void launch_build_rows(cudaStream_t s, DState* st, const int* win, PoolView pool, int W, int N, int G,
+                       int T, const int* rel_pos, int* tok, int* pos);
+void launch_prefill_rows(cudaStream_t s, const DState* st, const int* prompt, int P0, int n, int* tok,
+                         int* pos);
+void launch_verify_update(cudaStream_t s, DState* st, const int* tok, const int* amax, int* win,
+                          PoolView pool, int W, int N, int G);
+void launch_commit(cudaStream_t s, const DState* st, bool prefill, int n_prefill, int n_max, const void* KS,
+                   const void* VS, void* KC, void* VC, int L, int Hkv, int hd, int max_seq, int esz);
+void launch_pool_reset(cudaStream_t s, PoolView pool);
+void launch_set_state(cudaStream_t s, DState* st, int P, int c, bool reset);
+void launch_pool_insert(cudaStream_t s, PoolView pool, const int* keys, const int* grams, int gram_stride,
+                        int n);
+void launch_pool_lookup(cudaStream_t s, PoolView pool, const int* keys, int n, int* out, int* counts);
+
+// simt.cu (T = element type of weights/activations: float or bf16)
+template <typename T>
+void launch_embed(cudaStream_t s, const int* tok, const T* emb, float* X, int rows, int d);
+template <typename T>
+void launch_rmsnorm(cudaStream_t s, const float* X, const T* w, T* out, int rows, int d, float eps);
+template <typename T>
+void launch_gemm_simt_f32out(cudaStream_t s, const T* A, const T* W, float* out, int ld_out, int rows, int K,
+                             int Nout);
+template <typename T>
+void launch_gemm_simt_resid(cudaStream_t s, const T* A, const T* W, float* X, int rows, int K, int Nout);
+template <typename T>
+void launch_gemm_simt_swiglu(cudaStream_t s, const T* A, const T* Wg, const T* Wu, T* out, int rows, int K,
+                             int F);
+template <typename T>
+void launch_rope_split(cudaStream_t s, const float* qkv, const int* pos, const float* cosb, const float* sinb,
+                       T* Q, T* KS, T* VS, int rows, int H, int Hkv, int hd);
+template <typename T>
+void launch_attn_simt(cudaStream_t s, const DState* st, RowSet rs, const int* pos, const T* Q, const T* KC,
+                      const T* VC, const T* KS, const T* VS, T* out, int rows, int H, int Hkv, int hd,
+                      int max_seq, float scale);
+void launch_argmax(cudaStream_t s, const float* logits, int* amax, int rows, int V);
+
+}  // namespace la

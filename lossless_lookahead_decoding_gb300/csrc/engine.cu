@@ -1,0 +1,687 @@
+// engine.cu -- the C ABI of liblookahead.so (include/lookahead.h): context and
+// workspace, prefill, the combined lookahead decode step, generation, stats
+// and debug accessors.
+//
+// Method: Fu et al. 2024, "Break the Sequential Dependency of LLM Inference
+// Using Lookahead Decoding", summary page, "Summary" (one forward pass holds
+// the lookahead branch over a 2D window and the verification branch over pool
+// candidates; the output equals greedy decoding) and "Key points" (knobs W, N,
+// G).  A step is a fixed launch sequence on one stream: row assembly + pool
+// lookup, embedding, per layer RMSNorm -> QKV+RoPE -> masked attention ->
+// O-proj+residual -> RMSNorm -> gate/up+SwiGLU -> down+residual, final norm +
+// LM head + argmax, verify + harvest + window shift, KV commit, and one
+// device-to-host copy of the emitted tokens.  All decode state lives on the
+// device, so the sequence is captured once into a CUDA graph and replayed.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/lookahead.h"
+#include "common.cuh"
+#include "gemm_tc.cuh"
+
+using namespace la;
+
+namespace {
+
+struct Layout {
+    size_t off[40];
+    size_t total;
+    int n;
+    size_t add(size_t bytes)
+    {
+        size_t o = total;
+        off[n++] = o;
+        total += (bytes + 1023) & ~(size_t)1023;
+        return o;
+    }
+};
+
+int next_pow2_log2(int x)
+{
+    int l = 0;
+    while ((1 << l) < x) l++;
+    return l;
+}
+
+}  // namespace
+
+struct la_ctx {
+    la_model_desc d;
+    std::vector<const void*> lw;
+    int W = 0, N = 2, G = 0, T = 1, flags = 0;
+    uint64_t seed = 0;
+    cudaStream_t s = nullptr;
+    bool bf16 = false, use_tc = false;
+    int esz = 4, dq = 0, dkv = 0;
+    char* ws = nullptr;
+    size_t ws_bytes = 0;
+    bool own_ws = false;
+    // workspace views
+    char *KC = nullptr, *VC = nullptr, *KS = nullptr, *VS = nullptr;
+    char *XN = nullptr, *Q = nullptr, *ATT = nullptr, *HID = nullptr;
+    float *X = nullptr, *QKV32 = nullptr, *LOGITS = nullptr, *cosb = nullptr, *sinb = nullptr;
+    int *AMAX = nullptr, *tok = nullptr, *pos = nullptr, *prompt = nullptr, *win = nullptr;
+    int *dbg = nullptr;
+    unsigned long long* AMAXP = nullptr;
+    RowSet rs_step{}, rs_pre{};
+    PoolView pool{};
+    DState* st = nullptr;
+    DState* h_st = nullptr;
+    TcPlan tc{};
+    // host side
+    bool prefilled = false, have_step = false;
+    int P_host = 0;
+    la_stats stats{};
+    cudaEvent_t ev0 = nullptr, ev1 = nullptr;
+    cudaGraphExec_t gexec = nullptr;
+    std::string err;
+};
+
+#define LA_CK(call)                                                                                    \
+    do {                                                                                               \
+        cudaError_t e_ = (call);                                                                       \
+        if (e_ != cudaSuccess) {                                                                       \
+            ctx->err = std::string(#call) + ": " + cudaGetErrorString(e_);                             \
+            return LA_ERR_CUDA;                                                                        \
+        }                                                                                              \
+    } while (0)
+
+static int fail(la_ctx* ctx, int code, const char* msg)
+{
+    if (ctx) ctx->err = msg;
+    return code;
+}
+
+static int step_rows(int W, int N, int G) { return 1 + (W + G) * (N - 1); }
+
+static const char* check_desc(const la_model_desc* d, int W, int N, int G)
+{
+    if (!d) return "desc is NULL";
+    if (d->n_layers < 1 || d->d_model < 64 || d->d_model % 64) return "d_model must be a positive multiple of 64";
+    if (d->head_dim != 64 && d->head_dim != 128) return "head_dim must be 64 or 128";
+    if (d->n_heads < 1 || d->n_kv_heads < 1 || d->n_heads % d->n_kv_heads) return "n_heads % n_kv_heads != 0";
+    if (d->ffn < 8 || d->ffn % 8) return "ffn must be a positive multiple of 8";
+    if (d->vocab < 2 || d->max_seq < 2) return "bad vocab or max_seq";
+    if (d->dtype != LA_FP32 && d->dtype != LA_BF16) return "dtype must be LA_FP32 or LA_BF16";
+    if (!d->emb || !d->layer_w || !d->final_norm || !d->lm_head) return "missing weight pointer";
+    if (W < 0 || G < 0 || N < 2 || N > kMaxN) return "need W >= 0, G >= 0, 2 <= N <= 8";
+    if (step_rows(W, N, G) > kRows) return "1 + (W+G)(N-1) must be <= 128";
+    if ((N - 1) * W > 127) return "window too large";
+    return nullptr;
+}
+
+static Layout make_layout(const la_model_desc* d, int W, int N, int G, int* pool_log2)
+{
+    const int esz = d->dtype == LA_BF16 ? 2 : 4;
+    const size_t L = d->n_layers, dq = (size_t)d->n_heads * d->head_dim, dkv = (size_t)d->n_kv_heads * d->head_dim;
+    const int n1 = N - 1;
+    const int lg = next_pow2_log2(2 * d->vocab < 64 ? 64 : 2 * d->vocab);
+    if (pool_log2) *pool_log2 = lg;
+    const size_t cap = (size_t)1 << lg;
+    Layout ly{};
+    ly.add(L * dkv * d->max_seq * esz);                  // 0 KC
+    ly.add(L * dkv * d->max_seq * esz);                  // 1 VC
+    ly.add(L * kRows * dkv * esz);                       // 2 KS
+    ly.add(L * kRows * dkv * esz);                       // 3 VS
+    ly.add((size_t)kRows * d->d_model * 4);              // 4 X
+    ly.add((size_t)kRows * d->d_model * esz);            // 5 XN
+    ly.add((size_t)kRows * (dq + 2 * dkv) * 4);          // 6 QKV32
+    ly.add((size_t)kRows * dq * esz);                    // 7 Q
+    ly.add((size_t)kRows * dq * esz);                    // 8 ATT
+    ly.add((size_t)kRows * d->ffn * esz);                // 9 HID
+    ly.add((size_t)kRows * d->vocab * 4);                // 10 LOGITS
+    ly.add((size_t)d->max_seq * (d->head_dim / 2) * 4);  // 11 cos
+    ly.add((size_t)d->max_seq * (d->head_dim / 2) * 4);  // 12 sin
+    ly.add(kRows * 4);                                   // 13 AMAX
+    ly.add(kRows * 4);                                   // 14 tok
+    ly.add(kRows * 4);                                   // 15 pos
+    ly.add((size_t)d->max_seq * 4);                      // 16 prompt
+    ly.add((size_t)(n1 * (W > 0 ? W : 1)) * 4);          // 17 window
+    ly.add(kRows * 4 * 2);                               // 18 step rel_pos + grp
+    ly.add((size_t)kRows * kRows * 4);                   // 19 step grp_map
+    ly.add(kRows * 4 * 2);                               // 20 prefill rel_pos + grp
+    ly.add(kRows * 4);                                   // 21 prefill grp_map
+    ly.add(cap * 4 * 3);                                 // 22 pool keys, cnt, first
+    ly.add(cap * (size_t)(G > 0 ? G : 1) * n1 * 4);      // 23 pool entries
+    ly.add((size_t)d->max_seq * 4);                      // 24 pool slot_of
+    ly.add(sizeof(DState));                              // 25 state
+    ly.add(4096);                                        // 26 debug scratch
+    ly.add(kRows * 8);                                   // 27 packed argmax
+    return ly;
+}
+
+extern "C" size_t la_workspace_bytes(const la_model_desc* desc, int W, int N, int G)
+{
+    if (check_desc(desc, W, N, G)) return 0;
+    return make_layout(desc, W, N, G, nullptr).total;
+}
+
+template <typename T>
+static void forward(la_ctx* c, int rows, const RowSet& rs, bool logits)
+{
+    const la_model_desc& d = c->d;
+    const int L = d.n_layers, D = d.d_model, H = d.n_heads, Hkv = d.n_kv_heads, hd = d.head_dim, F = d.ffn;
+    const int dq = c->dq, dkv = c->dkv;
+    cudaStream_t s = c->s;
+    T* XN = (T*)c->XN;
+    T* Q = (T*)c->Q;
+    T* ATT = (T*)c->ATT;
+    T* HID = (T*)c->HID;
+    const float scale = 1.0f / sqrtf((float)hd);
+    launch_embed<T>(s, c->tok, (const T*)d.emb, c->X, rows, D);
+    for (int l = 0; l < L; l++) {
+        const T* const* w = (const T* const*)&c->lw[(size_t)l * 9];
+        T* KS = (T*)c->KS + (size_t)l * kRows * dkv;
+        T* VS = (T*)c->VS + (size_t)l * kRows * dkv;
+        const T* KC = (const T*)c->KC + (size_t)l * dkv * d.max_seq;
+        const T* VC = (const T*)c->VC + (size_t)l * dkv * d.max_seq;
+        launch_rmsnorm<T>(s, c->X, w[0], XN, rows, D, d.rms_eps);
+        if (c->use_tc) {
+            tc_qkv_rope(c->tc, s, l, rows, c->pos, c->cosb, c->sinb, (void*)Q, (void*)KS, (void*)VS);
+        } else {
+            const int ld = dq + 2 * dkv;
+            launch_gemm_simt_f32out<T>(s, XN, w[1], c->QKV32, ld, rows, D, dq);
+            launch_gemm_simt_f32out<T>(s, XN, w[2], c->QKV32 + dq, ld, rows, D, dkv);
+            launch_gemm_simt_f32out<T>(s, XN, w[3], c->QKV32 + dq + dkv, ld, rows, D, dkv);
+            launch_rope_split<T>(s, c->QKV32, c->pos, c->cosb, c->sinb, Q, KS, VS, rows, H, Hkv, hd);
+        }
+        if (c->use_tc && tc_attn_supported(c->tc))
+            tc_attention(c->tc, s, c->st, rs, c->pos, (const void*)Q, (const void*)KC, (const void*)VC,
+                         (const void*)KS, (const void*)VS, (void*)ATT, rows);
+        else
+            launch_attn_simt<T>(s, c->st, rs, c->pos, Q, KC, VC, KS, VS, ATT, rows, H, Hkv, hd, d.max_seq, scale);
+        if (c->use_tc) {
+            tc_oproj_resid(c->tc, s, l, rows, c->X);
+        } else {
+            launch_gemm_simt_resid<T>(s, ATT, w[4], c->X, rows, dq, D);
+        }
+        launch_rmsnorm<T>(s, c->X, w[5], XN, rows, D, d.rms_eps);
+        if (c->use_tc) {
+            tc_gateup_swiglu(c->tc, s, l, rows);
+            tc_down_resid(c->tc, s, l, rows, c->X);
+        } else {
+            launch_gemm_simt_swiglu<T>(s, XN, w[6], w[7], HID, rows, D, F);
+            launch_gemm_simt_resid<T>(s, HID, w[8], c->X, rows, F, D);
+        }
+    }
+    if (logits) {
+        launch_rmsnorm<T>(s, c->X, (const T*)d.final_norm, XN, rows, D, d.rms_eps);
+        if (c->use_tc) {
+            tc_lmhead_argmax(c->tc, s, rows, (c->flags & LA_DEBUG_LOGITS) ? c->LOGITS : nullptr, c->AMAXP, c->AMAX);
+        } else {
+            launch_gemm_simt_f32out<T>(s, XN, (const T*)d.lm_head, c->LOGITS, d.vocab, rows, D, d.vocab);
+            launch_argmax(s, c->LOGITS, c->AMAX, rows, d.vocab);
+        }
+    }
+}
+
+static void run_forward(la_ctx* c, int rows, const RowSet& rs, bool logits)
+{
+    if (c->bf16) forward<__nv_bfloat16>(c, rows, rs, logits);
+    else forward<float>(c, rows, rs, logits);
+}
+
+// The step's launch sequence (no host synchronisation inside).
+static void enqueue_step(la_ctx* c)
+{
+    launch_build_rows(c->s, c->st, c->win, c->pool, c->W, c->N, c->G, c->T, c->rs_step.rel_pos, c->tok, c->pos);
+    run_forward(c, c->T, c->rs_step, true);
+    launch_verify_update(c->s, c->st, c->tok, c->AMAX, c->win, c->pool, c->W, c->N, c->G);
+    launch_commit(c->s, c->st, false, 0, c->N, c->KS, c->VS, c->KC, c->VC, c->d.n_layers, c->d.n_kv_heads,
+                  c->d.head_dim, c->d.max_seq, c->esz);
+    cudaMemcpyAsync(c->h_st, c->st, sizeof(DState), cudaMemcpyDeviceToHost, c->s);
+}
+
+extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* workspace, size_t ws_bytes,
+                         uint64_t seed, int flags, la_ctx** out)
+{
+    if (!out) return LA_ERR_ARG;
+    *out = nullptr;
+    if (const char* why = check_desc(desc, W, N, G)) {
+        fprintf(stderr, "la_create: %s\n", why);
+        return LA_ERR_ARG;
+    }
+    la_ctx* ctx = new (std::nothrow) la_ctx();
+    if (!ctx) return LA_ERR_OOM;
+    ctx->d = *desc;
+    ctx->lw.assign(desc->layer_w, desc->layer_w + (size_t)desc->n_layers * 9);
+    for (const void* p : ctx->lw)
+        if (!p) {
+            delete ctx;
+            return LA_ERR_ARG;
+        }
+    ctx->d.layer_w = ctx->lw.data();
+    ctx->W = W;
+    ctx->N = N;
+    ctx->G = G;
+    ctx->T = step_rows(W, N, G);
+    // the legacy default stream cannot be captured: launch directly there
+    ctx->flags = desc->stream ? flags : (flags | LA_NO_GRAPH);
+    ctx->seed = seed;
+    ctx->s = (cudaStream_t)desc->stream;
+    ctx->bf16 = desc->dtype == LA_BF16;
+    ctx->esz = ctx->bf16 ? 2 : 4;
+    ctx->dq = desc->n_heads * desc->head_dim;
+    ctx->dkv = desc->n_kv_heads * desc->head_dim;
+    int lg = 0;
+    Layout ly = make_layout(desc, W, N, G, &lg);
+    if (workspace) {
+        if (ws_bytes < ly.total || ((uintptr_t)workspace & 1023)) {
+            delete ctx;
+            return LA_ERR_ARG;
+        }
+        ctx->ws = (char*)workspace;
+    } else {
+        if (cudaMalloc((void**)&ctx->ws, ly.total) != cudaSuccess) {
+            delete ctx;
+            return LA_ERR_OOM;
+        }
+        ctx->own_ws = true;
+    }
+    ctx->ws_bytes = ly.total;
+    char* b = ctx->ws;
+    ctx->KC = b + ly.off[0];
+    ctx->VC = b + ly.off[1];
+    ctx->KS = b + ly.off[2];
+    ctx->VS = b + ly.off[3];
+    ctx->X = (float*)(b + ly.off[4]);
+    ctx->XN = b + ly.off[5];
+    ctx->QKV32 = (float*)(b + ly.off[6]);
+    ctx->Q = b + ly.off[7];
+    ctx->ATT = b + ly.off[8];
+    ctx->HID = b + ly.off[9];
+    ctx->LOGITS = (float*)(b + ly.off[10]);
+    ctx->cosb = (float*)(b + ly.off[11]);
+    ctx->sinb = (float*)(b + ly.off[12]);
+    ctx->AMAX = (int*)(b + ly.off[13]);
+    ctx->tok = (int*)(b + ly.off[14]);
+    ctx->pos = (int*)(b + ly.off[15]);
+    ctx->prompt = (int*)(b + ly.off[16]);
+    ctx->win = (int*)(b + ly.off[17]);
+    int* rs1 = (int*)(b + ly.off[18]);
+    int* map1 = (int*)(b + ly.off[19]);
+    int* rs2 = (int*)(b + ly.off[20]);
+    int* map2 = (int*)(b + ly.off[21]);
+    int* pk = (int*)(b + ly.off[22]);
+    const int cap = 1 << lg;
+    ctx->st = (DState*)(b + ly.off[25]);
+    ctx->dbg = (int*)(b + ly.off[26]);
+    ctx->AMAXP = (unsigned long long*)(b + ly.off[27]);
+    ctx->pool = PoolView{pk, pk + cap, (int*)(b + ly.off[23]), pk + 2 * cap, (int*)(b + ly.off[24]),
+                         &ctx->st->status, cap, lg, G, N - 1};
+
+    // row tables: step (R2/R3 of the oracle's readings) and prefill (causal)
+    const int n1 = N - 1;
+    std::vector<int> rel(kRows, 0), grp(kRows, 0), map((size_t)kRows * kRows, 0);
+    int maxoff = 1;
+    for (int l = 0; l < n1; l++)
+        for (int j = 0; j < W; j++) {
+            int r = 1 + l * W + j;
+            rel[r] = 1 + j + l;
+            grp[r] = j;
+        }
+    for (int g = 0; g < G; g++)
+        for (int i = 0; i < n1; i++) {
+            int r = 1 + W * n1 + g * n1 + i;
+            rel[r] = 1 + i;
+            grp[r] = W + g;
+        }
+    for (int r = 0; r < ctx->T; r++) maxoff = rel[r] + 1 > maxoff ? rel[r] + 1 : maxoff;
+    const int ngrp = W + G > 0 ? W + G : 1;
+    for (int j = 0; j < W; j++) {
+        int* m = &map[(size_t)j * maxoff];
+        for (int jj = 0; jj <= j; jj++) m[1 + jj] = 1 + jj;          // level 0, columns 0..j
+        for (int l = 1; l < n1; l++) m[1 + j + l] = 1 + l * W + j;   // levels 1.. of column j
+    }
+    for (int g = 0; g < G; g++) {
+        int* m = &map[(size_t)(W + g) * maxoff];
+        for (int i = 0; i < n1; i++) m[1 + i] = 1 + W * n1 + g * n1 + i;
+    }
+    std::vector<int> prel(kRows), pgrp(kRows, 0), pmap(kRows);
+    for (int r = 0; r < kRows; r++) prel[r] = pmap[r] = r;
+    std::vector<float> cs((size_t)desc->max_seq * (desc->head_dim / 2)), sn(cs.size());
+    for (int p = 0; p < desc->max_seq; p++)
+        for (int i = 0; i < desc->head_dim / 2; i++) {
+            double ang = (double)p * std::pow((double)desc->rope_theta, -2.0 * i / (double)desc->head_dim);
+            cs[(size_t)p * (desc->head_dim / 2) + i] = (float)std::cos(ang);
+            sn[(size_t)p * (desc->head_dim / 2) + i] = (float)std::sin(ang);
+        }
+    int rc = LA_OK;
+    {
+        auto ck = [&](cudaError_t e) {
+            if (e != cudaSuccess && rc == LA_OK) {
+                ctx->err = cudaGetErrorString(e);
+                rc = LA_ERR_CUDA;
+            }
+        };
+        ck(cudaMemcpy(rs1, rel.data(), kRows * 4, cudaMemcpyHostToDevice));
+        ck(cudaMemcpy(rs1 + kRows, grp.data(), kRows * 4, cudaMemcpyHostToDevice));
+        ck(cudaMemcpy(map1, map.data(), (size_t)ngrp * maxoff * 4, cudaMemcpyHostToDevice));
+        ck(cudaMemcpy(rs2, prel.data(), kRows * 4, cudaMemcpyHostToDevice));
+        ck(cudaMemcpy(rs2 + kRows, pgrp.data(), kRows * 4, cudaMemcpyHostToDevice));
+        ck(cudaMemcpy(map2, pmap.data(), kRows * 4, cudaMemcpyHostToDevice));
+        ck(cudaMemcpy(ctx->cosb, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice));
+        ck(cudaMemcpy(ctx->sinb, sn.data(), sn.size() * 4, cudaMemcpyHostToDevice));
+        // zero the activations once so padded rows always hold finite values
+        ck(cudaMemset(ctx->ws + ly.off[2], 0, ly.off[13] - ly.off[2]));
+        ck(cudaHostAlloc((void**)&ctx->h_st, sizeof(DState), cudaHostAllocDefault));
+        ck(cudaEventCreate(&ctx->ev0));
+        ck(cudaEventCreate(&ctx->ev1));
+    }
+    ctx->rs_step = RowSet{rs1, rs1 + kRows, map1, maxoff, ngrp};
+    ctx->rs_pre = RowSet{rs2, rs2 + kRows, map2, kRows, 1};
+    if (rc == LA_OK && ctx->bf16 && !(flags & LA_SIMT)) {
+        int trc = tc_plan_create(&ctx->tc, ctx->d, ctx->lw.data(), ctx->XN, ctx->Q, ctx->ATT, ctx->HID, ctx->esz);
+        if (trc == 0) ctx->use_tc = true;
+        else if (trc < 0) {
+            ctx->err = "tcgen05 plan creation failed";
+            rc = LA_ERR_CUDA;
+        }
+    }
+    if (rc != LA_OK) {
+        fprintf(stderr, "la_create: %s\n", ctx->err.c_str());
+        la_destroy(ctx);
+        return rc;
+    }
+    ctx->stats.rows = ctx->T;
+    *out = ctx;
+    return LA_OK;
+}
+
+extern "C" void la_destroy(la_ctx* ctx)
+{
+    if (!ctx) return;
+    if (ctx->s) cudaStreamSynchronize(ctx->s);
+    else cudaDeviceSynchronize();
+    if (ctx->gexec) cudaGraphExecDestroy(ctx->gexec);
+    tc_plan_destroy(&ctx->tc);
+    if (ctx->own_ws && ctx->ws) cudaFree(ctx->ws);
+    if (ctx->h_st) cudaFreeHost(ctx->h_st);
+    if (ctx->ev0) cudaEventDestroy(ctx->ev0);
+    if (ctx->ev1) cudaEventDestroy(ctx->ev1);
+    delete ctx;
+}
+
+extern "C" const char* la_last_error(la_ctx* ctx) { return ctx ? ctx->err.c_str() : "no context"; }
+
+// splitmix64 (S. Vigna's published generator): the lookahead window is
+// initialised from prompt tokens picked by this stream (level-major order).
+static uint64_t splitmix64(uint64_t* x)
+{
+    uint64_t z = (*x += 0x9E3779B97F4A7C15ull);
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+extern "C" int la_prefill(la_ctx* ctx, const int32_t* prompt, int len)
+{
+    if (!ctx) return LA_ERR_ARG;
+    if (!prompt || len < 1) return fail(ctx, LA_ERR_ARG, "prompt must hold at least one token");
+    if (len + ctx->W + ctx->N > ctx->d.max_seq) return fail(ctx, LA_ERR_CAPACITY, "prompt too long for max_seq");
+    for (int i = 0; i < len; i++)
+        if (prompt[i] < 0 || prompt[i] >= ctx->d.vocab) return fail(ctx, LA_ERR_ARG, "token id out of range");
+    ctx->prefilled = false;
+    cudaStream_t s = ctx->s;
+    LA_CK(cudaMemcpyAsync(ctx->prompt, prompt, (size_t)len * 4, cudaMemcpyHostToDevice, s));
+    std::vector<int> win((size_t)(ctx->N - 1) * (ctx->W > 0 ? ctx->W : 1), 0);
+    uint64_t sm = ctx->seed;
+    for (int l = 0; l < ctx->N - 1; l++)
+        for (int j = 0; j < ctx->W; j++) win[(size_t)l * ctx->W + j] = prompt[splitmix64(&sm) % (uint64_t)len];
+    LA_CK(cudaMemcpyAsync(ctx->win, win.data(), win.size() * 4, cudaMemcpyHostToDevice, s));
+    LA_CK(cudaStreamSynchronize(s));  // win is a host temporary
+    launch_pool_reset(s, ctx->pool);
+    launch_set_state(s, ctx->st, 0, prompt[len - 1], true);
+    if ((ctx->flags & LA_PRESEED_PROMPT) && ctx->G > 0 && len >= ctx->N)
+        launch_pool_insert(s, ctx->pool, ctx->prompt, ctx->prompt + 1, 1, len - ctx->N + 1);
+    for (int P0 = 0; P0 < len - 1; P0 += kRows) {
+        const int n = (len - 1 - P0) < kRows ? (len - 1 - P0) : kRows;
+        launch_set_state(s, ctx->st, P0, prompt[len - 1], false);
+        launch_prefill_rows(s, ctx->st, ctx->prompt, P0, n, ctx->tok, ctx->pos);
+        run_forward(ctx, n, ctx->rs_pre, false);
+        launch_commit(s, ctx->st, true, n, n, ctx->KS, ctx->VS, ctx->KC, ctx->VC, ctx->d.n_layers,
+                      ctx->d.n_kv_heads, ctx->d.head_dim, ctx->d.max_seq, ctx->esz);
+    }
+    launch_set_state(s, ctx->st, len - 1, prompt[len - 1], false);
+    LA_CK(cudaGetLastError());
+    LA_CK(cudaMemcpyAsync(ctx->h_st, ctx->st, sizeof(DState), cudaMemcpyDeviceToHost, s));
+    LA_CK(cudaStreamSynchronize(s));
+    if (ctx->h_st->status) return fail(ctx, ctx->h_st->status, "device status set during prefill");
+    ctx->P_host = len - 1;
+    ctx->prefilled = true;
+    ctx->have_step = false;
+    memset(&ctx->stats, 0, sizeof(ctx->stats));
+    ctx->stats.prefill_tokens = len - 1;
+    ctx->stats.P = len - 1;
+    ctx->stats.rows = ctx->T;
+    return LA_OK;
+}
+
+extern "C" int la_step(la_ctx* ctx, int32_t* out, int cap, int* n_out)
+{
+    if (!ctx) return LA_ERR_ARG;
+    if (!out || !n_out || cap < ctx->N) return fail(ctx, LA_ERR_ARG, "out must hold N tokens");
+    if (!ctx->prefilled) return fail(ctx, LA_ERR_STATE, "la_step before la_prefill");
+    if (ctx->P_host + ctx->W + ctx->N > ctx->d.max_seq) return fail(ctx, LA_ERR_CAPACITY, "KV cache full");
+    cudaStream_t s = ctx->s;
+    LA_CK(cudaEventRecord(ctx->ev0, s));
+    if (!(ctx->flags & LA_NO_GRAPH)) {
+        if (!ctx->gexec) {
+            cudaGraph_t g;
+            LA_CK(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
+            enqueue_step(ctx);
+            cudaError_t e = cudaStreamEndCapture(s, &g);
+            if (e != cudaSuccess) {
+                ctx->err = std::string("graph capture: ") + cudaGetErrorString(e);
+                return LA_ERR_CUDA;
+            }
+            e = cudaGraphInstantiate(&ctx->gexec, g, 0);
+            cudaGraphDestroy(g);
+            if (e != cudaSuccess) {
+                ctx->gexec = nullptr;
+                ctx->err = std::string("graph instantiate: ") + cudaGetErrorString(e);
+                return LA_ERR_CUDA;
+            }
+        }
+        LA_CK(cudaGraphLaunch(ctx->gexec, s));
+    } else {
+        enqueue_step(ctx);
+    }
+    LA_CK(cudaEventRecord(ctx->ev1, s));
+    LA_CK(cudaGetLastError());
+    LA_CK(cudaEventSynchronize(ctx->ev1));
+    const DState& h = *ctx->h_st;
+    if (h.status) return fail(ctx, h.status, "device status set during step");
+    const int n = h.n_emit;
+    if (n < 1 || n > ctx->N) return fail(ctx, LA_ERR_STATE, "corrupt step result");
+    memcpy(out, h.emit, sizeof(int) * n);
+    *n_out = n;
+    ctx->P_host = h.P;
+    ctx->have_step = true;
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, ctx->ev0, ctx->ev1);
+    ctx->stats.steps++;
+    ctx->stats.emitted += n;
+    ctx->stats.accept_hist[n]++;
+    ctx->stats.P = h.P;
+    ctx->stats.last_step_ms = ms;
+    return LA_OK;
+}
+
+extern "C" int la_generate(la_ctx* ctx, const int32_t* prompt, int len, int max_new, int32_t* out, int* n_out)
+{
+    if (!ctx) return LA_ERR_ARG;
+    if (max_new < 0 || !n_out || (max_new > 0 && !out)) return fail(ctx, LA_ERR_ARG, "bad output buffer");
+    int rc = la_prefill(ctx, prompt, len);
+    if (rc) return rc;
+    int n = 0;
+    int32_t buf[kMaxN];
+    while (n < max_new) {
+        int k = 0;
+        rc = la_step(ctx, buf, kMaxN, &k);
+        if (rc) break;
+        for (int i = 0; i < k && n < max_new; i++) out[n++] = buf[i];
+    }
+    *n_out = n;
+    return rc;
+}
+
+extern "C" int la_get_stats(la_ctx* ctx, la_stats* out)
+{
+    if (!ctx || !out) return LA_ERR_ARG;
+    *out = ctx->stats;
+    return LA_OK;
+}
+
+extern "C" int la_debug_logits(la_ctx* ctx, float* host, size_t n)
+{
+    if (!ctx || !host) return LA_ERR_ARG;
+    if (!ctx->have_step) return fail(ctx, LA_ERR_STATE, "no step yet");
+    if (!(ctx->flags & LA_DEBUG_LOGITS)) return fail(ctx, LA_ERR_STATE, "context made without LA_DEBUG_LOGITS");
+    size_t need = (size_t)ctx->T * ctx->d.vocab;
+    if (n < need) return fail(ctx, LA_ERR_ARG, "buffer too small");
+    LA_CK(cudaMemcpyAsync(host, ctx->LOGITS, need * 4, cudaMemcpyDeviceToHost, ctx->s));
+    LA_CK(cudaStreamSynchronize(ctx->s));
+    return LA_OK;
+}
+
+extern "C" int la_debug_argmax(la_ctx* ctx, int32_t* host, int cap, int* T_out)
+{
+    if (!ctx || !host || !T_out) return LA_ERR_ARG;
+    if (!ctx->have_step) return fail(ctx, LA_ERR_STATE, "no step yet");
+    if (cap < ctx->T) return fail(ctx, LA_ERR_ARG, "buffer too small");
+    LA_CK(cudaMemcpyAsync(host, ctx->AMAX, (size_t)ctx->T * 4, cudaMemcpyDeviceToHost, ctx->s));
+    LA_CK(cudaStreamSynchronize(ctx->s));
+    *T_out = ctx->T;
+    return LA_OK;
+}
+
+extern "C" int la_debug_rows(la_ctx* ctx, int32_t* tok, int32_t* pos, int cap, int* T_out, int* ncand)
+{
+    if (!ctx || !tok || !pos || !T_out || !ncand) return LA_ERR_ARG;
+    if (!ctx->have_step) return fail(ctx, LA_ERR_STATE, "no step yet");
+    if (cap < ctx->T) return fail(ctx, LA_ERR_ARG, "buffer too small");
+    LA_CK(cudaMemcpyAsync(tok, ctx->tok, (size_t)ctx->T * 4, cudaMemcpyDeviceToHost, ctx->s));
+    LA_CK(cudaMemcpyAsync(pos, ctx->pos, (size_t)ctx->T * 4, cudaMemcpyDeviceToHost, ctx->s));
+    LA_CK(cudaStreamSynchronize(ctx->s));
+    *T_out = ctx->T;
+    *ncand = ctx->h_st->ncand;
+    return LA_OK;
+}
+
+extern "C" int la_debug_pool(la_ctx* ctx, int32_t key, int32_t* host, int cap, int* count)
+{
+    if (!ctx || !host || !count) return LA_ERR_ARG;
+    const int n1 = ctx->N - 1, tot = (ctx->G > 0 ? ctx->G : 1) * n1;
+    if (cap < tot) return fail(ctx, LA_ERR_ARG, "buffer too small");
+    if (ctx->G == 0) {
+        *count = 0;
+        return LA_OK;
+    }
+    int* dkey = ctx->dbg;
+    int* dcnt = ctx->dbg + 1;
+    int* dout = ctx->dbg + 2;
+    LA_CK(cudaMemcpyAsync(dkey, &key, 4, cudaMemcpyHostToDevice, ctx->s));
+    launch_pool_lookup(ctx->s, ctx->pool, dkey, 1, dout, dcnt);
+    LA_CK(cudaMemcpyAsync(host, dout, (size_t)tot * 4, cudaMemcpyDeviceToHost, ctx->s));
+    LA_CK(cudaMemcpyAsync(count, dcnt, 4, cudaMemcpyDeviceToHost, ctx->s));
+    LA_CK(cudaStreamSynchronize(ctx->s));
+    return LA_OK;
+}
+
+extern "C" int la_debug_window(la_ctx* ctx, int32_t* host, int cap)
+{
+    if (!ctx || !host) return LA_ERR_ARG;
+    const int n = (ctx->N - 1) * ctx->W;
+    if (cap < n) return fail(ctx, LA_ERR_ARG, "buffer too small");
+    if (n) {
+        LA_CK(cudaMemcpyAsync(host, ctx->win, (size_t)n * 4, cudaMemcpyDeviceToHost, ctx->s));
+        LA_CK(cudaStreamSynchronize(ctx->s));
+    }
+    return LA_OK;
+}
+
+// --------------------------------------------------------- standalone pool ---
+
+struct la_pool {
+    PoolView v;
+    cudaStream_t s;
+    int* mem;
+    int* status;
+    int max_bulk;
+};
+
+extern "C" int la_pool_create(int capacity, int N, int G, void* stream, la_pool** out)
+{
+    if (!out) return LA_ERR_ARG;
+    *out = nullptr;
+    if (capacity < 1 || N < 2 || N > kMaxN || G < 1 || G * (N - 1) > 1024) return LA_ERR_ARG;
+    int lg = next_pow2_log2(capacity < 64 ? 64 : capacity);
+    if (lg > 28) return LA_ERR_ARG;
+    const size_t cap = (size_t)1 << lg;
+    const int max_bulk = 1 << 22;
+    la_pool* p = new (std::nothrow) la_pool();
+    if (!p) return LA_ERR_OOM;
+    size_t ints = cap * 3 + cap * (size_t)G * (N - 1) + max_bulk + 1;
+    if (cudaMalloc((void**)&p->mem, ints * 4) != cudaSuccess) {
+        delete p;
+        return LA_ERR_OOM;
+    }
+    int* m = p->mem;
+    p->status = m + ints - 1;
+    p->v = PoolView{m, m + cap, m + 3 * cap, m + 2 * cap, m + 3 * cap + cap * (size_t)G * (N - 1), p->status,
+                    (int)cap, lg, G, N - 1};
+    p->s = (cudaStream_t)stream;
+    p->max_bulk = max_bulk;
+    launch_pool_reset(p->s, p->v);
+    if (cudaMemsetAsync(p->status, 0, 4, p->s) != cudaSuccess || cudaStreamSynchronize(p->s) != cudaSuccess) {
+        cudaFree(p->mem);
+        delete p;
+        return LA_ERR_CUDA;
+    }
+    *out = p;
+    return LA_OK;
+}
+
+extern "C" int la_pool_insert(la_pool* p, const int32_t* keys, const int32_t* grams, int n)
+{
+    if (!p || n < 0 || (n > 0 && (!keys || !grams))) return LA_ERR_ARG;
+    if (n > p->max_bulk) return LA_ERR_ARG;
+    launch_pool_insert(p->s, p->v, keys, grams, p->v.n1, n);
+    int st = 0;
+    if (cudaMemcpyAsync(&st, p->status, 4, cudaMemcpyDeviceToHost, p->s) != cudaSuccess) return LA_ERR_CUDA;
+    if (cudaStreamSynchronize(p->s) != cudaSuccess) return LA_ERR_CUDA;
+    return st ? LA_ERR_CAPACITY : LA_OK;
+}
+
+extern "C" int la_pool_lookup(la_pool* p, const int32_t* keys, int n, int32_t* out, int32_t* counts)
+{
+    if (!p || n < 0 || (n > 0 && (!keys || !out || !counts))) return LA_ERR_ARG;
+    launch_pool_lookup(p->s, p->v, keys, n, out, counts);
+    return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+}
+
+extern "C" int la_pool_size(la_pool* p, int* n_keys)
+{
+    if (!p || !n_keys) return LA_ERR_ARG;
+    std::vector<int> k(p->v.cap);
+    if (cudaMemcpyAsync(k.data(), p->v.keys, (size_t)p->v.cap * 4, cudaMemcpyDeviceToHost, p->s) != cudaSuccess)
+        return LA_ERR_CUDA;
+    if (cudaStreamSynchronize(p->s) != cudaSuccess) return LA_ERR_CUDA;
+    int c = 0;
+    for (int x : k) c += (x != -1);
+    *n_keys = c;
+    return LA_OK;
+}
+
+extern "C" void la_pool_destroy(la_pool* p)
+{
+    if (!p) return;
+    cudaStreamSynchronize(p->s);
+    cudaFree(p->mem);
+    delete p;
+}

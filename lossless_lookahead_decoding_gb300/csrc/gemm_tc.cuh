@@ -1,0 +1,31 @@
+// gemm_tc.cuh -- tensor-core (tcgen05/TMEM, TMA-fed) path of the bf16 decoder
+// forward: the projection/MLP/LM-head GEMMs with fused epilogues and the
+// masked attention.
+#pragma once
+#include <cuda_runtime.h>
+
+#include "../../include/lookahead.h"
+#include "common.cuh"
+
+namespace la {
+
+struct TcPlan {
+    bool ok = false;
+    void* impl = nullptr;  // owned state (tensor maps, split-K scratch)
+};
+
+// 0 = plan made, 1 = shape not supported (caller falls back to SIMT), < 0 error
+int tc_plan_create(TcPlan* p, const la_model_desc& d, const void* const* lw, void* XN, void* Q, void* ATT, void* HID,
+                   int esz);
+void tc_plan_destroy(TcPlan* p);
+void tc_qkv_rope(const TcPlan& p, cudaStream_t s, int layer, int rows, const int* pos, const float* cosb,
+                 const float* sinb, void* Q, void* KS, void* VS);
+bool tc_attn_supported(const TcPlan& p);
+void tc_attention(const TcPlan& p, cudaStream_t s, const DState* st, const RowSet& rs, const int* pos, const void* Q,
+                  const void* KC, const void* VC, const void* KS, const void* VS, void* out, int rows);
+void tc_oproj_resid(const TcPlan& p, cudaStream_t s, int layer, int rows, float* X);
+void tc_gateup_swiglu(const TcPlan& p, cudaStream_t s, int layer, int rows);
+void tc_down_resid(const TcPlan& p, cudaStream_t s, int layer, int rows, float* X);
+void tc_lmhead_argmax(const TcPlan& p, cudaStream_t s, int rows, float* logits, unsigned long long* amaxp, int* amax);
+
+}  // namespace la

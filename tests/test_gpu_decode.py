@@ -1,0 +1,113 @@
+"""GPU parity of the combined lookahead step against the oracle (through the
+C ABI), on the tiny Llama-style workload in fp32 and bf16:
+
+(1) lookahead tokens == the same library's greedy tokens, bit for bit;
+(2) rows, emitted tokens, window and pool == the oracle controller fed the
+    GPU's argmaxes, bit for bit, every step;
+(3) per-step logits of every row within max relative L2 error 1e-4 (fp32) /
+    1e-2 (bf16) of the fp32 oracle run on the same weights.
+"""
+import numpy as np
+import pytest
+
+import la_inputs as I
+import oracle as O
+from helpers import build_lib, gpu_decoder, replay_against_oracle
+
+pytestmark = pytest.mark.gpu
+
+TOL = {0: 1e-4, 1: 1e-2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build_lib()
+
+
+def _weights(cfg, bf16):
+    return I.make_weights(cfg, 0, bf16=bf16)
+
+
+@pytest.mark.parametrize("dtype", [0, 1], ids=["fp32", "bf16"])
+@pytest.mark.parametrize("flags", [0, 4], ids=["graph", "nograph"])
+def test_tiny_replay_against_oracle(dtype, flags):
+    import lossless_lookahead_decoding_gb300 as LA
+    cfg = I.MODELS["tiny"]
+    w = _weights(cfg, dtype == 1)
+    W, N, G = I.LOOKAHEAD["tiny"]
+    prompt = I.make_prompt("tiny")
+    dec = gpu_decoder(cfg, w, dtype, W, N, G, 256, flags=flags | LA.LA_DEBUG_LOGITS)
+    om = O.Model(cfg, w)
+    toks, worst = replay_against_oracle(dec, om, prompt, 24, TOL[dtype])
+    st = dec.stats()
+    assert st["steps"] == 24 and st["emitted"] == len(toks)
+    dec.close()
+
+
+@pytest.mark.parametrize("dtype", [0, 1], ids=["fp32", "bf16"])
+@pytest.mark.parametrize("WNG", [(4, 3, 4), (2, 4, 3), (5, 2, 5), (0, 3, 3), (3, 3, 0)])
+def test_lookahead_equals_gpu_greedy(dtype, WNG):
+    cfg = I.MODELS["tiny"]
+    w = _weights(cfg, dtype == 1)
+    prompt = I.make_prompt("tiny")
+    greedy = gpu_decoder(cfg, w, dtype, 0, 2, 0, 256)
+    g = greedy.generate(prompt, 64)
+    la = gpu_decoder(cfg, w, dtype, *WNG, 256)
+    t = la.generate(prompt, 64)
+    assert np.array_equal(t, g)
+    assert greedy.stats()["steps"] == 64
+    if WNG[2] > 0:
+        assert la.stats()["steps"] < 64
+    if dtype == 0:
+        # fp32: also equal to the oracle's greedy output
+        assert np.array_equal(g, O.greedy(O.Model(cfg, w), prompt, 64))
+
+
+def test_tiny_fp32_greedy_logits():
+    import lossless_lookahead_decoding_gb300 as LA
+    cfg = I.MODELS["tiny"]
+    w = _weights(cfg, False)
+    prompt = I.make_prompt("tiny")
+    dec = gpu_decoder(cfg, w, 0, 0, 2, 0, 256, flags=LA.LA_DEBUG_LOGITS)
+    ref_t, ref_l = O.greedy(O.Model(cfg, w), prompt, 16, logits=True)
+    dec.prefill(prompt)
+    for s in range(16):
+        e = dec.step()
+        assert e[0] == ref_t[s]
+        lg = dec.logits()[0]
+        assert np.linalg.norm(lg - ref_l[s]) / np.linalg.norm(ref_l[s]) < 1e-4
+
+
+def test_preseed_and_edge_prompts():
+    cfg = I.MODELS["tiny"]
+    w = _weights(cfg, True)
+    greedy = gpu_decoder(cfg, w, 1, 0, 2, 0, 256)
+    la = gpu_decoder(cfg, w, 1, 4, 3, 4, 256, flags=1)
+    for prompt in (np.array([5], np.int32), np.array([7, 7, 7, 7, 7, 7, 7, 7, 7], np.int32),
+                   I.random_prompt(150, cfg.vocab, 3), I.make_prompt("tiny")):
+        assert np.array_equal(la.generate(prompt, 40), greedy.generate(prompt, 40))
+
+
+def test_errors_and_capacity():
+    import lossless_lookahead_decoding_gb300 as LA
+    cfg = I.MODELS["tiny"]
+    w = _weights(cfg, True)
+    dec = gpu_decoder(cfg, w, 1, 4, 3, 4, 48)
+    with pytest.raises(LA.LAError) as e:
+        dec.step()
+    assert e.value.code == LA.LA_ERR_STATE
+    with pytest.raises(LA.LAError) as e:
+        dec.prefill(np.arange(50, dtype=np.int32))
+    assert e.value.code == LA.LA_ERR_CAPACITY
+    with pytest.raises(LA.LAError) as e:
+        dec.prefill(np.array([cfg.vocab], np.int32))
+    assert e.value.code == LA.LA_ERR_ARG
+    dec.prefill(I.make_prompt("tiny"))
+    n = 0
+    with pytest.raises(LA.LAError) as e:
+        for _ in range(100):
+            n += len(dec.step())
+    assert e.value.code == LA.LA_ERR_CAPACITY
+    assert dec.stats()["P"] + 4 + 3 > 48
+    with pytest.raises(LA.LAError):
+        gpu_decoder(cfg, w, 1, 40, 5, 40, 256)  # 1 + 80*4 rows > 128
