@@ -358,6 +358,9 @@ extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* w
                 rc = LA_ERR_CUDA;
             }
         };
+        // zero the activations once so padded rows always hold finite values
+        ck(cudaMemset(ctx->ws + ly.off[2], 0, ly.off[11] - ly.off[2]));
+        ck(cudaMemset(ctx->AMAXP, 0, kRows * 8));
         ck(cudaMemcpy(rs1, rel.data(), kRows * 4, cudaMemcpyHostToDevice));
         ck(cudaMemcpy(rs1 + kRows, grp.data(), kRows * 4, cudaMemcpyHostToDevice));
         ck(cudaMemcpy(map1, map.data(), (size_t)ngrp * maxoff * 4, cudaMemcpyHostToDevice));
@@ -366,8 +369,6 @@ extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* w
         ck(cudaMemcpy(map2, pmap.data(), kRows * 4, cudaMemcpyHostToDevice));
         ck(cudaMemcpy(ctx->cosb, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice));
         ck(cudaMemcpy(ctx->sinb, sn.data(), sn.size() * 4, cudaMemcpyHostToDevice));
-        // zero the activations once so padded rows always hold finite values
-        ck(cudaMemset(ctx->ws + ly.off[2], 0, ly.off[13] - ly.off[2]));
         ck(cudaHostAlloc((void**)&ctx->h_st, sizeof(DState), cudaHostAllocDefault));
         ck(cudaEventCreate(&ctx->ev0));
         ck(cudaEventCreate(&ctx->ev1));

@@ -1,22 +1,741 @@
-// gemm_tc.cu -- placeholder until the tcgen05 kernels land: reports every
-// shape as unsupported so bf16 models run on the SIMT kernels.
+// gemm_tc.cu -- the bf16 decoder GEMMs on the 5th-generation tensor cores.
+//
+// One decode step multiplies <= 128 activation rows (the step's tokens) by
+// every weight matrix once, so each GEMM streams its weights from HBM exactly
+// once and is bound by HBM bandwidth.  Layout ("swap AB"): the weight matrix
+// W [Nout][K] (row-major, K-major) is the 128-row A operand, the activations
+// X [128][K] the N = 128 B operand, and the fp32 accumulator D[feature][token]
+// lives in tensor memory.  Operands are staged by TMA (128-byte swizzle) into
+// a 6-deep shared-memory ring; one thread issues tcgen05.mma, one thread
+// issues TMA, and four warps drain TMEM.
+//
+// Work split (stream-K): the flattened (tile, k-block) space is cut into
+// equal contiguous ranges, one per CTA (one CTA per SM).  A CTA writes one
+// fp32 partial per tile it touches; a second kernel sums the partials of a
+// tile in ascending k order and applies the fused epilogue (RoPE, residual,
+// SwiGLU, logits + argmax).  The split depends only on the matrix shape and
+// the SM count, never on the number of rows, so every token's result is
+// bit-identical whether it is decoded alone (greedy) or among 121 step rows
+// (lookahead): this keeps lookahead output exactly the greedy output.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <vector>
+
 #include "gemm_tc.cuh"
 
 namespace la {
 
-int tc_plan_create(TcPlan* p, const la_model_desc&, const void* const*, void*, void*, void*, void*, int)
+namespace {
+
+constexpr int kBM = 128;                 // weight rows per tile (MMA M)
+constexpr int kBN = 128;                 // token columns (MMA N)
+constexpr int kBK = 64;                  // K per stage (one 128-byte swizzle row)
+constexpr int kStages = 6;
+constexpr int kStageA = kBM * kBK * 2;   // 16 KB
+constexpr int kStageB = kBN * kBK * 2;   // 16 KB
+constexpr int kThreads = 192;            // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kTmemCols = 256;           // two 128-column fp32 accumulators
+constexpr int kSmemBytes = kStages * (kStageA + kStageB) + 1024 + 256;
+constexpr unsigned long long kWaitNs = 2000000000ull;  // bounded waits: 2 s
+
+enum { MODE_ONE = 0, MODE_SEQ3 = 1, MODE_PAIR = 2 };
+enum { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3 };
+
+struct GemmArgs {
+    int tiles, KB, ctas, mode;
+    int t0, t1;      // MODE_SEQ3: tiles of map 0, map 1
+    int rows;        // tokens (columns) to store
+    float* partial;  // [ctas + tiles][rows][128]
+    int* err;        // device status word
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ unsigned long long globaltimer()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, int count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of the given parity; gives up after kWaitNs or when
+// another role has aborted.  Returns false on give-up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > kWaitNs) return false;
+    }
+}
+
+__device__ __forceinline__ void tma_load(const CUtensorMap* map, uint64_t* bar, void* dst, int x, int y)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
+        "[%2];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+// K-major operand, 128-byte swizzle: rows of 128 B, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFF) >> 4);  // start address
+    d |= (uint64_t)1 << 16;                   // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;         // stride byte offset: 8 rows x 128 B
+    d |= (uint64_t)1 << 46;                   // descriptor version
+    d |= (uint64_t)2 << 61;                   // SWIZZLE_128B
+    return d;
+}
+
+// kind::f16 instruction descriptor: bf16 x bf16 -> f32, both K-major.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N)
+{
+    return (1u << 4)                     // D format f32
+           | (1u << 7)                   // A format bf16
+           | (1u << 10)                  // B format bf16
+           | ((uint32_t)(N >> 3) << 17)  // N / 8
+           | ((uint32_t)(M >> 4) << 24); // M / 16
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+            d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v)
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+        "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+
+__host__ __device__ __forceinline__ long long range_lo(int c, long long total, int ctas)
+{
+    return (long long)c * total / ctas;
+}
+
+__device__ __forceinline__ void raise_err(int* err, int code)
+{
+    if (err) atomicCAS(err, 0, code);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap a0, const __grid_constant__ CUtensorMap a1,
+              const __grid_constant__ CUtensorMap a2, const __grid_constant__ CUtensorMap bmap, GemmArgs g)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + kStages * kStageA;
+    uint64_t* full = (uint64_t*)(sB + kStages * kStageB);
+    uint64_t* empty = full + kStages;
+    uint64_t* tfull = empty + kStages;
+    uint64_t* tempty = tfull + 2;
+    uint32_t* tmem_slot = (uint32_t*)(tempty + 2);
+    volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x;
+    const long long total = (long long)g.tiles * g.KB;
+    const long long lo = range_lo(c, total, g.ctas), hi = range_lo(c + 1, total, g.ctas);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_phase[kStages];
+            bool issued[kStages];
+            for (int s = 0; s < kStages; s++) issued[s] = false;
+            bool ok = true;
+            for (long long idx = lo; idx < hi; idx++) {
+                if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int t = (int)(idx / g.KB), kb = (int)(idx % g.KB);
+                const int kx = kb * kBK;
+                mbar_expect_tx(&full[stage], kStageA + kStageB);
+                uint8_t* dA = sA + stage * kStageA;
+                if (g.mode == MODE_PAIR) {
+                    tma_load(&a0, &full[stage], dA, kx, t * 64);
+                    tma_load(&a1, &full[stage], dA + 64 * 128, kx, t * 64);
+                } else if (g.mode == MODE_SEQ3) {
+                    if (t < g.t0) tma_load(&a0, &full[stage], dA, kx, t * kBM);
+                    else if (t < g.t0 + g.t1) tma_load(&a1, &full[stage], dA, kx, (t - g.t0) * kBM);
+                    else tma_load(&a2, &full[stage], dA, kx, (t - g.t0 - g.t1) * kBM);
+                } else {
+                    tma_load(&a0, &full[stage], dA, kx, t * kBM);
+                }
+                tma_load(&bmap, &full[stage], sB + stage * kStageB, kx, 0);
+                issued[stage] = true;
+                issued_phase[stage] = phase;
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                raise_err(g.err, LA_ERR_TIMEOUT);
+                // let copies already in flight land before the CTA exits
+                for (int s = 0; s < kStages; s++) {
+                    if (!issued[s]) continue;
+                    const unsigned long long t0 = globaltimer();
+                    while (!mbar_try_wait(&full[s], issued_phase[s]) && globaltimer() - t0 < kWaitNs) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            constexpr uint32_t idesc = make_idesc(kBM, kBN);
+            int stage = 0, buf = 0, segs = 0;
+            uint32_t phase = 0, tphase[2] = {0, 0};
+            bool ok = true;
+            for (long long idx = lo; idx < hi && ok; idx++) {
+                const int kb = (int)(idx % g.KB);
+                const bool first = (idx == lo) || kb == 0;
+                const bool last = (idx == hi - 1) || kb == g.KB - 1;
+                if (first && segs >= 2) {
+                    if (!mbar_wait(&tempty[buf], tphase[buf], abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tphase[buf] ^= 1;
+                    tc_fence_after();
+                }
+                if (!mbar_wait(&full[stage], phase, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_base = smem_u32(sA + stage * kStageA);
+                const uint32_t b_base = smem_u32(sB + stage * kStageB);
+                const uint32_t d = tmem + buf * kBN;
+#pragma unroll
+                for (int k = 0; k < kBK / 16; k++)
+                    mma_bf16(d, sw128_desc(a_base + k * 32), sw128_desc(b_base + k * 32), idesc,
+                             (first && k == 0) ? 0u : 1u);
+                mma_commit(&empty[stage]);
+                if (last) {
+                    mma_commit(&tfull[buf]);
+                    buf ^= 1;
+                    segs++;
+                }
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                raise_err(g.err, LA_ERR_TIMEOUT);
+            }
+        }
+    } else {
+        // ---------------- epilogue warps: TMEM -> fp32 partials
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        int buf = 0;
+        uint32_t tphase[2] = {0, 0};
+        if (lo < hi) {
+            const int t_lo = (int)(lo / g.KB), t_hi = (int)((hi - 1) / g.KB);
+            for (int t = t_lo; t <= t_hi; t++) {
+                if (!mbar_wait(&tfull[buf], tphase[buf], abort_flag)) {
+                    *abort_flag = 1;
+                    raise_err(g.err, LA_ERR_TIMEOUT);
+                    break;
+                }
+                tphase[buf] ^= 1;
+                tc_fence_after();
+                float* dst = g.partial + (size_t)(c + t) * g.rows * kBM + q * 32 + lane;
+                for (int col0 = 0; col0 < g.rows; col0 += 32) {
+                    float v[32];
+                    tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + buf * kBN + col0, v);
+#pragma unroll
+                    for (int j = 0; j < 32; j++)
+                        if (col0 + j < g.rows) dst[(size_t)(col0 + j) * kBM] = v[j];
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[buf]);
+                buf ^= 1;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    }
+}
+
+// ------------------------------------------------------------- epilogues ---
+
+struct EpiArgs {
+    int tiles, KB, ctas, rows, Nout;
+    const float* partial;
+    // QKV
+    int dq, dkv, hd;
+    const int* pos;
+    const float* cosb;
+    const float* sinb;
+    __nv_bfloat16 *Q, *KS, *VS;
+    // residual
+    float* X;
+    // SwiGLU
+    __nv_bfloat16* H;
+    // logits / argmax
+    float* logits;
+    unsigned long long* amaxp;
+};
+
+__device__ __forceinline__ int owner_cta(long long idx, long long total, int ctas)
+{
+    int c = (int)(idx * ctas / total);
+    while (c > 0 && range_lo(c, total, ctas) > idx) c--;
+    while (c + 1 < ctas && range_lo(c + 1, total, ctas) <= idx) c++;
+    return c;
+}
+
+constexpr int kEpiRows = 8;
+
+template <int EPI>
+__global__ void __launch_bounds__(128) k_gemm_epi(EpiArgs e)
+{
+    const int t = blockIdx.x, f = threadIdx.x;
+    const long long total = (long long)e.tiles * e.KB;
+    const int c_lo = owner_cta((long long)t * e.KB, total, e.ctas);
+    const int c_hi = owner_cta((long long)t * e.KB + e.KB - 1, total, e.ctas);
+    __shared__ float sx[kBM];
+    __shared__ float sbv[4];
+    __shared__ int sbi[4];
+    const int r0 = blockIdx.y * kEpiRows;
+    const int r1 = min(r0 + kEpiRows, e.rows);
+    for (int r = r0; r < r1; r++) {
+        float acc = e.partial[((size_t)(c_lo + t) * e.rows + r) * kBM + f];
+        for (int cc = c_lo + 1; cc <= c_hi; cc++) acc += e.partial[((size_t)(cc + t) * e.rows + r) * kBM + f];
+        if (EPI == EPI_QKV) {
+            const int fg = t * kBM + f;
+            sx[f] = acc;
+            __syncthreads();
+            const int half = e.hd >> 1;
+            if (fg < e.dq + e.dkv) {
+                const float other = sx[f ^ half];
+                const int region = fg < e.dq ? 0 : 1;
+                const int fl = region == 0 ? fg : fg - e.dq;
+                const int i = fl % e.hd, ip = i % half;
+                const int p = e.pos[r];
+                const float cs = e.cosb[(size_t)p * half + ip], sn = e.sinb[(size_t)p * half + ip];
+                const float y = (i < half) ? acc * cs - other * sn : acc * cs + other * sn;
+                if (region == 0) e.Q[(size_t)r * e.dq + fl] = __float2bfloat16_rn(y);
+                else e.KS[(size_t)r * e.dkv + fl] = __float2bfloat16_rn(y);
+            } else if (fg < e.dq + 2 * e.dkv) {
+                e.VS[(size_t)r * e.dkv + (fg - e.dq - e.dkv)] = __float2bfloat16_rn(acc);
+            }
+            __syncthreads();
+        } else if (EPI == EPI_RESID) {
+            const int fg = t * kBM + f;
+            if (fg < e.Nout) e.X[(size_t)r * e.Nout + fg] += acc;
+        } else if (EPI == EPI_SWIGLU) {
+            sx[f] = acc;
+            __syncthreads();
+            const int fo = t * 64 + f;
+            if (f < 64 && fo < e.Nout) {
+                const float gt = acc, up = sx[f + 64];
+                e.H[(size_t)r * e.Nout + fo] = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up);
+            }
+            __syncthreads();
+        } else {
+            const int fg = t * kBM + f;
+            const bool valid = fg < e.Nout;
+            if (valid && e.logits) e.logits[(size_t)r * e.Nout + fg] = acc;
+            float bv = valid ? acc : -INFINITY;
+            int bi = valid ? fg : 0x7fffffff;
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (ov > bv || (ov == bv && oi < bi)) {
+                    bv = ov;
+                    bi = oi;
+                }
+            }
+            if ((f & 31) == 0) {
+                sbv[f >> 5] = bv;
+                sbi[f >> 5] = bi;
+            }
+            __syncthreads();
+            if (f == 0) {
+                for (int w = 1; w < 4; w++)
+                    if (sbv[w] > bv || (sbv[w] == bv && sbi[w] < bi)) {
+                        bv = sbv[w];
+                        bi = sbi[w];
+                    }
+                if (bi != 0x7fffffff) {
+                    uint32_t u = __float_as_uint(bv);
+                    uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+                    unsigned long long packed = ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)bi);
+                    atomicMax(&e.amaxp[r], packed);
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+__global__ void k_argmax_unpack(unsigned long long* amaxp, int* amax, int rows)
+{
+    const int r = threadIdx.x;
+    if (r < rows) {
+        amax[r] = (int)(0xFFFFFFFFu - (uint32_t)(amaxp[r] & 0xFFFFFFFFull));
+        amaxp[r] = 0ull;
+    }
+}
+
+// ------------------------------------------------------------------ plan ---
+
+struct GemmCfg {
+    CUtensorMap a[3];
+    CUtensorMap b;
+    int tiles, KB, ctas, mode, t0, t1, Nout;
+};
+
+struct Impl {
+    int sms = 0;
+    int L = 0, d = 0, dq = 0, dkv = 0, hd = 0, F = 0, V = 0;
+    std::vector<GemmCfg> qkv, oproj, gateup, down;
+    GemmCfg lm;
+    float* partial = nullptr;
+    size_t partial_bytes = 0;
+    int* err = nullptr;  // points at the step's status word? (set per call)
+    void* Q = nullptr;
+    void* HID = nullptr;
+};
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+    }
+    return fn;
+}
+
+// 2D bf16 tensor map over a row-major [rows][cols] matrix, box {64, box_rows}.
+bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int box_rows)
+{
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+void finish_cfg(GemmCfg& g, int K, int sms)
+{
+    g.KB = (K + kBK - 1) / kBK;
+    long long total = (long long)g.tiles * g.KB;
+    g.ctas = (int)(total < sms ? total : sms);
+}
+
+size_t partial_need(const GemmCfg& g) { return (size_t)(g.ctas + g.tiles) * kRows * kBM * 4; }
+
+void launch_gemm(const Impl& im, const GemmCfg& g, cudaStream_t s, int rows, int* err)
+{
+    GemmArgs a{g.tiles, g.KB, g.ctas, g.mode, g.t0, g.t1, rows, im.partial, err};
+    k_gemm_tc<<<g.ctas, kThreads, kSmemBytes, s>>>(g.a[0], g.a[1], g.a[2], g.b, a);
+}
+
+EpiArgs epi_base(const Impl& im, const GemmCfg& g, int rows)
+{
+    EpiArgs e{};
+    e.tiles = g.tiles;
+    e.KB = g.KB;
+    e.ctas = g.ctas;
+    e.rows = rows;
+    e.Nout = g.Nout;
+    e.partial = im.partial;
+    return e;
+}
+
+dim3 epi_grid(const GemmCfg& g, int rows) { return dim3(g.tiles, (rows + kEpiRows - 1) / kEpiRows); }
+
+}  // namespace
+
+int tc_plan_create(TcPlan* p, const la_model_desc& d, const void* const* lw, void* XN, void* Q, void* ATT, void* HID,
+                   int esz)
 {
     p->ok = false;
-    return 1;
+    p->impl = nullptr;
+    if (esz != 2) return 1;
+    const int dq = d.n_heads * d.head_dim, dkv = d.n_kv_heads * d.head_dim;
+    if (dq % kBM || dkv % kBM || d.d_model % kBK) return 1;
+    if (!get_encode()) return 1;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    int major = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (major < 10) return 1;
+    Impl* im = new Impl();
+    im->sms = sms;
+    im->L = d.n_layers;
+    im->d = d.d_model;
+    im->dq = dq;
+    im->dkv = dkv;
+    im->hd = d.head_dim;
+    im->F = d.ffn;
+    im->V = d.vocab;
+    im->Q = Q;
+    im->HID = HID;
+    bool ok = true;
+    CUtensorMap bXN, bATT, bHID;
+    ok &= make_map(&bXN, XN, kRows, d.d_model, kBN);
+    ok &= make_map(&bATT, ATT, kRows, dq, kBN);
+    ok &= make_map(&bHID, HID, kRows, d.ffn, kBN);
+    size_t need = 0;
+    for (int l = 0; l < d.n_layers && ok; l++) {
+        const void* const* w = lw + (size_t)l * 9;
+        GemmCfg q{};
+        ok &= make_map(&q.a[0], w[1], dq, d.d_model, kBM);
+        ok &= make_map(&q.a[1], w[2], dkv, d.d_model, kBM);
+        ok &= make_map(&q.a[2], w[3], dkv, d.d_model, kBM);
+        q.b = bXN;
+        q.mode = MODE_SEQ3;
+        q.t0 = dq / kBM;
+        q.t1 = dkv / kBM;
+        q.tiles = q.t0 + 2 * q.t1;
+        q.Nout = dq + 2 * dkv;
+        finish_cfg(q, d.d_model, sms);
+        GemmCfg o{};
+        ok &= make_map(&o.a[0], w[4], d.d_model, dq, kBM);
+        o.a[1] = o.a[2] = o.a[0];
+        o.b = bATT;
+        o.mode = MODE_ONE;
+        o.tiles = (d.d_model + kBM - 1) / kBM;
+        o.Nout = d.d_model;
+        finish_cfg(o, dq, sms);
+        GemmCfg gu{};
+        ok &= make_map(&gu.a[0], w[6], d.ffn, d.d_model, 64);
+        ok &= make_map(&gu.a[1], w[7], d.ffn, d.d_model, 64);
+        gu.a[2] = gu.a[0];
+        gu.b = bXN;
+        gu.mode = MODE_PAIR;
+        gu.tiles = (d.ffn + 63) / 64;
+        gu.Nout = d.ffn;
+        finish_cfg(gu, d.d_model, sms);
+        GemmCfg dn{};
+        ok &= make_map(&dn.a[0], w[8], d.d_model, d.ffn, kBM);
+        dn.a[1] = dn.a[2] = dn.a[0];
+        dn.b = bHID;
+        dn.mode = MODE_ONE;
+        dn.tiles = (d.d_model + kBM - 1) / kBM;
+        dn.Nout = d.d_model;
+        finish_cfg(dn, d.ffn, sms);
+        for (const GemmCfg* g : {&q, &o, &gu, &dn}) need = partial_need(*g) > need ? partial_need(*g) : need;
+        im->qkv.push_back(q);
+        im->oproj.push_back(o);
+        im->gateup.push_back(gu);
+        im->down.push_back(dn);
+    }
+    if (ok) {
+        GemmCfg& lm = im->lm;
+        lm = GemmCfg{};
+        ok &= make_map(&lm.a[0], d.lm_head, d.vocab, d.d_model, kBM);
+        lm.a[1] = lm.a[2] = lm.a[0];
+        lm.b = bXN;
+        lm.mode = MODE_ONE;
+        lm.tiles = (d.vocab + kBM - 1) / kBM;
+        lm.Nout = d.vocab;
+        finish_cfg(lm, d.d_model, sms);
+        need = partial_need(lm) > need ? partial_need(lm) : need;
+    }
+    if (!ok) {
+        delete im;
+        return 1;
+    }
+    if (cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess ||
+        cudaMalloc((void**)&im->partial, need) != cudaSuccess || cudaMalloc((void**)&im->err, 4) != cudaSuccess ||
+        cudaMemset(im->err, 0, 4) != cudaSuccess) {
+        if (im->partial) cudaFree(im->partial);
+        delete im;
+        return -1;
+    }
+    im->partial_bytes = need;
+    p->impl = im;
+    p->ok = true;
+    return 0;
 }
-void tc_plan_destroy(TcPlan* p) { p->ok = false; }
-void tc_qkv_rope(const TcPlan&, cudaStream_t, int, int, const int*, const float*, const float*, void*, void*, void*) {}
+
+void tc_plan_destroy(TcPlan* p)
+{
+    if (p->impl) {
+        Impl* im = (Impl*)p->impl;
+        if (im->partial) cudaFree(im->partial);
+        if (im->err) cudaFree(im->err);
+        delete im;
+    }
+    p->impl = nullptr;
+    p->ok = false;
+}
+
+int* tc_status(const TcPlan& p) { return p.impl ? ((Impl*)p.impl)->err : nullptr; }
+
+void tc_qkv_rope(const TcPlan& p, cudaStream_t s, int layer, int rows, const int* pos, const float* cosb,
+                 const float* sinb, void* Q, void* KS, void* VS)
+{
+    const Impl& im = *(const Impl*)p.impl;
+    const GemmCfg& g = im.qkv[layer];
+    launch_gemm(im, g, s, rows, im.err);
+    EpiArgs e = epi_base(im, g, rows);
+    e.dq = im.dq;
+    e.dkv = im.dkv;
+    e.hd = im.hd;
+    e.pos = pos;
+    e.cosb = cosb;
+    e.sinb = sinb;
+    e.Q = (__nv_bfloat16*)Q;
+    e.KS = (__nv_bfloat16*)KS;
+    e.VS = (__nv_bfloat16*)VS;
+    k_gemm_epi<EPI_QKV><<<epi_grid(g, rows), 128, 0, s>>>(e);
+}
+
 bool tc_attn_supported(const TcPlan&) { return false; }
+
 void tc_attention(const TcPlan&, cudaStream_t, const DState*, const RowSet&, const int*, const void*, const void*,
-                  const void*, const void*, const void*, void*, int) {}
-void tc_oproj_resid(const TcPlan&, cudaStream_t, int, int, float*) {}
-void tc_gateup_swiglu(const TcPlan&, cudaStream_t, int, int) {}
-void tc_down_resid(const TcPlan&, cudaStream_t, int, int, float*) {}
-void tc_lmhead_argmax(const TcPlan&, cudaStream_t, int, float*, unsigned long long*, int*) {}
+                  const void*, const void*, const void*, void*, int)
+{
+}
+
+void tc_oproj_resid(const TcPlan& p, cudaStream_t s, int layer, int rows, float* X)
+{
+    const Impl& im = *(const Impl*)p.impl;
+    const GemmCfg& g = im.oproj[layer];
+    launch_gemm(im, g, s, rows, im.err);
+    EpiArgs e = epi_base(im, g, rows);
+    e.X = X;
+    k_gemm_epi<EPI_RESID><<<epi_grid(g, rows), 128, 0, s>>>(e);
+}
+
+void tc_gateup_swiglu(const TcPlan& p, cudaStream_t s, int layer, int rows)
+{
+    const Impl& im = *(const Impl*)p.impl;
+    const GemmCfg& g = im.gateup[layer];
+    launch_gemm(im, g, s, rows, im.err);
+    EpiArgs e = epi_base(im, g, rows);
+    e.H = (__nv_bfloat16*)im.HID;
+    k_gemm_epi<EPI_SWIGLU><<<epi_grid(g, rows), 128, 0, s>>>(e);
+}
+
+void tc_down_resid(const TcPlan& p, cudaStream_t s, int layer, int rows, float* X)
+{
+    const Impl& im = *(const Impl*)p.impl;
+    const GemmCfg& g = im.down[layer];
+    launch_gemm(im, g, s, rows, im.err);
+    EpiArgs e = epi_base(im, g, rows);
+    e.X = X;
+    k_gemm_epi<EPI_RESID><<<epi_grid(g, rows), 128, 0, s>>>(e);
+}
+
+void tc_lmhead_argmax(const TcPlan& p, cudaStream_t s, int rows, float* logits, unsigned long long* amaxp, int* amax)
+{
+    const Impl& im = *(const Impl*)p.impl;
+    const GemmCfg& g = im.lm;
+    launch_gemm(im, g, s, rows, im.err);
+    EpiArgs e = epi_base(im, g, rows);
+    e.logits = logits;
+    e.amaxp = amaxp;
+    k_gemm_epi<EPI_LOGITS><<<epi_grid(g, rows), 128, 0, s>>>(e);
+    k_argmax_unpack<<<1, kRows, 0, s>>>(amaxp, amax, rows);
+}
 
 }  // namespace la
