@@ -1,0 +1,419 @@
+#!/usr/bin/env python3
+"""Benchmark of the combined lookahead decode step (one JSON line on rank 0).
+
+Workload (default ``7b``): a Llama-2-7B-shaped decoder (32 layers, d 4096,
+32 heads x 128, SwiGLU FFN 11008, vocab 32000), random-init bf16 weights
+N(0, 0.02), batch 1, a 512-token Zipf(1.1) prompt with planted repeated
+16-token spans, lookahead W=15 N=5 G=15 (T = 121 rows per step), greedy.
+The pages' own settings for 7B (Key points); synthetic data stands in for
+their chat/code suites.
+
+A "step" is one ``la_step``: one combined decode step (row assembly, the
+32-layer forward over 121 rows, LM head + argmax, verification, n-gram
+harvest, KV commit, token readback).  W warm-up steps, then exactly K timed
+steps, each bracketed by CUDA events on the library's stream; when a
+generation reaches its configured length (256 new tokens) the prompt is
+prefilled again outside the step timers.  Weights (13.2 GB) exceed L2, so no
+flush is needed between steps.
+
+value      effective tokens/s = tokens emitted by the K steps / their device time
+e2e        tokens/s of ``la_generate`` (host prompt -> host tokens, prefill and
+           every step's token readback inside the wall-clock region)
+roofline   the tcgen05 weight-streaming GEMM kernel: algorithmic bytes / its
+           event-timed duration, vs the measured HBM copy bandwidth
+speedup    vs the same library's plain greedy step (W = G = 0)
+cpu_baseline / --impl reference: the CPU oracle, timed on a bounded sample
+           (1-layer slice of the same model, full widths) and scaled to the
+           full depth by the FLOP ratio.
+N > 1: independent replicas (the path does not shard); value sums ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import la_inputs as I  # noqa: E402
+
+GEN_TOKENS = {"tiny": 64, "7b": 256, "13b": 256, "34b": 512}
+PRESEED = {"34b": True}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="7b", choices=list(I.MODELS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
+
+
+def step_model(cfg, T, P):
+    """Algorithmic bytes and FLOPs of one step at cache length P (bf16)."""
+    w_bytes = cfg.streamed_params() * 2 + T * cfg.d_model * 2
+    kv_read = 2 * cfg.n_layers * P * cfg.d_kv * 2
+    kv_write = 2 * cfg.n_layers * cfg.d_kv * 2 * 5
+    flops = 2 * cfg.streamed_params() * T + 4 * T * P * cfg.n_heads * cfg.head_dim * cfg.n_layers
+    return w_bytes + kv_read + kv_write, flops
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if not self.p:
+            return None
+        self.p.terminate()
+        try:
+            out, _ = self.p.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+            out, _ = self.p.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n):
+    rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if n > 0 else "gloo"
+        dist.init_process_group(backend)
+    return rank, world
+
+
+def aggregate(tokens: float, seconds: float, device=None):
+    """Sum of tokens and max of seconds over ranks (replicas)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return tokens, seconds
+    t = torch.tensor([tokens], dtype=torch.float64, device=device)
+    s = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    dist.all_reduce(s, op=dist.ReduceOp.MAX)
+    return float(t.item()), float(s.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def build_model(cfg, dtype):
+    import torch
+    import lossless_lookahead_decoding_gb300 as LA
+    # fp32 draws, rounded to bf16 on the device (round-to-nearest-even, the
+    # same values la_inputs.bf16_round gives on the host)
+    return LA.device_weights(cfg, I.iter_weights(cfg, 0, bf16=False), dtype)
+
+
+def timed_steps(dec, prompt, gen_tokens, warmup, steps):
+    """W warm-up + K timed steps; returns (tokens, per-step device ms, wall s, accept list)."""
+    import torch
+    st = dec.stream
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    dec.prefill(prompt)
+    emitted = 0
+    for _ in range(warmup):
+        if emitted >= gen_tokens:
+            dec.prefill(prompt)
+            emitted = 0
+        emitted += len(dec.step())
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    tok, acc = 0, []
+    t0 = time.perf_counter()
+    for i in range(steps):
+        if emitted >= gen_tokens:
+            dec.prefill(prompt)
+            emitted = 0
+        ev[i][0].record(st)
+        n = len(dec.step())
+        ev[i][1].record(st)
+        emitted += n
+        tok += n
+        acc.append(n)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier()
+    return tok, [a.elapsed_time(b) for a, b in ev], wall, acc
+
+
+def run_ours(args, rank, world):
+    import torch
+    import lossless_lookahead_decoding_gb300 as LA
+    from lossless_lookahead_decoding_gb300 import build as B
+    B.build()
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    cfg = I.MODELS[args.workload]
+    W, N, G = I.LOOKAHEAD[args.workload]
+    T = 1 + (W + G) * (N - 1)
+    gen = GEN_TOKENS[args.workload]
+    prompt = I.make_prompt(args.workload)
+    max_seq = len(prompt) + gen + W + N + 16
+    flags = LA.LA_PRESEED_PROMPT if PRESEED.get(args.workload) else 0
+    t_gen = time.perf_counter()
+    dw = build_model(cfg, LA.LA_BF16)
+    torch.cuda.synchronize()
+    t_gen = time.perf_counter() - t_gen
+
+    la = LA.Decoder(cfg, dw, LA.LA_BF16, W, N, G, max_seq, flags=flags)
+    gr = LA.Decoder(cfg, dw, LA.LA_BF16, 0, 2, 0, max_seq)
+    clocks = Clocks(local)
+    clocks.start()
+    tok, step_ms_l, wall, acc = timed_steps(la, prompt, gen, args.warmup, args.steps)
+    g_tok, g_step_ms_l, g_wall, _ = timed_steps(gr, prompt, gen, args.warmup, args.steps)
+    ms, greedy_ms = sum(step_ms_l), sum(g_step_ms_l)
+    clk = clocks.stop()
+    kernels = la.stats()["kernels_per_step"]
+
+    # losslessness on the benchmark workload: one full generation each way
+    la_out = la.generate(prompt, gen)
+    gr_out = gr.generate(prompt, gen)
+    lossless = bool(np.array_equal(la_out, gr_out))
+    full_steps = la.stats()["steps"]
+
+    # e2e through la_generate (host prompt in, host tokens out)
+    e2e = None
+    if not args.no_e2e:
+        reps = 3
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            out = la.generate(prompt, gen)
+        torch.cuda.synchronize()
+        e2e_s = time.perf_counter() - t0
+        steps_e2e = la.stats()["steps"]
+        e2e = {"value": reps * len(out) / e2e_s, "unit": "tokens/s",
+               "h2d_bytes_per_step": round(4 * len(prompt) / max(steps_e2e, 1), 1),
+               "d2h_bytes_per_step": 104,
+               "what": f"la_generate({len(prompt)}-token host prompt, {gen} new tokens) incl. prefill"}
+    la.close()
+    gr.close()
+
+    # per-kernel-class timing (separate profiled pass: events around launches)
+    prof_dec = LA.Decoder(cfg, dw, LA.LA_BF16, W, N, G, max_seq, flags=flags | LA.LA_PROFILE | LA.LA_NO_GRAPH)
+    timed_steps(prof_dec, prompt, gen, 2, min(args.steps, 64))
+    prof = prof_dec.profile()
+    prof_dec.close()
+
+    tot_tok, tot_s = aggregate(tok, ms / 1e3, device=torch.device("cuda", local))
+    g_tot_tok, g_tot_s = aggregate(g_tok, greedy_ms / 1e3, device=torch.device("cuda", local))
+    if rank != 0:
+        return None
+    peaks = load_peaks()
+    gemm = [v for k, v in prof.items() if k.startswith("gemm_") and k != "gemm_epilogue"]
+    g_bytes = sum(v["bytes"] for v in gemm)
+    g_ms = sum(v["total_ms"] for v in gemm)
+    g_launch = sum(v["launches"] for v in gemm)
+    achieved = g_bytes / (g_ms / 1e3) / 1e9
+    traffic = read_traffic(args.workload)
+    roofline = {"bound": "hbm", "kernel": "k_gemm_tc (all projection/MLP/LM-head GEMMs)",
+                "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_src": peaks["src"],
+                "traffic": traffic, "algorithmic_bytes_per_launch": round(g_bytes / max(g_launch, 1)),
+                "avg_launch_us": round(1e3 * g_ms / max(g_launch, 1), 2)}
+    P_mid = len(prompt) - 1 + gen // 2
+    sbytes, sflops = step_model(cfg, T, P_mid)
+    t_roof = max(sbytes / (peaks["hbm_gbs"] * 1e9), sflops / (peaks["bf16_tflops"] * 1e12))
+    step_ms = ms / args.steps
+    g_step_ms = greedy_ms / args.steps
+    acc_per_step = tok / args.steps
+    value = tot_tok / tot_s
+    g_value = g_tot_tok / g_tot_s
+    out = {
+        "metric": "effective tokens/s & step latency at batch 1 vs step roofline; accepted tok/step",
+        "value": round(value, 2), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init weights)",
+        "config": {"workload": f"{args.workload}: {cfg.n_layers}L d{cfg.d_model} {cfg.n_heads}x{cfg.head_dim} "
+                               f"(kv {cfg.n_kv_heads}) ffn{cfg.ffn} V{cfg.vocab} bf16, prompt {len(prompt)}, "
+                               f"gen {gen}, W{W} N{N} G{G}, T={T} rows",
+                   "global_batch": 1, "seq_len": max_seq, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (weights 13.2 GB stream every step)"},
+        "accepted_tokens_per_step": round(acc_per_step, 4),
+        "accept_hist": {str(k): acc.count(k) for k in range(1, N + 1)},
+        "step_latency_ms": {"median": round(float(np.median(step_ms_l)), 4),
+                            "p10": round(float(np.percentile(step_ms_l, 10)), 4),
+                            "p90": round(float(np.percentile(step_ms_l, 90)), 4), "mean": round(step_ms, 4)},
+        "wall_s_timed": round(wall, 3),
+        "greedy": {"value": round(g_value, 2), "unit": "tokens/s", "ms_per_step": round(g_step_ms, 4)},
+        "speedup_vs_greedy": round(value / g_value, 4),
+        "lossless_vs_greedy": lossless, "full_generation_steps": full_steps,
+        "step_roofline": {"t_roof_ms": round(t_roof * 1e3, 4), "frac": round(t_roof * 1e3 / step_ms, 4),
+                          "bytes": sbytes, "flops": sflops, "P": P_mid, "peak_src": peaks["src"]},
+        "kernel_profile": {k: {"launches": v["launches"], "ms_per_step": round(v["total_ms"] / max(1, min(args.steps, 64)), 4),
+                               "GB/s": round(v["bytes"] / max(v["total_ms"], 1e-9) / 1e6, 1)}
+                           for k, v in prof.items()},
+        "gpu_launches": kernels * args.steps,
+        "kernels_per_step": kernels,
+        "roofline": roofline,
+        "clocks": clk,
+        "weights_gen_s": round(t_gen, 1),
+    }
+    if e2e:
+        out["e2e"] = e2e
+    if not args.no_cpu_baseline and world == 1:
+        out["cpu_baseline"] = cpu_baseline(cfg, args.workload, W, N, G, prompt, acc_per_step, steps=2)
+    return out
+
+
+def read_traffic(workload):
+    """DRAM bytes per GEMM launch from the committed ncu summary, if it was
+    taken on the current kernel source (else null)."""
+    p = os.path.join(ROOT, "profiles", f"gemm_tc_{workload}_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    src = open(os.path.join(ROOT, "lossless_lookahead_decoding_gb300", "csrc", "gemm_tc.cu"), "rb").read()
+    if d.get("gemm_tc_sha1") != hashlib.sha1(src).hexdigest():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_sample(cfg, W, N, G, prompt, n_steps, preseed=False):
+    """Time n_steps oracle lookahead steps on a 1-layer slice (same weights as
+    layer 0 / embedding / head of the full model); returns per-step seconds,
+    tokens emitted, and the full-depth/sample FLOP ratio."""
+    import oracle as O
+    sl = cfg.sliced(1)
+    full = I.make_weights(cfg, 0, bf16=True, layers=[0])  # same bytes as the full model's layer 0
+    w = {k: (v[:1] if isinstance(v, list) else v) for k, v in full.items()}
+    m = O.Model(sl, w)
+    seq = O.Seq(m, len(prompt) + 8 * n_steps + W + N + 8)
+    seq.prefill(prompt[:-1])
+    k = O.Controller(W, N, G, cfg.vocab)
+    k.init(prompt, seed=2, preseed=preseed)
+    c, P = int(prompt[-1]), len(prompt) - 1
+    times, toks = [], 0
+    for _ in range(n_steps):
+        tok, pos, vis = k.rows(c, P)
+        t0 = time.perf_counter()
+        _, amax = seq.step(P, tok, pos, vis, want_logits=False)
+        times.append(time.perf_counter() - t0)
+        emit, rows, _ = k.advance(amax)
+        seq.commit(P, rows)
+        P += len(emit)
+        c = int(emit[-1])
+        toks += len(emit)
+    T = 1 + (W + G) * (N - 1)
+    per_layer = (cfg.n_heads * cfg.head_dim * cfg.d_model * 2 + 2 * cfg.d_kv * cfg.d_model + 3 * cfg.ffn * cfg.d_model)
+    head = cfg.vocab * cfg.d_model
+    ratio = (cfg.n_layers * per_layer + head) / (per_layer + head)
+    return times, toks, ratio, O.threads()
+
+
+def cpu_baseline(cfg, workload, W, N, G, prompt, acc_per_step, steps=2):
+    times, toks, ratio, cores = oracle_sample(cfg, W, N, G, prompt, steps, PRESEED.get(workload, False))
+    full_step_s = float(np.mean(times)) * ratio
+    return {"value": round(acc_per_step / full_step_s, 5), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{steps} oracle lookahead steps (T={1 + (W + G) * (N - 1)} rows) on a 1-layer slice of the "
+                      f"{workload} model after prefilling the {len(prompt)}-token prompt; step time scaled x{ratio:.2f} "
+                      f"(full-depth/slice FLOPs) to {full_step_s:.1f} s; tokens/step from the GPU run "
+                      f"({acc_per_step:.3f})"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    cfg = I.MODELS[args.workload]
+    W, N, G = I.LOOKAHEAD[args.workload]
+    prompt = I.make_prompt(args.workload)
+    # every step is one oracle step on the 1-layer slice (bounded sample)
+    times, toks, ratio, cores = oracle_sample(cfg, W, N, G, prompt, args.warmup + args.steps,
+                                              PRESEED.get(args.workload, False))
+    t = times[args.warmup:]
+    full_s = float(np.sum(t)) * ratio
+    # tokens: the slice model's own accepted tokens over the timed steps
+    value = (toks * len(t) / len(times)) / full_s
+    return {"impl": "reference", "metric": "effective tokens/s & step latency at batch 1 vs step roofline; "
+            "accepted tok/step", "value": round(value, 5), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * full_s / len(t), 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (random-init weights)",
+            "config": {"workload": args.workload, "global_batch": 1, "seq_len": len(prompt) + GEN_TOKENS[args.workload],
+                       "parallelism": "cpu"},
+            "cpu_baseline": {"value": round(value, 5), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"each step = one oracle lookahead step on a 1-layer slice, time scaled "
+                                       f"x{ratio:.2f} to full depth; tokens from the slice model's own acceptance"},
+            "e2e": {"value": round(value, 5), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, world = dist_setup(args.gpus if args.impl == "ours" else 0)
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        out = run_ours(args, rank, world)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -53,6 +53,7 @@ extern "C" {
 #define LA_DEBUG_LOGITS 2   /* keep the last step's fp32 logits for la_debug_logits */
 #define LA_NO_GRAPH 4       /* launch kernels directly instead of a CUDA graph      */
 #define LA_SIMT 8           /* bf16 model on the SIMT kernels (debug)               */
+#define LA_PROFILE 16       /* time kernel classes with CUDA events (la_get_profile) */
 
 typedef struct la_ctx la_ctx;
 
@@ -88,7 +89,21 @@ typedef struct la_stats {
     int P;                    /* tokens whose KV is cached                   */
     int rows;                 /* T rows per step                             */
     float last_step_ms;       /* device time of the last step (CUDA events)  */
+    int kernels_per_step;     /* kernel launches in one captured step        */
 } la_stats;
+
+/* Per-kernel-class timing (LA_PROFILE): CUDA events recorded on the launching
+ * stream around every launch of the class, summed over the steps so far.
+ * bytes / flops are the ALGORITHMIC traffic and work of those launches
+ * (weights once, the rows' activations in and out once; attention: the KV
+ * cache once plus the rows' q, k, v and output). */
+typedef struct la_prof_entry {
+    char name[24];
+    long long launches;
+    double total_ms;
+    double bytes;
+    double flops;
+} la_prof_entry;
 
 /* Bytes of device workspace la_create needs for this model and (W,N,G):
  * KV cache, per-layer step K/V, activations, row tables, window and pool.
@@ -121,6 +136,9 @@ LA_API int la_step(la_ctx* ctx, int32_t* out, int cap, int* n_out);
 LA_API int la_generate(la_ctx* ctx, const int32_t* prompt, int len, int max_new, int32_t* out, int* n_out);
 
 LA_API int la_get_stats(la_ctx* ctx, la_stats* out);
+/* Copy up to cap entries (one per kernel class seen); *n_out = entries written.
+ * LA_ERR_STATE unless the context was made with LA_PROFILE. */
+LA_API int la_get_profile(la_ctx* ctx, la_prof_entry* out, int cap, int* n_out);
 
 /* ---- debug accessors (host copies of device state, after a step) ---- */
 

@@ -22,9 +22,10 @@ LIB_PATH = os.path.join(_HERE, "liblookahead.so")
 
 LA_OK, LA_ERR_ARG, LA_ERR_OOM, LA_ERR_CAPACITY, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_ERR_STATE = 0, -1, -2, -3, -4, -5, -6
 LA_FP32, LA_BF16 = 0, 1
-LA_PRESEED_PROMPT, LA_DEBUG_LOGITS, LA_NO_GRAPH, LA_SIMT = 1, 2, 4, 8
+LA_PRESEED_PROMPT, LA_DEBUG_LOGITS, LA_NO_GRAPH, LA_SIMT, LA_PROFILE = 1, 2, 4, 8, 16
 
 EXPORTS = ("la_workspace_bytes", "la_create", "la_prefill", "la_step", "la_generate", "la_get_stats",
+           "la_get_profile",
            "la_debug_logits", "la_debug_argmax", "la_debug_rows", "la_debug_pool", "la_debug_window",
            "la_last_error", "la_destroy", "la_pool_create", "la_pool_insert", "la_pool_lookup", "la_pool_size",
            "la_pool_destroy")
@@ -47,7 +48,12 @@ class la_model_desc(C.Structure):
 class la_stats(C.Structure):
     _fields_ = [("steps", C.c_longlong), ("emitted", C.c_longlong), ("prefill_tokens", C.c_longlong),
                 ("accept_hist", C.c_longlong * 9), ("P", C.c_int), ("rows", C.c_int),
-                ("last_step_ms", C.c_float)]
+                ("last_step_ms", C.c_float), ("kernels_per_step", C.c_int)]
+
+
+class la_prof_entry(C.Structure):
+    _fields_ = [("name", C.c_char * 24), ("launches", C.c_longlong), ("total_ms", C.c_double),
+                ("bytes", C.c_double), ("flops", C.c_double)]
 
 
 _lib = None
@@ -69,6 +75,7 @@ def lib():
             "la_step": (i32, [vp, vp, i32, vp]),
             "la_generate": (i32, [vp, vp, i32, i32, vp, vp]),
             "la_get_stats": (i32, [vp, vp]),
+            "la_get_profile": (i32, [vp, vp, i32, vp]),
             "la_debug_logits": (i32, [vp, vp, sz]),
             "la_debug_argmax": (i32, [vp, vp, i32, vp]),
             "la_debug_rows": (i32, [vp, vp, vp, i32, vp, vp]),
@@ -138,7 +145,16 @@ def la_get_stats(ctx) -> dict:
     s = la_stats()
     _check(ctx, lib().la_get_stats(ctx, C.byref(s)))
     return {"steps": s.steps, "emitted": s.emitted, "prefill_tokens": s.prefill_tokens,
-            "accept_hist": list(s.accept_hist), "P": s.P, "rows": s.rows, "last_step_ms": s.last_step_ms}
+            "accept_hist": list(s.accept_hist), "P": s.P, "rows": s.rows, "last_step_ms": s.last_step_ms,
+            "kernels_per_step": s.kernels_per_step}
+
+
+def la_get_profile(ctx) -> dict:
+    arr = (la_prof_entry * 16)()
+    n = C.c_int()
+    _check(ctx, lib().la_get_profile(ctx, arr, 16, C.byref(n)))
+    return {arr[i].name.decode(): {"launches": arr[i].launches, "total_ms": arr[i].total_ms,
+                                   "bytes": arr[i].bytes, "flops": arr[i].flops} for i in range(n.value)}
 
 
 def la_debug_logits(ctx, T: int, V: int) -> np.ndarray:
@@ -278,6 +294,9 @@ class Decoder:
 
     def stats(self):
         return la_get_stats(self.ctx)
+
+    def profile(self):
+        return la_get_profile(self.ctx)
 
     def logits(self):
         return la_debug_logits(self.ctx, self.T, self.cfg.vocab)

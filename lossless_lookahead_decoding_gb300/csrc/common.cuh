@@ -120,3 +120,56 @@ void launch_attn_simt(cudaStream_t s, const DState* st, RowSet rs, const int* po
 void launch_argmax(cudaStream_t s, const float* logits, int* amax, int rows, int V);
 
 }  // namespace la
+
+#include <vector>
+
+namespace la {
+
+// Optional per-kernel-class timing: CUDA event pairs recorded on the launching
+// stream around each instrumented launch (also inside a captured graph).
+enum ProfClass {
+    P_GEMM_QKV = 0, P_GEMM_O, P_GEMM_GU, P_GEMM_DOWN, P_GEMM_LM, P_GEMM_EPI, P_ATTN, P_NORM, P_CONTROL, P_NCLS
+};
+
+struct ProfPoint {
+    int cls;
+    double bytes, flops;  // algorithmic per launch (attention: filled per step)
+    cudaEvent_t a, b;
+};
+
+struct Profiler {
+    bool on = false;
+    std::vector<ProfPoint> pts;
+    size_t idx = 0;
+    double ms[P_NCLS] = {}, bytes[P_NCLS] = {}, flops[P_NCLS] = {};
+    long long n[P_NCLS] = {};
+    void begin(cudaStream_t s)
+    {
+        if (!on) return;
+        if (idx == pts.size()) {
+            ProfPoint p{};
+            cudaEventCreate(&p.a);
+            cudaEventCreate(&p.b);
+            pts.push_back(p);
+        }
+        cudaEventRecord(pts[idx].a, s);
+    }
+    void end(cudaStream_t s, int cls, double by, double fl)
+    {
+        if (!on) return;
+        ProfPoint& p = pts[idx++];
+        p.cls = cls;
+        p.bytes = by;
+        p.flops = fl;
+        cudaEventRecord(p.b, s);
+    }
+    ~Profiler()
+    {
+        for (auto& p : pts) {
+            cudaEventDestroy(p.a);
+            cudaEventDestroy(p.b);
+        }
+    }
+};
+
+}  // namespace la

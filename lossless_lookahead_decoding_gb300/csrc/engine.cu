@@ -72,6 +72,8 @@ struct la_ctx {
     DState* st = nullptr;
     DState* h_st = nullptr;
     TcPlan tc{};
+    Profiler prof;
+    int kernels_per_step = 0;
     // host side
     bool prefilled = false, have_step = false;
     int P_host = 0;
@@ -179,7 +181,9 @@ static void forward(la_ctx* c, int rows, const RowSet& rs, bool logits)
         T* VS = (T*)c->VS + (size_t)l * kRows * dkv;
         const T* KC = (const T*)c->KC + (size_t)l * dkv * d.max_seq;
         const T* VC = (const T*)c->VC + (size_t)l * dkv * d.max_seq;
+        c->prof.begin(s);
         launch_rmsnorm<T>(s, c->X, w[0], XN, rows, D, d.rms_eps);
+        c->prof.end(s, P_NORM, 0, 0);
         if (c->use_tc) {
             tc_qkv_rope(c->tc, s, l, rows, c->pos, c->cosb, c->sinb, (void*)Q, (void*)KS, (void*)VS);
         } else {
@@ -189,17 +193,21 @@ static void forward(la_ctx* c, int rows, const RowSet& rs, bool logits)
             launch_gemm_simt_f32out<T>(s, XN, w[3], c->QKV32 + dq + dkv, ld, rows, D, dkv);
             launch_rope_split<T>(s, c->QKV32, c->pos, c->cosb, c->sinb, Q, KS, VS, rows, H, Hkv, hd);
         }
+        c->prof.begin(s);
         if (c->use_tc && tc_attn_supported(c->tc))
             tc_attention(c->tc, s, c->st, rs, c->pos, (const void*)Q, (const void*)KC, (const void*)VC,
                          (const void*)KS, (const void*)VS, (void*)ATT, rows);
         else
             launch_attn_simt<T>(s, c->st, rs, c->pos, Q, KC, VC, KS, VS, ATT, rows, H, Hkv, hd, d.max_seq, scale);
+        c->prof.end(s, P_ATTN, rows, 0);  // bytes filled in per step (they depend on P)
         if (c->use_tc) {
             tc_oproj_resid(c->tc, s, l, rows, c->X);
         } else {
             launch_gemm_simt_resid<T>(s, ATT, w[4], c->X, rows, dq, D);
         }
+        c->prof.begin(s);
         launch_rmsnorm<T>(s, c->X, w[5], XN, rows, D, d.rms_eps);
+        c->prof.end(s, P_NORM, 0, 0);
         if (c->use_tc) {
             tc_gateup_swiglu(c->tc, s, l, rows);
             tc_down_resid(c->tc, s, l, rows, c->X);
@@ -228,12 +236,54 @@ static void run_forward(la_ctx* c, int rows, const RowSet& rs, bool logits)
 // The step's launch sequence (no host synchronisation inside).
 static void enqueue_step(la_ctx* c)
 {
+    c->prof.idx = 0;
+    c->prof.begin(c->s);
     launch_build_rows(c->s, c->st, c->win, c->pool, c->W, c->N, c->G, c->T, c->rs_step.rel_pos, c->tok, c->pos);
+    c->prof.end(c->s, P_CONTROL, 0, 0);
     run_forward(c, c->T, c->rs_step, true);
+    c->prof.begin(c->s);
     launch_verify_update(c->s, c->st, c->tok, c->AMAX, c->win, c->pool, c->W, c->N, c->G);
     launch_commit(c->s, c->st, false, 0, c->N, c->KS, c->VS, c->KC, c->VC, c->d.n_layers, c->d.n_kv_heads,
                   c->d.head_dim, c->d.max_seq, c->esz);
+    c->prof.end(c->s, P_CONTROL, 0, 0);
     cudaMemcpyAsync(c->h_st, c->st, sizeof(DState), cudaMemcpyDeviceToHost, c->s);
+}
+
+// Accumulate the last step's event timings (P_before = the step's cache length).
+static void collect_profile(la_ctx* c, int P_before)
+{
+    Profiler& pr = c->prof;
+    const double esz = c->esz, dq = c->dq, dkv = c->dkv, T = c->T;
+    for (size_t i = 0; i < pr.idx; i++) {
+        ProfPoint& p = pr.pts[i];
+        float ms = 0.f;
+        cudaEventElapsedTime(&ms, p.a, p.b);
+        double by = p.bytes, fl = p.flops;
+        if (p.cls == P_ATTN) {
+            // the cache [0,P) once per KV head, plus the rows' q, k, v and output
+            by = (2.0 * P_before * dkv + T * (2 * dq + 2 * dkv)) * esz;
+            fl = 4.0 * T * (P_before + 1) * dq;
+        }
+        pr.ms[p.cls] += ms;
+        pr.bytes[p.cls] += by;
+        pr.flops[p.cls] += fl;
+        pr.n[p.cls] += 1;
+    }
+}
+
+// Count the kernel nodes of one captured step (the launches a step makes).
+static int count_kernels(cudaGraph_t g)
+{
+    size_t n = 0;
+    if (cudaGraphGetNodes(g, nullptr, &n) != cudaSuccess || n == 0) return 0;
+    std::vector<cudaGraphNode_t> nodes(n);
+    if (cudaGraphGetNodes(g, nodes.data(), &n) != cudaSuccess) return 0;
+    int k = 0;
+    for (size_t i = 0; i < n; i++) {
+        cudaGraphNodeType t;
+        if (cudaGraphNodeGetType(nodes[i], &t) == cudaSuccess && t == cudaGraphNodeTypeKernel) k++;
+    }
+    return k;
 }
 
 extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* workspace, size_t ws_bytes,
@@ -376,7 +426,9 @@ extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* w
     ctx->rs_step = RowSet{rs1, rs1 + kRows, map1, maxoff, ngrp};
     ctx->rs_pre = RowSet{rs2, rs2 + kRows, map2, kRows, 1};
     if (rc == LA_OK && ctx->bf16 && !(flags & LA_SIMT)) {
-        int trc = tc_plan_create(&ctx->tc, ctx->d, ctx->lw.data(), ctx->XN, ctx->Q, ctx->ATT, ctx->HID, ctx->esz);
+        int trc = tc_plan_create(&ctx->tc, ctx->d, ctx->lw.data(), ctx->XN, ctx->Q, ctx->ATT, ctx->HID, ctx->esz,
+                                 &ctx->st->status);
+        ctx->tc.prof = &ctx->prof;
         if (trc == 0) ctx->use_tc = true;
         else if (trc < 0) {
             ctx->err = "tcgen05 plan creation failed";
@@ -389,6 +441,7 @@ extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* w
         return rc;
     }
     ctx->stats.rows = ctx->T;
+    ctx->prof.on = (flags & LA_PROFILE) != 0;
     *out = ctx;
     return LA_OK;
 }
@@ -480,6 +533,7 @@ extern "C" int la_step(la_ctx* ctx, int32_t* out, int cap, int* n_out)
                 ctx->err = std::string("graph capture: ") + cudaGetErrorString(e);
                 return LA_ERR_CUDA;
             }
+            ctx->kernels_per_step = count_kernels(g);
             e = cudaGraphInstantiate(&ctx->gexec, g, 0);
             cudaGraphDestroy(g);
             if (e != cudaSuccess) {
@@ -510,6 +564,8 @@ extern "C" int la_step(la_ctx* ctx, int32_t* out, int cap, int* n_out)
     ctx->stats.accept_hist[n]++;
     ctx->stats.P = h.P;
     ctx->stats.last_step_ms = ms;
+    ctx->stats.kernels_per_step = ctx->kernels_per_step;
+    if (ctx->prof.on) collect_profile(ctx, h.P_before);
     return LA_OK;
 }
 
@@ -529,6 +585,27 @@ extern "C" int la_generate(la_ctx* ctx, const int32_t* prompt, int len, int max_
     }
     *n_out = n;
     return rc;
+}
+
+extern "C" int la_get_profile(la_ctx* ctx, la_prof_entry* out, int cap, int* n_out)
+{
+    static const char* names[P_NCLS] = {"gemm_qkv", "gemm_o",    "gemm_gateup", "gemm_down", "gemm_lmhead",
+                                        "gemm_epilogue", "attention", "rmsnorm", "control"};
+    if (!ctx || !out || !n_out) return LA_ERR_ARG;
+    if (!ctx->prof.on) return fail(ctx, LA_ERR_STATE, "context made without LA_PROFILE");
+    int n = 0;
+    for (int c = 0; c < P_NCLS && n < cap; c++) {
+        if (!ctx->prof.n[c]) continue;
+        la_prof_entry& e = out[n++];
+        memset(&e, 0, sizeof(e));
+        snprintf(e.name, sizeof(e.name), "%s", names[c]);
+        e.launches = ctx->prof.n[c];
+        e.total_ms = ctx->prof.ms[c];
+        e.bytes = ctx->prof.bytes[c];
+        e.flops = ctx->prof.flops[c];
+    }
+    *n_out = n;
+    return LA_OK;
 }
 
 extern "C" int la_get_stats(la_ctx* ctx, la_stats* out)

@@ -486,7 +486,7 @@ struct Impl {
     GemmCfg lm;
     float* partial = nullptr;
     size_t partial_bytes = 0;
-    int* err = nullptr;  // points at the step's status word? (set per call)
+    int* err = nullptr;  // the context's device status word
     void* Q = nullptr;
     void* HID = nullptr;
 };
@@ -529,10 +529,26 @@ void finish_cfg(GemmCfg& g, int K, int sms)
 
 size_t partial_need(const GemmCfg& g) { return (size_t)(g.ctas + g.tiles) * kRows * kBM * 4; }
 
-void launch_gemm(const Impl& im, const GemmCfg& g, cudaStream_t s, int rows, int* err)
+void launch_gemm(const TcPlan& p, const GemmCfg& g, cudaStream_t s, int rows, int cls)
 {
-    GemmArgs a{g.tiles, g.KB, g.ctas, g.mode, g.t0, g.t1, rows, im.partial, err};
+    const Impl& im = *(const Impl*)p.impl;
+    GemmArgs a{g.tiles, g.KB, g.ctas, g.mode, g.t0, g.t1, rows, im.partial, im.err};
+    if (p.prof) p.prof->begin(s);
     k_gemm_tc<<<g.ctas, kThreads, kSmemBytes, s>>>(g.a[0], g.a[1], g.a[2], g.b, a);
+    if (p.prof) {
+        // algorithmic: every weight once, the rows' inputs once, the rows' outputs once
+        const double K = (double)g.KB * kBK, Nw = (double)g.tiles * (g.mode == MODE_PAIR ? 2 * 64 : kBM);
+        const double by = Nw * K * 2 + (double)rows * K * 2 + (double)rows * Nw * 2;
+        p.prof->end(s, cls, by, 2.0 * rows * K * Nw);
+    }
+}
+
+template <typename F>
+void launch_epi(const TcPlan& p, cudaStream_t s, F f)
+{
+    if (p.prof) p.prof->begin(s);
+    f();
+    if (p.prof) p.prof->end(s, P_GEMM_EPI, 0, 0);
 }
 
 EpiArgs epi_base(const Impl& im, const GemmCfg& g, int rows)
@@ -552,7 +568,7 @@ dim3 epi_grid(const GemmCfg& g, int rows) { return dim3(g.tiles, (rows + kEpiRow
 }  // namespace
 
 int tc_plan_create(TcPlan* p, const la_model_desc& d, const void* const* lw, void* XN, void* Q, void* ATT, void* HID,
-                   int esz)
+                   int esz, int* status)
 {
     p->ok = false;
     p->impl = nullptr;
@@ -643,9 +659,9 @@ int tc_plan_create(TcPlan* p, const la_model_desc& d, const void* const* lw, voi
         delete im;
         return 1;
     }
+    im->err = status;
     if (cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess ||
-        cudaMalloc((void**)&im->partial, need) != cudaSuccess || cudaMalloc((void**)&im->err, 4) != cudaSuccess ||
-        cudaMemset(im->err, 0, 4) != cudaSuccess) {
+        cudaMalloc((void**)&im->partial, need) != cudaSuccess) {
         if (im->partial) cudaFree(im->partial);
         delete im;
         return -1;
@@ -661,7 +677,6 @@ void tc_plan_destroy(TcPlan* p)
     if (p->impl) {
         Impl* im = (Impl*)p->impl;
         if (im->partial) cudaFree(im->partial);
-        if (im->err) cudaFree(im->err);
         delete im;
     }
     p->impl = nullptr;
@@ -675,7 +690,7 @@ void tc_qkv_rope(const TcPlan& p, cudaStream_t s, int layer, int rows, const int
 {
     const Impl& im = *(const Impl*)p.impl;
     const GemmCfg& g = im.qkv[layer];
-    launch_gemm(im, g, s, rows, im.err);
+    launch_gemm(p, g, s, rows, P_GEMM_QKV);
     EpiArgs e = epi_base(im, g, rows);
     e.dq = im.dq;
     e.dkv = im.dkv;
@@ -686,7 +701,7 @@ void tc_qkv_rope(const TcPlan& p, cudaStream_t s, int layer, int rows, const int
     e.Q = (__nv_bfloat16*)Q;
     e.KS = (__nv_bfloat16*)KS;
     e.VS = (__nv_bfloat16*)VS;
-    k_gemm_epi<EPI_QKV><<<epi_grid(g, rows), 128, 0, s>>>(e);
+    launch_epi(p, s, [&] { k_gemm_epi<EPI_QKV><<<epi_grid(g, rows), 128, 0, s>>>(e); });
 }
 
 bool tc_attn_supported(const TcPlan&) { return false; }
@@ -700,42 +715,44 @@ void tc_oproj_resid(const TcPlan& p, cudaStream_t s, int layer, int rows, float*
 {
     const Impl& im = *(const Impl*)p.impl;
     const GemmCfg& g = im.oproj[layer];
-    launch_gemm(im, g, s, rows, im.err);
+    launch_gemm(p, g, s, rows, P_GEMM_O);
     EpiArgs e = epi_base(im, g, rows);
     e.X = X;
-    k_gemm_epi<EPI_RESID><<<epi_grid(g, rows), 128, 0, s>>>(e);
+    launch_epi(p, s, [&] { k_gemm_epi<EPI_RESID><<<epi_grid(g, rows), 128, 0, s>>>(e); });
 }
 
 void tc_gateup_swiglu(const TcPlan& p, cudaStream_t s, int layer, int rows)
 {
     const Impl& im = *(const Impl*)p.impl;
     const GemmCfg& g = im.gateup[layer];
-    launch_gemm(im, g, s, rows, im.err);
+    launch_gemm(p, g, s, rows, P_GEMM_GU);
     EpiArgs e = epi_base(im, g, rows);
     e.H = (__nv_bfloat16*)im.HID;
-    k_gemm_epi<EPI_SWIGLU><<<epi_grid(g, rows), 128, 0, s>>>(e);
+    launch_epi(p, s, [&] { k_gemm_epi<EPI_SWIGLU><<<epi_grid(g, rows), 128, 0, s>>>(e); });
 }
 
 void tc_down_resid(const TcPlan& p, cudaStream_t s, int layer, int rows, float* X)
 {
     const Impl& im = *(const Impl*)p.impl;
     const GemmCfg& g = im.down[layer];
-    launch_gemm(im, g, s, rows, im.err);
+    launch_gemm(p, g, s, rows, P_GEMM_DOWN);
     EpiArgs e = epi_base(im, g, rows);
     e.X = X;
-    k_gemm_epi<EPI_RESID><<<epi_grid(g, rows), 128, 0, s>>>(e);
+    launch_epi(p, s, [&] { k_gemm_epi<EPI_RESID><<<epi_grid(g, rows), 128, 0, s>>>(e); });
 }
 
 void tc_lmhead_argmax(const TcPlan& p, cudaStream_t s, int rows, float* logits, unsigned long long* amaxp, int* amax)
 {
     const Impl& im = *(const Impl*)p.impl;
     const GemmCfg& g = im.lm;
-    launch_gemm(im, g, s, rows, im.err);
+    launch_gemm(p, g, s, rows, P_GEMM_LM);
     EpiArgs e = epi_base(im, g, rows);
     e.logits = logits;
     e.amaxp = amaxp;
-    k_gemm_epi<EPI_LOGITS><<<epi_grid(g, rows), 128, 0, s>>>(e);
-    k_argmax_unpack<<<1, kRows, 0, s>>>(amaxp, amax, rows);
+    launch_epi(p, s, [&] {
+        k_gemm_epi<EPI_LOGITS><<<epi_grid(g, rows), 128, 0, s>>>(e);
+        k_argmax_unpack<<<1, kRows, 0, s>>>(amaxp, amax, rows);
+    });
 }
 
 }  // namespace la

@@ -11,12 +11,14 @@ namespace la {
 
 struct TcPlan {
     bool ok = false;
-    void* impl = nullptr;  // owned state (tensor maps, split-K scratch)
+    void* impl = nullptr;        // owned state (tensor maps, split-K scratch)
+    Profiler* prof = nullptr;    // optional kernel timing
 };
 
-// 0 = plan made, 1 = shape not supported (caller falls back to SIMT), < 0 error
+// 0 = plan made, 1 = shape not supported (caller falls back to SIMT), < 0 error.
+// status: device word that bounded waits set to LA_ERR_TIMEOUT on give-up.
 int tc_plan_create(TcPlan* p, const la_model_desc& d, const void* const* lw, void* XN, void* Q, void* ATT, void* HID,
-                   int esz);
+                   int esz, int* status);
 void tc_plan_destroy(TcPlan* p);
 void tc_qkv_rope(const TcPlan& p, cudaStream_t s, int layer, int rows, const int* pos, const float* cosb,
                  const float* sinb, void* Q, void* KS, void* VS);

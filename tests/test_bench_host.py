@@ -1,0 +1,57 @@
+"""Host-side logic of bench.py: the replica aggregation across ranks (two gloo
+ranks on CPU), and the step roofline arithmetic against the pages' shapes."""
+import os
+import socket
+
+import pytest
+
+import bench
+import la_inputs as I
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    tok, sec = bench.aggregate(100.0 * (rank + 1), 1.0 + rank)
+    bench.barrier()
+    q.put((rank, tok, sec))
+    dist.destroy_process_group()
+
+
+def test_replica_aggregation_gloo_two_ranks():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    ps = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    for p in ps:
+        p.join(60)
+    res = sorted(q.get(timeout=10) for _ in range(2))
+    # tokens sum over replicas, time is the slowest rank's
+    assert res == [(0, 300.0, 2.0), (1, 300.0, 2.0)]
+
+
+def test_single_process_aggregation_is_identity():
+    assert bench.aggregate(7.0, 0.5) == (7.0, 0.5)
+
+
+@pytest.mark.parametrize("name,T", [("7b", 121), ("13b", 81), ("34b", 57)])
+def test_step_shapes_and_roofline_inputs(name, T):
+    cfg = I.MODELS[name]
+    W, N, G = I.LOOKAHEAD[name]
+    assert 1 + (W + G) * (N - 1) == T
+    by, fl = bench.step_model(cfg, T, 512)
+    # weights dominate the bytes; FLOPs ~ 2 * params * T
+    assert by > cfg.streamed_params() * 2
+    assert fl > 2 * cfg.streamed_params() * T
+    # arithmetic intensity is below the GB300 ridge (~290 FLOP/B): HBM bound
+    assert fl / by < 290
