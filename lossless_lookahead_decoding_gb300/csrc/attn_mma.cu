@@ -1,0 +1,501 @@
+// attn_mma.cu -- masked lookahead / verification attention on tensor cores.
+//
+// The combined step's rows attend to the KV cache [0,P) (shared by every
+// row) and to a few in-step rows: row r of group g sees, at position P + o
+// (o <= rel_pos[r]), the step row grp_map[g][o] (the 2D-window + verification
+// mask of the lookahead step; a prefill block is one causal group).
+//
+// Keys are walked in chunks of 64 ABSOLUTE positions; chunks are grouped into
+// fixed splits of 256 positions (one CTA per head and split) whose partial
+// softmax states (max, sum, unnormalised output) are merged in ascending
+// split order by a second kernel.  Inside a chunk, S = Q K^T and O += P V run
+// on bf16 mma.sync tiles with fp32 accumulation.  A chunk that lies entirely
+// below P is shared by all rows (16-row slabs, one per warp); a chunk that
+// reaches P is a "tail" chunk: for every row group the warp builds the
+// chunk's 64 key slots from the cache (positions < P) and from that group's
+// step rows (positions >= P) by per-lane ldmatrix row addresses, so that slot
+// j always holds position c*64 + j.  Every row therefore sees exactly the
+// arithmetic it would see if it were decoded alone by plain greedy decoding
+// (chunk and split boundaries at the same absolute positions, same
+// instruction shapes, same reduction order), which keeps lookahead output
+// identical to greedy output.
+#include "common.cuh"
+
+namespace la {
+
+namespace {
+
+constexpr int kChunk = 64;
+constexpr int kSplit = 256;
+constexpr int kWarps = 8;
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0));
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;"); }
+template <int N>
+__device__ __forceinline__ void cp_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t* r, uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t* r, uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void mma16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Row-major tile of HD bf16 per row, 16-byte chunks XOR-swizzled by row & 7.
+template <int HD>
+__device__ __forceinline__ uint32_t swz(uint32_t base, int row, int chunk)
+{
+    return base + row * (HD * 2) + ((chunk ^ (row & 7)) << 4);
+}
+
+// Softmax state of the two rows (g, g+8) a thread holds in a 16-row slab.
+template <int HD>
+struct SlabState {
+    float m[2], l[2];
+    float o[HD / 8][4];
+};
+
+// One 64-key chunk for one 16-row slab.  kaddr(j)/vaddr(j) give the shared
+// address of key slot j's row; vis(half, j) says whether the thread's row
+// (g or g+8) sees slot j.  The arithmetic is identical for shared and tail
+// chunks.
+template <int HD, bool MASKED, typename KA, typename VISF>
+__device__ __forceinline__ void chunk_update(const uint32_t (*qf)[4], SlabState<HD>& st, KA kaddr, KA vaddr, VISF vis,
+                                             float sl2)
+{
+    const int lane = threadIdx.x & 31;
+    float s[8][4];
+#pragma unroll
+    for (int n = 0; n < 8; n++) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < HD / 16; ks++) {
+#pragma unroll
+        for (int n2 = 0; n2 < 4; n2++) {
+            uint32_t b[4];
+            const int key = n2 * 16 + (lane & 7) + ((lane >> 4) << 3);
+            ldsm_x4(b, kaddr(key) + ((((2 * ks + ((lane >> 3) & 1)) ^ (kaddr.row(key) & 7))) << 4));
+            mma16816(s[2 * n2], qf[ks], b[0], b[1]);
+            mma16816(s[2 * n2 + 1], qf[ks], b[2], b[3]);
+        }
+    }
+    const int t = lane & 3;
+    float cm[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int n = 0; n < 8; n++) {
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            float v = s[n][i] * sl2;
+            if (MASKED && !vis(i >> 1, n * 8 + 2 * t + (i & 1))) v = -INFINITY;
+            s[n][i] = v;
+            cm[i >> 1] = fmaxf(cm[i >> 1], v);
+        }
+    }
+    float alpha[2], mu[2], rs[2] = {0.f, 0.f};
+#pragma unroll
+    for (int h = 0; h < 2; h++) {
+        cm[h] = fmaxf(cm[h], __shfl_xor_sync(0xffffffffu, cm[h], 1));
+        cm[h] = fmaxf(cm[h], __shfl_xor_sync(0xffffffffu, cm[h], 2));
+        const float mn = fmaxf(st.m[h], cm[h]);
+        mu[h] = (mn == -INFINITY) ? 0.f : mn;
+        alpha[h] = exp2f(st.m[h] - mu[h]);
+        st.m[h] = mn;
+    }
+#pragma unroll
+    for (int n = 0; n < 8; n++) {
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const float p = exp2f(s[n][i] - mu[i >> 1]);
+            s[n][i] = p;
+            rs[i >> 1] += p;
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; h++) {
+        rs[h] += __shfl_xor_sync(0xffffffffu, rs[h], 1);
+        rs[h] += __shfl_xor_sync(0xffffffffu, rs[h], 2);
+        st.l[h] = st.l[h] * alpha[h] + rs[h];
+    }
+#pragma unroll
+    for (int d = 0; d < HD / 8; d++) {
+        st.o[d][0] *= alpha[0];
+        st.o[d][1] *= alpha[0];
+        st.o[d][2] *= alpha[1];
+        st.o[d][3] *= alpha[1];
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; kk++) {
+        uint32_t a[4];
+        a[0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
+        a[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
+        a[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+        a[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+        const int key = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+        for (int d2 = 0; d2 < HD / 16; d2++) {
+            uint32_t b[4];
+            ldsm_x4_t(b, vaddr(key) + ((((2 * d2 + (lane >> 4)) ^ (vaddr.row(key) & 7))) << 4));
+            mma16816(st.o[2 * d2], a, b[0], b[1]);
+            mma16816(st.o[2 * d2 + 1], a, b[2], b[3]);
+        }
+    }
+}
+
+// Key-slot addressing: the row base address (unswizzled) and the row index
+// that sets the swizzle phase.
+template <int HD>
+struct TileAddr {  // slot j -> row j of a contiguous tile
+    uint32_t base;
+    __device__ __forceinline__ uint32_t operator()(int j) const { return base + j * (HD * 2); }
+    __device__ __forceinline__ int row(int j) const { return j; }
+};
+
+template <int HD>
+struct GatherAddr {  // slot j -> cache tile row, step row, or the zero row
+    uint32_t tile, step, zero;
+    int c0, P, tile0, maxoff;
+    const int* gmap;
+    __device__ __forceinline__ int src(int j, int* r) const
+    {
+        const int p = c0 + j;
+        if (p < P) {
+            *r = p - tile0;
+            return 0;
+        }
+        const int o = p - P;
+        if (o < maxoff) {
+            *r = gmap[o];
+            return 1;
+        }
+        *r = 0;
+        return 2;
+    }
+    __device__ __forceinline__ uint32_t operator()(int j) const
+    {
+        int r;
+        const int w = src(j, &r);
+        return w == 0 ? tile + r * (HD * 2) : (w == 1 ? step + r * (HD * 2) : zero);
+    }
+    __device__ __forceinline__ int row(int j) const
+    {
+        int r;
+        src(j, &r);
+        return r;
+    }
+};
+
+struct AttnArgs {
+    const DState* st;
+    RowSet rs;
+    const int* pos;
+    const __nv_bfloat16 *Q, *KC, *VC, *KS, *VS;
+    float* part;  // [H][nsplit][kRows][2 + HD]
+    __nv_bfloat16* out;
+    int rows, H, Hkv, max_seq, nsplit, max_rel;
+    float sl2;  // log2(e) / sqrt(hd)
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int RB = HD * 2, NCH = HD / 8, PS = 2 + HD;
+    uint8_t* sQ = smem;
+    uint8_t* sK0 = sQ + kRows * RB;
+    uint8_t* sV0 = sK0 + 2 * kChunk * RB;
+    uint8_t* sKS = sV0 + 2 * kChunk * RB;
+    uint8_t* sVS = sKS + kRows * RB;
+    uint8_t* sZero = sVS + kRows * RB;
+    int* gcnt = (int*)(sZero + RB);       // [kRows + 1] rows of each group (< a.rows)
+    int* gslab = gcnt + kRows + 1;        // [kRows + 1] slab prefix over groups
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int h = blockIdx.x, sp = blockIdx.y;
+    const int dq = a.H * HD, dkv = a.Hkv * HD, kvh = h / (a.H / a.Hkv);
+    const int P = a.st->P, maxpos = P + a.max_rel;
+    const int p0 = sp * kSplit;
+    if (p0 > maxpos) return;
+    const int c_begin = p0 / kChunk;
+    const int c_end = min(p0 + kSplit, maxpos + 1 + kChunk - 1) / kChunk;  // exclusive
+    const int c_shared_end = min(c_end, max(c_begin, P / kChunk));
+    const __nv_bfloat16* kc = a.KC + (size_t)kvh * a.max_seq * HD;
+    const __nv_bfloat16* vc = a.VC + (size_t)kvh * a.max_seq * HD;
+    float* part = a.part + ((size_t)h * a.nsplit + sp) * kRows * PS;
+
+    // Q tile of this head (rows beyond a.rows are zero)
+    for (int i = tid; i < kRows * NCH; i += blockDim.x) {
+        const int r = i / NCH, c = i % NCH;
+        const bool ok = r < a.rows;
+        cp_async16(swz<HD>(su32(sQ), r, c), a.Q + (size_t)(ok ? r : 0) * dq + h * HD + c * 8, ok);
+    }
+    auto load_chunk = [&](int cidx, int buf, int valid_end) {
+        uint8_t* dk = sK0 + buf * kChunk * RB;
+        uint8_t* dv = sV0 + buf * kChunk * RB;
+        for (int i = tid; i < kChunk * NCH; i += blockDim.x) {
+            const int r = i / NCH, c = i % NCH, p = cidx * kChunk + r;
+            const bool ok = p < valid_end;
+            const size_t off = (size_t)(ok ? p : 0) * HD + c * 8;
+            cp_async16(swz<HD>(su32(dk), r, c), kc + off, ok);
+            cp_async16(swz<HD>(su32(dv), r, c), vc + off, ok);
+        }
+    };
+    const int n_shared = c_shared_end - c_begin;
+    if (n_shared > 0) load_chunk(c_begin, 0, P);
+    cp_commit();
+
+    SlabState<HD> st;
+    st.m[0] = st.m[1] = -INFINITY;
+    st.l[0] = st.l[1] = 0.f;
+#pragma unroll
+    for (int d = 0; d < HD / 8; d++) st.o[d][0] = st.o[d][1] = st.o[d][2] = st.o[d][3] = 0.f;
+
+    uint32_t qf[HD / 16][4];
+    for (int i = 0; i < n_shared; i++) {
+        if (i + 1 < n_shared) load_chunk(c_begin + i + 1, (i + 1) & 1, P);
+        cp_commit();
+        cp_wait<1>();
+        __syncthreads();
+        if (warp * 16 < a.rows) {  // slabs of padding rows only are skipped
+            if (i == 0) {
+#pragma unroll
+                for (int ks = 0; ks < HD / 16; ks++)
+                    ldsm_x4(qf[ks], swz<HD>(su32(sQ), warp * 16 + (lane & 7) + (((lane >> 3) & 1) << 3),
+                                            2 * ks + (lane >> 4)));
+            }
+            TileAddr<HD> ka{su32(sK0 + (i & 1) * kChunk * RB)}, va{su32(sV0 + (i & 1) * kChunk * RB)};
+            chunk_update<HD, false>(qf, st, ka, va, [](int, int) { return true; }, a.sl2);
+        }
+        __syncthreads();
+    }
+    // state after the shared chunks -> this split's partial (read back below
+    // by the tail phase, which may regroup the rows)
+    {
+        const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++) {
+            const int r = warp * 16 + g + 8 * hh;
+            if (r < a.rows) {
+                float* pr = part + (size_t)r * PS;
+                if (t == 0) {
+                    pr[0] = st.m[hh];
+                    pr[1] = st.l[hh];
+                }
+#pragma unroll
+                for (int d = 0; d < HD / 8; d++) {
+                    pr[2 + d * 8 + 2 * t] = st.o[d][2 * hh];
+                    pr[2 + d * 8 + 2 * t + 1] = st.o[d][2 * hh + 1];
+                }
+            }
+        }
+    }
+    if (c_shared_end >= c_end) return;
+
+    // ---------------- tail chunks: per row group
+    cp_wait<0>();
+    __syncthreads();
+    const int tile0 = c_shared_end * kChunk;  // first tail chunk's cache rows
+    load_chunk(c_shared_end, 0, P);
+    for (int i = tid; i < kRows * NCH; i += blockDim.x) {
+        const int r = i / NCH, c = i % NCH;
+        const bool ok = r < a.rows;
+        const size_t off = (size_t)(ok ? r : 0) * dkv + kvh * HD + c * 8;
+        cp_async16(swz<HD>(su32(sKS), r, c), a.KS + off, ok);
+        cp_async16(swz<HD>(su32(sVS), r, c), a.VS + off, ok);
+    }
+    cp_commit();
+    if (tid < NCH) *(uint4*)(sZero + tid * 16) = make_uint4(0, 0, 0, 0);
+    // rows of each group, in row order (static lists, clipped to a.rows)
+    const int ng = a.rs.ngrp;
+    for (int g = tid; g < ng; g += blockDim.x) {
+        int n = 0;
+        for (int k = a.rs.grp_start[g]; k < a.rs.grp_start[g + 1]; k++) n += (a.rs.grp_rows[k] < a.rows);
+        gcnt[g] = n;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        gslab[0] = 0;
+        for (int g = 0; g < ng; g++) gslab[g + 1] = gslab[g] + (gcnt[g] + 15) / 16;
+    }
+    cp_wait<0>();
+    __syncthreads();
+    const int n_items = gslab[ng];
+    const int g4 = lane >> 2;
+    for (int it = warp; it < n_items; it += kWarps) {
+        int g = 0;
+        while (gslab[g + 1] <= it) g++;
+        const int* glist = a.rs.grp_rows + a.rs.grp_start[g];
+        const int r_begin = (it - gslab[g]) * 16, r_end = gcnt[g];
+        // rows of this slab (-1 = padding)
+        const int rA = (r_begin + g4 < r_end) ? glist[r_begin + g4] : -1;
+        const int rB = (r_begin + g4 + 8 < r_end) ? glist[r_begin + g4 + 8] : -1;
+        const int posA = rA >= 0 ? a.pos[rA] : -1, posB = rB >= 0 ? a.pos[rB] : -1;
+        // Q fragments of the gathered rows
+        {
+            const int li = (lane & 7) + (((lane >> 3) & 1) << 3);
+            const int rq = (r_begin + li < r_end) ? glist[r_begin + li] : -1;
+#pragma unroll
+            for (int ks = 0; ks < HD / 16; ks++) {
+                const int ch = 2 * ks + (lane >> 4);
+                const uint32_t addr = rq >= 0 ? swz<HD>(su32(sQ), rq, ch) : su32(sZero) + (ch << 4);
+                ldsm_x4(qf[ks], addr);
+            }
+        }
+        // resume the rows' states
+        SlabState<HD> ts;
+        {
+            const int t = lane & 3;
+#pragma unroll
+            for (int hh = 0; hh < 2; hh++) {
+                const int r = hh ? rB : rA;
+                if (r >= 0) {
+                    const float* pr = part + (size_t)r * PS;
+                    ts.m[hh] = pr[0];
+                    ts.l[hh] = pr[1];
+#pragma unroll
+                    for (int d = 0; d < HD / 8; d++) {
+                        ts.o[d][2 * hh] = pr[2 + d * 8 + 2 * t];
+                        ts.o[d][2 * hh + 1] = pr[2 + d * 8 + 2 * t + 1];
+                    }
+                } else {
+                    ts.m[hh] = -INFINITY;
+                    ts.l[hh] = 0.f;
+#pragma unroll
+                    for (int d = 0; d < HD / 8; d++) ts.o[d][2 * hh] = ts.o[d][2 * hh + 1] = 0.f;
+                }
+            }
+        }
+        const int* gmap = a.rs.grp_map + (size_t)g * a.rs.maxoff;
+        for (int c = c_shared_end; c < c_end; c++) {
+            const int c0 = c * kChunk;
+            GatherAddr<HD> ka{su32(sK0), su32(sKS), su32(sZero), c0, P, tile0, a.rs.maxoff, gmap};
+            GatherAddr<HD> va{su32(sV0), su32(sVS), su32(sZero), c0, P, tile0, a.rs.maxoff, gmap};
+            chunk_update<HD, true>(qf, ts, ka, va,
+                                   [&](int hh, int j) { return c0 + j <= (hh ? posB : posA); }, a.sl2);
+        }
+        {
+            const int t = lane & 3;
+#pragma unroll
+            for (int hh = 0; hh < 2; hh++) {
+                const int r = hh ? rB : rA;
+                if (r >= 0) {
+                    float* pr = part + (size_t)r * PS;
+                    if (t == 0) {
+                        pr[0] = ts.m[hh];
+                        pr[1] = ts.l[hh];
+                    }
+#pragma unroll
+                    for (int d = 0; d < HD / 8; d++) {
+                        pr[2 + d * 8 + 2 * t] = ts.o[d][2 * hh];
+                        pr[2 + d * 8 + 2 * t + 1] = ts.o[d][2 * hh + 1];
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Merge the splits of every (row, head) in ascending split order.
+template <int HD>
+__global__ void k_attn_combine(AttnArgs a)
+{
+    const int r = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
+    constexpr int PS = 2 + HD;
+    const int ns = a.pos[r] / kSplit + 1;
+    const float* base = a.part + (size_t)h * a.nsplit * kRows * PS + (size_t)r * PS;
+    float m = base[0], l = base[1], o = base[2 + d];
+    for (int s = 1; s < ns; s++) {
+        const float* pr = base + (size_t)s * kRows * PS;
+        const float ms = pr[0];
+        const float mn = fmaxf(m, ms);
+        const float mu = (mn == -INFINITY) ? 0.f : mn;
+        const float fa = exp2f(m - mu), fb = exp2f(ms - mu);
+        l = l * fa + pr[1] * fb;
+        o = o * fa + pr[2 + d] * fb;
+        m = mn;
+    }
+    a.out[(size_t)r * a.H * HD + h * HD + d] = __float2bfloat16_rn(o / l);
+}
+
+template <int HD>
+size_t attn_smem() { return (size_t)kRows * HD * 2 * 3 + 4 * kChunk * HD * 2 + HD * 2 + (2 * kRows + 2) * 4; }
+
+}  // namespace
+
+size_t attn_mma_partial_bytes(int H, int hd, int max_seq)
+{
+    const int nsplit = (max_seq + kSplit - 1) / kSplit;
+    return (size_t)H * nsplit * kRows * (2 + hd) * 4;
+}
+
+bool attn_mma_init(int hd)
+{
+    if (hd == 128)
+        return cudaFuncSetAttribute(k_attn_mma<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)attn_smem<128>()) == cudaSuccess;
+    if (hd == 64)
+        return cudaFuncSetAttribute(k_attn_mma<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)attn_smem<64>()) == cudaSuccess;
+    return false;
+}
+
+void launch_attn_mma(cudaStream_t s, const DState* st, RowSet rs, int max_rel, const int* pos, const void* Q,
+                     const void* KC, const void* VC, const void* KS, const void* VS, void* out, float* part, int rows,
+                     int H, int Hkv, int hd, int max_seq)
+{
+    AttnArgs a;
+    a.st = st;
+    a.rs = rs;
+    a.pos = pos;
+    a.Q = (const __nv_bfloat16*)Q;
+    a.KC = (const __nv_bfloat16*)KC;
+    a.VC = (const __nv_bfloat16*)VC;
+    a.KS = (const __nv_bfloat16*)KS;
+    a.VS = (const __nv_bfloat16*)VS;
+    a.part = part;
+    a.out = (__nv_bfloat16*)out;
+    a.rows = rows;
+    a.H = H;
+    a.Hkv = Hkv;
+    a.max_seq = max_seq;
+    a.nsplit = (max_seq + kSplit - 1) / kSplit;
+    a.max_rel = max_rel;
+    a.sl2 = 1.4426950408889634f / sqrtf((float)hd);
+    dim3 grid(H, a.nsplit);
+    if (hd == 128) {
+        k_attn_mma<128><<<grid, kWarps * 32, attn_smem<128>(), s>>>(a);
+        k_attn_combine<128><<<dim3(rows, H), 128, 0, s>>>(a);
+    } else {
+        k_attn_mma<64><<<grid, kWarps * 32, attn_smem<64>(), s>>>(a);
+        k_attn_combine<64><<<dim3(rows, H), 64, 0, s>>>(a);
+    }
+}
+
+}  // namespace la

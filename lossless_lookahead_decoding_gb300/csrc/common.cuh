@@ -34,6 +34,8 @@ struct RowSet {
     const int* rel_pos;
     const int* grp;
     const int* grp_map;
+    const int* grp_start;  // [ngrp + 1] offsets into grp_rows
+    const int* grp_rows;   // rows of each group in row order
     int maxoff;
     int ngrp;
 };
@@ -118,6 +120,13 @@ void launch_attn_simt(cudaStream_t s, const DState* st, RowSet rs, const int* po
                       const T* VC, const T* KS, const T* VS, T* out, int rows, int H, int Hkv, int hd,
                       int max_seq, float scale);
 void launch_argmax(cudaStream_t s, const float* logits, int* amax, int rows, int V);
+
+// attn_mma.cu (bf16, head_dim 64 or 128)
+size_t attn_mma_partial_bytes(int H, int hd, int max_seq);
+bool attn_mma_init(int hd);
+void launch_attn_mma(cudaStream_t s, const DState* st, RowSet rs, int max_rel, const int* pos, const void* Q,
+                     const void* KC, const void* VC, const void* KS, const void* VS, void* out, float* part, int rows,
+                     int H, int Hkv, int hd, int max_seq);
 
 }  // namespace la
 

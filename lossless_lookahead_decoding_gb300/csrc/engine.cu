@@ -55,7 +55,8 @@ struct la_ctx {
     int W = 0, N = 2, G = 0, T = 1, flags = 0;
     uint64_t seed = 0;
     cudaStream_t s = nullptr;
-    bool bf16 = false, use_tc = false;
+    bool bf16 = false, use_tc = false, use_attn_mma = false;
+    float* attn_part = nullptr;
     int esz = 4, dq = 0, dkv = 0;
     char* ws = nullptr;
     size_t ws_bytes = 0;
@@ -153,6 +154,9 @@ static Layout make_layout(const la_model_desc* d, int W, int N, int G, int* pool
     ly.add(sizeof(DState));                              // 25 state
     ly.add(4096);                                        // 26 debug scratch
     ly.add(kRows * 8);                                   // 27 packed argmax
+    ly.add((2 * kRows + 1) * 4);                         // 28 step group lists
+    ly.add((2 * kRows + 1) * 4);                         // 29 prefill group lists
+    ly.add(attn_mma_partial_bytes(d->n_heads, d->head_dim, d->max_seq));  // 30 attention split partials
     return ly;
 }
 
@@ -194,9 +198,10 @@ static void forward(la_ctx* c, int rows, const RowSet& rs, bool logits)
             launch_rope_split<T>(s, c->QKV32, c->pos, c->cosb, c->sinb, Q, KS, VS, rows, H, Hkv, hd);
         }
         c->prof.begin(s);
-        if (c->use_tc && tc_attn_supported(c->tc))
-            tc_attention(c->tc, s, c->st, rs, c->pos, (const void*)Q, (const void*)KC, (const void*)VC,
-                         (const void*)KS, (const void*)VS, (void*)ATT, rows);
+        if (c->use_attn_mma)
+            launch_attn_mma(s, c->st, rs, &rs == &c->rs_pre ? rows - 1 : rs.maxoff - 1, c->pos,
+                            (const void*)Q, (const void*)KC, (const void*)VC, (const void*)KS, (const void*)VS,
+                            (void*)ATT, c->attn_part, rows, H, Hkv, hd, d.max_seq);
         else
             launch_attn_simt<T>(s, c->st, rs, c->pos, Q, KC, VC, KS, VS, ATT, rows, H, Hkv, hd, d.max_seq, scale);
         c->prof.end(s, P_ATTN, rows, 0);  // bytes filled in per step (they depend on P)
@@ -363,6 +368,9 @@ extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* w
     ctx->AMAXP = (unsigned long long*)(b + ly.off[27]);
     ctx->pool = PoolView{pk, pk + cap, (int*)(b + ly.off[23]), pk + 2 * cap, (int*)(b + ly.off[24]),
                          &ctx->st->status, cap, lg, G, N - 1};
+    int* gl1 = (int*)(b + ly.off[28]);
+    int* gl2 = (int*)(b + ly.off[29]);
+    ctx->attn_part = (float*)(b + ly.off[30]);
 
     // row tables: step (R2/R3 of the oracle's readings) and prefill (causal)
     const int n1 = N - 1;
@@ -393,6 +401,20 @@ extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* w
     }
     std::vector<int> prel(kRows), pgrp(kRows, 0), pmap(kRows);
     for (int r = 0; r < kRows; r++) prel[r] = pmap[r] = r;
+    // rows of each group in row order: [ngrp + 1] starts, then the rows
+    std::vector<int> sgl(2 * kRows + 1, 0), pgl(2 * kRows + 1, 0);
+    {
+        int k = 0;
+        for (int g = 0; g < ngrp; g++) {
+            sgl[g] = k;
+            for (int r = 0; r < ctx->T; r++)
+                if (grp[r] == g) sgl[kRows + 1 + k++] = r;
+        }
+        sgl[ngrp] = k;
+        pgl[0] = 0;
+        pgl[1] = kRows;
+        for (int r = 0; r < kRows; r++) pgl[kRows + 1 + r] = r;
+    }
     std::vector<float> cs((size_t)desc->max_seq * (desc->head_dim / 2)), sn(cs.size());
     for (int p = 0; p < desc->max_seq; p++)
         for (int i = 0; i < desc->head_dim / 2; i++) {
@@ -417,19 +439,24 @@ extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* w
         ck(cudaMemcpy(rs2, prel.data(), kRows * 4, cudaMemcpyHostToDevice));
         ck(cudaMemcpy(rs2 + kRows, pgrp.data(), kRows * 4, cudaMemcpyHostToDevice));
         ck(cudaMemcpy(map2, pmap.data(), kRows * 4, cudaMemcpyHostToDevice));
+        ck(cudaMemcpy(gl1, sgl.data(), sgl.size() * 4, cudaMemcpyHostToDevice));
+        ck(cudaMemcpy(gl2, pgl.data(), pgl.size() * 4, cudaMemcpyHostToDevice));
         ck(cudaMemcpy(ctx->cosb, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice));
         ck(cudaMemcpy(ctx->sinb, sn.data(), sn.size() * 4, cudaMemcpyHostToDevice));
         ck(cudaHostAlloc((void**)&ctx->h_st, sizeof(DState), cudaHostAllocDefault));
         ck(cudaEventCreate(&ctx->ev0));
         ck(cudaEventCreate(&ctx->ev1));
     }
-    ctx->rs_step = RowSet{rs1, rs1 + kRows, map1, maxoff, ngrp};
-    ctx->rs_pre = RowSet{rs2, rs2 + kRows, map2, kRows, 1};
+    ctx->rs_step = RowSet{rs1, rs1 + kRows, map1, gl1, gl1 + kRows + 1, maxoff, ngrp};
+    ctx->rs_pre = RowSet{rs2, rs2 + kRows, map2, gl2, gl2 + kRows + 1, kRows, 1};
     if (rc == LA_OK && ctx->bf16 && !(flags & LA_SIMT)) {
         int trc = tc_plan_create(&ctx->tc, ctx->d, ctx->lw.data(), ctx->XN, ctx->Q, ctx->ATT, ctx->HID, ctx->esz,
                                  &ctx->st->status);
         ctx->tc.prof = &ctx->prof;
-        if (trc == 0) ctx->use_tc = true;
+        if (trc == 0) {
+            ctx->use_tc = true;
+            ctx->use_attn_mma = attn_mma_init(desc->head_dim);
+        }
         else if (trc < 0) {
             ctx->err = "tcgen05 plan creation failed";
             rc = LA_ERR_CUDA;
