@@ -104,7 +104,8 @@ static int step_rows(int W, int N, int G) { return 1 + (W + G) * (N - 1); }
 static const char* check_desc(const la_model_desc* d, int W, int N, int G)
 {
     if (!d) return "desc is NULL";
-    if (d->n_layers < 1 || d->d_model < 64 || d->d_model % 64) return "d_model must be a positive multiple of 64";
+    if (d->n_layers < 1 || d->d_model < 64 || d->d_model % 64 || d->d_model > 8192)
+        return "d_model must be a multiple of 64 in [64, 8192]";
     if (d->head_dim != 64 && d->head_dim != 128) return "head_dim must be 64 or 128";
     if (d->n_heads < 1 || d->n_kv_heads < 1 || d->n_heads % d->n_kv_heads) return "n_heads % n_kv_heads != 0";
     if (d->ffn < 8 || d->ffn % 8) return "ffn must be a positive multiple of 8";

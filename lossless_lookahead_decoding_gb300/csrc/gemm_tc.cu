@@ -377,8 +377,10 @@ __device__ __forceinline__ int owner_cta(long long idx, long long total, int cta
     return c;
 }
 
-constexpr int kEpiRows = 8;
+constexpr int kEpiRows = 16;
 
+// Sum a tile's partials in ascending k order (all loads of a segment in
+// flight together), then apply the fused epilogue for kEpiRows tokens.
 template <int EPI>
 __global__ void __launch_bounds__(128) k_gemm_epi(EpiArgs e)
 {
@@ -386,51 +388,76 @@ __global__ void __launch_bounds__(128) k_gemm_epi(EpiArgs e)
     const long long total = (long long)e.tiles * e.KB;
     const int c_lo = owner_cta((long long)t * e.KB, total, e.ctas);
     const int c_hi = owner_cta((long long)t * e.KB + e.KB - 1, total, e.ctas);
-    __shared__ float sx[kBM];
-    __shared__ float sbv[4];
-    __shared__ int sbi[4];
+    __shared__ float sx[kEpiRows][kBM];
+    __shared__ float sbv[kEpiRows][4];
+    __shared__ int sbi[kEpiRows][4];
     const int r0 = blockIdx.y * kEpiRows;
-    const int r1 = min(r0 + kEpiRows, e.rows);
-    for (int r = r0; r < r1; r++) {
-        float acc = e.partial[((size_t)(c_lo + t) * e.rows + r) * kBM + f];
-        for (int cc = c_lo + 1; cc <= c_hi; cc++) acc += e.partial[((size_t)(cc + t) * e.rows + r) * kBM + f];
-        if (EPI == EPI_QKV) {
-            const int fg = t * kBM + f;
-            sx[f] = acc;
-            __syncthreads();
-            const int half = e.hd >> 1;
-            if (fg < e.dq + e.dkv) {
-                const float other = sx[f ^ half];
-                const int region = fg < e.dq ? 0 : 1;
-                const int fl = region == 0 ? fg : fg - e.dq;
-                const int i = fl % e.hd, ip = i % half;
+    float acc[kEpiRows];
+#pragma unroll
+    for (int i = 0; i < kEpiRows; i++) {
+        const int r = r0 + i;
+        acc[i] = r < e.rows ? e.partial[((size_t)(c_lo + t) * e.rows + r) * kBM + f] : 0.f;
+    }
+    for (int cc = c_lo + 1; cc <= c_hi; cc++) {
+#pragma unroll
+        for (int i = 0; i < kEpiRows; i++) {
+            const int r = r0 + i;
+            if (r < e.rows) acc[i] += e.partial[((size_t)(cc + t) * e.rows + r) * kBM + f];
+        }
+    }
+    if (EPI == EPI_RESID) {
+        const int fg = t * kBM + f;
+        if (fg < e.Nout) {
+#pragma unroll
+            for (int i = 0; i < kEpiRows; i++)
+                if (r0 + i < e.rows) e.X[(size_t)(r0 + i) * e.Nout + fg] += acc[i];
+        }
+        return;
+    }
+    if (EPI == EPI_QKV || EPI == EPI_SWIGLU) {
+#pragma unroll
+        for (int i = 0; i < kEpiRows; i++) sx[i][f] = acc[i];
+        __syncthreads();
+    }
+    if (EPI == EPI_QKV) {
+        const int fg = t * kBM + f, half = e.hd >> 1;
+        if (fg < e.dq + e.dkv) {
+            const int region = fg < e.dq ? 0 : 1;
+            const int fl = region == 0 ? fg : fg - e.dq;
+            const int i0 = fl % e.hd, ip = i0 % half;
+            for (int i = 0; i < kEpiRows; i++) {
+                const int r = r0 + i;
+                if (r >= e.rows) break;
+                const float other = sx[i][f ^ half];
                 const int p = e.pos[r];
                 const float cs = e.cosb[(size_t)p * half + ip], sn = e.sinb[(size_t)p * half + ip];
-                const float y = (i < half) ? acc * cs - other * sn : acc * cs + other * sn;
+                const float y = (i0 < half) ? acc[i] * cs - other * sn : acc[i] * cs + other * sn;
                 if (region == 0) e.Q[(size_t)r * e.dq + fl] = __float2bfloat16_rn(y);
                 else e.KS[(size_t)r * e.dkv + fl] = __float2bfloat16_rn(y);
-            } else if (fg < e.dq + 2 * e.dkv) {
-                e.VS[(size_t)r * e.dkv + (fg - e.dq - e.dkv)] = __float2bfloat16_rn(acc);
             }
-            __syncthreads();
-        } else if (EPI == EPI_RESID) {
-            const int fg = t * kBM + f;
-            if (fg < e.Nout) e.X[(size_t)r * e.Nout + fg] += acc;
-        } else if (EPI == EPI_SWIGLU) {
-            sx[f] = acc;
-            __syncthreads();
-            const int fo = t * 64 + f;
-            if (f < 64 && fo < e.Nout) {
-                const float gt = acc, up = sx[f + 64];
-                e.H[(size_t)r * e.Nout + fo] = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up);
+        } else if (fg < e.dq + 2 * e.dkv) {
+            for (int i = 0; i < kEpiRows; i++)
+                if (r0 + i < e.rows) e.VS[(size_t)(r0 + i) * e.dkv + (fg - e.dq - e.dkv)] = __float2bfloat16_rn(acc[i]);
+        }
+    } else if (EPI == EPI_SWIGLU) {
+        const int fo = t * 64 + f;
+        if (f < 64 && fo < e.Nout) {
+            for (int i = 0; i < kEpiRows; i++) {
+                if (r0 + i >= e.rows) break;
+                const float gt = acc[i], up = sx[i][f + 64];
+                e.H[(size_t)(r0 + i) * e.Nout + fo] = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up);
             }
-            __syncthreads();
-        } else {
-            const int fg = t * kBM + f;
-            const bool valid = fg < e.Nout;
-            if (valid && e.logits) e.logits[(size_t)r * e.Nout + fg] = acc;
-            float bv = valid ? acc : -INFINITY;
+        }
+    } else if (EPI == EPI_LOGITS) {
+        const int fg = t * kBM + f;
+        const bool valid = fg < e.Nout;
+#pragma unroll
+        for (int i = 0; i < kEpiRows; i++) {
+            const int r = r0 + i;
+            if (valid && e.logits && r < e.rows) e.logits[(size_t)r * e.Nout + fg] = acc[i];
+            float bv = valid ? acc[i] : -INFINITY;
             int bi = valid ? fg : 0x7fffffff;
+#pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
                 const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
                 const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
@@ -440,24 +467,25 @@ __global__ void __launch_bounds__(128) k_gemm_epi(EpiArgs e)
                 }
             }
             if ((f & 31) == 0) {
-                sbv[f >> 5] = bv;
-                sbi[f >> 5] = bi;
+                sbv[i][f >> 5] = bv;
+                sbi[i][f >> 5] = bi;
             }
-            __syncthreads();
-            if (f == 0) {
-                for (int w = 1; w < 4; w++)
-                    if (sbv[w] > bv || (sbv[w] == bv && sbi[w] < bi)) {
-                        bv = sbv[w];
-                        bi = sbi[w];
-                    }
-                if (bi != 0x7fffffff) {
-                    uint32_t u = __float_as_uint(bv);
-                    uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-                    unsigned long long packed = ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)bi);
-                    atomicMax(&e.amaxp[r], packed);
+        }
+        __syncthreads();
+        if (f < kEpiRows && r0 + f < e.rows) {
+            float bv = sbv[f][0];
+            int bi = sbi[f][0];
+            for (int w = 1; w < 4; w++)
+                if (sbv[f][w] > bv || (sbv[f][w] == bv && sbi[f][w] < bi)) {
+                    bv = sbv[f][w];
+                    bi = sbi[f][w];
                 }
+            if (bi != 0x7fffffff) {
+                const uint32_t u = __float_as_uint(bv);
+                const uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+                const unsigned long long packed = ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)bi);
+                atomicMax(&e.amaxp[r0 + f], packed);
             }
-            __syncthreads();
         }
     }
 }

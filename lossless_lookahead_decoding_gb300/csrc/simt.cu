@@ -30,34 +30,70 @@ void launch_embed(cudaStream_t s, const int* tok, const T* emb, float* X, int ro
 
 // -------------------------------------------------------------- rmsnorm ---
 // x / sqrt(mean(x^2) + eps) * w  (Zhang and Sennrich 2019, cited by the
-// pages).  Sum of squares: per-thread strided partials, fixed xor tree, then
-// warps in order.
-template <typename T>
-__global__ void k_rmsnorm(const float* X, const T* w, T* out, int d, float eps)
+// pages).  One block per row; each thread loads its float4 slices up front
+// (all loads in flight at once), sums squares in a fixed order, then a fixed
+// xor tree and the warps in order.
+constexpr int kNormThreads = 256, kNormVec = 8;  // d <= 8 * 4 * 256 = 8192
+
+__device__ __forceinline__ void store4(float* o, float a, float b, float c, float d)
 {
-    const int r = blockIdx.x;
-    const float* x = X + (size_t)r * d;
+    *(float4*)o = make_float4(a, b, c, d);
+}
+__device__ __forceinline__ void store4(__nv_bfloat16* o, float a, float b, float c, float d)
+{
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&lo);
+    u.y = *reinterpret_cast<uint32_t*>(&hi);
+    *(uint2*)o = u;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kNormThreads) k_rmsnorm(const float* X, const T* w, T* out, int d, float eps)
+{
+    const int r = blockIdx.x, d4 = d >> 2;
+    const float4* x = (const float4*)(X + (size_t)r * d);
+    float4 v[kNormVec];
     float ss = 0.f;
-    for (int k = threadIdx.x; k < d; k += blockDim.x) ss += x[k] * x[k];
+#pragma unroll
+    for (int i = 0; i < kNormVec; i++) {
+        const int k = threadIdx.x + i * kNormThreads;
+        v[i] = k < d4 ? x[k] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < kNormVec; i++) {
+        ss += v[i].x * v[i].x;
+        ss += v[i].y * v[i].y;
+        ss += v[i].z * v[i].z;
+        ss += v[i].w * v[i].w;
+    }
     ss = warp_sum(ss);
-    __shared__ float part[32];
+    __shared__ float part[kNormThreads / 32];
     __shared__ float s_r;
     if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
     __syncthreads();
     if (threadIdx.x == 0) {
         float t = 0.f;
-        for (int i = 0; i < (int)(blockDim.x >> 5); i++) t += part[i];
+        for (int i = 0; i < kNormThreads / 32; i++) t += part[i];
         s_r = rsqrtf(t / (float)d + eps);
     }
     __syncthreads();
     const float rr = s_r;
-    for (int k = threadIdx.x; k < d; k += blockDim.x) out[(size_t)r * d + k] = from_f<T>(x[k] * rr * to_f(w[k]));
+#pragma unroll
+    for (int i = 0; i < kNormVec; i++) {
+        const int k = threadIdx.x + i * kNormThreads;
+        if (k < d4) {
+            const int e = 4 * k;
+            store4(out + (size_t)r * d + e, v[i].x * rr * to_f(w[e]), v[i].y * rr * to_f(w[e + 1]),
+                   v[i].z * rr * to_f(w[e + 2]), v[i].w * rr * to_f(w[e + 3]));
+        }
+    }
 }
 
 template <typename T>
 void launch_rmsnorm(cudaStream_t s, const float* X, const T* w, T* out, int rows, int d, float eps)
 {
-    k_rmsnorm<T><<<rows, 256, 0, s>>>(X, w, out, d, eps);
+    k_rmsnorm<T><<<rows, kNormThreads, 0, s>>>(X, w, out, d, eps);
 }
 
 // ---------------------------------------------------------- SIMT GEMMs ---

@@ -8,8 +8,9 @@
   121 rows per step) -- the full widths the benchmark runs, with the oracle
   on the same bytes.
 
-Checks: per-step logits of every row within rel-L2 1e-2 (bf16) of the fp32
-oracle, rows/window/pool/emitted tokens bit-exact against the oracle
+Checks: each step's logits within relative L2 error 1e-2 (bf16) of the fp32
+oracle's (every row within 2e-2: a CPU emulation of the kernels' bf16 rounding
+points gives ~1.1e-2 for single rows of the 2-layer 7B slice), rows/window/pool/emitted tokens bit-exact against the oracle
 controller fed the GPU's argmaxes, and lookahead tokens == GPU greedy tokens.
 """
 import numpy as np
@@ -37,7 +38,7 @@ def test_gqa_hd128_long_prompt(flags):
     prompt = I.plant_spans(I.zipf_tokens(300, cfg.vocab, 1.1, 7), 16, 4, 8)
     W, N, G = 7, 5, 7
     dec = gpu_decoder(cfg, w, 1, W, N, G, 512, flags=flags | LA.LA_DEBUG_LOGITS)
-    toks, worst = replay_against_oracle(dec, O.Model(cfg, w), prompt, 6, 1e-2)
+    toks, worst = replay_against_oracle(dec, O.Model(cfg, w), prompt, 6, 1e-2, row_tol=2e-2)
     g = gpu_decoder(cfg, w, 1, 0, 2, 0, 512, flags=flags).generate(prompt, 48)
     la = gpu_decoder(cfg, w, 1, W, N, G, 512, flags=flags).generate(prompt, 48)
     assert np.array_equal(la, g)
@@ -51,7 +52,7 @@ def test_7b_width_two_layer_slice():
     prompt = I.make_prompt("7b")
     W, N, G = I.LOOKAHEAD["7b"]
     dec = gpu_decoder(cfg, w, 1, W, N, G, 640, flags=LA.LA_DEBUG_LOGITS)
-    toks, worst = replay_against_oracle(dec, O.Model(cfg, w), prompt, 2, 1e-2)
+    toks, worst = replay_against_oracle(dec, O.Model(cfg, w), prompt, 2, 1e-2, row_tol=2e-2)
     g = gpu_decoder(cfg, w, 1, 0, 2, 0, 640).generate(prompt, 64)
     la = gpu_decoder(cfg, w, 1, W, N, G, 640).generate(prompt, 64)
     assert np.array_equal(la, g)
