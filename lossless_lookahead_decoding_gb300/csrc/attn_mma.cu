@@ -237,6 +237,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
     int* gcnt = (int*)(sZero + RB);       // [kRows + 1] rows of each group (< a.rows)
     int* gslab = gcnt + kRows + 1;        // [kRows + 1] slab prefix over groups
 
+    pdl_wait();
+    pdl_trigger();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int h = blockIdx.x, sp = blockIdx.y;
     const int dq = a.H * HD, dkv = a.Hkv * HD, kvh = h / (a.H / a.Hkv);
@@ -426,6 +428,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
 template <int HD>
 __global__ void k_attn_combine(AttnArgs a)
 {
+    pdl_wait();
+    pdl_trigger();
     const int r = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
     constexpr int PS = 2 + HD;
     const int ns = a.pos[r] / kSplit + 1;
@@ -490,11 +494,11 @@ void launch_attn_mma(cudaStream_t s, const DState* st, RowSet rs, int max_rel, c
     a.sl2 = 1.4426950408889634f / sqrtf((float)hd);
     dim3 grid(H, a.nsplit);
     if (hd == 128) {
-        k_attn_mma<128><<<grid, kWarps * 32, attn_smem<128>(), s>>>(a);
-        k_attn_combine<128><<<dim3(rows, H), 128, 0, s>>>(a);
+        launch_pdl(k_attn_mma<128>, grid, dim3(kWarps * 32), attn_smem<128>(), s, a);
+        launch_pdl(k_attn_combine<128>, dim3(rows, H), dim3(128), 0, s, a);
     } else {
-        k_attn_mma<64><<<grid, kWarps * 32, attn_smem<64>(), s>>>(a);
-        k_attn_combine<64><<<dim3(rows, H), 64, 0, s>>>(a);
+        launch_pdl(k_attn_mma<64>, grid, dim3(kWarps * 32), attn_smem<64>(), s, a);
+        launch_pdl(k_attn_combine<64>, dim3(rows, H), dim3(64), 0, s, a);
     }
 }
 

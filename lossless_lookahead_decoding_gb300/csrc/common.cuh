@@ -78,6 +78,32 @@ __device__ __forceinline__ float warp_max(float v)
     return v;
 }
 
+// ---- programmatic dependent launch (PDL) ----
+// Kernels of the layer chain are launched with programmatic stream
+// serialisation: a kernel may start while its predecessor drains.  Every such
+// kernel calls pdl_wait() before touching data produced upstream (it returns
+// once the predecessor grid has completed and its writes are visible) and
+// then pdl_trigger() so that its own successor can be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // ---- launchers (defined in the .cu files) ----
 struct Dims {
     int L, d, H, Hkv, hd, F, V, max_seq;

@@ -39,6 +39,7 @@ constexpr int kThreads = 192;            // warp 0 TMA, warp 1 MMA, warps 2..5 e
 constexpr int kTmemCols = 256;           // two 128-column fp32 accumulators
 constexpr int kSmemBytes = kStages * (kStageA + kStageB) + 1024 + 256;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // bounded waits: 2 s
+constexpr int kPrefetch = 8;             // weight tiles requested into L2 ahead of the smem ring
 
 enum { MODE_ONE = 0, MODE_SEQ3 = 1, MODE_PAIR = 2 };
 enum { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3 };
@@ -98,6 +99,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
         if (*abort_flag) return false;
         if (globaltimer() - t0 > kWaitNs) return false;
     }
+}
+
+__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
+                 : "memory");
 }
 
 __device__ __forceinline__ void tma_load(const CUtensorMap* map, uint64_t* bar, void* dst, int x, int y)
@@ -225,26 +232,62 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool issued[kStages];
             for (int s = 0; s < kStages; s++) issued[s] = false;
             bool ok = true;
-            for (long long idx = lo; idx < hi; idx++) {
+            // weight tile of flat k-block j -> L2 (no shared memory needed)
+            auto prefetch = [&](long long j) {
+                const int t = (int)(j / g.KB), kx = (int)(j % g.KB) * kBK;
+                if (g.mode == MODE_PAIR) {
+                    tma_prefetch_l2(&a0, kx, t * 64);
+                    tma_prefetch_l2(&a1, kx, t * 64);
+                } else if (g.mode == MODE_SEQ3) {
+                    if (t < g.t0) tma_prefetch_l2(&a0, kx, t * kBM);
+                    else if (t < g.t0 + g.t1) tma_prefetch_l2(&a1, kx, (t - g.t0) * kBM);
+                    else tma_prefetch_l2(&a2, kx, (t - g.t0 - g.t1) * kBM);
+                } else {
+                    tma_prefetch_l2(&a0, kx, t * kBM);
+                }
+            };
+            auto load_a = [&](long long idx, int st) {
+                const int t = (int)(idx / g.KB), kx = (int)(idx % g.KB) * kBK;
+                uint8_t* dA = sA + st * kStageA;
+                if (g.mode == MODE_PAIR) {
+                    tma_load(&a0, &full[st], dA, kx, t * 64);
+                    tma_load(&a1, &full[st], dA + 64 * 128, kx, t * 64);
+                } else if (g.mode == MODE_SEQ3) {
+                    if (t < g.t0) tma_load(&a0, &full[st], dA, kx, t * kBM);
+                    else if (t < g.t0 + g.t1) tma_load(&a1, &full[st], dA, kx, (t - g.t0) * kBM);
+                    else tma_load(&a2, &full[st], dA, kx, (t - g.t0 - g.t1) * kBM);
+                } else {
+                    tma_load(&a0, &full[st], dA, kx, t * kBM);
+                }
+            };
+            auto load_b = [&](long long idx, int st) {
+                tma_load(&bmap, &full[st], sB + st * kStageB, (int)(idx % g.KB) * kBK, 0);
+            };
+            // The weights do not depend on the preceding kernels: fill the
+            // ring with weight tiles (and request more into L2) before
+            // waiting for the activations the predecessor writes.
+            const int n_pre = (int)((hi - lo) < kStages ? (hi - lo) : kStages);
+            for (int j = 0; j < n_pre; j++) {
+                mbar_expect_tx(&full[j], kStageA + kStageB);
+                load_a(lo + j, j);
+                issued[j] = true;
+                issued_phase[j] = 0;
+            }
+            for (long long j = lo + kStages; j < hi && j < lo + kStages + kPrefetch; j++) prefetch(j);
+            pdl_wait();
+            pdl_trigger();
+            for (int j = 0; j < n_pre; j++) load_b(lo + j, j);
+            stage = n_pre % kStages;
+            phase = n_pre == kStages ? 1 : 0;
+            for (long long idx = lo + n_pre; idx < hi; idx++) {
+                if (idx + kPrefetch < hi) prefetch(idx + kPrefetch);
                 if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
                     ok = false;
                     break;
                 }
-                const int t = (int)(idx / g.KB), kb = (int)(idx % g.KB);
-                const int kx = kb * kBK;
                 mbar_expect_tx(&full[stage], kStageA + kStageB);
-                uint8_t* dA = sA + stage * kStageA;
-                if (g.mode == MODE_PAIR) {
-                    tma_load(&a0, &full[stage], dA, kx, t * 64);
-                    tma_load(&a1, &full[stage], dA + 64 * 128, kx, t * 64);
-                } else if (g.mode == MODE_SEQ3) {
-                    if (t < g.t0) tma_load(&a0, &full[stage], dA, kx, t * kBM);
-                    else if (t < g.t0 + g.t1) tma_load(&a1, &full[stage], dA, kx, (t - g.t0) * kBM);
-                    else tma_load(&a2, &full[stage], dA, kx, (t - g.t0 - g.t1) * kBM);
-                } else {
-                    tma_load(&a0, &full[stage], dA, kx, t * kBM);
-                }
-                tma_load(&bmap, &full[stage], sB + stage * kStageB, kx, 0);
+                load_a(idx, stage);
+                load_b(idx, stage);
                 issued[stage] = true;
                 issued_phase[stage] = phase;
                 if (++stage == kStages) {
@@ -313,6 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------- epilogue warps: TMEM -> fp32 partials
+        pdl_wait();  // the partial buffer may still be read by the predecessor
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         int buf = 0;
         uint32_t tphase[2] = {0, 0};
@@ -353,19 +397,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 struct EpiArgs {
     int tiles, KB, ctas, rows, Nout;
-    const float* partial;
+    const float* __restrict__ partial;
     // QKV
     int dq, dkv, hd;
-    const int* pos;
-    const float* cosb;
-    const float* sinb;
-    __nv_bfloat16 *Q, *KS, *VS;
+    const int* __restrict__ pos;
+    const float* __restrict__ cosb;
+    const float* __restrict__ sinb;
+    __nv_bfloat16 *__restrict__ Q, *__restrict__ KS, *__restrict__ VS;
     // residual
-    float* X;
+    float* __restrict__ X;
     // SwiGLU
-    __nv_bfloat16* H;
+    __nv_bfloat16* __restrict__ H;
     // logits / argmax
-    float* logits;
+    float* __restrict__ logits;
     unsigned long long* amaxp;
 };
 
@@ -384,6 +428,8 @@ constexpr int kEpiRows = 16;
 template <int EPI>
 __global__ void __launch_bounds__(128) k_gemm_epi(EpiArgs e)
 {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x, f = threadIdx.x;
     const long long total = (long long)e.tiles * e.KB;
     const int c_lo = owner_cta((long long)t * e.KB, total, e.ctas);
@@ -408,9 +454,13 @@ __global__ void __launch_bounds__(128) k_gemm_epi(EpiArgs e)
     if (EPI == EPI_RESID) {
         const int fg = t * kBM + f;
         if (fg < e.Nout) {
+            float x[kEpiRows];
 #pragma unroll
             for (int i = 0; i < kEpiRows; i++)
-                if (r0 + i < e.rows) e.X[(size_t)(r0 + i) * e.Nout + fg] += acc[i];
+                x[i] = (r0 + i < e.rows) ? e.X[(size_t)(r0 + i) * e.Nout + fg] : 0.f;
+#pragma unroll
+            for (int i = 0; i < kEpiRows; i++)
+                if (r0 + i < e.rows) e.X[(size_t)(r0 + i) * e.Nout + fg] = x[i] + acc[i];
         }
         return;
     }
@@ -425,15 +475,22 @@ __global__ void __launch_bounds__(128) k_gemm_epi(EpiArgs e)
             const int region = fg < e.dq ? 0 : 1;
             const int fl = region == 0 ? fg : fg - e.dq;
             const int i0 = fl % e.hd, ip = i0 % half;
+            float cs[kEpiRows], sn[kEpiRows];
+#pragma unroll
+            for (int i = 0; i < kEpiRows; i++) {
+                const int p = e.pos[min(r0 + i, e.rows - 1)];
+                cs[i] = e.cosb[(size_t)p * half + ip];
+                sn[i] = e.sinb[(size_t)p * half + ip];
+            }
+#pragma unroll
             for (int i = 0; i < kEpiRows; i++) {
                 const int r = r0 + i;
-                if (r >= e.rows) break;
-                const float other = sx[i][f ^ half];
-                const int p = e.pos[r];
-                const float cs = e.cosb[(size_t)p * half + ip], sn = e.sinb[(size_t)p * half + ip];
-                const float y = (i0 < half) ? acc[i] * cs - other * sn : acc[i] * cs + other * sn;
-                if (region == 0) e.Q[(size_t)r * e.dq + fl] = __float2bfloat16_rn(y);
-                else e.KS[(size_t)r * e.dkv + fl] = __float2bfloat16_rn(y);
+                if (r < e.rows) {
+                    const float other = sx[i][f ^ half];
+                    const float y = (i0 < half) ? acc[i] * cs[i] - other * sn[i] : acc[i] * cs[i] + other * sn[i];
+                    if (region == 0) e.Q[(size_t)r * e.dq + fl] = __float2bfloat16_rn(y);
+                    else e.KS[(size_t)r * e.dkv + fl] = __float2bfloat16_rn(y);
+                }
             }
         } else if (fg < e.dq + 2 * e.dkv) {
             for (int i = 0; i < kEpiRows; i++)
@@ -492,6 +549,8 @@ __global__ void __launch_bounds__(128) k_gemm_epi(EpiArgs e)
 
 __global__ void k_argmax_unpack(unsigned long long* amaxp, int* amax, int rows)
 {
+    pdl_wait();
+    pdl_trigger();
     const int r = threadIdx.x;
     if (r < rows) {
         amax[r] = (int)(0xFFFFFFFFu - (uint32_t)(amaxp[r] & 0xFFFFFFFFull));
@@ -562,7 +621,7 @@ void launch_gemm(const TcPlan& p, const GemmCfg& g, cudaStream_t s, int rows, in
     const Impl& im = *(const Impl*)p.impl;
     GemmArgs a{g.tiles, g.KB, g.ctas, g.mode, g.t0, g.t1, rows, im.partial, im.err};
     if (p.prof) p.prof->begin(s);
-    k_gemm_tc<<<g.ctas, kThreads, kSmemBytes, s>>>(g.a[0], g.a[1], g.a[2], g.b, a);
+    launch_pdl(k_gemm_tc, dim3(g.ctas), dim3(kThreads), kSmemBytes, s, g.a[0], g.a[1], g.a[2], g.b, a);
     if (p.prof) {
         // algorithmic: every weight once, the rows' inputs once, the rows' outputs once
         const double K = (double)g.KB * kBK, Nw = (double)g.tiles * (g.mode == MODE_PAIR ? 2 * 64 : kBM);
@@ -729,7 +788,7 @@ void tc_qkv_rope(const TcPlan& p, cudaStream_t s, int layer, int rows, const int
     e.Q = (__nv_bfloat16*)Q;
     e.KS = (__nv_bfloat16*)KS;
     e.VS = (__nv_bfloat16*)VS;
-    launch_epi(p, s, [&] { k_gemm_epi<EPI_QKV><<<epi_grid(g, rows), 128, 0, s>>>(e); });
+    launch_epi(p, s, [&] { launch_pdl(k_gemm_epi<EPI_QKV>, epi_grid(g, rows), dim3(128), 0, s, e); });
 }
 
 bool tc_attn_supported(const TcPlan&) { return false; }
@@ -746,7 +805,7 @@ void tc_oproj_resid(const TcPlan& p, cudaStream_t s, int layer, int rows, float*
     launch_gemm(p, g, s, rows, P_GEMM_O);
     EpiArgs e = epi_base(im, g, rows);
     e.X = X;
-    launch_epi(p, s, [&] { k_gemm_epi<EPI_RESID><<<epi_grid(g, rows), 128, 0, s>>>(e); });
+    launch_epi(p, s, [&] { launch_pdl(k_gemm_epi<EPI_RESID>, epi_grid(g, rows), dim3(128), 0, s, e); });
 }
 
 void tc_gateup_swiglu(const TcPlan& p, cudaStream_t s, int layer, int rows)
@@ -756,7 +815,7 @@ void tc_gateup_swiglu(const TcPlan& p, cudaStream_t s, int layer, int rows)
     launch_gemm(p, g, s, rows, P_GEMM_GU);
     EpiArgs e = epi_base(im, g, rows);
     e.H = (__nv_bfloat16*)im.HID;
-    launch_epi(p, s, [&] { k_gemm_epi<EPI_SWIGLU><<<epi_grid(g, rows), 128, 0, s>>>(e); });
+    launch_epi(p, s, [&] { launch_pdl(k_gemm_epi<EPI_SWIGLU>, epi_grid(g, rows), dim3(128), 0, s, e); });
 }
 
 void tc_down_resid(const TcPlan& p, cudaStream_t s, int layer, int rows, float* X)
@@ -766,7 +825,7 @@ void tc_down_resid(const TcPlan& p, cudaStream_t s, int layer, int rows, float* 
     launch_gemm(p, g, s, rows, P_GEMM_DOWN);
     EpiArgs e = epi_base(im, g, rows);
     e.X = X;
-    launch_epi(p, s, [&] { k_gemm_epi<EPI_RESID><<<epi_grid(g, rows), 128, 0, s>>>(e); });
+    launch_epi(p, s, [&] { launch_pdl(k_gemm_epi<EPI_RESID>, epi_grid(g, rows), dim3(128), 0, s, e); });
 }
 
 void tc_lmhead_argmax(const TcPlan& p, cudaStream_t s, int rows, float* logits, unsigned long long* amaxp, int* amax)
@@ -778,8 +837,8 @@ void tc_lmhead_argmax(const TcPlan& p, cudaStream_t s, int rows, float* logits, 
     e.logits = logits;
     e.amaxp = amaxp;
     launch_epi(p, s, [&] {
-        k_gemm_epi<EPI_LOGITS><<<epi_grid(g, rows), 128, 0, s>>>(e);
-        k_argmax_unpack<<<1, kRows, 0, s>>>(amaxp, amax, rows);
+        launch_pdl(k_gemm_epi<EPI_LOGITS>, epi_grid(g, rows), dim3(128), 0, s, e);
+        launch_pdl(k_argmax_unpack, dim3(1), dim3(kRows), 0, s, amaxp, amax, rows);
     });
 }
 

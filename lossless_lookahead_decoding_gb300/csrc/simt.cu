@@ -51,6 +51,8 @@ __device__ __forceinline__ void store4(__nv_bfloat16* o, float a, float b, float
 template <typename T>
 __global__ void __launch_bounds__(kNormThreads) k_rmsnorm(const float* X, const T* w, T* out, int d, float eps)
 {
+    pdl_wait();
+    pdl_trigger();
     const int r = blockIdx.x, d4 = d >> 2;
     const float4* x = (const float4*)(X + (size_t)r * d);
     float4 v[kNormVec];
@@ -93,7 +95,7 @@ __global__ void __launch_bounds__(kNormThreads) k_rmsnorm(const float* X, const 
 template <typename T>
 void launch_rmsnorm(cudaStream_t s, const float* X, const T* w, T* out, int rows, int d, float eps)
 {
-    k_rmsnorm<T><<<rows, kNormThreads, 0, s>>>(X, w, out, d, eps);
+    launch_pdl(k_rmsnorm<T>, dim3(rows), dim3(kNormThreads), 0, s, X, w, out, d, eps);
 }
 
 // ---------------------------------------------------------- SIMT GEMMs ---
