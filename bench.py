@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--workload", default="7b", choices=list(I.MODELS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="use only the first L decoder layers (small cases for profiler captures)")
     return ap.parse_args()
 
 
@@ -206,6 +208,8 @@ def run_ours(args, rank, world):
     local = int(os.environ.get("LOCAL_RANK", 0))
     torch.cuda.set_device(local)
     cfg = I.MODELS[args.workload]
+    if args.layers:
+        cfg = cfg.sliced(args.layers)
     W, N, G = I.LOOKAHEAD[args.workload]
     T = 1 + (W + G) * (N - 1)
     gen = GEN_TOKENS[args.workload]

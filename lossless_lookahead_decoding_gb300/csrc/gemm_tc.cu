@@ -32,14 +32,20 @@ namespace {
 constexpr int kBM = 128;                 // weight rows per tile (MMA M)
 constexpr int kBN = 128;                 // token columns (MMA N)
 constexpr int kBK = 64;                  // K per stage (one 128-byte swizzle row)
-constexpr int kStages = 6;
+#ifndef LA_GEMM_STAGES
+#define LA_GEMM_STAGES 6
+#endif
+#ifndef LA_GEMM_PREFETCH
+#define LA_GEMM_PREFETCH 8
+#endif
+constexpr int kStages = LA_GEMM_STAGES;
 constexpr int kStageA = kBM * kBK * 2;   // 16 KB
 constexpr int kStageB = kBN * kBK * 2;   // 16 KB
 constexpr int kThreads = 192;            // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kTmemCols = 256;           // two 128-column fp32 accumulators
 constexpr int kSmemBytes = kStages * (kStageA + kStageB) + 1024 + 256;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // bounded waits: 2 s
-constexpr int kPrefetch = 8;             // weight tiles requested into L2 ahead of the smem ring
+constexpr int kPrefetch = LA_GEMM_PREFETCH;  // weight tiles requested into L2 ahead of the smem ring
 
 enum { MODE_ONE = 0, MODE_SEQ3 = 1, MODE_PAIR = 2 };
 enum { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3 };
@@ -273,14 +279,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issued[j] = true;
                 issued_phase[j] = 0;
             }
-            for (long long j = lo + kStages; j < hi && j < lo + kStages + kPrefetch; j++) prefetch(j);
+            for (long long j = lo + kStages; kPrefetch > 0 && j < hi && j < lo + kStages + kPrefetch; j++)
+                prefetch(j);
             pdl_wait();
             pdl_trigger();
             for (int j = 0; j < n_pre; j++) load_b(lo + j, j);
             stage = n_pre % kStages;
             phase = n_pre == kStages ? 1 : 0;
             for (long long idx = lo + n_pre; idx < hi; idx++) {
-                if (idx + kPrefetch < hi) prefetch(idx + kPrefetch);
+                if (kPrefetch > 0 && idx + kPrefetch < hi) prefetch(idx + kPrefetch);
                 if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
                     ok = false;
                     break;
