@@ -11,9 +11,10 @@
 //
 // Work split (stream-K): the flattened (tile, k-block) space is cut into
 // equal contiguous ranges, one per CTA (one CTA per SM).  A CTA writes one
-// fp32 partial per tile it touches; the last CTA to finish a tile (atomic
-// per-tile counter) sums that tile's partials in ascending k order and
-// applies the fused epilogue (RoPE, residual add, SwiGLU, logits + argmax).
+// fp32 partial per tile it touches; when all of a tile's CTAs have arrived
+// (per-tile atomic counter), each of them sums its share of the tile's rows
+// over the tile's partials in ascending k order and applies the fused
+// epilogue (RoPE, residual add, SwiGLU, logits + argmax).
 // The split depends only on the matrix shape and the SM count, never on the
 // number of rows, so every token's result is bit-identical whether it is
 // decoded alone (greedy) or among 121 step rows (lookahead): this keeps
@@ -202,27 +203,33 @@ __device__ __forceinline__ int owner_cta(long long idx, long long total, int cta
 // Barrier of the four epilogue warps only (named barrier 1, 128 threads).
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-// Final reduction + epilogue of tile t by the 128 epilogue threads of the CTA
-// that completed it (f = feature row of the tile).  Partials are summed in
-// ascending k order, so the result does not depend on which CTA finishes last.
-template <int EPI>
-__device__ void tile_epilogue(const GemmArgs& e, int t, int f, float (*sx)[kBM], float (*sbv)[4], int (*sbi)[4])
+__device__ __forceinline__ int ld_acquire(const int* p)
 {
-    const long long total = (long long)e.tiles * e.KB;
-    const int c_lo = owner_cta((long long)t * e.KB, total, e.ctas);
-    const int c_hi = owner_cta((long long)t * e.KB + e.KB - 1, total, e.ctas);
-    for (int r0 = 0; r0 < e.rows; r0 += kEpiRows) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Final reduction + epilogue of rows [rb, re) of tile t by the 128 epilogue
+// threads of one of the tile's CTAs (f = feature row of the tile).  Partials
+// are summed in ascending k order, so the result does not depend on which
+// CTA reduces which rows.
+template <int EPI>
+__device__ void tile_epilogue(const GemmArgs& e, int t, int f, int rb, int re, int c_lo, int c_hi, float (*sx)[kBM],
+                              float (*sbv)[4], int (*sbi)[4])
+{
+    for (int r0 = rb; r0 < re; r0 += kEpiRows) {
         float acc[kEpiRows];
 #pragma unroll
         for (int i = 0; i < kEpiRows; i++) {
             const int r = r0 + i;
-            acc[i] = r < e.rows ? __ldcg(&e.partial[((size_t)(c_lo + t) * e.rows + r) * kBM + f]) : 0.f;
+            acc[i] = r < re ? __ldcg(&e.partial[((size_t)(c_lo + t) * e.rows + r) * kBM + f]) : 0.f;
         }
         for (int cc = c_lo + 1; cc <= c_hi; cc++) {
 #pragma unroll
             for (int i = 0; i < kEpiRows; i++) {
                 const int r = r0 + i;
-                if (r < e.rows) acc[i] += __ldcg(&e.partial[((size_t)(cc + t) * e.rows + r) * kBM + f]);
+                if (r < re) acc[i] += __ldcg(&e.partial[((size_t)(cc + t) * e.rows + r) * kBM + f]);
             }
         }
         if (EPI == EPI_RESID) {
@@ -231,10 +238,10 @@ __device__ void tile_epilogue(const GemmArgs& e, int t, int f, float (*sx)[kBM],
                 float x[kEpiRows];
 #pragma unroll
                 for (int i = 0; i < kEpiRows; i++)
-                    x[i] = (r0 + i < e.rows) ? e.X[(size_t)(r0 + i) * e.Nout + fg] : 0.f;
+                    x[i] = (r0 + i < re) ? e.X[(size_t)(r0 + i) * e.Nout + fg] : 0.f;
 #pragma unroll
                 for (int i = 0; i < kEpiRows; i++)
-                    if (r0 + i < e.rows) e.X[(size_t)(r0 + i) * e.Nout + fg] = x[i] + acc[i];
+                    if (r0 + i < re) e.X[(size_t)(r0 + i) * e.Nout + fg] = x[i] + acc[i];
             }
             continue;
         }
@@ -252,14 +259,14 @@ __device__ void tile_epilogue(const GemmArgs& e, int t, int f, float (*sx)[kBM],
                 float cs[kEpiRows], sn[kEpiRows];
 #pragma unroll
                 for (int i = 0; i < kEpiRows; i++) {
-                    const int p = e.pos[min(r0 + i, e.rows - 1)];
+                    const int p = e.pos[min(r0 + i, re - 1)];
                     cs[i] = e.cosb[(size_t)p * half + ip];
                     sn[i] = e.sinb[(size_t)p * half + ip];
                 }
 #pragma unroll
                 for (int i = 0; i < kEpiRows; i++) {
                     const int r = r0 + i;
-                    if (r < e.rows) {
+                    if (r < re) {
                         const float other = sx[i][f ^ half];
                         const float y = (i0 < half) ? acc[i] * cs[i] - other * sn[i] : acc[i] * cs[i] + other * sn[i];
                         if (region == 0) e.Q[(size_t)r * e.dq + fl] = __float2bfloat16_rn(y);
@@ -269,7 +276,7 @@ __device__ void tile_epilogue(const GemmArgs& e, int t, int f, float (*sx)[kBM],
             } else if (fg < e.dq + 2 * e.dkv) {
 #pragma unroll
                 for (int i = 0; i < kEpiRows; i++)
-                    if (r0 + i < e.rows)
+                    if (r0 + i < re)
                         e.VS[(size_t)(r0 + i) * e.dkv + (fg - e.dq - e.dkv)] = __float2bfloat16_rn(acc[i]);
             }
         } else if (EPI == EPI_SWIGLU) {
@@ -277,7 +284,7 @@ __device__ void tile_epilogue(const GemmArgs& e, int t, int f, float (*sx)[kBM],
             if (f < 64 && fo < e.Nout) {
 #pragma unroll
                 for (int i = 0; i < kEpiRows; i++) {
-                    if (r0 + i < e.rows) {
+                    if (r0 + i < re) {
                         const float gt = acc[i], up = sx[i][f + 64];
                         e.H[(size_t)(r0 + i) * e.Nout + fo] = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up);
                     }
@@ -289,7 +296,7 @@ __device__ void tile_epilogue(const GemmArgs& e, int t, int f, float (*sx)[kBM],
 #pragma unroll
             for (int i = 0; i < kEpiRows; i++) {
                 const int r = r0 + i;
-                if (valid && e.logits && r < e.rows) e.logits[(size_t)r * e.Nout + fg] = acc[i];
+                if (valid && e.logits && r < re) e.logits[(size_t)r * e.Nout + fg] = acc[i];
                 float bv = valid ? acc[i] : -INFINITY;
                 int bi = valid ? fg : 0x7fffffff;
 #pragma unroll
@@ -307,7 +314,7 @@ __device__ void tile_epilogue(const GemmArgs& e, int t, int f, float (*sx)[kBM],
                 }
             }
             epi_bar();
-            if (f < kEpiRows && r0 + f < e.rows) {
+            if (f < kEpiRows && r0 + f < re) {
                 float bv = sbv[f][0];
                 int bi = sbi[f][0];
                 for (int w = 1; w < 4; w++)
@@ -342,7 +349,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* tempty = tfull + 2;
     uint32_t* tmem_slot = (uint32_t*)(tempty + 2);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
-    volatile int* last_flag = (volatile int*)(tmem_slot + 2);
     volatile int* epi_abort = (volatile int*)(tmem_slot + 3);  // written by epilogue warps only
     float(*sx)[kBM] = (float(*)[kBM])(smem + kStages * (kStageA + kStageB) + 256);
     float(*sbv)[4] = (float(*)[4])((uint8_t*)sx + kEpiRows * kBM * 4);
@@ -523,20 +529,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[buf]);
                 buf ^= 1;
-                // tile arrival: the last of the tile's CTAs finishes it
+                // announce this CTA's partial of tile t
                 __threadfence();
                 epi_bar();
+                if (f == 0) atomicAdd(&g.cnt[t], 1);
+            }
+            // Fix-up: once every CTA of a tile has arrived, each reduces its
+            // own slice of the rows.  All CTAs are resident (one per SM), so
+            // the bounded wait only waits for work already in progress.
+            for (int t = t_lo; t <= t_hi && !*epi_abort; t++) {
+                const int c_lo = owner_cta((long long)t * g.KB, total, g.ctas);
+                const int c_hi = owner_cta((long long)t * g.KB + g.KB - 1, total, g.ctas);
+                const int n_seg = c_hi - c_lo + 1, me = c - c_lo;
                 if (f == 0) {
-                    const int n_seg = owner_cta((long long)t * g.KB + g.KB - 1, total, g.ctas) -
-                                      owner_cta((long long)t * g.KB, total, g.ctas) + 1;
-                    const int old = atomicAdd(&g.cnt[t], 1);
-                    *last_flag = (old == n_seg - 1);
-                    __threadfence();
+                    const unsigned long long t0 = globaltimer();
+                    while (ld_acquire(&g.cnt[t]) < n_seg) {
+                        if (globaltimer() - t0 > kWaitNs) {
+                            *epi_abort = 1;
+                            raise_err(g.err, LA_ERR_TIMEOUT);
+                            break;
+                        }
+                    }
                 }
                 epi_bar();
-                if (*last_flag) {
-                    tile_epilogue<EPI>(g, t, f, sx, sbv, sbi);
-                    if (f == 0) g.cnt[t] = 0;
+                if (*epi_abort) break;
+                const int rb = (int)((long long)me * g.rows / n_seg), re = (int)((long long)(me + 1) * g.rows / n_seg);
+                tile_epilogue<EPI>(g, t, f, rb, re, c_lo, c_hi, sx, sbv, sbi);
+                epi_bar();
+                if (f == 0) {
+                    __threadfence();
+                    // second round of arrivals: the last one out re-arms the counter
+                    if (atomicAdd(&g.cnt[t], 1) == 2 * n_seg - 1) atomicExch(&g.cnt[t], 0);
                 }
             }
         }
