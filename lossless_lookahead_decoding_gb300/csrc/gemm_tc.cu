@@ -11,14 +11,12 @@
 //
 // Work split (stream-K): the flattened (tile, k-block) space is cut into
 // equal contiguous ranges, one per CTA (one CTA per SM).  A CTA writes one
-// fp32 partial per tile it touches; when all of a tile's CTAs have arrived
-// (per-tile atomic counter), each of them sums its share of the tile's rows
-// over the tile's partials in ascending k order and applies the fused
-// epilogue (RoPE, residual add, SwiGLU, logits + argmax).
-// The split depends only on the matrix shape and the SM count, never on the
-// number of rows, so every token's result is bit-identical whether it is
-// decoded alone (greedy) or among 121 step rows (lookahead): this keeps
-// lookahead output exactly the greedy output.
+// fp32 partial per tile it touches; a second kernel sums the partials of a
+// tile in ascending k order and applies the fused epilogue (RoPE, residual,
+// SwiGLU, logits + argmax).  The split depends only on the matrix shape and
+// the SM count, never on the number of rows, so every token's result is
+// bit-identical whether it is decoded alone (greedy) or among 121 step rows
+// (lookahead): this keeps lookahead output exactly the greedy output.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -42,8 +40,7 @@ constexpr int kStageA = kBM * kBK * 2;   // 16 KB
 constexpr int kStageB = kBN * kBK * 2;   // 16 KB
 constexpr int kThreads = 192;            // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kTmemCols = 256;           // two 128-column fp32 accumulators
-constexpr int kEpiRows = 16;            // tokens per epilogue pass
-constexpr int kSmemBytes = kStages * (kStageA + kStageB) + 1024 + 256 + kEpiRows * kBM * 4 + kEpiRows * 4 * 8;
+constexpr int kSmemBytes = kStages * (kStageA + kStageB) + 1024 + 256;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // bounded waits: 2 s
 
 enum { MODE_ONE = 0, MODE_SEQ3 = 1, MODE_PAIR = 2 };
@@ -51,22 +48,10 @@ enum { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3 };
 
 struct GemmArgs {
     int tiles, KB, ctas, mode;
-    int t0, t1;       // MODE_SEQ3: tiles of map 0, map 1
-    int rows;         // tokens (columns) to store
-    int Nout;         // output features (ragged last tile)
-    float* partial;   // [ctas + tiles][rows][128]
-    int* cnt;         // [tiles] arrival counters (0 between launches)
-    int* err;         // device status word
-    // epilogue operands
-    int dq, dkv, hd;  // QKV + RoPE
-    const int* __restrict__ pos;
-    const float* __restrict__ cosb;
-    const float* __restrict__ sinb;
-    __nv_bfloat16 *__restrict__ Q, *__restrict__ KS, *__restrict__ VS;
-    float* __restrict__ X;                // residual stream (O-proj, down)
-    __nv_bfloat16* __restrict__ H;        // SwiGLU output
-    float* __restrict__ logits;           // optional fp32 logits
-    unsigned long long* amaxp;            // packed per-row argmax
+    int t0, t1;      // MODE_SEQ3: tiles of map 0, map 1
+    int rows;        // tokens (columns) to store
+    float* partial;  // [ctas + tiles][rows][128]
+    int* err;        // device status word
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -192,149 +177,6 @@ __device__ __forceinline__ void raise_err(int* err, int code)
     if (err) atomicCAS(err, 0, code);
 }
 
-__device__ __forceinline__ int owner_cta(long long idx, long long total, int ctas)
-{
-    int c = (int)(idx * ctas / total);
-    while (c > 0 && range_lo(c, total, ctas) > idx) c--;
-    while (c + 1 < ctas && range_lo(c + 1, total, ctas) <= idx) c++;
-    return c;
-}
-
-// Barrier of the four epilogue warps only (named barrier 1, 128 threads).
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-__device__ __forceinline__ int ld_acquire(const int* p)
-{
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Final reduction + epilogue of rows [rb, re) of tile t by the 128 epilogue
-// threads of one of the tile's CTAs (f = feature row of the tile).  Partials
-// are summed in ascending k order, so the result does not depend on which
-// CTA reduces which rows.
-template <int EPI>
-__device__ void tile_epilogue(const GemmArgs& e, int t, int f, int rb, int re, int c_lo, int c_hi, float (*sx)[kBM],
-                              float (*sbv)[4], int (*sbi)[4])
-{
-    for (int r0 = rb; r0 < re; r0 += kEpiRows) {
-        float acc[kEpiRows];
-#pragma unroll
-        for (int i = 0; i < kEpiRows; i++) {
-            const int r = r0 + i;
-            acc[i] = r < re ? __ldcg(&e.partial[((size_t)(c_lo + t) * e.rows + r) * kBM + f]) : 0.f;
-        }
-        for (int cc = c_lo + 1; cc <= c_hi; cc++) {
-#pragma unroll
-            for (int i = 0; i < kEpiRows; i++) {
-                const int r = r0 + i;
-                if (r < re) acc[i] += __ldcg(&e.partial[((size_t)(cc + t) * e.rows + r) * kBM + f]);
-            }
-        }
-        if (EPI == EPI_RESID) {
-            const int fg = t * kBM + f;
-            if (fg < e.Nout) {
-                float x[kEpiRows];
-#pragma unroll
-                for (int i = 0; i < kEpiRows; i++)
-                    x[i] = (r0 + i < re) ? e.X[(size_t)(r0 + i) * e.Nout + fg] : 0.f;
-#pragma unroll
-                for (int i = 0; i < kEpiRows; i++)
-                    if (r0 + i < re) e.X[(size_t)(r0 + i) * e.Nout + fg] = x[i] + acc[i];
-            }
-            continue;
-        }
-        if (EPI == EPI_QKV || EPI == EPI_SWIGLU) {
-#pragma unroll
-            for (int i = 0; i < kEpiRows; i++) sx[i][f] = acc[i];
-            epi_bar();
-        }
-        if (EPI == EPI_QKV) {
-            const int fg = t * kBM + f, half = e.hd >> 1;
-            if (fg < e.dq + e.dkv) {
-                const int region = fg < e.dq ? 0 : 1;
-                const int fl = region == 0 ? fg : fg - e.dq;
-                const int i0 = fl % e.hd, ip = i0 % half;
-                float cs[kEpiRows], sn[kEpiRows];
-#pragma unroll
-                for (int i = 0; i < kEpiRows; i++) {
-                    const int p = e.pos[min(r0 + i, re - 1)];
-                    cs[i] = e.cosb[(size_t)p * half + ip];
-                    sn[i] = e.sinb[(size_t)p * half + ip];
-                }
-#pragma unroll
-                for (int i = 0; i < kEpiRows; i++) {
-                    const int r = r0 + i;
-                    if (r < re) {
-                        const float other = sx[i][f ^ half];
-                        const float y = (i0 < half) ? acc[i] * cs[i] - other * sn[i] : acc[i] * cs[i] + other * sn[i];
-                        if (region == 0) e.Q[(size_t)r * e.dq + fl] = __float2bfloat16_rn(y);
-                        else e.KS[(size_t)r * e.dkv + fl] = __float2bfloat16_rn(y);
-                    }
-                }
-            } else if (fg < e.dq + 2 * e.dkv) {
-#pragma unroll
-                for (int i = 0; i < kEpiRows; i++)
-                    if (r0 + i < re)
-                        e.VS[(size_t)(r0 + i) * e.dkv + (fg - e.dq - e.dkv)] = __float2bfloat16_rn(acc[i]);
-            }
-        } else if (EPI == EPI_SWIGLU) {
-            const int fo = t * 64 + f;
-            if (f < 64 && fo < e.Nout) {
-#pragma unroll
-                for (int i = 0; i < kEpiRows; i++) {
-                    if (r0 + i < re) {
-                        const float gt = acc[i], up = sx[i][f + 64];
-                        e.H[(size_t)(r0 + i) * e.Nout + fo] = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up);
-                    }
-                }
-            }
-        } else if (EPI == EPI_LOGITS) {
-            const int fg = t * kBM + f;
-            const bool valid = fg < e.Nout;
-#pragma unroll
-            for (int i = 0; i < kEpiRows; i++) {
-                const int r = r0 + i;
-                if (valid && e.logits && r < re) e.logits[(size_t)r * e.Nout + fg] = acc[i];
-                float bv = valid ? acc[i] : -INFINITY;
-                int bi = valid ? fg : 0x7fffffff;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-                    if (ov > bv || (ov == bv && oi < bi)) {
-                        bv = ov;
-                        bi = oi;
-                    }
-                }
-                if ((f & 31) == 0) {
-                    sbv[i][f >> 5] = bv;
-                    sbi[i][f >> 5] = bi;
-                }
-            }
-            epi_bar();
-            if (f < kEpiRows && r0 + f < re) {
-                float bv = sbv[f][0];
-                int bi = sbi[f][0];
-                for (int w = 1; w < 4; w++)
-                    if (sbv[f][w] > bv || (sbv[f][w] == bv && sbi[f][w] < bi)) {
-                        bv = sbv[f][w];
-                        bi = sbi[f][w];
-                    }
-                if (bi != 0x7fffffff) {
-                    const uint32_t u = __float_as_uint(bv);
-                    const uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-                    const unsigned long long packed = ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)bi);
-                    atomicMax(&e.amaxp[r0 + f], packed);
-                }
-            }
-        }
-        epi_bar();  // sx / sbv reused by the next row group
-    }
-}
-
-template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap a0, const __grid_constant__ CUtensorMap a1,
               const __grid_constant__ CUtensorMap a2, const __grid_constant__ CUtensorMap bmap, GemmArgs g)
@@ -349,10 +191,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* tempty = tfull + 2;
     uint32_t* tmem_slot = (uint32_t*)(tempty + 2);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
-    volatile int* epi_abort = (volatile int*)(tmem_slot + 3);  // written by epilogue warps only
-    float(*sx)[kBM] = (float(*)[kBM])(smem + kStages * (kStageA + kStageB) + 256);
-    float(*sbv)[4] = (float(*)[4])((uint8_t*)sx + kEpiRows * kBM * 4);
-    int(*sbi)[4] = (int(*)[4])((uint8_t*)sbv + kEpiRows * 4 * 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x;
@@ -369,7 +207,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&tempty[b], 4);
         }
         *abort_flag = 0;
-        *epi_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -498,11 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // ---------------- epilogue warps: TMEM -> fp32 partials; the CTA
-        // that completes a tile also reduces it and applies the epilogue
-        pdl_wait();  // the partial buffer / outputs may still be in use upstream
+        // ---------------- epilogue warps: TMEM -> fp32 partials
+        pdl_wait();  // the partial buffer may still be read by the predecessor
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const int f = threadIdx.x - 64;
         int buf = 0;
         uint32_t tphase[2] = {0, 0};
         if (lo < hi) {
@@ -510,11 +345,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = t_lo; t <= t_hi; t++) {
                 if (!mbar_wait(&tfull[buf], tphase[buf], abort_flag)) {
                     *abort_flag = 1;
-                    *epi_abort = 1;
                     raise_err(g.err, LA_ERR_TIMEOUT);
+                    break;
                 }
-                epi_bar();  // the four warps leave together (no one is left at a barrier)
-                if (*epi_abort) break;
                 tphase[buf] ^= 1;
                 tc_fence_after();
                 float* dst = g.partial + (size_t)(c + t) * g.rows * kBM + q * 32 + lane;
@@ -529,38 +362,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[buf]);
                 buf ^= 1;
-                // announce this CTA's partial of tile t
-                __threadfence();
-                epi_bar();
-                if (f == 0) atomicAdd(&g.cnt[t], 1);
-            }
-            // Fix-up: once every CTA of a tile has arrived, each reduces its
-            // own slice of the rows.  All CTAs are resident (one per SM), so
-            // the bounded wait only waits for work already in progress.
-            for (int t = t_lo; t <= t_hi && !*epi_abort; t++) {
-                const int c_lo = owner_cta((long long)t * g.KB, total, g.ctas);
-                const int c_hi = owner_cta((long long)t * g.KB + g.KB - 1, total, g.ctas);
-                const int n_seg = c_hi - c_lo + 1, me = c - c_lo;
-                if (f == 0) {
-                    const unsigned long long t0 = globaltimer();
-                    while (ld_acquire(&g.cnt[t]) < n_seg) {
-                        if (globaltimer() - t0 > kWaitNs) {
-                            *epi_abort = 1;
-                            raise_err(g.err, LA_ERR_TIMEOUT);
-                            break;
-                        }
-                    }
-                }
-                epi_bar();
-                if (*epi_abort) break;
-                const int rb = (int)((long long)me * g.rows / n_seg), re = (int)((long long)(me + 1) * g.rows / n_seg);
-                tile_epilogue<EPI>(g, t, f, rb, re, c_lo, c_hi, sx, sbv, sbi);
-                epi_bar();
-                if (f == 0) {
-                    __threadfence();
-                    // second round of arrivals: the last one out re-arms the counter
-                    if (atomicAdd(&g.cnt[t], 1) == 2 * n_seg - 1) atomicExch(&g.cnt[t], 0);
-                }
             }
         }
     }
@@ -569,6 +370,160 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    }
+}
+
+// ------------------------------------------------------------- epilogues ---
+
+struct EpiArgs {
+    int tiles, KB, ctas, rows, Nout;
+    const float* __restrict__ partial;
+    // QKV
+    int dq, dkv, hd;
+    const int* __restrict__ pos;
+    const float* __restrict__ cosb;
+    const float* __restrict__ sinb;
+    __nv_bfloat16 *__restrict__ Q, *__restrict__ KS, *__restrict__ VS;
+    // residual
+    float* __restrict__ X;
+    // SwiGLU
+    __nv_bfloat16* __restrict__ H;
+    // logits / argmax
+    float* __restrict__ logits;
+    unsigned long long* amaxp;
+};
+
+__device__ __forceinline__ int owner_cta(long long idx, long long total, int ctas)
+{
+    int c = (int)(idx * ctas / total);
+    while (c > 0 && range_lo(c, total, ctas) > idx) c--;
+    while (c + 1 < ctas && range_lo(c + 1, total, ctas) <= idx) c++;
+    return c;
+}
+
+constexpr int kEpiRows = 16;
+
+// Sum a tile's partials in ascending k order (all loads of a segment in
+// flight together), then apply the fused epilogue for kEpiRows tokens.
+template <int EPI>
+__global__ void __launch_bounds__(128) k_gemm_epi(EpiArgs e)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int t = blockIdx.x, f = threadIdx.x;
+    const long long total = (long long)e.tiles * e.KB;
+    const int c_lo = owner_cta((long long)t * e.KB, total, e.ctas);
+    const int c_hi = owner_cta((long long)t * e.KB + e.KB - 1, total, e.ctas);
+    __shared__ float sx[kEpiRows][kBM];
+    __shared__ float sbv[kEpiRows][4];
+    __shared__ int sbi[kEpiRows][4];
+    const int r0 = blockIdx.y * kEpiRows;
+    float acc[kEpiRows];
+#pragma unroll
+    for (int i = 0; i < kEpiRows; i++) {
+        const int r = r0 + i;
+        acc[i] = r < e.rows ? e.partial[((size_t)(c_lo + t) * e.rows + r) * kBM + f] : 0.f;
+    }
+    for (int cc = c_lo + 1; cc <= c_hi; cc++) {
+#pragma unroll
+        for (int i = 0; i < kEpiRows; i++) {
+            const int r = r0 + i;
+            if (r < e.rows) acc[i] += e.partial[((size_t)(cc + t) * e.rows + r) * kBM + f];
+        }
+    }
+    if (EPI == EPI_RESID) {
+        const int fg = t * kBM + f;
+        if (fg < e.Nout) {
+            float x[kEpiRows];
+#pragma unroll
+            for (int i = 0; i < kEpiRows; i++)
+                x[i] = (r0 + i < e.rows) ? e.X[(size_t)(r0 + i) * e.Nout + fg] : 0.f;
+#pragma unroll
+            for (int i = 0; i < kEpiRows; i++)
+                if (r0 + i < e.rows) e.X[(size_t)(r0 + i) * e.Nout + fg] = x[i] + acc[i];
+        }
+        return;
+    }
+    if (EPI == EPI_QKV || EPI == EPI_SWIGLU) {
+#pragma unroll
+        for (int i = 0; i < kEpiRows; i++) sx[i][f] = acc[i];
+        __syncthreads();
+    }
+    if (EPI == EPI_QKV) {
+        const int fg = t * kBM + f, half = e.hd >> 1;
+        if (fg < e.dq + e.dkv) {
+            const int region = fg < e.dq ? 0 : 1;
+            const int fl = region == 0 ? fg : fg - e.dq;
+            const int i0 = fl % e.hd, ip = i0 % half;
+            float cs[kEpiRows], sn[kEpiRows];
+#pragma unroll
+            for (int i = 0; i < kEpiRows; i++) {
+                const int p = e.pos[min(r0 + i, e.rows - 1)];
+                cs[i] = e.cosb[(size_t)p * half + ip];
+                sn[i] = e.sinb[(size_t)p * half + ip];
+            }
+#pragma unroll
+            for (int i = 0; i < kEpiRows; i++) {
+                const int r = r0 + i;
+                if (r < e.rows) {
+                    const float other = sx[i][f ^ half];
+                    const float y = (i0 < half) ? acc[i] * cs[i] - other * sn[i] : acc[i] * cs[i] + other * sn[i];
+                    if (region == 0) e.Q[(size_t)r * e.dq + fl] = __float2bfloat16_rn(y);
+                    else e.KS[(size_t)r * e.dkv + fl] = __float2bfloat16_rn(y);
+                }
+            }
+        } else if (fg < e.dq + 2 * e.dkv) {
+            for (int i = 0; i < kEpiRows; i++)
+                if (r0 + i < e.rows) e.VS[(size_t)(r0 + i) * e.dkv + (fg - e.dq - e.dkv)] = __float2bfloat16_rn(acc[i]);
+        }
+    } else if (EPI == EPI_SWIGLU) {
+        const int fo = t * 64 + f;
+        if (f < 64 && fo < e.Nout) {
+            for (int i = 0; i < kEpiRows; i++) {
+                if (r0 + i >= e.rows) break;
+                const float gt = acc[i], up = sx[i][f + 64];
+                e.H[(size_t)(r0 + i) * e.Nout + fo] = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up);
+            }
+        }
+    } else if (EPI == EPI_LOGITS) {
+        const int fg = t * kBM + f;
+        const bool valid = fg < e.Nout;
+#pragma unroll
+        for (int i = 0; i < kEpiRows; i++) {
+            const int r = r0 + i;
+            if (valid && e.logits && r < e.rows) e.logits[(size_t)r * e.Nout + fg] = acc[i];
+            float bv = valid ? acc[i] : -INFINITY;
+            int bi = valid ? fg : 0x7fffffff;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (ov > bv || (ov == bv && oi < bi)) {
+                    bv = ov;
+                    bi = oi;
+                }
+            }
+            if ((f & 31) == 0) {
+                sbv[i][f >> 5] = bv;
+                sbi[i][f >> 5] = bi;
+            }
+        }
+        __syncthreads();
+        if (f < kEpiRows && r0 + f < e.rows) {
+            float bv = sbv[f][0];
+            int bi = sbi[f][0];
+            for (int w = 1; w < 4; w++)
+                if (sbv[f][w] > bv || (sbv[f][w] == bv && sbi[f][w] < bi)) {
+                    bv = sbv[f][w];
+                    bi = sbi[f][w];
+                }
+            if (bi != 0x7fffffff) {
+                const uint32_t u = __float_as_uint(bv);
+                const uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+                const unsigned long long packed = ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)bi);
+                atomicMax(&e.amaxp[r0 + f], packed);
+            }
+        }
     }
 }
 
@@ -597,7 +552,6 @@ struct Impl {
     std::vector<GemmCfg> qkv, oproj, gateup, down;
     GemmCfg lm;
     float* partial = nullptr;
-    int* cnt = nullptr;  // per-tile arrival counters
     size_t partial_bytes = 0;
     int* err = nullptr;  // the context's device status word
     void* Q = nullptr;
@@ -642,35 +596,41 @@ void finish_cfg(GemmCfg& g, int K, int sms)
 
 size_t partial_need(const GemmCfg& g) { return (size_t)(g.ctas + g.tiles) * kRows * kBM * 4; }
 
-GemmArgs gemm_args(const Impl& im, const GemmCfg& g, int rows)
+void launch_gemm(const TcPlan& p, const GemmCfg& g, cudaStream_t s, int rows, int cls)
 {
-    GemmArgs a{};
-    a.tiles = g.tiles;
-    a.KB = g.KB;
-    a.ctas = g.ctas;
-    a.mode = g.mode;
-    a.t0 = g.t0;
-    a.t1 = g.t1;
-    a.rows = rows;
-    a.Nout = g.Nout;
-    a.partial = im.partial;
-    a.cnt = im.cnt;
-    a.err = im.err;
-    return a;
-}
-
-template <int EPI>
-void launch_gemm(const TcPlan& p, const GemmCfg& g, cudaStream_t s, const GemmArgs& a, int cls)
-{
+    const Impl& im = *(const Impl*)p.impl;
+    GemmArgs a{g.tiles, g.KB, g.ctas, g.mode, g.t0, g.t1, rows, im.partial, im.err};
     if (p.prof) p.prof->begin(s);
-    launch_pdl(k_gemm_tc<EPI>, dim3(g.ctas), dim3(kThreads), kSmemBytes, s, g.a[0], g.a[1], g.a[2], g.b, a);
+    launch_pdl(k_gemm_tc, dim3(g.ctas), dim3(kThreads), kSmemBytes, s, g.a[0], g.a[1], g.a[2], g.b, a);
     if (p.prof) {
         // algorithmic: every weight once, the rows' inputs once, the rows' outputs once
         const double K = (double)g.KB * kBK, Nw = (double)g.tiles * (g.mode == MODE_PAIR ? 2 * 64 : kBM);
-        const double by = Nw * K * 2 + (double)a.rows * K * 2 + (double)a.rows * Nw * 2;
-        p.prof->end(s, cls, by, 2.0 * a.rows * K * Nw);
+        const double by = Nw * K * 2 + (double)rows * K * 2 + (double)rows * Nw * 2;
+        p.prof->end(s, cls, by, 2.0 * rows * K * Nw);
     }
 }
+
+template <typename F>
+void launch_epi(const TcPlan& p, cudaStream_t s, F f)
+{
+    if (p.prof) p.prof->begin(s);
+    f();
+    if (p.prof) p.prof->end(s, P_GEMM_EPI, 0, 0);
+}
+
+EpiArgs epi_base(const Impl& im, const GemmCfg& g, int rows)
+{
+    EpiArgs e{};
+    e.tiles = g.tiles;
+    e.KB = g.KB;
+    e.ctas = g.ctas;
+    e.rows = rows;
+    e.Nout = g.Nout;
+    e.partial = im.partial;
+    return e;
+}
+
+dim3 epi_grid(const GemmCfg& g, int rows) { return dim3(g.tiles, (rows + kEpiRows - 1) / kEpiRows); }
 
 }  // namespace
 
@@ -767,18 +727,9 @@ int tc_plan_create(TcPlan* p, const la_model_desc& d, const void* const* lw, voi
         return 1;
     }
     im->err = status;
-    int max_tiles = im->lm.tiles;
-    for (int l = 0; l < d.n_layers; l++)
-        for (const GemmCfg* g : {&im->qkv[l], &im->oproj[l], &im->gateup[l], &im->down[l]})
-            max_tiles = g->tiles > max_tiles ? g->tiles : max_tiles;
-    if (cudaFuncSetAttribute(k_gemm_tc<EPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) ||
-        cudaFuncSetAttribute(k_gemm_tc<EPI_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) ||
-        cudaFuncSetAttribute(k_gemm_tc<EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) ||
-        cudaFuncSetAttribute(k_gemm_tc<EPI_LOGITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) ||
-        cudaMalloc((void**)&im->partial, need) != cudaSuccess || cudaMalloc((void**)&im->cnt, max_tiles * 4) ||
-        cudaMemset(im->cnt, 0, max_tiles * 4)) {
+    if (cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess ||
+        cudaMalloc((void**)&im->partial, need) != cudaSuccess) {
         if (im->partial) cudaFree(im->partial);
-        if (im->cnt) cudaFree(im->cnt);
         delete im;
         return -1;
     }
@@ -793,7 +744,6 @@ void tc_plan_destroy(TcPlan* p)
     if (p->impl) {
         Impl* im = (Impl*)p->impl;
         if (im->partial) cudaFree(im->partial);
-        if (im->cnt) cudaFree(im->cnt);
         delete im;
     }
     p->impl = nullptr;
@@ -807,17 +757,18 @@ void tc_qkv_rope(const TcPlan& p, cudaStream_t s, int layer, int rows, const int
 {
     const Impl& im = *(const Impl*)p.impl;
     const GemmCfg& g = im.qkv[layer];
-    GemmArgs a = gemm_args(im, g, rows);
-    a.dq = im.dq;
-    a.dkv = im.dkv;
-    a.hd = im.hd;
-    a.pos = pos;
-    a.cosb = cosb;
-    a.sinb = sinb;
-    a.Q = (__nv_bfloat16*)Q;
-    a.KS = (__nv_bfloat16*)KS;
-    a.VS = (__nv_bfloat16*)VS;
-    launch_gemm<EPI_QKV>(p, g, s, a, P_GEMM_QKV);
+    launch_gemm(p, g, s, rows, P_GEMM_QKV);
+    EpiArgs e = epi_base(im, g, rows);
+    e.dq = im.dq;
+    e.dkv = im.dkv;
+    e.hd = im.hd;
+    e.pos = pos;
+    e.cosb = cosb;
+    e.sinb = sinb;
+    e.Q = (__nv_bfloat16*)Q;
+    e.KS = (__nv_bfloat16*)KS;
+    e.VS = (__nv_bfloat16*)VS;
+    launch_epi(p, s, [&] { launch_pdl(k_gemm_epi<EPI_QKV>, epi_grid(g, rows), dim3(128), 0, s, e); });
 }
 
 bool tc_attn_supported(const TcPlan&) { return false; }
@@ -831,40 +782,44 @@ void tc_oproj_resid(const TcPlan& p, cudaStream_t s, int layer, int rows, float*
 {
     const Impl& im = *(const Impl*)p.impl;
     const GemmCfg& g = im.oproj[layer];
-    GemmArgs a = gemm_args(im, g, rows);
-    a.X = X;
-    launch_gemm<EPI_RESID>(p, g, s, a, P_GEMM_O);
+    launch_gemm(p, g, s, rows, P_GEMM_O);
+    EpiArgs e = epi_base(im, g, rows);
+    e.X = X;
+    launch_epi(p, s, [&] { launch_pdl(k_gemm_epi<EPI_RESID>, epi_grid(g, rows), dim3(128), 0, s, e); });
 }
 
 void tc_gateup_swiglu(const TcPlan& p, cudaStream_t s, int layer, int rows)
 {
     const Impl& im = *(const Impl*)p.impl;
     const GemmCfg& g = im.gateup[layer];
-    GemmArgs a = gemm_args(im, g, rows);
-    a.H = (__nv_bfloat16*)im.HID;
-    launch_gemm<EPI_SWIGLU>(p, g, s, a, P_GEMM_GU);
+    launch_gemm(p, g, s, rows, P_GEMM_GU);
+    EpiArgs e = epi_base(im, g, rows);
+    e.H = (__nv_bfloat16*)im.HID;
+    launch_epi(p, s, [&] { launch_pdl(k_gemm_epi<EPI_SWIGLU>, epi_grid(g, rows), dim3(128), 0, s, e); });
 }
 
 void tc_down_resid(const TcPlan& p, cudaStream_t s, int layer, int rows, float* X)
 {
     const Impl& im = *(const Impl*)p.impl;
     const GemmCfg& g = im.down[layer];
-    GemmArgs a = gemm_args(im, g, rows);
-    a.X = X;
-    launch_gemm<EPI_RESID>(p, g, s, a, P_GEMM_DOWN);
+    launch_gemm(p, g, s, rows, P_GEMM_DOWN);
+    EpiArgs e = epi_base(im, g, rows);
+    e.X = X;
+    launch_epi(p, s, [&] { launch_pdl(k_gemm_epi<EPI_RESID>, epi_grid(g, rows), dim3(128), 0, s, e); });
 }
 
 void tc_lmhead_argmax(const TcPlan& p, cudaStream_t s, int rows, float* logits, unsigned long long* amaxp, int* amax)
 {
     const Impl& im = *(const Impl*)p.impl;
     const GemmCfg& g = im.lm;
-    GemmArgs a = gemm_args(im, g, rows);
-    a.logits = logits;
-    a.amaxp = amaxp;
-    launch_gemm<EPI_LOGITS>(p, g, s, a, P_GEMM_LM);
-    if (p.prof) p.prof->begin(s);
-    launch_pdl(k_argmax_unpack, dim3(1), dim3(kRows), 0, s, amaxp, amax, rows);
-    if (p.prof) p.prof->end(s, P_GEMM_EPI, 0, 0);
+    launch_gemm(p, g, s, rows, P_GEMM_LM);
+    EpiArgs e = epi_base(im, g, rows);
+    e.logits = logits;
+    e.amaxp = amaxp;
+    launch_epi(p, s, [&] {
+        launch_pdl(k_gemm_epi<EPI_LOGITS>, epi_grid(g, rows), dim3(128), 0, s, e);
+        launch_pdl(k_argmax_unpack, dim3(1), dim3(kRows), 0, s, amaxp, amax, rows);
+    });
 }
 
 }  // namespace la
