@@ -6,19 +6,23 @@
 // mask of the lookahead step; a prefill block is one causal group).
 //
 // Keys are walked in chunks of 64 ABSOLUTE positions; chunks are grouped into
-// fixed splits of 256 positions (one CTA per head and split) whose partial
-// softmax states (max, sum, unnormalised output) are merged in ascending
-// split order by a second kernel.  Inside a chunk, S = Q K^T and O += P V run
-// on bf16 mma.sync tiles with fp32 accumulation.  A chunk that lies entirely
-// below P is shared by all rows (16-row slabs, one per warp); a chunk that
-// reaches P is a "tail" chunk: for every row group the warp builds the
-// chunk's 64 key slots from the cache (positions < P) and from that group's
-// step rows (positions >= P) by per-lane ldmatrix row addresses, so that slot
-// j always holds position c*64 + j.  Every row therefore sees exactly the
-// arithmetic it would see if it were decoded alone by plain greedy decoding
-// (chunk and split boundaries at the same absolute positions, same
-// instruction shapes, same reduction order), which keeps lookahead output
-// identical to greedy output.
+// fixed splits of 128 positions whose partial softmax states (max, sum,
+// unnormalised output) are merged in ascending split order by a second
+// kernel.  Inside a chunk, S = Q K^T and O += P V run on bf16 mma.sync tiles
+// with fp32 accumulation.  A chunk that lies entirely below P is shared by
+// all rows (16-row slabs, one per warp); a chunk that reaches P is a "tail"
+// chunk: for every row group a warp builds the chunk's 64 key slots from the
+// cache (positions < P) and from that group's step rows (positions >= P) by
+// per-lane ldmatrix row addresses, so that slot j always holds position
+// c*64 + j.  Every row therefore sees exactly the arithmetic it would see if
+// it were decoded alone by plain greedy decoding (chunk and split boundaries
+// at the same absolute positions, same instruction shapes, same reduction
+// order, exact fp32 state hand-off), which keeps lookahead output identical
+// to greedy output.
+//
+// A split that holds tail chunks is run by kRep CTAs: each repeats the
+// split's shared chunks and then takes a share of the row groups, so the
+// per-group work is spread over more SMs.
 #include "common.cuh"
 
 namespace la {
@@ -26,8 +30,9 @@ namespace la {
 namespace {
 
 constexpr int kChunk = 64;
-constexpr int kSplit = 256;
+constexpr int kSplit = 128;
 constexpr int kWarps = 8;
+constexpr int kRep = 4;
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -84,12 +89,23 @@ struct SlabState {
     float o[HD / 8][4];
 };
 
-// One 64-key chunk for one 16-row slab.  kaddr(j)/vaddr(j) give the shared
-// address of key slot j's row; vis(half, j) says whether the thread's row
-// (g or g+8) sees slot j.  The arithmetic is identical for shared and tail
-// chunks.
-template <int HD, bool MASKED, typename KA, typename VISF>
-__device__ __forceinline__ void chunk_update(const uint32_t (*qf)[4], SlabState<HD>& st, KA kaddr, KA vaddr, VISF vis,
+// Per-lane key-row addressing of one chunk: the rows this lane feeds to
+// ldmatrix (4 for K: key n2*16 + (lane&7) + ((lane>>4)<<3); 4 for V: key
+// kk*16 + (lane&7) + (((lane>>3)&1)<<3)), as unswizzled row base addresses
+// plus the row index that sets the swizzle phase.
+struct KeyRows {
+    uint32_t kb[4], vb[4];
+    int ksw[4], vsw[4];
+};
+
+__device__ __forceinline__ int key_k(int n2, int lane) { return n2 * 16 + (lane & 7) + ((lane >> 4) << 3); }
+__device__ __forceinline__ int key_v(int kk, int lane) { return kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3); }
+
+// One 64-key chunk for one 16-row slab; vis(half, j) says whether the
+// thread's row (g or g+8) sees slot j.  The arithmetic is identical for
+// shared and tail chunks.
+template <int HD, bool MASKED, typename VISF>
+__device__ __forceinline__ void chunk_update(const uint32_t (*qf)[4], SlabState<HD>& st, const KeyRows& kr, VISF vis,
                                              float sl2)
 {
     const int lane = threadIdx.x & 31;
@@ -101,8 +117,7 @@ __device__ __forceinline__ void chunk_update(const uint32_t (*qf)[4], SlabState<
 #pragma unroll
         for (int n2 = 0; n2 < 4; n2++) {
             uint32_t b[4];
-            const int key = n2 * 16 + (lane & 7) + ((lane >> 4) << 3);
-            ldsm_x4(b, kaddr(key) + ((((2 * ks + ((lane >> 3) & 1)) ^ (kaddr.row(key) & 7))) << 4));
+            ldsm_x4(b, kr.kb[n2] + (((2 * ks + ((lane >> 3) & 1)) ^ (kr.ksw[n2] & 7)) << 4));
             mma16816(s[2 * n2], qf[ks], b[0], b[1]);
             mma16816(s[2 * n2 + 1], qf[ks], b[2], b[3]);
         }
@@ -158,59 +173,15 @@ __device__ __forceinline__ void chunk_update(const uint32_t (*qf)[4], SlabState<
         a[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
         a[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
         a[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-        const int key = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
         for (int d2 = 0; d2 < HD / 16; d2++) {
             uint32_t b[4];
-            ldsm_x4_t(b, vaddr(key) + ((((2 * d2 + (lane >> 4)) ^ (vaddr.row(key) & 7))) << 4));
+            ldsm_x4_t(b, kr.vb[kk] + (((2 * d2 + (lane >> 4)) ^ (kr.vsw[kk] & 7)) << 4));
             mma16816(st.o[2 * d2], a, b[0], b[1]);
             mma16816(st.o[2 * d2 + 1], a, b[2], b[3]);
         }
     }
 }
-
-// Key-slot addressing: the row base address (unswizzled) and the row index
-// that sets the swizzle phase.
-template <int HD>
-struct TileAddr {  // slot j -> row j of a contiguous tile
-    uint32_t base;
-    __device__ __forceinline__ uint32_t operator()(int j) const { return base + j * (HD * 2); }
-    __device__ __forceinline__ int row(int j) const { return j; }
-};
-
-template <int HD>
-struct GatherAddr {  // slot j -> cache tile row, step row, or the zero row
-    uint32_t tile, step, zero;
-    int c0, P, tile0, maxoff;
-    const int* gmap;
-    __device__ __forceinline__ int src(int j, int* r) const
-    {
-        const int p = c0 + j;
-        if (p < P) {
-            *r = p - tile0;
-            return 0;
-        }
-        const int o = p - P;
-        if (o < maxoff) {
-            *r = gmap[o];
-            return 1;
-        }
-        *r = 0;
-        return 2;
-    }
-    __device__ __forceinline__ uint32_t operator()(int j) const
-    {
-        int r;
-        const int w = src(j, &r);
-        return w == 0 ? tile + r * (HD * 2) : (w == 1 ? step + r * (HD * 2) : zero);
-    }
-    __device__ __forceinline__ int row(int j) const
-    {
-        int r;
-        src(j, &r);
-        return r;
-    }
-};
 
 struct AttnArgs {
     const DState* st;
@@ -224,30 +195,45 @@ struct AttnArgs {
 };
 
 template <int HD>
+struct AttnSmem {
+    static constexpr int RB = HD * 2, PS = 2 + HD;
+    static constexpr int kQ = 0;                                  // Q tile [kRows][HD]
+    static constexpr int kK0 = kQ + kRows * RB;                   // K chunk buffer 0
+    static constexpr int kV0 = kK0 + kChunk * RB;                 // V chunk buffer 0
+    static constexpr int kDump = kV0 + kChunk * RB;               // K/V buffer 1, later the state dump
+    static constexpr int kK1 = kDump, kV1 = kDump + kChunk * RB;
+    static constexpr int kDumpBytes = kRows * PS * 4 > 2 * kChunk * RB ? kRows * PS * 4 : 2 * kChunk * RB;
+    static constexpr int kKS = kDump + kDumpBytes;               // step K [kRows][HD]
+    static constexpr int kVS = kKS + kRows * RB;                  // step V
+    static constexpr int kZero = kVS + kRows * RB;                // one zero row
+    static constexpr int kInts = kZero + RB;                      // group bookkeeping
+    static constexpr int kBytes = kInts + (2 * kRows + 2) * 4;
+};
+
+template <int HD>
 __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
 {
-    extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int RB = HD * 2, NCH = HD / 8, PS = 2 + HD;
-    uint8_t* sQ = smem;
-    uint8_t* sK0 = sQ + kRows * RB;
-    uint8_t* sV0 = sK0 + 2 * kChunk * RB;
-    uint8_t* sKS = sV0 + 2 * kChunk * RB;
-    uint8_t* sVS = sKS + kRows * RB;
-    uint8_t* sZero = sVS + kRows * RB;
-    int* gcnt = (int*)(sZero + RB);       // [kRows + 1] rows of each group (< a.rows)
-    int* gslab = gcnt + kRows + 1;        // [kRows + 1] slab prefix over groups
-
     pdl_wait();
     pdl_trigger();
+    using L = AttnSmem<HD>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int RB = HD * 2, NCH = HD / 8, PS = L::PS;
+    const uint32_t sb = su32(smem);
+    float* dump = (float*)(smem + L::kDump);
+    int* gcnt = (int*)(smem + L::kInts);  // [kRows + 1] rows of each group (< a.rows)
+    int* gslab = gcnt + kRows + 1;        // [kRows + 1] slab prefix over groups
+
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int h = blockIdx.x, sp = blockIdx.y;
+    const int h = blockIdx.x, sp = blockIdx.y, rep = blockIdx.z;
     const int dq = a.H * HD, dkv = a.Hkv * HD, kvh = h / (a.H / a.Hkv);
     const int P = a.st->P, maxpos = P + a.max_rel;
     const int p0 = sp * kSplit;
     if (p0 > maxpos) return;
     const int c_begin = p0 / kChunk;
-    const int c_end = min(p0 + kSplit, maxpos + 1 + kChunk - 1) / kChunk;  // exclusive
+    const int c_end = min(p0 + kSplit, maxpos + kChunk) / kChunk;  // exclusive
     const int c_shared_end = min(c_end, max(c_begin, P / kChunk));
+    const bool has_tail = c_shared_end < c_end;
+    if (!has_tail && rep > 0) return;  // replicas only serve splits with tail chunks
     const __nv_bfloat16* kc = a.KC + (size_t)kvh * a.max_seq * HD;
     const __nv_bfloat16* vc = a.VC + (size_t)kvh * a.max_seq * HD;
     float* part = a.part + ((size_t)h * a.nsplit + sp) * kRows * PS;
@@ -256,21 +242,19 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
     for (int i = tid; i < kRows * NCH; i += blockDim.x) {
         const int r = i / NCH, c = i % NCH;
         const bool ok = r < a.rows;
-        cp_async16(swz<HD>(su32(sQ), r, c), a.Q + (size_t)(ok ? r : 0) * dq + h * HD + c * 8, ok);
+        cp_async16(swz<HD>(sb + L::kQ, r, c), a.Q + (size_t)(ok ? r : 0) * dq + h * HD + c * 8, ok);
     }
-    auto load_chunk = [&](int cidx, int buf, int valid_end) {
-        uint8_t* dk = sK0 + buf * kChunk * RB;
-        uint8_t* dv = sV0 + buf * kChunk * RB;
+    auto load_chunk = [&](int cidx, int kofs, int vofs, int valid_end) {
         for (int i = tid; i < kChunk * NCH; i += blockDim.x) {
             const int r = i / NCH, c = i % NCH, p = cidx * kChunk + r;
             const bool ok = p < valid_end;
             const size_t off = (size_t)(ok ? p : 0) * HD + c * 8;
-            cp_async16(swz<HD>(su32(dk), r, c), kc + off, ok);
-            cp_async16(swz<HD>(su32(dv), r, c), vc + off, ok);
+            cp_async16(swz<HD>(sb + kofs, r, c), kc + off, ok);
+            cp_async16(swz<HD>(sb + vofs, r, c), vc + off, ok);
         }
     };
     const int n_shared = c_shared_end - c_begin;
-    if (n_shared > 0) load_chunk(c_begin, 0, P);
+    if (n_shared > 0) load_chunk(c_begin, L::kK0, L::kV0, P);
     cp_commit();
 
     SlabState<HD> st;
@@ -281,7 +265,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
 
     uint32_t qf[HD / 16][4];
     for (int i = 0; i < n_shared; i++) {
-        if (i + 1 < n_shared) load_chunk(c_begin + i + 1, (i + 1) & 1, P);
+        if (i + 1 < n_shared)
+            load_chunk(c_begin + i + 1, ((i + 1) & 1) ? L::kK1 : L::kK0, ((i + 1) & 1) ? L::kV1 : L::kV0, P);
         cp_commit();
         cp_wait<1>();
         __syncthreads();
@@ -289,23 +274,31 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
             if (i == 0) {
 #pragma unroll
                 for (int ks = 0; ks < HD / 16; ks++)
-                    ldsm_x4(qf[ks], swz<HD>(su32(sQ), warp * 16 + (lane & 7) + (((lane >> 3) & 1) << 3),
+                    ldsm_x4(qf[ks], swz<HD>(sb + L::kQ, warp * 16 + (lane & 7) + (((lane >> 3) & 1) << 3),
                                             2 * ks + (lane >> 4)));
             }
-            TileAddr<HD> ka{su32(sK0 + (i & 1) * kChunk * RB)}, va{su32(sV0 + (i & 1) * kChunk * RB)};
-            chunk_update<HD, false>(qf, st, ka, va, [](int, int) { return true; }, a.sl2);
+            const uint32_t kt = sb + ((i & 1) ? L::kK1 : L::kK0), vt = sb + ((i & 1) ? L::kV1 : L::kV0);
+            KeyRows kr;
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                kr.kb[j] = kt + key_k(j, lane) * RB;
+                kr.ksw[j] = key_k(j, lane);
+                kr.vb[j] = vt + key_v(j, lane) * RB;
+                kr.vsw[j] = key_v(j, lane);
+            }
+            chunk_update<HD, false>(qf, st, kr, [](int, int) { return true; }, a.sl2);
         }
         __syncthreads();
     }
-    // state after the shared chunks -> this split's partial (read back below
-    // by the tail phase, which may regroup the rows)
+    // state after the shared chunks: final partial, or hand-off to the tail
     {
+        float* dst = has_tail ? dump : part;
         const int g = lane >> 2, t = lane & 3;
 #pragma unroll
         for (int hh = 0; hh < 2; hh++) {
             const int r = warp * 16 + g + 8 * hh;
             if (r < a.rows) {
-                float* pr = part + (size_t)r * PS;
+                float* pr = dst + (size_t)r * PS;
                 if (t == 0) {
                     pr[0] = st.m[hh];
                     pr[1] = st.l[hh];
@@ -318,22 +311,22 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
             }
         }
     }
-    if (c_shared_end >= c_end) return;
+    if (!has_tail) return;
 
     // ---------------- tail chunks: per row group
     cp_wait<0>();
     __syncthreads();
     const int tile0 = c_shared_end * kChunk;  // first tail chunk's cache rows
-    load_chunk(c_shared_end, 0, P);
+    load_chunk(c_shared_end, L::kK0, L::kV0, P);
     for (int i = tid; i < kRows * NCH; i += blockDim.x) {
         const int r = i / NCH, c = i % NCH;
         const bool ok = r < a.rows;
         const size_t off = (size_t)(ok ? r : 0) * dkv + kvh * HD + c * 8;
-        cp_async16(swz<HD>(su32(sKS), r, c), a.KS + off, ok);
-        cp_async16(swz<HD>(su32(sVS), r, c), a.VS + off, ok);
+        cp_async16(swz<HD>(sb + L::kKS, r, c), a.KS + off, ok);
+        cp_async16(swz<HD>(sb + L::kVS, r, c), a.VS + off, ok);
     }
     cp_commit();
-    if (tid < NCH) *(uint4*)(sZero + tid * 16) = make_uint4(0, 0, 0, 0);
+    if (tid < NCH) *(uint4*)(smem + L::kZero + tid * 16) = make_uint4(0, 0, 0, 0);
     // rows of each group, in row order (static lists, clipped to a.rows)
     const int ng = a.rs.ngrp;
     for (int g = tid; g < ng; g += blockDim.x) {
@@ -350,7 +343,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
     __syncthreads();
     const int n_items = gslab[ng];
     const int g4 = lane >> 2;
-    for (int it = warp; it < n_items; it += kWarps) {
+    for (int it = rep * kWarps + warp; it < n_items; it += kRep * kWarps) {
         int g = 0;
         while (gslab[g + 1] <= it) g++;
         const int* glist = a.rs.grp_rows + a.rs.grp_start[g];
@@ -366,11 +359,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
 #pragma unroll
             for (int ks = 0; ks < HD / 16; ks++) {
                 const int ch = 2 * ks + (lane >> 4);
-                const uint32_t addr = rq >= 0 ? swz<HD>(su32(sQ), rq, ch) : su32(sZero) + (ch << 4);
-                ldsm_x4(qf[ks], addr);
+                ldsm_x4(qf[ks], rq >= 0 ? swz<HD>(sb + L::kQ, rq, ch) : sb + L::kZero + (ch << 4));
             }
         }
-        // resume the rows' states
+        // resume the rows' states (exact fp32 hand-off)
         SlabState<HD> ts;
         {
             const int t = lane & 3;
@@ -378,7 +370,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
             for (int hh = 0; hh < 2; hh++) {
                 const int r = hh ? rB : rA;
                 if (r >= 0) {
-                    const float* pr = part + (size_t)r * PS;
+                    const float* pr = dump + (size_t)r * PS;
                     ts.m[hh] = pr[0];
                     ts.l[hh] = pr[1];
 #pragma unroll
@@ -397,10 +389,37 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
         const int* gmap = a.rs.grp_map + (size_t)g * a.rs.maxoff;
         for (int c = c_shared_end; c < c_end; c++) {
             const int c0 = c * kChunk;
-            GatherAddr<HD> ka{su32(sK0), su32(sKS), su32(sZero), c0, P, tile0, a.rs.maxoff, gmap};
-            GatherAddr<HD> va{su32(sV0), su32(sVS), su32(sZero), c0, P, tile0, a.rs.maxoff, gmap};
-            chunk_update<HD, true>(qf, ts, ka, va,
-                                   [&](int hh, int j) { return c0 + j <= (hh ? posB : posA); }, a.sl2);
+            // slot j -> cache tile row, this group's step row, or the zero row
+            KeyRows kr;
+#pragma unroll
+            for (int half = 0; half < 2; half++) {
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    const int key = half ? key_v(j, lane) : key_k(j, lane);
+                    const int p = c0 + key;
+                    int row = 0;
+                    uint32_t kb, vb;
+                    if (p < P) {
+                        row = p - tile0;
+                        kb = sb + L::kK0 + row * RB;
+                        vb = sb + L::kV0 + row * RB;
+                    } else if (p - P < a.rs.maxoff) {
+                        row = gmap[p - P];
+                        kb = sb + L::kKS + row * RB;
+                        vb = sb + L::kVS + row * RB;
+                    } else {
+                        kb = vb = sb + L::kZero;
+                    }
+                    if (half) {
+                        kr.vb[j] = vb;
+                        kr.vsw[j] = row;
+                    } else {
+                        kr.kb[j] = kb;
+                        kr.ksw[j] = row;
+                    }
+                }
+            }
+            chunk_update<HD, true>(qf, ts, kr, [&](int hh, int j) { return c0 + j <= (hh ? posB : posA); }, a.sl2);
         }
         {
             const int t = lane & 3;
@@ -448,9 +467,6 @@ __global__ void k_attn_combine(AttnArgs a)
     a.out[(size_t)r * a.H * HD + h * HD + d] = __float2bfloat16_rn(o / l);
 }
 
-template <int HD>
-size_t attn_smem() { return (size_t)kRows * HD * 2 * 3 + 4 * kChunk * HD * 2 + HD * 2 + (2 * kRows + 2) * 4; }
-
 }  // namespace
 
 size_t attn_mma_partial_bytes(int H, int hd, int max_seq)
@@ -463,10 +479,10 @@ bool attn_mma_init(int hd)
 {
     if (hd == 128)
         return cudaFuncSetAttribute(k_attn_mma<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)attn_smem<128>()) == cudaSuccess;
+                                    AttnSmem<128>::kBytes) == cudaSuccess;
     if (hd == 64)
         return cudaFuncSetAttribute(k_attn_mma<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)attn_smem<64>()) == cudaSuccess;
+                                    AttnSmem<64>::kBytes) == cudaSuccess;
     return false;
 }
 
@@ -492,12 +508,12 @@ void launch_attn_mma(cudaStream_t s, const DState* st, RowSet rs, int max_rel, c
     a.nsplit = (max_seq + kSplit - 1) / kSplit;
     a.max_rel = max_rel;
     a.sl2 = 1.4426950408889634f / sqrtf((float)hd);
-    dim3 grid(H, a.nsplit);
+    dim3 grid(H, a.nsplit, kRep);
     if (hd == 128) {
-        launch_pdl(k_attn_mma<128>, grid, dim3(kWarps * 32), attn_smem<128>(), s, a);
+        launch_pdl(k_attn_mma<128>, grid, dim3(kWarps * 32), AttnSmem<128>::kBytes, s, a);
         launch_pdl(k_attn_combine<128>, dim3(rows, H), dim3(128), 0, s, a);
     } else {
-        launch_pdl(k_attn_mma<64>, grid, dim3(kWarps * 32), attn_smem<64>(), s, a);
+        launch_pdl(k_attn_mma<64>, grid, dim3(kWarps * 32), AttnSmem<64>::kBytes, s, a);
         launch_pdl(k_attn_combine<64>, dim3(rows, H), dim3(64), 0, s, a);
     }
 }
