@@ -157,6 +157,25 @@ LA_API int la_debug_window(la_ctx* ctx, int32_t* host, int cap);
 LA_API const char* la_last_error(la_ctx* ctx);
 LA_API void la_destroy(la_ctx* ctx);
 
+/* ---- standalone attention (one layer of the combined step, bf16) ----
+ * The masked attention la_step runs in every layer, on its own: the T =
+ * 1 + (W+G)(N-1) rows of a step (current token, W x (N-1) lookahead-window
+ * rows, G full candidates x (N-1) verification rows, in that order) at
+ * positions P + offset attend to the cache [0,P) and to the in-step rows the
+ * combined 2D-window + verification mask lets them see (the lookahead
+ * branch and verification branch of the summary page's "Summary").
+ *   q       DEVICE bf16 [T][n_heads][head_dim]  (rotary embedding applied)
+ *   k_cache DEVICE bf16 [n_kv_heads][max_seq][head_dim], v_cache likewise;
+ *           positions [0,P) are read
+ *   k_step  DEVICE bf16 [T][n_kv_heads][head_dim], v_step likewise
+ *   out     DEVICE bf16 [T][n_heads * head_dim]
+ * head_dim 64 or 128; P + W + N - 1 <= max_seq (else LA_ERR_CAPACITY).
+ * Allocates its scratch with cudaMallocAsync on stream and synchronises the
+ * stream before returning. */
+LA_API int la_attention(const void* q, const void* k_cache, const void* v_cache, const void* k_step,
+                        const void* v_step, void* out, int n_heads, int n_kv_heads, int head_dim, int max_seq, int P,
+                        int W, int N, int G, void* stream);
+
 /* ---- standalone n-gram pool (the pool the step uses, exposed for bulk work) ----
  * A GPU hash table keyed on a token, each key holding up to G (N-1)-grams in
  * insertion order with first-in-first-out eviction; an insert of an n-gram

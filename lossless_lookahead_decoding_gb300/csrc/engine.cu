@@ -161,6 +161,61 @@ static Layout make_layout(const la_model_desc* d, int W, int N, int G, int* pool
     return ly;
 }
 
+// Static row tables of the combined step (rows in the order: current token,
+// lookahead rows (l, j) = 1 + l*W + j at offset 1 + j + l, verification rows
+// (g, i) = 1 + W(N-1) + g(N-1) + i at offset 1 + i).  Row groups: window
+// column j -> group j, candidate g -> group W + g, row 0 -> group 0.  map[grp]
+// gives, for each position offset o from P, the step row whose key the
+// group's rows see there (column j: the level-0 rows of columns 0..j, then
+// levels 1.. of column j; candidate g: its own rows).  groups lists every
+// group's rows in row order ([ngrp + 1] starts, then the rows).
+struct StepTables {
+    int T = 1, maxoff = 1, ngrp = 1;
+    std::vector<int> rel, grp, map, groups;
+};
+
+static StepTables step_tables(int W, int N, int G)
+{
+    StepTables tb;
+    const int n1 = N - 1;
+    tb.T = step_rows(W, N, G);
+    tb.rel.assign(kRows, 0);
+    tb.grp.assign(kRows, 0);
+    for (int l = 0; l < n1; l++)
+        for (int j = 0; j < W; j++) {
+            const int r = 1 + l * W + j;
+            tb.rel[r] = 1 + j + l;
+            tb.grp[r] = j;
+        }
+    for (int g = 0; g < G; g++)
+        for (int i = 0; i < n1; i++) {
+            const int r = 1 + W * n1 + g * n1 + i;
+            tb.rel[r] = 1 + i;
+            tb.grp[r] = W + g;
+        }
+    for (int r = 0; r < tb.T; r++) tb.maxoff = tb.rel[r] + 1 > tb.maxoff ? tb.rel[r] + 1 : tb.maxoff;
+    tb.ngrp = W + G > 0 ? W + G : 1;
+    tb.map.assign((size_t)tb.ngrp * tb.maxoff, 0);
+    for (int j = 0; j < W; j++) {
+        int* m = &tb.map[(size_t)j * tb.maxoff];
+        for (int jj = 0; jj <= j; jj++) m[1 + jj] = 1 + jj;         // level 0, columns 0..j
+        for (int l = 1; l < n1; l++) m[1 + j + l] = 1 + l * W + j;  // levels 1.. of column j
+    }
+    for (int g = 0; g < G; g++) {
+        int* m = &tb.map[(size_t)(W + g) * tb.maxoff];
+        for (int i = 0; i < n1; i++) m[1 + i] = 1 + W * n1 + g * n1 + i;
+    }
+    tb.groups.assign(2 * kRows + 1, 0);
+    int k = 0;
+    for (int g = 0; g < tb.ngrp; g++) {
+        tb.groups[g] = k;
+        for (int r = 0; r < tb.T; r++)
+            if (tb.grp[r] == g) tb.groups[kRows + 1 + k++] = r;
+    }
+    tb.groups[tb.ngrp] = k;
+    return tb;
+}
+
 extern "C" size_t la_workspace_bytes(const la_model_desc* desc, int W, int N, int G)
 {
     if (check_desc(desc, W, N, G)) return 0;
@@ -373,49 +428,16 @@ extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* w
     int* gl2 = (int*)(b + ly.off[29]);
     ctx->attn_part = (float*)(b + ly.off[30]);
 
-    // row tables: step (R2/R3 of the oracle's readings) and prefill (causal)
-    const int n1 = N - 1;
-    std::vector<int> rel(kRows, 0), grp(kRows, 0), map((size_t)kRows * kRows, 0);
-    int maxoff = 1;
-    for (int l = 0; l < n1; l++)
-        for (int j = 0; j < W; j++) {
-            int r = 1 + l * W + j;
-            rel[r] = 1 + j + l;
-            grp[r] = j;
-        }
-    for (int g = 0; g < G; g++)
-        for (int i = 0; i < n1; i++) {
-            int r = 1 + W * n1 + g * n1 + i;
-            rel[r] = 1 + i;
-            grp[r] = W + g;
-        }
-    for (int r = 0; r < ctx->T; r++) maxoff = rel[r] + 1 > maxoff ? rel[r] + 1 : maxoff;
-    const int ngrp = W + G > 0 ? W + G : 1;
-    for (int j = 0; j < W; j++) {
-        int* m = &map[(size_t)j * maxoff];
-        for (int jj = 0; jj <= j; jj++) m[1 + jj] = 1 + jj;          // level 0, columns 0..j
-        for (int l = 1; l < n1; l++) m[1 + j + l] = 1 + l * W + j;   // levels 1.. of column j
-    }
-    for (int g = 0; g < G; g++) {
-        int* m = &map[(size_t)(W + g) * maxoff];
-        for (int i = 0; i < n1; i++) m[1 + i] = 1 + W * n1 + g * n1 + i;
-    }
+    // row tables: step (rows, positions and mask of the combined step) and prefill (causal)
+    const StepTables tb = step_tables(W, N, G);
+    const std::vector<int>&rel = tb.rel, &grp = tb.grp, &map = tb.map, &sgl = tb.groups;
+    const int maxoff = tb.maxoff, ngrp = tb.ngrp;
     std::vector<int> prel(kRows), pgrp(kRows, 0), pmap(kRows);
     for (int r = 0; r < kRows; r++) prel[r] = pmap[r] = r;
-    // rows of each group in row order: [ngrp + 1] starts, then the rows
-    std::vector<int> sgl(2 * kRows + 1, 0), pgl(2 * kRows + 1, 0);
-    {
-        int k = 0;
-        for (int g = 0; g < ngrp; g++) {
-            sgl[g] = k;
-            for (int r = 0; r < ctx->T; r++)
-                if (grp[r] == g) sgl[kRows + 1 + k++] = r;
-        }
-        sgl[ngrp] = k;
-        pgl[0] = 0;
-        pgl[1] = kRows;
-        for (int r = 0; r < kRows; r++) pgl[kRows + 1 + r] = r;
-    }
+    std::vector<int> pgl(2 * kRows + 1, 0);
+    pgl[0] = 0;
+    pgl[1] = kRows;
+    for (int r = 0; r < kRows; r++) pgl[kRows + 1 + r] = r;
     std::vector<float> cs((size_t)desc->max_seq * (desc->head_dim / 2)), sn(cs.size());
     for (int p = 0; p < desc->max_seq; p++)
         for (int i = 0; i < desc->head_dim / 2; i++) {
@@ -436,7 +458,7 @@ extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* w
         ck(cudaMemset(ctx->AMAXP, 0, kRows * 8));
         ck(cudaMemcpy(rs1, rel.data(), kRows * 4, cudaMemcpyHostToDevice));
         ck(cudaMemcpy(rs1 + kRows, grp.data(), kRows * 4, cudaMemcpyHostToDevice));
-        ck(cudaMemcpy(map1, map.data(), (size_t)ngrp * maxoff * 4, cudaMemcpyHostToDevice));
+        ck(cudaMemcpy(map1, map.data(), map.size() * 4, cudaMemcpyHostToDevice));
         ck(cudaMemcpy(rs2, prel.data(), kRows * 4, cudaMemcpyHostToDevice));
         ck(cudaMemcpy(rs2 + kRows, pgrp.data(), kRows * 4, cudaMemcpyHostToDevice));
         ck(cudaMemcpy(map2, pmap.data(), kRows * 4, cudaMemcpyHostToDevice));
@@ -709,6 +731,99 @@ extern "C" int la_debug_window(la_ctx* ctx, int32_t* host, int cap)
         LA_CK(cudaStreamSynchronize(ctx->s));
     }
     return LA_OK;
+}
+
+// ------------------------------------------------------ standalone attention ---
+
+// Device scratch of one la_attention call: row tables, positions, the
+// decode state (P) and the split partials.
+struct AttnScratch {
+    int *rel, *grp, *map, *groups, *pos;
+    DState* st;
+    float* part;
+};
+
+static size_t attn_scratch_bytes(const StepTables& tb, int H, int hd, int max_seq)
+{
+    return (size_t)(5 * kRows + 1 + tb.map.size()) * 4 + 256 + sizeof(DState) + 256 +
+           attn_mma_partial_bytes(H, hd, max_seq);
+}
+
+static AttnScratch attn_scratch_carve(char* base, const StepTables& tb)
+{
+    AttnScratch a;
+    int* ip = (int*)base;
+    a.rel = ip;
+    a.grp = ip + kRows;
+    a.groups = ip + 2 * kRows;          // 2 * kRows + 1
+    a.pos = ip + 4 * kRows + 1;
+    a.map = ip + 5 * kRows + 1;
+    size_t off = ((size_t)(5 * kRows + 1 + tb.map.size()) * 4 + 255) & ~(size_t)255;
+    a.st = (DState*)(base + off);
+    off += (sizeof(DState) + 255) & ~(size_t)255;
+    a.part = (float*)(base + off);
+    return a;
+}
+
+// Checks shared by la_attention and its no-allocation variant; fills tb.
+static int attn_check(int H, int Hkv, int hd, int max_seq, int P, int W, int N, int G, StepTables* tb)
+{
+    if ((hd != 64 && hd != 128) || H < 1 || Hkv < 1 || H % Hkv) return LA_ERR_ARG;
+    if (W < 0 || G < 0 || N < 2 || N > kMaxN || step_rows(W, N, G) > kRows || (N - 1) * W > 127) return LA_ERR_ARG;
+    *tb = step_tables(W, N, G);
+    if (P < 0 || P + tb->maxoff > max_seq) return LA_ERR_CAPACITY;
+    return LA_OK;
+}
+
+// Upload the tables and launch; scratch is device memory of attn_scratch_bytes.
+static int attn_run(const StepTables& tb, char* scratch, const void* q, const void* k_cache, const void* v_cache,
+                    const void* k_step, const void* v_step, void* out, int H, int Hkv, int hd, int max_seq, int P,
+                    cudaStream_t s)
+{
+    static bool init64 = false, init128 = false;
+    bool& init = hd == 128 ? init128 : init64;
+    if (!init) {
+        if (!attn_mma_init(hd)) return LA_ERR_CUDA;
+        init = true;
+    }
+    AttnScratch a = attn_scratch_carve(scratch, tb);
+    std::vector<int> pos(kRows, P);
+    for (int r = 0; r < tb.T; r++) pos[r] = P + tb.rel[r];
+    DState hst{};
+    hst.P = P;
+    hst.T = tb.T;
+    hst.ncand = 0;
+    if (cudaMemcpyAsync(a.rel, tb.rel.data(), kRows * 4, cudaMemcpyHostToDevice, s) ||
+        cudaMemcpyAsync(a.grp, tb.grp.data(), kRows * 4, cudaMemcpyHostToDevice, s) ||
+        cudaMemcpyAsync(a.groups, tb.groups.data(), tb.groups.size() * 4, cudaMemcpyHostToDevice, s) ||
+        cudaMemcpyAsync(a.pos, pos.data(), kRows * 4, cudaMemcpyHostToDevice, s) ||
+        cudaMemcpyAsync(a.map, tb.map.data(), tb.map.size() * 4, cudaMemcpyHostToDevice, s) ||
+        cudaMemcpyAsync(a.st, &hst, sizeof(DState), cudaMemcpyHostToDevice, s))
+        return LA_ERR_CUDA;
+    RowSet rs{a.rel, a.grp, a.map, a.groups, a.groups + kRows + 1, tb.maxoff, tb.ngrp};
+    launch_attn_mma(s, a.st, rs, tb.maxoff - 1, a.pos, q, k_cache, v_cache, k_step, v_step, out, a.part, tb.T, H, Hkv,
+                    hd, max_seq);
+    // the host tables above are pageable: wait until the copies have been consumed
+    if (cudaStreamSynchronize(s) != cudaSuccess) return LA_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+}
+
+extern "C" int la_attention(const void* q, const void* k_cache, const void* v_cache, const void* k_step,
+                            const void* v_step, void* out, int n_heads, int n_kv_heads, int head_dim, int max_seq,
+                            int P, int W, int N, int G, void* stream)
+{
+    if (!q || !k_cache || !v_cache || !k_step || !v_step || !out) return LA_ERR_ARG;
+    StepTables tb;
+    int rc = attn_check(n_heads, n_kv_heads, head_dim, max_seq, P, W, N, G, &tb);
+    if (rc) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t bytes = attn_scratch_bytes(tb, n_heads, head_dim, max_seq);
+    char* scratch = nullptr;
+    if (cudaMallocAsync((void**)&scratch, bytes, s) != cudaSuccess) return LA_ERR_OOM;
+    rc = attn_run(tb, scratch, q, k_cache, v_cache, k_step, v_step, out, n_heads, n_kv_heads, head_dim, max_seq, P,
+                  s);
+    if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == LA_OK) rc = LA_ERR_CUDA;
+    return rc;
 }
 
 // --------------------------------------------------------- standalone pool ---

@@ -74,6 +74,7 @@ def lib():
             "om_ctrl_advance": (i32, [vp, vp, vp, vp, vp]), "om_ctrl_pool": (i32, [vp, i32, vp]),
             "om_ctrl_window": (None, [vp, vp]),
             "om_lookahead": (i32, [vp, vp, i32, i32, i32, i32, u64, i32, i32, i32, vp, vp, vp]),
+            "om_attention": (i32, [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -246,6 +247,23 @@ class Controller:
         out = np.zeros(max(self.W, 1) * (self.N - 1), np.int32)
         lib().om_ctrl_window(self.h, _p(out))
         return out[: self.W * (self.N - 1)].reshape(self.N - 1, self.W).copy()
+
+
+def attention(q, k_cache, v_cache, k_step, v_step, vis, pos, P: int):
+    """One layer's masked attention: q [T][H][hd], k/v_cache [Hkv][max_seq][hd]
+    (positions [0,P) used), k/v_step [T][Hkv][hd], vis [T][T], pos [T] ->
+    out [T][H][hd] (fp32)."""
+    f = lambda a: np.ascontiguousarray(a, dtype=np.float32)
+    q, kc, vc, ks, vs = f(q), f(k_cache), f(v_cache), f(k_step), f(v_step)
+    T, H, hd = q.shape
+    Hkv, max_seq = kc.shape[0], kc.shape[1]
+    vis = np.ascontiguousarray(np.asarray(vis, dtype=np.uint8).reshape(T, T))
+    pos = _i32(pos)
+    out = np.zeros((T, H, hd), np.float32)
+    if lib().om_attention(T, H, Hkv, hd, max_seq, P, _p(q), _p(kc), _p(vc), _p(ks), _p(vs), _p(vis), _p(pos),
+                          _p(out)):
+        raise ValueError("om_attention failed")
+    return out
 
 
 def threads() -> int:

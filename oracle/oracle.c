@@ -168,6 +168,84 @@ OM_EXPORT void om_rope(const om_seq* s, float* v, int pos)
     rope(v, s->m->head_dim, s->cosb, s->sinb, pos);
 }
 
+/* visible in-step rows of each row, sorted by (position, index) */
+static void visible_order(int T, const int* pos, const unsigned char* vis, int* order, int* nvis)
+{
+    for (int r = 0; r < T; r++) {
+        int n = 0;
+        for (int c = 0; c < T; c++) {
+            if (!vis[(size_t)r * T + c]) continue;
+            int k = n++;
+            while (k > 0 && pos[order[(size_t)r * T + k - 1]] > pos[c]) {
+                order[(size_t)r * T + k] = order[(size_t)r * T + k - 1];
+                k--;
+            }
+            order[(size_t)r * T + k] = c;
+        }
+        nvis[r] = n;
+    }
+}
+
+/* Softmax attention of one query head vector over the cache rows [0,P)
+ * (row j at kc + j*kv_stride) followed by the visible step rows order[0..nvis)
+ * (row c at ks + c*step_stride), in ascending position order: scores
+ * q.k / sqrt(hd), subtract the max, expf, sum, then the weighted V sum
+ * divided by the sum. */
+static void attend_row(const float* qh, const float* kc, const float* vc, int kv_stride, int P, const float* ks,
+                       const float* vs, int step_stride, const int* order, int nvis, int hd, float* out)
+{
+    const float scale_div = sqrtf((float)hd);
+    int nk = P + nvis;
+    float* sc = (float*)malloc(sizeof(float) * (size_t)(nk > 0 ? nk : 1));
+    for (int j = 0; j < P; j++) sc[j] = dot(qh, kc + (size_t)j * kv_stride, hd) / scale_div;
+    for (int t = 0; t < nvis; t++) sc[P + t] = dot(qh, ks + (size_t)order[t] * step_stride, hd) / scale_div;
+    float mx = -INFINITY;
+    for (int j = 0; j < nk; j++)
+        if (sc[j] > mx) mx = sc[j];
+    float sum = 0.0f;
+    for (int j = 0; j < nk; j++) {
+        sc[j] = expf(sc[j] - mx);
+        sum += sc[j];
+    }
+    for (int e = 0; e < hd; e++) {
+        float acc = 0.0f;
+        for (int j = 0; j < P; j++) acc += sc[j] * vc[(size_t)j * kv_stride + e];
+        for (int t = 0; t < nvis; t++) acc += sc[P + t] * vs[(size_t)order[t] * step_stride + e];
+        out[e] = acc / sum;
+    }
+    free(sc);
+}
+
+/*
+ * One layer's masked attention on its own (the lookahead step's attention
+ * with given q, k, v): q [T][H][hd], k_cache/v_cache [Hkv][max_seq][hd]
+ * (positions [0,P)), k_step/v_step [T][Hkv][hd], vis [T][T] (row r sees step
+ * row c), pos [T].  out [T][H][hd].  Query head h uses KV head h/(H/Hkv).
+ */
+OM_EXPORT int om_attention(int T, int H, int Hkv, int hd, int max_seq, int P, const float* q, const float* k_cache,
+                           const float* v_cache, const float* k_step, const float* v_step, const unsigned char* vis,
+                           const int* pos, float* out)
+{
+    if (T <= 0 || H % Hkv || P < 0 || P > max_seq) return -1;
+    int* order = (int*)malloc(sizeof(int) * (size_t)T * T);
+    int* nvis = (int*)malloc(sizeof(int) * T);
+    if (!order || !nvis) return -1;
+    visible_order(T, pos, vis, order, nvis);
+    const int grp = H / Hkv;
+    #pragma omp parallel for collapse(2) schedule(dynamic)
+    for (int r = 0; r < T; r++)
+        for (int h = 0; h < H; h++) {
+            int kvh = h / grp;
+            attend_row(q + ((size_t)r * H + h) * hd, k_cache + (size_t)kvh * max_seq * hd,
+                       v_cache + (size_t)kvh * max_seq * hd, hd, P, k_step + (size_t)kvh * hd,
+                       v_step + (size_t)kvh * hd, Hkv * hd, order + (size_t)r * T, nvis[r], hd,
+                       out + ((size_t)r * H + h) * hd);
+        }
+    free(order);
+    free(nvis);
+    return 0;
+}
+
 static float silu(float z) { return z / (1.0f + expf(-z)); }
 
 static int argmax_row(const float* x, int n)
@@ -212,25 +290,11 @@ OM_EXPORT int om_step_forward(om_seq* s, int P, int T, const int* tok, const int
     int* nvis = (int*)malloc(sizeof(int) * T);
     if (!x || !xn || !q || !att || !act || !order || !nvis) return -1;
 
-    /* visible in-step rows of each row, sorted by (position, index) */
-    for (int r = 0; r < T; r++) {
-        int n = 0;
-        for (int c = 0; c < T; c++) {
-            if (!vis[(size_t)r * T + c]) continue;
-            int k = n++;
-            while (k > 0 && pos[order[(size_t)r * T + k - 1]] > pos[c]) {
-                order[(size_t)r * T + k] = order[(size_t)r * T + k - 1];
-                k--;
-            }
-            order[(size_t)r * T + k] = c;
-        }
-        nvis[r] = n;
-    }
+    visible_order(T, pos, vis, order, nvis);
 
     for (int r = 0; r < T; r++)
         memcpy(x + (size_t)r * d, m->emb + (size_t)tok[r] * d, sizeof(float) * d);
 
-    const float scale_div = sqrtf((float)hd);
     for (int l = 0; l < L; l++) {
         float* skl = s->sk + (size_t)l * s->cap_rows * dkv;
         float* svl = s->sv + (size_t)l * s->cap_rows * dkv;
@@ -257,30 +321,8 @@ OM_EXPORT int om_step_forward(om_seq* s, int P, int T, const int* tok, const int
         for (int r = 0; r < T; r++)
             for (int h = 0; h < H; h++) {
                 int kvh = h / grp;
-                int nk = P + nvis[r];
-                float* sc = (float*)malloc(sizeof(float) * (size_t)(nk > 0 ? nk : 1));
-                const float* qh = q + (size_t)r * dq + h * hd;
-                for (int j = 0; j < P; j++)
-                    sc[j] = dot(qh, kcl + (size_t)j * dkv + kvh * hd, hd) / scale_div;
-                for (int t = 0; t < nvis[r]; t++) {
-                    int c = order[(size_t)r * T + t];
-                    sc[P + t] = dot(qh, skl + (size_t)c * dkv + kvh * hd, hd) / scale_div;
-                }
-                float mx = -INFINITY;
-                for (int j = 0; j < nk; j++) if (sc[j] > mx) mx = sc[j];
-                float sum = 0.0f;
-                for (int j = 0; j < nk; j++) { sc[j] = expf(sc[j] - mx); sum += sc[j]; }
-                float* out = att + (size_t)r * dq + h * hd;
-                for (int e = 0; e < hd; e++) {
-                    float acc = 0.0f;
-                    for (int j = 0; j < P; j++) acc += sc[j] * vcl[(size_t)j * dkv + kvh * hd + e];
-                    for (int t = 0; t < nvis[r]; t++) {
-                        int c = order[(size_t)r * T + t];
-                        acc += sc[P + t] * svl[(size_t)c * dkv + kvh * hd + e];
-                    }
-                    out[e] = acc / sum;
-                }
-                free(sc);
+                attend_row(q + (size_t)r * dq + h * hd, kcl + kvh * hd, vcl + kvh * hd, dkv, P, skl + kvh * hd,
+                           svl + kvh * hd, dkv, order + (size_t)r * T, nvis[r], hd, att + (size_t)r * dq + h * hd);
             }
 
         #pragma omp parallel for collapse(2) schedule(static)

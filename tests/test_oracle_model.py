@@ -121,3 +121,33 @@ def test_first_token_attention_is_its_own_value():
     lg, _ = s.step(0, [7], [0], [[1]])
     ref = forward64(cfg, w, np.array([7]))
     np.testing.assert_allclose(lg, ref, rtol=1e-5, atol=1e-6)
+
+
+def test_oracle_attention_matches_fp64_masked_softmax():
+    """om_attention against a dense fp64 formulation: keys = cache [0,P) then
+    the step rows, with an explicit mask matrix and a library softmax."""
+    torch = pytest.importorskip("torch")
+    g = np.random.default_rng(4)
+    T, H, Hkv, hd, P, max_seq = 9, 4, 2, 16, 11, 32
+    q = g.standard_normal((T, H, hd)).astype(np.float32)
+    kc = g.standard_normal((Hkv, max_seq, hd)).astype(np.float32)
+    vc = g.standard_normal((Hkv, max_seq, hd)).astype(np.float32)
+    ks = g.standard_normal((T, Hkv, hd)).astype(np.float32)
+    vs = g.standard_normal((T, Hkv, hd)).astype(np.float32)
+    k = O.Controller(2, 3, 2, 16)
+    k.init(np.arange(16, dtype=np.int32), seed=0)
+    for i in range(2):
+        k.insert(1, [i + 2, i + 5])
+    tok, pos, vis = k.rows(1, P)
+    assert len(tok) == T
+    out = O.attention(q, kc, vc, ks, vs, vis, pos, P)
+    ref = np.zeros_like(out, dtype=np.float64)
+    for h in range(H):
+        kvh = h // (H // Hkv)
+        keys = np.concatenate([kc[kvh, :P], ks[:, kvh]]).astype(np.float64)
+        vals = np.concatenate([vc[kvh, :P], vs[:, kvh]]).astype(np.float64)
+        mask = np.concatenate([np.ones((T, P), bool), vis.astype(bool)], axis=1)
+        s = torch.from_numpy(q[:, h].astype(np.float64) @ keys.T / np.sqrt(hd))
+        s = s.masked_fill(~torch.from_numpy(mask), float("-inf"))
+        ref[:, h] = torch.softmax(s, dim=-1).numpy() @ vals
+    np.testing.assert_allclose(out, ref, rtol=1e-5, atol=1e-5)
