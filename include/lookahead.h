@@ -176,6 +176,23 @@ LA_API int la_attention(const void* q, const void* k_cache, const void* v_cache,
                         const void* v_step, void* out, int n_heads, int n_kv_heads, int head_dim, int max_seq, int P,
                         int W, int N, int G, void* stream);
 
+/* la_attention without allocating device memory.  No counterpart in the
+ * paper: it exists for callers that cannot call cudaMalloc (for example code
+ * running while a CUDA graph is being captured, or runtimes whose device
+ * memory is fixed up front).  Same arguments and result as la_attention.
+ * Scratch (the step's row tables and the attention's split partials) lives
+ * in one fixed 16 MiB device array inside this library, which every GPU that
+ * loads the library holds until the process exits; configurations needing
+ * more (n_heads * ceil(max_seq/128) * 128 * (head_dim + 2) * 4 bytes plus a
+ * few KB) return LA_ERR_CAPACITY with a message on stderr.  The first call on
+ * a device looks up the array's device address (make it before any stream
+ * capture).  Every call shares the array: calls that overlap on the GPU race.
+ * Nothing in it needs to start at zero (each call rewrites what it reads).
+ * Synchronises the stream before returning. */
+LA_API int la_attention_noalloc(const void* q, const void* k_cache, const void* v_cache, const void* k_step,
+                                const void* v_step, void* out, int n_heads, int n_kv_heads, int head_dim, int max_seq,
+                                int P, int W, int N, int G, void* stream);
+
 /* ---- standalone n-gram pool (the pool the step uses, exposed for bulk work) ----
  * A GPU hash table keyed on a token, each key holding up to G (N-1)-grams in
  * insertion order with first-in-first-out eviction; an insert of an n-gram

@@ -27,7 +27,7 @@ LA_PRESEED_PROMPT, LA_DEBUG_LOGITS, LA_NO_GRAPH, LA_SIMT, LA_PROFILE = 1, 2, 4, 
 EXPORTS = ("la_workspace_bytes", "la_create", "la_prefill", "la_step", "la_generate", "la_get_stats",
            "la_get_profile",
            "la_debug_logits", "la_debug_argmax", "la_debug_rows", "la_debug_pool", "la_debug_window",
-           "la_last_error", "la_destroy", "la_attention", "la_pool_create", "la_pool_insert", "la_pool_lookup", "la_pool_size",
+           "la_last_error", "la_destroy", "la_attention", "la_attention_noalloc", "la_pool_create", "la_pool_insert", "la_pool_lookup", "la_pool_size",
            "la_pool_destroy")
 
 
@@ -84,6 +84,7 @@ def lib():
             "la_last_error": (C.c_char_p, [vp]),
             "la_destroy": (None, [vp]),
             "la_attention": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp]),
+            "la_attention_noalloc": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp]),
             "la_pool_create": (i32, [i32, i32, i32, vp, vp]),
             "la_pool_insert": (i32, [vp, vp, vp, i32]),
             "la_pool_lookup": (i32, [vp, vp, i32, vp, vp]),
@@ -206,6 +207,14 @@ def la_attention(q, k_cache, v_cache, k_step, v_step, out, n_heads, n_kv_heads, 
     """Pointers are device addresses (ints); returns the C status code."""
     return lib().la_attention(q, k_cache, v_cache, k_step, v_step, out, n_heads, n_kv_heads, head_dim, max_seq, P,
                               W, N, G, stream or None)
+
+
+def la_attention_noalloc(q, k_cache, v_cache, k_step, v_step, out, n_heads, n_kv_heads, head_dim, max_seq, P, W,
+                         N, G, stream: int = 0) -> int:
+    """la_attention with its scratch in the library's fixed device array (no
+    device allocation); returns the C status code."""
+    return lib().la_attention_noalloc(q, k_cache, v_cache, k_step, v_step, out, n_heads, n_kv_heads, head_dim,
+                                      max_seq, P, W, N, G, stream or None)
 
 
 def la_pool_create(capacity: int, N: int, G: int, stream: int = 0):

@@ -15,6 +15,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <string>
 #include <vector>
@@ -824,6 +825,133 @@ extern "C" int la_attention(const void* q, const void* k_cache, const void* v_ca
                   s);
     if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == LA_OK) rc = LA_ERR_CUDA;
     return rc;
+}
+
+// ------------------------------------------ attention without allocation ---
+//
+// For callers that must not allocate device memory: code running while a
+// CUDA graph is being captured in relaxed/global mode, allocator-free
+// embedded runtimes, or hosts whose memory budget is fixed up front.  The
+// scratch lives in one file-scope device array that every GPU loading this
+// library holds until the process exits.  No cudaMalloc/cudaFree, no host
+// heap: the row tables are built in fixed-size arrays on the stack.
+
+constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;  // 16 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_ptr[256];  // device address of the array, per device ordinal
+
+// Host code may not use the array's name as an address: look its device
+// address up once per device, with that device current.
+static int noalloc_scratch(char** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return LA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return LA_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = (char*)g_noalloc_ptr[dev];
+    return LA_OK;
+}
+
+// Fixed-size copy of the step tables (same content as step_tables()).
+struct FixedTables {
+    int T, maxoff, ngrp;
+    int rel[kRows], grp[kRows], groups[2 * kRows + 1], pos[kRows];
+    int map[kRows * kRows];
+};
+
+static int fixed_tables(int W, int N, int G, int P, FixedTables* tb)
+{
+    const int n1 = N - 1;
+    tb->T = step_rows(W, N, G);
+    for (int r = 0; r < kRows; r++) tb->rel[r] = tb->grp[r] = 0;
+    for (int l = 0; l < n1; l++)
+        for (int j = 0; j < W; j++) {
+            tb->rel[1 + l * W + j] = 1 + j + l;
+            tb->grp[1 + l * W + j] = j;
+        }
+    for (int g = 0; g < G; g++)
+        for (int i = 0; i < n1; i++) {
+            tb->rel[1 + W * n1 + g * n1 + i] = 1 + i;
+            tb->grp[1 + W * n1 + g * n1 + i] = W + g;
+        }
+    tb->maxoff = 1;
+    for (int r = 0; r < tb->T; r++) tb->maxoff = tb->rel[r] + 1 > tb->maxoff ? tb->rel[r] + 1 : tb->maxoff;
+    tb->ngrp = W + G > 0 ? W + G : 1;
+    for (int i = 0; i < tb->ngrp * tb->maxoff; i++) tb->map[i] = 0;
+    for (int j = 0; j < W; j++) {
+        int* m = &tb->map[j * tb->maxoff];
+        for (int jj = 0; jj <= j; jj++) m[1 + jj] = 1 + jj;
+        for (int l = 1; l < n1; l++) m[1 + j + l] = 1 + l * W + j;
+    }
+    for (int g = 0; g < G; g++)
+        for (int i = 0; i < n1; i++) tb->map[(W + g) * tb->maxoff + 1 + i] = 1 + W * n1 + g * n1 + i;
+    int k = 0;
+    for (int g = 0; g < tb->ngrp; g++) {
+        tb->groups[g] = k;
+        for (int r = 0; r < tb->T; r++)
+            if (tb->grp[r] == g) tb->groups[kRows + 1 + k++] = r;
+    }
+    tb->groups[tb->ngrp] = k;
+    for (int r = 0; r < kRows; r++) tb->pos[r] = P + (r < tb->T ? tb->rel[r] : 0);
+    return LA_OK;
+}
+
+extern "C" int la_attention_noalloc(const void* q, const void* k_cache, const void* v_cache, const void* k_step,
+                                    const void* v_step, void* out, int n_heads, int n_kv_heads, int head_dim,
+                                    int max_seq, int P, int W, int N, int G, void* stream)
+{
+    if (!q || !k_cache || !v_cache || !k_step || !v_step || !out) return LA_ERR_ARG;
+    if ((head_dim != 64 && head_dim != 128) || n_heads < 1 || n_kv_heads < 1 || n_heads % n_kv_heads) return LA_ERR_ARG;
+    if (W < 0 || G < 0 || N < 2 || N > kMaxN || step_rows(W, N, G) > kRows || (N - 1) * W > 127) return LA_ERR_ARG;
+    static thread_local FixedTables tb;  // 66 KB: kept off the stack, no heap
+    fixed_tables(W, N, G, P, &tb);
+    if (P < 0 || P + tb.maxoff > max_seq) return LA_ERR_CAPACITY;
+    // scratch layout: rel | grp | groups | pos | map | state | split partials
+    const size_t tables = ((size_t)(5 * kRows + 1 + tb.ngrp * tb.maxoff) * 4 + 255) & ~(size_t)255;
+    const size_t state = (sizeof(DState) + 255) & ~(size_t)255;
+    const size_t need = tables + state + attn_mma_partial_bytes(n_heads, head_dim, max_seq);
+    if (need > kNoAllocScratchBytes) {
+        fprintf(stderr, "la_attention_noalloc: needs %zu bytes of scratch, the fixed array holds %zu\n", need,
+                kNoAllocScratchBytes);
+        return LA_ERR_CAPACITY;
+    }
+    char* base = nullptr;
+    int rc = noalloc_scratch(&base);
+    if (rc) return rc;
+    static bool init64 = false, init128 = false;
+    bool& init = head_dim == 128 ? init128 : init64;
+    if (!init) {
+        if (!attn_mma_init(head_dim)) return LA_ERR_CUDA;
+        init = true;
+    }
+    int* ip = (int*)base;
+    DState* st = (DState*)(base + tables);
+    float* part = (float*)(base + tables + state);
+    DState hst{};
+    hst.P = P;
+    hst.T = tb.T;
+    cudaStream_t s = (cudaStream_t)stream;
+    // every piece the kernels read is rewritten here; the partials are
+    // written before they are read, so nothing needs clearing
+    if (cudaMemcpyAsync(ip, tb.rel, kRows * 4, cudaMemcpyHostToDevice, s) ||
+        cudaMemcpyAsync(ip + kRows, tb.grp, kRows * 4, cudaMemcpyHostToDevice, s) ||
+        cudaMemcpyAsync(ip + 2 * kRows, tb.groups, (2 * kRows + 1) * 4, cudaMemcpyHostToDevice, s) ||
+        cudaMemcpyAsync(ip + 4 * kRows + 1, tb.pos, kRows * 4, cudaMemcpyHostToDevice, s) ||
+        cudaMemcpyAsync(ip + 5 * kRows + 1, tb.map, (size_t)tb.ngrp * tb.maxoff * 4, cudaMemcpyHostToDevice, s) ||
+        cudaMemcpyAsync(st, &hst, sizeof(DState), cudaMemcpyHostToDevice, s))
+        return LA_ERR_CUDA;
+    RowSet rs{ip, ip + kRows, ip + 5 * kRows + 1, ip + 2 * kRows, ip + 3 * kRows + 1, tb.maxoff, tb.ngrp};
+    launch_attn_mma(s, st, rs, tb.maxoff - 1, ip + 4 * kRows + 1, q, k_cache, v_cache, k_step, v_step, out, part, tb.T,
+                    n_heads, n_kv_heads, head_dim, max_seq);
+    if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
+    // the host tables are reused by the next call on this thread
+    return cudaStreamSynchronize(s) == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 
 // --------------------------------------------------------- standalone pool ---
