@@ -35,6 +35,9 @@ constexpr int kBK = 64;                  // K per stage (one 128-byte swizzle ro
 #ifndef LA_GEMM_STAGES
 #define LA_GEMM_STAGES 6
 #endif
+#ifndef LA_GEMM_CTAS_PER_SM
+#define LA_GEMM_CTAS_PER_SM 1
+#endif
 constexpr int kStages = LA_GEMM_STAGES;
 constexpr int kStageA = kBM * kBK * 2;   // 16 KB
 constexpr int kStageB = kBN * kBK * 2;   // 16 KB
@@ -103,13 +106,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
-__device__ __forceinline__ void tma_load(const CUtensorMap* map, uint64_t* bar, void* dst, int x, int y)
+// TMA 2D tile load with an L2 eviction-priority hint (policy from
+// createpolicy): weights are read once (evict first), activations are
+// re-read by every CTA (evict last).
+__device__ __forceinline__ void tma_load(const CUtensorMap* map, uint64_t* bar, void* dst, int x, int y, uint64_t pol)
 {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
-        "[%2];" ::"r"(smem_u32(dst)),
-        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+        "{%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(pol)
         : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
 }
 
 // K-major operand, 128-byte swizzle: rows of 128 B, 8-row groups 1024 B apart.
@@ -177,7 +197,7 @@ __device__ __forceinline__ void raise_err(int* err, int code)
     if (err) atomicCAS(err, 0, code);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, LA_GEMM_CTAS_PER_SM)
     k_gemm_tc(const __grid_constant__ CUtensorMap a0, const __grid_constant__ CUtensorMap a1,
               const __grid_constant__ CUtensorMap a2, const __grid_constant__ CUtensorMap bmap, GemmArgs g)
 {
@@ -228,22 +248,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool issued[kStages];
             for (int s = 0; s < kStages; s++) issued[s] = false;
             bool ok = true;
+            const uint64_t pw = policy_evict_first(), pa = policy_evict_last();
             auto load_a = [&](long long idx, int st) {
                 const int t = (int)(idx / g.KB), kx = (int)(idx % g.KB) * kBK;
                 uint8_t* dA = sA + st * kStageA;
                 if (g.mode == MODE_PAIR) {
-                    tma_load(&a0, &full[st], dA, kx, t * 64);
-                    tma_load(&a1, &full[st], dA + 64 * 128, kx, t * 64);
+                    tma_load(&a0, &full[st], dA, kx, t * 64, pw);
+                    tma_load(&a1, &full[st], dA + 64 * 128, kx, t * 64, pw);
                 } else if (g.mode == MODE_SEQ3) {
-                    if (t < g.t0) tma_load(&a0, &full[st], dA, kx, t * kBM);
-                    else if (t < g.t0 + g.t1) tma_load(&a1, &full[st], dA, kx, (t - g.t0) * kBM);
-                    else tma_load(&a2, &full[st], dA, kx, (t - g.t0 - g.t1) * kBM);
+                    if (t < g.t0) tma_load(&a0, &full[st], dA, kx, t * kBM, pw);
+                    else if (t < g.t0 + g.t1) tma_load(&a1, &full[st], dA, kx, (t - g.t0) * kBM, pw);
+                    else tma_load(&a2, &full[st], dA, kx, (t - g.t0 - g.t1) * kBM, pw);
                 } else {
-                    tma_load(&a0, &full[st], dA, kx, t * kBM);
+                    tma_load(&a0, &full[st], dA, kx, t * kBM, pw);
                 }
             };
             auto load_b = [&](long long idx, int st) {
-                tma_load(&bmap, &full[st], sB + st * kStageB, (int)(idx % g.KB) * kBK, 0);
+                tma_load(&bmap, &full[st], sB + st * kStageB, (int)(idx % g.KB) * kBK, 0, pa);
             };
             // The weights do not depend on the preceding kernels: fill the
             // ring with weight tiles before waiting for the activations the
@@ -591,7 +612,8 @@ void finish_cfg(GemmCfg& g, int K, int sms)
 {
     g.KB = (K + kBK - 1) / kBK;
     long long total = (long long)g.tiles * g.KB;
-    g.ctas = (int)(total < sms ? total : sms);
+    const int slots = sms * LA_GEMM_CTAS_PER_SM;
+    g.ctas = (int)(total < slots ? total : slots);
 }
 
 size_t partial_need(const GemmCfg& g) { return (size_t)(g.ctas + g.tiles) * kRows * kBM * 4; }
