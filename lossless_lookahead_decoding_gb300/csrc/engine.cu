@@ -236,15 +236,28 @@ static void forward(la_ctx* c, int rows, const RowSet& rs, bool logits)
     T* HID = (T*)c->HID;
     const float scale = 1.0f / sqrtf((float)hd);
     launch_embed<T>(s, c->tok, (const T*)d.emb, c->X, rows, D);
+    // tensor-core path: the down projection's residual add is folded into the
+    // next RMSNorm (tc_resid_rmsnorm), so it stays pending across the loop
+    TcResid pend{};
+    bool pending = false;
+    auto norm = [&](const T* w, T* out) {
+        if (pending) tc_resid_rmsnorm(c->tc, s, pend, c->X, w, out, D, d.rms_eps);
+        else launch_rmsnorm<T>(s, c->X, w, out, rows, D, d.rms_eps);
+        pending = false;
+    };
     for (int l = 0; l < L; l++) {
         const T* const* w = (const T* const*)&c->lw[(size_t)l * 9];
         T* KS = (T*)c->KS + (size_t)l * kRows * dkv;
         T* VS = (T*)c->VS + (size_t)l * kRows * dkv;
         const T* KC = (const T*)c->KC + (size_t)l * dkv * d.max_seq;
         const T* VC = (const T*)c->VC + (size_t)l * dkv * d.max_seq;
-        c->prof.begin(s);
-        launch_rmsnorm<T>(s, c->X, w[0], XN, rows, D, d.rms_eps);
-        c->prof.end(s, P_NORM, 0, 0);
+        if (pending) {
+            norm(w[0], XN);
+        } else {
+            c->prof.begin(s);
+            launch_rmsnorm<T>(s, c->X, w[0], XN, rows, D, d.rms_eps);
+            c->prof.end(s, P_NORM, 0, 0);
+        }
         if (c->use_tc) {
             tc_qkv_rope(c->tc, s, l, rows, c->pos, c->cosb, c->sinb, (void*)Q, (void*)KS, (void*)VS);
         } else {
@@ -263,23 +276,32 @@ static void forward(la_ctx* c, int rows, const RowSet& rs, bool logits)
             launch_attn_simt<T>(s, c->st, rs, c->pos, Q, KC, VC, KS, VS, ATT, rows, H, Hkv, hd, d.max_seq, scale);
         c->prof.end(s, P_ATTN, rows, 0);  // bytes filled in per step (they depend on P)
         if (c->use_tc) {
-            tc_oproj_resid(c->tc, s, l, rows, c->X);
+            pend = tc_oproj(c->tc, s, l, rows);
+            pending = true;
+            norm(w[5], XN);
         } else {
             launch_gemm_simt_resid<T>(s, ATT, w[4], c->X, rows, dq, D);
+            c->prof.begin(s);
+            launch_rmsnorm<T>(s, c->X, w[5], XN, rows, D, d.rms_eps);
+            c->prof.end(s, P_NORM, 0, 0);
         }
-        c->prof.begin(s);
-        launch_rmsnorm<T>(s, c->X, w[5], XN, rows, D, d.rms_eps);
-        c->prof.end(s, P_NORM, 0, 0);
         if (c->use_tc) {
             tc_gateup_swiglu(c->tc, s, l, rows);
-            tc_down_resid(c->tc, s, l, rows, c->X);
+            pend = tc_down(c->tc, s, l, rows);
+            pending = true;
         } else {
             launch_gemm_simt_swiglu<T>(s, XN, w[6], w[7], HID, rows, D, F);
             launch_gemm_simt_resid<T>(s, HID, w[8], c->X, rows, F, D);
         }
     }
     if (logits) {
-        launch_rmsnorm<T>(s, c->X, (const T*)d.final_norm, XN, rows, D, d.rms_eps);
+        if (pending) {
+            norm((const T*)d.final_norm, XN);
+        } else {
+            c->prof.begin(s);
+            launch_rmsnorm<T>(s, c->X, (const T*)d.final_norm, XN, rows, D, d.rms_eps);
+            c->prof.end(s, P_NORM, 0, 0);
+        }
         if (c->use_tc) {
             tc_lmhead_argmax(c->tc, s, rows, (c->flags & LA_DEBUG_LOGITS) ? c->LOGITS : nullptr, c->AMAXP, c->AMAX);
         } else {

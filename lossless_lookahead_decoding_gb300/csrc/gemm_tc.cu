@@ -414,6 +414,11 @@ struct EpiArgs {
     unsigned long long* amaxp;
 };
 
+struct ResidArgs {
+    int tiles, KB, ctas, rows;
+    const float* __restrict__ partial;
+};
+
 __device__ __forceinline__ int owner_cta(long long idx, long long total, int ctas)
 {
     int c = (int)(idx * ctas / total);
@@ -422,7 +427,7 @@ __device__ __forceinline__ int owner_cta(long long idx, long long total, int cta
     return c;
 }
 
-constexpr int kEpiRows = 16;
+constexpr int kEpiRows = 8;
 
 // Sum a tile's partials in ascending k order (all loads of a segment in
 // flight together), then apply the fused epilogue for kEpiRows tokens.
@@ -556,6 +561,82 @@ __global__ void k_argmax_unpack(unsigned long long* amaxp, int* amax, int rows)
     if (r < rows) {
         amax[r] = (int)(0xFFFFFFFFu - (uint32_t)(amaxp[r] & 0xFFFFFFFFull));
         amaxp[r] = 0ull;
+    }
+}
+
+// Residual add of a stream-K GEMM folded into the RMSNorm that follows it:
+// per row, X += (the tile partials summed in ascending k order) -- the same
+// sums, in the same order, as the residual epilogue -- then
+// XN = X / sqrt(mean(X^2) + eps) * w in bf16.  One block per row.
+constexpr int kRnThreads = 256, kRnVec = 8;  // d <= 8 * 4 * 256
+
+__global__ void __launch_bounds__(kRnThreads) k_resid_rmsnorm(ResidArgs a, float* __restrict__ X,
+                                                             const __nv_bfloat16* __restrict__ w,
+                                                             __nv_bfloat16* __restrict__ out, int d, float eps)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int r = blockIdx.x, d4 = d >> 2;
+    float4* x = (float4*)(X + (size_t)r * d);
+    const long long total = (long long)a.tiles * a.KB;
+    float4 v[kRnVec];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < kRnVec; i++) {
+        const int k = threadIdx.x + i * kRnThreads;
+        if (k < d4) {
+            const int t = (4 * k) / kBM, f = (4 * k) % kBM;
+            const int c_lo = owner_cta((long long)t * a.KB, total, a.ctas);
+            const int c_hi = owner_cta((long long)t * a.KB + a.KB - 1, total, a.ctas);
+            float4 acc = __ldcg((const float4*)&a.partial[((size_t)(c_lo + t) * a.rows + r) * kBM + f]);
+            for (int cc = c_lo + 1; cc <= c_hi; cc++) {
+                const float4 p = __ldcg((const float4*)&a.partial[((size_t)(cc + t) * a.rows + r) * kBM + f]);
+                acc.x += p.x;
+                acc.y += p.y;
+                acc.z += p.z;
+                acc.w += p.w;
+            }
+            const float4 old = x[k];
+            v[i] = make_float4(old.x + acc.x, old.y + acc.y, old.z + acc.z, old.w + acc.w);
+            x[k] = v[i];
+        } else {
+            v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kRnVec; i++) {
+        ss += v[i].x * v[i].x;
+        ss += v[i].y * v[i].y;
+        ss += v[i].z * v[i].z;
+        ss += v[i].w * v[i].w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    __shared__ float part[kRnThreads / 32];
+    __shared__ float s_r;
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float tt = 0.f;
+        for (int i = 0; i < kRnThreads / 32; i++) tt += part[i];
+        s_r = rsqrtf(tt / (float)d + eps);
+    }
+    __syncthreads();
+    const float rr = s_r;
+#pragma unroll
+    for (int i = 0; i < kRnVec; i++) {
+        const int k = threadIdx.x + i * kRnThreads;
+        if (k < d4) {
+            const int e = 4 * k;
+            __nv_bfloat162 lo = __floats2bfloat162_rn(v[i].x * rr * __bfloat162float(w[e]),
+                                                      v[i].y * rr * __bfloat162float(w[e + 1]));
+            __nv_bfloat162 hi = __floats2bfloat162_rn(v[i].z * rr * __bfloat162float(w[e + 2]),
+                                                      v[i].w * rr * __bfloat162float(w[e + 3]));
+            uint2 u;
+            u.x = *reinterpret_cast<uint32_t*>(&lo);
+            u.y = *reinterpret_cast<uint32_t*>(&hi);
+            *(uint2*)(out + (size_t)r * d + e) = u;
+        }
     }
 }
 
@@ -798,6 +879,32 @@ bool tc_attn_supported(const TcPlan&) { return false; }
 void tc_attention(const TcPlan&, cudaStream_t, const DState*, const RowSet&, const int*, const void*, const void*,
                   const void*, const void*, const void*, void*, int)
 {
+}
+
+TcResid tc_oproj(const TcPlan& p, cudaStream_t s, int layer, int rows)
+{
+    const Impl& im = *(const Impl*)p.impl;
+    const GemmCfg& g = im.oproj[layer];
+    launch_gemm(p, g, s, rows, P_GEMM_O);
+    return TcResid{g.tiles, g.KB, g.ctas, rows, im.partial};
+}
+
+TcResid tc_down(const TcPlan& p, cudaStream_t s, int layer, int rows)
+{
+    const Impl& im = *(const Impl*)p.impl;
+    const GemmCfg& g = im.down[layer];
+    launch_gemm(p, g, s, rows, P_GEMM_DOWN);
+    return TcResid{g.tiles, g.KB, g.ctas, rows, im.partial};
+}
+
+void tc_resid_rmsnorm(const TcPlan& p, cudaStream_t s, const TcResid& pend, float* X, const void* w, void* XN, int d,
+                      float eps)
+{
+    ResidArgs a{pend.tiles, pend.KB, pend.ctas, pend.rows, pend.partial};
+    if (p.prof) p.prof->begin(s);
+    launch_pdl(k_resid_rmsnorm, dim3(pend.rows), dim3(kRnThreads), 0, s, a, X, (const __nv_bfloat16*)w,
+               (__nv_bfloat16*)XN, d, eps);
+    if (p.prof) p.prof->end(s, P_NORM, 0, 0);
 }
 
 void tc_oproj_resid(const TcPlan& p, cudaStream_t s, int layer, int rows, float* X)

@@ -26,6 +26,17 @@ bool tc_attn_supported(const TcPlan& p);
 void tc_attention(const TcPlan& p, cudaStream_t s, const DState* st, const RowSet& rs, const int* pos, const void* Q,
                   const void* KC, const void* VC, const void* KS, const void* VS, void* out, int rows);
 void tc_oproj_resid(const TcPlan& p, cudaStream_t s, int layer, int rows, float* X);
+
+// O-proj / down GEMMs whose residual add is left pending, to be folded into
+// the RMSNorm that follows (tc_resid_rmsnorm): X += partial sums, XN = norm(X).
+struct TcResid {
+    int tiles, KB, ctas, rows;
+    const float* partial;
+};
+TcResid tc_oproj(const TcPlan& p, cudaStream_t s, int layer, int rows);
+TcResid tc_down(const TcPlan& p, cudaStream_t s, int layer, int rows);
+void tc_resid_rmsnorm(const TcPlan& p, cudaStream_t s, const TcResid& pend, float* X, const void* w, void* XN, int d,
+                      float eps);
 void tc_gateup_swiglu(const TcPlan& p, cudaStream_t s, int layer, int rows);
 void tc_down_resid(const TcPlan& p, cudaStream_t s, int layer, int rows, float* X);
 void tc_lmhead_argmax(const TcPlan& p, cudaStream_t s, int rows, float* logits, unsigned long long* amaxp, int* amax);
