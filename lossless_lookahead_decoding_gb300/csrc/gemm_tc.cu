@@ -579,30 +579,63 @@ __global__ void __launch_bounds__(kRnThreads) k_resid_rmsnorm(ResidArgs a, float
     const int r = blockIdx.x, d4 = d >> 2;
     float4* x = (float4*)(X + (size_t)r * d);
     const long long total = (long long)a.tiles * a.KB;
-    float4 v[kRnVec];
-    float ss = 0.f;
+    __shared__ int s_lo[kRnVec * kRnThreads * 4 / kBM], s_n[kRnVec * kRnThreads * 4 / kBM];
+    __shared__ int s_maxn;
+    if (threadIdx.x == 0) s_maxn = 0;
+    __syncthreads();
+    for (int t = threadIdx.x; t < a.tiles; t += kRnThreads) {
+        const int lo = owner_cta((long long)t * a.KB, total, a.ctas);
+        s_lo[t] = lo;
+        s_n[t] = owner_cta((long long)t * a.KB + a.KB - 1, total, a.ctas) - lo + 1;
+        atomicMax(&s_maxn, s_n[t]);
+    }
+    __syncthreads();
+    // all of this thread's loads for one segment index in flight together;
+    // each feature still sums its segments in ascending k order
+    float4 v[kRnVec], acc[kRnVec];
+    int tt[kRnVec], ff[kRnVec];
+#pragma unroll
+    for (int i = 0; i < kRnVec; i++) {
+        const int k = threadIdx.x + i * kRnThreads;
+        tt[i] = k < d4 ? (4 * k) / kBM : -1;
+        ff[i] = (4 * k) % kBM;
+        v[i] = k < d4 ? x[k] : make_float4(0.f, 0.f, 0.f, 0.f);
+        acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const int maxn = s_maxn;
+    for (int sg = 0; sg < maxn; sg++) {
+        float4 p[kRnVec];
+#pragma unroll
+        for (int i = 0; i < kRnVec; i++) {
+            const int t = tt[i];
+            p[i] = (t >= 0 && sg < s_n[t])
+                       ? __ldcg((const float4*)&a.partial[((size_t)(s_lo[t] + sg + t) * a.rows + r) * kBM + ff[i]])
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < kRnVec; i++) {
+            const int t = tt[i];
+            if (t >= 0 && sg < s_n[t]) {
+                if (sg == 0) {
+                    acc[i] = p[i];
+                } else {
+                    acc[i].x += p[i].x;
+                    acc[i].y += p[i].y;
+                    acc[i].z += p[i].z;
+                    acc[i].w += p[i].w;
+                }
+            }
+        }
+    }
 #pragma unroll
     for (int i = 0; i < kRnVec; i++) {
         const int k = threadIdx.x + i * kRnThreads;
         if (k < d4) {
-            const int t = (4 * k) / kBM, f = (4 * k) % kBM;
-            const int c_lo = owner_cta((long long)t * a.KB, total, a.ctas);
-            const int c_hi = owner_cta((long long)t * a.KB + a.KB - 1, total, a.ctas);
-            float4 acc = __ldcg((const float4*)&a.partial[((size_t)(c_lo + t) * a.rows + r) * kBM + f]);
-            for (int cc = c_lo + 1; cc <= c_hi; cc++) {
-                const float4 p = __ldcg((const float4*)&a.partial[((size_t)(cc + t) * a.rows + r) * kBM + f]);
-                acc.x += p.x;
-                acc.y += p.y;
-                acc.z += p.z;
-                acc.w += p.w;
-            }
-            const float4 old = x[k];
-            v[i] = make_float4(old.x + acc.x, old.y + acc.y, old.z + acc.z, old.w + acc.w);
+            v[i] = make_float4(v[i].x + acc[i].x, v[i].y + acc[i].y, v[i].z + acc[i].z, v[i].w + acc[i].w);
             x[k] = v[i];
-        } else {
-            v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
+    float ss = 0.f;
 #pragma unroll
     for (int i = 0; i < kRnVec; i++) {
         ss += v[i].x * v[i].x;
