@@ -46,7 +46,7 @@ constexpr int kTmemCols = 256;           // two 128-column fp32 accumulators
 constexpr int kSmemBytes = kStages * (kStageA + kStageB) + 1024 + 256;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // bounded waits: 2 s
 
-enum { MODE_ONE = 0, MODE_SEQ3 = 1, MODE_PAIR = 2 };
+enum { MODE_ONE = 0, MODE_SEQ3 = 1 };
 enum { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3 };
 
 struct GemmArgs {
@@ -252,10 +252,7 @@ __global__ void __launch_bounds__(kThreads, LA_GEMM_CTAS_PER_SM)
             auto load_a = [&](long long idx, int st) {
                 const int t = (int)(idx / g.KB), kx = (int)(idx % g.KB) * kBK;
                 uint8_t* dA = sA + st * kStageA;
-                if (g.mode == MODE_PAIR) {
-                    tma_load(&a0, &full[st], dA, kx, t * 64, pw);
-                    tma_load(&a1, &full[st], dA + 64 * 128, kx, t * 64, pw);
-                } else if (g.mode == MODE_SEQ3) {
+                if (g.mode == MODE_SEQ3) {
                     if (t < g.t0) tma_load(&a0, &full[st], dA, kx, t * kBM, pw);
                     else if (t < g.t0 + g.t1) tma_load(&a1, &full[st], dA, kx, (t - g.t0) * kBM, pw);
                     else tma_load(&a2, &full[st], dA, kx, (t - g.t0 - g.t1) * kBM, pw);
@@ -438,25 +435,29 @@ __global__ void __launch_bounds__(128) k_gemm_epi(EpiArgs e)
     pdl_trigger();
     const int t = blockIdx.x, f = threadIdx.x;
     const long long total = (long long)e.tiles * e.KB;
-    const int c_lo = owner_cta((long long)t * e.KB, total, e.ctas);
-    const int c_hi = owner_cta((long long)t * e.KB + e.KB - 1, total, e.ctas);
     __shared__ float sx[kEpiRows][kBM];
     __shared__ float sbv[kEpiRows][4];
     __shared__ int sbi[kEpiRows][4];
     const int r0 = blockIdx.y * kEpiRows;
-    float acc[kEpiRows];
-#pragma unroll
-    for (int i = 0; i < kEpiRows; i++) {
-        const int r = r0 + i;
-        acc[i] = r < e.rows ? e.partial[((size_t)(c_lo + t) * e.rows + r) * kBM + f] : 0.f;
-    }
-    for (int cc = c_lo + 1; cc <= c_hi; cc++) {
+    // tile tt's partials for this thread's feature, rows r0.., ascending k
+    auto sum_tile = [&](int tt, float* acc) {
+        const int c_lo = owner_cta((long long)tt * e.KB, total, e.ctas);
+        const int c_hi = owner_cta((long long)tt * e.KB + e.KB - 1, total, e.ctas);
 #pragma unroll
         for (int i = 0; i < kEpiRows; i++) {
             const int r = r0 + i;
-            if (r < e.rows) acc[i] += e.partial[((size_t)(cc + t) * e.rows + r) * kBM + f];
+            acc[i] = r < e.rows ? e.partial[((size_t)(c_lo + tt) * e.rows + r) * kBM + f] : 0.f;
         }
-    }
+        for (int cc = c_lo + 1; cc <= c_hi; cc++) {
+#pragma unroll
+            for (int i = 0; i < kEpiRows; i++) {
+                const int r = r0 + i;
+                if (r < e.rows) acc[i] += e.partial[((size_t)(cc + tt) * e.rows + r) * kBM + f];
+            }
+        }
+    };
+    float acc[kEpiRows];
+    sum_tile(t, acc);
     if (EPI == EPI_RESID) {
         const int fg = t * kBM + f;
         if (fg < e.Nout) {
@@ -470,7 +471,7 @@ __global__ void __launch_bounds__(128) k_gemm_epi(EpiArgs e)
         }
         return;
     }
-    if (EPI == EPI_QKV || EPI == EPI_SWIGLU) {
+    if (EPI == EPI_QKV) {
 #pragma unroll
         for (int i = 0; i < kEpiRows; i++) sx[i][f] = acc[i];
         __syncthreads();
@@ -503,12 +504,17 @@ __global__ void __launch_bounds__(128) k_gemm_epi(EpiArgs e)
                 if (r0 + i < e.rows) e.VS[(size_t)(r0 + i) * e.dkv + (fg - e.dq - e.dkv)] = __float2bfloat16_rn(acc[i]);
         }
     } else if (EPI == EPI_SWIGLU) {
-        const int fo = t * 64 + f;
-        if (f < 64 && fo < e.Nout) {
+        // gate tiles come first, then the up tiles of the same features
+        float up[kEpiRows];
+        sum_tile(t + e.tiles / 2, up);
+        const int fo = t * kBM + f;
+        if (fo < e.Nout) {
+#pragma unroll
             for (int i = 0; i < kEpiRows; i++) {
-                if (r0 + i >= e.rows) break;
-                const float gt = acc[i], up = sx[i][f + 64];
-                e.H[(size_t)(r0 + i) * e.Nout + fo] = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up);
+                if (r0 + i < e.rows) {
+                    const float gt = acc[i];
+                    e.H[(size_t)(r0 + i) * e.Nout + fo] = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up[i]);
+                }
             }
         }
     } else if (EPI == EPI_LOGITS) {
@@ -568,7 +574,7 @@ __global__ void k_argmax_unpack(unsigned long long* amaxp, int* amax, int rows)
 // per row, X += (the tile partials summed in ascending k order) -- the same
 // sums, in the same order, as the residual epilogue -- then
 // XN = X / sqrt(mean(X^2) + eps) * w in bf16.  One block per row.
-constexpr int kRnThreads = 256, kRnVec = 8;  // d <= 8 * 4 * 256
+constexpr int kRnThreads = 1024, kRnVec = 2, kRnSeg = 8;  // d <= 2 * 4 * 1024
 
 __global__ void __launch_bounds__(kRnThreads) k_resid_rmsnorm(ResidArgs a, float* __restrict__ X,
                                                              const __nv_bfloat16* __restrict__ w,
@@ -580,62 +586,47 @@ __global__ void __launch_bounds__(kRnThreads) k_resid_rmsnorm(ResidArgs a, float
     float4* x = (float4*)(X + (size_t)r * d);
     const long long total = (long long)a.tiles * a.KB;
     __shared__ int s_lo[kRnVec * kRnThreads * 4 / kBM], s_n[kRnVec * kRnThreads * 4 / kBM];
-    __shared__ int s_maxn;
-    if (threadIdx.x == 0) s_maxn = 0;
-    __syncthreads();
     for (int t = threadIdx.x; t < a.tiles; t += kRnThreads) {
         const int lo = owner_cta((long long)t * a.KB, total, a.ctas);
         s_lo[t] = lo;
         s_n[t] = owner_cta((long long)t * a.KB + a.KB - 1, total, a.ctas) - lo + 1;
-        atomicMax(&s_maxn, s_n[t]);
     }
     __syncthreads();
-    // all of this thread's loads for one segment index in flight together;
-    // each feature still sums its segments in ascending k order
-    float4 v[kRnVec], acc[kRnVec];
-    int tt[kRnVec], ff[kRnVec];
+    float4 v[kRnVec];
+    float ss = 0.f;
 #pragma unroll
     for (int i = 0; i < kRnVec; i++) {
         const int k = threadIdx.x + i * kRnThreads;
-        tt[i] = k < d4 ? (4 * k) / kBM : -1;
-        ff[i] = (4 * k) % kBM;
-        v[i] = k < d4 ? x[k] : make_float4(0.f, 0.f, 0.f, 0.f);
-        acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    const int maxn = s_maxn;
-    for (int sg = 0; sg < maxn; sg++) {
-        float4 p[kRnVec];
-#pragma unroll
-        for (int i = 0; i < kRnVec; i++) {
-            const int t = tt[i];
-            p[i] = (t >= 0 && sg < s_n[t])
-                       ? __ldcg((const float4*)&a.partial[((size_t)(s_lo[t] + sg + t) * a.rows + r) * kBM + ff[i]])
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (k >= d4) {
+            v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            continue;
         }
+        const int t = (4 * k) / kBM, f = (4 * k) % kBM, lo = s_lo[t], n = s_n[t];
+        const float4* src = (const float4*)&a.partial[((size_t)(lo + t) * a.rows + r) * kBM + f];
+        const size_t seg = (size_t)a.rows * kBM / 4;  // float4 stride between segments
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s0 = 0; s0 < n; s0 += kRnSeg) {
+            float4 p[kRnSeg];  // up to kRnSeg loads in flight, then summed in order
 #pragma unroll
-        for (int i = 0; i < kRnVec; i++) {
-            const int t = tt[i];
-            if (t >= 0 && sg < s_n[t]) {
-                if (sg == 0) {
-                    acc[i] = p[i];
+            for (int j = 0; j < kRnSeg; j++)
+                p[j] = s0 + j < n ? __ldcg(src + (size_t)(s0 + j) * seg) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < kRnSeg; j++) {
+                if (s0 + j >= n) break;
+                if (s0 + j == 0) {
+                    acc = p[j];
                 } else {
-                    acc[i].x += p[i].x;
-                    acc[i].y += p[i].y;
-                    acc[i].z += p[i].z;
-                    acc[i].w += p[i].w;
+                    acc.x += p[j].x;
+                    acc.y += p[j].y;
+                    acc.z += p[j].z;
+                    acc.w += p[j].w;
                 }
             }
         }
+        const float4 old = x[k];
+        v[i] = make_float4(old.x + acc.x, old.y + acc.y, old.z + acc.z, old.w + acc.w);
+        x[k] = v[i];
     }
-#pragma unroll
-    for (int i = 0; i < kRnVec; i++) {
-        const int k = threadIdx.x + i * kRnThreads;
-        if (k < d4) {
-            v[i] = make_float4(v[i].x + acc[i].x, v[i].y + acc[i].y, v[i].z + acc[i].z, v[i].w + acc[i].w);
-            x[k] = v[i];
-        }
-    }
-    float ss = 0.f;
 #pragma unroll
     for (int i = 0; i < kRnVec; i++) {
         ss += v[i].x * v[i].x;
@@ -740,7 +731,7 @@ void launch_gemm(const TcPlan& p, const GemmCfg& g, cudaStream_t s, int rows, in
     launch_pdl(k_gemm_tc, dim3(g.ctas), dim3(kThreads), kSmemBytes, s, g.a[0], g.a[1], g.a[2], g.b, a);
     if (p.prof) {
         // algorithmic: every weight once, the rows' inputs once, the rows' outputs once
-        const double K = (double)g.KB * kBK, Nw = (double)g.tiles * (g.mode == MODE_PAIR ? 2 * 64 : kBM);
+        const double K = (double)g.KB * kBK, Nw = (double)g.tiles * kBM;
         const double by = Nw * K * 2 + (double)rows * K * 2 + (double)rows * Nw * 2;
         p.prof->end(s, cls, by, 2.0 * rows * K * Nw);
     }
@@ -823,13 +814,14 @@ int tc_plan_create(TcPlan* p, const la_model_desc& d, const void* const* lw, voi
         o.tiles = (d.d_model + kBM - 1) / kBM;
         o.Nout = d.d_model;
         finish_cfg(o, dq, sms);
-        GemmCfg gu{};
-        ok &= make_map(&gu.a[0], w[6], d.ffn, d.d_model, 64);
-        ok &= make_map(&gu.a[1], w[7], d.ffn, d.d_model, 64);
+        GemmCfg gu{};  // gate tiles, then up tiles (128 rows each)
+        ok &= make_map(&gu.a[0], w[6], d.ffn, d.d_model, kBM);
+        ok &= make_map(&gu.a[1], w[7], d.ffn, d.d_model, kBM);
         gu.a[2] = gu.a[0];
         gu.b = bXN;
-        gu.mode = MODE_PAIR;
-        gu.tiles = (d.ffn + 63) / 64;
+        gu.mode = MODE_SEQ3;
+        gu.t0 = gu.t1 = (d.ffn + kBM - 1) / kBM;
+        gu.tiles = 2 * gu.t0;
         gu.Nout = d.ffn;
         finish_cfg(gu, d.d_model, sms);
         GemmCfg dn{};
@@ -957,7 +949,9 @@ void tc_gateup_swiglu(const TcPlan& p, cudaStream_t s, int layer, int rows)
     launch_gemm(p, g, s, rows, P_GEMM_GU);
     EpiArgs e = epi_base(im, g, rows);
     e.H = (__nv_bfloat16*)im.HID;
-    launch_epi(p, s, [&] { launch_pdl(k_gemm_epi<EPI_SWIGLU>, epi_grid(g, rows), dim3(128), 0, s, e); });
+    launch_epi(p, s, [&] {
+        launch_pdl(k_gemm_epi<EPI_SWIGLU>, dim3(g.tiles / 2, (rows + kEpiRows - 1) / kEpiRows), dim3(128), 0, s, e);
+    });
 }
 
 void tc_down_resid(const TcPlan& p, cudaStream_t s, int layer, int rows, float* X)
