@@ -6,7 +6,8 @@
 // W [Nout][K] (row-major, K-major) is the 128-row A operand, the activations
 // X [128][K] the N = 128 B operand, and the fp32 accumulator D[feature][token]
 // lives in tensor memory.  Operands are staged by TMA (128-byte swizzle) into
-// a 6-deep shared-memory ring; one thread issues tcgen05.mma, one thread
+// a 3-deep shared-memory ring of 128-K stages (two 64-K swizzle atoms per
+// operand: fewer barrier round trips per byte); one thread issues tcgen05.mma, one thread
 // issues TMA, and four warps drain TMEM.
 //
 // Work split (stream-K): the flattened (tile, k-block) space is cut into
@@ -31,15 +32,20 @@ namespace {
 
 constexpr int kBM = 128;                 // weight rows per tile (MMA M)
 constexpr int kBN = 128;                 // token columns (MMA N)
-constexpr int kBK = 64;                  // K per stage (one 128-byte swizzle row)
+#ifndef LA_GEMM_ATOMS
+#define LA_GEMM_ATOMS 2
+#endif
+constexpr int kAtom = 64;                // K per swizzle atom (one 128-byte row)
+constexpr int kAtoms = LA_GEMM_ATOMS;    // atoms per pipeline stage
+constexpr int kBK = kAtom * kAtoms;      // K per stage
 #ifndef LA_GEMM_STAGES
-#define LA_GEMM_STAGES 6
+#define LA_GEMM_STAGES 3
 #endif
 #ifndef LA_GEMM_CTAS_PER_SM
 #define LA_GEMM_CTAS_PER_SM 1
 #endif
 constexpr int kStages = LA_GEMM_STAGES;
-constexpr int kStageA = kBM * kBK * 2;   // 16 KB
+constexpr int kStageA = kBM * kBK * 2;   // 16 KB per atom
 constexpr int kStageB = kBN * kBK * 2;   // 16 KB
 constexpr int kThreads = 192;            // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kTmemCols = 256;           // two 128-column fp32 accumulators
@@ -250,18 +256,30 @@ __global__ void __launch_bounds__(kThreads, LA_GEMM_CTAS_PER_SM)
             bool ok = true;
             const uint64_t pw = policy_evict_first(), pa = policy_evict_last();
             auto load_a = [&](long long idx, int st) {
-                const int t = (int)(idx / g.KB), kx = (int)(idx % g.KB) * kBK;
-                uint8_t* dA = sA + st * kStageA;
+                const int t = (int)(idx / g.KB);
+                const CUtensorMap* m = &a0;
+                int row = t * kBM;
                 if (g.mode == MODE_SEQ3) {
-                    if (t < g.t0) tma_load(&a0, &full[st], dA, kx, t * kBM, pw);
-                    else if (t < g.t0 + g.t1) tma_load(&a1, &full[st], dA, kx, (t - g.t0) * kBM, pw);
-                    else tma_load(&a2, &full[st], dA, kx, (t - g.t0 - g.t1) * kBM, pw);
-                } else {
-                    tma_load(&a0, &full[st], dA, kx, t * kBM, pw);
+                    if (t < g.t0) {
+                        m = &a0;
+                    } else if (t < g.t0 + g.t1) {
+                        m = &a1;
+                        row = (t - g.t0) * kBM;
+                    } else {
+                        m = &a2;
+                        row = (t - g.t0 - g.t1) * kBM;
+                    }
                 }
+#pragma unroll
+                for (int a = 0; a < kAtoms; a++)
+                    tma_load(m, &full[st], sA + st * kStageA + a * (kBM * kAtom * 2),
+                             (int)(idx % g.KB) * kBK + a * kAtom, row, pw);
             };
             auto load_b = [&](long long idx, int st) {
-                tma_load(&bmap, &full[st], sB + st * kStageB, (int)(idx % g.KB) * kBK, 0, pa);
+#pragma unroll
+                for (int a = 0; a < kAtoms; a++)
+                    tma_load(&bmap, &full[st], sB + st * kStageB + a * (kBN * kAtom * 2),
+                             (int)(idx % g.KB) * kBK + a * kAtom, 0, pa);
             };
             // The weights do not depend on the preceding kernels: fill the
             // ring with weight tiles before waiting for the activations the
@@ -333,9 +351,12 @@ __global__ void __launch_bounds__(kThreads, LA_GEMM_CTAS_PER_SM)
                 const uint32_t b_base = smem_u32(sB + stage * kStageB);
                 const uint32_t d = tmem + buf * kBN;
 #pragma unroll
-                for (int k = 0; k < kBK / 16; k++)
-                    mma_bf16(d, sw128_desc(a_base + k * 32), sw128_desc(b_base + k * 32), idesc,
-                             (first && k == 0) ? 0u : 1u);
+                for (int a = 0; a < kAtoms; a++)
+#pragma unroll
+                    for (int k = 0; k < kAtom / 16; k++)
+                        mma_bf16(d, sw128_desc(a_base + a * (kBM * kAtom * 2) + k * 32),
+                                 sw128_desc(b_base + a * (kBN * kAtom * 2) + k * 32), idesc,
+                                 (first && a == 0 && k == 0) ? 0u : 1u);
                 mma_commit(&empty[stage]);
                 if (last) {
                     mma_commit(&tfull[buf]);
@@ -705,7 +726,7 @@ bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int box_rows
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+    cuuint32_t box[2] = {(cuuint32_t)kAtom, (cuuint32_t)box_rows};
     cuuint32_t es[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -768,7 +789,7 @@ int tc_plan_create(TcPlan* p, const la_model_desc& d, const void* const* lw, voi
     p->impl = nullptr;
     if (esz != 2) return 1;
     const int dq = d.n_heads * d.head_dim, dkv = d.n_kv_heads * d.head_dim;
-    if (dq % kBM || dkv % kBM || d.d_model % kBK) return 1;
+    if (dq % kBM || dkv % kBM || d.d_model % kAtom) return 1;
     if (!get_encode()) return 1;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
