@@ -20,9 +20,9 @@
 // order, exact fp32 state hand-off), which keeps lookahead output identical
 // to greedy output.
 //
-// A split that holds tail chunks is run by kRep CTAs: each repeats the
-// split's shared chunks and then takes a share of the row groups, so the
-// per-group work is spread over more SMs.
+// The split that holds the first tail chunk is run by kRep CTAs: each
+// repeats the split's shared chunks and then takes a share of the row
+// groups, so the per-group work is spread over more SMs.
 #include "common.cuh"
 
 namespace la {
@@ -224,9 +224,15 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
     int* gslab = gcnt + kRows + 1;        // [kRows + 1] slab prefix over groups
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int h = blockIdx.x, sp = blockIdx.y, rep = blockIdx.z;
-    const int dq = a.H * HD, dkv = a.Hkv * HD, kvh = h / (a.H / a.Hkv);
+    const int dq = a.H * HD, dkv = a.Hkv * HD;
     const int P = a.st->P, maxpos = P + a.max_rel;
+    // blockIdx.y < nsplit: split y; beyond: extra CTAs for the split that
+    // holds the first tail chunk (the chunk containing position P)
+    const int h = blockIdx.x, kvh = h / (a.H / a.Hkv);
+    const int tail_split = (P / kChunk) * kChunk / kSplit;
+    const int sp = blockIdx.y < a.nsplit ? blockIdx.y : tail_split;
+    const int rep = blockIdx.y < a.nsplit ? 0 : blockIdx.y - a.nsplit + 1;
+    const int n_rep = sp == tail_split ? kRep : 1;
     const int p0 = sp * kSplit;
     if (p0 > maxpos) return;
     const int c_begin = p0 / kChunk;
@@ -343,7 +349,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
     __syncthreads();
     const int n_items = gslab[ng];
     const int g4 = lane >> 2;
-    for (int it = rep * kWarps + warp; it < n_items; it += kRep * kWarps) {
+    for (int it = rep * kWarps + warp; it < n_items; it += n_rep * kWarps) {
         int g = 0;
         while (gslab[g + 1] <= it) g++;
         const int* glist = a.rs.grp_rows + a.rs.grp_start[g];
@@ -508,7 +514,7 @@ void launch_attn_mma(cudaStream_t s, const DState* st, RowSet rs, int max_rel, c
     a.nsplit = (max_seq + kSplit - 1) / kSplit;
     a.max_rel = max_rel;
     a.sl2 = 1.4426950408889634f / sqrtf((float)hd);
-    dim3 grid(H, a.nsplit, kRep);
+    dim3 grid(H, a.nsplit + kRep - 1);
     if (hd == 128) {
         launch_pdl(k_attn_mma<128>, grid, dim3(kWarps * 32), AttnSmem<128>::kBytes, s, a);
         launch_pdl(k_attn_combine<128>, dim3(rows, H), dim3(128), 0, s, a);
