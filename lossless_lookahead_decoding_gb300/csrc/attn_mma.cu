@@ -449,26 +449,45 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
     }
 }
 
-// Merge the splits of every (row, head) in ascending split order.
+// Merge the splits of every (row, head) in ascending split order (the loads
+// of up to 8 splits are issued together, the merge runs in order).
 template <int HD>
 __global__ void k_attn_combine(AttnArgs a)
 {
     pdl_wait();
     pdl_trigger();
     const int r = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
-    constexpr int PS = 2 + HD;
+    constexpr int PS = 2 + HD, kB = 8;
     const int ns = a.pos[r] / kSplit + 1;
     const float* base = a.part + (size_t)h * a.nsplit * kRows * PS + (size_t)r * PS;
-    float m = base[0], l = base[1], o = base[2 + d];
-    for (int s = 1; s < ns; s++) {
-        const float* pr = base + (size_t)s * kRows * PS;
-        const float ms = pr[0];
-        const float mn = fmaxf(m, ms);
-        const float mu = (mn == -INFINITY) ? 0.f : mn;
-        const float fa = exp2f(m - mu), fb = exp2f(ms - mu);
-        l = l * fa + pr[1] * fb;
-        o = o * fa + pr[2 + d] * fb;
-        m = mn;
+    const size_t stride = (size_t)kRows * PS;
+    float m = -INFINITY, l = 0.f, o = 0.f;
+    for (int s0 = 0; s0 < ns; s0 += kB) {
+        float ms[kB], ls[kB], os[kB];
+#pragma unroll
+        for (int j = 0; j < kB; j++) {
+            const bool ok = s0 + j < ns;
+            const float* pr = base + (size_t)(s0 + j) * stride;
+            ms[j] = ok ? pr[0] : -INFINITY;
+            ls[j] = ok ? pr[1] : 0.f;
+            os[j] = ok ? pr[2 + d] : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < kB; j++) {
+            if (s0 + j >= ns) break;
+            if (s0 + j == 0) {
+                m = ms[j];
+                l = ls[j];
+                o = os[j];
+                continue;
+            }
+            const float mn = fmaxf(m, ms[j]);
+            const float mu = (mn == -INFINITY) ? 0.f : mn;
+            const float fa = exp2f(m - mu), fb = exp2f(ms[j] - mu);
+            l = l * fa + ls[j] * fb;
+            o = o * fa + os[j] * fb;
+            m = mn;
+        }
     }
     a.out[(size_t)r * a.H * HD + h * HD + d] = __float2bfloat16_rn(o / l);
 }
