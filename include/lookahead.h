@@ -58,7 +58,8 @@ extern "C" {
 typedef struct la_ctx la_ctx;
 
 /* Decoder description.  Weight pointers are DEVICE pointers of `dtype`
- * elements, borrowed (not copied) until la_destroy.
+ * elements, borrowed until la_destroy (the bf16 tensor-core path also packs
+ * a copy of the matrices at la_create, see there).
  *   emb        [vocab][d_model]
  *   layer_w    n_layers*9 pointers, per layer in this order:
  *              attn_norm [d_model], wq [H*hd][d_model], wk [Hkv*hd][d_model],
@@ -115,7 +116,11 @@ LA_API size_t la_workspace_bytes(const la_model_desc* desc, int W, int N, int G)
  * workspace: DEVICE buffer of ws_bytes >= la_workspace_bytes(), borrowed; or
  * NULL, and the library allocates (and frees) its own.  seed initialises the
  * lookahead window (splitmix64 stream).  flags: LA_PRESEED_PROMPT |
- * LA_DEBUG_LOGITS | LA_NO_GRAPH | LA_SIMT.  On success *out owns the context. */
+ * LA_DEBUG_LOGITS | LA_NO_GRAPH | LA_SIMT.  On success *out owns the context.
+ * On the bf16 tensor-core path la_create also makes, and the context owns, a
+ * tile-packed copy of every projection, MLP and LM-head matrix (their size
+ * again, in device memory outside the workspace); later changes to those
+ * caller buffers are not seen.  LA_ERR_CUDA if that allocation fails. */
 LA_API int la_create(const la_model_desc* desc, int W, int N, int G, void* workspace, size_t ws_bytes,
               uint64_t seed, int flags, la_ctx** out);
 

@@ -5,10 +5,19 @@
 // once and is bound by HBM bandwidth.  Layout ("swap AB"): the weight matrix
 // W [Nout][K] (row-major, K-major) is the 128-row A operand, the activations
 // X [128][K] the N = 128 B operand, and the fp32 accumulator D[feature][token]
-// lives in tensor memory.  Operands are staged by TMA (128-byte swizzle) into
-// a 3-deep shared-memory ring of 128-K stages (two 64-K swizzle atoms per
-// operand: fewer barrier round trips per byte); one thread issues tcgen05.mma, one thread
-// issues TMA, and four warps drain TMEM.
+// lives in tensor memory.  Operands are staged into a 3-deep shared-memory
+// ring of 128-K stages (two 64-K 128-byte-swizzle atoms per operand); one
+// thread issues tcgen05.mma, one thread issues the copies, and four warps
+// drain TMEM.
+//
+// Weight packing: at plan creation every weight matrix is copied once into
+// "units" of 128 rows x 128 K, each stored as the exact shared-memory image
+// the MMA reads (two 128-byte-swizzled 64-K atoms, zero padded past the
+// matrix edge), units ordered tile-major then k.  A stage's weights are then
+// one contiguous 32 KB bulk copy (cp.async.bulk) and a CTA's stream-K range
+// is one contiguous stretch of HBM, instead of 128 scattered 256-byte row
+// pieces per stage.  The activations stay row-major and come through a TMA
+// tensor map (they are L2-resident and re-read by every CTA).
 //
 // Work split (stream-K): the flattened (tile, k-block) space is cut into
 // equal contiguous ranges, one per CTA (one CTA per SM).  A CTA writes one
@@ -22,6 +31,8 @@
 #include <cudaTypedefs.h>
 
 #include <cstdio>
+#include <initializer_list>
+#include <utility>
 #include <vector>
 
 #include "gemm_tc.cuh"
@@ -52,13 +63,12 @@ constexpr int kTmemCols = 256;           // two 128-column fp32 accumulators
 constexpr int kSmemBytes = kStages * (kStageA + kStageB) + 1024 + 256;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // bounded waits: 2 s
 
-enum { MODE_ONE = 0, MODE_SEQ3 = 1 };
 enum { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3 };
 
 struct GemmArgs {
-    int tiles, KB, ctas, mode;
-    int t0, t1;      // MODE_SEQ3: tiles of map 0, map 1
+    int tiles, KB, ctas;
     int rows;        // tokens (columns) to store
+    const uint8_t* wpack;  // packed weight units [tiles][KB] x kStageA bytes
     float* partial;  // [ctas + tiles][rows][128]
     int* err;        // device status word
 };
@@ -110,6 +120,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
         if (*abort_flag) return false;
         if (globaltimer() - t0 > kWaitNs) return false;
     }
+}
+
+// Contiguous global -> shared bulk copy (16-byte aligned, size a multiple of
+// 16) completing on an mbarrier, with an L2 eviction-priority hint.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
 }
 
 // TMA 2D tile load with an L2 eviction-priority hint (policy from
@@ -204,8 +225,7 @@ __device__ __forceinline__ void raise_err(int* err, int code)
 }
 
 __global__ void __launch_bounds__(kThreads, LA_GEMM_CTAS_PER_SM)
-    k_gemm_tc(const __grid_constant__ CUtensorMap a0, const __grid_constant__ CUtensorMap a1,
-              const __grid_constant__ CUtensorMap a2, const __grid_constant__ CUtensorMap bmap, GemmArgs g)
+    k_gemm_tc(const __grid_constant__ CUtensorMap bmap, GemmArgs g)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -256,24 +276,7 @@ __global__ void __launch_bounds__(kThreads, LA_GEMM_CTAS_PER_SM)
             bool ok = true;
             const uint64_t pw = policy_evict_first(), pa = policy_evict_last();
             auto load_a = [&](long long idx, int st) {
-                const int t = (int)(idx / g.KB);
-                const CUtensorMap* m = &a0;
-                int row = t * kBM;
-                if (g.mode == MODE_SEQ3) {
-                    if (t < g.t0) {
-                        m = &a0;
-                    } else if (t < g.t0 + g.t1) {
-                        m = &a1;
-                        row = (t - g.t0) * kBM;
-                    } else {
-                        m = &a2;
-                        row = (t - g.t0 - g.t1) * kBM;
-                    }
-                }
-#pragma unroll
-                for (int a = 0; a < kAtoms; a++)
-                    tma_load(m, &full[st], sA + st * kStageA + a * (kBM * kAtom * 2),
-                             (int)(idx % g.KB) * kBK + a * kAtom, row, pw);
+                bulk_load(sA + st * kStageA, g.wpack + (size_t)idx * kStageA, kStageA, &full[st], pw);
             };
             auto load_b = [&](long long idx, int st) {
 #pragma unroll
@@ -409,6 +412,45 @@ __global__ void __launch_bounds__(kThreads, LA_GEMM_CTAS_PER_SM)
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    }
+}
+
+// Pack one weight matrix W [rows][K] (bf16, row-major) into units of the
+// GEMM's ring: unit (t, kb) holds rows t*128.. and K columns kb*128.. as
+// kAtoms 16 KB atoms; in an atom, 16-byte chunk c of row r (8 elements) sits
+// at r*128 + ((c ^ (r & 7)) * 16), the 128-byte swizzle of the MMA operand
+// descriptor.  Elements past the matrix edge are zero.  One thread per chunk.
+__global__ void k_pack_sw128(const __nv_bfloat16* __restrict__ w, int rows, int K, int KB, int ntiles,
+                             uint4* __restrict__ dst)
+{
+    const long long n = (long long)ntiles * KB * kAtoms * kBM * 8;
+    const bool vec = (K % 8) == 0 && ((uintptr_t)w & 15) == 0;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int p = (int)(i & 7), r = (int)((i >> 3) & (kBM - 1));
+        const long long atom = i >> 10;  // 8 chunks x 128 rows per atom
+        const int a = (int)(atom % kAtoms);
+        const long long unit = atom / kAtoms;
+        const int kb = (int)(unit % KB), t = (int)(unit / KB);
+        const int c = p ^ (r & 7);
+        const int R = t * kBM + r, C = kb * kBK + a * kAtom + c * 8;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (R < rows) {
+            const __nv_bfloat16* src = w + (size_t)R * K + C;
+            if (vec && C + 8 <= K) {
+                v = *(const uint4*)src;
+            } else {
+                uint32_t u[4];
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    const uint32_t lo = C + 2 * j < K ? __bfloat16_as_ushort(src[2 * j]) : 0u;
+                    const uint32_t hi = C + 2 * j + 1 < K ? __bfloat16_as_ushort(src[2 * j + 1]) : 0u;
+                    u[j] = lo | (hi << 16);
+                }
+                v = make_uint4(u[0], u[1], u[2], u[3]);
+            }
+        }
+        dst[i] = v;
     }
 }
 
@@ -688,9 +730,9 @@ __global__ void __launch_bounds__(kRnThreads) k_resid_rmsnorm(ResidArgs a, float
 // ------------------------------------------------------------------ plan ---
 
 struct GemmCfg {
-    CUtensorMap a[3];
     CUtensorMap b;
-    int tiles, KB, ctas, mode, t0, t1, Nout;
+    int tiles, KB, ctas, Nout;
+    size_t unit0;  // first packed unit of this GEMM
 };
 
 struct Impl {
@@ -700,6 +742,8 @@ struct Impl {
     GemmCfg lm;
     float* partial = nullptr;
     size_t partial_bytes = 0;
+    uint8_t* wpack = nullptr;  // packed weight units of every GEMM
+    size_t wpack_bytes = 0;
     int* err = nullptr;  // the context's device status word
     void* Q = nullptr;
     void* HID = nullptr;
@@ -747,9 +791,9 @@ size_t partial_need(const GemmCfg& g) { return (size_t)(g.ctas + g.tiles) * kRow
 void launch_gemm(const TcPlan& p, const GemmCfg& g, cudaStream_t s, int rows, int cls)
 {
     const Impl& im = *(const Impl*)p.impl;
-    GemmArgs a{g.tiles, g.KB, g.ctas, g.mode, g.t0, g.t1, rows, im.partial, im.err};
+    GemmArgs a{g.tiles, g.KB, g.ctas, rows, im.wpack + g.unit0 * kStageA, im.partial, im.err};
     if (p.prof) p.prof->begin(s);
-    launch_pdl(k_gemm_tc, dim3(g.ctas), dim3(kThreads), kSmemBytes, s, g.a[0], g.a[1], g.a[2], g.b, a);
+    launch_pdl(k_gemm_tc, dim3(g.ctas), dim3(kThreads), kSmemBytes, s, g.b, a);
     if (p.prof) {
         // algorithmic: every weight once, the rows' inputs once, the rows' outputs once
         const double K = (double)g.KB * kBK, Nw = (double)g.tiles * kBM;
@@ -813,46 +857,39 @@ int tc_plan_create(TcPlan* p, const la_model_desc& d, const void* const* lw, voi
     ok &= make_map(&bXN, XN, kRows, d.d_model, kBN);
     ok &= make_map(&bATT, ATT, kRows, dq, kBN);
     ok &= make_map(&bHID, HID, kRows, d.ffn, kBN);
+    // Packing jobs: (source matrix, its rows, K, first packed unit).
+    struct PackJob {
+        const void* w;
+        int rows, K, KB, tiles;
+        size_t unit0;
+    };
+    std::vector<PackJob> jobs;
+    size_t units = 0;
+    // A GEMM over the row-concatenation of up to three matrices [rows_i][K];
+    // each matrix starts on a fresh 128-row tile.
+    auto add_gemm = [&](GemmCfg& g, const CUtensorMap& b, int K, std::initializer_list<std::pair<const void*, int>> mats,
+                        int Nout) {
+        g.b = b;
+        g.tiles = 0;
+        g.Nout = Nout;
+        g.KB = (K + kBK - 1) / kBK;
+        g.unit0 = units;
+        for (const auto& m : mats) {
+            const int t = (m.second + kBM - 1) / kBM;
+            jobs.push_back(PackJob{m.first, m.second, K, g.KB, t, units});
+            units += (size_t)t * g.KB;
+            g.tiles += t;
+        }
+        finish_cfg(g, K, sms);
+    };
     size_t need = 0;
     for (int l = 0; l < d.n_layers && ok; l++) {
         const void* const* w = lw + (size_t)l * 9;
-        GemmCfg q{};
-        ok &= make_map(&q.a[0], w[1], dq, d.d_model, kBM);
-        ok &= make_map(&q.a[1], w[2], dkv, d.d_model, kBM);
-        ok &= make_map(&q.a[2], w[3], dkv, d.d_model, kBM);
-        q.b = bXN;
-        q.mode = MODE_SEQ3;
-        q.t0 = dq / kBM;
-        q.t1 = dkv / kBM;
-        q.tiles = q.t0 + 2 * q.t1;
-        q.Nout = dq + 2 * dkv;
-        finish_cfg(q, d.d_model, sms);
-        GemmCfg o{};
-        ok &= make_map(&o.a[0], w[4], d.d_model, dq, kBM);
-        o.a[1] = o.a[2] = o.a[0];
-        o.b = bATT;
-        o.mode = MODE_ONE;
-        o.tiles = (d.d_model + kBM - 1) / kBM;
-        o.Nout = d.d_model;
-        finish_cfg(o, dq, sms);
-        GemmCfg gu{};  // gate tiles, then up tiles (128 rows each)
-        ok &= make_map(&gu.a[0], w[6], d.ffn, d.d_model, kBM);
-        ok &= make_map(&gu.a[1], w[7], d.ffn, d.d_model, kBM);
-        gu.a[2] = gu.a[0];
-        gu.b = bXN;
-        gu.mode = MODE_SEQ3;
-        gu.t0 = gu.t1 = (d.ffn + kBM - 1) / kBM;
-        gu.tiles = 2 * gu.t0;
-        gu.Nout = d.ffn;
-        finish_cfg(gu, d.d_model, sms);
-        GemmCfg dn{};
-        ok &= make_map(&dn.a[0], w[8], d.d_model, d.ffn, kBM);
-        dn.a[1] = dn.a[2] = dn.a[0];
-        dn.b = bHID;
-        dn.mode = MODE_ONE;
-        dn.tiles = (d.d_model + kBM - 1) / kBM;
-        dn.Nout = d.d_model;
-        finish_cfg(dn, d.ffn, sms);
+        GemmCfg q{}, o{}, gu{}, dn{};
+        add_gemm(q, bXN, d.d_model, {{w[1], dq}, {w[2], dkv}, {w[3], dkv}}, dq + 2 * dkv);
+        add_gemm(o, bATT, dq, {{w[4], d.d_model}}, d.d_model);
+        add_gemm(gu, bXN, d.d_model, {{w[6], d.ffn}, {w[7], d.ffn}}, d.ffn);  // gate tiles, then up tiles
+        add_gemm(dn, bHID, d.ffn, {{w[8], d.d_model}}, d.d_model);
         for (const GemmCfg* g : {&q, &o, &gu, &dn}) need = partial_need(*g) > need ? partial_need(*g) : need;
         im->qkv.push_back(q);
         im->oproj.push_back(o);
@@ -860,25 +897,31 @@ int tc_plan_create(TcPlan* p, const la_model_desc& d, const void* const* lw, voi
         im->down.push_back(dn);
     }
     if (ok) {
-        GemmCfg& lm = im->lm;
-        lm = GemmCfg{};
-        ok &= make_map(&lm.a[0], d.lm_head, d.vocab, d.d_model, kBM);
-        lm.a[1] = lm.a[2] = lm.a[0];
-        lm.b = bXN;
-        lm.mode = MODE_ONE;
-        lm.tiles = (d.vocab + kBM - 1) / kBM;
-        lm.Nout = d.vocab;
-        finish_cfg(lm, d.d_model, sms);
-        need = partial_need(lm) > need ? partial_need(lm) : need;
+        add_gemm(im->lm, bXN, d.d_model, {{d.lm_head, d.vocab}}, d.vocab);
+        need = partial_need(im->lm) > need ? partial_need(im->lm) : need;
     }
     if (!ok) {
         delete im;
         return 1;
     }
     im->err = status;
+    im->wpack_bytes = units * kStageA;
     if (cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess ||
-        cudaMalloc((void**)&im->partial, need) != cudaSuccess) {
+        cudaMalloc((void**)&im->partial, need) != cudaSuccess ||
+        cudaMalloc((void**)&im->wpack, im->wpack_bytes) != cudaSuccess) {
         if (im->partial) cudaFree(im->partial);
+        delete im;
+        return -1;
+    }
+    for (const PackJob& j : jobs) {
+        const long long chunks = (long long)j.tiles * j.KB * kStageA / 16;
+        const long long blocks = (chunks + 255) / 256;
+        k_pack_sw128<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256>>>(
+            (const __nv_bfloat16*)j.w, j.rows, j.K, j.KB, j.tiles, (uint4*)(im->wpack + j.unit0 * kStageA));
+    }
+    if (cudaGetLastError() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+        cudaFree(im->partial);
+        cudaFree(im->wpack);
         delete im;
         return -1;
     }
@@ -893,6 +936,7 @@ void tc_plan_destroy(TcPlan* p)
     if (p->impl) {
         Impl* im = (Impl*)p->impl;
         if (im->partial) cudaFree(im->partial);
+        if (im->wpack) cudaFree(im->wpack);
         delete im;
     }
     p->impl = nullptr;
