@@ -23,6 +23,8 @@
 // The split that holds the first tail chunk is run by kRep CTAs: each
 // repeats the split's shared chunks and then takes a share of the row
 // groups, so the per-group work is spread over more SMs.
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace la {
@@ -196,7 +198,7 @@ struct AttnArgs {
 
 template <int HD>
 struct AttnSmem {
-    static constexpr int RB = HD * 2, PS = 2 + HD;
+    static constexpr int RB = HD * 2, PS = HD + 4;  // state: o[HD], m, l, 2 pad
     static constexpr int kQ = 0;                                  // Q tile [kRows][HD]
     static constexpr int kK0 = kQ + kRows * RB;                   // K chunk buffer 0
     static constexpr int kV0 = kK0 + kChunk * RB;                 // V chunk buffer 0
@@ -305,15 +307,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
             const int r = warp * 16 + g + 8 * hh;
             if (r < a.rows) {
                 float* pr = dst + (size_t)r * PS;
-                if (t == 0) {
-                    pr[0] = st.m[hh];
-                    pr[1] = st.l[hh];
-                }
+                if (t == 0) *(float2*)(pr + HD) = make_float2(st.m[hh], st.l[hh]);
 #pragma unroll
-                for (int d = 0; d < HD / 8; d++) {
-                    pr[2 + d * 8 + 2 * t] = st.o[d][2 * hh];
-                    pr[2 + d * 8 + 2 * t + 1] = st.o[d][2 * hh + 1];
-                }
+                for (int d = 0; d < HD / 8; d++)
+                    *(float2*)(pr + d * 8 + 2 * t) = make_float2(st.o[d][2 * hh], st.o[d][2 * hh + 1]);
             }
         }
     }
@@ -377,12 +374,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
                 const int r = hh ? rB : rA;
                 if (r >= 0) {
                     const float* pr = dump + (size_t)r * PS;
-                    ts.m[hh] = pr[0];
-                    ts.l[hh] = pr[1];
+                    ts.m[hh] = pr[HD];
+                    ts.l[hh] = pr[HD + 1];
 #pragma unroll
                     for (int d = 0; d < HD / 8; d++) {
-                        ts.o[d][2 * hh] = pr[2 + d * 8 + 2 * t];
-                        ts.o[d][2 * hh + 1] = pr[2 + d * 8 + 2 * t + 1];
+                        const float2 v = *(const float2*)(pr + d * 8 + 2 * t);
+                        ts.o[d][2 * hh] = v.x;
+                        ts.o[d][2 * hh + 1] = v.y;
                     }
                 } else {
                     ts.m[hh] = -INFINITY;
@@ -434,62 +432,70 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
                 const int r = hh ? rB : rA;
                 if (r >= 0) {
                     float* pr = part + (size_t)r * PS;
-                    if (t == 0) {
-                        pr[0] = ts.m[hh];
-                        pr[1] = ts.l[hh];
-                    }
+                    if (t == 0) *(float2*)(pr + HD) = make_float2(ts.m[hh], ts.l[hh]);
 #pragma unroll
-                    for (int d = 0; d < HD / 8; d++) {
-                        pr[2 + d * 8 + 2 * t] = ts.o[d][2 * hh];
-                        pr[2 + d * 8 + 2 * t + 1] = ts.o[d][2 * hh + 1];
-                    }
+                    for (int d = 0; d < HD / 8; d++)
+                        *(float2*)(pr + d * 8 + 2 * t) = make_float2(ts.o[d][2 * hh], ts.o[d][2 * hh + 1]);
                 }
             }
         }
     }
 }
 
-// Merge the splits of every (row, head) in ascending split order (the loads
-// of up to 8 splits are issued together, the merge runs in order).
+// Merge the splits of every (row, head) in ascending split order.  One warp
+// per (row, head), each lane HD/32 consecutive output dims; the loads of up
+// to 8 splits are issued together, the merge runs in split order.
+constexpr int kCombWarps = 8;
+
 template <int HD>
-__global__ void k_attn_combine(AttnArgs a)
+__global__ void __launch_bounds__(kCombWarps * 32) k_attn_combine(AttnArgs a)
 {
     pdl_wait();
     pdl_trigger();
-    const int r = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
-    constexpr int PS = 2 + HD, kB = 8;
+    constexpr int PS = HD + 4, V = HD / 32, kB = 8;
+    using VecT = typename std::conditional<V == 4, float4, float2>::type;
+    const int w = blockIdx.x * kCombWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (w >= a.rows * a.H) return;
+    const int r = w / a.H, h = w % a.H;
     const int ns = a.pos[r] / kSplit + 1;
     const float* base = a.part + (size_t)h * a.nsplit * kRows * PS + (size_t)r * PS;
     const size_t stride = (size_t)kRows * PS;
-    float m = -INFINITY, l = 0.f, o = 0.f;
+    float m = -INFINITY, l = 0.f, o[V];
+#pragma unroll
+    for (int k = 0; k < V; k++) o[k] = 0.f;
     for (int s0 = 0; s0 < ns; s0 += kB) {
-        float ms[kB], ls[kB], os[kB];
+        float2 ml[kB];
+        VecT ov[kB];
 #pragma unroll
         for (int j = 0; j < kB; j++) {
             const bool ok = s0 + j < ns;
-            const float* pr = base + (size_t)(s0 + j) * stride;
-            ms[j] = ok ? pr[0] : -INFINITY;
-            ls[j] = ok ? pr[1] : 0.f;
-            os[j] = ok ? pr[2 + d] : 0.f;
+            const float* pr = base + (size_t)(ok ? s0 + j : 0) * stride;
+            ml[j] = ok ? *(const float2*)(pr + HD) : make_float2(-INFINITY, 0.f);
+            ov[j] = *(const VecT*)(pr + lane * V);
         }
 #pragma unroll
         for (int j = 0; j < kB; j++) {
             if (s0 + j >= ns) break;
+            const float* os = (const float*)&ov[j];
             if (s0 + j == 0) {
-                m = ms[j];
-                l = ls[j];
-                o = os[j];
+                m = ml[j].x;
+                l = ml[j].y;
+#pragma unroll
+                for (int k = 0; k < V; k++) o[k] = os[k];
                 continue;
             }
-            const float mn = fmaxf(m, ms[j]);
+            const float mn = fmaxf(m, ml[j].x);
             const float mu = (mn == -INFINITY) ? 0.f : mn;
-            const float fa = exp2f(m - mu), fb = exp2f(ms[j] - mu);
-            l = l * fa + ls[j] * fb;
-            o = o * fa + os[j] * fb;
+            const float fa = exp2f(m - mu), fb = exp2f(ml[j].x - mu);
+            l = l * fa + ml[j].y * fb;
+#pragma unroll
+            for (int k = 0; k < V; k++) o[k] = o[k] * fa + os[k] * fb;
             m = mn;
         }
     }
-    a.out[(size_t)r * a.H * HD + h * HD + d] = __float2bfloat16_rn(o / l);
+    __nv_bfloat16* dst = a.out + (size_t)r * a.H * HD + h * HD + lane * V;
+#pragma unroll
+    for (int k = 0; k < V; k += 2) *(__nv_bfloat162*)(dst + k) = __floats2bfloat162_rn(o[k] / l, o[k + 1] / l);
 }
 
 }  // namespace
@@ -497,7 +503,7 @@ __global__ void k_attn_combine(AttnArgs a)
 size_t attn_mma_partial_bytes(int H, int hd, int max_seq)
 {
     const int nsplit = (max_seq + kSplit - 1) / kSplit;
-    return (size_t)H * nsplit * kRows * (2 + hd) * 4;
+    return (size_t)H * nsplit * kRows * (hd + 4) * 4;
 }
 
 bool attn_mma_init(int hd)
@@ -536,10 +542,10 @@ void launch_attn_mma(cudaStream_t s, const DState* st, RowSet rs, int max_rel, c
     dim3 grid(H, a.nsplit + kRep - 1);
     if (hd == 128) {
         launch_pdl(k_attn_mma<128>, grid, dim3(kWarps * 32), AttnSmem<128>::kBytes, s, a);
-        launch_pdl(k_attn_combine<128>, dim3(rows, H), dim3(128), 0, s, a);
+        launch_pdl(k_attn_combine<128>, dim3((rows * H + kCombWarps - 1) / kCombWarps), dim3(kCombWarps * 32), 0, s, a);
     } else {
         launch_pdl(k_attn_mma<64>, grid, dim3(kWarps * 32), AttnSmem<64>::kBytes, s, a);
-        launch_pdl(k_attn_combine<64>, dim3(rows, H), dim3(64), 0, s, a);
+        launch_pdl(k_attn_combine<64>, dim3((rows * H + kCombWarps - 1) / kCombWarps), dim3(kCombWarps * 32), 0, s, a);
     }
 }
 

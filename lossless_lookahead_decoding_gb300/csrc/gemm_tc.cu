@@ -63,7 +63,7 @@ constexpr int kTmemCols = 256;           // two 128-column fp32 accumulators
 constexpr int kSmemBytes = kStages * (kStageA + kStageB) + 1024 + 256;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // bounded waits: 2 s
 
-enum { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3 };
+enum { EPI_LOGITS = 3 };
 
 struct GemmArgs {
     int tiles, KB, ctas;
@@ -465,8 +465,6 @@ struct EpiArgs {
     const float* __restrict__ cosb;
     const float* __restrict__ sinb;
     __nv_bfloat16 *__restrict__ Q, *__restrict__ KS, *__restrict__ VS;
-    // residual
-    float* __restrict__ X;
     // SwiGLU
     __nv_bfloat16* __restrict__ H;
     // logits / argmax
@@ -498,7 +496,6 @@ __global__ void __launch_bounds__(128) k_gemm_epi(EpiArgs e)
     pdl_trigger();
     const int t = blockIdx.x, f = threadIdx.x;
     const long long total = (long long)e.tiles * e.KB;
-    __shared__ float sx[kEpiRows][kBM];
     __shared__ float sbv[kEpiRows][4];
     __shared__ int sbi[kEpiRows][4];
     const int r0 = blockIdx.y * kEpiRows;
@@ -521,66 +518,7 @@ __global__ void __launch_bounds__(128) k_gemm_epi(EpiArgs e)
     };
     float acc[kEpiRows];
     sum_tile(t, acc);
-    if (EPI == EPI_RESID) {
-        const int fg = t * kBM + f;
-        if (fg < e.Nout) {
-            float x[kEpiRows];
-#pragma unroll
-            for (int i = 0; i < kEpiRows; i++)
-                x[i] = (r0 + i < e.rows) ? e.X[(size_t)(r0 + i) * e.Nout + fg] : 0.f;
-#pragma unroll
-            for (int i = 0; i < kEpiRows; i++)
-                if (r0 + i < e.rows) e.X[(size_t)(r0 + i) * e.Nout + fg] = x[i] + acc[i];
-        }
-        return;
-    }
-    if (EPI == EPI_QKV) {
-#pragma unroll
-        for (int i = 0; i < kEpiRows; i++) sx[i][f] = acc[i];
-        __syncthreads();
-    }
-    if (EPI == EPI_QKV) {
-        const int fg = t * kBM + f, half = e.hd >> 1;
-        if (fg < e.dq + e.dkv) {
-            const int region = fg < e.dq ? 0 : 1;
-            const int fl = region == 0 ? fg : fg - e.dq;
-            const int i0 = fl % e.hd, ip = i0 % half;
-            float cs[kEpiRows], sn[kEpiRows];
-#pragma unroll
-            for (int i = 0; i < kEpiRows; i++) {
-                const int p = e.pos[min(r0 + i, e.rows - 1)];
-                cs[i] = e.cosb[(size_t)p * half + ip];
-                sn[i] = e.sinb[(size_t)p * half + ip];
-            }
-#pragma unroll
-            for (int i = 0; i < kEpiRows; i++) {
-                const int r = r0 + i;
-                if (r < e.rows) {
-                    const float other = sx[i][f ^ half];
-                    const float y = (i0 < half) ? acc[i] * cs[i] - other * sn[i] : acc[i] * cs[i] + other * sn[i];
-                    if (region == 0) e.Q[(size_t)r * e.dq + fl] = __float2bfloat16_rn(y);
-                    else e.KS[(size_t)r * e.dkv + fl] = __float2bfloat16_rn(y);
-                }
-            }
-        } else if (fg < e.dq + 2 * e.dkv) {
-            for (int i = 0; i < kEpiRows; i++)
-                if (r0 + i < e.rows) e.VS[(size_t)(r0 + i) * e.dkv + (fg - e.dq - e.dkv)] = __float2bfloat16_rn(acc[i]);
-        }
-    } else if (EPI == EPI_SWIGLU) {
-        // gate tiles come first, then the up tiles of the same features
-        float up[kEpiRows];
-        sum_tile(t + e.tiles / 2, up);
-        const int fo = t * kBM + f;
-        if (fo < e.Nout) {
-#pragma unroll
-            for (int i = 0; i < kEpiRows; i++) {
-                if (r0 + i < e.rows) {
-                    const float gt = acc[i];
-                    e.H[(size_t)(r0 + i) * e.Nout + fo] = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up[i]);
-                }
-            }
-        }
-    } else if (EPI == EPI_LOGITS) {
+    if (EPI == EPI_LOGITS) {
         const int fg = t * kBM + f;
         const bool valid = fg < e.Nout;
 #pragma unroll
@@ -617,6 +555,119 @@ __global__ void __launch_bounds__(128) k_gemm_epi(EpiArgs e)
                 const uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
                 const unsigned long long packed = ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)bi);
                 atomicMax(&e.amaxp[r0 + f], packed);
+            }
+        }
+    }
+}
+
+// Sum of stream-K partials for J (tile, feature) columns and R rows from
+// r0: acc[j][i] = partials of tile tt[j], feature column f[j], row r0 + i,
+// added in ascending k order; the loads of up to kSumBatch partials of all
+// columns are in flight together.
+constexpr int kSumBatch = 3;
+
+template <int J, int R>
+__device__ __forceinline__ void sum_partials(const EpiArgs& e, const int* tt, const int* f, int r0, float (*acc)[R])
+{
+    const long long total = (long long)e.tiles * e.KB;
+    int lo[J], cnt[J], n = 0;
+#pragma unroll
+    for (int j = 0; j < J; j++) {
+        lo[j] = owner_cta((long long)tt[j] * e.KB, total, e.ctas);
+        cnt[j] = owner_cta((long long)tt[j] * e.KB + e.KB - 1, total, e.ctas) - lo[j] + 1;
+        n = max(n, cnt[j]);
+    }
+    for (int q0 = 0; q0 < n; q0 += kSumBatch) {
+        float v[kSumBatch][J][R];
+#pragma unroll
+        for (int q = 0; q < kSumBatch; q++)
+#pragma unroll
+            for (int j = 0; j < J; j++)
+#pragma unroll
+                for (int i = 0; i < R; i++) {
+                    const bool ok = q0 + q < cnt[j] && r0 + i < e.rows;
+                    v[q][j][i] = ok ? e.partial[((size_t)(lo[j] + q0 + q + tt[j]) * e.rows + r0 + i) * kBM + f[j]] : 0.f;
+                }
+#pragma unroll
+        for (int q = 0; q < kSumBatch; q++)
+#pragma unroll
+            for (int j = 0; j < J; j++)
+                if (q0 + q < cnt[j]) {
+#pragma unroll
+                    for (int i = 0; i < R; i++) acc[j][i] = (q0 + q == 0) ? v[q][j][i] : acc[j][i] + v[q][j][i];
+                }
+    }
+}
+
+constexpr int kQkvRows = 16;  // rows per CTA of the QKV epilogue (8 per thread)
+
+// QKV epilogue: Q, K (rotate-half RoPE at each row's position) and V of the
+// step rows, bf16.  Thread = (RoPE pair (fa, fa + hd/2) of the tile, 8 rows);
+// the RoPE table entries do not depend on the GEMM and are fetched before
+// waiting for it.
+__global__ void __launch_bounds__(128) k_epi_qkv(EpiArgs e)
+{
+    constexpr int R = kQkvRows / 2;
+    const int t = blockIdx.x, pr = threadIdx.x & 63;
+    const int r0 = blockIdx.y * kQkvRows + (threadIdx.x >> 6) * R;
+    const int half = e.hd >> 1;
+    const int fa = (pr / half) * e.hd + pr % half, fb = fa + half;
+    const int ga = t * kBM + fa;
+    const bool rope = ga < e.dq + e.dkv;
+    float cs[R], sn[R];
+#pragma unroll
+    for (int i = 0; i < R; i++) {
+        const int p = rope ? __ldcg(e.pos + min(r0 + i, e.rows - 1)) : 0;
+        cs[i] = rope ? e.cosb[(size_t)p * half + pr % half] : 0.f;
+        sn[i] = rope ? e.sinb[(size_t)p * half + pr % half] : 0.f;
+    }
+    pdl_wait();
+    pdl_trigger();
+    const int tt[2] = {t, t}, ff[2] = {fa, fb};
+    float x[2][R];
+    sum_partials<2, R>(e, tt, ff, r0, x);
+    if (rope) {
+        const bool isq = ga < e.dq;
+        __nv_bfloat16* dst = isq ? e.Q : e.KS;
+        const int ld = isq ? e.dq : e.dkv, fl = isq ? ga : ga - e.dq;
+#pragma unroll
+        for (int i = 0; i < R; i++) {
+            if (r0 + i < e.rows) {
+                dst[(size_t)(r0 + i) * ld + fl] = __float2bfloat16_rn(x[0][i] * cs[i] - x[1][i] * sn[i]);
+                dst[(size_t)(r0 + i) * ld + fl + half] = __float2bfloat16_rn(x[1][i] * cs[i] + x[0][i] * sn[i]);
+            }
+        }
+    } else if (ga < e.dq + 2 * e.dkv) {
+        const int fl = ga - e.dq - e.dkv;
+#pragma unroll
+        for (int i = 0; i < R; i++) {
+            if (r0 + i < e.rows) {
+                e.VS[(size_t)(r0 + i) * e.dkv + fl] = __float2bfloat16_rn(x[0][i]);
+                e.VS[(size_t)(r0 + i) * e.dkv + fl + half] = __float2bfloat16_rn(x[1][i]);
+            }
+        }
+    }
+}
+
+constexpr int kGluRows = 8;  // rows per CTA of the SwiGLU epilogue
+
+// SwiGLU epilogue: gate tiles come first, then the up tiles of the same
+// features; H = silu(gate) * up in bf16.  Thread = (feature, 8 rows).
+__global__ void __launch_bounds__(128) k_epi_swiglu(EpiArgs e)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int t = blockIdx.x, f = threadIdx.x, r0 = blockIdx.y * kGluRows;
+    const int tt[2] = {t, t + e.tiles / 2}, ff[2] = {f, f};
+    float x[2][kGluRows];
+    sum_partials<2, kGluRows>(e, tt, ff, r0, x);
+    const int fo = t * kBM + f;
+    if (fo < e.Nout) {
+#pragma unroll
+        for (int i = 0; i < kGluRows; i++) {
+            if (r0 + i < e.rows) {
+                const float gt = x[0][i];
+                e.H[(size_t)(r0 + i) * e.Nout + fo] = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * x[1][i]);
             }
         }
     }
@@ -833,7 +884,7 @@ int tc_plan_create(TcPlan* p, const la_model_desc& d, const void* const* lw, voi
     p->impl = nullptr;
     if (esz != 2) return 1;
     const int dq = d.n_heads * d.head_dim, dkv = d.n_kv_heads * d.head_dim;
-    if (dq % kBM || dkv % kBM || d.d_model % kAtom) return 1;
+    if (dq % kBM || dkv % kBM || d.d_model % kAtom || kBM % d.head_dim || d.head_dim % 2) return 1;
     if (!get_encode()) return 1;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
@@ -961,14 +1012,9 @@ void tc_qkv_rope(const TcPlan& p, cudaStream_t s, int layer, int rows, const int
     e.Q = (__nv_bfloat16*)Q;
     e.KS = (__nv_bfloat16*)KS;
     e.VS = (__nv_bfloat16*)VS;
-    launch_epi(p, s, [&] { launch_pdl(k_gemm_epi<EPI_QKV>, epi_grid(g, rows), dim3(128), 0, s, e); });
-}
-
-bool tc_attn_supported(const TcPlan&) { return false; }
-
-void tc_attention(const TcPlan&, cudaStream_t, const DState*, const RowSet&, const int*, const void*, const void*,
-                  const void*, const void*, const void*, void*, int)
-{
+    launch_epi(p, s, [&] {
+        launch_pdl(k_epi_qkv, dim3(g.tiles, (rows + kQkvRows - 1) / kQkvRows), dim3(128), 0, s, e);
+    });
 }
 
 TcResid tc_oproj(const TcPlan& p, cudaStream_t s, int layer, int rows)
@@ -997,16 +1043,6 @@ void tc_resid_rmsnorm(const TcPlan& p, cudaStream_t s, const TcResid& pend, floa
     if (p.prof) p.prof->end(s, P_NORM, 0, 0);
 }
 
-void tc_oproj_resid(const TcPlan& p, cudaStream_t s, int layer, int rows, float* X)
-{
-    const Impl& im = *(const Impl*)p.impl;
-    const GemmCfg& g = im.oproj[layer];
-    launch_gemm(p, g, s, rows, P_GEMM_O);
-    EpiArgs e = epi_base(im, g, rows);
-    e.X = X;
-    launch_epi(p, s, [&] { launch_pdl(k_gemm_epi<EPI_RESID>, epi_grid(g, rows), dim3(128), 0, s, e); });
-}
-
 void tc_gateup_swiglu(const TcPlan& p, cudaStream_t s, int layer, int rows)
 {
     const Impl& im = *(const Impl*)p.impl;
@@ -1015,18 +1051,8 @@ void tc_gateup_swiglu(const TcPlan& p, cudaStream_t s, int layer, int rows)
     EpiArgs e = epi_base(im, g, rows);
     e.H = (__nv_bfloat16*)im.HID;
     launch_epi(p, s, [&] {
-        launch_pdl(k_gemm_epi<EPI_SWIGLU>, dim3(g.tiles / 2, (rows + kEpiRows - 1) / kEpiRows), dim3(128), 0, s, e);
+        launch_pdl(k_epi_swiglu, dim3(g.tiles / 2, (rows + kGluRows - 1) / kGluRows), dim3(128), 0, s, e);
     });
-}
-
-void tc_down_resid(const TcPlan& p, cudaStream_t s, int layer, int rows, float* X)
-{
-    const Impl& im = *(const Impl*)p.impl;
-    const GemmCfg& g = im.down[layer];
-    launch_gemm(p, g, s, rows, P_GEMM_DOWN);
-    EpiArgs e = epi_base(im, g, rows);
-    e.X = X;
-    launch_epi(p, s, [&] { launch_pdl(k_gemm_epi<EPI_RESID>, epi_grid(g, rows), dim3(128), 0, s, e); });
 }
 
 void tc_lmhead_argmax(const TcPlan& p, cudaStream_t s, int rows, float* logits, unsigned long long* amaxp, int* amax)

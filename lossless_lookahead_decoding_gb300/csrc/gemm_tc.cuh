@@ -22,11 +22,6 @@ int tc_plan_create(TcPlan* p, const la_model_desc& d, const void* const* lw, voi
 void tc_plan_destroy(TcPlan* p);
 void tc_qkv_rope(const TcPlan& p, cudaStream_t s, int layer, int rows, const int* pos, const float* cosb,
                  const float* sinb, void* Q, void* KS, void* VS);
-bool tc_attn_supported(const TcPlan& p);
-void tc_attention(const TcPlan& p, cudaStream_t s, const DState* st, const RowSet& rs, const int* pos, const void* Q,
-                  const void* KC, const void* VC, const void* KS, const void* VS, void* out, int rows);
-void tc_oproj_resid(const TcPlan& p, cudaStream_t s, int layer, int rows, float* X);
-
 // O-proj / down GEMMs whose residual add is left pending, to be folded into
 // the RMSNorm that follows (tc_resid_rmsnorm): X += partial sums, XN = norm(X).
 struct TcResid {
@@ -38,7 +33,6 @@ TcResid tc_down(const TcPlan& p, cudaStream_t s, int layer, int rows);
 void tc_resid_rmsnorm(const TcPlan& p, cudaStream_t s, const TcResid& pend, float* X, const void* w, void* XN, int d,
                       float eps);
 void tc_gateup_swiglu(const TcPlan& p, cudaStream_t s, int layer, int rows);
-void tc_down_resid(const TcPlan& p, cudaStream_t s, int layer, int rows, float* X);
 void tc_lmhead_argmax(const TcPlan& p, cudaStream_t s, int rows, float* logits, unsigned long long* amaxp, int* amax);
 
 }  // namespace la
