@@ -6,7 +6,7 @@
 // mask of the lookahead step; a prefill block is one causal group).
 //
 // Keys are walked in chunks of 64 ABSOLUTE positions; chunks are grouped into
-// fixed splits of 128 positions whose partial softmax states (max, sum,
+// fixed splits of 256 positions (one CTA each) whose partial softmax states (max, sum,
 // unnormalised output) are merged in ascending split order by a second
 // kernel.  Inside a chunk, S = Q K^T and O += P V run on bf16 mma.sync tiles
 // with fp32 accumulation.  A chunk that lies entirely below P is shared by
@@ -32,9 +32,15 @@ namespace la {
 namespace {
 
 constexpr int kChunk = 64;
-constexpr int kSplit = 128;
+#ifndef LA_ATTN_SPLIT
+#define LA_ATTN_SPLIT 256
+#endif
+#ifndef LA_ATTN_REP
+#define LA_ATTN_REP 2
+#endif
+constexpr int kSplit = LA_ATTN_SPLIT;
 constexpr int kWarps = 8;
-constexpr int kRep = 4;
+constexpr int kRep = LA_ATTN_REP;
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
