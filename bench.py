@@ -61,7 +61,23 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="use only the first L decoder layers (small cases for profiler captures)")
+    ap.add_argument("--wng", default="",
+                    help="W,N,G to use instead of the workload's lookahead settings")
+    ap.add_argument("--preseed", default="auto", choices=["auto", "on", "off"],
+                    help="seed the n-gram pool with the prompt's n-grams (auto: the workload's setting)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the benchmark line: one JSON line per (W,N,G) of a sweep, plus "
+                         "the prompt-lookup mode (W=0, G>0, pool seeded from the prompt) and greedy")
     return ap.parse_args()
+
+
+def lookahead_of(args):
+    """(W, N, G, preseed) of a run: the workload's, or the --wng / --preseed overrides."""
+    W, N, G = I.LOOKAHEAD[args.workload]
+    if args.wng:
+        W, N, G = (int(x) for x in args.wng.split(","))
+    pre = PRESEED.get(args.workload, False) if args.preseed == "auto" else args.preseed == "on"
+    return W, N, G, pre
 
 
 def load_peaks():
@@ -210,12 +226,12 @@ def run_ours(args, rank, world):
     cfg = I.MODELS[args.workload]
     if args.layers:
         cfg = cfg.sliced(args.layers)
-    W, N, G = I.LOOKAHEAD[args.workload]
+    W, N, G, pre = lookahead_of(args)
     T = 1 + (W + G) * (N - 1)
     gen = GEN_TOKENS[args.workload]
     prompt = I.make_prompt(args.workload)
     max_seq = len(prompt) + gen + W + N + 16
-    flags = LA.LA_PRESEED_PROMPT if PRESEED.get(args.workload) else 0
+    flags = LA.LA_PRESEED_PROMPT if pre else 0
     t_gen = time.perf_counter()
     dw = build_model(cfg, LA.LA_BF16)
     torch.cuda.synchronize()
@@ -292,9 +308,9 @@ def run_ours(args, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init weights)",
         "config": {"workload": f"{args.workload}: {cfg.n_layers}L d{cfg.d_model} {cfg.n_heads}x{cfg.head_dim} "
                                f"(kv {cfg.n_kv_heads}) ffn{cfg.ffn} V{cfg.vocab} bf16, prompt {len(prompt)}, "
-                               f"gen {gen}, W{W} N{N} G{G}, T={T} rows",
+                               f"gen {gen}, W{W} N{N} G{G}, T={T} rows" + (", prompt-seeded pool" if pre else ""),
                    "global_batch": 1, "seq_len": max_seq, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (weights 13.2 GB stream every step)"},
+                   "l2": f"inputs larger than L2 (weights {cfg.streamed_params() * 2 / 1e9:.1f} GB stream every step)"},
         "accepted_tokens_per_step": round(acc_per_step, 4),
         "accept_hist": {str(k): acc.count(k) for k in range(1, N + 1)},
         "step_latency_ms": {"median": round(float(np.median(step_ms_l)), 4),
@@ -318,8 +334,51 @@ def run_ours(args, rank, world):
     if e2e:
         out["e2e"] = e2e
     if not args.no_cpu_baseline and world == 1:
-        out["cpu_baseline"] = cpu_baseline(cfg, args.workload, W, N, G, prompt, acc_per_step, steps=2)
+        out["cpu_baseline"] = cpu_baseline(cfg, args.workload, W, N, G, prompt, acc_per_step, steps=2, preseed=pre)
     return out
+
+
+# (W, N, G, prompt-seeded pool) of the sweep: T = 1 + (W+G)(N-1) <= 128 rows
+SWEEP = [(0, 2, 0, False),                                     # greedy
+         (0, 3, 4, True), (0, 5, 4, True),                      # prompt lookup: no window, prompt n-grams
+         (5, 5, 5, False), (7, 5, 7, False), (10, 5, 10, False), (15, 5, 15, False),
+         (15, 3, 15, False), (31, 3, 31, False), (20, 4, 20, False), (10, 7, 10, False),
+         (15, 5, 15, True)]
+
+
+def run_sweep(args, rank, world):
+    """One JSON line per (W, N, G): step latency, accepted tokens/step,
+    tokens/s, speedup over greedy and losslessness (same library, same
+    prompt).  W = 0 with a prompt-seeded pool is the prompt-lookup mode."""
+    import torch
+    import lossless_lookahead_decoding_gb300 as LA
+    from lossless_lookahead_decoding_gb300 import build as B
+    B.build()
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    cfg = I.MODELS[args.workload]
+    if args.layers:
+        cfg = cfg.sliced(args.layers)
+    gen = GEN_TOKENS[args.workload]
+    prompt = I.make_prompt(args.workload)
+    max_seq = len(prompt) + gen + max(w + n for w, n, _, _ in SWEEP) + 16
+    dw = build_model(cfg, LA.LA_BF16)
+    lines, ref_out, greedy_tps = [], None, None
+    for W, N, G, pre in SWEEP:
+        dec = LA.Decoder(cfg, dw, LA.LA_BF16, W, N, G, max_seq, flags=LA.LA_PRESEED_PROMPT if pre else 0)
+        tok, step_ms_l, _, _ = timed_steps(dec, prompt, gen, args.warmup, args.steps)
+        out = dec.generate(prompt, gen)
+        dec.close()
+        tps = tok / (sum(step_ms_l) / 1e3)
+        if ref_out is None:
+            ref_out, greedy_tps = out, tps
+        T = 1 + (W + G) * (N - 1)
+        lines.append({"sweep": args.workload, "mode": "greedy" if W == 0 and G == 0 else
+                      ("prompt-lookup" if W == 0 else "lookahead"), "W": W, "N": N, "G": G, "T": T,
+                      "prompt_seeded_pool": pre, "ms_per_step": round(float(np.mean(step_ms_l)), 4),
+                      "accepted_tokens_per_step": round(tok / args.steps, 4), "tokens_per_s": round(tps, 2),
+                      "speedup_vs_greedy": round(tps / greedy_tps, 4),
+                      "lossless_vs_greedy": bool(np.array_equal(out, ref_out)), "steps": args.steps})
+    return lines if rank == 0 else None
 
 
 def read_traffic(workload):
@@ -369,8 +428,8 @@ def oracle_sample(cfg, W, N, G, prompt, n_steps, preseed=False):
     return times, toks, ratio, O.threads()
 
 
-def cpu_baseline(cfg, workload, W, N, G, prompt, acc_per_step, steps=2):
-    times, toks, ratio, cores = oracle_sample(cfg, W, N, G, prompt, steps, PRESEED.get(workload, False))
+def cpu_baseline(cfg, workload, W, N, G, prompt, acc_per_step, steps=2, preseed=False):
+    times, toks, ratio, cores = oracle_sample(cfg, W, N, G, prompt, steps, preseed)
     full_step_s = float(np.mean(times)) * ratio
     return {"value": round(acc_per_step / full_step_s, 5), "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"{steps} oracle lookahead steps (T={1 + (W + G) * (N - 1)} rows) on a 1-layer slice of the "
@@ -383,11 +442,10 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     cfg = I.MODELS[args.workload]
-    W, N, G = I.LOOKAHEAD[args.workload]
+    W, N, G, pre = lookahead_of(args)
     prompt = I.make_prompt(args.workload)
     # every step is one oracle step on the 1-layer slice (bounded sample)
-    times, toks, ratio, cores = oracle_sample(cfg, W, N, G, prompt, args.warmup + args.steps,
-                                              PRESEED.get(args.workload, False))
+    times, toks, ratio, cores = oracle_sample(cfg, W, N, G, prompt, args.warmup + args.steps, pre)
     t = times[args.warmup:]
     full_s = float(np.sum(t)) * ratio
     # tokens: the slice model's own accepted tokens over the timed steps
@@ -410,10 +468,13 @@ def main():
     rank, world = dist_setup(args.gpus if args.impl == "ours" else 0)
     if args.impl == "reference":
         out = run_reference(args, rank, world)
+    elif args.sweep:
+        out = run_sweep(args, rank, world)
     else:
         out = run_ours(args, rank, world)
     if rank == 0 and out is not None:
-        print(json.dumps(out), flush=True)
+        for line in out if isinstance(out, list) else [out]:
+            print(json.dumps(line), flush=True)
     import torch.distributed as dist
     if dist.is_available() and dist.is_initialized():
         dist.destroy_process_group()

@@ -55,3 +55,21 @@ def test_step_shapes_and_roofline_inputs(name, T):
     assert fl > 2 * cfg.streamed_params() * T
     # arithmetic intensity is below the GB300 ridge (~290 FLOP/B): HBM bound
     assert fl / by < 290
+
+
+def test_lookahead_overrides_and_sweep_shapes():
+    """--wng / --preseed override the workload's settings; every sweep point
+    fits the 128-row step and W = 0 points are the prompt-lookup mode (a
+    prompt-seeded pool, no window)."""
+    import argparse
+    a = argparse.Namespace(workload="7b", wng="", preseed="auto")
+    assert bench.lookahead_of(a) == (15, 5, 15, False)
+    a = argparse.Namespace(workload="34b", wng="", preseed="auto")
+    assert bench.lookahead_of(a) == (7, 5, 7, True)
+    a = argparse.Namespace(workload="7b", wng="0,4,6", preseed="on")
+    assert bench.lookahead_of(a) == (0, 4, 6, True)
+    assert bench.SWEEP[0] == (0, 2, 0, False)
+    for W, N, G, pre in bench.SWEEP:
+        assert 1 + (W + G) * (N - 1) <= 128 and N >= 2
+        if W == 0 and G > 0:
+            assert pre
