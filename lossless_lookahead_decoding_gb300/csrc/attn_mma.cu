@@ -202,18 +202,23 @@ struct AttnArgs {
     float sl2;  // log2(e) / sqrt(hd)
 };
 
+// Shared memory: the Q tile, kBufs chunk buffers (K then V of one chunk; up
+// to kBufs chunk loads in flight), the step rows' K and V, and the state
+// hand-off (o in buffers 1..2 once the cached chunks are done, m and l apart).
+constexpr int kBufs = 3;
+
 template <int HD>
 struct AttnSmem {
-    static constexpr int RB = HD * 2, PS = HD + 4;  // state: o[HD], m, l, 2 pad
+    static constexpr int RB = HD * 2, PS = HD + 4;  // global partial state: o[HD], m, l, 2 pad
     static constexpr int kQ = 0;                                  // Q tile [kRows][HD]
-    static constexpr int kK0 = kQ + kRows * RB;                   // K chunk buffer 0
-    static constexpr int kV0 = kK0 + kChunk * RB;                 // V chunk buffer 0
-    static constexpr int kDump = kV0 + kChunk * RB;               // K/V buffer 1, later the state dump
-    static constexpr int kK1 = kDump, kV1 = kDump + kChunk * RB;
-    static constexpr int kDumpBytes = kRows * PS * 4 > 2 * kChunk * RB ? kRows * PS * 4 : 2 * kChunk * RB;
-    static constexpr int kKS = kDump + kDumpBytes;               // step K [kRows][HD]
+    static constexpr int kBuf0 = kQ + kRows * RB;                 // chunk buffers
+    static constexpr int kBufBytes = 2 * kChunk * RB;             // K [kChunk][HD] then V
+    static constexpr int kDumpO = kBuf0 + kBufBytes;              // o [kRows][HD] fp32 (buffers 1, 2)
+    static_assert(kRows * HD * 4 <= (kBufs - 1) * kBufBytes, "hand-off fits two chunk buffers");
+    static constexpr int kKS = kBuf0 + kBufs * kBufBytes;         // step K [kRows][HD]
     static constexpr int kVS = kKS + kRows * RB;                  // step V
-    static constexpr int kZero = kVS + kRows * RB;                // one zero row
+    static constexpr int kML = kVS + kRows * RB;                  // m, l [kRows][2] fp32
+    static constexpr int kZero = kML + kRows * 8;                 // one zero row
     static constexpr int kInts = kZero + RB;                      // group bookkeeping
     static constexpr int kBytes = kInts + (2 * kRows + 2) * 4;
 };
@@ -227,7 +232,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int RB = HD * 2, NCH = HD / 8, PS = L::PS;
     const uint32_t sb = su32(smem);
-    float* dump = (float*)(smem + L::kDump);
+    float* dump_o = (float*)(smem + L::kDumpO);
+    float* dump_ml = (float*)(smem + L::kML);
     int* gcnt = (int*)(smem + L::kInts);  // [kRows + 1] rows of each group (< a.rows)
     int* gslab = gcnt + kRows + 1;        // [kRows + 1] slab prefix over groups
 
@@ -267,9 +273,25 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
             cp_async16(swz<HD>(sb + vofs, r, c), vc + off, ok);
         }
     };
-    const int n_shared = c_shared_end - c_begin;
-    if (n_shared > 0) load_chunk(c_begin, L::kK0, L::kV0, P);
+    auto buf = [&](int i) { return L::kBuf0 + (i % kBufs) * L::kBufBytes; };
+    // group 0: Q, and the step rows' K/V of this KV head when the CTA has tail work
+    if (has_tail) {
+        for (int i = tid; i < kRows * NCH; i += blockDim.x) {
+            const int r = i / NCH, c = i % NCH;
+            const bool ok = r < a.rows;
+            const size_t off = (size_t)(ok ? r : 0) * dkv + kvh * HD + c * 8;
+            cp_async16(swz<HD>(sb + L::kKS, r, c), a.KS + off, ok);
+            cp_async16(swz<HD>(sb + L::kVS, r, c), a.VS + off, ok);
+        }
+    }
     cp_commit();
+    // groups 1..kBufs: the first cached chunks (empty groups keep the count uniform)
+    const int n_shared = c_shared_end - c_begin;
+#pragma unroll
+    for (int j = 0; j < kBufs; j++) {
+        if (j < n_shared) load_chunk(c_begin + j, buf(j), buf(j) + kChunk * RB, P);
+        cp_commit();
+    }
 
     SlabState<HD> st;
     st.m[0] = st.m[1] = -INFINITY;
@@ -279,10 +301,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
 
     uint32_t qf[HD / 16][4];
     for (int i = 0; i < n_shared; i++) {
-        if (i + 1 < n_shared)
-            load_chunk(c_begin + i + 1, ((i + 1) & 1) ? L::kK1 : L::kK0, ((i + 1) & 1) ? L::kV1 : L::kV0, P);
-        cp_commit();
-        cp_wait<1>();
+        cp_wait<kBufs - 1>();  // chunk i (and everything before it) has landed
         __syncthreads();
         if (warp * 16 < a.rows) {  // slabs of padding rows only are skipped
             if (i == 0) {
@@ -291,7 +310,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
                     ldsm_x4(qf[ks], swz<HD>(sb + L::kQ, warp * 16 + (lane & 7) + (((lane >> 3) & 1) << 3),
                                             2 * ks + (lane >> 4)));
             }
-            const uint32_t kt = sb + ((i & 1) ? L::kK1 : L::kK0), vt = sb + ((i & 1) ? L::kV1 : L::kV0);
+            const uint32_t kt = sb + buf(i), vt = kt + kChunk * RB;
             KeyRows kr;
 #pragma unroll
             for (int j = 0; j < 4; j++) {
@@ -302,38 +321,35 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
             }
             chunk_update<HD, false>(qf, st, kr, [](int, int) { return true; }, a.sl2);
         }
-        __syncthreads();
+        __syncthreads();  // buffer i is free again
+        if (i + kBufs < n_shared) load_chunk(c_begin + i + kBufs, buf(i), buf(i) + kChunk * RB, P);
+        cp_commit();
     }
     // state after the shared chunks: final partial, or hand-off to the tail
+    if (has_tail) {
+        cp_wait<0>();
+        __syncthreads();  // chunk buffers 1, 2 become the hand-off
+    }
     {
-        float* dst = has_tail ? dump : part;
         const int g = lane >> 2, t = lane & 3;
 #pragma unroll
         for (int hh = 0; hh < 2; hh++) {
             const int r = warp * 16 + g + 8 * hh;
             if (r < a.rows) {
-                float* pr = dst + (size_t)r * PS;
-                if (t == 0) *(float2*)(pr + HD) = make_float2(st.m[hh], st.l[hh]);
+                float* po = has_tail ? dump_o + (size_t)r * HD : part + (size_t)r * PS;
+                float* pml = has_tail ? dump_ml + 2 * r : part + (size_t)r * PS + HD;
+                if (t == 0) *(float2*)pml = make_float2(st.m[hh], st.l[hh]);
 #pragma unroll
                 for (int d = 0; d < HD / 8; d++)
-                    *(float2*)(pr + d * 8 + 2 * t) = make_float2(st.o[d][2 * hh], st.o[d][2 * hh + 1]);
+                    *(float2*)(po + d * 8 + 2 * t) = make_float2(st.o[d][2 * hh], st.o[d][2 * hh + 1]);
             }
         }
     }
     if (!has_tail) return;
 
     // ---------------- tail chunks: per row group
-    cp_wait<0>();
-    __syncthreads();
-    const int tile0 = c_shared_end * kChunk;  // first tail chunk's cache rows
-    load_chunk(c_shared_end, L::kK0, L::kV0, P);
-    for (int i = tid; i < kRows * NCH; i += blockDim.x) {
-        const int r = i / NCH, c = i % NCH;
-        const bool ok = r < a.rows;
-        const size_t off = (size_t)(ok ? r : 0) * dkv + kvh * HD + c * 8;
-        cp_async16(swz<HD>(sb + L::kKS, r, c), a.KS + off, ok);
-        cp_async16(swz<HD>(sb + L::kVS, r, c), a.VS + off, ok);
-    }
+    const int tile0 = c_shared_end * kChunk;  // first tail chunk's cache rows (buffer 0)
+    load_chunk(c_shared_end, L::kBuf0, L::kBuf0 + kChunk * RB, P);
     cp_commit();
     if (tid < NCH) *(uint4*)(smem + L::kZero + tid * 16) = make_uint4(0, 0, 0, 0);
     // rows of each group, in row order (static lists, clipped to a.rows)
@@ -379,9 +395,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
             for (int hh = 0; hh < 2; hh++) {
                 const int r = hh ? rB : rA;
                 if (r >= 0) {
-                    const float* pr = dump + (size_t)r * PS;
-                    ts.m[hh] = pr[HD];
-                    ts.l[hh] = pr[HD + 1];
+                    const float* pr = dump_o + (size_t)r * HD;
+                    ts.m[hh] = dump_ml[2 * r];
+                    ts.l[hh] = dump_ml[2 * r + 1];
 #pragma unroll
                     for (int d = 0; d < HD / 8; d++) {
                         const float2 v = *(const float2*)(pr + d * 8 + 2 * t);
@@ -411,8 +427,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
                     uint32_t kb, vb;
                     if (p < P) {
                         row = p - tile0;
-                        kb = sb + L::kK0 + row * RB;
-                        vb = sb + L::kV0 + row * RB;
+                        kb = sb + L::kBuf0 + row * RB;
+                        vb = sb + L::kBuf0 + kChunk * RB + row * RB;
                     } else if (p - P < a.rs.maxoff) {
                         row = gmap[p - P];
                         kb = sb + L::kKS + row * RB;

@@ -6,7 +6,12 @@
 * a 2-layer slice of the Llama-2-7B-shaped workload (d 4096, 32 heads x 128,
   FFN 11008, vocab 32000, the 512-token planted-span prompt, W=15 N=5 G=15,
   121 rows per step) -- the full widths the benchmark runs, with the oracle
-  on the same bytes.
+  on the same bytes;
+* a 1-layer slice of the CodeLlama-34B-shaped workload (d 8192, 64 query
+  heads sharing 8 KV heads, FFN 22016, vocab 32000, W=7 N=5 G=7 with the
+  prompt-seeded pool, 57 rows per step) on a 256-token Zipf(1.2) prompt
+  over 4000 ids with planted spans (shorter than the benchmark's 2048 so the
+  oracle's prefill stays within seconds).
 
 Checks: each step's logits within relative L2 error 1e-2 (bf16) of the fp32
 oracle's (every row within 2e-2: a CPU emulation of the kernels' bf16 rounding
@@ -55,4 +60,19 @@ def test_7b_width_two_layer_slice():
     toks, worst = replay_against_oracle(dec, O.Model(cfg, w), prompt, 2, 1e-2, row_tol=2e-2)
     g = gpu_decoder(cfg, w, 1, 0, 2, 0, 640).generate(prompt, 64)
     la = gpu_decoder(cfg, w, 1, W, N, G, 640).generate(prompt, 64)
+    assert np.array_equal(la, g)
+
+
+def test_34b_width_one_layer_slice():
+    import lossless_lookahead_decoding_gb300 as LA
+    cfg = I.MODELS["34b"].sliced(1)
+    full = I.make_weights(I.MODELS["34b"], 0, bf16=True, layers=[0])
+    w = {k: (v[:1] if isinstance(v, list) else v) for k, v in full.items()}
+    prompt = I.plant_spans(I.zipf_tokens(256, 4000, 1.2, 11), 16, 6, 12)
+    W, N, G = I.LOOKAHEAD["34b"]
+    flags = LA.LA_PRESEED_PROMPT
+    dec = gpu_decoder(cfg, w, 1, W, N, G, 384, flags=flags | LA.LA_DEBUG_LOGITS)
+    toks, worst = replay_against_oracle(dec, O.Model(cfg, w), prompt, 2, 1e-2, preseed=True, row_tol=2e-2)
+    g = gpu_decoder(cfg, w, 1, 0, 2, 0, 384).generate(prompt, 48)
+    la = gpu_decoder(cfg, w, 1, W, N, G, 384, flags=flags).generate(prompt, 48)
     assert np.array_equal(la, g)
