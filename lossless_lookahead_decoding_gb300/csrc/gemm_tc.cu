@@ -564,7 +564,7 @@ __global__ void __launch_bounds__(128) k_gemm_epi(EpiArgs e)
 // r0: acc[j][i] = partials of tile tt[j], feature column f[j], row r0 + i,
 // added in ascending k order; the loads of up to kSumBatch partials of all
 // columns are in flight together.
-constexpr int kSumBatch = 3;
+constexpr int kSumBatch = 2;  // fewer in flight, fewer registers: more CTAs resident beside the GEMM
 
 template <int J, int R>
 __device__ __forceinline__ void sum_partials(const EpiArgs& e, const int* tt, const int* f, int r0, float (*acc)[R])
