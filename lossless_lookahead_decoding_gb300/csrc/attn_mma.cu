@@ -466,7 +466,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
 
 // Merge the splits of every (row, head) in ascending split order.  One warp
 // per (row, head), each lane HD/32 consecutive output dims; the loads of up
-// to 8 splits are issued together, the merge runs in split order.
+// to 4 splits are issued together, the merge runs in split order.
 constexpr int kCombWarps = 8;
 
 template <int HD>
@@ -474,7 +474,7 @@ __global__ void __launch_bounds__(kCombWarps * 32) k_attn_combine(AttnArgs a)
 {
     pdl_wait();
     pdl_trigger();
-    constexpr int PS = HD + 4, V = HD / 32, kB = 8;
+    constexpr int PS = HD + 4, V = HD / 32, kB = 4;  // few registers: the whole grid fits in one wave
     using VecT = typename std::conditional<V == 4, float4, float2>::type;
     const int w = blockIdx.x * kCombWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (w >= a.rows * a.H) return;

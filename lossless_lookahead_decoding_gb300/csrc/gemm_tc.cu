@@ -562,11 +562,12 @@ __global__ void __launch_bounds__(128) k_gemm_epi(EpiArgs e)
 
 // Sum of stream-K partials for J (tile, feature) columns and R rows from
 // r0: acc[j][i] = partials of tile tt[j], feature column f[j], row r0 + i,
-// added in ascending k order; the loads of up to kSumBatch partials of all
-// columns are in flight together.
-constexpr int kSumBatch = 2;  // fewer in flight, fewer registers: more CTAs resident beside the GEMM
+// added in ascending k order; the loads of up to B partials of all columns
+// are in flight together (a small B keeps registers low, so more epilogue
+// CTAs are resident beside the GEMM they wait for).
+constexpr int kSumBatch = 2;  // QKV epilogue
 
-template <int J, int R>
+template <int J, int R, int B>
 __device__ __forceinline__ void sum_partials(const EpiArgs& e, const int* tt, const int* f, int r0, float (*acc)[R])
 {
     const long long total = (long long)e.tiles * e.KB;
@@ -577,10 +578,10 @@ __device__ __forceinline__ void sum_partials(const EpiArgs& e, const int* tt, co
         cnt[j] = owner_cta((long long)tt[j] * e.KB + e.KB - 1, total, e.ctas) - lo[j] + 1;
         n = max(n, cnt[j]);
     }
-    for (int q0 = 0; q0 < n; q0 += kSumBatch) {
-        float v[kSumBatch][J][R];
+    for (int q0 = 0; q0 < n; q0 += B) {
+        float v[B][J][R];
 #pragma unroll
-        for (int q = 0; q < kSumBatch; q++)
+        for (int q = 0; q < B; q++)
 #pragma unroll
             for (int j = 0; j < J; j++)
 #pragma unroll
@@ -589,7 +590,7 @@ __device__ __forceinline__ void sum_partials(const EpiArgs& e, const int* tt, co
                     v[q][j][i] = ok ? e.partial[((size_t)(lo[j] + q0 + q + tt[j]) * e.rows + r0 + i) * kBM + f[j]] : 0.f;
                 }
 #pragma unroll
-        for (int q = 0; q < kSumBatch; q++)
+        for (int q = 0; q < B; q++)
 #pragma unroll
             for (int j = 0; j < J; j++)
                 if (q0 + q < cnt[j]) {
@@ -625,7 +626,7 @@ __global__ void __launch_bounds__(128) k_epi_qkv(EpiArgs e)
     pdl_trigger();
     const int tt[2] = {t, t}, ff[2] = {fa, fb};
     float x[2][R];
-    sum_partials<2, R>(e, tt, ff, r0, x);
+    sum_partials<2, R, kSumBatch>(e, tt, ff, r0, x);
     if (rope) {
         const bool isq = ga < e.dq;
         __nv_bfloat16* dst = isq ? e.Q : e.KS;
@@ -650,6 +651,7 @@ __global__ void __launch_bounds__(128) k_epi_qkv(EpiArgs e)
 }
 
 constexpr int kGluRows = 8;  // rows per CTA of the SwiGLU epilogue
+constexpr int kGluBatch = 2;  // partial loads per batch in the SwiGLU epilogue
 
 // SwiGLU epilogue: gate tiles come first, then the up tiles of the same
 // features; H = silu(gate) * up in bf16.  Thread = (feature, 8 rows).
@@ -660,7 +662,7 @@ __global__ void __launch_bounds__(128) k_epi_swiglu(EpiArgs e)
     const int t = blockIdx.x, f = threadIdx.x, r0 = blockIdx.y * kGluRows;
     const int tt[2] = {t, t + e.tiles / 2}, ff[2] = {f, f};
     float x[2][kGluRows];
-    sum_partials<2, kGluRows>(e, tt, ff, r0, x);
+    sum_partials<2, kGluRows, kGluBatch>(e, tt, ff, r0, x);
     const int fo = t * kBM + f;
     if (fo < e.Nout) {
 #pragma unroll
