@@ -500,20 +500,26 @@ __global__ void __launch_bounds__(128) k_gemm_epi(EpiArgs e)
     __shared__ int sbi[kEpiRows][4];
     const int r0 = blockIdx.y * kEpiRows;
     // tile tt's partials for this thread's feature, rows r0.., ascending k
+    // (the loads of two partials in flight together)
     auto sum_tile = [&](int tt, float* acc) {
         const int c_lo = owner_cta((long long)tt * e.KB, total, e.ctas);
-        const int c_hi = owner_cta((long long)tt * e.KB + e.KB - 1, total, e.ctas);
+        const int n = owner_cta((long long)tt * e.KB + e.KB - 1, total, e.ctas) - c_lo + 1;
+        for (int q0 = 0; q0 < n; q0 += 2) {
+            float v[2][kEpiRows];
 #pragma unroll
-        for (int i = 0; i < kEpiRows; i++) {
-            const int r = r0 + i;
-            acc[i] = r < e.rows ? e.partial[((size_t)(c_lo + tt) * e.rows + r) * kBM + f] : 0.f;
-        }
-        for (int cc = c_lo + 1; cc <= c_hi; cc++) {
+            for (int q = 0; q < 2; q++)
 #pragma unroll
-            for (int i = 0; i < kEpiRows; i++) {
-                const int r = r0 + i;
-                if (r < e.rows) acc[i] += e.partial[((size_t)(cc + tt) * e.rows + r) * kBM + f];
-            }
+                for (int i = 0; i < kEpiRows; i++) {
+                    const int r = r0 + i;
+                    v[q][i] = (q0 + q < n && r < e.rows) ? e.partial[((size_t)(c_lo + q0 + q + tt) * e.rows + r) * kBM + f]
+                                                         : 0.f;
+                }
+#pragma unroll
+            for (int q = 0; q < 2; q++)
+                if (q0 + q < n) {
+#pragma unroll
+                    for (int i = 0; i < kEpiRows; i++) acc[i] = (q0 + q == 0) ? v[q][i] : acc[i] + v[q][i];
+                }
         }
     };
     float acc[kEpiRows];

@@ -14,12 +14,36 @@
 namespace la {
 
 // ---------------------------------------------------------------- embed ---
+// One block per row; 16-byte loads of the embedding row (all of a thread's
+// loads in flight together) when d and the table allow, else one element at
+// a time.
+constexpr int kEmbVec = 4;  // 16-byte loads per thread: d <= 4 * 256 * (16 / sizeof(T))
+
 template <typename T>
 __global__ void k_embed(const int* tok, const T* emb, float* X, int d)
 {
+    constexpr int E = 16 / sizeof(T);  // elements per 16-byte load
     const int r = blockIdx.x;
     const T* e = emb + (size_t)tok[r] * d;
-    for (int k = threadIdx.x; k < d; k += blockDim.x) X[(size_t)r * d + k] = to_f(e[k]);
+    float* x = X + (size_t)r * d;
+    if (d % E == 0 && d <= kEmbVec * E * (int)blockDim.x && ((uintptr_t)emb & 15) == 0) {
+        uint4 v[kEmbVec];
+#pragma unroll
+        for (int i = 0; i < kEmbVec; i++) {
+            const int k = (threadIdx.x + i * blockDim.x) * E;
+            v[i] = k < d ? *(const uint4*)(e + k) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int i = 0; i < kEmbVec; i++) {
+            const int k = (threadIdx.x + i * blockDim.x) * E;
+            if (k >= d) continue;
+            const T* t = reinterpret_cast<const T*>(&v[i]);
+#pragma unroll
+            for (int j = 0; j < E; j += 4) *(float4*)(x + k + j) = make_float4(to_f(t[j]), to_f(t[j + 1]), to_f(t[j + 2]), to_f(t[j + 3]));
+        }
+        return;
+    }
+    for (int k = threadIdx.x; k < d; k += blockDim.x) x[k] = to_f(e[k]);
 }
 
 template <typename T>
