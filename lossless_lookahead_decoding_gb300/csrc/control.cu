@@ -253,80 +253,105 @@ void launch_prefill_rows(cudaStream_t s, const DState* st, const int* prompt, in
 // the m accepted rows.  Harvest: for j ascending insert key win[0][j] ->
 // (win[1..N-2][j], argmax of row (N-2,j)).  Then shift the window up one
 // level with those argmaxes as the new last level.  Finally advance P and c.
-__global__ void k_verify_update(DState* st, const int* tok, const int* amax, int* win, PoolView pool, int W,
-                                int N, int G)
+// Verification, n-gram harvest and window shift of one step.  Warp 0
+// verifies (longest accepted prefix, lowest g on ties) and updates the decode
+// state.  Harvest: warp j claims the slot of window column j's key; each key's
+// lowest column then inserts that key's n-grams in ascending column order, so
+// the pool holds what inserting columns 0..W-1 one after another gives (only
+// the physical slot of colliding keys may differ, which lookups do not see).
+// Then every thread shifts the window (after all harvest reads of it).
+constexpr int kVerifyWarps = 32;  // window columns harvested at once (W <= kMaxW handled in rounds)
+
+__global__ void __launch_bounds__(kVerifyWarps * 32) k_verify_update(DState* st, const int* tok, const int* amax,
+                                                                     int* win, PoolView pool, int W, int N, int G)
 {
-    const int lane = threadIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int n1 = N - 1, ncand = st->ncand, P = st->P;
     const int a0 = amax[0];
     const int vbase = 1 + W * n1;
-    int best = -1;  // (m << 16) | (0xffff - g)
-    for (int g0 = 0; g0 < ncand; g0 += 32) {
-        int g = g0 + lane, key = -1;
-        if (g < ncand) {
-            int m = 0;
-            while (m < n1) {
-                int expect = (m == 0) ? a0 : amax[vbase + g * n1 + m - 1];
-                if (tok[vbase + g * n1 + m] != expect) break;
-                m++;
+    if (warp == 0) {
+        int best = -1;  // (m << 16) | (0xffff - g)
+        for (int g0 = 0; g0 < ncand; g0 += 32) {
+            int g = g0 + lane, key = -1;
+            if (g < ncand) {
+                int m = 0;
+                while (m < n1) {
+                    int expect = (m == 0) ? a0 : amax[vbase + g * n1 + m - 1];
+                    if (tok[vbase + g * n1 + m] != expect) break;
+                    m++;
+                }
+                key = (m << 16) | (0xffff - g);
             }
-            key = (m << 16) | (0xffff - g);
+            for (int o = 16; o > 0; o >>= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, o));
+            best = max(best, key);
         }
-        for (int o = 16; o > 0; o >>= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, o));
-        best = max(best, key);
-    }
-    const int m = best < 0 ? 0 : (best >> 16);
-    const int gs = best < 0 ? -1 : (0xffff - (best & 0xffff));
-    if (lane == 0) {
-        st->emit[0] = a0;
-        st->commit_rows[0] = 0;
-        for (int k = 0; k < m; k++) {
-            st->emit[k + 1] = amax[vbase + gs * n1 + k];
-            st->commit_rows[k + 1] = vbase + gs * n1 + k;
+        const int m = best < 0 ? 0 : (best >> 16);
+        const int gs = best < 0 ? -1 : (0xffff - (best & 0xffff));
+        if (lane == 0) {
+            st->emit[0] = a0;
+            st->commit_rows[0] = 0;
+            for (int k = 0; k < m; k++) {
+                st->emit[k + 1] = amax[vbase + gs * n1 + k];
+                st->commit_rows[k + 1] = vbase + gs * n1 + k;
+            }
+            st->n_emit = m + 1;
+            st->gstar = gs;
+            st->P_before = P;
+            st->P = P + m + 1;
+            st->c = (m == 0) ? a0 : amax[vbase + gs * n1 + m - 1];
+            st->steps += 1;
         }
-        st->n_emit = m + 1;
-        st->gstar = gs;
-        st->P_before = P;
-        st->P = P + m + 1;
-        st->c = (m == 0) ? a0 : amax[vbase + gs * n1 + m - 1];
-        st->steps += 1;
     }
-    // harvest, j ascending, from the window before the shift
+    // harvest from the window before the shift, in rounds of kVerifyWarps columns
+    __shared__ int slot_of[kVerifyWarps];
+    __shared__ int s_err;
+    if (threadIdx.x == 0) s_err = 0;
+    __syncthreads();
     if (G > 0) {
-        int val[kMaxN];
-        for (int j = 0; j < W; j++) {
-            int key = win[j];
-            for (int l = 1; l < n1; l++) val[l - 1] = win[l * W + j];
-            val[n1 - 1] = amax[1 + (n1 - 1) * W + j];
-            bool found;
-            int s = pool_probe(pool, key, &found);
-            if (s < 0) {
-                if (lane == 0) st->status = LA_ERR_CAPACITY;
-                break;
+        for (int j0 = 0; j0 < W; j0 += kVerifyWarps) {
+            const int j = j0 + warp;
+            if (j < W) {
+                const int s = pool_claim(pool, win[j]);
+                if (lane == 0) {
+                    slot_of[warp] = s;
+                    if (s < 0) s_err = 1;
+                }
             }
-            if (!found && lane == 0) {
-                pool.keys[s] = key;
-                pool.cnt[s] = 0;
+            __syncthreads();
+            if (!s_err && j < W) {
+                const int s = slot_of[warp];
+                bool leader = true;
+                for (int k = 0; k < warp; k++) leader = leader && slot_of[k] != s;
+                if (leader) {
+                    for (int jj = warp; jj < kVerifyWarps && j0 + jj < W; jj++) {
+                        if (slot_of[jj] != s) continue;
+                        const int c = j0 + jj;
+                        int val[kMaxN];
+                        for (int l = 1; l < n1; l++) val[l - 1] = win[l * W + c];
+                        val[n1 - 1] = amax[1 + (n1 - 1) * W + c];
+                        pool_insert_slot(pool, s, val);
+                    }
+                }
             }
-            __syncwarp();
-            pool_insert_slot(pool, s, val);
+            __syncthreads();
         }
+        if (threadIdx.x == 0 && s_err) st->status = LA_ERR_CAPACITY;
     }
-    __syncwarp();
+    __syncthreads();
     // window shift: level l <- level l+1; last level <- argmax of last level rows
     const int nw = n1 * W;
     int tmp[4];
     int k = 0;
-    for (int idx = lane; idx < nw; idx += 32) tmp[k++] = (idx < (n1 - 1) * W) ? win[idx + W] : amax[1 + idx];
-    __syncwarp();
+    for (int idx = threadIdx.x; idx < nw; idx += blockDim.x) tmp[k++] = (idx < (n1 - 1) * W) ? win[idx + W] : amax[1 + idx];
+    __syncthreads();
     k = 0;
-    for (int idx = lane; idx < nw; idx += 32) win[idx] = tmp[k++];
+    for (int idx = threadIdx.x; idx < nw; idx += blockDim.x) win[idx] = tmp[k++];
 }
 
 void launch_verify_update(cudaStream_t s, DState* st, const int* tok, const int* amax, int* win, PoolView pool,
                           int W, int N, int G)
 {
-    k_verify_update<<<1, 32, 0, s>>>(st, tok, amax, win, pool, W, N, G);
+    k_verify_update<<<1, kVerifyWarps * 32, 0, s>>>(st, tok, amax, win, pool, W, N, G);
 }
 
 // ------------------------------------------------------------------ commit ---
