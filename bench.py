@@ -65,6 +65,8 @@ def parse():
                     help="W,N,G to use instead of the workload's lookahead settings")
     ap.add_argument("--preseed", default="auto", choices=["auto", "on", "off"],
                     help="seed the n-gram pool with the prompt's n-grams (auto: the workload's setting)")
+    ap.add_argument("--micro", action="store_true",
+                    help="instead of the benchmark line: the attention and n-gram pool micro-benchmarks")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the benchmark line: one JSON line per (W,N,G) of a sweep, plus "
                          "the prompt-lookup mode (W=0, G>0, pool seeded from the prompt) and greedy")
@@ -381,6 +383,129 @@ def run_sweep(args, rank, world):
     return lines if rank == 0 else None
 
 
+def _event_times(fn, reps, stream, before=None):
+    """Device time (µs) of fn() per rep on stream, CUDA events around each;
+    before() (e.g. an L2 flush) runs outside the timed region."""
+    import torch
+    ts = []
+    for _ in range(reps):
+        if before:
+            before()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b) * 1e3)
+    return ts
+
+
+def run_micro(args, rank, world):
+    """Attention micro-benchmark (32 heads x 128, 2048 cached tokens ~ N(0,1),
+    the 121 rows of W=15 N=5 G=15 under the lookahead mask), cold (L2 flushed
+    by a 256 MB write before each rep) and warm; n-gram pool micro-benchmark
+    (4096 Zipf(1.1) keys x 20 4-grams inserted, then a bulk lookup of the
+    4096 keys and a bulk insert of 2048 further n-grams).  One JSON line each."""
+    import torch
+    import lossless_lookahead_decoding_gb300 as LA
+    from lossless_lookahead_decoding_gb300 import build as B
+    B.build()
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    peaks = load_peaks()
+    st = torch.cuda.Stream()
+    lines = []
+    # ---- attention
+    H, hd, P, W, N, G = 32, 128, 2048, 15, 5, 15
+    T = 1 + (W + G) * (N - 1)
+    max_seq = P + 64
+    inp = I.attention_bench_inputs(heads=H, head_dim=hd, ctx=P, rows=T)
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda().to(torch.bfloat16)
+    kc = torch.zeros((H, max_seq, hd), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    kc[:, :P] = bf(inp["k_cache"])
+    vc[:, :P] = bf(inp["v_cache"])
+    q, ks, vs = bf(inp["q"]), bf(inp["k_step"]), bf(inp["v_step"])
+    out = torch.empty((T, H * hd), dtype=torch.bfloat16, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+
+    def attn():
+        rc = LA.la_attention(q.data_ptr(), kc.data_ptr(), vc.data_ptr(), ks.data_ptr(), vs.data_ptr(),
+                             out.data_ptr(), H, H, hd, max_seq, P, W, N, G, st.cuda_stream)
+        assert rc == 0, rc
+
+    def flush_l2():
+        with torch.cuda.stream(st):
+            flush.zero_()
+
+    for _ in range(3):
+        attn()
+    op = _event_times(attn, 10, st)
+    by = 2 * P * H * hd * 2 + T * (2 * H * hd + 2 * H * hd) * 2
+    roof_us = by / (peaks["hbm_gbs"] * 1e3)
+    # kernel time: the attention + split-merge launches of decode steps at
+    # P = 2048 inside a decoder (event pairs around them, LA_PROFILE): the
+    # 32-layer 7B-width model (each layer's 33.6 MB of KV is evicted by the
+    # other layers' weights: cold) and a 1-layer slice of it (KV stays in L2:
+    # warm); synthetic Zipf prompt, random-init weights
+    kern = {}
+    for name, layers in (("cold", 0), ("warm", 1)):
+        cfg = I.MODELS["7b"] if not layers else I.MODELS["7b"].sliced(layers)
+        dw = build_model(cfg, LA.LA_BF16)
+        prompt = I.zipf_tokens(P + 1, cfg.vocab, 1.1, 21)
+        dec = LA.Decoder(cfg, dw, LA.LA_BF16, W, N, G, P + 1 + 64, flags=LA.LA_PROFILE | LA.LA_NO_GRAPH)
+        dec.prefill(prompt)
+        dec.step()
+        p0 = dec.profile()["attention"]  # cumulative since creation: prefill blocks included
+        for _ in range(8):
+            dec.step()
+        p1 = dec.profile()["attention"]
+        kern[name] = 1e3 * (p1["total_ms"] - p0["total_ms"]) / (p1["launches"] - p0["launches"])
+        dec.close()
+        del dw
+        torch.cuda.empty_cache()
+    lines.append({"micro": "attention", "config": f"{H}x{hd} heads, {P} cached tokens, W{W} N{N} G{G} ({T} rows)",
+                  "us_cold": round(kern["cold"], 2), "us_warm": round(kern["warm"], 2),
+                  "algorithmic_bytes": by, "roofline_us": round(roof_us, 2), "peak_gbs": peaks["hbm_gbs"],
+                  "frac_cold": round(roof_us / kern["cold"], 4),
+                  "la_attention_call_us": round(float(np.median(op)), 1),
+                  "note": "us_cold/us_warm: attention + split merge per layer inside a decoder at P=2048 (the "
+                          "decode steps' P grows by the accepted tokens); la_attention_call_us: the standalone "
+                          "ABI op incl. its table uploads, scratch allocation and synchronisation"})
+    # ---- n-gram pool
+    Np, Gp, V = 5, 15, 32000
+    keys, grams = I.pool_bench_inserts(4096, 20, V, Np - 1)
+    pool = LA.la_pool_create(2 * 4096 + 64, Np, Gp, st.cuda_stream)
+    dk = torch.from_numpy(keys).cuda()
+    dg = torch.from_numpy(np.ascontiguousarray(grams)).cuda()
+    torch.cuda.synchronize()
+    t_fill = _event_times(lambda: LA.la_pool_insert(pool, dk.data_ptr(), dg.data_ptr(), len(keys)), 1, st)[0]
+    uq = torch.from_numpy(np.unique(keys)).cuda()
+    lo = torch.empty((len(uq), Gp, Np - 1), dtype=torch.int32, device="cuda")
+    lc = torch.empty(len(uq), dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+
+    def lookup():
+        assert LA.la_pool_lookup(pool, uq.data_ptr(), len(uq), lo.data_ptr(), lc.data_ptr()) == 0
+
+    for _ in range(3):
+        lookup()
+    t_look = _event_times(lookup, 20, st)
+    k2, g2 = I.pool_bench_ngrams(2048, V, Np - 1)
+    dk2, dg2 = torch.from_numpy(k2).cuda(), torch.from_numpy(np.ascontiguousarray(g2)).cuda()
+    torch.cuda.synchronize()
+    t_ins = _event_times(lambda: LA.la_pool_insert(pool, dk2.data_ptr(), dg2.data_ptr(), len(k2)), 5, st)
+    look_bytes = len(uq) * (4 + Gp * (Np - 1) * 4 + 4)
+    lines.append({"micro": "ngram_pool", "config": f"{len(uq)} keys x {Gp} {Np - 1}-grams, vocab {V}, Zipf(1.1)",
+                  "fill_us": round(t_fill, 1), "fill_inserts": int(len(keys)),
+                  "lookup_us": round(float(np.median(t_look)), 2), "lookup_keys": int(len(uq)),
+                  "lookup_bytes": look_bytes,
+                  "insert_us": round(float(np.median(t_ins)), 2), "insert_ngrams": int(len(k2)),
+                  "note": "insert times include the status read-back of la_pool_insert"})
+    LA.la_pool_destroy(pool)
+    return lines if rank == 0 else None
+
+
 def read_traffic(workload):
     """DRAM bytes per GEMM launch from the committed ncu summary, if it was
     taken on the current kernel source (else null)."""
@@ -470,6 +595,8 @@ def main():
         out = run_reference(args, rank, world)
     elif args.sweep:
         out = run_sweep(args, rank, world)
+    elif args.micro:
+        out = run_micro(args, rank, world)
     else:
         out = run_ours(args, rank, world)
     if rank == 0 and out is not None:
