@@ -199,6 +199,7 @@ struct AttnArgs {
     float* part;  // [H][nsplit][kRows][2 + HD]
     __nv_bfloat16* out;
     int rows, H, Hkv, max_seq, nsplit, max_rel;
+    int hpc;    // query heads per CTA (of one KV head): their rows stacked in the Q tile
     float sl2;  // log2(e) / sqrt(hd)
 };
 
@@ -242,7 +243,11 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
     const int P = a.st->P, maxpos = P + a.max_rel;
     // blockIdx.y < nsplit: split y; beyond: extra CTAs for the split that
     // holds the first tail chunk (the chunk containing position P)
-    const int h = blockIdx.x, kvh = h / (a.H / a.Hkv);
+    // this CTA's query heads h0 .. h0 + hpc - 1 share KV head kvh; their rows
+    // are stacked as virtual rows v = (h - h0) * rows + r (v < vrows <= 128):
+    // the cached chunks serve every virtual row at once, since all read the
+    // same keys; the arithmetic of each row is unchanged
+    const int h0 = blockIdx.x * a.hpc, kvh = h0 / (a.H / a.Hkv), vrows = a.hpc * a.rows;
     const int tail_split = (P / kChunk) * kChunk / kSplit;
     const int sp = blockIdx.y < a.nsplit ? blockIdx.y : tail_split;
     const int rep = blockIdx.y < a.nsplit ? 0 : blockIdx.y - a.nsplit + 1;
@@ -256,13 +261,18 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
     if (!has_tail && rep > 0) return;  // replicas only serve splits with tail chunks
     const __nv_bfloat16* kc = a.KC + (size_t)kvh * a.max_seq * HD;
     const __nv_bfloat16* vc = a.VC + (size_t)kvh * a.max_seq * HD;
-    float* part = a.part + ((size_t)h * a.nsplit + sp) * kRows * PS;
+    // partial state of (virtual row v) in this split
+    auto part_row = [&](int v) {
+        const int hl = v / a.rows, r = v - hl * a.rows;
+        return a.part + (((size_t)(h0 + hl) * a.nsplit + sp) * kRows + r) * PS;
+    };
 
-    // Q tile of this head (rows beyond a.rows are zero)
+    // Q tile: virtual rows of the CTA's heads (beyond vrows zero)
     for (int i = tid; i < kRows * NCH; i += blockDim.x) {
-        const int r = i / NCH, c = i % NCH;
-        const bool ok = r < a.rows;
-        cp_async16(swz<HD>(sb + L::kQ, r, c), a.Q + (size_t)(ok ? r : 0) * dq + h * HD + c * 8, ok);
+        const int v = i / NCH, c = i % NCH;
+        const bool ok = v < vrows;
+        const int hl = ok ? v / a.rows : 0, r = ok ? v - hl * a.rows : 0;
+        cp_async16(swz<HD>(sb + L::kQ, v, c), a.Q + (size_t)r * dq + (h0 + hl) * HD + c * 8, ok);
     }
     auto load_chunk = [&](int cidx, int kofs, int vofs, int valid_end) {
         for (int i = tid; i < kChunk * NCH; i += blockDim.x) {
@@ -303,7 +313,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
     for (int i = 0; i < n_shared; i++) {
         cp_wait<kBufs - 1>();  // chunk i (and everything before it) has landed
         __syncthreads();
-        if (warp * 16 < a.rows) {  // slabs of padding rows only are skipped
+        if (warp * 16 < vrows) {  // slabs of padding rows only are skipped
             if (i == 0) {
 #pragma unroll
                 for (int ks = 0; ks < HD / 16; ks++)
@@ -334,10 +344,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
         const int g = lane >> 2, t = lane & 3;
 #pragma unroll
         for (int hh = 0; hh < 2; hh++) {
-            const int r = warp * 16 + g + 8 * hh;
-            if (r < a.rows) {
-                float* po = has_tail ? dump_o + (size_t)r * HD : part + (size_t)r * PS;
-                float* pml = has_tail ? dump_ml + 2 * r : part + (size_t)r * PS + HD;
+            const int v = warp * 16 + g + 8 * hh;
+            if (v < vrows) {
+                float* po = has_tail ? dump_o + (size_t)v * HD : part_row(v);
+                float* pml = has_tail ? dump_ml + 2 * v : part_row(v) + HD;
                 if (t == 0) *(float2*)pml = make_float2(st.m[hh], st.l[hh]);
 #pragma unroll
                 for (int d = 0; d < HD / 8; d++)
@@ -366,9 +376,11 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
     }
     cp_wait<0>();
     __syncthreads();
-    const int n_items = gslab[ng];
+    const int n_group_items = gslab[ng], n_items = a.hpc * n_group_items;
     const int g4 = lane >> 2;
-    for (int it = rep * kWarps + warp; it < n_items; it += n_rep * kWarps) {
+    for (int it_all = rep * kWarps + warp; it_all < n_items; it_all += n_rep * kWarps) {
+        // item = (head of the CTA, slab of a row group); rows r, virtual rows hl * rows + r
+        const int hl = it_all / n_group_items, it = it_all - hl * n_group_items, vofs = hl * a.rows;
         int g = 0;
         while (gslab[g + 1] <= it) g++;
         const int* glist = a.rs.grp_rows + a.rs.grp_start[g];
@@ -384,7 +396,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
 #pragma unroll
             for (int ks = 0; ks < HD / 16; ks++) {
                 const int ch = 2 * ks + (lane >> 4);
-                ldsm_x4(qf[ks], rq >= 0 ? swz<HD>(sb + L::kQ, rq, ch) : sb + L::kZero + (ch << 4));
+                ldsm_x4(qf[ks], rq >= 0 ? swz<HD>(sb + L::kQ, vofs + rq, ch) : sb + L::kZero + (ch << 4));
             }
         }
         // resume the rows' states (exact fp32 hand-off)
@@ -395,9 +407,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
             for (int hh = 0; hh < 2; hh++) {
                 const int r = hh ? rB : rA;
                 if (r >= 0) {
-                    const float* pr = dump_o + (size_t)r * HD;
-                    ts.m[hh] = dump_ml[2 * r];
-                    ts.l[hh] = dump_ml[2 * r + 1];
+                    const float* pr = dump_o + (size_t)(vofs + r) * HD;
+                    ts.m[hh] = dump_ml[2 * (vofs + r)];
+                    ts.l[hh] = dump_ml[2 * (vofs + r) + 1];
 #pragma unroll
                     for (int d = 0; d < HD / 8; d++) {
                         const float2 v = *(const float2*)(pr + d * 8 + 2 * t);
@@ -453,7 +465,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
             for (int hh = 0; hh < 2; hh++) {
                 const int r = hh ? rB : rA;
                 if (r >= 0) {
-                    float* pr = part + (size_t)r * PS;
+                    float* pr = part_row(vofs + r);
                     if (t == 0) *(float2*)(pr + HD) = make_float2(ts.m[hh], ts.l[hh]);
 #pragma unroll
                     for (int d = 0; d < HD / 8; d++)
@@ -561,7 +573,12 @@ void launch_attn_mma(cudaStream_t s, const DState* st, RowSet rs, int max_rel, c
     a.nsplit = (max_seq + kSplit - 1) / kSplit;
     a.max_rel = max_rel;
     a.sl2 = 1.4426950408889634f / sqrtf((float)hd);
-    dim3 grid(H, a.nsplit + kRep - 1);
+    // query heads per CTA: the largest power of two dividing the GQA group
+    // whose stacked rows still fit the 128-row tile (1 without GQA)
+    const int group = H / Hkv;
+    a.hpc = 1;
+    while (group % (2 * a.hpc) == 0 && 2 * a.hpc * rows <= kRows) a.hpc *= 2;
+    dim3 grid(H / a.hpc, a.nsplit + kRep - 1);
     if (hd == 128) {
         launch_pdl(k_attn_mma<128>, grid, dim3(kWarps * 32), AttnSmem<128>::kBytes, s, a);
         launch_pdl(k_attn_combine<128>, dim3((rows * H + kCombWarps - 1) / kCombWarps), dim3(kCombWarps * 32), 0, s, a);
