@@ -695,34 +695,47 @@ __global__ void k_argmax_unpack(unsigned long long* amaxp, int* amax, int rows)
 // Residual add of a stream-K GEMM folded into the RMSNorm that follows it:
 // per row, X += (the tile partials summed in ascending k order) -- the same
 // sums, in the same order, as the residual epilogue -- then
-// XN = X / sqrt(mean(X^2) + eps) * w in bf16.  One block per row.
-constexpr int kRnThreads = 1024, kRnVec = 2, kRnSeg = 8;  // d <= 2 * 4 * 1024
+// XN = X / sqrt(mean(X^2) + eps) * w in bf16.  One block of 1024 threads
+// per row, VEC float4 per thread.
+constexpr int kRnThreads = 1024, kRnSeg = 6;  // d <= VEC * 4 * 1024
 
-__global__ void __launch_bounds__(kRnThreads) k_resid_rmsnorm(ResidArgs a, float* __restrict__ X,
-                                                             const __nv_bfloat16* __restrict__ w,
-                                                             __nv_bfloat16* __restrict__ out, int d, float eps)
+template <int VEC>
+__device__ __forceinline__ void resid_rmsnorm(const ResidArgs& a, float* __restrict__ X,
+                                              const __nv_bfloat16* __restrict__ w, __nv_bfloat16* __restrict__ out,
+                                              int d, float eps)
 {
-    pdl_wait();
-    pdl_trigger();
     const int r = blockIdx.x, d4 = d >> 2;
     float4* x = (float4*)(X + (size_t)r * d);
     const long long total = (long long)a.tiles * a.KB;
-    __shared__ int s_lo[kRnVec * kRnThreads * 4 / kBM], s_n[kRnVec * kRnThreads * 4 / kBM];
+    __shared__ int s_lo[VEC * kRnThreads * 4 / kBM], s_n[VEC * kRnThreads * 4 / kBM];
+    // Before the wait, what does not depend on the GEMM: the owner table, the
+    // residual row (its last writer finished before the GEMM started) and the
+    // norm weights.
     for (int t = threadIdx.x; t < a.tiles; t += kRnThreads) {
         const int lo = owner_cta((long long)t * a.KB, total, a.ctas);
         s_lo[t] = lo;
         s_n[t] = owner_cta((long long)t * a.KB + a.KB - 1, total, a.ctas) - lo + 1;
     }
+    float4 v[VEC], wf[VEC];
+#pragma unroll
+    for (int i = 0; i < VEC; i++) {
+        const int k = threadIdx.x + i * kRnThreads;
+        if (k < d4) {
+            v[i] = x[k];
+            wf[i] = make_float4(__bfloat162float(w[4 * k]), __bfloat162float(w[4 * k + 1]),
+                                __bfloat162float(w[4 * k + 2]), __bfloat162float(w[4 * k + 3]));
+        } else {
+            v[i] = wf[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    pdl_wait();
+    pdl_trigger();
     __syncthreads();
-    float4 v[kRnVec];
     float ss = 0.f;
 #pragma unroll
-    for (int i = 0; i < kRnVec; i++) {
+    for (int i = 0; i < VEC; i++) {
         const int k = threadIdx.x + i * kRnThreads;
-        if (k >= d4) {
-            v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            continue;
-        }
+        if (k >= d4) continue;
         const int t = (4 * k) / kBM, f = (4 * k) % kBM, lo = s_lo[t], n = s_n[t];
         const float4* src = (const float4*)&a.partial[((size_t)(lo + t) * a.rows + r) * kBM + f];
         const size_t seg = (size_t)a.rows * kBM / 4;  // float4 stride between segments
@@ -745,12 +758,11 @@ __global__ void __launch_bounds__(kRnThreads) k_resid_rmsnorm(ResidArgs a, float
                 }
             }
         }
-        const float4 old = x[k];
-        v[i] = make_float4(old.x + acc.x, old.y + acc.y, old.z + acc.z, old.w + acc.w);
+        v[i] = make_float4(v[i].x + acc.x, v[i].y + acc.y, v[i].z + acc.z, v[i].w + acc.w);
         x[k] = v[i];
     }
 #pragma unroll
-    for (int i = 0; i < kRnVec; i++) {
+    for (int i = 0; i < VEC; i++) {
         ss += v[i].x * v[i].x;
         ss += v[i].y * v[i].y;
         ss += v[i].z * v[i].z;
@@ -770,21 +782,36 @@ __global__ void __launch_bounds__(kRnThreads) k_resid_rmsnorm(ResidArgs a, float
     __syncthreads();
     const float rr = s_r;
 #pragma unroll
-    for (int i = 0; i < kRnVec; i++) {
+    for (int i = 0; i < VEC; i++) {
         const int k = threadIdx.x + i * kRnThreads;
         if (k < d4) {
-            const int e = 4 * k;
-            __nv_bfloat162 lo = __floats2bfloat162_rn(v[i].x * rr * __bfloat162float(w[e]),
-                                                      v[i].y * rr * __bfloat162float(w[e + 1]));
-            __nv_bfloat162 hi = __floats2bfloat162_rn(v[i].z * rr * __bfloat162float(w[e + 2]),
-                                                      v[i].w * rr * __bfloat162float(w[e + 3]));
+            __nv_bfloat162 lo = __floats2bfloat162_rn(v[i].x * rr * wf[i].x, v[i].y * rr * wf[i].y);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(v[i].z * rr * wf[i].z, v[i].w * rr * wf[i].w);
             uint2 u;
             u.x = *reinterpret_cast<uint32_t*>(&lo);
             u.y = *reinterpret_cast<uint32_t*>(&hi);
-            *(uint2*)(out + (size_t)r * d + e) = u;
+            *(uint2*)(out + (size_t)r * d + 4 * k) = u;
         }
     }
 }
+
+// d <= 4096: at most 48 registers, so that the next GEMM's CTA (12 K
+// registers) fits beside the norm's block and starts fetching its weights
+// while the norm runs.
+__global__ void __maxnreg__(48) k_resid_rmsnorm(ResidArgs a, float* __restrict__ X, const __nv_bfloat16* __restrict__ w,
+                                                __nv_bfloat16* __restrict__ out, int d, float eps)
+{
+    resid_rmsnorm<1>(a, X, w, out, d, eps);
+}
+
+// 4096 < d <= 8192
+__global__ void __launch_bounds__(kRnThreads) k_resid_rmsnorm_wide(ResidArgs a, float* __restrict__ X,
+                                                                  const __nv_bfloat16* __restrict__ w,
+                                                                  __nv_bfloat16* __restrict__ out, int d, float eps)
+{
+    resid_rmsnorm<2>(a, X, w, out, d, eps);
+}
+
 
 // ------------------------------------------------------------------ plan ---
 
@@ -893,6 +920,7 @@ int tc_plan_create(TcPlan* p, const la_model_desc& d, const void* const* lw, voi
     if (esz != 2) return 1;
     const int dq = d.n_heads * d.head_dim, dkv = d.n_kv_heads * d.head_dim;
     if (dq % kBM || dkv % kBM || d.d_model % kAtom || kBM % d.head_dim || d.head_dim % 2) return 1;
+    if (d.d_model > 2 * 4 * kRnThreads) return 1;  // the residual norm's row limit
     if (!get_encode()) return 1;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
@@ -1046,8 +1074,12 @@ void tc_resid_rmsnorm(const TcPlan& p, cudaStream_t s, const TcResid& pend, floa
 {
     ResidArgs a{pend.tiles, pend.KB, pend.ctas, pend.rows, pend.partial};
     if (p.prof) p.prof->begin(s);
-    launch_pdl(k_resid_rmsnorm, dim3(pend.rows), dim3(kRnThreads), 0, s, a, X, (const __nv_bfloat16*)w,
-               (__nv_bfloat16*)XN, d, eps);
+    if (d <= 4 * kRnThreads)
+        launch_pdl(k_resid_rmsnorm, dim3(pend.rows), dim3(kRnThreads), 0, s, a, X, (const __nv_bfloat16*)w,
+                   (__nv_bfloat16*)XN, d, eps);
+    else
+        launch_pdl(k_resid_rmsnorm_wide, dim3(pend.rows), dim3(kRnThreads), 0, s, a, X, (const __nv_bfloat16*)w,
+                   (__nv_bfloat16*)XN, d, eps);
     if (p.prof) p.prof->end(s, P_NORM, 0, 0);
 }
 
