@@ -606,17 +606,17 @@ __device__ __forceinline__ void sum_partials(const EpiArgs& e, const int* tt, co
     }
 }
 
-constexpr int kQkvRows = 16;  // rows per CTA of the QKV epilogue (8 per thread)
-
 // QKV epilogue: Q, K (rotate-half RoPE at each row's position) and V of the
-// step rows, bf16.  Thread = (RoPE pair (fa, fa + hd/2) of the tile, 8 rows);
-// the RoPE table entries do not depend on the GEMM and are fetched before
-// waiting for it.
+// step rows, bf16.  Thread = (RoPE pair (fa, fa + hd/2) of the tile, R rows),
+// a CTA 2R rows; the RoPE table entries do not depend on the GEMM and are
+// fetched before waiting for it.  R = 8 for few rows; R = 11 for many (121
+// rows: 576 CTAs of 128 registers a thread, one wave at 4 CTAs per SM, where
+// R = 8 makes 768 CTAs of 96 registers and 5 per SM: 760 in the first wave).
+template <int R>
 __global__ void __launch_bounds__(128) k_epi_qkv(EpiArgs e)
 {
-    constexpr int R = kQkvRows / 2;
     const int t = blockIdx.x, pr = threadIdx.x & 63;
-    const int r0 = blockIdx.y * kQkvRows + (threadIdx.x >> 6) * R;
+    const int r0 = blockIdx.y * 2 * R + (threadIdx.x >> 6) * R;
     const int half = e.hd >> 1;
     const int fa = (pr / half) * e.hd + pr % half, fb = fa + half;
     const int ga = t * kBM + fa;
@@ -656,23 +656,27 @@ __global__ void __launch_bounds__(128) k_epi_qkv(EpiArgs e)
     }
 }
 
-constexpr int kGluRows = 8;  // rows per CTA of the SwiGLU epilogue
-constexpr int kGluBatch = 2;  // partial loads per batch in the SwiGLU epilogue
-
 // SwiGLU epilogue: gate tiles come first, then the up tiles of the same
-// features; H = silu(gate) * up in bf16.  Thread = (feature, 8 rows).
-__global__ void __launch_bounds__(128) k_epi_swiglu(EpiArgs e)
+// features; H = silu(gate) * up in bf16.  Thread = (feature, ROWS rows), the
+// loads of BATCH partials in flight at a time (the sums are the same for
+// every ROWS and BATCH).  Few rows: ROWS = 8, BATCH = 2 (one round of loads).
+// Many rows: ROWS = 16, BATCH = 1, at most 80 registers, so that the whole
+// grid is resident beside the gate/up GEMM it waits for and, as it drains,
+// still leaves room on every SM for the down GEMM's CTA to start fetching
+// its weights.
+template <int ROWS, int BATCH>
+__global__ void __maxnreg__(80) k_epi_swiglu(EpiArgs e)
 {
     pdl_wait();
     pdl_trigger();
-    const int t = blockIdx.x, f = threadIdx.x, r0 = blockIdx.y * kGluRows;
+    const int t = blockIdx.x, f = threadIdx.x, r0 = blockIdx.y * ROWS;
     const int tt[2] = {t, t + e.tiles / 2}, ff[2] = {f, f};
-    float x[2][kGluRows];
-    sum_partials<2, kGluRows, kGluBatch>(e, tt, ff, r0, x);
+    float x[2][ROWS];
+    sum_partials<2, ROWS, BATCH>(e, tt, ff, r0, x);
     const int fo = t * kBM + f;
     if (fo < e.Nout) {
 #pragma unroll
-        for (int i = 0; i < kGluRows; i++) {
+        for (int i = 0; i < ROWS; i++) {
             if (r0 + i < e.rows) {
                 const float gt = x[0][i];
                 e.H[(size_t)(r0 + i) * e.Nout + fo] = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * x[1][i]);
@@ -1049,7 +1053,10 @@ void tc_qkv_rope(const TcPlan& p, cudaStream_t s, int layer, int rows, const int
     e.KS = (__nv_bfloat16*)KS;
     e.VS = (__nv_bfloat16*)VS;
     launch_epi(p, s, [&] {
-        launch_pdl(k_epi_qkv, dim3(g.tiles, (rows + kQkvRows - 1) / kQkvRows), dim3(128), 0, s, e);
+        if (rows <= 16)
+            launch_pdl(k_epi_qkv<8>, dim3(g.tiles, (rows + 15) / 16), dim3(128), 0, s, e);
+        else
+            launch_pdl(k_epi_qkv<11>, dim3(g.tiles, (rows + 21) / 22), dim3(128), 0, s, e);
     });
 }
 
@@ -1091,7 +1098,10 @@ void tc_gateup_swiglu(const TcPlan& p, cudaStream_t s, int layer, int rows)
     EpiArgs e = epi_base(im, g, rows);
     e.H = (__nv_bfloat16*)im.HID;
     launch_epi(p, s, [&] {
-        launch_pdl(k_epi_swiglu, dim3(g.tiles / 2, (rows + kGluRows - 1) / kGluRows), dim3(128), 0, s, e);
+        if (rows <= 16)
+            launch_pdl(k_epi_swiglu<8, 2>, dim3(g.tiles / 2, (rows + 7) / 8), dim3(128), 0, s, e);
+        else
+            launch_pdl(k_epi_swiglu<16, 1>, dim3(g.tiles / 2, (rows + 15) / 16), dim3(128), 0, s, e);
     });
 }
 
