@@ -697,9 +697,8 @@ __global__ void k_argmax_unpack(unsigned long long* amaxp, int* amax, int rows)
 }
 
 // Residual add of a stream-K GEMM folded into the RMSNorm that follows it:
-// per row, X += (the tile partials summed in ascending k order) -- the same
-// sums, in the same order, as the residual epilogue -- then
-// XN = X / sqrt(mean(X^2) + eps) * w in bf16.  One block of 1024 threads
+// per row, X += (the tile partials summed in ascending k order, as in every
+// epilogue) then XN = X / sqrt(mean(X^2) + eps) * w in bf16.  One block of 1024 threads
 // per row, VEC float4 per thread.
 constexpr int kRnThreads = 1024, kRnSeg = 6;  // d <= VEC * 4 * 1024
 
@@ -713,8 +712,9 @@ __device__ __forceinline__ void resid_rmsnorm(const ResidArgs& a, float* __restr
     const long long total = (long long)a.tiles * a.KB;
     __shared__ int s_lo[VEC * kRnThreads * 4 / kBM], s_n[VEC * kRnThreads * 4 / kBM];
     // Before the wait, what does not depend on the GEMM: the owner table, the
-    // residual row (its last writer finished before the GEMM started) and the
-    // norm weights.
+    // residual row and the norm weights.  The row's last writer (the previous
+    // norm or the embedding) completed before the GEMM's CTAs passed their
+    // own wait, and this kernel is launched only after all of them did.
     for (int t = threadIdx.x; t < a.tiles; t += kRnThreads) {
         const int lo = owner_cta((long long)t * a.KB, total, a.ctas);
         s_lo[t] = lo;
