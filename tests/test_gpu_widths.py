@@ -13,6 +13,12 @@
   over 4000 ids with planted spans (shorter than the benchmark's 2048 so the
   oracle's prefill stays within seconds).
 
+* the full 32-layer 7B-shaped model in the configuration the benchmark times
+  (512-token prompt, W=15 N=5 G=15, no debug logits): the oracle cannot run
+  that forward in seconds, so there only what holds at any size is checked
+  -- every step's rows, emitted tokens, window and pool bit-exact against the
+  oracle controller fed the GPU's argmaxes, and the tokens equal to GPU greedy.
+
 Checks: each step's logits within relative L2 error 1e-2 (bf16) of the fp32
 oracle's (every row within 2e-2: a CPU emulation of the kernels' bf16 rounding
 points gives ~1.1e-2 for single rows of the 2-layer 7B slice), rows/window/pool/emitted tokens bit-exact against the oracle
@@ -76,3 +82,40 @@ def test_34b_width_one_layer_slice():
     g = gpu_decoder(cfg, w, 1, 0, 2, 0, 384).generate(prompt, 48)
     la = gpu_decoder(cfg, w, 1, W, N, G, 384, flags=flags).generate(prompt, 48)
     assert np.array_equal(la, g)
+
+
+def test_7b_full_depth_controller_replay():
+    import oracle as O
+    import lossless_lookahead_decoding_gb300 as LA
+    cfg = I.MODELS["7b"]
+    dw = LA.device_weights(cfg, I.iter_weights(cfg, 0, bf16=False), LA.LA_BF16)
+    prompt = I.make_prompt("7b")
+    W, N, G = I.LOOKAHEAD["7b"]
+    dec = LA.Decoder(cfg, dw, LA.LA_BF16, W, N, G, 768)
+    ctrl = O.Controller(W, N, G, cfg.vocab)
+    ctrl.init(prompt, seed=2)
+    dec.prefill(prompt)
+    assert np.array_equal(dec.window(), ctrl.window())
+    c, P = int(prompt[-1]), len(prompt) - 1
+    out = []
+    for _ in range(24):
+        emit = dec.step()
+        tok_g, pos_g, ncand = dec.rows()
+        amax = dec.argmax()
+        tok, pos, _ = ctrl.rows(c, P)
+        T = len(tok)
+        assert T == 1 + (W + ncand) * (N - 1)
+        assert np.array_equal(tok_g[:T], tok) and np.array_equal(pos_g[:T], pos)
+        emit_o, _, _ = ctrl.advance(amax[:T])
+        assert np.array_equal(emit, emit_o), (emit, emit_o)
+        assert np.array_equal(dec.window(), ctrl.window())
+        for key in set(int(x) for x in tok):
+            assert np.array_equal(dec.pool(key), ctrl.pool(key)), key
+        out.extend(emit.tolist())
+        P += len(emit)
+        c = int(emit[-1])
+    dec.close()
+    greedy = LA.Decoder(cfg, dw, LA.LA_BF16, 0, 2, 0, 768)
+    g = greedy.generate(prompt, len(out))
+    greedy.close()
+    assert np.array_equal(np.array(out, np.int32), g)
