@@ -17,7 +17,15 @@ Functions and what pins them (the tests under tests/test_oracle_*.py):
                   figures, per-row equivalence of the masked forward with the
                   plain causal forward, a brute-force LCP check of verification
                   and a list-based replay of the pool.
-  Controller      the window/pool/verify state machine fed external argmaxes.
+  Controller      the window/pool/verify state machine fed external argmaxes
+                  (or, for sampling verification, the rows' logits).
+  sample_decode / lookahead_sample / sample_logits
+                  temperature sampling and the sampling verification (R10) --
+                  pinned by an exact rational enumeration of the verification
+                  rule, Monte-Carlo agreement of the oracle's draws with the
+                  softmax and, on a Markov toy model, of the sampled lookahead's
+                  token sequences with plain ancestral sampling's exact
+                  probabilities, and the tau -> 0 reduction to greedy decoding.
   Parity unpinned: acceptance rate and the choice among the readings R1, R3,
   R6, R7 (nothing on the pages fixes them).
 """
@@ -59,7 +67,7 @@ def lib():
     global _lib
     if _lib is None:
         L = C.CDLL(build())
-        vp, i32, u64 = C.c_void_p, C.c_int, C.c_uint64
+        vp, i32, u64, f32, f64 = C.c_void_p, C.c_int, C.c_uint64, C.c_float, C.c_double
         sig = {
             "om_seq_new": (vp, [vp, i32]), "om_seq_free": (None, [vp]),
             "om_threads": (i32, []), "om_rope_table": (None, [vp, vp, vp]),
@@ -75,6 +83,11 @@ def lib():
             "om_ctrl_window": (None, [vp, vp]),
             "om_lookahead": (i32, [vp, vp, i32, i32, i32, i32, u64, i32, i32, i32, vp, vp, vp]),
             "om_attention": (i32, [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]),
+            "om_uniform": (f64, [vp]),
+            "om_sample_logits": (None, [vp, i32, f32, vp, i32, vp]),
+            "om_ctrl_advance_sample": (i32, [vp, vp, f32, vp, vp, vp, vp]),
+            "om_sample_decode": (i32, [vp, vp, i32, i32, i32, f32, u64, vp]),
+            "om_lookahead_sample": (i32, [vp, vp, i32, i32, i32, i32, u64, i32, f32, u64, i32, i32, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -195,6 +208,53 @@ def lookahead(model: Model, prompt, W: int, N: int, G: int, max_new: int, seed: 
     return out, int(steps[0]), hist
 
 
+def sample_decode(model: Model, prompt, max_new: int, tau: float, rng_seed: int, max_seq: int | None = None):
+    """Plain ancestral sampling at temperature tau."""
+    p = _i32(prompt)
+    max_seq = max_seq or (len(p) + max_new + 8)
+    out = np.zeros(max_new, np.int32)
+    if lib().om_sample_decode(model.ptr, _p(p), len(p), max_new, max_seq, tau, rng_seed, _p(out)):
+        raise ValueError("om_sample_decode failed")
+    return out
+
+
+def lookahead_sample(model: Model, prompt, W: int, N: int, G: int, max_new: int, tau: float, rng_seed: int,
+                     seed: int = 2, preseed: bool = False, max_seq: int | None = None):
+    """Lookahead decoding with sampling verification; (tokens, steps, accept_hist)."""
+    p = _i32(prompt)
+    max_seq = max_seq or (len(p) + max_new + W + N + 8)
+    out = np.zeros(max_new, np.int32)
+    steps = np.zeros(1, np.int32)
+    hist = np.zeros(N + 1, np.int32)
+    rc = lib().om_lookahead_sample(model.ptr, _p(p), len(p), W, N, G, seed, int(preseed), tau, rng_seed, max_new,
+                                   max_seq, _p(out), _p(steps), _p(hist))
+    if rc:
+        raise ValueError("om_lookahead_sample failed")
+    return out, int(steps[0]), hist
+
+
+class Rng:
+    """The splitmix64 stream the sampling functions draw their uniforms from."""
+
+    def __init__(self, seed: int):
+        self.state = (C.c_uint64 * 1)(seed)
+
+    @property
+    def ptr(self):
+        return C.cast(self.state, C.c_void_p)
+
+    def uniform(self) -> float:
+        return lib().om_uniform(self.ptr)
+
+
+def sample_logits(z, tau: float, rng: Rng, n: int):
+    """n draws from softmax(z / tau) (one uniform each)."""
+    z = np.ascontiguousarray(z, dtype=np.float32)
+    out = np.zeros(n, np.int32)
+    lib().om_sample_logits(_p(z), len(z), tau, rng.ptr, n, _p(out))
+    return out
+
+
 def splitmix64_stream(seed: int, n: int):
     st = (C.c_uint64 * 1)(seed)
     return [lib().om_splitmix64(C.cast(st, C.c_void_p)) for _ in range(n)]
@@ -236,6 +296,16 @@ class Controller:
         rows = np.zeros(self.N + 1, np.int32)
         g = (C.c_int * 1)()
         n = lib().om_ctrl_advance(self.h, _p(a), _p(emit), _p(rows), C.cast(g, C.c_void_p))
+        return emit[:n].copy(), rows[:n].copy(), int(g[0])
+
+    def advance_sample(self, logits, tau: float, rng: Rng):
+        """R10 verification by sampling from the rows' logits [T][V], then the
+        R6/R7 harvest and shift with the rows' argmaxes."""
+        lg = np.ascontiguousarray(logits, dtype=np.float32)
+        emit = np.zeros(self.N + 1, np.int32)
+        rows = np.zeros(self.N + 1, np.int32)
+        g = (C.c_int * 1)()
+        n = lib().om_ctrl_advance_sample(self.h, _p(lg), tau, rng.ptr, _p(emit), _p(rows), C.cast(g, C.c_void_p))
         return emit[:n].copy(), rows[:n].copy(), int(g[0])
 
     def pool(self, key: int):

@@ -37,6 +37,16 @@
  *  R8 commit KV of row 0 and of the accepted candidate rows;
  *  R9 optional prompt pre-seed: insert (prompt[i], prompt[i+1..i+N-1]) for
  *     i ascending ("Key points": prompt n-grams in the pool help).
+ *  R10 sampling verification (the summary says the method supports sampling
+ *     and keeps the output distribution; it gives no algorithm, so this one
+ *     is designed here): temperature softmax p = softmax(z / tau) of a row;
+ *     at each candidate level the distinct candidate tokens v are tried in
+ *     candidate order, v accepted with probability p(v) / (1 - mass of the
+ *     tokens already rejected at this level); if none is accepted, the token
+ *     is drawn from p restricted to the tokens not rejected.  Each emitted
+ *     token is then distributed exactly as p of its row (the acceptance
+ *     probabilities telescope), so the emitted sequence has the distribution
+ *     of plain ancestral sampling.  The lookahead branch keeps using argmaxes.
  *
  * Model (M1-M3): h = x + Wo*Attn(RMSNorm(x)); y = h + Wd*(silu(Wg n) . Wu n),
  * n = RMSNorm(h); RMSNorm(x) = x / sqrt(mean(x^2) + eps) * w (Zhang and
@@ -531,6 +541,24 @@ OM_EXPORT int om_ctrl_rows(om_ctrl* k, int c, int P, int* tok, int* pos, unsigne
     return T;
 }
 
+/* R6 harvest (j ascending, from the window before the shift) and R7 window
+ * shift, given the argmax of every row of the step. */
+static void harvest_and_shift(om_ctrl* k, const int* amax)
+{
+    const int W = k->W, n1 = k->N - 1;
+    int* val = (int*)malloc(sizeof(int) * n1);
+    for (int j = 0; j < W; j++) {
+        int key = k->win[j];
+        for (int l = 1; l < n1; l++) val[l - 1] = k->win[(size_t)l * W + j];
+        val[n1 - 1] = amax[row_la(k, n1 - 1, j)];
+        om_pool_insert(k, key, val);
+    }
+    free(val);
+    for (int l = 0; l + 1 < n1; l++)
+        memcpy(k->win + (size_t)l * W, k->win + (size_t)(l + 1) * W, sizeof(int) * W);
+    for (int j = 0; j < W; j++) k->win[(size_t)(n1 - 1) * W + j] = amax[row_la(k, n1 - 1, j)];
+}
+
 /*
  * R5-R7 after the forward of the rows built by the last om_ctrl_rows call.
  * amax: argmax of every row.  Writes the emitted tokens (m+1 of them) to emit,
@@ -539,7 +567,7 @@ OM_EXPORT int om_ctrl_rows(om_ctrl* k, int c, int P, int* tok, int* pos, unsigne
  */
 OM_EXPORT int om_ctrl_advance(om_ctrl* k, const int* amax, int* emit, int* rows, int* gstar)
 {
-    const int W = k->W, n1 = k->N - 1;
+    const int n1 = k->N - 1;
     int best_m = 0, best_g = -1;
     for (int g = 0; g < k->Gp; g++) {
         int m = 0;
@@ -557,20 +585,7 @@ OM_EXPORT int om_ctrl_advance(om_ctrl* k, const int* amax, int* emit, int* rows,
         rows[i + 1] = row_vf(k, best_g, i);
     }
     if (gstar) *gstar = best_g;
-
-    /* R6 harvest, j ascending, from the window before the shift */
-    int* val = (int*)malloc(sizeof(int) * n1);
-    for (int j = 0; j < W; j++) {
-        int key = k->win[j];
-        for (int l = 1; l < n1; l++) val[l - 1] = k->win[(size_t)l * W + j];
-        val[n1 - 1] = amax[row_la(k, n1 - 1, j)];
-        om_pool_insert(k, key, val);
-    }
-    free(val);
-    /* R7 window shift */
-    for (int l = 0; l + 1 < n1; l++)
-        memcpy(k->win + (size_t)l * W, k->win + (size_t)(l + 1) * W, sizeof(int) * W);
-    for (int j = 0; j < W; j++) k->win[(size_t)(n1 - 1) * W + j] = amax[row_la(k, n1 - 1, j)];
+    harvest_and_shift(k, amax);
     return best_m + 1;
 }
 
@@ -585,6 +600,124 @@ OM_EXPORT int om_ctrl_pool(const om_ctrl* k, int key, int* out)
 OM_EXPORT void om_ctrl_window(const om_ctrl* k, int* out)
 {
     memcpy(out, k->win, sizeof(int) * (size_t)(k->N - 1) * k->W);
+}
+
+/* --------------------------------------------------------- sampling (R10) */
+
+/* Uniform draw in [0,1): the top 24 bits of the next splitmix64 output. */
+OM_EXPORT double om_uniform(uint64_t* rng) { return (double)(om_splitmix64(rng) >> 40) * (1.0 / 16777216.0); }
+
+/* p = softmax(z / tau) in double: the maximum first, then exp((z - max) /
+ * tau) and their sum in ascending token order. */
+static void softmax_tau(const float* z, int V, float tau, double* p)
+{
+    float mx = z[0];
+    for (int v = 1; v < V; v++)
+        if (z[v] > mx) mx = z[v];
+    double sum = 0.0;
+    for (int v = 0; v < V; v++) {
+        p[v] = exp(((double)z[v] - (double)mx) / (double)tau);
+        sum += p[v];
+    }
+    for (int v = 0; v < V; v++) p[v] /= sum;
+}
+
+static int in_list(const int* a, int n, int x)
+{
+    for (int i = 0; i < n; i++)
+        if (a[i] == x) return 1;
+    return 0;
+}
+
+/* Draw from p restricted to the tokens not in excl[0..ne-1] (whose mass is
+ * mass_excl): the first token, in ascending order, whose running sum of p
+ * exceeds u * (1 - mass_excl); the last admissible token of nonzero mass if
+ * rounding leaves the target unreached. */
+static int draw_excluding(const double* p, int V, const int* excl, int ne, double mass_excl, double u)
+{
+    const double target = u * (1.0 - mass_excl);
+    double acc = 0.0;
+    int last = -1;
+    for (int v = 0; v < V; v++) {
+        if (in_list(excl, ne, v)) continue;
+        if (p[v] > 0.0) last = v;
+        acc += p[v];
+        if (acc > target) return v;
+    }
+    return last >= 0 ? last : 0;
+}
+
+/* n plain draws from softmax(z / tau) (the primitive every sampled token
+ * goes through). */
+OM_EXPORT void om_sample_logits(const float* z, int V, float tau, uint64_t* rng, int n, int* out)
+{
+    double* p = (double*)malloc(sizeof(double) * V);
+    softmax_tau(z, V, tau, p);
+    for (int i = 0; i < n; i++) out[i] = draw_excluding(p, V, NULL, 0, 0.0, om_uniform(rng));
+    free(p);
+}
+
+/*
+ * R10 + R6/R7 after the forward of the rows built by the last om_ctrl_rows
+ * call.  logits: [T][V] of every row.  Verification by sampling (one uniform
+ * per candidate try, one per drawn token, in the order below); the
+ * lookahead branch's harvest and shift use the rows' argmaxes as in R6/R7.
+ * Writes the emitted tokens and the rows whose KV is committed; returns m+1.
+ */
+OM_EXPORT int om_ctrl_advance_sample(om_ctrl* k, const float* logits, float tau, uint64_t* rng, int* emit,
+                                     int* rows, int* gstar)
+{
+    const int V = k->V, n1 = k->N - 1, Gp = k->Gp;
+    double* p = (double*)malloc(sizeof(double) * V);
+    int* alive = (int*)malloc(sizeof(int) * (Gp > 0 ? Gp : 1));
+    int* rej = (int*)malloc(sizeof(int) * (Gp > 0 ? Gp : 1));
+    int* amax = (int*)malloc(sizeof(int) * k->T);
+    for (int r = 0; r < k->T; r++) amax[r] = argmax_row(logits + (size_t)r * V, V);
+    for (int g = 0; g < Gp; g++) alive[g] = 1;
+    int row = 0, m = 0, g_best = -1, done = 0;
+    rows[0] = 0;
+    for (int i = 0; i < n1 && !done; i++) {
+        softmax_tau(logits + (size_t)row * V, V, tau, p);
+        int nrej = 0, acc_g = -1;
+        double mass_rej = 0.0;
+        for (int g = 0; g < Gp && acc_g < 0; g++) {
+            if (!alive[g]) continue;
+            const int v = k->cands[(size_t)g * n1 + i];
+            if (in_list(rej, nrej, v)) continue;  /* a value already tried at this level */
+            const double u = om_uniform(rng);
+            if (u * (1.0 - mass_rej) < p[v]) {
+                acc_g = g;
+            } else {
+                rej[nrej++] = v;
+                mass_rej += p[v];
+            }
+        }
+        if (acc_g < 0) {
+            emit[m] = draw_excluding(p, V, rej, nrej, mass_rej, om_uniform(rng));
+            done = 1;
+            break;
+        }
+        const int v = k->cands[(size_t)acc_g * n1 + i];
+        emit[m] = v;
+        for (int g = 0; g < Gp; g++)
+            if (alive[g] && k->cands[(size_t)g * n1 + i] != v) alive[g] = 0;
+        g_best = acc_g;  /* the lowest candidate still alive */
+        row = row_vf(k, g_best, i);
+        m++;
+    }
+    /* committed rows: row 0 and the accepted levels of the lowest candidate
+     * alive at the end (every candidate alive at a level has the same
+     * visible tokens there, so its rows hold the same keys and values) */
+    for (int i = 0; i < m; i++) rows[i + 1] = row_vf(k, g_best, i);
+    if (!done) {
+        /* every level accepted: the bonus token from the last accepted row */
+        softmax_tau(logits + (size_t)row * V, V, tau, p);
+        emit[m] = draw_excluding(p, V, NULL, 0, 0.0, om_uniform(rng));
+    }
+    if (gstar) *gstar = g_best;
+    harvest_and_shift(k, amax);
+    free(p); free(alive); free(rej); free(amax);
+    return m + 1;
 }
 
 /* ---------------------------------------------------------------- lookahead */
@@ -628,6 +761,80 @@ OM_EXPORT int om_lookahead(const om_model* m, const int* prompt, int len, int W,
     }
     if (steps_out) *steps_out = steps;
     free(tok); free(pos); free(amax); free(vis);
+    om_ctrl_free(k);
+    om_seq_free(s);
+    return rc;
+}
+
+/* ------------------------------------------------------ sampled decoding */
+
+/* Plain ancestral sampling (the definition the sampled lookahead must match
+ * in distribution): like om_greedy, with each token drawn from
+ * softmax(logits / tau) by om_sample_logits' rule, one uniform per token from
+ * the splitmix64 stream seeded with rng_seed. */
+OM_EXPORT int om_sample_decode(const om_model* m, const int* prompt, int len, int max_new, int max_seq, float tau,
+                               uint64_t rng_seed, int* out)
+{
+    if (len < 1 || max_new < 0 || len - 1 + max_new > max_seq || !(tau > 0.0f)) return -1;
+    om_seq* s = om_seq_new(m, max_seq);
+    if (!s) return -1;
+    int rc = om_prefill(s, 0, prompt, len - 1);
+    float* z = (float*)malloc(sizeof(float) * m->vocab);
+    int c = prompt[len - 1], P = len - 1, a = 0;
+    const unsigned char one = 1;
+    uint64_t rng = rng_seed;
+    for (int t = 0; t < max_new && !rc; t++) {
+        rc = om_step_forward(s, P, 1, &c, &P, &one, z, &a);
+        if (rc) break;
+        const int row0 = 0;
+        rc = om_commit(s, P, 1, &row0);
+        om_sample_logits(z, m->vocab, tau, &rng, 1, &out[t]);
+        c = out[t];
+        P++;
+    }
+    free(z);
+    om_seq_free(s);
+    return rc;
+}
+
+/* Lookahead decoding with sampling verification (R10): as om_lookahead, the
+ * verification drawing from softmax(logits / tau) with the splitmix64 stream
+ * seeded with rng_seed. */
+OM_EXPORT int om_lookahead_sample(const om_model* m, const int* prompt, int len, int W, int N, int G, uint64_t seed,
+                                  int preseed, float tau, uint64_t rng_seed, int max_new, int max_seq, int* out,
+                                  int* steps_out, int* accept_hist)
+{
+    if (len < 1 || max_new < 0 || !(tau > 0.0f)) return -1;
+    if (len - 1 + max_new + W + N > max_seq) return -1;
+    om_ctrl* k = om_ctrl_new(W, N, G, m->vocab);
+    om_seq* s = om_seq_new(m, max_seq);
+    if (!k || !s) return -1;
+    om_ctrl_init(k, prompt, len, seed, preseed);
+    int rc = om_prefill(s, 0, prompt, len - 1);
+    int Tmax = om_ctrl_rows_max(k);
+    int* tok = (int*)malloc(sizeof(int) * Tmax);
+    int* pos = (int*)malloc(sizeof(int) * Tmax);
+    int* amax = (int*)malloc(sizeof(int) * Tmax);
+    float* logits = (float*)malloc(sizeof(float) * (size_t)Tmax * m->vocab);
+    unsigned char* vis = (unsigned char*)malloc((size_t)Tmax * Tmax);
+    int emit[64], rows[64];
+    int c = prompt[len - 1], P = len - 1, n = 0, steps = 0;
+    uint64_t rng = rng_seed;
+    if (accept_hist) memset(accept_hist, 0, sizeof(int) * (N + 1));
+    while (n < max_new && !rc) {
+        int T = om_ctrl_rows(k, c, P, tok, pos, vis);
+        rc = om_step_forward(s, P, T, tok, pos, vis, logits, amax);
+        if (rc) break;
+        int ne = om_ctrl_advance_sample(k, logits, tau, &rng, emit, rows, NULL);
+        rc = om_commit(s, P, ne, rows);
+        for (int i = 0; i < ne && n < max_new; i++) out[n++] = emit[i];
+        if (accept_hist) accept_hist[ne]++;
+        P += ne;
+        c = emit[ne - 1];
+        steps++;
+    }
+    if (steps_out) *steps_out = steps;
+    free(tok); free(pos); free(amax); free(logits); free(vis);
     om_ctrl_free(k);
     om_seq_free(s);
     return rc;
