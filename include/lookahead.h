@@ -136,6 +136,25 @@ LA_API int la_prefill(la_ctx* ctx, const int32_t* prompt, int len);
  * step (P + W + N > max_seq); LA_ERR_STATE before la_prefill. */
 LA_API int la_step(la_ctx* ctx, int32_t* out, int cap, int* n_out);
 
+/* Sampling verification (temperature sampling, lossless in distribution;
+ * the method's summary page says sampling is supported and the output
+ * distribution kept, without giving the rule).  temperature > 0: every
+ * emitted token is drawn from softmax(logits / temperature) of its row.  At
+ * each candidate level the distinct candidate tokens v are tried in
+ * candidate order, v accepted with probability p(v) / (1 - mass of the
+ * values already rejected at that level).  If none is accepted, the token
+ * is drawn from p without the rejected values.  After the last level a bonus
+ * token is drawn.  The uniforms are the top 24 bits of a splitmix64 stream
+ * seeded with `seed`, one per candidate try and one per drawn token.
+ * temperature <= 0 restores greedy verification.  The lookahead branch
+ * keeps using argmaxes either way.  Takes effect at the next la_step (the
+ * step is captured again); la_prefill keeps the stream's position.  Costs
+ * the logits of the step in device memory (already in the workspace) and a
+ * row-statistics kernel per step.  LA_ERR_ARG for a NULL context or a
+ * non-finite temperature; LA_ERR_CUDA if the stream state cannot be
+ * written. */
+LA_API int la_set_sampling(la_ctx* ctx, float temperature, uint64_t seed);
+
 /* la_prefill, then la_step until max_new tokens; out: HOST int32[max_new]
  * receives exactly min(max_new, emitted) tokens, count in *n_out. */
 LA_API int la_generate(la_ctx* ctx, const int32_t* prompt, int len, int max_new, int32_t* out, int* n_out);

@@ -24,7 +24,7 @@ LA_OK, LA_ERR_ARG, LA_ERR_OOM, LA_ERR_CAPACITY, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_
 LA_FP32, LA_BF16 = 0, 1
 LA_PRESEED_PROMPT, LA_DEBUG_LOGITS, LA_NO_GRAPH, LA_SIMT, LA_PROFILE = 1, 2, 4, 8, 16
 
-EXPORTS = ("la_workspace_bytes", "la_create", "la_prefill", "la_step", "la_generate", "la_get_stats",
+EXPORTS = ("la_workspace_bytes", "la_create", "la_prefill", "la_step", "la_generate", "la_set_sampling", "la_get_stats",
            "la_get_profile",
            "la_debug_logits", "la_debug_argmax", "la_debug_rows", "la_debug_pool", "la_debug_window",
            "la_last_error", "la_destroy", "la_attention", "la_attention_noalloc", "la_pool_create", "la_pool_insert", "la_pool_lookup", "la_pool_size",
@@ -74,6 +74,7 @@ def lib():
             "la_prefill": (i32, [vp, vp, i32]),
             "la_step": (i32, [vp, vp, i32, vp]),
             "la_generate": (i32, [vp, vp, i32, i32, vp, vp]),
+            "la_set_sampling": (i32, [vp, C.c_float, u64]),
             "la_get_stats": (i32, [vp, vp]),
             "la_get_profile": (i32, [vp, vp, i32, vp]),
             "la_debug_logits": (i32, [vp, vp, sz]),
@@ -133,6 +134,10 @@ def la_step(ctx, N: int = 8) -> np.ndarray:
     n = C.c_int()
     _check(ctx, lib().la_step(ctx, _p(out), len(out), C.byref(n)))
     return out[: n.value].copy()
+
+
+def la_set_sampling(ctx, temperature: float, seed: int) -> None:
+    _check(ctx, lib().la_set_sampling(ctx, float(temperature), int(seed)))
 
 
 def la_generate(ctx, prompt, max_new: int) -> np.ndarray:
@@ -305,6 +310,10 @@ class Decoder:
 
     def step(self):
         return la_step(self.ctx, self.N)
+
+    def set_sampling(self, temperature: float, seed: int):
+        """Sampling verification at this temperature (<= 0: greedy)."""
+        la_set_sampling(self.ctx, temperature, seed)
 
     def generate(self, prompt, max_new: int):
         return la_generate(self.ctx, prompt, max_new)

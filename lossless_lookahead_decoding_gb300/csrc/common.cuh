@@ -24,6 +24,7 @@ struct DState {
     int emit[kMaxN];
     int commit_rows[kMaxN];
     long long steps;
+    unsigned long long rng;  // sampling verification: splitmix64 stream state
 };
 
 // Static description of which in-step row provides the key at each position
@@ -116,7 +117,9 @@ void launch_build_rows(cudaStream_t s, DState* st, const int* win, PoolView pool
 void launch_prefill_rows(cudaStream_t s, const DState* st, const int* prompt, int P0, int n, int* tok,
                          int* pos);
 void launch_verify_update(cudaStream_t s, DState* st, const int* tok, const int* amax, int* win,
-                          PoolView pool, int W, int N, int G);
+                          PoolView pool, int W, int N, int G, const float* logits, int V, float tau,
+                          const double* stats);
+void launch_row_stats(cudaStream_t s, const float* logits, int V, float tau, int vbase, int T, double* stats);
 void launch_commit(cudaStream_t s, const DState* st, bool prefill, int n_prefill, int n_max, const void* KS,
                    const void* VS, void* KC, void* VC, int L, int Hkv, int hd, int max_seq, int esz);
 void launch_pool_reset(cudaStream_t s, PoolView pool);

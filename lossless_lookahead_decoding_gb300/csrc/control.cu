@@ -1,6 +1,7 @@
 // control.cu -- integer kernels of the lookahead step: row assembly with the
-// pool lookup, greedy verification + n-gram harvest + window shift, KV commit,
-// and the GPU n-gram pool (hash table) with warp-cooperative lookup/insert.
+// pool lookup, greedy (or sampling) verification + n-gram harvest + window
+// shift, KV commit, and the GPU n-gram pool (hash table) with
+// warp-cooperative lookup/insert.
 //
 // Method: Fu et al. 2024, "Break the Sequential Dependency of LLM Inference
 // Using Lookahead Decoding" (summary page, "Summary"): a lookahead branch over
@@ -244,6 +245,73 @@ void launch_prefill_rows(cudaStream_t s, const DState* st, const int* prompt, in
     k_prefill_rows<<<1, 128, 0, s>>>(st, prompt, P0, n, tok, pos);
 }
 
+
+// ------------------------------------------------- sampling verification ---
+//
+// The summary page says the method supports sampling and keeps the output
+// distribution; it gives no algorithm.  The rule used here: p = softmax(z /
+// tau) of a row.  At each level, the distinct values of the still-matching
+// candidates are tried in candidate order, value v accepted with probability
+// p(v) / (1 - mass of the values already rejected at this level); if none is
+// accepted the token is drawn from p without the rejected values.  The
+// acceptance probabilities telescope, so every emitted token is distributed
+// exactly as its row's softmax.  After the last level a bonus token is drawn
+// from the last accepted row.  One uniform per candidate try and one per
+// drawn token, in that order, from a splitmix64 stream in the decode state.
+
+// splitmix64 (S. Vigna's published generator): add the golden gamma, then
+// two xor-shift-multiply rounds and a final xor-shift.
+__device__ __forceinline__ unsigned long long smix64(unsigned long long* x)
+{
+    unsigned long long z = (*x += 0x9E3779B97F4A7C15ull);
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+// Uniform in [0,1): the top 24 bits of the next output.
+__device__ __forceinline__ double uniform24(unsigned long long* x) { return (double)(smix64(x) >> 40) * (1.0 / 16777216.0); }
+
+// Row max and sum of exp((z - max) / tau) in fp64 for row 0 (block 0) and the
+// verification rows vbase.. (blocks 1..): the rows whose softmax sampling
+// verification reads.  stats[2r] = max, stats[2r+1] = sum.
+constexpr int kStatThreads = 256;
+
+__global__ void __launch_bounds__(kStatThreads) k_row_stats(const float* __restrict__ logits, int V, float tau,
+                                                           int vbase, double* __restrict__ stats)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int r = blockIdx.x == 0 ? 0 : vbase + blockIdx.x - 1;
+    const float* z = logits + (size_t)r * V;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __shared__ float s_m[kStatThreads / 32];
+    __shared__ double s_s[kStatThreads / 32];
+    float mx = -INFINITY;
+    for (int v = threadIdx.x; v < V; v += kStatThreads) mx = fmaxf(mx, z[v]);
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) s_m[warp] = mx;
+    __syncthreads();
+    mx = s_m[0];
+    for (int w = 1; w < kStatThreads / 32; w++) mx = fmaxf(mx, s_m[w]);
+    double sum = 0.0;
+    for (int v = threadIdx.x; v < V; v += kStatThreads) sum += exp(((double)z[v] - (double)mx) / (double)tau);
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) s_s[warp] = sum;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int w = 0; w < kStatThreads / 32; w++) t += s_s[w];
+        stats[2 * r] = mx;
+        stats[2 * r + 1] = t;
+    }
+}
+
+void launch_row_stats(cudaStream_t s, const float* logits, int V, float tau, int vbase, int T, double* stats)
+{
+    launch_pdl(k_row_stats, dim3(1 + T - vbase), dim3(kStatThreads), 0, s, logits, V, tau, vbase, stats);
+}
+
 // ------------------------------------------------- verify + harvest + shift ---
 
 // One warp.  Verification: for each candidate g < G', m_g = number of leading
@@ -262,14 +330,174 @@ void launch_prefill_rows(cudaStream_t s, const DState* st, const int* prompt, in
 // Then every thread shifts the window (after all harvest reads of it).
 constexpr int kVerifyWarps = 32;  // window columns harvested at once (W <= kMaxW handled in rounds)
 
-__global__ void __launch_bounds__(kVerifyWarps * 32) k_verify_update(DState* st, const int* tok, const int* amax,
-                                                                     int* win, PoolView pool, int W, int N, int G)
+// Draw from softmax(z / tau) (row max mx, exp-sum S) restricted to the
+// tokens not in rej[0..nrej): the first token, in ascending order, whose
+// running sum of probabilities exceeds target; the last admissible token of
+// nonzero probability if rounding leaves target unreached.  Every thread of
+// the block takes part (a contiguous chunk of tokens each, chunks summed by a
+// block scan in fp64).
+__device__ int block_draw(const float* z, int V, float tau, double mx, double S, const int* rej, int nrej,
+                          double target)
+{
+    __shared__ double s_part[kVerifyWarps];
+    __shared__ int s_pick, s_last;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x;
+    const int chunk = (V + nt - 1) / nt, v0 = min(tid * chunk, V), v1 = min(v0 + chunk, V);
+    auto prob = [&](int v) -> double {
+        for (int k = 0; k < nrej; k++)
+            if (rej[k] == v) return 0.0;
+        return exp(((double)z[v] - mx) / (double)tau) / S;
+    };
+    double loc = 0.0;
+    int last = -1;
+    for (int v = v0; v < v1; v++) {
+        const double p = prob(v);
+        loc += p;
+        if (p > 0.0) last = v;
+    }
+    double x = loc;  // inclusive scan within the warp
+    for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_part[warp] = x;
+    if (tid == 0) {
+        s_pick = INT_MAX;
+        s_last = -1;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        double y = lane < nt / 32 ? s_part[lane] : 0.0;
+        for (int o = 1; o < 32; o <<= 1) {
+            const double t = __shfl_up_sync(0xffffffffu, y, o);
+            if (lane >= o) y += t;
+        }
+        s_part[lane] = y;
+    }
+    __syncthreads();
+    const double pre = (warp ? s_part[warp - 1] : 0.0) + x - loc;  // mass of the tokens before this chunk
+    if (last >= 0) atomicMax(&s_last, last);
+    if (pre + loc > target) {
+        double acc = pre;
+        for (int v = v0; v < v1; v++) {
+            acc += prob(v);
+            if (acc > target) {
+                atomicMin(&s_pick, v);
+                break;
+            }
+        }
+    }
+    __syncthreads();
+    const int r = s_pick != INT_MAX ? s_pick : (s_last >= 0 ? s_last : 0);
+    __syncthreads();
+    return r;
+}
+
+// Sampling verification of one step (all threads of the block): writes the
+// emitted tokens, committed rows and the advanced decode state, like the
+// greedy branch of k_verify_update.
+__device__ void sample_verify(DState* st, const int* tok, const float* logits, int V, float tau,
+                              const double* stats, int W, int N)
+{
+    __shared__ unsigned char s_alive[kRows];
+    __shared__ int s_rej[kRows];
+    __shared__ int s_nrej, s_acc, s_row, s_m, s_done, s_gbest, s_emit[kMaxN];
+    __shared__ double s_target;
+    __shared__ unsigned long long s_rng;
+    const int tid = threadIdx.x, n1 = N - 1, ncand = st->ncand, vbase = 1 + W * n1;
+    if (tid == 0) {
+        s_rng = st->rng;
+        s_row = 0;
+        s_m = 0;
+        s_done = 0;
+        s_gbest = -1;
+    }
+    for (int g = tid; g < kRows; g += blockDim.x) s_alive[g] = g < ncand;
+    __syncthreads();
+    for (int i = 0; i < n1; i++) {
+        if (tid == 0) {
+            const int row = s_row;
+            const float* z = logits + (size_t)row * V;
+            const double mx = stats[2 * row], S = stats[2 * row + 1];
+            int nrej = 0, acc = -1;
+            double R = 0.0;
+            for (int g = 0; g < ncand && acc < 0; g++) {
+                if (!s_alive[g]) continue;
+                const int v = tok[vbase + g * n1 + i];
+                bool seen = false;
+                for (int k = 0; k < nrej; k++) seen = seen || s_rej[k] == v;
+                if (seen) continue;  // a value already tried at this level
+                const double u = uniform24(&s_rng);
+                const double pv = exp(((double)z[v] - mx) / (double)tau) / S;
+                if (u * (1.0 - R) < pv) {
+                    acc = g;
+                } else {
+                    s_rej[nrej++] = v;
+                    R += pv;
+                }
+            }
+            s_acc = acc;
+            s_nrej = nrej;
+            if (acc < 0) s_target = uniform24(&s_rng) * (1.0 - R);
+        }
+        __syncthreads();
+        if (s_acc < 0) {
+            const int row = s_row;
+            const int v = block_draw(logits + (size_t)row * V, V, tau, stats[2 * row], stats[2 * row + 1], s_rej,
+                                     s_nrej, s_target);
+            if (tid == 0) {
+                s_emit[s_m] = v;
+                s_done = 1;
+            }
+            __syncthreads();
+            break;
+        }
+        if (tid == 0) {
+            const int g = s_acc, v = tok[vbase + g * n1 + i];
+            s_emit[s_m] = v;
+            for (int h = 0; h < ncand; h++)
+                if (s_alive[h] && tok[vbase + h * n1 + i] != v) s_alive[h] = 0;
+            s_gbest = g;  // the lowest candidate still matching
+            s_row = vbase + g * n1 + i;
+            s_m = s_m + 1;
+        }
+        __syncthreads();
+    }
+    if (!s_done) {
+        if (tid == 0) s_target = uniform24(&s_rng);
+        __syncthreads();
+        const int row = s_row;
+        const int v = block_draw(logits + (size_t)row * V, V, tau, stats[2 * row], stats[2 * row + 1], nullptr, 0,
+                                 s_target);
+        if (tid == 0) s_emit[s_m] = v;
+        __syncthreads();
+    }
+    if (tid == 0) {
+        const int m = s_m, gs = s_gbest, P = st->P;
+        for (int k = 0; k <= m; k++) st->emit[k] = s_emit[k];
+        st->commit_rows[0] = 0;
+        for (int k = 0; k < m; k++) st->commit_rows[k + 1] = vbase + gs * n1 + k;
+        st->n_emit = m + 1;
+        st->gstar = gs;
+        st->P_before = P;
+        st->P = P + m + 1;
+        st->c = s_emit[m];
+        st->steps += 1;
+        st->rng = s_rng;
+    }
+}
+
+__global__ void __launch_bounds__(kVerifyWarps * 32)
+    k_verify_update(DState* st, const int* tok, const int* amax, int* win, PoolView pool, int W, int N, int G,
+                    const float* logits, int V, float tau, const double* stats)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int n1 = N - 1, ncand = st->ncand, P = st->P;
     const int a0 = amax[0];
     const int vbase = 1 + W * n1;
-    if (warp == 0) {
+    if (tau > 0.f) {
+        sample_verify(st, tok, logits, V, tau, stats, W, N);
+    } else if (warp == 0) {
         int best = -1;  // (m << 16) | (0xffff - g)
         for (int g0 = 0; g0 < ncand; g0 += 32) {
             int g = g0 + lane, key = -1;
@@ -349,9 +577,9 @@ __global__ void __launch_bounds__(kVerifyWarps * 32) k_verify_update(DState* st,
 }
 
 void launch_verify_update(cudaStream_t s, DState* st, const int* tok, const int* amax, int* win, PoolView pool,
-                          int W, int N, int G)
+                          int W, int N, int G, const float* logits, int V, float tau, const double* stats)
 {
-    k_verify_update<<<1, kVerifyWarps * 32, 0, s>>>(st, tok, amax, win, pool, W, N, G);
+    k_verify_update<<<1, kVerifyWarps * 32, 0, s>>>(st, tok, amax, win, pool, W, N, G, logits, V, tau, stats);
 }
 
 // ------------------------------------------------------------------ commit ---

@@ -55,6 +55,8 @@ struct la_ctx {
     std::vector<const void*> lw;
     int W = 0, N = 2, G = 0, T = 1, flags = 0;
     uint64_t seed = 0;
+    float tau = 0.f;              // > 0: sampling verification at this temperature
+    double* SSTAT = nullptr;      // per-row softmax max / exp-sum for sampling
     cudaStream_t s = nullptr;
     bool bf16 = false, use_tc = false, use_attn_mma = false;
     float* attn_part = nullptr;
@@ -159,6 +161,7 @@ static Layout make_layout(const la_model_desc* d, int W, int N, int G, int* pool
     ly.add((2 * kRows + 1) * 4);                         // 28 step group lists
     ly.add((2 * kRows + 1) * 4);                         // 29 prefill group lists
     ly.add(attn_mma_partial_bytes(d->n_heads, d->head_dim, d->max_seq));  // 30 attention split partials
+    ly.add(kRows * 16);                                  // 31 sampling row statistics
     return ly;
 }
 
@@ -303,7 +306,8 @@ static void forward(la_ctx* c, int rows, const RowSet& rs, bool logits)
             c->prof.end(s, P_NORM, 0, 0);
         }
         if (c->use_tc) {
-            tc_lmhead_argmax(c->tc, s, rows, (c->flags & LA_DEBUG_LOGITS) ? c->LOGITS : nullptr, c->AMAXP, c->AMAX);
+            tc_lmhead_argmax(c->tc, s, rows, ((c->flags & LA_DEBUG_LOGITS) || c->tau > 0.f) ? c->LOGITS : nullptr,
+                             c->AMAXP, c->AMAX);
         } else {
             launch_gemm_simt_f32out<T>(s, XN, (const T*)d.lm_head, c->LOGITS, d.vocab, rows, D, d.vocab);
             launch_argmax(s, c->LOGITS, c->AMAX, rows, d.vocab);
@@ -326,7 +330,10 @@ static void enqueue_step(la_ctx* c)
     c->prof.end(c->s, P_CONTROL, 0, 0);
     run_forward(c, c->T, c->rs_step, true);
     c->prof.begin(c->s);
-    launch_verify_update(c->s, c->st, c->tok, c->AMAX, c->win, c->pool, c->W, c->N, c->G);
+    const int vbase = 1 + c->W * (c->N - 1);
+    if (c->tau > 0.f) launch_row_stats(c->s, c->LOGITS, c->d.vocab, c->tau, vbase, c->T, c->SSTAT);
+    launch_verify_update(c->s, c->st, c->tok, c->AMAX, c->win, c->pool, c->W, c->N, c->G, c->LOGITS, c->d.vocab,
+                         c->tau, c->SSTAT);
     launch_commit(c->s, c->st, false, 0, c->N, c->KS, c->VS, c->KC, c->VC, c->d.n_layers, c->d.n_kv_heads,
                   c->d.head_dim, c->d.max_seq, c->esz);
     c->prof.end(c->s, P_CONTROL, 0, 0);
@@ -445,6 +452,7 @@ extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* w
     ctx->st = (DState*)(b + ly.off[25]);
     ctx->dbg = (int*)(b + ly.off[26]);
     ctx->AMAXP = (unsigned long long*)(b + ly.off[27]);
+    ctx->SSTAT = (double*)(b + ly.off[31]);
     ctx->pool = PoolView{pk, pk + cap, (int*)(b + ly.off[23]), pk + 2 * cap, (int*)(b + ly.off[24]),
                          &ctx->st->status, cap, lg, G, N - 1};
     int* gl1 = (int*)(b + ly.off[28]);
@@ -639,6 +647,21 @@ extern "C" int la_step(la_ctx* ctx, int32_t* out, int cap, int* n_out)
     ctx->stats.last_step_ms = ms;
     ctx->stats.kernels_per_step = ctx->kernels_per_step;
     if (ctx->prof.on) collect_profile(ctx, h.P_before);
+    return LA_OK;
+}
+
+extern "C" int la_set_sampling(la_ctx* ctx, float temperature, uint64_t seed)
+{
+    if (!ctx) return LA_ERR_ARG;
+    if (temperature != temperature || temperature > 3.0e38f) return fail(ctx, LA_ERR_ARG, "temperature must be finite");
+    ctx->tau = temperature > 0.f ? temperature : 0.f;
+    const unsigned long long v = seed;
+    LA_CK(cudaMemcpyAsync(&ctx->st->rng, &v, sizeof(v), cudaMemcpyHostToDevice, ctx->s));
+    LA_CK(cudaStreamSynchronize(ctx->s));
+    if (ctx->gexec) {  // the step's launch sequence changes: capture it again
+        cudaGraphExecDestroy(ctx->gexec);
+        ctx->gexec = nullptr;
+    }
     return LA_OK;
 }
 
