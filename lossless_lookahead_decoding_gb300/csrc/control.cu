@@ -314,20 +314,6 @@ void launch_row_stats(cudaStream_t s, const float* logits, int V, float tau, int
 
 // ------------------------------------------------- verify + harvest + shift ---
 
-// One warp.  Verification: for each candidate g < G', m_g = number of leading
-// candidate tokens equal to the model's greedy choice at that point (the
-// argmax of row 0 for the first, of row (g,i-1) for the i-th); take the
-// largest m, lowest g on ties; emit argmax(row 0) followed by the argmaxes of
-// the m accepted rows.  Harvest: for j ascending insert key win[0][j] ->
-// (win[1..N-2][j], argmax of row (N-2,j)).  Then shift the window up one
-// level with those argmaxes as the new last level.  Finally advance P and c.
-// Verification, n-gram harvest and window shift of one step.  Warp 0
-// verifies (longest accepted prefix, lowest g on ties) and updates the decode
-// state.  Harvest: warp j claims the slot of window column j's key; each key's
-// lowest column then inserts that key's n-grams in ascending column order, so
-// the pool holds what inserting columns 0..W-1 one after another gives (only
-// the physical slot of colliding keys may differ, which lookups do not see).
-// Then every thread shifts the window (after all harvest reads of it).
 constexpr int kVerifyWarps = 32;  // window columns harvested at once (W <= kMaxW handled in rounds)
 
 // Draw from softmax(z / tau) (row max mx, exp-sum S) restricted to the
@@ -487,6 +473,21 @@ __device__ void sample_verify(DState* st, const int* tok, const float* logits, i
     }
 }
 
+// Verification, n-gram harvest and window shift of one step.
+// Greedy verification (tau <= 0, warp 0): for each candidate g < G', m_g =
+// the number of leading candidate tokens equal to the model's greedy choice
+// at that point (the argmax of row 0 for the first, of row (g,i-1) for the
+// i-th); the largest m wins, lowest g on ties; emit argmax(row 0) and the
+// argmaxes of the m accepted rows.  Sampling verification (tau > 0, the
+// whole block): sample_verify above.  Either way the decode state advances
+// (P, c, emitted tokens, committed rows).  Harvest, from the window before
+// the shift: warp j claims the slot of window column j's key; each key's
+// lowest column then inserts that key's n-grams (win[1..N-2][j], argmax of
+// row (N-2,j)) in ascending column order, so the pool holds what inserting
+// columns 0..W-1 one after another gives (only the physical slot of
+// colliding keys may differ, which lookups do not see).  Then every thread
+// shifts the window up one level, the last level becoming the argmaxes of
+// the last level's rows.
 __global__ void __launch_bounds__(kVerifyWarps * 32)
     k_verify_update(DState* st, const int* tok, const int* amax, int* win, PoolView pool, int W, int N, int G,
                     const float* logits, int V, float tau, const double* stats)
