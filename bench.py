@@ -359,7 +359,10 @@ SWEEP = [(0, 2, 0, False),                                     # greedy
          (0, 3, 4, True), (0, 5, 4, True),                      # prompt lookup: no window, prompt n-grams
          (5, 5, 5, False), (7, 5, 7, False), (10, 5, 10, False), (15, 5, 15, False),
          (15, 3, 15, False), (31, 3, 31, False), (20, 4, 20, False), (10, 7, 10, False),
-         (15, 5, 15, True)]
+         (15, 5, 15, True),
+         # branch balance at T = 121 (W + G = 30, N = 5): lopsided to balanced
+         (28, 5, 2, False), (25, 5, 5, False), (20, 5, 10, False), (10, 5, 20, False), (5, 5, 25, False),
+         (2, 5, 28, False)]
 
 
 def run_sweep(args, rank, world):

@@ -197,6 +197,14 @@ def test_lossless_tiny_workload(bf16):
     assert steps < 64  # some candidate was accepted on the planted-span prompt
 
 
+@pytest.mark.parametrize("W,G", [(28, 2), (25, 5), (20, 10), (15, 15), (10, 20), (5, 25), (2, 28)])
+def test_lossless_branch_balance_at_121_rows(W, G):
+    """The branch-balance splits of the sweep (W + G = 30, N = 5, T = 121 rows,
+    the 7B step's row count) on the tiny model: lossless at every split."""
+    steps, hist = _lossless(I.MODELS["tiny"], False, W, 5, G, 2, 64, I.make_prompt("tiny"))
+    assert 1 + (W + G) * 4 == 121 and steps < 64
+
+
 def test_lossless_random_cases():
     g = np.random.default_rng(123)
     for case in range(40):
