@@ -40,3 +40,29 @@ def test_product_path_does_not_reference_oracle():
             if fn.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 src = open(os.path.join(dirpath, fn)).read()
                 assert "import oracle" not in src and "from oracle" not in src and "liboracle" not in src, fn
+
+
+def test_workspace_bytes_is_host_only_and_checks_shapes():
+    """la_workspace_bytes needs no GPU: it holds at least the bf16 KV cache
+    (2 x L x d_kv x max_seq x 2 bytes, growing with max_seq at that rate) and
+    returns 0 for a shape the library refuses."""
+    import lossless_lookahead_decoding_gb300 as LA
+    from helpers import build_lib
+    build_lib()
+
+    def desc(**kw):
+        f = dict(n_layers=32, d_model=4096, n_heads=32, n_kv_heads=32, head_dim=128, ffn=11008,
+                 vocab=32000, max_seq=804, rms_eps=1e-5, rope_theta=1e4, dtype=LA.LA_BF16,
+                 emb=1, layer_w=1, final_norm=1, lm_head=1, stream=None)
+        f.update(kw)
+        return LA.la_model_desc(**f)
+
+    kv = lambda m: 2 * 32 * 32 * 128 * m * 2
+    ws = LA.la_workspace_bytes(desc(), 15, 5, 15)
+    assert kv(804) <= ws < kv(804) + (1 << 30)
+    assert LA.la_workspace_bytes(desc(max_seq=804 + 1024), 15, 5, 15) - ws >= kv(1024)
+    assert LA.la_workspace_bytes(desc(dtype=LA.LA_FP32), 15, 5, 15) > ws  # fp32 cache and activations
+    for bad, wng in [(dict(head_dim=96), (15, 5, 15)), (dict(n_kv_heads=3), (15, 5, 15)),
+                     (dict(d_model=4000), (15, 5, 15)), (dict(emb=None), (15, 5, 15)),
+                     (dict(), (40, 5, 0)), (dict(), (4, 1, 4)), (dict(), (4, 9, 4)), (dict(), (-1, 5, 2))]:
+        assert LA.la_workspace_bytes(desc(**bad), *wng) == 0, (bad, wng)
