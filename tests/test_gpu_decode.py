@@ -118,3 +118,22 @@ def test_errors_and_capacity():
     assert dec.stats()["P"] + 4 + 3 > 48
     with pytest.raises(LA.LAError):
         gpu_decoder(cfg, w, 1, 40, 5, 40, 256)  # 1 + 80*4 rows > 128
+
+
+def test_profiled_launches_keep_the_output():
+    """The benchmark's profiled pass (LA_PROFILE | LA_NO_GRAPH: CUDA events
+    around every kernel class) emits the same tokens as the graph-launched
+    greedy decode and reports the tensor-core path's kernel classes."""
+    import lossless_lookahead_decoding_gb300 as LA
+    cfg = I.MODELS["tiny"]
+    w = _weights(cfg, True)
+    W, N, G = I.LOOKAHEAD["tiny"]
+    prompt = I.make_prompt("tiny")
+    g = gpu_decoder(cfg, w, 1, 0, 2, 0, 256).generate(prompt, 32)
+    dec = gpu_decoder(cfg, w, 1, W, N, G, 256, flags=LA.LA_PROFILE | LA.LA_NO_GRAPH)
+    assert np.array_equal(dec.generate(prompt, 32), g)
+    prof = dec.profile()
+    for name in ("gemm_qkv", "gemm_o", "gemm_gateup", "gemm_down", "gemm_lmhead", "attention", "control"):
+        assert name in prof and prof[name]["launches"] > 0 and prof[name]["total_ms"] > 0, name
+    assert prof["gemm_qkv"]["bytes"] > 0
+    dec.close()
