@@ -11,7 +11,8 @@ mathematics fix (not against the oracle itself):
 * the pool: replay against a list-of-tuples simulator;
 * reductions: W=G=0 is greedy, G=0 emits one token per step, W=0 with a
   prompt-seeded pool only ever holds prompt n-grams;
-* splitmix64 known-answer outputs.
+* splitmix64 known-answer outputs, the window initialisation (reading R1)
+  and the sampling uniforms written out from them.
 """
 import itertools
 import os
@@ -40,6 +41,42 @@ def test_splitmix64_known_answers():
     for row in _golden("splitmix64_kat.txt"):
         seed, vals = int(row[0]), [int(v) for v in row[1:]]
         assert O.splitmix64_stream(seed, len(vals)) == vals
+
+
+def _kat_stream(seed):
+    for row in _golden("splitmix64_kat.txt"):
+        if int(row[0]) == seed:
+            return [int(v) for v in row[1:]]
+    raise KeyError(seed)
+
+
+@pytest.mark.parametrize("W,N", [(5, 2), (2, 3), (1, 6), (1, 2)])
+def test_window_init_from_the_splitmix64_stream(W, N):
+    """Reading R1, written out from the golden known answers (not from the
+    oracle's generator): win[l][j] = prompt[x_k mod len], x_k the k-th output
+    of the stream seeded with the window seed, k = l*W + j (level-major).  The
+    prompt's tokens are distinct, so a swapped l/j order, an off-by-one in the
+    index or a wrong modulus all change the window."""
+    xs = _kat_stream(1234567)
+    assert len(xs) >= W * (N - 1)
+    prompt = (1000 + 7 * np.arange(97)).astype(np.int32)
+    k = O.Controller(W, N, 0, 2000)
+    k.init(prompt, seed=1234567)
+    expect = np.array([prompt[x % len(prompt)] for x in xs[:W * (N - 1)]], np.int32).reshape(N - 1, W)
+    assert np.array_equal(k.window(), expect)
+    # a one-token prompt fills the whole window with that token
+    k.init(np.array([42], np.int32), seed=1234567)
+    assert (k.window() == 42).all()
+
+
+def test_uniform_is_the_top_24_bits_of_the_stream():
+    """The sampling verification's uniforms: (x >> 40) / 2^24 for the stream's
+    outputs x, written out from the golden known answers."""
+    xs = _kat_stream(1234567)
+    r = O.Rng(1234567)
+    got = [r.uniform() for _ in xs]
+    assert got == [(x >> 40) / 2.0 ** 24 for x in xs]
+    assert all(0.0 <= u < 1.0 for u in got)
 
 
 @pytest.mark.parametrize("row", _golden("page_settings.txt"), ids=lambda r: r[0])

@@ -1,0 +1,173 @@
+"""Why the bf16 GPU parity tests bound single rows at 2e-2 and whole steps at 1e-2.
+
+The bf16 logits bound of the method's GPU checks is a maximum relative L2 error
+of 1e-2 against the fp32 oracle.  The parity tests read it as the relative L2
+error of each step's T x V logits (every step), and bound each single row at
+2e-2.  This test backs that reading with arithmetic, on the CPU: it models the
+bf16 path's rounding points -- fp32 accumulation everywhere, but bf16 storage
+of the normed activations (the GEMM input), of Q, K and V (and so of the KV
+cache), of the attention probabilities fed to the P.V product, of the
+attention output and of the SwiGLU activations -- and compares that model with
+an fp32 model without those roundings (the oracle's arithmetic, up to fp32
+summation order), on the first lookahead step of the 2-layer slice of the
+7B-shaped workload (512-token prompt, W=15 N=5 G=15, 121 rows), the same
+bytes the GPU slice test runs.
+
+What it shows (measured: 0.89e-2 per step, 0.997e-2 for the worst row): the
+rounding alone already takes a single row to the 1e-2 mark, before any of the
+accumulation-order differences that every tensor-core implementation has
+(fused multiply-add trees inside the MMA, split-K partial sums), while the
+step's T x V error stays within 1e-2.  A per-row bound of 1e-2 would thus
+leave no room for the arithmetic of a correct bf16 path; 2e-2 per row keeps
+a margin, and the per-step 1e-2 bound is kept as stated.  Most of it comes
+from the bf16 GEMM inputs (the normed activations alone give 0.63e-2 per
+step), which no bf16 tensor-core GEMM can avoid.  The tiny workload is
+checked the same way.
+"""
+import numpy as np
+import pytest
+
+import la_inputs as I
+import oracle as O
+
+torch = pytest.importorskip("torch")
+
+
+def _rb(t):
+    """Round to bf16 (nearest, ties to even) and back to fp32."""
+    return t.to(torch.bfloat16).to(torch.float32)
+
+
+class Model:
+    """A Llama-style decoder in torch fp32 on the CPU with optional bf16
+    storage at the bf16 path's rounding points."""
+
+    def __init__(self, cfg, w, bf16_points: bool):
+        self.cfg, self.bf = cfg, bf16_points
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+        self.emb, self.lm, self.fnorm = t(w["emb"]), t(w["lm_head"]), t(w["final_norm"])
+        self.layers = [{n: t(w[n][l]) for n in I.LAYER_TENSORS} for l in range(cfg.n_layers)]
+        half = cfg.head_dim // 2
+        p = np.arange(4096, dtype=np.float64)[:, None]
+        ang = p * np.power(float(cfg.rope_theta), -2.0 * np.arange(half) / cfg.head_dim)[None, :]
+        self.cos, self.sin = t(np.cos(ang)), t(np.sin(ang))
+        self.kc = [None] * cfg.n_layers  # [Hkv][P][hd]
+        self.vc = [None] * cfg.n_layers
+
+    def _r(self, x):
+        return _rb(x) if self.bf else x
+
+    def _norm(self, x, w):
+        return self._r(x * torch.rsqrt((x * x).mean(-1, keepdim=True) + self.cfg.rms_eps) * w)
+
+    def _rope(self, x, pos):  # x [T][heads][hd], rotate-half pairing
+        half = self.cfg.head_dim // 2
+        c, s = self.cos[pos][:, None, :], self.sin[pos][:, None, :]
+        a, b = x[..., :half], x[..., half:]
+        return torch.cat([a * c - b * s, b * c + a * s], -1)
+
+    def forward(self, tok, pos, vis, P):
+        """Rows tok at positions pos; row r sees the cache [0, P) and the step
+        rows s with vis[r, s].  Returns (logits, per-layer step K, step V)."""
+        cfg = self.cfg
+        T, H, Hkv, hd = len(tok), cfg.n_heads, cfg.n_kv_heads, cfg.head_dim
+        pos_t = torch.from_numpy(np.asarray(pos, np.int64))
+        mask = torch.from_numpy(np.asarray(vis, bool))
+        x = self.emb[torch.from_numpy(np.asarray(tok, np.int64))].clone()
+        ks, vs = [], []
+        for l, w in enumerate(self.layers):
+            xn = self._norm(x, w["attn_norm"])
+            q = self._r(self._rope((xn @ w["wq"].T).view(T, H, hd), pos_t))
+            k = self._r(self._rope((xn @ w["wk"].T).view(T, Hkv, hd), pos_t))
+            v = self._r((xn @ w["wv"].T).view(T, Hkv, hd))
+            ks.append(k)
+            vs.append(v)
+            att = torch.empty(T, H, hd)
+            for h in range(H):
+                g = h // (H // Hkv)
+                kk = torch.cat([self.kc[l][g], k[:, g]]) if P else k[:, g]
+                vv = torch.cat([self.vc[l][g], v[:, g]]) if P else v[:, g]
+                s = (q[:, h] @ kk.T) / np.sqrt(hd)
+                allowed = torch.cat([torch.ones(T, P, dtype=torch.bool), mask], 1)
+                s = s.masked_fill(~allowed, float("-inf"))
+                p = torch.exp(s - s.max(-1, keepdim=True).values)
+                att[:, h] = (self._r(p) @ vv) / p.sum(-1, keepdim=True)
+            x = x + self._r(att.reshape(T, H * hd)) @ w["wo"].T
+            xn = self._norm(x, w["ffn_norm"])
+            gt, up = xn @ w["wg"].T, xn @ w["wu"].T
+            x = x + self._r(gt * torch.sigmoid(gt) * up) @ w["wd"].T
+        return self._norm(x, self.fnorm) @ self.lm.T, ks, vs
+
+    def prefill(self, prompt):
+        P = len(prompt) - 1
+        causal = np.tril(np.ones((P, P), bool))
+        _, ks, vs = self.forward(prompt[:-1], np.arange(P), causal, 0)
+        for l in range(self.cfg.n_layers):
+            self.kc[l] = ks[l].permute(1, 0, 2).contiguous()
+            self.vc[l] = vs[l].permute(1, 0, 2).contiguous()
+
+
+def _first_step_errors(cfg, w, prompt, W, N, G):
+    torch.set_num_threads(min(8, torch.get_num_threads()))
+    ctrl = O.Controller(W, N, G, cfg.vocab)
+    ctrl.init(prompt, seed=2)
+    # a full set of G candidates for the current token (prompt n-grams at
+    # seeded offsets), so that the step has all 1 + (W+G)(N-1) rows
+    c = int(prompt[-1])
+    for i in np.random.default_rng(9).choice(len(prompt) - N, size=G, replace=False):
+        ctrl.insert(c, prompt[i + 1:i + N])
+    tok, pos, vis = ctrl.rows(c, len(prompt) - 1)
+    out = []
+    for bf in (False, True):
+        m = Model(cfg, w, bf)
+        with torch.no_grad():
+            m.prefill(prompt)
+            lg, _, _ = m.forward(tok, pos, vis, len(prompt) - 1)
+        out.append(lg.double().numpy())
+    ref, emu = out
+    step = np.linalg.norm(emu - ref) / np.linalg.norm(ref)
+    rows = np.linalg.norm(emu - ref, axis=1) / np.linalg.norm(ref, axis=1)
+    return step, rows, len(tok)
+
+
+def test_fp32_model_is_the_oracle():
+    """Without the rounding points the torch model is the oracle's arithmetic
+    (same rows, mask and weights; only the fp32 summation order differs)."""
+    cfg = I.MODELS["tiny"]
+    w = I.make_weights(cfg, 0, bf16=True)
+    prompt = I.make_prompt("tiny")
+    W, N, G = I.LOOKAHEAD["tiny"]
+    ctrl = O.Controller(W, N, G, cfg.vocab)
+    ctrl.init(prompt, seed=2)
+    tok, pos, vis = ctrl.rows(int(prompt[-1]), len(prompt) - 1)
+    seq = O.Seq(O.Model(cfg, w), 128)
+    seq.prefill(prompt[:-1])
+    ref, _ = seq.step(len(prompt) - 1, tok, pos, vis)
+    m = Model(cfg, w, False)
+    with torch.no_grad():
+        m.prefill(prompt)
+        lg, _, _ = m.forward(tok, pos, vis, len(prompt) - 1)
+    err = np.linalg.norm(lg.numpy() - ref, axis=1) / np.linalg.norm(ref, axis=1)
+    assert err.max() < 1e-5
+
+
+def test_bf16_rounding_points_on_the_7b_slice():
+    """2-layer slice of the 7B-shaped workload, first step (121 rows)."""
+    cfg = I.MODELS["7b"].sliced(2)
+    full = I.make_weights(I.MODELS["7b"], 0, bf16=True, layers=[0, 1])
+    w = {k: (v[:2] if isinstance(v, list) else v) for k, v in full.items()}
+    W, N, G = I.LOOKAHEAD["7b"]
+    step, rows, T = _first_step_errors(cfg, w, I.make_prompt("7b"), W, N, G)
+    assert T == 1 + (W + G) * (N - 1)
+    assert step <= 1e-2, step  # the per-step bound holds for the rounding alone
+    # the rounding alone brings single rows to the 1e-2 mark (>= 95 % of it)
+    assert rows.max() >= 0.95e-2, rows.max()
+    assert rows.max() * 1.5 <= 2e-2, rows.max()  # 2e-2 per row leaves a margin
+
+
+def test_bf16_rounding_points_on_the_tiny_workload():
+    cfg = I.MODELS["tiny"]
+    w = I.make_weights(cfg, 0, bf16=True)
+    W, N, G = I.LOOKAHEAD["tiny"]
+    step, rows, _ = _first_step_errors(cfg, w, I.make_prompt("tiny"), W, N, G)
+    assert step <= 1e-2 and rows.max() <= 2e-2, (step, rows.max())
