@@ -108,10 +108,13 @@ typedef struct la_prof_entry {
 
 /* Bytes of device workspace la_create needs for this model and (W,N,G):
  * KV cache, per-layer step K/V, activations, row tables, window and pool.
- * Returns 0 for unsupported arguments. */
+ * Returns 0 for unsupported arguments.
+ * No counterpart on the pages: sizing of this library's device memory. */
 LA_API size_t la_workspace_bytes(const la_model_desc* desc, int W, int N, int G);
 
-/* Create a decoding context.  W >= 0 lookahead columns, N >= 2 n-gram size,
+/* Pages: summary page, "Key points" (the knobs: window size W, n-gram size N,
+ * verification candidates G; G = W in the pages' settings).
+ * Create a decoding context.  W >= 0 lookahead columns, N >= 2 n-gram size,
  * G >= 0 verification candidates per step; W = G = 0 is plain greedy.
  * workspace: DEVICE buffer of ws_bytes >= la_workspace_bytes(), borrowed; or
  * NULL, and the library allocates (and frees) its own.  seed initialises the
@@ -124,19 +127,27 @@ LA_API size_t la_workspace_bytes(const la_model_desc* desc, int W, int N, int G)
 LA_API int la_create(const la_model_desc* desc, int W, int N, int G, void* workspace, size_t ws_bytes,
               uint64_t seed, int flags, la_ctx** out);
 
-/* Prefill: write the KV of prompt[0..len-2] into the cache, reset the window
+/* Pages: "Summary" (the lookahead branch's 2D window of W columns x N-1
+ * levels, set up here) and "Key points" (prompt n-grams added to the pool:
+ * LA_PRESEED_PROMPT).
+ * Prefill: write the KV of prompt[0..len-2] into the cache, reset the window
  * and the pool (optionally seed it with the prompt's n-grams) and make
  * prompt[len-1] the current token.  prompt: HOST int32[len], len >= 1,
  * len + W + N <= max_seq.  Blocks until done. */
 LA_API int la_prefill(la_ctx* ctx, const int32_t* prompt, int len);
 
-/* One combined lookahead decode step.  Writes the 1..N emitted tokens to the
+/* Pages: "Summary" (one forward pass holds the lookahead branch over the 2D
+ * window and the verification branch over pool candidates; new n-grams go to
+ * the pool; the output stays exactly the greedy output).
+ * One combined lookahead decode step.  Writes the 1..N emitted tokens to the
  * HOST buffer out (cap >= N entries) and their count to *n_out.  Blocks until
  * the tokens are on the host.  LA_ERR_CAPACITY if the cache cannot hold the
  * step (P + W + N > max_seq); LA_ERR_STATE before la_prefill. */
 LA_API int la_step(la_ctx* ctx, int32_t* out, int cap, int* n_out);
 
-/* Sampling verification (temperature sampling, lossless in distribution;
+/* Pages: "Summary" (the method supports sampling and keeps the output
+ * distribution; the pages give no rule, so the rule below is this library's).
+ * Sampling verification (temperature sampling, lossless in distribution;
  * the method's summary page says sampling is supported and the output
  * distribution kept, without giving the rule).  temperature > 0: every
  * emitted token is drawn from softmax(logits / temperature) of its row.  At
@@ -155,33 +166,47 @@ LA_API int la_step(la_ctx* ctx, int32_t* out, int cap, int* n_out);
  * written. */
 LA_API int la_set_sampling(la_ctx* ctx, float temperature, uint64_t seed);
 
-/* la_prefill, then la_step until max_new tokens; out: HOST int32[max_new]
+/* Pages: "Summary" (decoding that emits what plain greedy decoding emits,
+ * several tokens per step).
+ * la_prefill, then la_step until max_new tokens; out: HOST int32[max_new]
  * receives exactly min(max_new, emitted) tokens, count in *n_out. */
 LA_API int la_generate(la_ctx* ctx, const int32_t* prompt, int len, int max_new, int32_t* out, int* n_out);
 
+/* Pages: "Key points" (steps taken against tokens emitted: the step count
+ * the scaling law is about).  Counters since the last la_prefill. */
 LA_API int la_get_stats(la_ctx* ctx, la_stats* out);
-/* Copy up to cap entries (one per kernel class seen); *n_out = entries written.
+/* No counterpart on the pages: this library's kernel timing.
+ * Copy up to cap entries (one per kernel class seen); *n_out = entries written.
  * LA_ERR_STATE unless the context was made with LA_PROFILE. */
 LA_API int la_get_profile(la_ctx* ctx, la_prof_entry* out, int cap, int* n_out);
 
 /* ---- debug accessors (host copies of device state, after a step) ---- */
 
-/* Last step's logits, fp32 [T][vocab]; needs LA_DEBUG_LOGITS; n >= T*vocab. */
+/* No counterpart on the pages (a parity accessor).
+ * Last step's logits, fp32 [T][vocab]; needs LA_DEBUG_LOGITS; n >= T*vocab. */
 LA_API int la_debug_logits(la_ctx* ctx, float* host, size_t n);
-/* Last step's per-row argmax, int32[T]; *T_out = T. */
+/* Pages: "Summary" (greedy verification compares candidates with the model's
+ * own choices).  Last step's per-row argmax, int32[T]; *T_out = T. */
 LA_API int la_debug_argmax(la_ctx* ctx, int32_t* host, int cap, int* T_out);
-/* Last step's row table: tokens and positions int32[T]; *ncand = candidates
+/* Pages: "Summary" (the step's lookahead-branch and verification-branch rows).
+ * Last step's row table: tokens and positions int32[T]; *ncand = candidates
  * found in the pool (rows of missing candidates are padding). */
 LA_API int la_debug_rows(la_ctx* ctx, int32_t* tok, int32_t* pos, int cap, int* T_out, int* ncand);
-/* Pool entries of key, oldest first: int32[count][N-1] into host (cap ints). */
+/* Pages: "Summary" (n-grams cached in a pool).
+ * Pool entries of key, oldest first: int32[count][N-1] into host (cap ints). */
 LA_API int la_debug_pool(la_ctx* ctx, int32_t key, int32_t* host, int cap, int* count);
-/* Lookahead window, int32[N-1][W] into host (cap ints). */
+/* Pages: "Summary" (the 2D window of Jacobi iteration history).
+ * Lookahead window, int32[N-1][W] into host (cap ints). */
 LA_API int la_debug_window(la_ctx* ctx, int32_t* host, int cap);
 
+/* No counterpart on the pages: message of the last failure on ctx. */
 LA_API const char* la_last_error(la_ctx* ctx);
+/* No counterpart on the pages: frees the context (and its own workspace). */
 LA_API void la_destroy(la_ctx* ctx);
 
 /* ---- standalone attention (one layer of the combined step, bf16) ----
+ * Pages: "Summary" (both branches share one forward pass; the method works
+ * with FlashAttention-style attention).
  * The masked attention la_step runs in every layer, on its own: the T =
  * 1 + (W+G)(N-1) rows of a step (current token, W x (N-1) lookahead-window
  * rows, G full candidates x (N-1) verification rows, in that order) at
@@ -201,38 +226,55 @@ LA_API int la_attention(const void* q, const void* k_cache, const void* v_cache,
                         int W, int N, int G, void* stream);
 
 /* la_attention without allocating device memory.  No counterpart in the
- * paper: it exists for callers that cannot call cudaMalloc (for example code
- * running while a CUDA graph is being captured, or runtimes whose device
- * memory is fixed up front).  Same arguments and result as la_attention.
- * Scratch (the step's row tables and the attention's split partials) lives
- * in one fixed 16 MiB device array inside this library, which every GPU that
- * loads the library holds until the process exits; configurations needing
- * more (n_heads * ceil(max_seq/128) * 128 * (head_dim + 2) * 4 bytes plus a
- * few KB) return LA_ERR_CAPACITY with a message on stderr.  The first call on
- * a device looks up the array's device address (make it before any stream
- * capture).  Every call shares the array: calls that overlap on the GPU race.
- * Nothing in it needs to start at zero (each call rewrites what it reads).
- * Synchronises the stream before returning. */
+ * paper.  It is for callers that cannot call cudaMalloc: runtimes that carve
+ * all device memory out of one pool at start-up and forbid further device
+ * allocation, and latency-bound callers for which the allocator's implicit
+ * device-wide synchronisation or its failure modes are not acceptable.  Same
+ * arguments and result as la_attention.  Scratch (the step's row tables, the
+ * decode-state word and the attention's split partials) lives in one fixed
+ * 16 MiB device array inside this library, which every GPU that loads the
+ * library holds until the process exits.  The call needs
+ *   ceil256((5*128 + 1 + g * o) * 4) + ceil256(sizeof decode state)
+ *   + n_heads * ceil(max_seq / 256) * 128 * (head_dim + 4) * 4   bytes,
+ * g = max(1, W + G) row groups, o = 1 + the largest position offset of a
+ * step row (W + N - 2 with a window, N - 1 with candidates only, 0 for plain
+ * greedy); more than the array holds
+ * returns LA_ERR_CAPACITY with a message on stderr.  The first call on a
+ * device, with that device current, looks up the array's device address and
+ * sets the kernels' shared-memory limit (thread-safe, once per device).
+ * Every call shares the array: calls that overlap on the GPU race.  Nothing
+ * in it needs to start at zero (each call rewrites what it reads).  The
+ * tables are uploaded from host memory and the call synchronises the stream
+ * before returning. */
 LA_API int la_attention_noalloc(const void* q, const void* k_cache, const void* v_cache, const void* k_step,
                                 const void* v_step, void* out, int n_heads, int n_kv_heads, int head_dim, int max_seq,
                                 int P, int W, int N, int G, void* stream);
 
 /* ---- standalone n-gram pool (the pool the step uses, exposed for bulk work) ----
+ * Pages: "Summary" (the n-grams the lookahead branch produces are cached in a
+ * pool and checked by the verification branch).
  * A GPU hash table keyed on a token, each key holding up to G (N-1)-grams in
  * insertion order with first-in-first-out eviction; an insert of an n-gram
  * already held is a no-op.  Open addressing with warp-cooperative probing.
  * capacity: number of key slots (rounded up to a power of two, >= 64). */
 typedef struct la_pool la_pool;
+/* Pages: "Summary" (the pool).  Keys are tokens, >= 0. */
 LA_API int la_pool_create(int capacity, int N, int G, void* stream, la_pool** out);
-/* Insert n (key, (N-1)-gram) pairs in index order (equal keys keep their
+/* Pages: "Summary" (n-grams cached in the pool).
+ * Insert n (key, (N-1)-gram) pairs in index order (equal keys keep their
  * order; distinct keys are inserted in parallel).  keys: DEVICE int32[n],
- * grams: DEVICE int32[n][N-1].  LA_ERR_CAPACITY when the table is full. */
+ * grams: DEVICE int32[n][N-1].  LA_ERR_CAPACITY when the table is full;
+ * LA_ERR_ARG when a key is negative (that insert is skipped, the others are
+ * made).  Synchronises the pool's stream. */
 LA_API int la_pool_insert(la_pool* pool, const int32_t* keys, const int32_t* grams, int n);
-/* Look up n keys.  out: DEVICE int32[n][G][N-1] (oldest first, unused slots
- * -1), counts: DEVICE int32[n].  Asynchronous on the pool's stream. */
+/* Pages: "Summary" (candidates for verification come from the pool).
+ * Look up n keys.  out: DEVICE int32[n][G][N-1] (oldest first, unused slots
+ * -1), counts: DEVICE int32[n] (0 for absent or negative keys).
+ * Asynchronous on the pool's stream. */
 LA_API int la_pool_lookup(la_pool* pool, const int32_t* keys, int n, int32_t* out, int32_t* counts);
-/* Number of keys held (synchronises the stream). */
+/* Pages: "Summary" (the pool).  Number of keys held (synchronises the stream). */
 LA_API int la_pool_size(la_pool* pool, int* n_keys);
+/* No counterpart on the pages: frees the pool. */
 LA_API void la_pool_destroy(la_pool* pool);
 
 #ifdef __cplusplus

@@ -115,15 +115,24 @@ __global__ void k_pool_reset(PoolView p)
 }
 
 // bulk insert, phase 1: every insert finds/claims its key's slot; the lowest
-// insert index of each slot becomes that key's leader.
+// insert index of each slot becomes that key's leader.  Keys below 0 (-1 is
+// the empty-slot marker) are refused: status LA_ERR_ARG, the insert skipped.
 __global__ void k_pool_claim(PoolView p, const int* keys, int n)
 {
     int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (w >= n) return;
-    int s = pool_claim(p, keys[w]);
+    const int key = keys[w];
+    if (key < 0) {
+        if ((threadIdx.x & 31) == 0) {
+            p.slot_of[w] = -1;
+            atomicCAS(p.status, 0, LA_ERR_ARG);
+        }
+        return;
+    }
+    int s = pool_claim(p, key);
     if ((threadIdx.x & 31) == 0) {
         p.slot_of[w] = s;
-        if (s < 0) atomicExch(p.status, LA_ERR_CAPACITY);
+        if (s < 0) atomicCAS(p.status, 0, LA_ERR_CAPACITY);
         else atomicMin(&p.first[s], w);
     }
 }
@@ -158,8 +167,9 @@ __global__ void k_pool_lookup(PoolView p, const int* keys, int n, int* out, int*
     int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (w >= n) return;
-    bool found;
-    int s = pool_probe(p, keys[w], &found);
+    bool found = false;
+    // a negative key is never held (-1 marks empty slots): absent
+    int s = keys[w] >= 0 ? pool_probe(p, keys[w], &found) : -1;
     int cnt = (found && s >= 0) ? p.cnt[s] : 0;
     const int tot = p.G * p.n1;
     for (int i = lane; i < tot; i += 32)

@@ -821,17 +821,31 @@ static int attn_check(int H, int Hkv, int hd, int max_seq, int P, int W, int N, 
     return LA_OK;
 }
 
+// One-time kernel set-up (dynamic shared-memory limit) of the standalone
+// attention ops, per device and head_dim: cudaFuncSetAttribute applies to
+// the current device only.  Thread-safe.
+static std::mutex g_attn_init_mu;
+static unsigned char g_attn_ready[256][2];
+
+static int attn_ready(int hd)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return LA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_attn_init_mu);
+    unsigned char& done = g_attn_ready[dev][hd == 128 ? 1 : 0];
+    if (!done) {
+        if (!attn_mma_init(hd)) return LA_ERR_CUDA;
+        done = 1;
+    }
+    return LA_OK;
+}
+
 // Upload the tables and launch; scratch is device memory of attn_scratch_bytes.
 static int attn_run(const StepTables& tb, char* scratch, const void* q, const void* k_cache, const void* v_cache,
                     const void* k_step, const void* v_step, void* out, int H, int Hkv, int hd, int max_seq, int P,
                     cudaStream_t s)
 {
-    static bool init64 = false, init128 = false;
-    bool& init = hd == 128 ? init128 : init64;
-    if (!init) {
-        if (!attn_mma_init(hd)) return LA_ERR_CUDA;
-        init = true;
-    }
+    if (int rc = attn_ready(hd)) return rc;
     AttnScratch a = attn_scratch_carve(scratch, tb);
     std::vector<int> pos(kRows, P);
     for (int r = 0; r < tb.T; r++) pos[r] = P + tb.rel[r];
@@ -874,12 +888,13 @@ extern "C" int la_attention(const void* q, const void* k_cache, const void* v_ca
 
 // ------------------------------------------ attention without allocation ---
 //
-// For callers that must not allocate device memory: code running while a
-// CUDA graph is being captured in relaxed/global mode, allocator-free
-// embedded runtimes, or hosts whose memory budget is fixed up front.  The
-// scratch lives in one file-scope device array that every GPU loading this
-// library holds until the process exits.  No cudaMalloc/cudaFree, no host
-// heap: the row tables are built in fixed-size arrays on the stack.
+// For callers that must not allocate device memory: runtimes that take all
+// device memory into one pool at start-up and forbid further allocation, and
+// latency-bound callers that cannot accept cudaMalloc's implicit device-wide
+// synchronisation.  The scratch lives in one file-scope device array that
+// every GPU loading this library holds until the process exits.  No
+// cudaMalloc/cudaFree and no host heap: the row tables are built in a
+// fixed-size per-thread buffer.
 
 constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;  // 16 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -969,12 +984,7 @@ extern "C" int la_attention_noalloc(const void* q, const void* k_cache, const vo
     char* base = nullptr;
     int rc = noalloc_scratch(&base);
     if (rc) return rc;
-    static bool init64 = false, init128 = false;
-    bool& init = head_dim == 128 ? init128 : init64;
-    if (!init) {
-        if (!attn_mma_init(head_dim)) return LA_ERR_CUDA;
-        init = true;
-    }
+    if ((rc = attn_ready(head_dim))) return rc;
     int* ip = (int*)base;
     DState* st = (DState*)(base + tables);
     float* part = (float*)(base + tables + state);
@@ -1045,11 +1055,12 @@ extern "C" int la_pool_insert(la_pool* p, const int32_t* keys, const int32_t* gr
 {
     if (!p || n < 0 || (n > 0 && (!keys || !grams))) return LA_ERR_ARG;
     if (n > p->max_bulk) return LA_ERR_ARG;
+    if (cudaMemsetAsync(p->status, 0, 4, p->s) != cudaSuccess) return LA_ERR_CUDA;
     launch_pool_insert(p->s, p->v, keys, grams, p->v.n1, n);
     int st = 0;
     if (cudaMemcpyAsync(&st, p->status, 4, cudaMemcpyDeviceToHost, p->s) != cudaSuccess) return LA_ERR_CUDA;
     if (cudaStreamSynchronize(p->s) != cudaSuccess) return LA_ERR_CUDA;
-    return st ? LA_ERR_CAPACITY : LA_OK;
+    return st;  // LA_OK, LA_ERR_CAPACITY (table full) or LA_ERR_ARG (a negative key)
 }
 
 extern "C" int la_pool_lookup(la_pool* p, const int32_t* keys, int n, int32_t* out, int32_t* counts)

@@ -70,7 +70,7 @@ def lib():
         vp, i32, u64, f32, f64 = C.c_void_p, C.c_int, C.c_uint64, C.c_float, C.c_double
         sig = {
             "om_seq_new": (vp, [vp, i32]), "om_seq_free": (None, [vp]),
-            "om_threads": (i32, []), "om_rope_table": (None, [vp, vp, vp]),
+            "om_threads": (i32, []), "om_set_threads": (None, [i32]), "om_rope_table": (None, [vp, vp, vp]),
             "om_rope": (None, [vp, vp, i32]),
             "om_step_forward": (i32, [vp, i32, i32, vp, vp, vp, vp, vp]),
             "om_commit": (i32, [vp, i32, i32, vp]), "om_prefill": (i32, [vp, i32, vp, i32]),
@@ -338,3 +338,8 @@ def attention(q, k_cache, v_cache, k_step, v_step, vis, pos, P: int):
 
 def threads() -> int:
     return lib().om_threads()
+
+
+def set_threads(n: int) -> None:
+    """Threads of the oracle's parallel loops (results do not depend on it)."""
+    lib().om_set_threads(int(n))

@@ -137,6 +137,17 @@ OM_EXPORT int om_threads(void)
 #endif
 }
 
+/* Threads of the parallel loops that follow (results do not depend on it:
+ * every parallel loop is over independent output elements). */
+OM_EXPORT void om_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 OM_EXPORT void om_rope_table(const om_seq* s, float* cos_out, float* sin_out)
 {
     size_t n = (size_t)s->max_seq * (s->m->head_dim / 2);

@@ -66,3 +66,22 @@ def test_workspace_bytes_is_host_only_and_checks_shapes():
                      (dict(d_model=4000), (15, 5, 15)), (dict(emb=None), (15, 5, 15)),
                      (dict(), (40, 5, 0)), (dict(), (4, 1, 4)), (dict(), (4, 9, 4)), (dict(), (-1, 5, 2))]:
         assert LA.la_workspace_bytes(desc(**bad), *wng) == 0, (bad, wng)
+
+
+def test_every_declaration_cites_the_pages_or_says_there_is_none():
+    """Each LA_API declaration is preceded by a comment that names the section
+    of the method's summary page defining the call ("Pages: ...") or says the
+    pages have no counterpart."""
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        src = open(os.path.join(ROOT, "include", fn)).read()
+        prev_end, n = 0, 0
+        for m in re.finditer(r"LA_API[^;(]*?\b(la_\w+)\s*\(", src):
+            start = src.rfind("/*", prev_end, m.start())
+            assert start >= 0, m.group(1)
+            comment = src[start:m.start()]
+            assert "Pages:" in comment or "No counterpart" in comment, m.group(1)
+            prev_end = src.index(";", m.end()) + 1
+            n += 1
+        assert n == len(_declared()) or fn != "lookahead.h"

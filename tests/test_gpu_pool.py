@@ -63,3 +63,28 @@ def test_pool_capacity_error():
     grams = torch.zeros((100, 2), dtype=torch.int32, device="cuda")
     assert LA.la_pool_insert(pool, keys.data_ptr(), grams.data_ptr(), 100) == LA.LA_ERR_CAPACITY
     LA.la_pool_destroy(pool)
+
+
+def test_negative_keys_are_refused_and_absent():
+    """-1 marks empty slots, so a negative key is refused by insert
+    (LA_ERR_ARG; the other inserts of the batch are made) and looked up as
+    absent; a later insert succeeds again (the status is per call)."""
+    import torch
+    import lossless_lookahead_decoding_gb300 as LA
+    N, G = 3, 2
+    pool = LA.la_pool_create(64, N, G)
+    keys = torch.tensor([5, -1, 7, -3], dtype=torch.int32, device="cuda")
+    grams = torch.tensor([[1, 2], [3, 4], [5, 6], [7, 8]], dtype=torch.int32, device="cuda")
+    assert LA.la_pool_insert(pool, keys.data_ptr(), grams.data_ptr(), 4) == LA.LA_ERR_ARG
+    assert LA.la_pool_size(pool) == 2
+    q = torch.tensor([5, 7, -1, -3, 9], dtype=torch.int32, device="cuda")
+    out = torch.empty((5, G, N - 1), dtype=torch.int32, device="cuda")
+    cnt = torch.empty(5, dtype=torch.int32, device="cuda")
+    assert LA.la_pool_lookup(pool, q.data_ptr(), 5, out.data_ptr(), cnt.data_ptr()) == 0
+    torch.cuda.synchronize()
+    assert cnt.cpu().tolist() == [1, 1, 0, 0, 0]
+    assert out[0, 0].cpu().tolist() == [1, 2] and out[1, 0].cpu().tolist() == [5, 6]
+    assert (out[2:].cpu() == -1).all()
+    ok = torch.tensor([9], dtype=torch.int32, device="cuda")
+    assert LA.la_pool_insert(pool, ok.data_ptr(), grams.data_ptr(), 1) == LA.LA_OK
+    LA.la_pool_destroy(pool)
