@@ -123,7 +123,13 @@ LA_API size_t la_workspace_bytes(const la_model_desc* desc, int W, int N, int G)
  * On the bf16 tensor-core path la_create also makes, and the context owns, a
  * tile-packed copy of every projection, MLP and LM-head matrix (their size
  * again, in device memory outside the workspace); later changes to those
- * caller buffers are not seen.  LA_ERR_CUDA if that allocation fails. */
+ * caller buffers are not seen.  LA_ERR_CUDA if that allocation fails.
+ * Fault injection for tests of callers' error handling, from the host only:
+ * the environment variable LA_FAULT, read here, = "alloc" (la_create returns
+ * LA_ERR_OOM) | "badarg" (LA_ERR_ARG) | "timeout@K" (the K-th la_step after
+ * a prefill returns LA_ERR_TIMEOUT: the host sets the device status word a
+ * bounded device wait sets when it gives up) | "capacity@K" (the K-th
+ * la_step returns LA_ERR_CAPACITY); each fires once per context. */
 LA_API int la_create(const la_model_desc* desc, int W, int N, int G, void* workspace, size_t ws_bytes,
               uint64_t seed, int flags, la_ctx** out);
 
@@ -142,7 +148,9 @@ LA_API int la_prefill(la_ctx* ctx, const int32_t* prompt, int len);
  * One combined lookahead decode step.  Writes the 1..N emitted tokens to the
  * HOST buffer out (cap >= N entries) and their count to *n_out.  Blocks until
  * the tokens are on the host.  LA_ERR_CAPACITY if the cache cannot hold the
- * step (P + W + N > max_seq); LA_ERR_STATE before la_prefill. */
+ * step (P + W + N > max_seq); LA_ERR_STATE before la_prefill.  After an error
+ * raised on the device (LA_ERR_TIMEOUT, or a full pool: LA_ERR_CAPACITY) the
+ * context returns LA_ERR_STATE until the next la_prefill. */
 LA_API int la_step(la_ctx* ctx, int32_t* out, int cap, int* n_out);
 
 /* Pages: "Summary" (the method supports sampling and keeps the output

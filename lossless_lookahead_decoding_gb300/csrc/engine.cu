@@ -14,6 +14,7 @@
 // device, so the sequence is captured once into a CUDA graph and replayed.
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -85,7 +86,36 @@ struct la_ctx {
     cudaEvent_t ev0 = nullptr, ev1 = nullptr;
     cudaGraphExec_t gexec = nullptr;
     std::string err;
+    // host-side fault injection (LA_FAULT, read at la_create)
+    int fault_kind = 0;  // 0 none, 1 timeout, 2 capacity
+    long long fault_step = 0;
 };
+
+// Fault injection for tests of the error paths, from the host only (no
+// kernel is made to fail or wait): LA_FAULT=alloc | badarg | timeout@K |
+// capacity@K.  alloc / badarg make la_create fail as if the workspace
+// allocation failed / the arguments were refused; timeout@K writes
+// LA_ERR_TIMEOUT into the device status word before the K-th step since the
+// last prefill (as a bounded device-side wait that gave up would), so that
+// step returns it; capacity@K makes the K-th step report a full KV cache.
+// Each fires once per context.
+enum { FAULT_NONE = 0, FAULT_TIMEOUT = 1, FAULT_CAPACITY = 2, FAULT_ALLOC = 3, FAULT_BADARG = 4 };
+
+static int parse_fault(long long* step)
+{
+    const char* f = getenv("LA_FAULT");
+    *step = 0;
+    if (!f || !*f) return FAULT_NONE;
+    if (!strcmp(f, "alloc")) return FAULT_ALLOC;
+    if (!strcmp(f, "badarg")) return FAULT_BADARG;
+    const char* at = strchr(f, '@');
+    if (!at) return FAULT_NONE;
+    *step = atoll(at + 1);
+    if (*step < 1) return FAULT_NONE;
+    if (!strncmp(f, "timeout@", 8)) return FAULT_TIMEOUT;
+    if (!strncmp(f, "capacity@", 9)) return FAULT_CAPACITY;
+    return FAULT_NONE;
+}
 
 #define LA_CK(call)                                                                                    \
     do {                                                                                               \
@@ -386,8 +416,20 @@ extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* w
         fprintf(stderr, "la_create: %s\n", why);
         return LA_ERR_ARG;
     }
+    long long fault_step = 0;
+    const int fault = parse_fault(&fault_step);
+    if (fault == FAULT_BADARG) {
+        fprintf(stderr, "la_create: arguments refused (injected by LA_FAULT)\n");
+        return LA_ERR_ARG;
+    }
+    if (fault == FAULT_ALLOC) {
+        fprintf(stderr, "la_create: workspace allocation failed (injected by LA_FAULT)\n");
+        return LA_ERR_OOM;
+    }
     la_ctx* ctx = new (std::nothrow) la_ctx();
     if (!ctx) return LA_ERR_OOM;
+    ctx->fault_kind = fault;
+    ctx->fault_step = fault_step;
     ctx->d = *desc;
     ctx->lw.assign(desc->layer_w, desc->layer_w + (size_t)desc->n_layers * 9);
     for (const void* p : ctx->lw)
@@ -603,6 +645,13 @@ extern "C" int la_step(la_ctx* ctx, int32_t* out, int cap, int* n_out)
     if (!ctx->prefilled) return fail(ctx, LA_ERR_STATE, "la_step before la_prefill");
     if (ctx->P_host + ctx->W + ctx->N > ctx->d.max_seq) return fail(ctx, LA_ERR_CAPACITY, "KV cache full");
     cudaStream_t s = ctx->s;
+    const int inject = (ctx->fault_kind && ctx->stats.steps + 1 == ctx->fault_step) ? ctx->fault_kind : 0;
+    if (inject) ctx->fault_kind = FAULT_NONE;  // once per context
+    if (inject == FAULT_CAPACITY) return fail(ctx, LA_ERR_CAPACITY, "KV cache full (injected)");
+    if (inject == FAULT_TIMEOUT) {
+        static const int code = LA_ERR_TIMEOUT;
+        LA_CK(cudaMemcpyAsync(&ctx->st->status, &code, sizeof(int), cudaMemcpyHostToDevice, s));
+    }
     LA_CK(cudaEventRecord(ctx->ev0, s));
     if (!(ctx->flags & LA_NO_GRAPH)) {
         if (!ctx->gexec) {
@@ -631,7 +680,12 @@ extern "C" int la_step(la_ctx* ctx, int32_t* out, int cap, int* n_out)
     LA_CK(cudaGetLastError());
     LA_CK(cudaEventSynchronize(ctx->ev1));
     const DState& h = *ctx->h_st;
-    if (h.status) return fail(ctx, h.status, "device status set during step");
+    if (h.status) {
+        // the device state is not trusted after a device-side error: the
+        // context needs la_prefill again (which clears the status word)
+        ctx->prefilled = false;
+        return fail(ctx, h.status, "device status set during step");
+    }
     const int n = h.n_emit;
     if (n < 1 || n > ctx->N) return fail(ctx, LA_ERR_STATE, "corrupt step result");
     memcpy(out, h.emit, sizeof(int) * n);
