@@ -26,8 +26,12 @@ Functions and what pins them (the tests under tests/test_oracle_*.py):
                   softmax and, on a Markov toy model, of the sampled lookahead's
                   token sequences with plain ancestral sampling's exact
                   probabilities, and the tau -> 0 reduction to greedy decoding.
+  The "diagonal levels" mask reading R3' (variant=DIAGONAL) is pinned the
+  same way: losslessness, a brute-force walk of its visibility sets with the
+  gap-free invariant, per-row equivalence with the causal forward and a
+  list-based replay of its diagonal harvest and Jacobi window update.
   Parity unpinned: acceptance rate and the choice among the readings R1, R3,
-  R6, R7 (nothing on the pages fixes them).
+  R3', R6, R7 (nothing on the pages fixes them).
 """
 from __future__ import annotations
 
@@ -81,13 +85,15 @@ def lib():
             "om_ctrl_rows": (i32, [vp, i32, i32, vp, vp, vp]),
             "om_ctrl_advance": (i32, [vp, vp, vp, vp, vp]), "om_ctrl_pool": (i32, [vp, i32, vp]),
             "om_ctrl_window": (None, [vp, vp]),
-            "om_lookahead": (i32, [vp, vp, i32, i32, i32, i32, u64, i32, i32, i32, vp, vp, vp]),
+            "om_lookahead": (i32, [vp, vp, i32, i32, i32, i32, u64, i32, i32, i32, i32, vp, vp, vp]),
+            "om_ctrl_set_variant": (i32, [vp, i32]),
             "om_attention": (i32, [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]),
             "om_uniform": (f64, [vp]),
             "om_sample_logits": (None, [vp, i32, f32, vp, i32, vp]),
             "om_ctrl_advance_sample": (i32, [vp, vp, f32, vp, vp, vp, vp]),
             "om_sample_decode": (i32, [vp, vp, i32, i32, i32, f32, u64, vp]),
-            "om_lookahead_sample": (i32, [vp, vp, i32, i32, i32, i32, u64, i32, f32, u64, i32, i32, vp, vp, vp]),
+            "om_lookahead_sample": (i32, [vp, vp, i32, i32, i32, i32, u64, i32, i32, f32, u64, i32, i32, vp, vp,
+                                          vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -193,15 +199,19 @@ def greedy(model: Model, prompt, max_new: int, max_seq: int | None = None, logit
     return (out, lg) if logits else out
 
 
+DIAGONAL = 1  # mask reading R3' ("diagonal levels"); 0 is R3
+
+
 def lookahead(model: Model, prompt, W: int, N: int, G: int, max_new: int, seed: int = 2,
-              preseed: bool = False, max_seq: int | None = None):
-    """Returns (tokens, steps, accept_hist[0..N])."""
+              preseed: bool = False, max_seq: int | None = None, variant: int = 0):
+    """Returns (tokens, steps, accept_hist[0..N]).  variant: 0 = mask reading
+    R3, DIAGONAL = R3'."""
     p = _i32(prompt)
     max_seq = max_seq or (len(p) + max_new + W + N + 8)
     out = np.zeros(max_new, np.int32)
     steps = np.zeros(1, np.int32)
     hist = np.zeros(N + 1, np.int32)
-    rc = lib().om_lookahead(model.ptr, _p(p), len(p), W, N, G, seed, int(preseed), max_new, max_seq,
+    rc = lib().om_lookahead(model.ptr, _p(p), len(p), W, N, G, seed, int(preseed), variant, max_new, max_seq,
                             _p(out), _p(steps), _p(hist))
     if rc:
         raise ValueError("om_lookahead failed")
@@ -219,15 +229,15 @@ def sample_decode(model: Model, prompt, max_new: int, tau: float, rng_seed: int,
 
 
 def lookahead_sample(model: Model, prompt, W: int, N: int, G: int, max_new: int, tau: float, rng_seed: int,
-                     seed: int = 2, preseed: bool = False, max_seq: int | None = None):
+                     seed: int = 2, preseed: bool = False, max_seq: int | None = None, variant: int = 0):
     """Lookahead decoding with sampling verification; (tokens, steps, accept_hist)."""
     p = _i32(prompt)
     max_seq = max_seq or (len(p) + max_new + W + N + 8)
     out = np.zeros(max_new, np.int32)
     steps = np.zeros(1, np.int32)
     hist = np.zeros(N + 1, np.int32)
-    rc = lib().om_lookahead_sample(model.ptr, _p(p), len(p), W, N, G, seed, int(preseed), tau, rng_seed, max_new,
-                                   max_seq, _p(out), _p(steps), _p(hist))
+    rc = lib().om_lookahead_sample(model.ptr, _p(p), len(p), W, N, G, seed, int(preseed), variant, tau, rng_seed,
+                                   max_new, max_seq, _p(out), _p(steps), _p(hist))
     if rc:
         raise ValueError("om_lookahead_sample failed")
     return out, int(steps[0]), hist
@@ -263,10 +273,10 @@ def splitmix64_stream(seed: int, n: int):
 class Controller:
     """Window / pool / verification state machine (R1-R9) fed external argmaxes."""
 
-    def __init__(self, W: int, N: int, G: int, V: int):
-        self.W, self.N, self.G, self.V = W, N, G, V
+    def __init__(self, W: int, N: int, G: int, V: int, variant: int = 0):
+        self.W, self.N, self.G, self.V, self.variant = W, N, G, V, variant
         self.h = lib().om_ctrl_new(W, N, G, V)
-        if not self.h:
+        if not self.h or lib().om_ctrl_set_variant(self.h, variant):
             raise ValueError("bad controller arguments")
         self.Tmax = lib().om_ctrl_rows_max(self.h)
 

@@ -27,6 +27,12 @@
  *  R3 mask: row 0 sees {0}; (l,j) sees {0} u {(0,j'): j'<=j} u {(l',j):
  *     1<=l'<=l}; (g,i) sees {0} u {(g,i'): i'<=i}; every row also sees the
  *     cache [0,P) and itself;
+ *  R3' (variant "diagonal levels", om_ctrl_set_variant): each level is one
+ *     Jacobi iterate over the same positions: (l,j) at P+1+j sees {0} u
+ *     {(l,j'): j'<=j}; the new last level is the Jacobi update (argmax of
+ *     row 0, then the argmax of the last level's row j-1 at column j); the
+ *     n-grams run along diagonals: key win[0][j], value (win[1][j+1], ...,
+ *     win[N-2][j+N-2], argmax of row (N-2,j+N-2)) for j = 0..W-N+1;
  *  R5 verify: longest candidate prefix equal to the model's argmaxes, ties to
  *     the lowest g, plus one bonus token;
  *  R6 harvest: for j ascending, key win[0][j], value (win[1..N-2][j],
@@ -444,6 +450,7 @@ OM_EXPORT int om_greedy(const om_model* m, const int* prompt, int len, int max_n
 
 typedef struct om_ctrl {
     int W, N, G, V;
+    int diag;      /* 0: R3 (levels along columns), 1: R3' (diagonal levels) */
     int* win;      /* [N-1][W] */
     int* pool_cnt; /* [V] */
     int* pool;     /* [V][G][N-1], oldest first */
@@ -468,6 +475,14 @@ OM_EXPORT void om_ctrl_free(om_ctrl* k)
 {
     if (!k) return;
     free(k->win); free(k->pool_cnt); free(k->pool); free(k->cands); free(k);
+}
+
+/* Select the mask reading: 0 = R3, 1 = R3' (diagonal levels). */
+OM_EXPORT int om_ctrl_set_variant(om_ctrl* k, int diag)
+{
+    if (diag != 0 && diag != 1) return -1;
+    k->diag = diag;
+    return 0;
 }
 
 /* splitmix64 (S. Vigna): state += golden gamma, then two xor-shift-multiply
@@ -536,10 +551,16 @@ OM_EXPORT int om_ctrl_rows(om_ctrl* k, int c, int P, int* tok, int* pos, unsigne
         for (int j = 0; j < W; j++) {
             int r = row_la(k, l, j);
             tok[r] = k->win[(size_t)l * W + j];
-            pos[r] = P + 1 + j + l;
             vis[(size_t)r * T + 0] = 1;
-            for (int jj = 0; jj <= j; jj++) vis[(size_t)r * T + row_la(k, 0, jj)] = 1;
-            for (int ll = 1; ll <= l; ll++) vis[(size_t)r * T + row_la(k, ll, j)] = 1;
+            if (k->diag) {
+                /* R3': the row's own level, columns 0..j */
+                pos[r] = P + 1 + j;
+                for (int jj = 0; jj <= j; jj++) vis[(size_t)r * T + row_la(k, l, jj)] = 1;
+            } else {
+                pos[r] = P + 1 + j + l;
+                for (int jj = 0; jj <= j; jj++) vis[(size_t)r * T + row_la(k, 0, jj)] = 1;
+                for (int ll = 1; ll <= l; ll++) vis[(size_t)r * T + row_la(k, ll, j)] = 1;
+            }
         }
     for (int g = 0; g < Gp; g++)
         for (int i = 0; i < n1; i++) {
@@ -553,21 +574,29 @@ OM_EXPORT int om_ctrl_rows(om_ctrl* k, int c, int P, int* tok, int* pos, unsigne
 }
 
 /* R6 harvest (j ascending, from the window before the shift) and R7 window
- * shift, given the argmax of every row of the step. */
+ * shift, given the argmax of every row of the step.  Under R3' the n-gram
+ * starting at column j steps one column right per level, and the new last
+ * level is the Jacobi update of the last level. */
 static void harvest_and_shift(om_ctrl* k, const int* amax)
 {
-    const int W = k->W, n1 = k->N - 1;
+    const int W = k->W, n1 = k->N - 1, d = k->diag;
     int* val = (int*)malloc(sizeof(int) * n1);
-    for (int j = 0; j < W; j++) {
+    const int n_grams = d ? W - (n1 - 1) : W;
+    for (int j = 0; j < n_grams; j++) {
         int key = k->win[j];
-        for (int l = 1; l < n1; l++) val[l - 1] = k->win[(size_t)l * W + j];
-        val[n1 - 1] = amax[row_la(k, n1 - 1, j)];
+        for (int l = 1; l < n1; l++) val[l - 1] = k->win[(size_t)l * W + j + d * l];
+        val[n1 - 1] = amax[row_la(k, n1 - 1, j + d * (n1 - 1))];
         om_pool_insert(k, key, val);
     }
     free(val);
     for (int l = 0; l + 1 < n1; l++)
         memcpy(k->win + (size_t)l * W, k->win + (size_t)(l + 1) * W, sizeof(int) * W);
-    for (int j = 0; j < W; j++) k->win[(size_t)(n1 - 1) * W + j] = amax[row_la(k, n1 - 1, j)];
+    for (int j = 0; j < W; j++) {
+        int a;
+        if (!d) a = amax[row_la(k, n1 - 1, j)];
+        else a = (j == 0) ? amax[0] : amax[row_la(k, n1 - 1, j - 1)];
+        k->win[(size_t)(n1 - 1) * W + j] = a;
+    }
 }
 
 /*
@@ -739,7 +768,7 @@ OM_EXPORT int om_ctrl_advance_sample(om_ctrl* k, const float* logits, float tau,
  * number of tokens they emitted.  Returns 0, or -1 on bad arguments.
  */
 OM_EXPORT int om_lookahead(const om_model* m, const int* prompt, int len, int W, int N, int G,
-                           uint64_t seed, int preseed, int max_new, int max_seq, int* out,
+                           uint64_t seed, int preseed, int variant, int max_new, int max_seq, int* out,
                            int* steps_out, int* accept_hist)
 {
     if (len < 1 || max_new < 0) return -1;
@@ -747,7 +776,7 @@ OM_EXPORT int om_lookahead(const om_model* m, const int* prompt, int len, int W,
     if (len - 1 + max_new + W + N > max_seq) return -1;
     om_ctrl* k = om_ctrl_new(W, N, G, m->vocab);
     om_seq* s = om_seq_new(m, max_seq);
-    if (!k || !s) return -1;
+    if (!k || !s || om_ctrl_set_variant(k, variant)) return -1;
     om_ctrl_init(k, prompt, len, seed, preseed);
     int rc = om_prefill(s, 0, prompt, len - 1);
     int Tmax = om_ctrl_rows_max(k);
@@ -812,14 +841,14 @@ OM_EXPORT int om_sample_decode(const om_model* m, const int* prompt, int len, in
  * verification drawing from softmax(logits / tau) with the splitmix64 stream
  * seeded with rng_seed. */
 OM_EXPORT int om_lookahead_sample(const om_model* m, const int* prompt, int len, int W, int N, int G, uint64_t seed,
-                                  int preseed, float tau, uint64_t rng_seed, int max_new, int max_seq, int* out,
-                                  int* steps_out, int* accept_hist)
+                                  int preseed, int variant, float tau, uint64_t rng_seed, int max_new, int max_seq,
+                                  int* out, int* steps_out, int* accept_hist)
 {
     if (len < 1 || max_new < 0 || !(tau > 0.0f)) return -1;
     if (len - 1 + max_new + W + N > max_seq) return -1;
     om_ctrl* k = om_ctrl_new(W, N, G, m->vocab);
     om_seq* s = om_seq_new(m, max_seq);
-    if (!k || !s) return -1;
+    if (!k || !s || om_ctrl_set_variant(k, variant)) return -1;
     om_ctrl_init(k, prompt, len, seed, preseed);
     int rc = om_prefill(s, 0, prompt, len - 1);
     int Tmax = om_ctrl_rows_max(k);

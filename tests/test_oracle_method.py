@@ -12,7 +12,13 @@ mathematics fix (not against the oracle itself):
 * reductions: W=G=0 is greedy, G=0 emits one token per step, W=0 with a
   prompt-seeded pool only ever holds prompt n-grams;
 * splitmix64 known-answer outputs, the window initialisation (reading R1)
-  and the sampling uniforms written out from them.
+  and the sampling uniforms written out from them;
+* the "diagonal levels" mask reading R3' (each level one Jacobi iterate over
+  the same positions, n-grams along diagonals): the same visibility,
+  per-row, pool-replay and losslessness pins, plus a bigram model on which
+  every harvested n-gram must be a chain of the model's own predictions --
+  true of the harvest direction that matches the window update (columns
+  under R3, diagonals under R3') and false of the other.
 """
 import itertools
 import os
@@ -100,37 +106,47 @@ def test_attention_microbench_row_count():
     assert k.Tmax == 121
 
 
-def _check_visibility(tok, pos, vis, P, W, N, G):
+def _check_visibility(tok, pos, vis, P, W, N, G, variant=0):
     T = len(tok)
     for r in range(T):
         seen = sorted(pos[s] for s in range(T) if vis[r, s])
         assert seen == list(range(P, pos[r] + 1)), (r, seen)
-    # each lookahead column is a run of consecutive positions, level by level
-    for j in range(W):
-        ps = [pos[1 + l * W + j] for l in range(N - 1)]
-        assert ps == list(range(P + 1 + j, P + 1 + j + N - 1))
+    if variant == 0:
+        # each lookahead column is a run of consecutive positions, level by level
+        for j in range(W):
+            ps = [pos[1 + l * W + j] for l in range(N - 1)]
+            assert ps == list(range(P + 1 + j, P + 1 + j + N - 1))
+    else:
+        # each level covers P+1..P+W and sees only itself (and row 0)
+        for l in range(N - 1):
+            lv = [1 + l * W + j for j in range(W)]
+            assert [pos[r] for r in lv] == list(range(P + 1, P + 1 + W))
+            for j, r in enumerate(lv):
+                assert sorted(np.flatnonzero(vis[r]).tolist()) == [0] + lv[:j + 1]
 
 
-def test_mask_brute_force_gap_free():
+@pytest.mark.parametrize("variant", [0, O.DIAGONAL], ids=["R3", "diagonal"])
+def test_mask_brute_force_gap_free(variant):
     for W, N, G in itertools.product(range(5), range(2, 5), range(4)):
-        k = O.Controller(W, N, G, 32)
+        k = O.Controller(W, N, G, 32, variant=variant)
         k.init(np.arange(32, dtype=np.int32), seed=W * 100 + N * 10 + G)
         for g in range(G):
             k.insert(3, [(g + 7 * i) % 32 for i in range(N - 1)])
         tok, pos, vis = k.rows(3, 11)
         assert len(tok) == 1 + (W + G) * (N - 1)
-        _check_visibility(tok, pos, vis, 11, W, N, G)
+        _check_visibility(tok, pos, vis, 11, W, N, G, variant)
 
 
+@pytest.mark.parametrize("variant", [0, O.DIAGONAL], ids=["R3", "diagonal"])
 @pytest.mark.parametrize("W,N,G", [(4, 3, 4), (2, 4, 3), (3, 2, 2), (0, 3, 2), (3, 3, 0)])
-def test_masked_rows_equal_plain_causal_forward(W, N, G):
+def test_masked_rows_equal_plain_causal_forward(W, N, G, variant):
     """Row r of the combined step equals, bit for bit, the plain causal forward
     of the token sequence row r sees (its visible positions in order)."""
     cfg = SMALL
     m = O.Model(cfg, I.make_weights(cfg, 0))
     prompt = I.random_prompt(9, cfg.vocab, 11)
     P = len(prompt) - 1
-    k = O.Controller(W, N, G, cfg.vocab)
+    k = O.Controller(W, N, G, cfg.vocab, variant=variant)
     k.init(prompt, seed=5)
     c = int(prompt[-1])
     g = np.random.default_rng(2)
@@ -189,12 +205,13 @@ def _sim_insert(pool, key, val, G):
     lst.append(val)
 
 
-@pytest.mark.parametrize("W,N,G", [(4, 3, 4), (5, 4, 2), (3, 2, 3), (6, 5, 1), (2, 3, 0)])
-def test_pool_replay_against_list_simulator(W, N, G):
+@pytest.mark.parametrize("variant", [0, O.DIAGONAL], ids=["R3", "diagonal"])
+@pytest.mark.parametrize("W,N,G", [(4, 3, 4), (5, 4, 2), (3, 2, 3), (6, 5, 1), (2, 3, 0), (2, 4, 3)])
+def test_pool_replay_against_list_simulator(W, N, G, variant):
     V = 12
     g = np.random.default_rng(W * 31 + N * 7 + G)
     prompt = g.integers(0, V, 20).astype(np.int32)
-    k = O.Controller(W, N, G, V)
+    k = O.Controller(W, N, G, V, variant=variant)
     k.init(prompt, seed=9, preseed=True)
     pool = {}
     for i in range(len(prompt) - N + 1):
@@ -205,9 +222,17 @@ def test_pool_replay_against_list_simulator(W, N, G):
         tok, pos, vis = k.rows(c, 19 + step)
         amax = g.integers(0, V, len(tok))
         emit, rows, gstar = k.advance(amax)
-        last = [int(amax[1 + (N - 2) * W + j]) for j in range(W)]
-        for j in range(W):
-            _sim_insert(pool, win[0][j], tuple(win[l][j] for l in range(1, N - 1)) + (last[j],), G)
+        out = [int(amax[1 + (N - 2) * W + j]) for j in range(W)]  # the last level's rows
+        if variant == 0:
+            for j in range(W):
+                _sim_insert(pool, win[0][j], tuple(win[l][j] for l in range(1, N - 1)) + (out[j],), G)
+            last = out
+        else:
+            # an n-gram steps one column right per level; only those that stay
+            # inside the window are harvested
+            for j in range(W - (N - 2)):
+                _sim_insert(pool, win[0][j], tuple(win[l][j + l] for l in range(1, N - 1)) + (out[j + N - 2],), G)
+            last = [int(amax[0])] + out[:W - 1]  # Jacobi update: column j from column j-1
         win = win[1:] + [last]
         assert k.window().tolist() == win
         for key in range(V):
@@ -217,20 +242,66 @@ def test_pool_replay_against_list_simulator(W, N, G):
         c = int(emit[-1])
 
 
-def _lossless(cfg, bf16, W, N, G, seed, n_new, prompt, preseed=False):
+@pytest.mark.parametrize("variant", [0, O.DIAGONAL], ids=["R3", "diagonal"])
+@pytest.mark.parametrize("W,N", [(6, 4), (5, 2), (4, 5)])
+def test_harvested_ngrams_are_the_models_own_chains(W, N, variant):
+    """Bigram model f (every row's argmax is f of its own token).  Once the
+    window's levels have been replaced by model outputs (N-2 updates), each
+    level follows from the one before it by the window update, so every
+    n-gram harvested after that is a chain (x, f(x), f(f(x)), ...) -- along
+    columns under R3, along diagonals under R3'.  Harvesting the other
+    direction (or with an off-by-one column) puts non-chains into the pool.
+    Under R3' the Jacobi update puts the current token's own continuation
+    into column 0, so its chain reaches the pool and later steps emit N
+    tokens."""
+    V = 23
+    table = np.random.default_rng(5).permutation(V)  # a permutation: chains never collapse
+    f = lambda t: int(table[t])
+    G = 4
+    k = O.Controller(W, N, G, V, variant=variant)
+    prompt = np.random.default_rng(6).integers(0, V, 17).astype(np.int32)
+    k.init(prompt, seed=3)
+    c, P = int(prompt[-1]), len(prompt) - 1
+    full = 0
+    snap = lambda: {(key, tuple(v.tolist())) for key in range(V) for v in k.pool(key)}
+    new_total = 0
+    for step in range(40):
+        tok, pos, vis = k.rows(c, P)
+        before = snap()
+        emit, rows, gstar = k.advance([f(t) for t in tok])
+        # lossless on this model: the emitted tokens are c's greedy chain
+        chain = [f(c)]
+        while len(chain) < len(emit):
+            chain.append(f(chain[-1]))
+        assert emit.tolist() == chain
+        if step >= N - 2:  # the harvest reads the window after `step` updates
+            for key, v in snap() - before:
+                x = [key, *v]
+                assert all(x[i + 1] == f(x[i]) for i in range(N - 1)), (step, x)
+                new_total += 1
+            full += len(emit) == N
+        P += len(emit)
+        c = int(emit[-1])
+    assert new_total > 0
+    if variant == O.DIAGONAL:
+        assert full > 0
+
+
+def _lossless(cfg, bf16, W, N, G, seed, n_new, prompt, preseed=False, variant=0):
     m = O.Model(cfg, I.make_weights(cfg, 0, bf16=bf16))
     g = O.greedy(m, prompt, n_new)
-    la, steps, hist = O.lookahead(m, prompt, W, N, G, n_new, seed=seed, preseed=preseed)
+    la, steps, hist = O.lookahead(m, prompt, W, N, G, n_new, seed=seed, preseed=preseed, variant=variant)
     assert np.array_equal(la, g), (W, N, G, seed)
     assert hist.sum() == steps and hist[0] == 0
     assert (hist[N + 1:] == 0).all() if len(hist) > N + 1 else True
     return steps, hist
 
 
+@pytest.mark.parametrize("variant", [0, O.DIAGONAL], ids=["R3", "diagonal"])
 @pytest.mark.parametrize("bf16", [False, True])
-def test_lossless_tiny_workload(bf16):
+def test_lossless_tiny_workload(bf16, variant):
     W, N, G = I.LOOKAHEAD["tiny"]
-    steps, hist = _lossless(I.MODELS["tiny"], bf16, W, N, G, 2, 64, I.make_prompt("tiny"))
+    steps, hist = _lossless(I.MODELS["tiny"], bf16, W, N, G, 2, 64, I.make_prompt("tiny"), variant=variant)
     assert steps < 64  # some candidate was accepted on the planted-span prompt
 
 
@@ -242,13 +313,14 @@ def test_lossless_branch_balance_at_121_rows(W, G):
     assert 1 + (W + G) * 4 == 121 and steps < 64
 
 
-def test_lossless_random_cases():
-    g = np.random.default_rng(123)
+@pytest.mark.parametrize("variant", [0, O.DIAGONAL], ids=["R3", "diagonal"])
+def test_lossless_random_cases(variant):
+    g = np.random.default_rng(123 + variant)
     for case in range(40):
         W, N, G = int(g.integers(0, 6)), int(g.integers(2, 6)), int(g.integers(0, 6))
         prompt = g.integers(0, MICRO.vocab, int(g.integers(1, 12))).astype(np.int32)
         _lossless(MICRO, bool(case % 2), W, N, G, int(g.integers(0, 1 << 30)), 24, prompt,
-                  preseed=bool(case % 3 == 0))
+                  preseed=bool(case % 3 == 0), variant=variant)
 
 
 def test_reduction_greedy_and_no_verification():
