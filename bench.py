@@ -66,6 +66,9 @@ def parse():
                     help="W,N,G to use instead of the workload's lookahead settings")
     ap.add_argument("--preseed", default="auto", choices=["auto", "on", "off"],
                     help="seed the n-gram pool with the prompt's n-grams (auto: the workload's setting)")
+    ap.add_argument("--attn", default="mma", choices=["mma", "tc"],
+                    help="the step's attention kernel: mma (mma.sync, the default) or tc (tcgen05 + TMA, "
+                         "LA_ATTN_TC; needs W + N - 2 <= 31)")
     ap.add_argument("--micro", action="store_true",
                     help="instead of the benchmark line: the attention and n-gram pool micro-benchmarks")
     ap.add_argument("--sample", type=float, default=0.0,
@@ -239,13 +242,15 @@ def run_ours(args, rank, world):
     prompt = I.make_prompt(args.workload)
     max_seq = len(prompt) + gen + W + N + 16
     flags = LA.LA_PRESEED_PROMPT if pre else 0
+    attn_flag = LA.LA_ATTN_TC if getattr(args, "attn", "mma") == "tc" else 0
+    flags |= attn_flag
     t_gen = time.perf_counter()
     dw = build_model(cfg, LA.LA_BF16)
     torch.cuda.synchronize()
     t_gen = time.perf_counter() - t_gen
 
     la = LA.Decoder(cfg, dw, LA.LA_BF16, W, N, G, max_seq, flags=flags)
-    gr = LA.Decoder(cfg, dw, LA.LA_BF16, 0, 2, 0, max_seq)
+    gr = LA.Decoder(cfg, dw, LA.LA_BF16, 0, 2, 0, max_seq, flags=attn_flag)
     sample = getattr(args, "sample", 0.0)
     if sample > 0:
         for d in (la, gr):
@@ -325,7 +330,8 @@ def run_ours(args, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init weights)",
         "config": {"workload": f"{args.workload}: {cfg.n_layers}L d{cfg.d_model} {cfg.n_heads}x{cfg.head_dim} "
                                f"(kv {cfg.n_kv_heads}) ffn{cfg.ffn} V{cfg.vocab} bf16, prompt {len(prompt)}, "
-                               f"gen {gen}, W{W} N{N} G{G}, T={T} rows" + (", prompt-seeded pool" if pre else ""),
+                               f"gen {gen}, W{W} N{N} G{G}, T={T} rows" + (", prompt-seeded pool" if pre else "")
+                               + (", tcgen05 attention" if attn_flag else ""),
                    "global_batch": 1, "seq_len": max_seq, "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2 (weights {cfg.streamed_params() * 2 / 1e9:.1f} GB stream every step)"},
         "accepted_tokens_per_step": round(acc_per_step, 4),
@@ -357,19 +363,22 @@ def run_ours(args, rank, world):
     return out
 
 
-# (W, N, G, prompt-seeded pool) of the sweep: T = 1 + (W+G)(N-1) <= 128 rows
-SWEEP = [(0, 2, 0, False),                                     # greedy
-         (0, 3, 4, True), (0, 5, 4, True),                      # prompt lookup: no window, prompt n-grams
-         (5, 5, 5, False), (7, 5, 7, False), (10, 5, 10, False), (15, 5, 15, False),
-         (15, 3, 15, False), (31, 3, 31, False), (20, 4, 20, False), (10, 7, 10, False),
-         (15, 5, 15, True),
+# (W, N, G, prompt-seeded pool, diagonal levels) of the sweep: T = 1 + (W+G)(N-1) <= 128 rows
+SWEEP = [(0, 2, 0, False, False),                                            # greedy
+         (0, 3, 4, True, False), (0, 5, 4, True, False),                      # prompt lookup: prompt n-grams
+         (5, 5, 5, False, False), (7, 5, 7, False, False), (10, 5, 10, False, False), (15, 5, 15, False, False),
+         (15, 3, 15, False, False), (31, 3, 31, False, False), (20, 4, 20, False, False),
+         (10, 7, 10, False, False), (15, 5, 15, True, False),
          # branch balance at T = 121 (W + G = 30, N = 5): lopsided to balanced
-         (28, 5, 2, False), (25, 5, 5, False), (20, 5, 10, False), (10, 5, 20, False), (5, 5, 25, False),
-         (2, 5, 28, False)]
+         (28, 5, 2, False, False), (25, 5, 5, False, False), (20, 5, 10, False, False),
+         (10, 5, 20, False, False), (5, 5, 25, False, False), (2, 5, 28, False, False),
+         # the other mask reading (LA_MASK_DIAG) at the same shapes
+         (5, 5, 5, False, True), (7, 5, 7, False, True), (10, 5, 10, False, True), (15, 5, 15, False, True),
+         (15, 3, 15, False, True), (20, 4, 20, False, True), (10, 7, 10, False, True)]
 
 
 def run_sweep(args, rank, world):
-    """One JSON line per (W, N, G): step latency, accepted tokens/step,
+    """One JSON line per (W, N, G, mask): step latency, accepted tokens/step,
     tokens/s, speedup over greedy and losslessness (same library, same
     prompt).  W = 0 with a prompt-seeded pool is the prompt-lookup mode."""
     import torch
@@ -382,11 +391,12 @@ def run_sweep(args, rank, world):
         cfg = cfg.sliced(args.layers)
     gen = GEN_TOKENS[args.workload]
     prompt = I.make_prompt(args.workload)
-    max_seq = len(prompt) + gen + max(w + n for w, n, _, _ in SWEEP) + 16
+    max_seq = len(prompt) + gen + max(w + n for w, n, _, _, _ in SWEEP) + 16
     dw = build_model(cfg, LA.LA_BF16)
     lines, ref_out, greedy_tps = [], None, None
-    for W, N, G, pre in SWEEP:
-        dec = LA.Decoder(cfg, dw, LA.LA_BF16, W, N, G, max_seq, flags=LA.LA_PRESEED_PROMPT if pre else 0)
+    for W, N, G, pre, diag in SWEEP:
+        flags = (LA.LA_PRESEED_PROMPT if pre else 0) | (LA.LA_MASK_DIAG if diag else 0)
+        dec = LA.Decoder(cfg, dw, LA.LA_BF16, W, N, G, max_seq, flags=flags)
         tok, step_ms_l, _, _ = timed_steps(dec, prompt, gen, args.warmup, args.steps)
         out = dec.generate(prompt, gen)
         dec.close()
@@ -396,7 +406,8 @@ def run_sweep(args, rank, world):
         T = 1 + (W + G) * (N - 1)
         lines.append({"sweep": args.workload, "mode": "greedy" if W == 0 and G == 0 else
                       ("prompt-lookup" if W == 0 else "lookahead"), "W": W, "N": N, "G": G, "T": T,
-                      "prompt_seeded_pool": pre, "ms_per_step": round(float(np.mean(step_ms_l)), 4),
+                      "prompt_seeded_pool": pre, "mask": "diagonal levels" if diag else "columns",
+                      "ms_per_step": round(float(np.mean(step_ms_l)), 4),
                       "accepted_tokens_per_step": round(tok / args.steps, 4), "tokens_per_s": round(tps, 2),
                       "speedup_vs_greedy": round(tps / greedy_tps, 4),
                       "lossless_vs_greedy": bool(np.array_equal(out, ref_out)), "steps": args.steps})

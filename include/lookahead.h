@@ -54,6 +54,9 @@ extern "C" {
 #define LA_NO_GRAPH 4       /* launch kernels directly instead of a CUDA graph      */
 #define LA_SIMT 8           /* bf16 model on the SIMT kernels (debug)               */
 #define LA_PROFILE 16       /* time kernel classes with CUDA events (la_get_profile) */
+#define LA_ATTN_TC 32       /* bf16: the step's attention on tcgen05 + TMA (needs      \
+                               W + N - 2 <= 31 and max_seq <= 4096; see la_create)   */
+#define LA_MASK_DIAG 64     /* lookahead branch as diagonal levels (see la_create)     */
 
 typedef struct la_ctx la_ctx;
 
@@ -119,7 +122,23 @@ LA_API size_t la_workspace_bytes(const la_model_desc* desc, int W, int N, int G)
  * workspace: DEVICE buffer of ws_bytes >= la_workspace_bytes(), borrowed; or
  * NULL, and the library allocates (and frees) its own.  seed initialises the
  * lookahead window (splitmix64 stream).  flags: LA_PRESEED_PROMPT |
- * LA_DEBUG_LOGITS | LA_NO_GRAPH | LA_SIMT.  On success *out owns the context.
+ * LA_DEBUG_LOGITS | LA_NO_GRAPH | LA_SIMT | LA_PROFILE | LA_ATTN_TC |
+ * LA_MASK_DIAG.  On success *out owns the context.
+ * LA_MASK_DIAG reads the pages' 2D window the other way their text allows:
+ * each of the N-1 levels is one Jacobi iterate over positions P+1..P+W and
+ * its rows see only their own level (row (l,j) sees c and (l,0..j)); the new
+ * last level is the Jacobi update of the last one (argmax of row 0, then of
+ * row (N-2, j-1) at column j); the n-grams run along diagonals (key
+ * win[0][j], value win[1][j+1], ..., win[N-2][j+N-2], argmax of row
+ * (N-2, j+N-2)).  The row count and the verification branch are unchanged;
+ * the default is the column reading (row (l,j) at P+1+j+l sees level 0 up to
+ * column j and column j up to level l).  LA_ATTN_TC (bf16 tensor-core path) runs the
+ * step's attention on a second kernel pair: each row's keys older than its
+ * 31..46 most recent positions in splits of 128 positions on tcgen05 (TMA-fed,
+ * accumulators in tensor memory), the recent window per row group on
+ * mma.sync, merged per row; LA_ERR_ARG when W + N - 2 > 31 or max_seq > 4096.
+ * Its arithmetic differs from the default kernel's, so a greedy context
+ * compared token for token with a lookahead context must use the same flag.
  * On the bf16 tensor-core path la_create also makes, and the context owns, a
  * tile-packed copy of every projection, MLP and LM-head matrix (their size
  * again, in device memory outside the workspace); later changes to those

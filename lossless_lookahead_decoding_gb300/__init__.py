@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_HERE, "liblookahead.so")
 
 LA_OK, LA_ERR_ARG, LA_ERR_OOM, LA_ERR_CAPACITY, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_ERR_STATE = 0, -1, -2, -3, -4, -5, -6
 LA_FP32, LA_BF16 = 0, 1
-LA_PRESEED_PROMPT, LA_DEBUG_LOGITS, LA_NO_GRAPH, LA_SIMT, LA_PROFILE = 1, 2, 4, 8, 16
+LA_PRESEED_PROMPT, LA_DEBUG_LOGITS, LA_NO_GRAPH, LA_SIMT, LA_PROFILE, LA_ATTN_TC, LA_MASK_DIAG = 1, 2, 4, 8, 16, 32, 64
 
 EXPORTS = ("la_workspace_bytes", "la_create", "la_prefill", "la_step", "la_generate", "la_set_sampling", "la_get_stats",
            "la_get_profile",
@@ -281,7 +281,7 @@ class Decoder:
     def __init__(self, cfg, weights, dtype: int, W: int, N: int, G: int, max_seq: int, seed: int = 2,
                  flags: int = 0, stream=None):
         import torch
-        self.cfg, self.W, self.N, self.G, self.dtype = cfg, W, N, G, dtype
+        self.cfg, self.W, self.N, self.G, self.dtype, self.flags = cfg, W, N, G, dtype, flags
         self.w = weights
         self._ptrs = (C.c_void_p * (cfg.n_layers * 9))(
             *[weights[n][l].data_ptr() for l in range(cfg.n_layers) for n in LAYER_ORDER])

@@ -1,5 +1,6 @@
 // common.cuh -- types shared by the kernels and the engine of liblookahead.so.
 #pragma once
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -118,7 +119,7 @@ void launch_prefill_rows(cudaStream_t s, const DState* st, const int* prompt, in
                          int* pos);
 void launch_verify_update(cudaStream_t s, DState* st, const int* tok, const int* amax, int* win,
                           PoolView pool, int W, int N, int G, const float* logits, int V, float tau,
-                          const double* stats);
+                          const double* stats, bool diag);
 void launch_row_stats(cudaStream_t s, const float* logits, int V, float tau, int vbase, int T, double* stats);
 void launch_commit(cudaStream_t s, const DState* st, bool prefill, int n_prefill, int n_max, const void* KS,
                    const void* VS, void* KC, void* VC, int L, int Hkv, int hd, int max_seq, int esz);
@@ -150,7 +151,33 @@ void launch_attn_simt(cudaStream_t s, const DState* st, RowSet rs, const int* po
                       int max_seq, float scale);
 void launch_argmax(cudaStream_t s, const float* logits, int* amax, int rows, int V);
 
-// attn_mma.cu (bf16, head_dim 64 or 128)
+// attn_tc.cu (bf16, head_dim 64 or 128): the decode step's attention on
+// tcgen05 (cached keys older than the row's recent window) + mma.sync (the
+// recent window, per row group), merged per row
+struct AttnTcPlan {
+    CUtensorMap qmap, kmap, vmap, ksmap, vsmap;
+    int H, Hkv, hd, max_seq, hpc, bq, nsa, cta_cap, n_items;
+    bool ok;
+};
+int attn_tc_delta();  // rows may sit at most this many positions past P
+size_t attn_tc_partial_bytes(int H, int hd, int max_seq);
+bool attn_tc_init(int hd);
+// Q: [q_rows][H*hd]; KC/VC: [kv_rows][hd] (layers x KV heads x max_seq rows);
+// KS/VS: [ks_rows][Hkv*hd] (step rows of every layer); n_items: row-group
+// slabs of 16 rows of the step's row table
+int attn_tc_plan(AttnTcPlan* pl, const void* Q, int q_rows, const void* KC, const void* VC, long long kv_rows,
+                 const void* KS, const void* VS, long long ks_rows, int H, int Hkv, int hd, int max_seq, int rows,
+                 int n_items);
+// cta_y: region-A CTAs per head group (the cache kernel's grid.y), from
+// attn_tc_splits() for the step's P; attn_tc_cache_kernel() identifies that
+// kernel's launches in a captured graph, whose grids the caller updates when
+// the split count changes
+void launch_attn_tc(cudaStream_t s, const AttnTcPlan& pl, int layer, int ks_row0, const DState* st, RowSet rs,
+                    int max_rel, const int* pos, const void* Q, void* out, float* part, int rows, int* err, int cta_y);
+int attn_tc_splits(const AttnTcPlan& pl, int P, int max_rel);
+const void* attn_tc_cache_kernel(int hd);
+
+// attn_mma.cu (bf16, head_dim 64 or 128): prefill blocks (causal)
 size_t attn_mma_partial_bytes(int H, int hd, int max_seq);
 bool attn_mma_init(int hd);
 void launch_attn_mma(cudaStream_t s, const DState* st, RowSet rs, int max_rel, const int* pos, const void* Q,

@@ -498,9 +498,14 @@ __device__ void sample_verify(DState* st, const int* tok, const float* logits, i
 // colliding keys may differ, which lookups do not see).  Then every thread
 // shifts the window up one level, the last level becoming the argmaxes of
 // the last level's rows.
+// Diagonal levels (diag): the n-gram keyed on win[0][j] steps one column
+// right per level (win[l][j+l], then the argmax of row (N-2, j+N-2)), for
+// the W-N+2 columns j whose diagonal stays inside the window; the new last
+// level is the Jacobi update: argmax of row 0 in column 0, the argmax of the
+// last level's row j-1 in column j.
 __global__ void __launch_bounds__(kVerifyWarps * 32)
     k_verify_update(DState* st, const int* tok, const int* amax, int* win, PoolView pool, int W, int N, int G,
-                    const float* logits, int V, float tau, const double* stats)
+                    const float* logits, int V, float tau, const double* stats, int diag)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int n1 = N - 1, ncand = st->ncand, P = st->P;
@@ -546,10 +551,11 @@ __global__ void __launch_bounds__(kVerifyWarps * 32)
     __shared__ int s_err;
     if (threadIdx.x == 0) s_err = 0;
     __syncthreads();
+    const int n_grams = diag ? W - (n1 - 1) : W;  // keys win[0][0 .. n_grams)
     if (G > 0) {
-        for (int j0 = 0; j0 < W; j0 += kVerifyWarps) {
+        for (int j0 = 0; j0 < n_grams; j0 += kVerifyWarps) {
             const int j = j0 + warp;
-            if (j < W) {
+            if (j < n_grams) {
                 const int s = pool_claim(pool, win[j]);
                 if (lane == 0) {
                     slot_of[warp] = s;
@@ -557,17 +563,17 @@ __global__ void __launch_bounds__(kVerifyWarps * 32)
                 }
             }
             __syncthreads();
-            if (!s_err && j < W) {
+            if (!s_err && j < n_grams) {
                 const int s = slot_of[warp];
                 bool leader = true;
                 for (int k = 0; k < warp; k++) leader = leader && slot_of[k] != s;
                 if (leader) {
-                    for (int jj = warp; jj < kVerifyWarps && j0 + jj < W; jj++) {
+                    for (int jj = warp; jj < kVerifyWarps && j0 + jj < n_grams; jj++) {
                         if (slot_of[jj] != s) continue;
                         const int c = j0 + jj;
                         int val[kMaxN];
-                        for (int l = 1; l < n1; l++) val[l - 1] = win[l * W + c];
-                        val[n1 - 1] = amax[1 + (n1 - 1) * W + c];
+                        for (int l = 1; l < n1; l++) val[l - 1] = win[l * W + c + diag * l];
+                        val[n1 - 1] = amax[1 + (n1 - 1) * W + c + diag * (n1 - 1)];
                         pool_insert_slot(pool, s, val);
                     }
                 }
@@ -577,20 +583,23 @@ __global__ void __launch_bounds__(kVerifyWarps * 32)
         if (threadIdx.x == 0 && s_err) st->status = LA_ERR_CAPACITY;
     }
     __syncthreads();
-    // window shift: level l <- level l+1; last level <- argmax of last level rows
-    const int nw = n1 * W;
+    // window shift: level l <- level l+1; last level <- argmax of last level
+    // rows (diagonal levels: of row 0, then of the last level's row j-1)
+    const int nw = n1 * W, last0 = (n1 - 1) * W;
     int tmp[4];
     int k = 0;
-    for (int idx = threadIdx.x; idx < nw; idx += blockDim.x) tmp[k++] = (idx < (n1 - 1) * W) ? win[idx + W] : amax[1 + idx];
+    for (int idx = threadIdx.x; idx < nw; idx += blockDim.x)
+        tmp[k++] = (idx < last0) ? win[idx + W] : (diag ? (idx == last0 ? a0 : amax[idx]) : amax[1 + idx]);
     __syncthreads();
     k = 0;
     for (int idx = threadIdx.x; idx < nw; idx += blockDim.x) win[idx] = tmp[k++];
 }
 
 void launch_verify_update(cudaStream_t s, DState* st, const int* tok, const int* amax, int* win, PoolView pool,
-                          int W, int N, int G, const float* logits, int V, float tau, const double* stats)
+                          int W, int N, int G, const float* logits, int V, float tau, const double* stats, bool diag)
 {
-    k_verify_update<<<1, kVerifyWarps * 32, 0, s>>>(st, tok, amax, win, pool, W, N, G, logits, V, tau, stats);
+    k_verify_update<<<1, kVerifyWarps * 32, 0, s>>>(st, tok, amax, win, pool, W, N, G, logits, V, tau, stats,
+                                                    diag ? 1 : 0);
 }
 
 // ------------------------------------------------------------------ commit ---

@@ -59,7 +59,12 @@ struct la_ctx {
     float tau = 0.f;              // > 0: sampling verification at this temperature
     double* SSTAT = nullptr;      // per-row softmax max / exp-sum for sampling
     cudaStream_t s = nullptr;
-    bool bf16 = false, use_tc = false, use_attn_mma = false;
+    bool bf16 = false, use_tc = false, use_attn_mma = false, use_attn_tc = false;
+    AttnTcPlan atc{};  // the step's attention on the tensor cores (tensor maps, launch shape)
+    int atc_cta_y = 1;                          // its cache kernel's grid.y for the step being enqueued
+    int graph_cta_y = 0;                        // ... as captured in (or last set on) the graph
+    cudaGraph_t graph = nullptr;                // the captured step (kept to update node grids)
+    std::vector<cudaGraphNode_t> atc_nodes;     // its cache-kernel launches
     float* attn_part = nullptr;
     int esz = 4, dq = 0, dkv = 0;
     char* ws = nullptr;
@@ -190,7 +195,9 @@ static Layout make_layout(const la_model_desc* d, int W, int N, int G, int* pool
     ly.add(kRows * 8);                                   // 27 packed argmax
     ly.add((2 * kRows + 1) * 4);                         // 28 step group lists
     ly.add((2 * kRows + 1) * 4);                         // 29 prefill group lists
-    ly.add(attn_mma_partial_bytes(d->n_heads, d->head_dim, d->max_seq));  // 30 attention split partials
+    const size_t pa = attn_mma_partial_bytes(d->n_heads, d->head_dim, d->max_seq);
+    const size_t pt = attn_tc_partial_bytes(d->n_heads, d->head_dim, d->max_seq);
+    ly.add(pa > pt ? pa : pt);                           // 30 attention split partials
     ly.add(kRows * 16);                                  // 31 sampling row statistics
     return ly;
 }
@@ -203,40 +210,51 @@ static Layout make_layout(const la_model_desc* d, int W, int N, int G, int* pool
 // group's rows see there (column j: the level-0 rows of columns 0..j, then
 // levels 1.. of column j; candidate g: its own rows).  groups lists every
 // group's rows in row order ([ngrp + 1] starts, then the rows).
+// Diagonal levels (LA_MASK_DIAG): lookahead row (l, j) sits at offset 1 + j
+// and sees only its own level, so level l is group l (candidates follow) and
+// its map holds the level's rows at offsets 1..W.
 struct StepTables {
     int T = 1, maxoff = 1, ngrp = 1;
     std::vector<int> rel, grp, map, groups;
 };
 
-static StepTables step_tables(int W, int N, int G)
+static StepTables step_tables(int W, int N, int G, bool diag = false)
 {
     StepTables tb;
     const int n1 = N - 1;
+    const int lgrp = diag ? (W > 0 ? n1 : 0) : W;  // groups of the lookahead rows
     tb.T = step_rows(W, N, G);
     tb.rel.assign(kRows, 0);
     tb.grp.assign(kRows, 0);
     for (int l = 0; l < n1; l++)
         for (int j = 0; j < W; j++) {
             const int r = 1 + l * W + j;
-            tb.rel[r] = 1 + j + l;
-            tb.grp[r] = j;
+            tb.rel[r] = diag ? 1 + j : 1 + j + l;
+            tb.grp[r] = diag ? l : j;
         }
     for (int g = 0; g < G; g++)
         for (int i = 0; i < n1; i++) {
             const int r = 1 + W * n1 + g * n1 + i;
             tb.rel[r] = 1 + i;
-            tb.grp[r] = W + g;
+            tb.grp[r] = lgrp + g;
         }
     for (int r = 0; r < tb.T; r++) tb.maxoff = tb.rel[r] + 1 > tb.maxoff ? tb.rel[r] + 1 : tb.maxoff;
-    tb.ngrp = W + G > 0 ? W + G : 1;
+    tb.ngrp = lgrp + G > 0 ? lgrp + G : 1;
     tb.map.assign((size_t)tb.ngrp * tb.maxoff, 0);
-    for (int j = 0; j < W; j++) {
-        int* m = &tb.map[(size_t)j * tb.maxoff];
-        for (int jj = 0; jj <= j; jj++) m[1 + jj] = 1 + jj;         // level 0, columns 0..j
-        for (int l = 1; l < n1; l++) m[1 + j + l] = 1 + l * W + j;  // levels 1.. of column j
+    if (diag) {
+        for (int l = 0; l < lgrp; l++) {
+            int* m = &tb.map[(size_t)l * tb.maxoff];
+            for (int jj = 0; jj < W; jj++) m[1 + jj] = 1 + l * W + jj;  // level l, columns in order
+        }
+    } else {
+        for (int j = 0; j < W; j++) {
+            int* m = &tb.map[(size_t)j * tb.maxoff];
+            for (int jj = 0; jj <= j; jj++) m[1 + jj] = 1 + jj;         // level 0, columns 0..j
+            for (int l = 1; l < n1; l++) m[1 + j + l] = 1 + l * W + j;  // levels 1.. of column j
+        }
     }
     for (int g = 0; g < G; g++) {
-        int* m = &tb.map[(size_t)(W + g) * tb.maxoff];
+        int* m = &tb.map[(size_t)(lgrp + g) * tb.maxoff];
         for (int i = 0; i < n1; i++) m[1 + i] = 1 + W * n1 + g * n1 + i;
     }
     tb.groups.assign(2 * kRows + 1, 0);
@@ -301,7 +319,10 @@ static void forward(la_ctx* c, int rows, const RowSet& rs, bool logits)
             launch_rope_split<T>(s, c->QKV32, c->pos, c->cosb, c->sinb, Q, KS, VS, rows, H, Hkv, hd);
         }
         c->prof.begin(s);
-        if (c->use_attn_mma)
+        if (c->use_attn_tc && &rs == &c->rs_step)
+            launch_attn_tc(s, c->atc, l, l * kRows, c->st, rs, rs.maxoff - 1, c->pos, (const void*)Q, (void*)ATT,
+                           c->attn_part, rows, &c->st->status, c->atc_cta_y);
+        else if (c->use_attn_mma)
             launch_attn_mma(s, c->st, rs, &rs == &c->rs_pre ? rows - 1 : rs.maxoff - 1, c->pos,
                             (const void*)Q, (const void*)KC, (const void*)VC, (const void*)KS, (const void*)VS,
                             (void*)ATT, c->attn_part, rows, H, Hkv, hd, d.max_seq);
@@ -363,7 +384,7 @@ static void enqueue_step(la_ctx* c)
     const int vbase = 1 + c->W * (c->N - 1);
     if (c->tau > 0.f) launch_row_stats(c->s, c->LOGITS, c->d.vocab, c->tau, vbase, c->T, c->SSTAT);
     launch_verify_update(c->s, c->st, c->tok, c->AMAX, c->win, c->pool, c->W, c->N, c->G, c->LOGITS, c->d.vocab,
-                         c->tau, c->SSTAT);
+                         c->tau, c->SSTAT, (c->flags & LA_MASK_DIAG) != 0);
     launch_commit(c->s, c->st, false, 0, c->N, c->KS, c->VS, c->KC, c->VC, c->d.n_layers, c->d.n_kv_heads,
                   c->d.head_dim, c->d.max_seq, c->esz);
     c->prof.end(c->s, P_CONTROL, 0, 0);
@@ -389,6 +410,22 @@ static void collect_profile(la_ctx* c, int P_before)
         pr.bytes[p.cls] += by;
         pr.flops[p.cls] += fl;
         pr.n[p.cls] += 1;
+    }
+}
+
+// The kernel nodes of a captured graph that launch `fn`.
+static void find_kernel_nodes(cudaGraph_t g, const void* fn, std::vector<cudaGraphNode_t>* out)
+{
+    size_t n = 0;
+    if (cudaGraphGetNodes(g, nullptr, &n) != cudaSuccess || n == 0) return;
+    std::vector<cudaGraphNode_t> nodes(n);
+    if (cudaGraphGetNodes(g, nodes.data(), &n) != cudaSuccess) return;
+    for (size_t i = 0; i < n; i++) {
+        cudaGraphNodeType t;
+        cudaKernelNodeParams kp;
+        if (cudaGraphNodeGetType(nodes[i], &t) == cudaSuccess && t == cudaGraphNodeTypeKernel &&
+            cudaGraphKernelNodeGetParams(nodes[i], &kp) == cudaSuccess && kp.func == fn)
+            out->push_back(nodes[i]);
     }
 }
 
@@ -502,7 +539,7 @@ extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* w
     ctx->attn_part = (float*)(b + ly.off[30]);
 
     // row tables: step (rows, positions and mask of the combined step) and prefill (causal)
-    const StepTables tb = step_tables(W, N, G);
+    const StepTables tb = step_tables(W, N, G, (flags & LA_MASK_DIAG) != 0);
     const std::vector<int>&rel = tb.rel, &grp = tb.grp, &map = tb.map, &sgl = tb.groups;
     const int maxoff = tb.maxoff, ngrp = tb.ngrp;
     std::vector<int> prel(kRows), pgrp(kRows, 0), pmap(kRows);
@@ -526,8 +563,10 @@ extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* w
                 rc = LA_ERR_CUDA;
             }
         };
-        // zero the activations once so padded rows always hold finite values
-        ck(cudaMemset(ctx->ws + ly.off[2], 0, ly.off[11] - ly.off[2]));
+        // zero the KV cache and the activations once: padded rows, and cache
+        // positions not yet written that a tensor-core tile covers with zero
+        // weight, must hold finite values
+        ck(cudaMemset(ctx->ws + ly.off[0], 0, ly.off[11] - ly.off[0]));
         ck(cudaMemset(ctx->AMAXP, 0, kRows * 8));
         ck(cudaMemcpy(rs1, rel.data(), kRows * 4, cudaMemcpyHostToDevice));
         ck(cudaMemcpy(rs1 + kRows, grp.data(), kRows * 4, cudaMemcpyHostToDevice));
@@ -553,6 +592,34 @@ extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* w
             ctx->use_tc = true;
             ctx->use_attn_mma = attn_mma_init(desc->head_dim);
         }
+        // the step's rows sit at most W + N - 2 positions past P (N - 1 for
+        // candidate rows); the tensor-core attention keeps every row's recent
+        // window of attn_tc_delta() positions out of its cache-only part
+        if (trc == 0 && (flags & LA_ATTN_TC) && (W > 0 ? W + N - 2 : N - 1) > attn_tc_delta()) {
+            ctx->err = "LA_ATTN_TC needs W + N - 2 <= 31";
+            rc = LA_ERR_ARG;
+        } else if (trc == 0 && (flags & LA_ATTN_TC)) {
+            int items = 0;
+            for (int g = 0; g < ngrp; g++) {
+                int n = 0;
+                for (int r = 0; r < tb.T; r++) n += grp[r] == g;
+                items += (n + 15) / 16;
+            }
+            const long long kv_rows = (long long)desc->n_layers * desc->n_kv_heads * desc->max_seq;
+            const int arc = !attn_tc_init(desc->head_dim)
+                                ? LA_ERR_CUDA
+                                : attn_tc_plan(&ctx->atc, ctx->Q, kRows, ctx->KC, ctx->VC, kv_rows, ctx->KS, ctx->VS,
+                                               (long long)desc->n_layers * kRows, desc->n_heads, desc->n_kv_heads,
+                                               desc->head_dim, desc->max_seq, tb.T, items);
+            ctx->use_attn_tc = arc == LA_OK;
+            if (arc == LA_ERR_ARG) {
+                ctx->err = "max_seq must be <= 4096 on the bf16 tensor-core path";
+                rc = LA_ERR_ARG;
+            } else if (arc) {
+                ctx->err = "tensor-core attention set-up failed";
+                rc = LA_ERR_CUDA;
+            }
+        }
         else if (trc < 0) {
             ctx->err = "tcgen05 plan creation failed";
             rc = LA_ERR_CUDA;
@@ -575,6 +642,7 @@ extern "C" void la_destroy(la_ctx* ctx)
     if (ctx->s) cudaStreamSynchronize(ctx->s);
     else cudaDeviceSynchronize();
     if (ctx->gexec) cudaGraphExecDestroy(ctx->gexec);
+    if (ctx->graph) cudaGraphDestroy(ctx->graph);
     tc_plan_destroy(&ctx->tc);
     if (ctx->own_ws && ctx->ws) cudaFree(ctx->ws);
     if (ctx->h_st) cudaFreeHost(ctx->h_st);
@@ -645,6 +713,8 @@ extern "C" int la_step(la_ctx* ctx, int32_t* out, int cap, int* n_out)
     if (!ctx->prefilled) return fail(ctx, LA_ERR_STATE, "la_step before la_prefill");
     if (ctx->P_host + ctx->W + ctx->N > ctx->d.max_seq) return fail(ctx, LA_ERR_CAPACITY, "KV cache full");
     cudaStream_t s = ctx->s;
+    // the attention's cache kernel: one CTA per split the step's rows reach
+    if (ctx->use_attn_tc) ctx->atc_cta_y = attn_tc_splits(ctx->atc, ctx->P_host, ctx->rs_step.maxoff - 1);
     const int inject = (ctx->fault_kind && ctx->stats.steps + 1 == ctx->fault_step) ? ctx->fault_kind : 0;
     if (inject) ctx->fault_kind = FAULT_NONE;  // once per context
     if (inject == FAULT_CAPACITY) return fail(ctx, LA_ERR_CAPACITY, "KV cache full (injected)");
@@ -665,12 +735,27 @@ extern "C" int la_step(la_ctx* ctx, int32_t* out, int cap, int* n_out)
             }
             ctx->kernels_per_step = count_kernels(g);
             e = cudaGraphInstantiate(&ctx->gexec, g, 0);
-            cudaGraphDestroy(g);
             if (e != cudaSuccess) {
+                cudaGraphDestroy(g);
                 ctx->gexec = nullptr;
                 ctx->err = std::string("graph instantiate: ") + cudaGetErrorString(e);
                 return LA_ERR_CUDA;
             }
+            ctx->graph = g;
+            ctx->atc_nodes.clear();
+            if (ctx->use_attn_tc) find_kernel_nodes(g, attn_tc_cache_kernel(ctx->d.head_dim), &ctx->atc_nodes);
+            ctx->graph_cta_y = ctx->atc_cta_y;
+        }
+        if (ctx->use_attn_tc && ctx->atc_cta_y != ctx->graph_cta_y) {
+            // the split count changed with P: resize the cache kernel's grids
+            for (cudaGraphNode_t node : ctx->atc_nodes) {
+                cudaKernelNodeParams kp;
+                LA_CK(cudaGraphKernelNodeGetParams(node, &kp));
+                kp.gridDim.y = ctx->atc_cta_y;
+                LA_CK(cudaGraphKernelNodeSetParams(node, &kp));
+                LA_CK(cudaGraphExecKernelNodeSetParams(ctx->gexec, node, &kp));
+            }
+            ctx->graph_cta_y = ctx->atc_cta_y;
         }
         LA_CK(cudaGraphLaunch(ctx->gexec, s));
     } else {
@@ -715,6 +800,8 @@ extern "C" int la_set_sampling(la_ctx* ctx, float temperature, uint64_t seed)
     if (ctx->gexec) {  // the step's launch sequence changes: capture it again
         cudaGraphExecDestroy(ctx->gexec);
         ctx->gexec = nullptr;
+        cudaGraphDestroy(ctx->graph);
+        ctx->graph = nullptr;
     }
     return LA_OK;
 }
@@ -894,6 +981,17 @@ static int attn_ready(int hd)
     return LA_OK;
 }
 
+// Launch the step attention on device tables and scratch, wait for it and
+// return its status.
+static int attn_launch_sync(DState* st, RowSet rs, int max_rel, const int* pos, const void* q, const void* k_cache,
+                            const void* v_cache, const void* k_step, const void* v_step, void* out, float* part, int T,
+                            int H, int Hkv, int hd, int max_seq, cudaStream_t s)
+{
+    launch_attn_mma(s, st, rs, max_rel, pos, q, k_cache, v_cache, k_step, v_step, out, part, T, H, Hkv, hd, max_seq);
+    if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) return LA_ERR_CUDA;
+    return LA_OK;
+}
+
 // Upload the tables and launch; scratch is device memory of attn_scratch_bytes.
 static int attn_run(const StepTables& tb, char* scratch, const void* q, const void* k_cache, const void* v_cache,
                     const void* k_step, const void* v_step, void* out, int H, int Hkv, int hd, int max_seq, int P,
@@ -915,11 +1013,9 @@ static int attn_run(const StepTables& tb, char* scratch, const void* q, const vo
         cudaMemcpyAsync(a.st, &hst, sizeof(DState), cudaMemcpyHostToDevice, s))
         return LA_ERR_CUDA;
     RowSet rs{a.rel, a.grp, a.map, a.groups, a.groups + kRows + 1, tb.maxoff, tb.ngrp};
-    launch_attn_mma(s, a.st, rs, tb.maxoff - 1, a.pos, q, k_cache, v_cache, k_step, v_step, out, a.part, tb.T, H, Hkv,
-                    hd, max_seq);
-    // the host tables above are pageable: wait until the copies have been consumed
-    if (cudaStreamSynchronize(s) != cudaSuccess) return LA_ERR_CUDA;
-    return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+    // synchronises: the host tables above are pageable
+    return attn_launch_sync(a.st, rs, tb.maxoff - 1, a.pos, q, k_cache, v_cache, k_step, v_step, out, a.part, tb.T, H,
+                            Hkv, hd, max_seq, s);
 }
 
 extern "C" int la_attention(const void* q, const void* k_cache, const void* v_cache, const void* k_step,
@@ -972,7 +1068,8 @@ static int noalloc_scratch(char** out)
     return LA_OK;
 }
 
-// Fixed-size copy of the step tables (same content as step_tables()).
+// Fixed-size copy of the step tables (same content as step_tables() for the
+// column mask; the standalone attention has no diagonal-levels option).
 struct FixedTables {
     int T, maxoff, ngrp;
     int rel[kRows], grp[kRows], groups[2 * kRows + 1], pos[kRows];
@@ -1056,11 +1153,9 @@ extern "C" int la_attention_noalloc(const void* q, const void* k_cache, const vo
         cudaMemcpyAsync(st, &hst, sizeof(DState), cudaMemcpyHostToDevice, s))
         return LA_ERR_CUDA;
     RowSet rs{ip, ip + kRows, ip + 5 * kRows + 1, ip + 2 * kRows, ip + 3 * kRows + 1, tb.maxoff, tb.ngrp};
-    launch_attn_mma(s, st, rs, tb.maxoff - 1, ip + 4 * kRows + 1, q, k_cache, v_cache, k_step, v_step, out, part, tb.T,
-                    n_heads, n_kv_heads, head_dim, max_seq);
-    if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
-    // the host tables are reused by the next call on this thread
-    return cudaStreamSynchronize(s) == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+    // synchronises: the host tables are reused by the next call on this thread
+    return attn_launch_sync(st, rs, tb.maxoff - 1, ip + 4 * kRows + 1, q, k_cache, v_cache, k_step, v_step, out, part,
+                            tb.T, n_heads, n_kv_heads, head_dim, max_seq, s);
 }
 
 // --------------------------------------------------------- standalone pool ---

@@ -33,8 +33,9 @@ def replay_against_oracle(dec, om, prompt, n_steps, tol, seed=2, preseed=False, 
     logits error)."""
     row_tol = tol if row_tol is None else row_tol
     import oracle as O
+    import lossless_lookahead_decoding_gb300 as LA
     W, N, G, V = dec.W, dec.N, dec.G, dec.cfg.vocab
-    ctrl = O.Controller(W, N, G, V)
+    ctrl = O.Controller(W, N, G, V, variant=O.DIAGONAL if dec.flags & LA.LA_MASK_DIAG else 0)
     ctrl.init(prompt, seed=seed, preseed=preseed)
     seq = O.Seq(om, len(prompt) + n_steps * N + W + N + 8)
     seq.prefill(prompt[:-1])

@@ -62,6 +62,8 @@ def test_workspace_bytes_is_host_only_and_checks_shapes():
     assert kv(804) <= ws < kv(804) + (1 << 30)
     assert LA.la_workspace_bytes(desc(max_seq=804 + 1024), 15, 5, 15) - ws >= kv(1024)
     assert LA.la_workspace_bytes(desc(dtype=LA.LA_FP32), 15, 5, 15) > ws  # fp32 cache and activations
+    # the widest windows of 128 rows are accepted (LA_ATTN_TC's own limit is checked by la_create)
+    assert LA.la_workspace_bytes(desc(), 31, 3, 31) > 0 and LA.la_workspace_bytes(desc(), 32, 2, 0) > 0
     for bad, wng in [(dict(head_dim=96), (15, 5, 15)), (dict(n_kv_heads=3), (15, 5, 15)),
                      (dict(d_model=4000), (15, 5, 15)), (dict(emb=None), (15, 5, 15)),
                      (dict(), (40, 5, 0)), (dict(), (4, 1, 4)), (dict(), (4, 9, 4)), (dict(), (-1, 5, 2))]:

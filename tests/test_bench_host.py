@@ -68,8 +68,9 @@ def test_lookahead_overrides_and_sweep_shapes():
     assert bench.lookahead_of(a) == (7, 5, 7, True)
     a = argparse.Namespace(workload="7b", wng="0,4,6", preseed="on")
     assert bench.lookahead_of(a) == (0, 4, 6, True)
-    assert bench.SWEEP[0] == (0, 2, 0, False)
-    for W, N, G, pre in bench.SWEEP:
+    assert bench.SWEEP[0] == (0, 2, 0, False, False)
+    assert any(d for *_, d in bench.SWEEP) and (15, 5, 15, False, True) in bench.SWEEP
+    for W, N, G, pre, diag in bench.SWEEP:
         assert 1 + (W + G) * (N - 1) <= 128 and N >= 2
         if W == 0 and G > 0:
             assert pre

@@ -8,7 +8,9 @@
   case.
 * Bit-exactness that keeps lookahead lossless: each step row's output equals,
   bit for bit, the output of decoding that row alone (W = G = 0) after its
-  visible step rows have been appended to the cache in position order.
+  visible step rows have been appended to the cache in position order --
+  around the kernel's 64-position chunk and 256-position split boundaries and
+  at a 31-position-wide window.
 """
 import numpy as np
 import pytest
@@ -84,17 +86,39 @@ def test_microbench_case_against_oracle():
 
 
 @pytest.mark.parametrize("H,Hkv,hd,P,W,N,G", [(32, 8, 64, 1000, 4, 3, 4), (8, 8, 128, 777, 0, 2, 0),
-                                               (4, 2, 128, 63, 7, 5, 7), (4, 4, 64, 0, 3, 4, 2)])
+                                               (4, 2, 128, 63, 7, 5, 7), (4, 4, 64, 0, 3, 4, 2),
+                                               # short caches, and caches ending next to chunk and split
+                                               # boundaries
+                                               (4, 4, 128, 10, 15, 5, 15), (4, 4, 128, 40, 15, 5, 15),
+                                               (8, 2, 128, 256 + 31, 7, 5, 7), (4, 1, 64, 129, 5, 3, 5),
+                                               # windows 31 positions wide: W + N - 2 = 31
+                                               (8, 8, 128, 300, 28, 5, 2), (4, 4, 128, 517, 30, 3, 30)])
 def test_shapes_against_oracle(H, Hkv, hd, P, W, N, G):
     _check_against_oracle(H, Hkv, hd, P, W, N, G, seed=H + P)
 
 
-@pytest.mark.parametrize("P", [250, 319, 1023])
+@pytest.mark.parametrize("P", [0, 17, 127, 128, 143, 250, 319, 1023])
 def test_rows_equal_their_greedy_decoding_bitwise(P):
     H, Hkv, hd, W, N, G = 4, 2, 128, 7, 5, 7
     q, kc, vc, ks, vs, max_seq, pos, vis, got = _check_against_oracle(H, Hkv, hd, P, W, N, G, seed=P)
     T = len(q)
     for r in [0, 1, 7, 8, 1 + 3 * W + 6, 1 + W * (N - 1), T - 1, T - 2]:
+        seen = sorted((pos[c], c) for c in range(T) if vis[r, c] and c != r)
+        kc2, vc2 = kc.copy(), vc.copy()
+        for p, c in seen:
+            kc2[:, p], vc2[:, p] = ks[c], vs[c]
+        alone = _run(q[r:r + 1], kc2, vc2, ks[r:r + 1], vs[r:r + 1], H, Hkv, hd, max_seq, int(pos[r]), 0, 2, 0)
+        assert np.array_equal(alone[0], got[r]), r
+
+
+@pytest.mark.parametrize("P", [33, 300, 641])
+def test_widest_window_rows_equal_their_greedy_decoding_bitwise(P):
+    """W + N - 2 = 31: the lookahead rows reach 31 positions past the
+    cache."""
+    H, Hkv, hd, W, N, G = 4, 4, 64, 28, 5, 2
+    q, kc, vc, ks, vs, max_seq, pos, vis, got = _check_against_oracle(H, Hkv, hd, P, W, N, G, seed=P + 5)
+    T = len(q)
+    for r in [0, 1, 28, 29, 1 + 3 * W + W - 1, T - 1]:
         seen = sorted((pos[c], c) for c in range(T) if vis[r, c] and c != r)
         kc2, vc2 = kc.copy(), vc.copy()
         for p, c in seen:

@@ -18,8 +18,9 @@ pytestmark = pytest.mark.gpu
 
 TOL = {0: 1e-4, 1: 1e-2}
 # (dtype, flags): fp32 SIMT debug path, bf16 on the SIMT kernels, bf16 on the
-# tensor-core path (tcgen05 GEMMs)
-MODES = {"fp32": (0, 0), "bf16simt": (1, 8), "bf16": (1, 0)}
+# tensor-core path (tcgen05 GEMMs), and that path with the step's attention on
+# tcgen05 too (LA_ATTN_TC)
+MODES = {"fp32": (0, 0), "bf16simt": (1, 8), "bf16": (1, 0), "bf16attntc": (1, 32)}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -83,7 +84,7 @@ def test_tiny_fp32_greedy_logits():
         assert np.linalg.norm(lg - ref_l[s]) / np.linalg.norm(ref_l[s]) < 1e-4
 
 
-@pytest.mark.parametrize("mode", ["bf16simt", "bf16"])
+@pytest.mark.parametrize("mode", ["bf16simt", "bf16", "bf16attntc"])
 def test_preseed_and_edge_prompts(mode):
     dtype, mflags = MODES[mode]
     cfg = I.MODELS["tiny"]
@@ -118,6 +119,13 @@ def test_errors_and_capacity():
     assert dec.stats()["P"] + 4 + 3 > 48
     with pytest.raises(LA.LAError):
         gpu_decoder(cfg, w, 1, 40, 5, 40, 256)  # 1 + 80*4 rows > 128
+    # the tensor-core attention's limits: W + N - 2 <= 31, max_seq <= 4096
+    gpu_decoder(cfg, w, 1, 30, 3, 30, 256, flags=LA.LA_ATTN_TC).close()
+    gpu_decoder(cfg, w, 1, 31, 3, 31, 256).close()
+    for wng, ms in (((31, 3, 31), 256), ((32, 2, 0), 256), ((4, 3, 4), 4096 + 64)):
+        with pytest.raises(LA.LAError) as e:
+            gpu_decoder(cfg, w, 1, *wng, ms, flags=LA.LA_ATTN_TC)
+        assert e.value.code == LA.LA_ERR_ARG
 
 
 def test_profiled_launches_keep_the_output():
@@ -137,3 +145,23 @@ def test_profiled_launches_keep_the_output():
         assert name in prof and prof[name]["launches"] > 0 and prof[name]["total_ms"] > 0, name
     assert prof["gemm_qkv"]["bytes"] > 0
     dec.close()
+
+
+@pytest.mark.parametrize("mode", ["fp32", "bf16"])
+@pytest.mark.parametrize("WNG", [(4, 3, 4), (5, 4, 3), (3, 2, 3), (2, 5, 2)])
+def test_diagonal_levels_against_oracle(mode, WNG):
+    """LA_MASK_DIAG: rows, positions, window, pool and emitted tokens
+    bit-exact against the oracle controller's diagonal-levels variant fed
+    the GPU's argmaxes, logits within the bounds, and the output equal to
+    greedy (W < N - 1 included: no n-gram fits a diagonal)."""
+    import lossless_lookahead_decoding_gb300 as LA
+    dtype, mflags = MODES[mode]
+    cfg = I.MODELS["tiny"]
+    w = _weights(cfg, dtype == 1)
+    prompt = I.make_prompt("tiny")
+    dec = gpu_decoder(cfg, w, dtype, *WNG, 256, flags=mflags | LA.LA_MASK_DIAG | LA.LA_DEBUG_LOGITS)
+    replay_against_oracle(dec, O.Model(cfg, w), prompt, 16, TOL[dtype], row_tol=2 * TOL[dtype] if dtype else None)
+    dec.close()
+    g = gpu_decoder(cfg, w, dtype, 0, 2, 0, 256, flags=mflags).generate(prompt, 64)
+    la = gpu_decoder(cfg, w, dtype, *WNG, 256, flags=mflags | LA.LA_MASK_DIAG).generate(prompt, 64)
+    assert np.array_equal(la, g)
