@@ -279,24 +279,77 @@ __device__ __forceinline__ unsigned long long smix64(unsigned long long* x)
     return z ^ (z >> 31);
 }
 
-// Uniform in [0,1): the top 24 bits of the next output.
-__device__ __forceinline__ double uniform24(unsigned long long* x) { return (double)(smix64(x) >> 40) * (1.0 / 16777216.0); }
 
-// Row max and sum of exp((z - max) / tau) in fp64 for row 0 (block 0) and the
+// exp(x) for x <= 0 in fp32 for the sampling probabilities: range reduction
+// after Cody and Waite, k = nearest integer to x log2(e), t = x - k ln 2 with
+// ln 2 split into a float and its float remainder (two fused multiply-adds),
+// e^x = 2^k e^t; e^t by its degree-7 Taylor series (Horner, fused
+// multiply-adds), times 2^k; 0 below 2^-125.  Each step is one correctly
+// rounded fp32 operation (no contraction left to the compiler), so the
+// result does not depend on the device or the compiler.
+__device__ __forceinline__ float exp_neg(float x)
+{
+    const float k = rintf(__fmul_rn(x, 0x1.715476p+0f));
+    if (k < -125.0f) return 0.0f;
+    float t = __fmaf_rn(-k, 0x1.62e430p-1f, x);
+    t = __fmaf_rn(-k, -0x1.05c610p-29f, t);
+    float q = 0x1.a01a02p-13f;
+    q = __fmaf_rn(q, t, 0x1.6c16c2p-10f);
+    q = __fmaf_rn(q, t, 0x1.111112p-7f);
+    q = __fmaf_rn(q, t, 0x1.555556p-5f);
+    q = __fmaf_rn(q, t, 0x1.555556p-3f);
+    q = __fmaf_rn(q, t, 0.5f);
+    q = __fmaf_rn(q, t, 1.0f);
+    q = __fmaf_rn(q, t, 1.0f);
+    return ldexpf(q, (int)k);
+}
+
+// The sampling distribution as exact integers: token v weighs E(v) =
+// floor(exp_neg((z_v - max) / tau) 2^B), the argument by an fp32 subtraction
+// and division (correctly rounded), B = 63 - ceil(log2(V + 1)) so that the
+// row total S < 2^63; p(v) =
+// E(v) / S.  Sums of weights are exact in any order, and the comparisons
+// with a uniform U / 2^24 are exact 128-bit products, so the sampling
+// decisions do not depend on how the work is split across threads.
+__host__ __device__ __forceinline__ int sample_bits(int V)
+{
+    int b = 0;
+    while ((1LL << b) < (long long)V + 1) b++;
+    return 63 - b;
+}
+
+__device__ __forceinline__ unsigned long long weight_of(float z, float mx, float tau, int B)
+{
+    const float e = exp_neg(__fdiv_rn(__fsub_rn(z, mx), tau));
+    return __float2ull_rz(ldexpf(e, B));
+}
+
+// a * b as 128 bits (hi, lo)
+struct U128 {
+    unsigned long long hi, lo;
+};
+__device__ __forceinline__ U128 mul128(unsigned long long a, unsigned long long b) { return {__umul64hi(a, b), a * b}; }
+__device__ __forceinline__ U128 shl24(unsigned long long a) { return {a >> 40, a << 24}; }
+__device__ __forceinline__ bool lt128(U128 a, U128 b) { return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo); }
+
+// Uniform U: the top 24 bits of the next output (u = U / 2^24).
+__device__ __forceinline__ unsigned long long uniform_u24(unsigned long long* x) { return smix64(x) >> 40; }
+
+// Row max and total weight S (weight_of) for row 0 (block 0) and the
 // verification rows vbase.. (blocks 1..): the rows whose softmax sampling
-// verification reads.  stats[2r] = max, stats[2r+1] = sum.
+// verification reads.  stats[2r] = the max's float bits, stats[2r+1] = S.
 constexpr int kStatThreads = 256;
 
 __global__ void __launch_bounds__(kStatThreads) k_row_stats(const float* __restrict__ logits, int V, float tau,
-                                                           int vbase, double* __restrict__ stats)
+                                                           int vbase, unsigned long long* __restrict__ stats)
 {
     pdl_wait();
     pdl_trigger();
     const int r = blockIdx.x == 0 ? 0 : vbase + blockIdx.x - 1;
     const float* z = logits + (size_t)r * V;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, B = sample_bits(V);
     __shared__ float s_m[kStatThreads / 32];
-    __shared__ double s_s[kStatThreads / 32];
+    __shared__ unsigned long long s_s[kStatThreads / 32];
     float mx = -INFINITY;
     for (int v = threadIdx.x; v < V; v += kStatThreads) mx = fmaxf(mx, z[v]);
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -304,20 +357,21 @@ __global__ void __launch_bounds__(kStatThreads) k_row_stats(const float* __restr
     __syncthreads();
     mx = s_m[0];
     for (int w = 1; w < kStatThreads / 32; w++) mx = fmaxf(mx, s_m[w]);
-    double sum = 0.0;
-    for (int v = threadIdx.x; v < V; v += kStatThreads) sum += exp(((double)z[v] - (double)mx) / (double)tau);
+    unsigned long long sum = 0;
+    for (int v = threadIdx.x; v < V; v += kStatThreads) sum += weight_of(z[v], mx, tau, B);
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     if (lane == 0) s_s[warp] = sum;
     __syncthreads();
     if (threadIdx.x == 0) {
-        double t = 0.0;
+        unsigned long long t = 0;
         for (int w = 0; w < kStatThreads / 32; w++) t += s_s[w];
-        stats[2 * r] = mx;
+        stats[2 * r] = __float_as_uint(mx);
         stats[2 * r + 1] = t;
     }
 }
 
-void launch_row_stats(cudaStream_t s, const float* logits, int V, float tau, int vbase, int T, double* stats)
+void launch_row_stats(cudaStream_t s, const float* logits, int V, float tau, int vbase, int T,
+                      unsigned long long* stats)
 {
     launch_pdl(k_row_stats, dim3(1 + T - vbase), dim3(kStatThreads), 0, s, logits, V, tau, vbase, stats);
 }
@@ -326,34 +380,34 @@ void launch_row_stats(cudaStream_t s, const float* logits, int V, float tau, int
 
 constexpr int kVerifyWarps = 32;  // window columns harvested at once (W <= kMaxW handled in rounds)
 
-// Draw from softmax(z / tau) (row max mx, exp-sum S) restricted to the
-// tokens not in rej[0..nrej): the first token, in ascending order, whose
-// running sum of probabilities exceeds target; the last admissible token of
-// nonzero probability if rounding leaves target unreached.  Every thread of
-// the block takes part (a contiguous chunk of tokens each, chunks summed by a
-// block scan in fp64).
-__device__ int block_draw(const float* z, int V, float tau, double mx, double S, const int* rej, int nrej,
-                          double target)
+// Draw from the row's weights (max mx, total S) restricted to the tokens not
+// in rej[0..nrej) (whose weight is R): the first token, in ascending order,
+// whose running weight A has A 2^24 > U (S - R); the last admissible token of
+// nonzero weight if none.  Every thread of the block takes part (a
+// contiguous chunk of tokens each; chunk totals by a block scan, exact).
+__device__ int block_draw(const float* z, int V, float tau, float mx, unsigned long long S, const int* rej, int nrej,
+                          unsigned long long R, unsigned long long U)
 {
-    __shared__ double s_part[kVerifyWarps];
+    __shared__ unsigned long long s_part[kVerifyWarps];
     __shared__ int s_pick, s_last;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x, B = sample_bits(V);
     const int chunk = (V + nt - 1) / nt, v0 = min(tid * chunk, V), v1 = min(v0 + chunk, V);
-    auto prob = [&](int v) -> double {
+    const U128 target = mul128(U, S - R);
+    auto weight = [&](int v) -> unsigned long long {
         for (int k = 0; k < nrej; k++)
-            if (rej[k] == v) return 0.0;
-        return exp(((double)z[v] - mx) / (double)tau) / S;
+            if (rej[k] == v) return 0ull;
+        return weight_of(z[v], mx, tau, B);
     };
-    double loc = 0.0;
+    unsigned long long loc = 0;
     int last = -1;
     for (int v = v0; v < v1; v++) {
-        const double p = prob(v);
-        loc += p;
-        if (p > 0.0) last = v;
+        const unsigned long long w = weight(v);
+        loc += w;
+        if (w) last = v;
     }
-    double x = loc;  // inclusive scan within the warp
+    unsigned long long x = loc;  // inclusive scan within the warp
     for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xffffffffu, x, o);
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
     }
     if (lane == 31) s_part[warp] = x;
@@ -363,21 +417,21 @@ __device__ int block_draw(const float* z, int V, float tau, double mx, double S,
     }
     __syncthreads();
     if (warp == 0) {
-        double y = lane < nt / 32 ? s_part[lane] : 0.0;
+        unsigned long long y = lane < nt / 32 ? s_part[lane] : 0ull;
         for (int o = 1; o < 32; o <<= 1) {
-            const double t = __shfl_up_sync(0xffffffffu, y, o);
+            const unsigned long long t = __shfl_up_sync(0xffffffffu, y, o);
             if (lane >= o) y += t;
         }
         s_part[lane] = y;
     }
     __syncthreads();
-    const double pre = (warp ? s_part[warp - 1] : 0.0) + x - loc;  // mass of the tokens before this chunk
+    const unsigned long long pre = (warp ? s_part[warp - 1] : 0ull) + x - loc;  // weight before this chunk
     if (last >= 0) atomicMax(&s_last, last);
-    if (pre + loc > target) {
-        double acc = pre;
+    if (lt128(target, shl24(pre + loc))) {
+        unsigned long long acc = pre;
         for (int v = v0; v < v1; v++) {
-            acc += prob(v);
-            if (acc > target) {
+            acc += weight(v);
+            if (lt128(target, shl24(acc))) {
                 atomicMin(&s_pick, v);
                 break;
             }
@@ -393,12 +447,12 @@ __device__ int block_draw(const float* z, int V, float tau, double mx, double S,
 // emitted tokens, committed rows and the advanced decode state, like the
 // greedy branch of k_verify_update.
 __device__ void sample_verify(DState* st, const int* tok, const float* logits, int V, float tau,
-                              const double* stats, int W, int N)
+                              const unsigned long long* stats, int W, int N)
 {
     __shared__ unsigned char s_alive[kRows];
     __shared__ int s_rej[kRows];
     __shared__ int s_nrej, s_acc, s_row, s_m, s_done, s_gbest, s_emit[kMaxN];
-    __shared__ double s_target;
+    __shared__ unsigned long long s_u, s_R;
     __shared__ unsigned long long s_rng;
     const int tid = threadIdx.x, n1 = N - 1, ncand = st->ncand, vbase = 1 + W * n1;
     if (tid == 0) {
@@ -412,35 +466,36 @@ __device__ void sample_verify(DState* st, const int* tok, const float* logits, i
     __syncthreads();
     for (int i = 0; i < n1; i++) {
         if (tid == 0) {
-            const int row = s_row;
+            const int row = s_row, B = sample_bits(V);
             const float* z = logits + (size_t)row * V;
-            const double mx = stats[2 * row], S = stats[2 * row + 1];
+            const float mx = __uint_as_float((unsigned)stats[2 * row]);
+            const unsigned long long S = stats[2 * row + 1];
             int nrej = 0, acc = -1;
-            double R = 0.0;
+            unsigned long long R = 0;
             for (int g = 0; g < ncand && acc < 0; g++) {
                 if (!s_alive[g]) continue;
                 const int v = tok[vbase + g * n1 + i];
                 bool seen = false;
                 for (int k = 0; k < nrej; k++) seen = seen || s_rej[k] == v;
                 if (seen) continue;  // a value already tried at this level
-                const double u = uniform24(&s_rng);
-                const double pv = exp(((double)z[v] - mx) / (double)tau) / S;
-                if (u * (1.0 - R) < pv) {
+                const unsigned long long U = uniform_u24(&s_rng), E = weight_of(z[v], mx, tau, B);
+                if (lt128(mul128(U, S - R), shl24(E))) {  // u (1 - R/S) < E/S
                     acc = g;
                 } else {
                     s_rej[nrej++] = v;
-                    R += pv;
+                    R += E;
                 }
             }
             s_acc = acc;
             s_nrej = nrej;
-            if (acc < 0) s_target = uniform24(&s_rng) * (1.0 - R);
+            s_R = R;
+            if (acc < 0) s_u = uniform_u24(&s_rng);
         }
         __syncthreads();
         if (s_acc < 0) {
             const int row = s_row;
-            const int v = block_draw(logits + (size_t)row * V, V, tau, stats[2 * row], stats[2 * row + 1], s_rej,
-                                     s_nrej, s_target);
+            const int v = block_draw(logits + (size_t)row * V, V, tau, __uint_as_float((unsigned)stats[2 * row]),
+                                     stats[2 * row + 1], s_rej, s_nrej, s_R, s_u);
             if (tid == 0) {
                 s_emit[s_m] = v;
                 s_done = 1;
@@ -460,11 +515,11 @@ __device__ void sample_verify(DState* st, const int* tok, const float* logits, i
         __syncthreads();
     }
     if (!s_done) {
-        if (tid == 0) s_target = uniform24(&s_rng);
+        if (tid == 0) s_u = uniform_u24(&s_rng);
         __syncthreads();
         const int row = s_row;
-        const int v = block_draw(logits + (size_t)row * V, V, tau, stats[2 * row], stats[2 * row + 1], nullptr, 0,
-                                 s_target);
+        const int v = block_draw(logits + (size_t)row * V, V, tau, __uint_as_float((unsigned)stats[2 * row]),
+                                 stats[2 * row + 1], nullptr, 0, 0ull, s_u);
         if (tid == 0) s_emit[s_m] = v;
         __syncthreads();
     }
@@ -505,7 +560,7 @@ __device__ void sample_verify(DState* st, const int* tok, const float* logits, i
 // last level's row j-1 in column j.
 __global__ void __launch_bounds__(kVerifyWarps * 32)
     k_verify_update(DState* st, const int* tok, const int* amax, int* win, PoolView pool, int W, int N, int G,
-                    const float* logits, int V, float tau, const double* stats, int diag)
+                    const float* logits, int V, float tau, const unsigned long long* stats, int diag)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int n1 = N - 1, ncand = st->ncand, P = st->P;
@@ -596,7 +651,8 @@ __global__ void __launch_bounds__(kVerifyWarps * 32)
 }
 
 void launch_verify_update(cudaStream_t s, DState* st, const int* tok, const int* amax, int* win, PoolView pool,
-                          int W, int N, int G, const float* logits, int V, float tau, const double* stats, bool diag)
+                          int W, int N, int G, const float* logits, int V, float tau,
+                          const unsigned long long* stats, bool diag)
 {
     k_verify_update<<<1, kVerifyWarps * 32, 0, s>>>(st, tok, amax, win, pool, W, N, G, logits, V, tau, stats,
                                                     diag ? 1 : 0);

@@ -57,7 +57,7 @@ struct la_ctx {
     int W = 0, N = 2, G = 0, T = 1, flags = 0;
     uint64_t seed = 0;
     float tau = 0.f;              // > 0: sampling verification at this temperature
-    double* SSTAT = nullptr;      // per-row softmax max / exp-sum for sampling
+    unsigned long long* SSTAT = nullptr;  // per-row softmax max (float bits) / integer weight total for sampling
     cudaStream_t s = nullptr;
     bool bf16 = false, use_tc = false, use_attn_mma = false, use_attn_tc = false;
     AttnTcPlan atc{};  // the step's attention on the tensor cores (tensor maps, launch shape)
@@ -531,7 +531,7 @@ extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* w
     ctx->st = (DState*)(b + ly.off[25]);
     ctx->dbg = (int*)(b + ly.off[26]);
     ctx->AMAXP = (unsigned long long*)(b + ly.off[27]);
-    ctx->SSTAT = (double*)(b + ly.off[31]);
+    ctx->SSTAT = (unsigned long long*)(b + ly.off[31]);
     ctx->pool = PoolView{pk, pk + cap, (int*)(b + ly.off[23]), pk + 2 * cap, (int*)(b + ly.off[24]),
                          &ctx->st->status, cap, lg, G, N - 1};
     int* gl1 = (int*)(b + ly.off[28]);

@@ -88,7 +88,8 @@ def lib():
             "om_lookahead": (i32, [vp, vp, i32, i32, i32, i32, u64, i32, i32, i32, i32, vp, vp, vp]),
             "om_ctrl_set_variant": (i32, [vp, i32]),
             "om_attention": (i32, [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]),
-            "om_uniform": (f64, [vp]),
+            "om_uniform": (f64, [vp]), "om_exp_neg": (f32, [f32]),
+            "om_sample_weight": (C.c_uint64, [f32, f32, f32, i32]),
             "om_sample_logits": (None, [vp, i32, f32, vp, i32, vp]),
             "om_ctrl_advance_sample": (i32, [vp, vp, f32, vp, vp, vp, vp]),
             "om_sample_decode": (i32, [vp, vp, i32, i32, i32, f32, u64, vp]),
@@ -255,6 +256,17 @@ class Rng:
 
     def uniform(self) -> float:
         return lib().om_uniform(self.ptr)
+
+
+def exp_neg(x: float) -> float:
+    """The fp32 exponential (x <= 0) of the sampling probabilities."""
+    return lib().om_exp_neg(float(x))
+
+
+def sample_weight(z: float, mx: float, tau: float, V: int) -> int:
+    """Integer weight floor(exp((z - mx) / tau) 2^B) of a token, B = 63 -
+    ceil(log2(V + 1)): p(v) = weight / sum of weights."""
+    return int(lib().om_sample_weight(float(z), float(mx), float(tau), int(V)))
 
 
 def sample_logits(z, tau: float, rng: Rng, n: int):

@@ -45,7 +45,9 @@
  *     i ascending ("Key points": prompt n-grams in the pool help).
  *  R10 sampling verification (the summary says the method supports sampling
  *     and keeps the output distribution; it gives no algorithm, so this one
- *     is designed here): temperature softmax p = softmax(z / tau) of a row;
+ *     is designed here): temperature softmax p = softmax(z / tau) of a row
+ *     (exponentials in fp32 by om_exp_neg, as exact integer weights: see
+ *     om_sample_weight);
  *     at each candidate level the distinct candidate tokens v are tried in
  *     candidate order, v accepted with probability p(v) / (1 - mass of the
  *     tokens already rejected at this level); if none is accepted, the token
@@ -647,19 +649,79 @@ OM_EXPORT void om_ctrl_window(const om_ctrl* k, int* out)
 /* Uniform draw in [0,1): the top 24 bits of the next splitmix64 output. */
 OM_EXPORT double om_uniform(uint64_t* rng) { return (double)(om_splitmix64(rng) >> 40) * (1.0 / 16777216.0); }
 
-/* p = softmax(z / tau) in double: the maximum first, then exp((z - max) /
- * tau) and their sum in ascending token order. */
-static void softmax_tau(const float* z, int V, float tau, double* p)
+/* exp(x) for x <= 0 in fp32, the exponential of the sampling probabilities.
+ * Range reduction after Cody and Waite: k = the integer nearest x log2(e),
+ * t = x - k ln 2 with ln 2 split into a float and the float remainder
+ * (two fused multiply-adds, so that t keeps its precision for large |x|),
+ * |t| <= 0.35; e^t by its Taylor series to degree 7 (truncation below 6e-9
+ * relative), by Horner's rule with fused multiply-adds; then scaled by 2^k
+ * (exact).  Results below 2^-125 are flushed to 0.  Every step is a
+ * correctly rounded IEEE fp32 operation, so any implementation performing
+ * the same operations (the CUDA library's sampling kernels do) returns the
+ * same bits. */
+OM_EXPORT float om_exp_neg(float x)
+{
+    const float k = rintf(x * 0x1.715476p+0f); /* log2(e) */
+    if (k < -125.0f) return 0.0f;
+    float t = fmaf(-k, 0x1.62e430p-1f, x);  /* ln 2, float part */
+    t = fmaf(-k, -0x1.05c610p-29f, t);      /* ln 2, remainder */
+    float q = 0x1.a01a02p-13f;              /* 1/7! */
+    q = fmaf(q, t, 0x1.6c16c2p-10f);        /* 1/6! */
+    q = fmaf(q, t, 0x1.111112p-7f);         /* 1/5! */
+    q = fmaf(q, t, 0x1.555556p-5f);         /* 1/4! */
+    q = fmaf(q, t, 0x1.555556p-3f);         /* 1/3! */
+    q = fmaf(q, t, 0.5f);
+    q = fmaf(q, t, 1.0f);
+    q = fmaf(q, t, 1.0f);
+    return ldexpf(q, (int)k);
+}
+
+/* The sampling distribution as exact integers.  e(v) = om_exp_neg of
+ * (z_v - max) / tau (an fp32 subtraction, then an fp32 division); the weight of
+ * token v is E(v) = floor(e(v) 2^B) with B = 63 - ceil(log2(V + 1)), so that
+ * S = sum of all E(v) < 2^63; p(v) = E(v) / S.  Every sum and comparison
+ * below is exact integer arithmetic (products in 128 bits), so the result
+ * does not depend on the order of the sums.  A uniform u = U / 2^24 (U the
+ * top 24 bits of the next splitmix64 output):
+ *  - accepts v against the mass R already rejected at a level when
+ *    u (1 - R/S) < p(v), i.e. U (S - R) < E(v) 2^24;
+ *  - draws from p restricted to the tokens not excluded the first token, in
+ *    ascending order, whose running weight A has A 2^24 > U (S - R); the last
+ *    admissible token of nonzero weight if none (cannot happen unless every
+ *    admissible weight is 0). */
+static int sample_bits(int V)
+{
+    int b = 0;
+    while ((1LL << b) < (long long)V + 1) b++;
+    return 63 - b;
+}
+
+OM_EXPORT uint64_t om_sample_weight(float z, float mx, float tau, int V)
+{
+    const float d = z - mx;
+    const float e = om_exp_neg(d / tau);
+    return (uint64_t)ldexpf(e, sample_bits(V));
+}
+
+static uint64_t weights_tau(const float* z, int V, float tau, uint64_t* E)
 {
     float mx = z[0];
     for (int v = 1; v < V; v++)
         if (z[v] > mx) mx = z[v];
-    double sum = 0.0;
+    uint64_t S = 0;
     for (int v = 0; v < V; v++) {
-        p[v] = exp(((double)z[v] - (double)mx) / (double)tau);
-        sum += p[v];
+        E[v] = om_sample_weight(z[v], mx, tau, V);
+        S += E[v];
     }
-    for (int v = 0; v < V; v++) p[v] /= sum;
+    return S;
+}
+
+static uint64_t uniform24(uint64_t* rng) { return om_splitmix64(rng) >> 40; }
+
+/* U (S - R) < E 2^24 */
+static int accepts(uint64_t U, uint64_t S, uint64_t R, uint64_t E)
+{
+    return (unsigned __int128)U * (S - R) < ((unsigned __int128)E << 24);
 }
 
 static int in_list(const int* a, int n, int x)
@@ -669,20 +731,18 @@ static int in_list(const int* a, int n, int x)
     return 0;
 }
 
-/* Draw from p restricted to the tokens not in excl[0..ne-1] (whose mass is
- * mass_excl): the first token, in ascending order, whose running sum of p
- * exceeds u * (1 - mass_excl); the last admissible token of nonzero mass if
- * rounding leaves the target unreached. */
-static int draw_excluding(const double* p, int V, const int* excl, int ne, double mass_excl, double u)
+/* Draw with weights E (total S) restricted to the tokens not in
+ * excl[0..ne-1] (whose weight is R), uniform U. */
+static int draw_excluding(const uint64_t* E, int V, uint64_t S, const int* excl, int ne, uint64_t R, uint64_t U)
 {
-    const double target = u * (1.0 - mass_excl);
-    double acc = 0.0;
+    const unsigned __int128 target = (unsigned __int128)U * (S - R);
+    uint64_t acc = 0;
     int last = -1;
     for (int v = 0; v < V; v++) {
         if (in_list(excl, ne, v)) continue;
-        if (p[v] > 0.0) last = v;
-        acc += p[v];
-        if (acc > target) return v;
+        if (E[v] > 0) last = v;
+        acc += E[v];
+        if (((unsigned __int128)acc << 24) > target) return v;
     }
     return last >= 0 ? last : 0;
 }
@@ -691,10 +751,10 @@ static int draw_excluding(const double* p, int V, const int* excl, int ne, doubl
  * goes through). */
 OM_EXPORT void om_sample_logits(const float* z, int V, float tau, uint64_t* rng, int n, int* out)
 {
-    double* p = (double*)malloc(sizeof(double) * V);
-    softmax_tau(z, V, tau, p);
-    for (int i = 0; i < n; i++) out[i] = draw_excluding(p, V, NULL, 0, 0.0, om_uniform(rng));
-    free(p);
+    uint64_t* E = (uint64_t*)malloc(sizeof(uint64_t) * V);
+    const uint64_t S = weights_tau(z, V, tau, E);
+    for (int i = 0; i < n; i++) out[i] = draw_excluding(E, V, S, NULL, 0, 0, uniform24(rng));
+    free(E);
 }
 
 /*
@@ -708,7 +768,7 @@ OM_EXPORT int om_ctrl_advance_sample(om_ctrl* k, const float* logits, float tau,
                                      int* rows, int* gstar)
 {
     const int V = k->V, n1 = k->N - 1, Gp = k->Gp;
-    double* p = (double*)malloc(sizeof(double) * V);
+    uint64_t* E = (uint64_t*)malloc(sizeof(uint64_t) * V);
     int* alive = (int*)malloc(sizeof(int) * (Gp > 0 ? Gp : 1));
     int* rej = (int*)malloc(sizeof(int) * (Gp > 0 ? Gp : 1));
     int* amax = (int*)malloc(sizeof(int) * k->T);
@@ -717,23 +777,22 @@ OM_EXPORT int om_ctrl_advance_sample(om_ctrl* k, const float* logits, float tau,
     int row = 0, m = 0, g_best = -1, done = 0;
     rows[0] = 0;
     for (int i = 0; i < n1 && !done; i++) {
-        softmax_tau(logits + (size_t)row * V, V, tau, p);
+        const uint64_t S = weights_tau(logits + (size_t)row * V, V, tau, E);
         int nrej = 0, acc_g = -1;
-        double mass_rej = 0.0;
+        uint64_t R = 0;
         for (int g = 0; g < Gp && acc_g < 0; g++) {
             if (!alive[g]) continue;
             const int v = k->cands[(size_t)g * n1 + i];
             if (in_list(rej, nrej, v)) continue;  /* a value already tried at this level */
-            const double u = om_uniform(rng);
-            if (u * (1.0 - mass_rej) < p[v]) {
+            if (accepts(uniform24(rng), S, R, E[v])) {
                 acc_g = g;
             } else {
                 rej[nrej++] = v;
-                mass_rej += p[v];
+                R += E[v];
             }
         }
         if (acc_g < 0) {
-            emit[m] = draw_excluding(p, V, rej, nrej, mass_rej, om_uniform(rng));
+            emit[m] = draw_excluding(E, V, S, rej, nrej, R, uniform24(rng));
             done = 1;
             break;
         }
@@ -751,12 +810,12 @@ OM_EXPORT int om_ctrl_advance_sample(om_ctrl* k, const float* logits, float tau,
     for (int i = 0; i < m; i++) rows[i + 1] = row_vf(k, g_best, i);
     if (!done) {
         /* every level accepted: the bonus token from the last accepted row */
-        softmax_tau(logits + (size_t)row * V, V, tau, p);
-        emit[m] = draw_excluding(p, V, NULL, 0, 0.0, om_uniform(rng));
+        const uint64_t S = weights_tau(logits + (size_t)row * V, V, tau, E);
+        emit[m] = draw_excluding(E, V, S, NULL, 0, 0, uniform24(rng));
     }
     if (gstar) *gstar = g_best;
     harvest_and_shift(k, amax);
-    free(p); free(alive); free(rej); free(amax);
+    free(E); free(alive); free(rej); free(amax);
     return m + 1;
 }
 
