@@ -225,6 +225,14 @@ LA_API int la_debug_pool(la_ctx* ctx, int32_t key, int32_t* host, int cap, int* 
 /* Pages: "Summary" (the 2D window of Jacobi iteration history).
  * Lookahead window, int32[N-1][W] into host (cap ints). */
 LA_API int la_debug_window(la_ctx* ctx, int32_t* host, int cap);
+/* No counterpart on the pages (a parity accessor for the controller).
+ * Replace the model's argmaxes seen by verification, harvest and window
+ * update with host[0..n) (one token per step row, n = T) for every following
+ * la_step until called with host = NULL.  The forward still runs; only the
+ * integer controller reads the override, so that a test can drive it through
+ * any acceptance pattern.  LA_ERR_ARG for n != T or a token outside the
+ * vocabulary.  Synchronises the context's stream. */
+LA_API int la_debug_set_argmax_override(la_ctx* ctx, const int32_t* host, int n);
 
 /* No counterpart on the pages: message of the last failure on ctx. */
 LA_API const char* la_last_error(la_ctx* ctx);

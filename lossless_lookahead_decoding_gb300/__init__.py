@@ -27,6 +27,7 @@ LA_PRESEED_PROMPT, LA_DEBUG_LOGITS, LA_NO_GRAPH, LA_SIMT, LA_PROFILE, LA_ATTN_TC
 EXPORTS = ("la_workspace_bytes", "la_create", "la_prefill", "la_step", "la_generate", "la_set_sampling", "la_get_stats",
            "la_get_profile",
            "la_debug_logits", "la_debug_argmax", "la_debug_rows", "la_debug_pool", "la_debug_window",
+           "la_debug_set_argmax_override",
            "la_last_error", "la_destroy", "la_attention", "la_attention_noalloc", "la_pool_create", "la_pool_insert", "la_pool_lookup", "la_pool_size",
            "la_pool_destroy")
 
@@ -82,6 +83,7 @@ def lib():
             "la_debug_rows": (i32, [vp, vp, vp, i32, vp, vp]),
             "la_debug_pool": (i32, [vp, i32, vp, i32, vp]),
             "la_debug_window": (i32, [vp, vp, i32]),
+            "la_debug_set_argmax_override": (i32, [vp, vp, i32]),
             "la_last_error": (C.c_char_p, [vp]),
             "la_destroy": (None, [vp]),
             "la_attention": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp]),
@@ -196,6 +198,15 @@ def la_debug_window(ctx, W: int, N: int) -> np.ndarray:
     out = np.zeros(max(W * (N - 1), 1), np.int32)
     _check(ctx, lib().la_debug_window(ctx, _p(out), len(out)))
     return out[: W * (N - 1)].reshape(N - 1, W).copy()
+
+
+def la_debug_set_argmax_override(ctx, amax) -> None:
+    """amax: one token per step row, or None to clear the override."""
+    if amax is None:
+        _check(ctx, lib().la_debug_set_argmax_override(ctx, None, 0))
+        return
+    a = np.ascontiguousarray(amax, dtype=np.int32)
+    _check(ctx, lib().la_debug_set_argmax_override(ctx, _p(a), len(a)))
 
 
 def la_last_error(ctx) -> str:
@@ -338,3 +349,6 @@ class Decoder:
 
     def window(self):
         return la_debug_window(self.ctx, self.W, self.N)
+
+    def override_argmax(self, amax):
+        la_debug_set_argmax_override(self.ctx, amax)

@@ -119,7 +119,7 @@ void launch_prefill_rows(cudaStream_t s, const DState* st, const int* prompt, in
                          int* pos);
 void launch_verify_update(cudaStream_t s, DState* st, const int* tok, const int* amax, int* win,
                           PoolView pool, int W, int N, int G, const float* logits, int V, float tau,
-                          const unsigned long long* stats, bool diag);
+                          const unsigned long long* stats, bool diag, const int* ovr);
 void launch_row_stats(cudaStream_t s, const float* logits, int V, float tau, int vbase, int T,
                       unsigned long long* stats);
 void launch_commit(cudaStream_t s, const DState* st, bool prefill, int n_prefill, int n_max, const void* KS,

@@ -560,8 +560,10 @@ __device__ void sample_verify(DState* st, const int* tok, const float* logits, i
 // last level's row j-1 in column j.
 __global__ void __launch_bounds__(kVerifyWarps * 32)
     k_verify_update(DState* st, const int* tok, const int* amax, int* win, PoolView pool, int W, int N, int G,
-                    const float* logits, int V, float tau, const unsigned long long* stats, int diag)
+                    const float* logits, int V, float tau, const unsigned long long* stats, int diag,
+                    const int* ovr)
 {
+    if (ovr[0]) amax = ovr + 1;  // debug: the rows' argmaxes set from the host
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int n1 = N - 1, ncand = st->ncand, P = st->P;
     const int a0 = amax[0];
@@ -652,10 +654,10 @@ __global__ void __launch_bounds__(kVerifyWarps * 32)
 
 void launch_verify_update(cudaStream_t s, DState* st, const int* tok, const int* amax, int* win, PoolView pool,
                           int W, int N, int G, const float* logits, int V, float tau,
-                          const unsigned long long* stats, bool diag)
+                          const unsigned long long* stats, bool diag, const int* ovr)
 {
     k_verify_update<<<1, kVerifyWarps * 32, 0, s>>>(st, tok, amax, win, pool, W, N, G, logits, V, tau, stats,
-                                                    diag ? 1 : 0);
+                                                    diag ? 1 : 0, ovr);
 }
 
 // ------------------------------------------------------------------ commit ---

@@ -58,6 +58,7 @@ struct la_ctx {
     uint64_t seed = 0;
     float tau = 0.f;              // > 0: sampling verification at this temperature
     unsigned long long* SSTAT = nullptr;  // per-row softmax max (float bits) / integer weight total for sampling
+    int* AOVR = nullptr;                  // debug argmax override: [0] on, [1..T] the rows' argmaxes
     cudaStream_t s = nullptr;
     bool bf16 = false, use_tc = false, use_attn_mma = false, use_attn_tc = false;
     AttnTcPlan atc{};  // the step's attention on the tensor cores (tensor maps, launch shape)
@@ -199,6 +200,7 @@ static Layout make_layout(const la_model_desc* d, int W, int N, int G, int* pool
     const size_t pt = attn_tc_partial_bytes(d->n_heads, d->head_dim, d->max_seq);
     ly.add(pa > pt ? pa : pt);                           // 30 attention split partials
     ly.add(kRows * 16);                                  // 31 sampling row statistics
+    ly.add((kRows + 1) * 4);                             // 32 argmax override: [0] on, [1..] rows
     return ly;
 }
 
@@ -384,7 +386,7 @@ static void enqueue_step(la_ctx* c)
     const int vbase = 1 + c->W * (c->N - 1);
     if (c->tau > 0.f) launch_row_stats(c->s, c->LOGITS, c->d.vocab, c->tau, vbase, c->T, c->SSTAT);
     launch_verify_update(c->s, c->st, c->tok, c->AMAX, c->win, c->pool, c->W, c->N, c->G, c->LOGITS, c->d.vocab,
-                         c->tau, c->SSTAT, (c->flags & LA_MASK_DIAG) != 0);
+                         c->tau, c->SSTAT, (c->flags & LA_MASK_DIAG) != 0, c->AOVR);
     launch_commit(c->s, c->st, false, 0, c->N, c->KS, c->VS, c->KC, c->VC, c->d.n_layers, c->d.n_kv_heads,
                   c->d.head_dim, c->d.max_seq, c->esz);
     c->prof.end(c->s, P_CONTROL, 0, 0);
@@ -532,6 +534,7 @@ extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* w
     ctx->dbg = (int*)(b + ly.off[26]);
     ctx->AMAXP = (unsigned long long*)(b + ly.off[27]);
     ctx->SSTAT = (unsigned long long*)(b + ly.off[31]);
+    ctx->AOVR = (int*)(b + ly.off[32]);
     ctx->pool = PoolView{pk, pk + cap, (int*)(b + ly.off[23]), pk + 2 * cap, (int*)(b + ly.off[24]),
                          &ctx->st->status, cap, lg, G, N - 1};
     int* gl1 = (int*)(b + ly.off[28]);
@@ -568,6 +571,7 @@ extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* w
         // weight, must hold finite values
         ck(cudaMemset(ctx->ws + ly.off[0], 0, ly.off[11] - ly.off[0]));
         ck(cudaMemset(ctx->AMAXP, 0, kRows * 8));
+        ck(cudaMemset(ctx->AOVR, 0, (kRows + 1) * 4));
         ck(cudaMemcpy(rs1, rel.data(), kRows * 4, cudaMemcpyHostToDevice));
         ck(cudaMemcpy(rs1 + kRows, grp.data(), kRows * 4, cudaMemcpyHostToDevice));
         ck(cudaMemcpy(map1, map.data(), map.size() * 4, cudaMemcpyHostToDevice));
@@ -905,6 +909,22 @@ extern "C" int la_debug_pool(la_ctx* ctx, int32_t key, int32_t* host, int cap, i
     LA_CK(cudaMemcpyAsync(host, dout, (size_t)tot * 4, cudaMemcpyDeviceToHost, ctx->s));
     LA_CK(cudaMemcpyAsync(count, dcnt, 4, cudaMemcpyDeviceToHost, ctx->s));
     LA_CK(cudaStreamSynchronize(ctx->s));
+    return LA_OK;
+}
+
+extern "C" int la_debug_set_argmax_override(la_ctx* ctx, const int32_t* host, int n)
+{
+    if (!ctx) return LA_ERR_ARG;
+    if (host && n != ctx->T) return fail(ctx, LA_ERR_ARG, "the override needs one argmax per step row");
+    std::vector<int> buf((size_t)ctx->T + 1, 0);
+    if (host) {
+        for (int i = 0; i < n; i++)
+            if (host[i] < 0 || host[i] >= ctx->d.vocab) return fail(ctx, LA_ERR_ARG, "token id out of range");
+        buf[0] = 1;
+        memcpy(buf.data() + 1, host, (size_t)n * 4);
+    }
+    LA_CK(cudaMemcpyAsync(ctx->AOVR, buf.data(), buf.size() * 4, cudaMemcpyHostToDevice, ctx->s));
+    LA_CK(cudaStreamSynchronize(ctx->s));  // buf is a host temporary
     return LA_OK;
 }
 

@@ -165,3 +165,58 @@ def test_diagonal_levels_against_oracle(mode, WNG):
     g = gpu_decoder(cfg, w, dtype, 0, 2, 0, 256, flags=mflags).generate(prompt, 64)
     la = gpu_decoder(cfg, w, dtype, *WNG, 256, flags=mflags | LA.LA_MASK_DIAG).generate(prompt, 64)
     assert np.array_equal(la, g)
+
+
+def _override_replay(cfg, w, W, N, G, n_steps, seed, flags=0, max_seq=256, prompt=None):
+    """Drive the GPU controller with chosen argmaxes (la_debug_set_argmax_override)
+    through every acceptance length, and the oracle controller with the same
+    ones: rows, emitted tokens, committed length, window and pool bit-exact
+    every step."""
+    import lossless_lookahead_decoding_gb300 as LA
+    prompt = I.make_prompt("tiny") if prompt is None else prompt
+    dec = gpu_decoder(cfg, w, 1, W, N, G, max_seq, flags=flags)
+    ctrl = O.Controller(W, N, G, cfg.vocab, variant=O.DIAGONAL if flags & LA.LA_MASK_DIAG else 0)
+    ctrl.init(prompt, seed=2, preseed=bool(flags & LA.LA_PRESEED_PROMPT))
+    dec.prefill(prompt)
+    g = np.random.default_rng(seed)
+    vocab = np.unique(prompt)
+    c, P = int(prompt[-1]), len(prompt) - 1
+    seen = set()
+    for step in range(n_steps):
+        tok, pos, _ = ctrl.rows(c, P)
+        T = len(tok)
+        # argmaxes from the prompt's few distinct tokens, so that the pool
+        # soon holds n-grams for the current token
+        amax = g.choice(vocab, dec.T).astype(np.int32)
+        ncand = (T - 1 - W * (N - 1)) // (N - 1)
+        if ncand and step % 4:
+            # accept the first m tokens of candidate gs: row 0's argmax is its
+            # first token, row (gs, i-1)'s its i-th
+            gs, m = int(g.integers(0, ncand)), int(g.integers(0, N))
+            base = 1 + W * (N - 1) + gs * (N - 1)
+            for i in range(m):
+                amax[0 if i == 0 else base + i - 1] = tok[base + i]
+        dec.override_argmax(amax)
+        emit = dec.step()
+        tok_g, pos_g, _ = dec.rows()
+        assert np.array_equal(tok_g[:T], tok) and np.array_equal(pos_g[:T], pos)
+        emit_o, _, _ = ctrl.advance(amax[:T])
+        assert np.array_equal(emit, emit_o), (step, emit, emit_o)
+        seen.add(len(emit))
+        assert np.array_equal(dec.window(), ctrl.window())
+        for key in set(int(x) for x in tok):
+            assert np.array_equal(dec.pool(key), ctrl.pool(key)), key
+        P += len(emit)
+        c = int(emit[-1])
+    dec.override_argmax(None)
+    dec.close()
+    return seen
+
+
+@pytest.mark.parametrize("WNG,flags", [((4, 3, 4), 0), ((5, 4, 3), 0), ((3, 5, 4), 1), ((4, 4, 4), 64)],
+                         ids=["columns", "N4", "preseed", "diagonal"])
+def test_argmax_override_drives_every_acceptance_length(WNG, flags):
+    cfg = I.MODELS["tiny"]
+    w = _weights(cfg, True)
+    seen = _override_replay(cfg, w, *WNG, 40, seed=sum(WNG) + flags, flags=flags)
+    assert seen == set(range(1, WNG[1] + 1)), seen  # 1..N tokens per step all occurred

@@ -150,3 +150,15 @@ def test_full_depth_controller_replay(workload, max_seq):
     g = greedy.generate(prompt, len(out))
     greedy.close()
     assert np.array_equal(np.array(out, np.int32), g)
+
+
+def test_7b_width_controller_under_argmax_override():
+    """The 121-row step's controller (15 window columns, 15 candidates of 4
+    tokens) driven through every acceptance length by overriding the argmaxes,
+    against the oracle controller fed the same ones (2-layer 7B slice)."""
+    import test_gpu_decode as D
+    cfg = I.MODELS["7b"].sliced(2)
+    full = I.make_weights(I.MODELS["7b"], 0, bf16=True, layers=[0, 1])
+    w = {k: (v[:2] if isinstance(v, list) else v) for k, v in full.items()}
+    seen = D._override_replay(cfg, w, 15, 5, 15, 40, seed=8, max_seq=768, prompt=I.make_prompt("7b"))
+    assert seen == {1, 2, 3, 4, 5}, seen
