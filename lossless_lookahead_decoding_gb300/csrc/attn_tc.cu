@@ -430,10 +430,12 @@ __device__ __forceinline__ uint32_t tile_chunk(uint32_t base, int rows, int row,
     return base + (c >> 3) * rows * 128 + row * 128 + (((c & 7) ^ (row & 7)) << 4);
 }
 
-// at most 128 registers a thread: a window CTA (256 threads) and a cache CTA
-// fit on one SM together, so the two kernels overlap
+// at most 112 registers a thread: a window CTA (8 warps) then fits on an SM
+// beside a cache CTA (10 warps at 96 registers) -- each of the SM's four
+// register-file quarters holds 2 window warps next to up to 3 cache warps --
+// so the two kernels overlap wherever the cache kernel's CTAs landed
 template <int HD>
-__global__ void __launch_bounds__(kBWarps * 32, 2)
+__global__ void __maxnreg__(112)
     k_attn_window(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const __grid_constant__ CUtensorMap ksmap, const __grid_constant__ CUtensorMap vsmap, TcAttnArgs a)
 {
@@ -710,16 +712,23 @@ __global__ void __launch_bounds__(kBWarps * 32, 2)
         if (r >= 0) {
             const int nA = sNA[slot];
             const float* pr = part_row<HD>(a, h, 0, r) + HD;
+            // every split's (max, sum) in flight together, then max, weights
+            // and the sum in ascending split order from registers
+            float2 ml[kMaxSp];
+#pragma unroll
+            for (int sp = 0; sp < kMaxSp; sp++)
+                ml[sp] = sp < nA ? __ldcg((const float2*)(pr + sp * pstride)) : make_float2(-INFINITY, 0.f);
             float M = sMB[slot];
-#pragma unroll 8
-            for (int sp = 0; sp < nA; sp++) M = fmaxf(M, pr[sp * pstride]);
+#pragma unroll
+            for (int sp = 0; sp < kMaxSp; sp++) M = fmaxf(M, ml[sp].x);
             float Ls = 0.f;
-#pragma unroll 8
-            for (int sp = 0; sp < nA; sp++) {
-                const float2 ml = *(const float2*)(pr + sp * pstride);
-                const float w = ex2(ml.x - M);
-                sW[slot * kMaxSp + sp] = w;
-                Ls += ml.y * w;
+#pragma unroll
+            for (int sp = 0; sp < kMaxSp; sp++) {
+                if (sp < nA) {
+                    const float w = ex2(ml[sp].x - M);
+                    sW[slot * kMaxSp + sp] = w;
+                    Ls += ml[sp].y * w;
+                }
             }
             const float wB = ex2(sMB[slot] - M);
             sWB[slot] = wB;
@@ -729,30 +738,60 @@ __global__ void __launch_bounds__(kBWarps * 32, 2)
     }
     __syncthreads();
     // O = sum over splits (ascending) of w O_split, + wB O_B; out = O / sum
-    constexpr int C4 = HD / 4;
+    // Items (slot, 4 output dims), kIB per thread at a time, the loads of
+    // kSB splits of all of them in flight together; each item's sum runs in
+    // ascending split order.
+    constexpr int C4 = HD / 4, kIB = 4, kSB = 4;
     const int n_items = sList[kRows] * C4;
-#pragma unroll 2
-    for (int i = tid; i < n_items; i += blockDim.x) {
-        const int slot = sList[i / C4], c4 = i % C4, r = sRow[slot], nA = sNA[slot];
-        const float* pr = part_row<HD>(a, h, 0, r) + c4 * 4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-        for (int sp = 0; sp < nA; sp++) {
-            const float4 x = *(const float4*)(pr + sp * pstride);
-            const float w = sW[slot * kMaxSp + sp];
-            acc.x += x.x * w;
-            acc.y += x.y * w;
-            acc.z += x.z * w;
-            acc.w += x.w * w;
+    for (int i0 = tid; i0 < n_items; i0 += kIB * blockDim.x) {
+        int slot[kIB], nA[kIB];
+        const float* pr[kIB];
+        float4 acc[kIB];
+        int nmax = 0;
+#pragma unroll
+        for (int k = 0; k < kIB; k++) {
+            const int i = i0 + k * blockDim.x;
+            slot[k] = i < n_items ? sList[i / C4] : 0;
+            nA[k] = i < n_items ? sNA[slot[k]] : 0;
+            pr[k] = part_row<HD>(a, h, 0, i < n_items ? sRow[slot[k]] : 0) + (i % C4) * 4;
+            acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            nmax = max(nmax, nA[k]);
         }
-        const float wB = sWB[slot], inv = sLs[slot];
-        const float4 ob = *(const float4*)(sO + slot * (HD + 4) + c4 * 4);
-        __nv_bfloat162 lo2 = __floats2bfloat162_rn((acc.x + ob.x * wB) / inv, (acc.y + ob.y * wB) / inv);
-        __nv_bfloat162 hi2 = __floats2bfloat162_rn((acc.z + ob.z * wB) / inv, (acc.w + ob.w * wB) / inv);
-        uint2 u;
-        u.x = *reinterpret_cast<uint32_t*>(&lo2);
-        u.y = *reinterpret_cast<uint32_t*>(&hi2);
-        *(uint2*)(a.out + (size_t)r * dq + h * HD + c4 * 4) = u;
+        for (int s0 = 0; s0 < nmax; s0 += kSB) {
+            float4 x[kIB][kSB];
+#pragma unroll
+            for (int k = 0; k < kIB; k++)
+#pragma unroll
+                for (int j = 0; j < kSB; j++)
+                    x[k][j] = s0 + j < nA[k] ? __ldcg((const float4*)(pr[k] + (s0 + j) * pstride))
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < kIB; k++)
+#pragma unroll
+                for (int j = 0; j < kSB; j++) {
+                    if (s0 + j < nA[k]) {
+                        const float w = sW[slot[k] * kMaxSp + s0 + j];
+                        acc[k].x += x[k][j].x * w;
+                        acc[k].y += x[k][j].y * w;
+                        acc[k].z += x[k][j].z * w;
+                        acc[k].w += x[k][j].w * w;
+                    }
+                }
+        }
+#pragma unroll
+        for (int k = 0; k < kIB; k++) {
+            const int i = i0 + k * blockDim.x;
+            if (i >= n_items) continue;
+            const int sl = slot[k], c4 = i % C4, r = sRow[sl];
+            const float wB = sWB[sl], inv = sLs[sl];
+            const float4 ob = *(const float4*)(sO + sl * (HD + 4) + c4 * 4);
+            __nv_bfloat162 lo2 = __floats2bfloat162_rn((acc[k].x + ob.x * wB) / inv, (acc[k].y + ob.y * wB) / inv);
+            __nv_bfloat162 hi2 = __floats2bfloat162_rn((acc[k].z + ob.z * wB) / inv, (acc[k].w + ob.w * wB) / inv);
+            uint2 u;
+            u.x = *reinterpret_cast<uint32_t*>(&lo2);
+            u.y = *reinterpret_cast<uint32_t*>(&hi2);
+            *(uint2*)(a.out + (size_t)r * dq + h * HD + c4 * 4) = u;
+        }
     }
 }
 
@@ -864,6 +903,7 @@ int attn_tc_plan(AttnTcPlan* pl, const void* Q, int q_rows, const void* KC, cons
     pl->bq = bq;
     pl->nsa = nsa;
     pl->cta_cap = cap;
+    pl->cache_smem = (hd == 128 ? ASmem<128>::kBytes : ASmem<64>::kBytes) + 1024;
     pl->n_items = n_items;
     pl->ok = true;
     return LA_OK;
@@ -893,11 +933,11 @@ void launch_attn_tc(cudaStream_t s, const AttnTcPlan& pl, int layer, int ks_row0
     a.sl2 = 1.4426950408889634f / sqrtf((float)pl.hd);
     const dim3 gc(pl.H / pl.hpc, cta_y < 1 ? 1 : cta_y), gw(pl.H, (pl.n_items + kBWarps - 1) / kBWarps);
     if (pl.hd == 128) {
-        launch_pdl(k_attn_cache<128>, gc, dim3(kAThreads), ASmem<128>::kBytes + 1024, s, pl.qmap, pl.kmap, pl.vmap, a);
+        launch_pdl(k_attn_cache<128>, gc, dim3(kAThreads), pl.cache_smem, s, pl.qmap, pl.kmap, pl.vmap, a);
         launch_pdl(k_attn_window<128>, gw, dim3(kBWarps * 32), BSmem<128>::kBytes + 1024, s, pl.kmap, pl.vmap,
                    pl.ksmap, pl.vsmap, a);
     } else {
-        launch_pdl(k_attn_cache<64>, gc, dim3(kAThreads), ASmem<64>::kBytes + 1024, s, pl.qmap, pl.kmap, pl.vmap, a);
+        launch_pdl(k_attn_cache<64>, gc, dim3(kAThreads), pl.cache_smem, s, pl.qmap, pl.kmap, pl.vmap, a);
         launch_pdl(k_attn_window<64>, gw, dim3(kBWarps * 32), BSmem<64>::kBytes + 1024, s, pl.kmap, pl.vmap,
                    pl.ksmap, pl.vsmap, a);
     }

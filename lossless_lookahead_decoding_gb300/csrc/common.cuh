@@ -157,7 +157,7 @@ void launch_argmax(cudaStream_t s, const float* logits, int* amax, int rows, int
 // recent window, per row group), merged per row
 struct AttnTcPlan {
     CUtensorMap qmap, kmap, vmap, ksmap, vsmap;
-    int H, Hkv, hd, max_seq, hpc, bq, nsa, cta_cap, n_items;
+    int H, Hkv, hd, max_seq, hpc, bq, nsa, cta_cap, n_items, cache_smem;
     bool ok;
 };
 int attn_tc_delta();  // rows may sit at most this many positions past P
