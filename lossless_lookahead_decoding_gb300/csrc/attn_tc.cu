@@ -741,7 +741,7 @@ __global__ void __maxnreg__(112)
     // Items (slot, 4 output dims), kIB per thread at a time, the loads of
     // kSB splits of all of them in flight together; each item's sum runs in
     // ascending split order.
-    constexpr int C4 = HD / 4, kIB = 4, kSB = 4;
+    constexpr int C4 = HD / 4, kIB = 2, kSB = 4;
     const int n_items = sList[kRows] * C4;
     for (int i0 = tid; i0 < n_items; i0 += kIB * blockDim.x) {
         int slot[kIB], nA[kIB];
