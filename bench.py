@@ -342,6 +342,9 @@ def run_ours(args, rank, world):
         "wall_s_timed": round(wall, 3),
         "greedy": {"value": round(g_value, 2), "unit": "tokens/s", "ms_per_step": round(g_step_ms, 4)},
         "speedup_vs_greedy": round(value / g_value, 4),
+        # the cost of the T - 1 extra rows: lookahead step time minus the
+        # same library's greedy step time over the same prompt and steps
+        "lookahead_premium_ms": round(step_ms - g_step_ms, 4),
         "lossless_vs_greedy": lossless, "full_generation_steps": full_steps,
         "verification": {"mode": "sampling", "temperature": sample} if sample > 0 else {"mode": "greedy"},
         "step_roofline": {"t_roof_ms": round(t_roof * 1e3, 4), "frac": round(t_roof * 1e3 / step_ms, 4),
