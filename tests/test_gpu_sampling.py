@@ -3,10 +3,12 @@
 The GPU runs the tiny workload with sampling verification; after every step
 the oracle controller is fed the GPU's own logits and its uniform stream
 (same splitmix64 seed).  The emitted tokens, window and pool must then be
-bit-exact: both sides take every accept/reject decision and every draw in
-fp64 from the same logits, so they differ only if a uniform lands within
-~1e-15 of a threshold.  tau -> 0 must reproduce greedy decoding, and a
-temperature of 0 must restore it.
+bit-exact: both sides turn the same logits into the same integer weights
+(the same fp32 exponential, operation for operation) and take every
+accept/reject decision and every draw in exact integer arithmetic.  Also
+with the diagonal-levels mask and with the tensor-core attention option.
+tau -> 0 must reproduce greedy decoding, and a temperature of 0 must restore
+it.
 """
 import math
 
@@ -31,14 +33,15 @@ def _setup(dtype):
     return cfg, w, I.make_prompt("tiny"), I.LOOKAHEAD["tiny"]
 
 
-@pytest.mark.parametrize("dtype", [0, 1], ids=["fp32", "bf16"])
-def test_sampled_steps_replay_the_oracle_rule(dtype):
+@pytest.mark.parametrize("dtype,flags", [(0, 0), (1, 0), (1, 64), (1, 32)],
+                         ids=["fp32", "bf16", "bf16-diagonal", "bf16-attntc"])
+def test_sampled_steps_replay_the_oracle_rule(dtype, flags):
     import lossless_lookahead_decoding_gb300 as LA
     cfg, w, prompt, (W, N, G) = _setup(dtype)
     tau, seed = 0.05, 77
-    dec = gpu_decoder(cfg, w, dtype, W, N, G, 256, flags=LA.LA_DEBUG_LOGITS)
+    dec = gpu_decoder(cfg, w, dtype, W, N, G, 256, flags=flags | LA.LA_DEBUG_LOGITS)
     dec.set_sampling(tau, seed)
-    ctrl = O.Controller(W, N, G, cfg.vocab)
+    ctrl = O.Controller(W, N, G, cfg.vocab, variant=O.DIAGONAL if flags & LA.LA_MASK_DIAG else 0)
     ctrl.init(prompt, seed=2)
     rng = O.Rng(seed)
     dec.prefill(prompt)
