@@ -62,7 +62,6 @@ constexpr int kAThreads = 320;      // warp 0 TMA, warp 1 MMA + TMEM, warps 2..9
 constexpr uint32_t kTmemCols = 256; // S [128 columns] + O [head_dim columns]
 constexpr int kBWarps = 8;          // region B: one row-group slab per warp
 constexpr int kMaxSp = 32;          // region-A splits a row may have (max_seq <= 4096)
-constexpr int kMergeWarps = 8;
 
 __host__ __device__ __forceinline__ int region_b_start(int p) { return p < kDelta ? 0 : ((p - kDelta) >> 4) << 4; }
 
@@ -166,35 +165,38 @@ __global__ void __launch_bounds__(kAThreads, 2)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // Q is written by the QKV epilogue.  Every CTA waits for it before it
-    // triggers: the window kernel launched next relies on that for its reads.
-    pdl_wait();
-    pdl_trigger();
 
     auto split_blocks = [&](int sp) {
         const int lo = sp * kSA, hi = min(lo + kSA, bmax);
         return (hi - lo + kBlk - 1) / kBlk;
     };
+    const uint64_t pol_kv = policy_evict_first();
+    auto issue_kv = [&](int sp) {
+        const int nb = split_blocks(sp), y0 = kv_row + sp * kSA;
+        mbar_expect_tx(full_k, nb * L::kKBlock);
+        for (int b = 0; b < nb; b++)
+            for (int at = 0; at < L::kAtoms; at++)
+                tma_load_2d(&kmap, full_k, sm + L::kK + b * L::kKBlock + at * (kBlk * 128), at * 64, y0 + b * kBlk,
+                            pol_kv);
+        mbar_expect_tx(full_v, nb * L::kKBlock);
+        for (int b = 0; b < nb; b++)
+            for (int at = 0; at < L::kAtoms; at++)
+                tma_load_2d(&vmap, full_v, sm + L::kV + b * L::kKBlock + at * (kBlk * 128), at * 64, y0 + b * kBlk,
+                            pol_kv);
+    };
+    // The first split's cached K and V were written by earlier steps: their
+    // copies start before the wait.  Q is written by the QKV epilogue.  Every
+    // CTA waits for it before it triggers: the window kernel launched next
+    // relies on that for its reads.
+    if (warp == 0 && lane == 0 && (int)blockIdx.y < nsp) issue_kv(blockIdx.y);
+    pdl_wait();
+    pdl_trigger();
 
     if ((int)blockIdx.y < nsp) {
         if (warp == 0) {
             if (lane == 0) {
                 // ---------------- TMA producer
-                const uint64_t pol_kv = policy_evict_first(), pol_q = policy_evict_last();
-                auto issue_kv = [&](int sp) {
-                    const int nb = split_blocks(sp), y0 = kv_row + sp * kSA;
-                    mbar_expect_tx(full_k, nb * L::kKBlock);
-                    for (int b = 0; b < nb; b++)
-                        for (int at = 0; at < L::kAtoms; at++)
-                            tma_load_2d(&kmap, full_k, sm + L::kK + b * L::kKBlock + at * (kBlk * 128), at * 64,
-                                        y0 + b * kBlk, pol_kv);
-                    mbar_expect_tx(full_v, nb * L::kKBlock);
-                    for (int b = 0; b < nb; b++)
-                        for (int at = 0; at < L::kAtoms; at++)
-                            tma_load_2d(&vmap, full_v, sm + L::kV + b * L::kKBlock + at * (kBlk * 128), at * 64,
-                                        y0 + b * kBlk, pol_kv);
-                };
-                issue_kv(blockIdx.y);
+                const uint64_t pol_q = policy_evict_last();
                 mbar_expect_tx(full_q, a.hpc * L::kAtoms * a.bq * 128);
                 for (int hl = 0; hl < a.hpc; hl++)
                     for (int at = 0; at < L::kAtoms; at++)
@@ -422,13 +424,6 @@ struct BSmem {
     static constexpr int kSlot = kInts + ((2 * kRows + 2) * 4 + 15) / 16 * 16;  // per-slot merge state
     static constexpr int kBytes = kSlot + 7 * kRows * 4 + 16;
 };
-
-// Address of 16-byte chunk c (head_dim / 8 chunks per row) of row `row` in a
-// TMA tile of `rows` rows: atoms of 64 elements, 128-byte swizzle.
-__device__ __forceinline__ uint32_t tile_chunk(uint32_t base, int rows, int row, int c)
-{
-    return base + (c >> 3) * rows * 128 + row * 128 + (((c & 7) ^ (row & 7)) << 4);
-}
 
 // at most 112 registers a thread: a window CTA (8 warps) then fits on an SM
 // beside a cache CTA (10 warps at 96 registers) -- each of the SM's four
