@@ -75,6 +75,9 @@ def parse():
                     help="sampling verification at this temperature (0: greedy verification); the "
                          "comparison decoder then samples too, and the output is lossless in distribution "
                          "instead of token for token")
+    ap.add_argument("--batch-sweep", action="store_true",
+                    help="instead of the benchmark line: one JSON line per (W,N,G,batch) of batched decoding "
+                         "(several sequences in one forward pass per step, batch x T <= 128 rows)")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the benchmark line: one JSON line per (W,N,G) of a sweep, plus "
                          "the prompt-lookup mode (W=0, G>0, pool seeded from the prompt) and greedy")
@@ -417,6 +420,63 @@ def run_sweep(args, rank, world):
     return lines if rank == 0 else None
 
 
+# (W, N, G, batch) of the batch sweep: batch x (1 + (W+G)(N-1)) <= 128 rows
+BATCH_SWEEP = [(0, 2, 0, 1), (0, 2, 0, 2), (0, 2, 0, 4), (0, 2, 0, 8), (0, 2, 0, 16), (0, 2, 0, 32),
+               (0, 2, 0, 64), (0, 2, 0, 128),
+               (15, 5, 15, 1), (7, 5, 7, 1), (7, 5, 7, 2), (5, 5, 5, 3), (3, 5, 3, 5), (3, 4, 3, 6)]
+
+
+def run_batch_sweep(args, rank, world):
+    """Batched decoding: per (W, N, G, batch), the step latency and the
+    tokens/s of all sequences together (prompts of the workload's recipe,
+    seeds 1..batch), and whether sequence 0's tokens equal a batch-1 greedy
+    context's on the same prompt."""
+    import torch
+    import lossless_lookahead_decoding_gb300 as LA
+    from lossless_lookahead_decoding_gb300 import build as B
+    B.build()
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    cfg = I.MODELS[args.workload]
+    if args.layers:
+        cfg = cfg.sliced(args.layers)
+    n_steps = args.warmup + args.steps
+    prompts = [I.make_prompt(args.workload, seed=1 + b) for b in range(max(b for *_, b in BATCH_SWEEP))]
+    max_seq = len(prompts[0]) + n_steps * 8 + 32
+    dw = build_model(cfg, LA.LA_BF16)
+    ref = LA.Decoder(cfg, dw, LA.LA_BF16, 0, 2, 0, max_seq)
+    want = ref.generate(prompts[0], n_steps)  # one token per greedy step: enough for every point
+    ref.close()
+    lines = []
+    for W, N, G, bsz in BATCH_SWEEP:
+        dec = LA.Decoder(cfg, dw, LA.LA_BF16, W, N, G, max_seq, batch=bsz)
+        for b in range(bsz):
+            dec.prefill_seq(b, prompts[b])
+        out0, tok = [], 0
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i in range(n_steps):
+            k = i - args.warmup
+            if k >= 0:
+                ev[k][0].record(dec.stream)
+            got = dec.step_batch()
+            if k >= 0:
+                ev[k][1].record(dec.stream)
+                tok += sum(len(t) for t in got)
+            out0.extend(got[0].tolist())
+        torch.cuda.synchronize()
+        dec.close()
+        ms = [a.elapsed_time(b) for a, b in ev]
+        T = 1 + (W + G) * (N - 1)
+        lines.append({"batch_sweep": args.workload, "W": W, "N": N, "G": G, "batch": bsz, "T": T,
+                      "rows_per_pass": bsz * T, "ms_per_step": round(float(np.mean(ms)), 4),
+                      "tokens_per_step": round(tok / args.steps, 4),
+                      "tokens_per_s": round(tok / (sum(ms) / 1e3), 2),
+                      "tokens_per_s_per_sequence": round(tok / bsz / (sum(ms) / 1e3), 2),
+                      "seq0_equals_batch1_greedy": bool(np.array_equal(np.array(out0[:len(want)], np.int32),
+                                                                       want[:len(out0)])),
+                      "steps": args.steps, "warmup": args.warmup, "data": "synthetic prompts, random-init weights"})
+    return lines if rank == 0 else None
+
+
 def _event_times(fn, reps, stream, before=None):
     """Device time (µs) of fn() per rep on stream, CUDA events around each;
     before() (e.g. an L2 flush) runs outside the timed region."""
@@ -655,6 +715,8 @@ def main():
         out = run_reference(args, rank, world)
     elif args.sweep:
         out = run_sweep(args, rank, world)
+    elif args.batch_sweep:
+        out = run_batch_sweep(args, rank, world)
     elif args.micro:
         out = run_micro(args, rank, world)
     else:

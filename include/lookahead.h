@@ -199,8 +199,50 @@ LA_API int la_set_sampling(la_ctx* ctx, float temperature, uint64_t seed);
  * receives exactly min(max_new, emitted) tokens, count in *n_out. */
 LA_API int la_generate(la_ctx* ctx, const int32_t* prompt, int len, int max_new, int32_t* out, int* n_out);
 
+/* ---- batched decoding: several sequences in one forward pass per step ----
+ * Pages: "Key points" (main limitation: the per-step FLOPs the lookahead and
+ * verification rows add make the method gain less when the GPU serves large
+ * batches, since the step is then no longer bandwidth bound).  A batched
+ * context decodes B independent sequences with the same model and the same
+ * (W, N, G): each step's forward pass holds every sequence's 1 + (W+G)(N-1)
+ * rows (sequence b's are rows b*T .. b*T+T-1), so the weights stream once for
+ * all of them; attention, verification, harvest, window and KV commit run per
+ * sequence on its own cache, window and pool.  Every sequence's output is the
+ * output of a batch-1 context with the same seed (bit for bit: no row's
+ * arithmetic depends on the other rows).  B * (1 + (W+G)(N-1)) <= 128.
+ * Not with LA_ATTN_TC (LA_ERR_ARG).  la_prefill, la_step and la_generate
+ * return LA_ERR_STATE on a batched context. */
+
+/* No counterpart on the pages: sizing of this library's device memory.
+ * Workspace of a batched context (la_workspace_bytes is batch = 1): the KV
+ * cache, window, pool and decode state once per sequence, the rest shared.
+ * 0 for unsupported arguments. */
+LA_API size_t la_workspace_bytes_batch(const la_model_desc* desc, int W, int N, int G, int batch);
+/* Pages: "Key points" (main limitation, serving batches; the knobs W, N, G).
+ * la_create for `batch` sequences (la_create is batch = 1); same arguments
+ * and ownership.  LA_ERR_ARG when batch < 1, batch * T > 128 or LA_ATTN_TC
+ * is asked for with batch > 1. */
+LA_API int la_create_batch(const la_model_desc* desc, int W, int N, int G, int batch, void* workspace,
+                           size_t ws_bytes, uint64_t seed, int flags, la_ctx** out);
+/* Pages: "Summary" (the 2D window set up from the prompt), per sequence.
+ * la_prefill of sequence seq (0 <= seq < batch) alone; its window is drawn
+ * from `seed` as in la_prefill.  Every sequence must be prefilled before
+ * la_step_batch; prefilling sequence 0 starts new la_get_stats counters. */
+LA_API int la_prefill_seq(la_ctx* ctx, int seq, const int32_t* prompt, int len);
+/* Pages: "Summary" (one forward pass holds both branches; output equal to
+ * greedy decoding) and "Key points" (main limitation: batches).
+ * One combined step of every sequence.  out: HOST int32[batch][cap]
+ * (cap >= N): sequence b's 1..N tokens at out[b*cap ..], their count in
+ * n_out[b] (HOST int32[batch]).  Errors as la_step, for any sequence (a
+ * device error makes every sequence need its prefill again).  Sampling
+ * verification (la_set_sampling) gives sequence b the stream seeded with
+ * seed + b. */
+LA_API int la_step_batch(la_ctx* ctx, int32_t* out, int cap, int* n_out);
+
 /* Pages: "Key points" (steps taken against tokens emitted: the step count
- * the scaling law is about).  Counters since the last la_prefill. */
+ * the scaling law is about).  Counters since the last la_prefill (batched:
+ * since sequence 0's; emitted and accept_hist count every sequence, steps
+ * count batched steps, P is sequence 0's, rows = batch * T). */
 LA_API int la_get_stats(la_ctx* ctx, la_stats* out);
 /* No counterpart on the pages: this library's kernel timing.
  * Copy up to cap entries (one per kernel class seen); *n_out = entries written.
@@ -225,6 +267,10 @@ LA_API int la_debug_pool(la_ctx* ctx, int32_t key, int32_t* host, int cap, int* 
 /* Pages: "Summary" (the 2D window of Jacobi iteration history).
  * Lookahead window, int32[N-1][W] into host (cap ints). */
 LA_API int la_debug_window(la_ctx* ctx, int32_t* host, int cap);
+/* No counterpart on the pages (a parity accessor of batched decoding).
+ * Make the debug accessors above and below read sequence seq of a batched
+ * context (0 at creation).  LA_ERR_ARG for seq outside 0..batch-1. */
+LA_API int la_debug_select(la_ctx* ctx, int seq);
 /* No counterpart on the pages (a parity accessor for the controller).
  * Replace the model's argmaxes seen by verification, harvest and window
  * update with host[0..n) (one token per step row, n = T) for every following

@@ -25,9 +25,9 @@ LA_FP32, LA_BF16 = 0, 1
 LA_PRESEED_PROMPT, LA_DEBUG_LOGITS, LA_NO_GRAPH, LA_SIMT, LA_PROFILE, LA_ATTN_TC, LA_MASK_DIAG = 1, 2, 4, 8, 16, 32, 64
 
 EXPORTS = ("la_workspace_bytes", "la_create", "la_prefill", "la_step", "la_generate", "la_set_sampling", "la_get_stats",
-           "la_get_profile",
+           "la_get_profile", "la_workspace_bytes_batch", "la_create_batch", "la_prefill_seq", "la_step_batch",
            "la_debug_logits", "la_debug_argmax", "la_debug_rows", "la_debug_pool", "la_debug_window",
-           "la_debug_set_argmax_override",
+           "la_debug_set_argmax_override", "la_debug_select",
            "la_last_error", "la_destroy", "la_attention", "la_attention_noalloc", "la_pool_create", "la_pool_insert", "la_pool_lookup", "la_pool_size",
            "la_pool_destroy")
 
@@ -75,6 +75,11 @@ def lib():
             "la_prefill": (i32, [vp, vp, i32]),
             "la_step": (i32, [vp, vp, i32, vp]),
             "la_generate": (i32, [vp, vp, i32, i32, vp, vp]),
+            "la_workspace_bytes_batch": (sz, [vp, i32, i32, i32, i32]),
+            "la_create_batch": (i32, [vp, i32, i32, i32, i32, vp, sz, u64, i32, vp]),
+            "la_prefill_seq": (i32, [vp, i32, vp, i32]),
+            "la_step_batch": (i32, [vp, vp, i32, vp]),
+            "la_debug_select": (i32, [vp, i32]),
             "la_set_sampling": (i32, [vp, C.c_float, u64]),
             "la_get_stats": (i32, [vp, vp]),
             "la_get_profile": (i32, [vp, vp, i32, vp]),
@@ -136,6 +141,37 @@ def la_step(ctx, N: int = 8) -> np.ndarray:
     n = C.c_int()
     _check(ctx, lib().la_step(ctx, _p(out), len(out), C.byref(n)))
     return out[: n.value].copy()
+
+
+def la_workspace_bytes_batch(desc: la_model_desc, W: int, N: int, G: int, batch: int) -> int:
+    return int(lib().la_workspace_bytes_batch(C.byref(desc), W, N, G, batch))
+
+
+def la_create_batch(desc: la_model_desc, W: int, N: int, G: int, batch: int, workspace: int = 0, ws_bytes: int = 0,
+                    seed: int = 2, flags: int = 0):
+    h = C.c_void_p()
+    rc = lib().la_create_batch(C.byref(desc), W, N, G, batch, workspace or None, ws_bytes, seed, flags, C.byref(h))
+    if rc != LA_OK:
+        raise LAError(rc, "la_create_batch failed")
+    return h
+
+
+def la_prefill_seq(ctx, seq: int, prompt) -> None:
+    p = np.ascontiguousarray(prompt, dtype=np.int32)
+    _check(ctx, lib().la_prefill_seq(ctx, seq, _p(p), len(p)))
+
+
+def la_step_batch(ctx, batch: int, N: int = 8) -> list:
+    """One step of every sequence: a list of `batch` token arrays."""
+    cap = max(N, 8)
+    out = np.zeros((batch, cap), np.int32)
+    n = np.zeros(batch, np.int32)
+    _check(ctx, lib().la_step_batch(ctx, _p(out), cap, _p(n)))
+    return [out[b, : n[b]].copy() for b in range(batch)]
+
+
+def la_debug_select(ctx, seq: int) -> None:
+    _check(ctx, lib().la_debug_select(ctx, seq))
 
 
 def la_set_sampling(ctx, temperature: float, seed: int) -> None:
@@ -287,10 +323,11 @@ def device_weights(cfg, tensors, dtype: int, device="cuda"):
 
 
 class Decoder:
-    """A model description + device weights + one decoding context."""
+    """A model description + device weights + one decoding context (batch > 1:
+    a batched context of that many sequences, see ``la_create_batch``)."""
 
     def __init__(self, cfg, weights, dtype: int, W: int, N: int, G: int, max_seq: int, seed: int = 2,
-                 flags: int = 0, stream=None):
+                 flags: int = 0, stream=None, batch: int = 1):
         import torch
         self.cfg, self.W, self.N, self.G, self.dtype, self.flags = cfg, W, N, G, dtype, flags
         self.w = weights
@@ -306,7 +343,9 @@ class Decoder:
                                   weights["final_norm"].data_ptr(), weights["lm_head"].data_ptr(),
                                   self.stream.cuda_stream)
         self.T = 1 + (W + G) * (N - 1)
-        self.ctx = la_create(self.desc, W, N, G, 0, 0, seed, flags)
+        self.batch = batch
+        self.ctx = (la_create(self.desc, W, N, G, 0, 0, seed, flags) if batch == 1 else
+                    la_create_batch(self.desc, W, N, G, batch, 0, 0, seed, flags))
 
     def close(self):
         if getattr(self, "ctx", None):
@@ -321,6 +360,16 @@ class Decoder:
 
     def step(self):
         return la_step(self.ctx, self.N)
+
+    def prefill_seq(self, seq: int, prompt):
+        la_prefill_seq(self.ctx, seq, prompt)
+
+    def step_batch(self):
+        return la_step_batch(self.ctx, self.batch, self.N)
+
+    def select(self, seq: int):
+        """Point the debug accessors at sequence seq."""
+        la_debug_select(self.ctx, seq)
 
     def set_sampling(self, temperature: float, seed: int):
         """Sampling verification at this temperature (<= 0: greedy)."""

@@ -196,9 +196,10 @@ struct AttnArgs {
     RowSet rs;
     const int* pos;
     const __nv_bfloat16 *Q, *KC, *VC, *KS, *VS;
-    float* part;  // [H][nsplit][kRows][2 + HD]
+    float* part;  // [H][nsplit][128][2 + HD]; batched: [B][H][nsplit][rows][2 + HD]
     __nv_bfloat16* out;
     int rows, H, Hkv, max_seq, nsplit, max_rel;
+    size_t sb;  // batched: byte stride between the sequences' decode states and caches (grid z = sequence)
     int hpc;    // query heads per CTA (of one KV head): their rows stacked in the Q tile
     float sl2;  // log2(e) / sqrt(hd)
 };
@@ -224,7 +225,9 @@ struct AttnSmem {
     static constexpr int kBytes = kInts + (2 * kRows + 2) * 4;
 };
 
-template <int HD>
+// kBatch: grid z is the sequence of a batched step (one sequence: z = 0 and
+// none of the per-sequence offsets is computed).
+template <int HD, bool kBatch>
 __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
 {
     pdl_wait();
@@ -240,7 +243,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int dq = a.H * HD, dkv = a.Hkv * HD;
-    const int P = a.st->P, maxpos = P + a.max_rel;
+    // sequence b of a batch: its own decode state and cache, rows b*rows ..
+    const int b = kBatch ? blockIdx.z : 0;
+    const size_t row0 = (size_t)b * a.rows;
+    const int P = seq_ptr(a.st, a.sb, b)->P, maxpos = P + a.max_rel;
     // blockIdx.y < nsplit: split y; beyond: extra CTAs for the split that
     // holds the first tail chunk (the chunk containing position P)
     // this CTA's query heads h0 .. h0 + hpc - 1 share KV head kvh; their rows
@@ -259,12 +265,17 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
     const int c_shared_end = min(c_end, max(c_begin, P / kChunk));
     const bool has_tail = c_shared_end < c_end;
     if (!has_tail && rep > 0) return;  // replicas only serve splits with tail chunks
-    const __nv_bfloat16* kc = a.KC + (size_t)kvh * a.max_seq * HD;
-    const __nv_bfloat16* vc = a.VC + (size_t)kvh * a.max_seq * HD;
+    const __nv_bfloat16* kc = seq_ptr(a.KC, a.sb, b) + (size_t)kvh * a.max_seq * HD;
+    const __nv_bfloat16* vc = seq_ptr(a.VC, a.sb, b) + (size_t)kvh * a.max_seq * HD;
+    const __nv_bfloat16* qrows = a.Q + row0 * dq;
+    const int* pos = a.pos + row0;
+    // partials [B][H][nsplit][prow][PS]: one sequence keeps the 128-row stride
+    const int prow = kBatch ? a.rows : kRows;
+    float* part = a.part + row0 * a.H * a.nsplit * PS;
     // partial state of (virtual row v) in this split
     auto part_row = [&](int v) {
         const int hl = v / a.rows, r = v - hl * a.rows;
-        return a.part + (((size_t)(h0 + hl) * a.nsplit + sp) * kRows + r) * PS;
+        return part + (((size_t)(h0 + hl) * a.nsplit + sp) * prow + r) * PS;
     };
 
     // Q tile: virtual rows of the CTA's heads (beyond vrows zero)
@@ -272,7 +283,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
         const int v = i / NCH, c = i % NCH;
         const bool ok = v < vrows;
         const int hl = ok ? v / a.rows : 0, r = ok ? v - hl * a.rows : 0;
-        cp_async16(swz<HD>(sb + L::kQ, v, c), a.Q + (size_t)r * dq + (h0 + hl) * HD + c * 8, ok);
+        cp_async16(swz<HD>(sb + L::kQ, v, c), qrows + (size_t)r * dq + (h0 + hl) * HD + c * 8, ok);
     }
     auto load_chunk = [&](int cidx, int kofs, int vofs, int valid_end) {
         for (int i = tid; i < kChunk * NCH; i += blockDim.x) {
@@ -289,7 +300,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
         for (int i = tid; i < kRows * NCH; i += blockDim.x) {
             const int r = i / NCH, c = i % NCH;
             const bool ok = r < a.rows;
-            const size_t off = (size_t)(ok ? r : 0) * dkv + kvh * HD + c * 8;
+            const size_t off = (row0 + (ok ? r : 0)) * dkv + kvh * HD + c * 8;
             cp_async16(swz<HD>(sb + L::kKS, r, c), a.KS + off, ok);
             cp_async16(swz<HD>(sb + L::kVS, r, c), a.VS + off, ok);
         }
@@ -388,7 +399,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
         // rows of this slab (-1 = padding)
         const int rA = (r_begin + g4 < r_end) ? glist[r_begin + g4] : -1;
         const int rB = (r_begin + g4 + 8 < r_end) ? glist[r_begin + g4 + 8] : -1;
-        const int posA = rA >= 0 ? a.pos[rA] : -1, posB = rB >= 0 ? a.pos[rB] : -1;
+        const int posA = rA >= 0 ? pos[rA] : -1, posB = rB >= 0 ? pos[rB] : -1;
         // Q fragments of the gathered rows
         {
             const int li = (lane & 7) + (((lane >> 3) & 1) << 3);
@@ -481,8 +492,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
 // to 4 splits are issued together, the merge runs in split order.
 constexpr int kCombWarps = 8;
 
-template <int HD>
-__global__ void __launch_bounds__(kCombWarps * 32) k_attn_combine(AttnArgs a)
+template <int HD, bool kBatch>
+__global__ void __launch_bounds__(kCombWarps * 32, 5) k_attn_combine(AttnArgs a)
 {
     pdl_wait();
     pdl_trigger();
@@ -491,9 +502,11 @@ __global__ void __launch_bounds__(kCombWarps * 32) k_attn_combine(AttnArgs a)
     const int w = blockIdx.x * kCombWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (w >= a.rows * a.H) return;
     const int r = w / a.H, h = w % a.H;
-    const int ns = a.pos[r] / kSplit + 1;
-    const float* base = a.part + (size_t)h * a.nsplit * kRows * PS + (size_t)r * PS;
-    const size_t stride = (size_t)kRows * PS;
+    const size_t row0 = kBatch ? (size_t)blockIdx.y * a.rows : 0;  // sequence blockIdx.y of a batch
+    const int ns = a.pos[row0 + r] / kSplit + 1;
+    const int prow = kBatch ? a.rows : kRows;  // the partials' row stride (k_attn_mma)
+    const float* base = a.part + row0 * a.H * a.nsplit * PS + ((size_t)h * a.nsplit * prow + r) * PS;
+    const size_t stride = (size_t)prow * PS;
     float m = -INFINITY, l = 0.f, o[V];
 #pragma unroll
     for (int k = 0; k < V; k++) o[k] = 0.f;
@@ -527,7 +540,7 @@ __global__ void __launch_bounds__(kCombWarps * 32) k_attn_combine(AttnArgs a)
             m = mn;
         }
     }
-    __nv_bfloat16* dst = a.out + (size_t)r * a.H * HD + h * HD + lane * V;
+    __nv_bfloat16* dst = a.out + (row0 + r) * a.H * HD + h * HD + lane * V;
 #pragma unroll
     for (int k = 0; k < V; k += 2) *(__nv_bfloat162*)(dst + k) = __floats2bfloat162_rn(o[k] / l, o[k + 1] / l);
 }
@@ -543,19 +556,24 @@ size_t attn_mma_partial_bytes(int H, int hd, int max_seq)
 bool attn_mma_init(int hd)
 {
     if (hd == 128)
-        return cudaFuncSetAttribute(k_attn_mma<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        return cudaFuncSetAttribute(k_attn_mma<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    AttnSmem<128>::kBytes) == cudaSuccess &&
+               cudaFuncSetAttribute(k_attn_mma<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     AttnSmem<128>::kBytes) == cudaSuccess;
     if (hd == 64)
-        return cudaFuncSetAttribute(k_attn_mma<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        return cudaFuncSetAttribute(k_attn_mma<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    AttnSmem<64>::kBytes) == cudaSuccess &&
+               cudaFuncSetAttribute(k_attn_mma<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     AttnSmem<64>::kBytes) == cudaSuccess;
     return false;
 }
 
 void launch_attn_mma(cudaStream_t s, const DState* st, RowSet rs, int max_rel, const int* pos, const void* Q,
                      const void* KC, const void* VC, const void* KS, const void* VS, void* out, float* part, int rows,
-                     int H, int Hkv, int hd, int max_seq)
+                     int H, int Hkv, int hd, int max_seq, int B, size_t sb)
 {
     AttnArgs a;
+    a.sb = sb;
     a.st = st;
     a.rs = rs;
     a.pos = pos;
@@ -578,14 +596,16 @@ void launch_attn_mma(cudaStream_t s, const DState* st, RowSet rs, int max_rel, c
     const int group = H / Hkv;
     a.hpc = 1;
     while (group % (2 * a.hpc) == 0 && 2 * a.hpc * rows <= kRows) a.hpc *= 2;
-    dim3 grid(H / a.hpc, a.nsplit + kRep - 1);
-    if (hd == 128) {
-        launch_pdl(k_attn_mma<128>, grid, dim3(kWarps * 32), AttnSmem<128>::kBytes, s, a);
-        launch_pdl(k_attn_combine<128>, dim3((rows * H + kCombWarps - 1) / kCombWarps), dim3(kCombWarps * 32), 0, s, a);
-    } else {
-        launch_pdl(k_attn_mma<64>, grid, dim3(kWarps * 32), AttnSmem<64>::kBytes, s, a);
-        launch_pdl(k_attn_combine<64>, dim3((rows * H + kCombWarps - 1) / kCombWarps), dim3(kCombWarps * 32), 0, s, a);
-    }
+    dim3 grid(H / a.hpc, a.nsplit + kRep - 1, B);
+    dim3 cgrid((rows * H + kCombWarps - 1) / kCombWarps, B);
+    auto go = [&](auto mma, auto comb, int smem) {
+        launch_pdl(mma, grid, dim3(kWarps * 32), smem, s, a);
+        launch_pdl(comb, cgrid, dim3(kCombWarps * 32), 0, s, a);
+    };
+    if (hd == 128 && B == 1) go(k_attn_mma<128, false>, k_attn_combine<128, false>, AttnSmem<128>::kBytes);
+    else if (hd == 128) go(k_attn_mma<128, true>, k_attn_combine<128, true>, AttnSmem<128>::kBytes);
+    else if (B == 1) go(k_attn_mma<64, false>, k_attn_combine<64, false>, AttnSmem<64>::kBytes);
+    else go(k_attn_mma<64, true>, k_attn_combine<64, true>, AttnSmem<64>::kBytes);
 }
 
 }  // namespace la

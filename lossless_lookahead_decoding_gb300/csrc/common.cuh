@@ -58,6 +58,27 @@ struct PoolView {
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Batched decoding: the per-sequence state (KV cache, prompt, window, pool,
+// decode state, argmax override) of sequence b sits b * sb bytes after
+// sequence 0's; the sequences' step rows are consecutive T-row slices of the
+// shared row arrays.  A kernel serving all sequences takes b from its grid.
+template <typename P>
+__host__ __device__ inline P* seq_ptr(P* p, size_t sb, int b)
+{
+    return reinterpret_cast<P*>(reinterpret_cast<uintptr_t>(p) + sb * (size_t)b);
+}
+
+__host__ __device__ inline PoolView seq_pool(PoolView p, size_t sb, int b)
+{
+    p.keys = seq_ptr(p.keys, sb, b);
+    p.cnt = seq_ptr(p.cnt, sb, b);
+    p.ent = seq_ptr(p.ent, sb, b);
+    p.first = seq_ptr(p.first, sb, b);
+    p.slot_of = seq_ptr(p.slot_of, sb, b);
+    p.status = seq_ptr(p.status, sb, b);
+    return p;
+}
+
 template <typename T> __device__ __forceinline__ float to_f(T x);
 template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
 template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -114,16 +135,17 @@ struct Dims {
 
 // control.cu
 void launch_build_rows(cudaStream_t s, DState* st, const int* win, PoolView pool, int W, int N, int G,
-                       int T, const int* rel_pos, int* tok, int* pos);
+                       int T, const int* rel_pos, int* tok, int* pos, int B = 1, size_t sb = 0);
 void launch_prefill_rows(cudaStream_t s, const DState* st, const int* prompt, int P0, int n, int* tok,
                          int* pos);
 void launch_verify_update(cudaStream_t s, DState* st, const int* tok, const int* amax, int* win,
                           PoolView pool, int W, int N, int G, const float* logits, int V, float tau,
-                          const unsigned long long* stats, bool diag, const int* ovr);
+                          const unsigned long long* stats, bool diag, const int* ovr, int B = 1, size_t sb = 0);
 void launch_row_stats(cudaStream_t s, const float* logits, int V, float tau, int vbase, int T,
-                      unsigned long long* stats);
+                      unsigned long long* stats, int B = 1);
 void launch_commit(cudaStream_t s, const DState* st, bool prefill, int n_prefill, int n_max, const void* KS,
-                   const void* VS, void* KC, void* VC, int L, int Hkv, int hd, int max_seq, int esz);
+                   const void* VS, void* KC, void* VC, int L, int Hkv, int hd, int max_seq, int esz, int B = 1,
+                   int T = 0, size_t sb = 0);
 void launch_pool_reset(cudaStream_t s, PoolView pool);
 void launch_set_state(cudaStream_t s, DState* st, int P, int c, bool reset);
 void launch_pool_insert(cudaStream_t s, PoolView pool, const int* keys, const int* grams, int gram_stride,
@@ -183,7 +205,7 @@ size_t attn_mma_partial_bytes(int H, int hd, int max_seq);
 bool attn_mma_init(int hd);
 void launch_attn_mma(cudaStream_t s, const DState* st, RowSet rs, int max_rel, const int* pos, const void* Q,
                      const void* KC, const void* VC, const void* KS, const void* VS, void* out, float* part, int rows,
-                     int H, int Hkv, int hd, int max_seq);
+                     int H, int Hkv, int hd, int max_seq, int B = 1, size_t sb = 0);
 
 }  // namespace la
 

@@ -202,10 +202,18 @@ void launch_pool_lookup(cudaStream_t s, PoolView pool, const int* keys, int n, i
 // win[l][j]; verification row (g,i) = 1 + W(N-1) + g(N-1) + i holds the g-th
 // candidate's i-th token), positions P + rel_pos[r].  Candidates are the pool
 // entries of c, oldest first; missing candidates' rows are padding (token 0).
+// Batched (gridDim.x = B > 1): block b builds sequence b's T rows only.
 __global__ void k_build_rows(DState* st, const int* win, PoolView pool, int W, int N, int G, int T,
-                             const int* rel_pos, int* tok, int* pos)
+                             const int* rel_pos, int* tok, int* pos, size_t sb)
 {
     __shared__ int s_slot, s_cnt;
+    const int b = blockIdx.x;
+    st = seq_ptr(st, sb, b);
+    win = seq_ptr(win, sb, b);
+    pool = seq_pool(pool, sb, b);
+    tok += (size_t)b * T;
+    pos += (size_t)b * T;
+    const int nrows = gridDim.x > 1 ? T : kRows;
     const int c = st->c, P = st->P;
     if (threadIdx.x < 32) {
         bool found = false;
@@ -217,7 +225,7 @@ __global__ void k_build_rows(DState* st, const int* win, PoolView pool, int W, i
     }
     __syncthreads();
     const int n1 = N - 1, slot = s_slot, cnt = s_cnt;
-    for (int r = threadIdx.x; r < kRows; r += blockDim.x) {
+    for (int r = threadIdx.x; r < nrows; r += blockDim.x) {
         int t = 0;
         if (r == 0) {
             t = c;
@@ -237,9 +245,9 @@ __global__ void k_build_rows(DState* st, const int* win, PoolView pool, int W, i
 }
 
 void launch_build_rows(cudaStream_t s, DState* st, const int* win, PoolView pool, int W, int N, int G, int T,
-                       const int* rel_pos, int* tok, int* pos)
+                       const int* rel_pos, int* tok, int* pos, int B, size_t sb)
 {
-    k_build_rows<<<1, 128, 0, s>>>(st, win, pool, W, N, G, T, rel_pos, tok, pos);
+    k_build_rows<<<B, 128, 0, s>>>(st, win, pool, W, N, G, T, rel_pos, tok, pos, sb);
 }
 
 __global__ void k_prefill_rows(const DState* st, const int* prompt, int P0, int n, int* tok, int* pos)
@@ -341,10 +349,13 @@ __device__ __forceinline__ unsigned long long uniform_u24(unsigned long long* x)
 constexpr int kStatThreads = 256;
 
 __global__ void __launch_bounds__(kStatThreads) k_row_stats(const float* __restrict__ logits, int V, float tau,
-                                                           int vbase, unsigned long long* __restrict__ stats)
+                                                           int vbase, int T, unsigned long long* __restrict__ stats)
 {
     pdl_wait();
     pdl_trigger();
+    // sequence blockIdx.y of a batch: its rows are T rows further on
+    logits += (size_t)blockIdx.y * T * V;
+    stats += (size_t)blockIdx.y * T * 2;
     const int r = blockIdx.x == 0 ? 0 : vbase + blockIdx.x - 1;
     const float* z = logits + (size_t)r * V;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, B = sample_bits(V);
@@ -371,9 +382,9 @@ __global__ void __launch_bounds__(kStatThreads) k_row_stats(const float* __restr
 }
 
 void launch_row_stats(cudaStream_t s, const float* logits, int V, float tau, int vbase, int T,
-                      unsigned long long* stats)
+                      unsigned long long* stats, int B)
 {
-    launch_pdl(k_row_stats, dim3(1 + T - vbase), dim3(kStatThreads), 0, s, logits, V, tau, vbase, stats);
+    launch_pdl(k_row_stats, dim3(1 + T - vbase, B), dim3(kStatThreads), 0, s, logits, V, tau, vbase, T, stats);
 }
 
 // ------------------------------------------------- verify + harvest + shift ---
@@ -561,8 +572,20 @@ __device__ void sample_verify(DState* st, const int* tok, const float* logits, i
 __global__ void __launch_bounds__(kVerifyWarps * 32)
     k_verify_update(DState* st, const int* tok, const int* amax, int* win, PoolView pool, int W, int N, int G,
                     const float* logits, int V, float tau, const unsigned long long* stats, int diag,
-                    const int* ovr)
+                    const int* ovr, size_t sb)
 {
+    {  // block b serves sequence b of a batch
+        const int b = blockIdx.x;
+        const size_t T = 1 + (size_t)(W + G) * (N - 1);
+        st = seq_ptr(st, sb, b);
+        win = seq_ptr(win, sb, b);
+        pool = seq_pool(pool, sb, b);
+        ovr = seq_ptr(ovr, sb, b);
+        tok += b * T;
+        amax += b * T;
+        logits += b * T * V;
+        stats += b * T * 2;
+    }
     if (ovr[0]) amax = ovr + 1;  // debug: the rows' argmaxes set from the host
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int n1 = N - 1, ncand = st->ncand, P = st->P;
@@ -654,10 +677,10 @@ __global__ void __launch_bounds__(kVerifyWarps * 32)
 
 void launch_verify_update(cudaStream_t s, DState* st, const int* tok, const int* amax, int* win, PoolView pool,
                           int W, int N, int G, const float* logits, int V, float tau,
-                          const unsigned long long* stats, bool diag, const int* ovr)
+                          const unsigned long long* stats, bool diag, const int* ovr, int B, size_t sb)
 {
-    k_verify_update<<<1, kVerifyWarps * 32, 0, s>>>(st, tok, amax, win, pool, W, N, G, logits, V, tau, stats,
-                                                    diag ? 1 : 0, ovr);
+    k_verify_update<<<B, kVerifyWarps * 32, 0, s>>>(st, tok, amax, win, pool, W, N, G, logits, V, tau, stats,
+                                                    diag ? 1 : 0, ovr, sb);
 }
 
 // ------------------------------------------------------------------ commit ---
@@ -665,14 +688,18 @@ void launch_verify_update(cudaStream_t s, DState* st, const int* tok, const int*
 // Copy the step K/V of the committed rows into the cache for every layer:
 // step layout [L][kRows][Hkv][hd], cache layout [L][Hkv][max_seq][hd].
 // Step mode: rows st->commit_rows[0..n_emit) to positions P_before + i.
-// Prefill mode: rows 0..n-1 to positions P + i.
+// Prefill mode: rows 0..n-1 to positions P + i.  Batched: grid z is the
+// sequence, whose step rows start at row z * T.
 __global__ void k_commit(const DState* st, int prefill, int n_prefill, const uint4* KS, const uint4* VS,
-                         uint4* KC, uint4* VC, int Hkv, int hd_vec, int max_seq)
+                         uint4* KC, uint4* VC, int Hkv, int hd_vec, int max_seq, int T, size_t sb)
 {
-    const int i = blockIdx.x, l = blockIdx.y;
+    const int i = blockIdx.x, l = blockIdx.y, b = blockIdx.z;
+    st = seq_ptr(st, sb, b);
+    KC = seq_ptr(KC, sb, b);
+    VC = seq_ptr(VC, sb, b);
     const int n = prefill ? n_prefill : st->n_emit;
     if (i >= n) return;
-    const int row = prefill ? i : st->commit_rows[i];
+    const int row = (prefill ? i : st->commit_rows[i]) + b * T;
     const int p = (prefill ? st->P : st->P_before) + i;
     const int dkv_vec = Hkv * hd_vec;
     const size_t src = ((size_t)l * kRows + row) * dkv_vec;
@@ -685,12 +712,13 @@ __global__ void k_commit(const DState* st, int prefill, int n_prefill, const uin
 }
 
 void launch_commit(cudaStream_t s, const DState* st, bool prefill, int n_prefill, int n_max, const void* KS,
-                   const void* VS, void* KC, void* VC, int L, int Hkv, int hd, int max_seq, int esz)
+                   const void* VS, void* KC, void* VC, int L, int Hkv, int hd, int max_seq, int esz, int B, int T,
+                   size_t sb)
 {
     int hd_vec = hd * esz / 16;
-    dim3 grid(prefill ? n_prefill : n_max, L);
+    dim3 grid(prefill ? n_prefill : n_max, L, B);
     k_commit<<<grid, 256, 0, s>>>(st, prefill ? 1 : 0, n_prefill, (const uint4*)KS, (const uint4*)VS, (uint4*)KC,
-                                  (uint4*)VC, Hkv, hd_vec, max_seq);
+                                  (uint4*)VC, Hkv, hd_vec, max_seq, T, sb);
 }
 
 }  // namespace la

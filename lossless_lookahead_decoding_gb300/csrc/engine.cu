@@ -30,7 +30,7 @@ using namespace la;
 namespace {
 
 struct Layout {
-    size_t off[40];
+    size_t off[32];
     size_t total;
     int n;
     size_t add(size_t bytes)
@@ -55,6 +55,12 @@ struct la_ctx {
     la_model_desc d;
     std::vector<const void*> lw;
     int W = 0, N = 2, G = 0, T = 1, flags = 0;
+    // batched decoding: B sequences share each step's forward pass (rows
+    // b*T .. b*T+T-1 are sequence b's); their state blocks are sb bytes apart
+    // and the views below (KC, VC, prompt, win, pool, st, AOVR) are sequence 0's
+    int B = 1;
+    size_t sb = 0;
+    int dseq = 0;  // the sequence the debug accessors read
     uint64_t seed = 0;
     float tau = 0.f;              // > 0: sampling verification at this temperature
     unsigned long long* SSTAT = nullptr;  // per-row softmax max (float bits) / integer weight total for sampling
@@ -85,8 +91,10 @@ struct la_ctx {
     TcPlan tc{};
     Profiler prof;
     int kernels_per_step = 0;
-    // host side
-    bool prefilled = false, have_step = false;
+    // host side (per sequence: prefilled, P)
+    std::vector<char> prefilled_seq;
+    std::vector<int> P_seq;
+    bool prefilled = false, have_step = false;  // every sequence prefilled; a step ran since
     int P_host = 0;
     la_stats stats{};
     cudaEvent_t ev0 = nullptr, ev1 = nullptr;
@@ -140,7 +148,7 @@ static int fail(la_ctx* ctx, int code, const char* msg)
 
 static int step_rows(int W, int N, int G) { return 1 + (W + G) * (N - 1); }
 
-static const char* check_desc(const la_model_desc* d, int W, int N, int G)
+static const char* check_desc(const la_model_desc* d, int W, int N, int G, int B = 1)
 {
     if (!d) return "desc is NULL";
     if (d->n_layers < 1 || d->d_model < 64 || d->d_model % 64 || d->d_model > 8192)
@@ -153,54 +161,85 @@ static const char* check_desc(const la_model_desc* d, int W, int N, int G)
     if (!d->emb || !d->layer_w || !d->final_norm || !d->lm_head) return "missing weight pointer";
     if (W < 0 || G < 0 || N < 2 || N > kMaxN) return "need W >= 0, G >= 0, 2 <= N <= 8";
     if (step_rows(W, N, G) > kRows) return "1 + (W+G)(N-1) must be <= 128";
+    if (B < 1 || B * step_rows(W, N, G) > kRows) return "batch * (1 + (W+G)(N-1)) must be <= 128";
     if ((N - 1) * W > 127) return "window too large";
     return nullptr;
 }
 
-static Layout make_layout(const la_model_desc* d, int W, int N, int G, int* pool_log2)
+// One sequence's decode state: its KV cache, prompt, lookahead window, n-gram
+// pool, device decode state and argmax override.  A batched context holds B
+// such blocks back to back, sb bytes apart (seq_ptr / seq_pool).
+struct SeqLayout {
+    size_t kc, vc, prompt, win, pk, ent, slot, st, aovr, bytes;
+};
+
+static SeqLayout seq_layout(const la_model_desc* d, int W, int N, int G, int lg)
+{
+    const int esz = d->dtype == LA_BF16 ? 2 : 4;
+    const size_t L = d->n_layers, dkv = (size_t)d->n_kv_heads * d->head_dim, cap = (size_t)1 << lg;
+    const int n1 = N - 1;
+    SeqLayout q{};
+    size_t o = 0;
+    auto add = [&](size_t bytes) {
+        const size_t at = o;
+        o += (bytes + 1023) & ~(size_t)1023;
+        return at;
+    };
+    q.kc = add(L * dkv * d->max_seq * esz);                   // K cache [L][Hkv][max_seq][hd]
+    q.vc = add(L * dkv * d->max_seq * esz);                   // V cache
+    q.prompt = add((size_t)d->max_seq * 4);                   // prompt tokens
+    q.win = add((size_t)(n1 * (W > 0 ? W : 1)) * 4);          // window [N-1][W]
+    q.pk = add(cap * 4 * 3);                                  // pool keys, counts, bulk-insert firsts
+    q.ent = add(cap * (size_t)(G > 0 ? G : 1) * n1 * 4);      // pool entries
+    q.slot = add((size_t)d->max_seq * 4);                     // pool bulk-insert slots
+    q.st = add(sizeof(DState));                               // decode state
+    q.aovr = add((kRows + 1) * 4);                            // argmax override: [0] on, [1..] rows
+    q.bytes = o;
+    return q;
+}
+
+enum LayoutItem {
+    L_SEQ, L_KS, L_VS, L_X, L_XN, L_QKV32, L_Q, L_ATT, L_HID, L_LOGITS, L_COS, L_SIN, L_AMAX, L_TOK, L_POS,
+    L_RS_STEP, L_MAP_STEP, L_RS_PRE, L_MAP_PRE, L_DEBUG, L_AMAXP, L_GL_STEP, L_GL_PRE, L_ATTN_PART, L_SSTAT,
+    L_COUNT
+};
+
+static Layout make_layout(const la_model_desc* d, int W, int N, int G, int B, int* pool_log2, SeqLayout* sq)
 {
     const int esz = d->dtype == LA_BF16 ? 2 : 4;
     const size_t L = d->n_layers, dq = (size_t)d->n_heads * d->head_dim, dkv = (size_t)d->n_kv_heads * d->head_dim;
-    const int n1 = N - 1;
     const int lg = next_pow2_log2(2 * d->vocab < 64 ? 64 : 2 * d->vocab);
     if (pool_log2) *pool_log2 = lg;
-    const size_t cap = (size_t)1 << lg;
+    const SeqLayout q = seq_layout(d, W, N, G, lg);
+    if (sq) *sq = q;
     Layout ly{};
-    ly.add(L * dkv * d->max_seq * esz);                  // 0 KC
-    ly.add(L * dkv * d->max_seq * esz);                  // 1 VC
-    ly.add(L * kRows * dkv * esz);                       // 2 KS
-    ly.add(L * kRows * dkv * esz);                       // 3 VS
-    ly.add((size_t)kRows * d->d_model * 4);              // 4 X
-    ly.add((size_t)kRows * d->d_model * esz);            // 5 XN
-    ly.add((size_t)kRows * (dq + 2 * dkv) * 4);          // 6 QKV32
-    ly.add((size_t)kRows * dq * esz);                    // 7 Q
-    ly.add((size_t)kRows * dq * esz);                    // 8 ATT
-    ly.add((size_t)kRows * d->ffn * esz);                // 9 HID
-    ly.add((size_t)kRows * d->vocab * 4);                // 10 LOGITS
-    ly.add((size_t)d->max_seq * (d->head_dim / 2) * 4);  // 11 cos
-    ly.add((size_t)d->max_seq * (d->head_dim / 2) * 4);  // 12 sin
-    ly.add(kRows * 4);                                   // 13 AMAX
-    ly.add(kRows * 4);                                   // 14 tok
-    ly.add(kRows * 4);                                   // 15 pos
-    ly.add((size_t)d->max_seq * 4);                      // 16 prompt
-    ly.add((size_t)(n1 * (W > 0 ? W : 1)) * 4);          // 17 window
-    ly.add(kRows * 4 * 2);                               // 18 step rel_pos + grp
-    ly.add((size_t)kRows * kRows * 4);                   // 19 step grp_map
-    ly.add(kRows * 4 * 2);                               // 20 prefill rel_pos + grp
-    ly.add(kRows * 4);                                   // 21 prefill grp_map
-    ly.add(cap * 4 * 3);                                 // 22 pool keys, cnt, first
-    ly.add(cap * (size_t)(G > 0 ? G : 1) * n1 * 4);      // 23 pool entries
-    ly.add((size_t)d->max_seq * 4);                      // 24 pool slot_of
-    ly.add(sizeof(DState));                              // 25 state
-    ly.add(4096);                                        // 26 debug scratch
-    ly.add(kRows * 8);                                   // 27 packed argmax
-    ly.add((2 * kRows + 1) * 4);                         // 28 step group lists
-    ly.add((2 * kRows + 1) * 4);                         // 29 prefill group lists
+    ly.add(q.bytes * B);                                 // L_SEQ: the sequences' blocks
+    ly.add(L * kRows * dkv * esz);                       // L_KS step K [L][kRows][dkv]
+    ly.add(L * kRows * dkv * esz);                       // L_VS step V
+    ly.add((size_t)kRows * d->d_model * 4);              // L_X residual stream
+    ly.add((size_t)kRows * d->d_model * esz);            // L_XN normalised rows
+    ly.add((size_t)kRows * (dq + 2 * dkv) * 4);          // L_QKV32
+    ly.add((size_t)kRows * dq * esz);                    // L_Q
+    ly.add((size_t)kRows * dq * esz);                    // L_ATT
+    ly.add((size_t)kRows * d->ffn * esz);                // L_HID
+    ly.add((size_t)kRows * d->vocab * 4);                // L_LOGITS
+    ly.add((size_t)d->max_seq * (d->head_dim / 2) * 4);  // L_COS
+    ly.add((size_t)d->max_seq * (d->head_dim / 2) * 4);  // L_SIN
+    ly.add(kRows * 4);                                   // L_AMAX
+    ly.add(kRows * 4);                                   // L_TOK
+    ly.add(kRows * 4);                                   // L_POS
+    ly.add(kRows * 4 * 2);                               // L_RS_STEP rel_pos + grp
+    ly.add((size_t)kRows * kRows * 4);                   // L_MAP_STEP grp_map
+    ly.add(kRows * 4 * 2);                               // L_RS_PRE
+    ly.add(kRows * 4);                                   // L_MAP_PRE
+    ly.add(4096);                                        // L_DEBUG scratch
+    ly.add(kRows * 8);                                   // L_AMAXP packed argmax
+    ly.add((2 * kRows + 1) * 4);                         // L_GL_STEP group lists
+    ly.add((2 * kRows + 1) * 4);                         // L_GL_PRE
     const size_t pa = attn_mma_partial_bytes(d->n_heads, d->head_dim, d->max_seq);
     const size_t pt = attn_tc_partial_bytes(d->n_heads, d->head_dim, d->max_seq);
-    ly.add(pa > pt ? pa : pt);                           // 30 attention split partials
-    ly.add(kRows * 16);                                  // 31 sampling row statistics
-    ly.add((kRows + 1) * 4);                             // 32 argmax override: [0] on, [1..] rows
+    ly.add(pa > pt ? pa : pt);                           // L_ATTN_PART split partials
+    ly.add(kRows * 16);                                  // L_SSTAT sampling row statistics
     return ly;
 }
 
@@ -272,12 +311,19 @@ static StepTables step_tables(int W, int N, int G, bool diag = false)
 
 extern "C" size_t la_workspace_bytes(const la_model_desc* desc, int W, int N, int G)
 {
-    if (check_desc(desc, W, N, G)) return 0;
-    return make_layout(desc, W, N, G, nullptr).total;
+    return la_workspace_bytes_batch(desc, W, N, G, 1);
 }
 
+extern "C" size_t la_workspace_bytes_batch(const la_model_desc* desc, int W, int N, int G, int batch)
+{
+    if (check_desc(desc, W, N, G, batch)) return 0;
+    return make_layout(desc, W, N, G, batch, nullptr, nullptr).total;
+}
+
+// One forward pass over `rows` rows: nseq sequences from seq0 on, rows / nseq
+// consecutive rows each (a prefill block: one sequence; a step: all B).
 template <typename T>
-static void forward(la_ctx* c, int rows, const RowSet& rs, bool logits)
+static void forward(la_ctx* c, int rows, const RowSet& rs, bool logits, int seq0, int nseq)
 {
     const la_model_desc& d = c->d;
     const int L = d.n_layers, D = d.d_model, H = d.n_heads, Hkv = d.n_kv_heads, hd = d.head_dim, F = d.ffn;
@@ -302,8 +348,10 @@ static void forward(la_ctx* c, int rows, const RowSet& rs, bool logits)
         const T* const* w = (const T* const*)&c->lw[(size_t)l * 9];
         T* KS = (T*)c->KS + (size_t)l * kRows * dkv;
         T* VS = (T*)c->VS + (size_t)l * kRows * dkv;
-        const T* KC = (const T*)c->KC + (size_t)l * dkv * d.max_seq;
-        const T* VC = (const T*)c->VC + (size_t)l * dkv * d.max_seq;
+        const T* KC = seq_ptr((const T*)c->KC, c->sb, seq0) + (size_t)l * dkv * d.max_seq;
+        const T* VC = seq_ptr((const T*)c->VC, c->sb, seq0) + (size_t)l * dkv * d.max_seq;
+        const DState* st = seq_ptr(c->st, c->sb, seq0);
+        const int rps = rows / nseq;  // rows of one sequence
         if (pending) {
             norm(w[0], XN);
         } else {
@@ -325,11 +373,16 @@ static void forward(la_ctx* c, int rows, const RowSet& rs, bool logits)
             launch_attn_tc(s, c->atc, l, l * kRows, c->st, rs, rs.maxoff - 1, c->pos, (const void*)Q, (void*)ATT,
                            c->attn_part, rows, &c->st->status, c->atc_cta_y);
         else if (c->use_attn_mma)
-            launch_attn_mma(s, c->st, rs, &rs == &c->rs_pre ? rows - 1 : rs.maxoff - 1, c->pos,
-                            (const void*)Q, (const void*)KC, (const void*)VC, (const void*)KS, (const void*)VS,
-                            (void*)ATT, c->attn_part, rows, H, Hkv, hd, d.max_seq);
+            launch_attn_mma(s, st, rs, &rs == &c->rs_pre ? rows - 1 : rs.maxoff - 1, c->pos, (const void*)Q,
+                            (const void*)KC, (const void*)VC, (const void*)KS, (const void*)VS, (void*)ATT,
+                            c->attn_part, rps, H, Hkv, hd, d.max_seq, nseq, c->sb);
         else
-            launch_attn_simt<T>(s, c->st, rs, c->pos, Q, KC, VC, KS, VS, ATT, rows, H, Hkv, hd, d.max_seq, scale);
+            for (int k = 0; k < nseq; k++) {
+                const size_t r0 = (size_t)k * rps;
+                launch_attn_simt<T>(s, seq_ptr(st, c->sb, k), rs, c->pos + r0, Q + r0 * dq, seq_ptr(KC, c->sb, k),
+                                    seq_ptr(VC, c->sb, k), KS + r0 * dkv, VS + r0 * dkv, ATT + r0 * dq, rps, H, Hkv,
+                                    hd, d.max_seq, scale);
+            }
         c->prof.end(s, P_ATTN, rows, 0);  // bytes filled in per step (they depend on P)
         if (c->use_tc) {
             pend = tc_oproj(c->tc, s, l, rows);
@@ -368,10 +421,10 @@ static void forward(la_ctx* c, int rows, const RowSet& rs, bool logits)
     }
 }
 
-static void run_forward(la_ctx* c, int rows, const RowSet& rs, bool logits)
+static void run_forward(la_ctx* c, int rows, const RowSet& rs, bool logits, int seq0, int nseq)
 {
-    if (c->bf16) forward<__nv_bfloat16>(c, rows, rs, logits);
-    else forward<float>(c, rows, rs, logits);
+    if (c->bf16) forward<__nv_bfloat16>(c, rows, rs, logits, seq0, nseq);
+    else forward<float>(c, rows, rs, logits, seq0, nseq);
 }
 
 // The step's launch sequence (no host synchronisation inside).
@@ -379,25 +432,30 @@ static void enqueue_step(la_ctx* c)
 {
     c->prof.idx = 0;
     c->prof.begin(c->s);
-    launch_build_rows(c->s, c->st, c->win, c->pool, c->W, c->N, c->G, c->T, c->rs_step.rel_pos, c->tok, c->pos);
+    launch_build_rows(c->s, c->st, c->win, c->pool, c->W, c->N, c->G, c->T, c->rs_step.rel_pos, c->tok, c->pos,
+                      c->B, c->sb);
     c->prof.end(c->s, P_CONTROL, 0, 0);
-    run_forward(c, c->T, c->rs_step, true);
+    run_forward(c, c->B * c->T, c->rs_step, true, 0, c->B);
     c->prof.begin(c->s);
     const int vbase = 1 + c->W * (c->N - 1);
-    if (c->tau > 0.f) launch_row_stats(c->s, c->LOGITS, c->d.vocab, c->tau, vbase, c->T, c->SSTAT);
+    if (c->tau > 0.f) launch_row_stats(c->s, c->LOGITS, c->d.vocab, c->tau, vbase, c->T, c->SSTAT, c->B);
     launch_verify_update(c->s, c->st, c->tok, c->AMAX, c->win, c->pool, c->W, c->N, c->G, c->LOGITS, c->d.vocab,
-                         c->tau, c->SSTAT, (c->flags & LA_MASK_DIAG) != 0, c->AOVR);
+                         c->tau, c->SSTAT, (c->flags & LA_MASK_DIAG) != 0, c->AOVR, c->B, c->sb);
     launch_commit(c->s, c->st, false, 0, c->N, c->KS, c->VS, c->KC, c->VC, c->d.n_layers, c->d.n_kv_heads,
-                  c->d.head_dim, c->d.max_seq, c->esz);
+                  c->d.head_dim, c->d.max_seq, c->esz, c->B, c->T, c->sb);
     c->prof.end(c->s, P_CONTROL, 0, 0);
-    cudaMemcpyAsync(c->h_st, c->st, sizeof(DState), cudaMemcpyDeviceToHost, c->s);
+    if (c->B == 1)
+        cudaMemcpyAsync(c->h_st, c->st, sizeof(DState), cudaMemcpyDeviceToHost, c->s);
+    else  // one strided copy gathers the B decode states
+        cudaMemcpy2DAsync(c->h_st, sizeof(DState), c->st, c->sb, sizeof(DState), c->B, cudaMemcpyDeviceToHost, c->s);
 }
 
-// Accumulate the last step's event timings (P_before = the step's cache length).
-static void collect_profile(la_ctx* c, int P_before)
+// Accumulate the last step's event timings (P_before = the step's cache
+// lengths summed over the sequences).
+static void collect_profile(la_ctx* c, double P_before)
 {
     Profiler& pr = c->prof;
-    const double esz = c->esz, dq = c->dq, dkv = c->dkv, T = c->T;
+    const double esz = c->esz, dq = c->dq, dkv = c->dkv, T = c->T, B = c->B;
     for (size_t i = 0; i < pr.idx; i++) {
         ProfPoint& p = pr.pts[i];
         float ms = 0.f;
@@ -405,8 +463,8 @@ static void collect_profile(la_ctx* c, int P_before)
         double by = p.bytes, fl = p.flops;
         if (p.cls == P_ATTN) {
             // the cache [0,P) once per KV head, plus the rows' q, k, v and output
-            by = (2.0 * P_before * dkv + T * (2 * dq + 2 * dkv)) * esz;
-            fl = 4.0 * T * (P_before + 1) * dq;
+            by = (2.0 * P_before * dkv + B * T * (2 * dq + 2 * dkv)) * esz;
+            fl = 4.0 * T * (P_before + B) * dq;
         }
         pr.ms[p.cls] += ms;
         pr.bytes[p.cls] += by;
@@ -449,9 +507,15 @@ static int count_kernels(cudaGraph_t g)
 extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* workspace, size_t ws_bytes,
                          uint64_t seed, int flags, la_ctx** out)
 {
+    return la_create_batch(desc, W, N, G, 1, workspace, ws_bytes, seed, flags, out);
+}
+
+extern "C" int la_create_batch(const la_model_desc* desc, int W, int N, int G, int batch, void* workspace,
+                               size_t ws_bytes, uint64_t seed, int flags, la_ctx** out)
+{
     if (!out) return LA_ERR_ARG;
     *out = nullptr;
-    if (const char* why = check_desc(desc, W, N, G)) {
+    if (const char* why = check_desc(desc, W, N, G, batch)) {
         fprintf(stderr, "la_create: %s\n", why);
         return LA_ERR_ARG;
     }
@@ -459,6 +523,10 @@ extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* w
     const int fault = parse_fault(&fault_step);
     if (fault == FAULT_BADARG) {
         fprintf(stderr, "la_create: arguments refused (injected by LA_FAULT)\n");
+        return LA_ERR_ARG;
+    }
+    if (batch > 1 && (flags & LA_ATTN_TC)) {
+        fprintf(stderr, "la_create: LA_ATTN_TC serves one sequence (batch 1)\n");
         return LA_ERR_ARG;
     }
     if (fault == FAULT_ALLOC) {
@@ -481,6 +549,9 @@ extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* w
     ctx->N = N;
     ctx->G = G;
     ctx->T = step_rows(W, N, G);
+    ctx->B = batch;
+    ctx->prefilled_seq.assign(batch, 0);
+    ctx->P_seq.assign(batch, 0);
     // the legacy default stream cannot be captured: launch directly there
     ctx->flags = desc->stream ? flags : (flags | LA_NO_GRAPH);
     ctx->seed = seed;
@@ -490,7 +561,9 @@ extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* w
     ctx->dq = desc->n_heads * desc->head_dim;
     ctx->dkv = desc->n_kv_heads * desc->head_dim;
     int lg = 0;
-    Layout ly = make_layout(desc, W, N, G, &lg);
+    SeqLayout sq{};
+    Layout ly = make_layout(desc, W, N, G, batch, &lg, &sq);
+    ctx->sb = sq.bytes;
     if (workspace) {
         if (ws_bytes < ly.total || ((uintptr_t)workspace & 1023)) {
             delete ctx;
@@ -506,40 +579,41 @@ extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* w
     }
     ctx->ws_bytes = ly.total;
     char* b = ctx->ws;
-    ctx->KC = b + ly.off[0];
-    ctx->VC = b + ly.off[1];
-    ctx->KS = b + ly.off[2];
-    ctx->VS = b + ly.off[3];
-    ctx->X = (float*)(b + ly.off[4]);
-    ctx->XN = b + ly.off[5];
-    ctx->QKV32 = (float*)(b + ly.off[6]);
-    ctx->Q = b + ly.off[7];
-    ctx->ATT = b + ly.off[8];
-    ctx->HID = b + ly.off[9];
-    ctx->LOGITS = (float*)(b + ly.off[10]);
-    ctx->cosb = (float*)(b + ly.off[11]);
-    ctx->sinb = (float*)(b + ly.off[12]);
-    ctx->AMAX = (int*)(b + ly.off[13]);
-    ctx->tok = (int*)(b + ly.off[14]);
-    ctx->pos = (int*)(b + ly.off[15]);
-    ctx->prompt = (int*)(b + ly.off[16]);
-    ctx->win = (int*)(b + ly.off[17]);
-    int* rs1 = (int*)(b + ly.off[18]);
-    int* map1 = (int*)(b + ly.off[19]);
-    int* rs2 = (int*)(b + ly.off[20]);
-    int* map2 = (int*)(b + ly.off[21]);
-    int* pk = (int*)(b + ly.off[22]);
+    char* s0 = b + ly.off[L_SEQ];  // sequence 0's block
+    ctx->KC = s0 + sq.kc;
+    ctx->VC = s0 + sq.vc;
+    ctx->prompt = (int*)(s0 + sq.prompt);
+    ctx->win = (int*)(s0 + sq.win);
+    int* pk = (int*)(s0 + sq.pk);
     const int cap = 1 << lg;
-    ctx->st = (DState*)(b + ly.off[25]);
-    ctx->dbg = (int*)(b + ly.off[26]);
-    ctx->AMAXP = (unsigned long long*)(b + ly.off[27]);
-    ctx->SSTAT = (unsigned long long*)(b + ly.off[31]);
-    ctx->AOVR = (int*)(b + ly.off[32]);
-    ctx->pool = PoolView{pk, pk + cap, (int*)(b + ly.off[23]), pk + 2 * cap, (int*)(b + ly.off[24]),
+    ctx->st = (DState*)(s0 + sq.st);
+    ctx->AOVR = (int*)(s0 + sq.aovr);
+    ctx->pool = PoolView{pk, pk + cap, (int*)(s0 + sq.ent), pk + 2 * cap, (int*)(s0 + sq.slot),
                          &ctx->st->status, cap, lg, G, N - 1};
-    int* gl1 = (int*)(b + ly.off[28]);
-    int* gl2 = (int*)(b + ly.off[29]);
-    ctx->attn_part = (float*)(b + ly.off[30]);
+    ctx->KS = b + ly.off[L_KS];
+    ctx->VS = b + ly.off[L_VS];
+    ctx->X = (float*)(b + ly.off[L_X]);
+    ctx->XN = b + ly.off[L_XN];
+    ctx->QKV32 = (float*)(b + ly.off[L_QKV32]);
+    ctx->Q = b + ly.off[L_Q];
+    ctx->ATT = b + ly.off[L_ATT];
+    ctx->HID = b + ly.off[L_HID];
+    ctx->LOGITS = (float*)(b + ly.off[L_LOGITS]);
+    ctx->cosb = (float*)(b + ly.off[L_COS]);
+    ctx->sinb = (float*)(b + ly.off[L_SIN]);
+    ctx->AMAX = (int*)(b + ly.off[L_AMAX]);
+    ctx->tok = (int*)(b + ly.off[L_TOK]);
+    ctx->pos = (int*)(b + ly.off[L_POS]);
+    int* rs1 = (int*)(b + ly.off[L_RS_STEP]);
+    int* map1 = (int*)(b + ly.off[L_MAP_STEP]);
+    int* rs2 = (int*)(b + ly.off[L_RS_PRE]);
+    int* map2 = (int*)(b + ly.off[L_MAP_PRE]);
+    ctx->dbg = (int*)(b + ly.off[L_DEBUG]);
+    ctx->AMAXP = (unsigned long long*)(b + ly.off[L_AMAXP]);
+    int* gl1 = (int*)(b + ly.off[L_GL_STEP]);
+    int* gl2 = (int*)(b + ly.off[L_GL_PRE]);
+    ctx->attn_part = (float*)(b + ly.off[L_ATTN_PART]);
+    ctx->SSTAT = (unsigned long long*)(b + ly.off[L_SSTAT]);
 
     // row tables: step (rows, positions and mask of the combined step) and prefill (causal)
     const StepTables tb = step_tables(W, N, G, (flags & LA_MASK_DIAG) != 0);
@@ -569,9 +643,9 @@ extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* w
         // zero the KV cache and the activations once: padded rows, and cache
         // positions not yet written that a tensor-core tile covers with zero
         // weight, must hold finite values
-        ck(cudaMemset(ctx->ws + ly.off[0], 0, ly.off[11] - ly.off[0]));
+        // (with the sequences' blocks: decode states and argmax overrides start cleared)
+        ck(cudaMemset(ctx->ws + ly.off[L_SEQ], 0, ly.off[L_COS] - ly.off[L_SEQ]));
         ck(cudaMemset(ctx->AMAXP, 0, kRows * 8));
-        ck(cudaMemset(ctx->AOVR, 0, (kRows + 1) * 4));
         ck(cudaMemcpy(rs1, rel.data(), kRows * 4, cudaMemcpyHostToDevice));
         ck(cudaMemcpy(rs1 + kRows, grp.data(), kRows * 4, cudaMemcpyHostToDevice));
         ck(cudaMemcpy(map1, map.data(), map.size() * 4, cudaMemcpyHostToDevice));
@@ -582,7 +656,7 @@ extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* w
         ck(cudaMemcpy(gl2, pgl.data(), pgl.size() * 4, cudaMemcpyHostToDevice));
         ck(cudaMemcpy(ctx->cosb, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice));
         ck(cudaMemcpy(ctx->sinb, sn.data(), sn.size() * 4, cudaMemcpyHostToDevice));
-        ck(cudaHostAlloc((void**)&ctx->h_st, sizeof(DState), cudaHostAllocDefault));
+        ck(cudaHostAlloc((void**)&ctx->h_st, sizeof(DState) * batch, cudaHostAllocDefault));
         ck(cudaEventCreate(&ctx->ev0));
         ck(cudaEventCreate(&ctx->ev1));
     }
@@ -634,7 +708,7 @@ extern "C" int la_create(const la_model_desc* desc, int W, int N, int G, void* w
         la_destroy(ctx);
         return rc;
     }
-    ctx->stats.rows = ctx->T;
+    ctx->stats.rows = ctx->T * ctx->B;
     ctx->prof.on = (flags & LA_PROFILE) != 0;
     *out = ctx;
     return LA_OK;
@@ -667,55 +741,81 @@ static uint64_t splitmix64(uint64_t* x)
     return z ^ (z >> 31);
 }
 
-extern "C" int la_prefill(la_ctx* ctx, const int32_t* prompt, int len)
+// Prefill of sequence `seq`: its prompt's KV into its cache, its window and
+// pool initialised, its decode state reset.
+static int prefill_seq(la_ctx* ctx, int seq, const int32_t* prompt, int len)
 {
-    if (!ctx) return LA_ERR_ARG;
     if (!prompt || len < 1) return fail(ctx, LA_ERR_ARG, "prompt must hold at least one token");
     if (len + ctx->W + ctx->N > ctx->d.max_seq) return fail(ctx, LA_ERR_CAPACITY, "prompt too long for max_seq");
     for (int i = 0; i < len; i++)
         if (prompt[i] < 0 || prompt[i] >= ctx->d.vocab) return fail(ctx, LA_ERR_ARG, "token id out of range");
     ctx->prefilled = false;
+    ctx->prefilled_seq[seq] = 0;
     cudaStream_t s = ctx->s;
-    LA_CK(cudaMemcpyAsync(ctx->prompt, prompt, (size_t)len * 4, cudaMemcpyHostToDevice, s));
+    const size_t sb = ctx->sb;
+    DState* st = seq_ptr(ctx->st, sb, seq);
+    DState* h = ctx->h_st + seq;
+    int* dprompt = seq_ptr(ctx->prompt, sb, seq);
+    const PoolView pool = seq_pool(ctx->pool, sb, seq);
+    LA_CK(cudaMemcpyAsync(dprompt, prompt, (size_t)len * 4, cudaMemcpyHostToDevice, s));
     std::vector<int> win((size_t)(ctx->N - 1) * (ctx->W > 0 ? ctx->W : 1), 0);
     uint64_t sm = ctx->seed;
     for (int l = 0; l < ctx->N - 1; l++)
         for (int j = 0; j < ctx->W; j++) win[(size_t)l * ctx->W + j] = prompt[splitmix64(&sm) % (uint64_t)len];
-    LA_CK(cudaMemcpyAsync(ctx->win, win.data(), win.size() * 4, cudaMemcpyHostToDevice, s));
+    LA_CK(cudaMemcpyAsync(seq_ptr(ctx->win, sb, seq), win.data(), win.size() * 4, cudaMemcpyHostToDevice, s));
     LA_CK(cudaStreamSynchronize(s));  // win is a host temporary
-    launch_pool_reset(s, ctx->pool);
-    launch_set_state(s, ctx->st, 0, prompt[len - 1], true);
+    launch_pool_reset(s, pool);
+    launch_set_state(s, st, 0, prompt[len - 1], true);
     if ((ctx->flags & LA_PRESEED_PROMPT) && ctx->G > 0 && len >= ctx->N)
-        launch_pool_insert(s, ctx->pool, ctx->prompt, ctx->prompt + 1, 1, len - ctx->N + 1);
+        launch_pool_insert(s, pool, dprompt, dprompt + 1, 1, len - ctx->N + 1);
     for (int P0 = 0; P0 < len - 1; P0 += kRows) {
         const int n = (len - 1 - P0) < kRows ? (len - 1 - P0) : kRows;
-        launch_set_state(s, ctx->st, P0, prompt[len - 1], false);
-        launch_prefill_rows(s, ctx->st, ctx->prompt, P0, n, ctx->tok, ctx->pos);
-        run_forward(ctx, n, ctx->rs_pre, false);
-        launch_commit(s, ctx->st, true, n, n, ctx->KS, ctx->VS, ctx->KC, ctx->VC, ctx->d.n_layers,
-                      ctx->d.n_kv_heads, ctx->d.head_dim, ctx->d.max_seq, ctx->esz);
+        launch_set_state(s, st, P0, prompt[len - 1], false);
+        launch_prefill_rows(s, st, dprompt, P0, n, ctx->tok, ctx->pos);
+        run_forward(ctx, n, ctx->rs_pre, false, seq, 1);
+        launch_commit(s, st, true, n, n, ctx->KS, ctx->VS, seq_ptr(ctx->KC, sb, seq), seq_ptr(ctx->VC, sb, seq),
+                      ctx->d.n_layers, ctx->d.n_kv_heads, ctx->d.head_dim, ctx->d.max_seq, ctx->esz);
     }
-    launch_set_state(s, ctx->st, len - 1, prompt[len - 1], false);
+    launch_set_state(s, st, len - 1, prompt[len - 1], false);
     LA_CK(cudaGetLastError());
-    LA_CK(cudaMemcpyAsync(ctx->h_st, ctx->st, sizeof(DState), cudaMemcpyDeviceToHost, s));
+    LA_CK(cudaMemcpyAsync(h, st, sizeof(DState), cudaMemcpyDeviceToHost, s));
     LA_CK(cudaStreamSynchronize(s));
-    if (ctx->h_st->status) return fail(ctx, ctx->h_st->status, "device status set during prefill");
-    ctx->P_host = len - 1;
-    ctx->prefilled = true;
+    if (h->status) return fail(ctx, h->status, "device status set during prefill");
+    ctx->P_seq[seq] = len - 1;
+    ctx->prefilled_seq[seq] = 1;
+    bool all = true;
+    for (char f : ctx->prefilled_seq) all = all && f;
+    ctx->prefilled = all;
     ctx->have_step = false;
-    memset(&ctx->stats, 0, sizeof(ctx->stats));
-    ctx->stats.prefill_tokens = len - 1;
-    ctx->stats.P = len - 1;
-    ctx->stats.rows = ctx->T;
+    if (seq == 0) memset(&ctx->stats, 0, sizeof(ctx->stats));  // sequence 0's prefill starts new statistics
+    ctx->stats.prefill_tokens += len - 1;
+    ctx->P_host = ctx->P_seq[0];
+    ctx->stats.P = ctx->P_seq[0];
+    ctx->stats.rows = ctx->T * ctx->B;
     return LA_OK;
 }
 
-extern "C" int la_step(la_ctx* ctx, int32_t* out, int cap, int* n_out)
+extern "C" int la_prefill(la_ctx* ctx, const int32_t* prompt, int len)
 {
     if (!ctx) return LA_ERR_ARG;
-    if (!out || !n_out || cap < ctx->N) return fail(ctx, LA_ERR_ARG, "out must hold N tokens");
-    if (!ctx->prefilled) return fail(ctx, LA_ERR_STATE, "la_step before la_prefill");
-    if (ctx->P_host + ctx->W + ctx->N > ctx->d.max_seq) return fail(ctx, LA_ERR_CAPACITY, "KV cache full");
+    if (ctx->B > 1) return fail(ctx, LA_ERR_STATE, "a batched context: use la_prefill_seq");
+    return prefill_seq(ctx, 0, prompt, len);
+}
+
+extern "C" int la_prefill_seq(la_ctx* ctx, int seq, const int32_t* prompt, int len)
+{
+    if (!ctx) return LA_ERR_ARG;
+    if (seq < 0 || seq >= ctx->B) return fail(ctx, LA_ERR_ARG, "seq out of range");
+    return prefill_seq(ctx, seq, prompt, len);
+}
+
+// One combined step of every sequence: the step's graph (captured on first
+// use), then the B decode states on the host.
+static int run_step(la_ctx* ctx)
+{
+    if (!ctx->prefilled) return fail(ctx, LA_ERR_STATE, "la_step before every sequence was prefilled");
+    for (int b = 0; b < ctx->B; b++)
+        if (ctx->P_seq[b] + ctx->W + ctx->N > ctx->d.max_seq) return fail(ctx, LA_ERR_CAPACITY, "KV cache full");
     cudaStream_t s = ctx->s;
     // the attention's cache kernel: one CTA per split the step's rows reach
     if (ctx->use_attn_tc) ctx->atc_cta_y = attn_tc_splits(ctx->atc, ctx->P_host, ctx->rs_step.maxoff - 1);
@@ -768,28 +868,61 @@ extern "C" int la_step(la_ctx* ctx, int32_t* out, int cap, int* n_out)
     LA_CK(cudaEventRecord(ctx->ev1, s));
     LA_CK(cudaGetLastError());
     LA_CK(cudaEventSynchronize(ctx->ev1));
-    const DState& h = *ctx->h_st;
-    if (h.status) {
-        // the device state is not trusted after a device-side error: the
-        // context needs la_prefill again (which clears the status word)
-        ctx->prefilled = false;
-        return fail(ctx, h.status, "device status set during step");
+    for (int b = 0; b < ctx->B; b++) {
+        const DState& h = ctx->h_st[b];
+        if (h.status) {
+            // the device state is not trusted after a device-side error: the
+            // context needs la_prefill again (which clears the status word)
+            ctx->prefilled = false;
+            for (char& f : ctx->prefilled_seq) f = 0;
+            return fail(ctx, h.status, "device status set during step");
+        }
+        if (h.n_emit < 1 || h.n_emit > ctx->N) return fail(ctx, LA_ERR_STATE, "corrupt step result");
     }
-    const int n = h.n_emit;
-    if (n < 1 || n > ctx->N) return fail(ctx, LA_ERR_STATE, "corrupt step result");
-    memcpy(out, h.emit, sizeof(int) * n);
-    *n_out = n;
-    ctx->P_host = h.P;
+    double P_before = 0;
+    for (int b = 0; b < ctx->B; b++) {
+        const DState& h = ctx->h_st[b];
+        ctx->P_seq[b] = h.P;
+        ctx->stats.emitted += h.n_emit;
+        ctx->stats.accept_hist[h.n_emit]++;
+        P_before += h.P_before;
+    }
+    ctx->P_host = ctx->P_seq[0];
     ctx->have_step = true;
     float ms = 0.f;
     cudaEventElapsedTime(&ms, ctx->ev0, ctx->ev1);
     ctx->stats.steps++;
-    ctx->stats.emitted += n;
-    ctx->stats.accept_hist[n]++;
-    ctx->stats.P = h.P;
+    ctx->stats.P = ctx->P_seq[0];
     ctx->stats.last_step_ms = ms;
     ctx->stats.kernels_per_step = ctx->kernels_per_step;
-    if (ctx->prof.on) collect_profile(ctx, h.P_before);
+    if (ctx->prof.on) collect_profile(ctx, P_before);
+    return LA_OK;
+}
+
+extern "C" int la_step(la_ctx* ctx, int32_t* out, int cap, int* n_out)
+{
+    if (!ctx) return LA_ERR_ARG;
+    if (ctx->B > 1) return fail(ctx, LA_ERR_STATE, "a batched context: use la_step_batch");
+    if (!out || !n_out || cap < ctx->N) return fail(ctx, LA_ERR_ARG, "out must hold N tokens");
+    const int rc = run_step(ctx);
+    if (rc) return rc;
+    const DState& h = ctx->h_st[0];
+    memcpy(out, h.emit, sizeof(int) * h.n_emit);
+    *n_out = h.n_emit;
+    return LA_OK;
+}
+
+extern "C" int la_step_batch(la_ctx* ctx, int32_t* out, int cap, int* n_out)
+{
+    if (!ctx) return LA_ERR_ARG;
+    if (!out || !n_out || cap < ctx->N) return fail(ctx, LA_ERR_ARG, "out must hold N tokens per sequence");
+    const int rc = run_step(ctx);
+    if (rc) return rc;
+    for (int b = 0; b < ctx->B; b++) {
+        const DState& h = ctx->h_st[b];
+        memcpy(out + (size_t)b * cap, h.emit, sizeof(int) * h.n_emit);
+        n_out[b] = h.n_emit;
+    }
     return LA_OK;
 }
 
@@ -798,9 +931,13 @@ extern "C" int la_set_sampling(la_ctx* ctx, float temperature, uint64_t seed)
     if (!ctx) return LA_ERR_ARG;
     if (temperature != temperature || temperature > 3.0e38f) return fail(ctx, LA_ERR_ARG, "temperature must be finite");
     ctx->tau = temperature > 0.f ? temperature : 0.f;
-    const unsigned long long v = seed;
-    LA_CK(cudaMemcpyAsync(&ctx->st->rng, &v, sizeof(v), cudaMemcpyHostToDevice, ctx->s));
-    LA_CK(cudaStreamSynchronize(ctx->s));
+    // sequence b of a batch draws from the stream seeded with seed + b
+    std::vector<unsigned long long> v(ctx->B);
+    for (int b = 0; b < ctx->B; b++) {
+        v[b] = seed + (uint64_t)b;
+        LA_CK(cudaMemcpyAsync(&seq_ptr(ctx->st, ctx->sb, b)->rng, &v[b], sizeof(v[b]), cudaMemcpyHostToDevice, ctx->s));
+    }
+    LA_CK(cudaStreamSynchronize(ctx->s));  // v is a host temporary
     if (ctx->gexec) {  // the step's launch sequence changes: capture it again
         cudaGraphExecDestroy(ctx->gexec);
         ctx->gexec = nullptr;
@@ -863,7 +1000,7 @@ extern "C" int la_debug_logits(la_ctx* ctx, float* host, size_t n)
     if (!(ctx->flags & LA_DEBUG_LOGITS)) return fail(ctx, LA_ERR_STATE, "context made without LA_DEBUG_LOGITS");
     size_t need = (size_t)ctx->T * ctx->d.vocab;
     if (n < need) return fail(ctx, LA_ERR_ARG, "buffer too small");
-    LA_CK(cudaMemcpyAsync(host, ctx->LOGITS, need * 4, cudaMemcpyDeviceToHost, ctx->s));
+    LA_CK(cudaMemcpyAsync(host, ctx->LOGITS + (size_t)ctx->dseq * need, need * 4, cudaMemcpyDeviceToHost, ctx->s));
     LA_CK(cudaStreamSynchronize(ctx->s));
     return LA_OK;
 }
@@ -873,7 +1010,8 @@ extern "C" int la_debug_argmax(la_ctx* ctx, int32_t* host, int cap, int* T_out)
     if (!ctx || !host || !T_out) return LA_ERR_ARG;
     if (!ctx->have_step) return fail(ctx, LA_ERR_STATE, "no step yet");
     if (cap < ctx->T) return fail(ctx, LA_ERR_ARG, "buffer too small");
-    LA_CK(cudaMemcpyAsync(host, ctx->AMAX, (size_t)ctx->T * 4, cudaMemcpyDeviceToHost, ctx->s));
+    LA_CK(cudaMemcpyAsync(host, ctx->AMAX + (size_t)ctx->dseq * ctx->T, (size_t)ctx->T * 4, cudaMemcpyDeviceToHost,
+                          ctx->s));
     LA_CK(cudaStreamSynchronize(ctx->s));
     *T_out = ctx->T;
     return LA_OK;
@@ -884,11 +1022,12 @@ extern "C" int la_debug_rows(la_ctx* ctx, int32_t* tok, int32_t* pos, int cap, i
     if (!ctx || !tok || !pos || !T_out || !ncand) return LA_ERR_ARG;
     if (!ctx->have_step) return fail(ctx, LA_ERR_STATE, "no step yet");
     if (cap < ctx->T) return fail(ctx, LA_ERR_ARG, "buffer too small");
-    LA_CK(cudaMemcpyAsync(tok, ctx->tok, (size_t)ctx->T * 4, cudaMemcpyDeviceToHost, ctx->s));
-    LA_CK(cudaMemcpyAsync(pos, ctx->pos, (size_t)ctx->T * 4, cudaMemcpyDeviceToHost, ctx->s));
+    const size_t r0 = (size_t)ctx->dseq * ctx->T;
+    LA_CK(cudaMemcpyAsync(tok, ctx->tok + r0, (size_t)ctx->T * 4, cudaMemcpyDeviceToHost, ctx->s));
+    LA_CK(cudaMemcpyAsync(pos, ctx->pos + r0, (size_t)ctx->T * 4, cudaMemcpyDeviceToHost, ctx->s));
     LA_CK(cudaStreamSynchronize(ctx->s));
     *T_out = ctx->T;
-    *ncand = ctx->h_st->ncand;
+    *ncand = ctx->h_st[ctx->dseq].ncand;
     return LA_OK;
 }
 
@@ -905,7 +1044,7 @@ extern "C" int la_debug_pool(la_ctx* ctx, int32_t key, int32_t* host, int cap, i
     int* dcnt = ctx->dbg + 1;
     int* dout = ctx->dbg + 2;
     LA_CK(cudaMemcpyAsync(dkey, &key, 4, cudaMemcpyHostToDevice, ctx->s));
-    launch_pool_lookup(ctx->s, ctx->pool, dkey, 1, dout, dcnt);
+    launch_pool_lookup(ctx->s, seq_pool(ctx->pool, ctx->sb, ctx->dseq), dkey, 1, dout, dcnt);
     LA_CK(cudaMemcpyAsync(host, dout, (size_t)tot * 4, cudaMemcpyDeviceToHost, ctx->s));
     LA_CK(cudaMemcpyAsync(count, dcnt, 4, cudaMemcpyDeviceToHost, ctx->s));
     LA_CK(cudaStreamSynchronize(ctx->s));
@@ -923,8 +1062,17 @@ extern "C" int la_debug_set_argmax_override(la_ctx* ctx, const int32_t* host, in
         buf[0] = 1;
         memcpy(buf.data() + 1, host, (size_t)n * 4);
     }
-    LA_CK(cudaMemcpyAsync(ctx->AOVR, buf.data(), buf.size() * 4, cudaMemcpyHostToDevice, ctx->s));
+    LA_CK(cudaMemcpyAsync(seq_ptr(ctx->AOVR, ctx->sb, ctx->dseq), buf.data(), buf.size() * 4, cudaMemcpyHostToDevice,
+                          ctx->s));
     LA_CK(cudaStreamSynchronize(ctx->s));  // buf is a host temporary
+    return LA_OK;
+}
+
+extern "C" int la_debug_select(la_ctx* ctx, int seq)
+{
+    if (!ctx) return LA_ERR_ARG;
+    if (seq < 0 || seq >= ctx->B) return fail(ctx, LA_ERR_ARG, "seq out of range");
+    ctx->dseq = seq;
     return LA_OK;
 }
 
@@ -934,7 +1082,8 @@ extern "C" int la_debug_window(la_ctx* ctx, int32_t* host, int cap)
     const int n = (ctx->N - 1) * ctx->W;
     if (cap < n) return fail(ctx, LA_ERR_ARG, "buffer too small");
     if (n) {
-        LA_CK(cudaMemcpyAsync(host, ctx->win, (size_t)n * 4, cudaMemcpyDeviceToHost, ctx->s));
+        LA_CK(cudaMemcpyAsync(host, seq_ptr(ctx->win, ctx->sb, ctx->dseq), (size_t)n * 4, cudaMemcpyDeviceToHost,
+                              ctx->s));
         LA_CK(cudaStreamSynchronize(ctx->s));
     }
     return LA_OK;

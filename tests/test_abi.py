@@ -87,3 +87,26 @@ def test_every_declaration_cites_the_pages_or_says_there_is_none():
             prev_end = src.index(";", m.end()) + 1
             n += 1
         assert n == len(_declared()) or fn != "lookahead.h"
+
+
+def test_batched_workspace_grows_by_one_sequence_block_per_sequence():
+    """la_workspace_bytes_batch needs no GPU: batch 1 is la_workspace_bytes;
+    each further sequence adds the same block, which holds at least that
+    sequence's bf16 KV cache; batch x T > 128 rows is refused."""
+    import lossless_lookahead_decoding_gb300 as LA
+    from helpers import build_lib
+    build_lib()
+    d = LA.la_model_desc(n_layers=32, d_model=4096, n_heads=32, n_kv_heads=32, head_dim=128, ffn=11008,
+                         vocab=32000, max_seq=804, rms_eps=1e-5, rope_theta=1e4, dtype=LA.LA_BF16,
+                         emb=1, layer_w=1, final_norm=1, lm_head=1, stream=None)
+    W, N, G = 7, 5, 7  # T = 57 rows: two sequences fit one 128-row pass
+    one = LA.la_workspace_bytes(d, W, N, G)
+    assert LA.la_workspace_bytes_batch(d, W, N, G, 1) == one
+    two = LA.la_workspace_bytes_batch(d, W, N, G, 2)
+    assert two - one >= 2 * 32 * 32 * 128 * 804 * 2
+    assert LA.la_workspace_bytes_batch(d, W, N, G, 3) == 0      # 171 rows
+    assert LA.la_workspace_bytes_batch(d, W, N, G, 0) == 0
+    # greedy rows: one per sequence, up to 128 sequences
+    g1, g2 = LA.la_workspace_bytes_batch(d, 0, 2, 0, 1), LA.la_workspace_bytes_batch(d, 0, 2, 0, 2)
+    assert LA.la_workspace_bytes_batch(d, 0, 2, 0, 128) == g1 + 127 * (g2 - g1)
+    assert LA.la_workspace_bytes_batch(d, 0, 2, 0, 129) == 0

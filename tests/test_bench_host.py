@@ -74,3 +74,15 @@ def test_lookahead_overrides_and_sweep_shapes():
         assert 1 + (W + G) * (N - 1) <= 128 and N >= 2
         if W == 0 and G > 0:
             assert pre
+
+
+def test_batch_sweep_points_fit_one_pass():
+    """Every point of bench.py --batch-sweep fits one 128-row forward pass,
+    greedy runs from 1 to 128 sequences, and the workload's own lookahead
+    setting is a batch-1 point."""
+    import bench
+    for W, N, G, b in bench.BATCH_SWEEP:
+        assert b >= 1 and b * (1 + (W + G) * (N - 1)) <= 128, (W, N, G, b)
+    greedy = sorted(b for W, N, G, b in bench.BATCH_SWEEP if W == 0 and G == 0)
+    assert greedy[0] == 1 and greedy[-1] == 128
+    assert (15, 5, 15, 1) in bench.BATCH_SWEEP
