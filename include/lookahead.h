@@ -91,7 +91,7 @@ typedef struct la_stats {
     long long prefill_tokens; /* prompt tokens written to the cache          */
     long long accept_hist[9]; /* steps by tokens emitted (1..N)              */
     int P;                    /* tokens whose KV is cached                   */
-    int rows;                 /* T rows per step                             */
+    int rows;                 /* rows per step: T (batched: batch x T)       */
     float last_step_ms;       /* device time of the last step (CUDA events)  */
     int kernels_per_step;     /* kernel launches in one captured step        */
 } la_stats;
