@@ -206,6 +206,8 @@ void launch_pool_lookup(cudaStream_t s, PoolView pool, const int* keys, int n, i
 __global__ void k_build_rows(DState* st, const int* win, PoolView pool, int W, int N, int G, int T,
                              const int* rel_pos, int* tok, int* pos, size_t sb)
 {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int s_slot, s_cnt;
     const int b = blockIdx.x;
     st = seq_ptr(st, sb, b);
@@ -247,7 +249,7 @@ __global__ void k_build_rows(DState* st, const int* win, PoolView pool, int W, i
 void launch_build_rows(cudaStream_t s, DState* st, const int* win, PoolView pool, int W, int N, int G, int T,
                        const int* rel_pos, int* tok, int* pos, int B, size_t sb)
 {
-    k_build_rows<<<B, 128, 0, s>>>(st, win, pool, W, N, G, T, rel_pos, tok, pos, sb);
+    launch_pdl(k_build_rows, dim3(B), dim3(128), 0, s, st, win, pool, W, N, G, T, rel_pos, tok, pos, sb);
 }
 
 __global__ void k_prefill_rows(const DState* st, const int* prompt, int P0, int n, int* tok, int* pos)
@@ -574,6 +576,8 @@ __global__ void __launch_bounds__(kVerifyWarps * 32)
                     const float* logits, int V, float tau, const unsigned long long* stats, int diag,
                     const int* ovr, size_t sb)
 {
+    pdl_wait();
+    pdl_trigger();
     {  // block b serves sequence b of a batch
         const int b = blockIdx.x;
         const size_t T = 1 + (size_t)(W + G) * (N - 1);
@@ -679,8 +683,8 @@ void launch_verify_update(cudaStream_t s, DState* st, const int* tok, const int*
                           int W, int N, int G, const float* logits, int V, float tau,
                           const unsigned long long* stats, bool diag, const int* ovr, int B, size_t sb)
 {
-    k_verify_update<<<B, kVerifyWarps * 32, 0, s>>>(st, tok, amax, win, pool, W, N, G, logits, V, tau, stats,
-                                                    diag ? 1 : 0, ovr, sb);
+    launch_pdl(k_verify_update, dim3(B), dim3(kVerifyWarps * 32), 0, s, st, tok, amax, win, pool, W, N, G, logits,
+               V, tau, stats, diag ? 1 : 0, ovr, sb);
 }
 
 // ------------------------------------------------------------------ commit ---
@@ -693,6 +697,8 @@ void launch_verify_update(cudaStream_t s, DState* st, const int* tok, const int*
 __global__ void k_commit(const DState* st, int prefill, int n_prefill, const uint4* KS, const uint4* VS,
                          uint4* KC, uint4* VC, int Hkv, int hd_vec, int max_seq, int T, size_t sb)
 {
+    pdl_wait();
+    pdl_trigger();
     const int i = blockIdx.x, l = blockIdx.y, b = blockIdx.z;
     st = seq_ptr(st, sb, b);
     KC = seq_ptr(KC, sb, b);
@@ -717,8 +723,8 @@ void launch_commit(cudaStream_t s, const DState* st, bool prefill, int n_prefill
 {
     int hd_vec = hd * esz / 16;
     dim3 grid(prefill ? n_prefill : n_max, L, B);
-    k_commit<<<grid, 256, 0, s>>>(st, prefill ? 1 : 0, n_prefill, (const uint4*)KS, (const uint4*)VS, (uint4*)KC,
-                                  (uint4*)VC, Hkv, hd_vec, max_seq, T, sb);
+    launch_pdl(k_commit, grid, dim3(256), 0, s, st, prefill ? 1 : 0, n_prefill, (const uint4*)KS, (const uint4*)VS,
+               (uint4*)KC, (uint4*)VC, Hkv, hd_vec, max_seq, T, sb);
 }
 
 }  // namespace la

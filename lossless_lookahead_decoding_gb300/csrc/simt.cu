@@ -22,6 +22,8 @@ constexpr int kEmbVec = 4;  // 16-byte loads per thread: d <= 4 * 256 * (16 / si
 template <typename T>
 __global__ void k_embed(const int* tok, const T* emb, float* X, int d)
 {
+    pdl_wait();
+    pdl_trigger();
     constexpr int E = 16 / sizeof(T);  // elements per 16-byte load
     const int r = blockIdx.x;
     const T* e = emb + (size_t)tok[r] * d;
@@ -49,7 +51,7 @@ __global__ void k_embed(const int* tok, const T* emb, float* X, int d)
 template <typename T>
 void launch_embed(cudaStream_t s, const int* tok, const T* emb, float* X, int rows, int d)
 {
-    k_embed<T><<<rows, 256, 0, s>>>(tok, emb, X, d);
+    launch_pdl(k_embed<T>, dim3(rows), dim3(256), 0, s, tok, emb, X, d);
 }
 
 // -------------------------------------------------------------- rmsnorm ---

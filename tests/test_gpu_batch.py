@@ -196,3 +196,23 @@ def test_batch_errors():
         for _ in range(16):
             small.step_batch()
     assert e.value.code == LA.LA_ERR_CAPACITY
+
+
+def test_batch_7b_full_depth():
+    """The full 32-layer 7B model: two sequences (W=7 N=5 G=7, 512- and
+    496-token prompts) in one pass equal their batch-1 decodings bit for bit
+    (tokens, rows, argmaxes, windows, pools) for 8 steps, and sequence 0's
+    tokens equal the same library's greedy decode of its prompt."""
+    import lossless_lookahead_decoding_gb300 as LA
+    cfg = I.MODELS["7b"]
+    dw = LA.device_weights(cfg, I.iter_weights(cfg, 0, bf16=False), LA.LA_BF16)
+    batched = LA.Decoder(cfg, dw, LA.LA_BF16, 7, 5, 7, 640, batch=2)
+    singles = [LA.Decoder(cfg, dw, LA.LA_BF16, 7, 5, 7, 640) for _ in range(2)]
+    prompts = _prompts("7b", 2, cut=16)
+    outs = _run(batched, singles, prompts, 8, logits=False)
+    for d in [batched] + singles:
+        d.close()
+    greedy = LA.Decoder(cfg, dw, LA.LA_BF16, 0, 2, 0, 640)
+    g = greedy.generate(prompts[0], len(outs[0]))
+    greedy.close()
+    assert np.array_equal(np.array(outs[0], np.int32), g)
