@@ -216,3 +216,34 @@ def test_batch_7b_full_depth():
     g = greedy.generate(prompts[0], len(outs[0]))
     greedy.close()
     assert np.array_equal(np.array(outs[0], np.int32), g)
+
+
+@pytest.mark.parametrize("WNG,B", [((0, 2, 0), 128), ((1, 2, 0), 64)], ids=["greedy-b128", "w1-b64"])
+def test_batch_fills_the_128_row_pass(WNG, B):
+    """A pass of exactly 128 rows on the tcgen05 GEMMs at 7B widths (2-layer
+    slice): 128 greedy sequences, or 64 of two rows; the first, a middle and
+    the last sequence against their batch-1 contexts, bit for bit."""
+    import lossless_lookahead_decoding_gb300 as LA
+    cfg = I.MODELS["7b"].sliced(2)
+    full = I.make_weights(I.MODELS["7b"], 0, bf16=True, layers=[0, 1])
+    w = {k: (v[:2] if isinstance(v, list) else v) for k, v in full.items()}
+    dw = LA.device_weights(cfg, w, LA.LA_BF16)
+    flags = LA.LA_DEBUG_LOGITS
+    batched = LA.Decoder(cfg, dw, LA.LA_BF16, *WNG, 320, flags=flags, batch=B)
+    prompts = [I.random_prompt(64 + (7 * b) % 97, cfg.vocab, 100 + b) for b in range(B)]
+    for b, p in enumerate(prompts):
+        batched.prefill_seq(b, p)
+    picks = [0, B // 2, B - 1]
+    singles = {b: LA.Decoder(cfg, dw, LA.LA_BF16, *WNG, 320, flags=flags) for b in picks}
+    for b, d in singles.items():
+        d.prefill(prompts[b])
+    for _ in range(3):
+        got = batched.step_batch()
+        assert all(1 <= len(t) <= WNG[1] for t in got)
+        for b, d in singles.items():
+            assert np.array_equal(got[b], d.step()), b
+            batched.select(b)
+            assert np.array_equal(batched.argmax(), d.argmax()), b
+            assert np.array_equal(batched.logits().view(np.uint32), d.logits().view(np.uint32)), b
+    for d in [batched] + list(singles.values()):
+        d.close()
