@@ -37,8 +37,8 @@
 // maxima, O = the sum of exp2(m_part - M) O_part over region A's splits in
 // ascending order and then region B (likewise the softmax sum), output
 // O / sum in bf16.  The cache kernel's grid holds one CTA per (head group,
-// split) up to a cap, each CTA taking splits blockIdx.y, + gridDim.y, ...; the
-// caller sizes it to the splits the step needs.
+// split), sized by the caller to the splits the step needs (a smaller grid
+// would have each CTA take splits blockIdx.y, + gridDim.y, ...).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -875,16 +875,13 @@ int attn_tc_plan(AttnTcPlan* pl, const void* Q, int q_rows, const void* KC, cons
     int hpc = 1;
     const int group = H / Hkv;
     while (group % (2 * hpc) == 0 && 2 * hpc * bq <= kRows) hpc *= 2;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))
-        return LA_ERR_CUDA;
-    const int groups = H / hpc, nsa = (max_seq + kSA - 1) / kSA;
+    const int nsa = (max_seq + kSA - 1) / kSA;
     if (nsa > kMaxSp) return LA_ERR_ARG;
-    const int window_ctas = H * ((n_items + kBWarps - 1) / kBWarps);
-    // two CTAs of either kernel fit on an SM: the cache kernel's CTAs take the
-    // places the window kernel's leave, so both grids are resident together
-    int cap = (2 * sms - window_ctas) / groups;
-    cap = cap < 1 ? 1 : (cap > nsa ? nsa : cap);
+    // one cache-kernel CTA per split: at long contexts its grid outgrows the
+    // SMs' two slots per SM, and the window kernel's CTAs start as cache CTAs
+    // leave; capping the grid so that both stay resident (each CTA taking
+    // several splits in turn) was slower at the 13B and 34B contexts
+    const int cap = nsa;
     const int dq = H * hd, dkv = Hkv * hd;
     if (!encode_map(&pl->qmap, Q, q_rows, dq, bq) || !encode_map(&pl->kmap, KC, kv_rows, hd, kBlk) ||
         !encode_map(&pl->vmap, VC, kv_rows, hd, kBlk) || !encode_map(&pl->ksmap, KS, ks_rows, dkv, kRows) ||
