@@ -66,9 +66,10 @@ def parse():
                     help="W,N,G to use instead of the workload's lookahead settings")
     ap.add_argument("--preseed", default="auto", choices=["auto", "on", "off"],
                     help="seed the n-gram pool with the prompt's n-grams (auto: the workload's setting)")
-    ap.add_argument("--attn", default="mma", choices=["mma", "tc"],
-                    help="the step's attention kernel: mma (mma.sync, the default) or tc (tcgen05 + TMA, "
-                         "LA_ATTN_TC; needs W + N - 2 <= 31)")
+    ap.add_argument("--attn", default="auto", choices=["auto", "mma", "tc"],
+                    help="the step's attention kernel: tc (tcgen05 + TMA, LA_ATTN_TC; needs W + N - 2 <= 31 and "
+                         "max_seq <= 4096), mma (mma.sync, the library's default), or auto (tc where it applies, "
+                         "else mma; the lookahead and greedy decoders always use the same one)")
     ap.add_argument("--micro", action="store_true",
                     help="instead of the benchmark line: the attention and n-gram pool micro-benchmarks")
     ap.add_argument("--sample", type=float, default=0.0,
@@ -91,6 +92,12 @@ def lookahead_of(args):
         W, N, G = (int(x) for x in args.wng.split(","))
     pre = PRESEED.get(args.workload, False) if args.preseed == "auto" else args.preseed == "on"
     return W, N, G, pre
+
+
+def attn_tc_applies(W, N, max_seq):
+    """Whether the tcgen05 attention (LA_ATTN_TC) serves this window: every
+    step row within 31 positions of P, max_seq <= 4096."""
+    return (W + N - 2 if W > 0 else N - 1) <= 31 and max_seq <= 4096
 
 
 def load_peaks():
@@ -245,7 +252,9 @@ def run_ours(args, rank, world):
     prompt = I.make_prompt(args.workload)
     max_seq = len(prompt) + gen + W + N + 16
     flags = LA.LA_PRESEED_PROMPT if pre else 0
-    attn_flag = LA.LA_ATTN_TC if getattr(args, "attn", "mma") == "tc" else 0
+    attn = getattr(args, "attn", "mma")
+    use_tc = attn == "tc" or (attn == "auto" and attn_tc_applies(W, N, max_seq))
+    attn_flag = LA.LA_ATTN_TC if use_tc else 0
     flags |= attn_flag
     t_gen = time.perf_counter()
     dw = build_model(cfg, LA.LA_BF16)

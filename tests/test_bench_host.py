@@ -86,3 +86,16 @@ def test_batch_sweep_points_fit_one_pass():
     greedy = sorted(b for W, N, G, b in bench.BATCH_SWEEP if W == 0 and G == 0)
     assert greedy[0] == 1 and greedy[-1] == 128
     assert (15, 5, 15, 1) in bench.BATCH_SWEEP
+
+
+def test_attention_choice_of_the_benchmark():
+    """--attn auto takes the tcgen05 attention where the library allows it
+    (every step row within 31 positions of P, max_seq <= 4096): the 7B, 13B
+    and 34B settings and greedy, not a 31-column window."""
+    import bench
+    for wl in ("7b", "13b", "34b"):
+        W, N, G = bench.I.LOOKAHEAD[wl]
+        assert bench.attn_tc_applies(W, N, 2600)
+    assert bench.attn_tc_applies(0, 2, 800)
+    assert not bench.attn_tc_applies(31, 3, 800)      # rows up to 32 positions past P
+    assert not bench.attn_tc_applies(15, 5, 4097)
