@@ -109,11 +109,13 @@ def test_34b_width_one_layer_slice():
     assert np.array_equal(la, g)
 
 
+@pytest.mark.parametrize("attn", [0, 32], ids=["mma", "attntc"])
 @pytest.mark.parametrize("workload,max_seq", [("7b", 768), ("13b", 1024 + 256), ("34b", 2048 + 256)])
-def test_full_depth_controller_replay(workload, max_seq):
+def test_full_depth_controller_replay(workload, max_seq, attn):
     """The full-depth models the benchmark times (7B: 32 layers; 13B: 40
     layers, 1024-token prompt; 34B: 48 layers, 8 KV heads, prompt-seeded
-    pool, 2048-token prompt)."""
+    pool, 2048-token prompt), with either attention kernel (the benchmark
+    runs the tcgen05 pair)."""
     import oracle as O
     import lossless_lookahead_decoding_gb300 as LA
     cfg = I.MODELS[workload]
@@ -121,7 +123,7 @@ def test_full_depth_controller_replay(workload, max_seq):
     prompt = I.make_prompt(workload)
     W, N, G = I.LOOKAHEAD[workload]
     preseed = workload == "34b"
-    flags = LA.LA_PRESEED_PROMPT if preseed else 0
+    flags = (LA.LA_PRESEED_PROMPT if preseed else 0) | attn
     dec = LA.Decoder(cfg, dw, LA.LA_BF16, W, N, G, max_seq, flags=flags)
     ctrl = O.Controller(W, N, G, cfg.vocab)
     ctrl.init(prompt, seed=2, preseed=preseed)
@@ -146,7 +148,7 @@ def test_full_depth_controller_replay(workload, max_seq):
         P += len(emit)
         c = int(emit[-1])
     dec.close()
-    greedy = LA.Decoder(cfg, dw, LA.LA_BF16, 0, 2, 0, max_seq)
+    greedy = LA.Decoder(cfg, dw, LA.LA_BF16, 0, 2, 0, max_seq, flags=attn)
     g = greedy.generate(prompt, len(out))
     greedy.close()
     assert np.array_equal(np.array(out, np.int32), g)
