@@ -551,30 +551,37 @@ def run_micro(args, rank, world):
     # 32-layer 7B-width model (each layer's 33.6 MB of KV is evicted by the
     # other layers' weights: cold) and a 1-layer slice of it (KV stays in L2:
     # warm); synthetic Zipf prompt, random-init weights
+    # (the mma.sync kernel + split merge, and the tcgen05 pair, LA_ATTN_TC)
     kern = {}
     for name, layers in (("cold", 0), ("warm", 1)):
         cfg = I.MODELS["7b"] if not layers else I.MODELS["7b"].sliced(layers)
         dw = build_model(cfg, LA.LA_BF16)
         prompt = I.zipf_tokens(P + 1, cfg.vocab, 1.1, 21)
-        dec = LA.Decoder(cfg, dw, LA.LA_BF16, W, N, G, P + 1 + 64, flags=LA.LA_PROFILE | LA.LA_NO_GRAPH)
-        dec.prefill(prompt)
-        dec.step()
-        p0 = dec.profile()["attention"]  # cumulative since creation: prefill blocks included
-        for _ in range(8):
+        for suffix, extra in (("", 0), ("_tc", LA.LA_ATTN_TC)):
+            dec = LA.Decoder(cfg, dw, LA.LA_BF16, W, N, G, P + 1 + 64,
+                             flags=LA.LA_PROFILE | LA.LA_NO_GRAPH | extra)
+            dec.prefill(prompt)
             dec.step()
-        p1 = dec.profile()["attention"]
-        kern[name] = 1e3 * (p1["total_ms"] - p0["total_ms"]) / (p1["launches"] - p0["launches"])
-        dec.close()
+            p0 = dec.profile()["attention"]  # cumulative since creation: prefill blocks included
+            for _ in range(8):
+                dec.step()
+            p1 = dec.profile()["attention"]
+            kern[name + suffix] = 1e3 * (p1["total_ms"] - p0["total_ms"]) / (p1["launches"] - p0["launches"])
+            dec.close()
         del dw
         torch.cuda.empty_cache()
     lines.append({"micro": "attention", "config": f"{H}x{hd} heads, {P} cached tokens, W{W} N{N} G{G} ({T} rows)",
                   "us_cold": round(kern["cold"], 2), "us_warm": round(kern["warm"], 2),
+                  "us_cold_tcgen05": round(kern["cold_tc"], 2), "us_warm_tcgen05": round(kern["warm_tc"], 2),
+                  "frac_cold_tcgen05": round(roof_us / kern["cold_tc"], 4),
                   "algorithmic_bytes": by, "roofline_us": round(roof_us, 2), "peak_gbs": peaks["hbm_gbs"],
                   "frac_cold": round(roof_us / kern["cold"], 4),
                   "la_attention_call_us": round(float(np.median(op)), 1),
-                  "note": "us_cold/us_warm: attention + split merge per layer inside a decoder at P=2048 (the "
-                          "decode steps' P grows by the accepted tokens); la_attention_call_us: the standalone "
-                          "ABI op incl. its table uploads, scratch allocation and synchronisation"})
+                  "note": "us_cold/us_warm: the mma.sync attention + split merge per layer inside a decoder at "
+                          "P=2048 (the decode steps' P grows by the accepted tokens); *_tcgen05: the same for the "
+                          "tcgen05 + TMA pair (LA_ATTN_TC) that bench.py's step runs; la_attention_call_us: the "
+                          "standalone ABI op (mma.sync) incl. its table uploads, scratch allocation and "
+                          "synchronisation"})
     # ---- n-gram pool
     Np, Gp, V = 5, 15, 32000
     keys, grams = I.pool_bench_inserts(4096, 20, V, Np - 1)
