@@ -69,6 +69,24 @@ def test_lookahead_equals_gpu_greedy(mode, WNG):
         assert np.array_equal(g, O.greedy(O.Model(cfg, w), prompt, 64))
 
 
+@pytest.mark.parametrize("mode", ["fp32", "bf16"])
+@pytest.mark.parametrize("WNG", [(64, 2, 63), (42, 4, 0), (31, 3, 32)], ids=["T128", "T127-window", "T127"])
+def test_full_and_near_full_steps_equal_greedy(mode, WNG):
+    """Steps of 128 and 127 rows (the pass's limit): a 64-column window with
+    63 single-token candidates, a 42 x 3 window without verification, and 31
+    columns with 32 candidates; lossless against the same library's greedy
+    decode, and against the oracle's greedy output in fp32."""
+    dtype, mflags = MODES[mode]
+    cfg = I.MODELS["tiny"]
+    w = _weights(cfg, dtype == 1)
+    prompt = I.make_prompt("tiny")
+    g = gpu_decoder(cfg, w, dtype, 0, 2, 0, 320, flags=mflags).generate(prompt, 48)
+    t = gpu_decoder(cfg, w, dtype, *WNG, 320, flags=mflags).generate(prompt, 48)
+    assert np.array_equal(t, g)
+    if dtype == 0:
+        assert np.array_equal(g, O.greedy(O.Model(cfg, w), prompt, 48))
+
+
 def test_tiny_fp32_greedy_logits():
     import lossless_lookahead_decoding_gb300 as LA
     cfg = I.MODELS["tiny"]
