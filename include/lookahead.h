@@ -19,8 +19,9 @@
  *  - "host" pointers are caller-owned host memory; "device" pointers are
  *    caller-owned device memory that must stay valid until la_destroy.
  *  - Matrices are row-major [out][in] (PyTorch nn.Linear layout).
- *  - Compiled limits: rows per step T = 1 + (W+G)(N-1) <= 128, N <= 8,
- *    head_dim in {64, 128}, n_heads % n_kv_heads == 0, d_model % 64 == 0.
+ *  - Compiled limits: rows per step T = 1 + (W+G)(N-1) <= 128 (batched:
+ *    batch x T <= 128), N <= 8, head_dim in {64, 128},
+ *    n_heads % n_kv_heads == 0, d_model % 64 == 0.
  */
 #ifndef LOOKAHEAD_H
 #define LOOKAHEAD_H

@@ -12,6 +12,9 @@
 // LM head + argmax, verify + harvest + window shift, KV commit, and one
 // device-to-host copy of the emitted tokens.  All decode state lives on the
 // device, so the sequence is captured once into a CUDA graph and replayed.
+// A batched context runs B independent sequences through the same launches:
+// the forward pass over all B*T rows, the per-sequence kernels with the
+// sequence as a grid dimension, one strided copy of the B decode states.
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
