@@ -6,6 +6,8 @@ import socket
 import pytest
 
 import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 import la_inputs as I
 
 
@@ -99,3 +101,27 @@ def test_attention_choice_of_the_benchmark():
     assert bench.attn_tc_applies(0, 2, 800)
     assert not bench.attn_tc_applies(31, 3, 800)      # rows up to 32 positions past P
     assert not bench.attn_tc_applies(15, 5, 4097)
+
+
+def test_reference_arm_line_on_the_tiny_workload():
+    """bench.py --impl reference (the CPU oracle, no GPU) prints one JSON line
+    with the benchmark contract's keys: the oracle's own tokens/s on the
+    metric, a cpu_baseline describing the run and an e2e equal to the value
+    with no host-device copies."""
+    import json
+    import subprocess
+    import sys
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "tiny",
+                          "--steps", "3", "--warmup", "3"], capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["steps"] == 3 and d["warmup"] == 3 and d["value"] > 0
+    assert d["unit"] == "tokens/s" and d["higher_is_better"] is True
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
