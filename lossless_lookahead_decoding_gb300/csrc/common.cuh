@@ -127,6 +127,27 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
     return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 
+// launch_pdl with a preferred shared-memory carveout (percent of the unified
+// L1/shared array) for this launch; carveout < 0: the function's own setting.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl_carve(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                    int carveout, Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    at[1].id = cudaLaunchAttributePreferredSharedMemoryCarveout;
+    at[1].val.sharedMemCarveout = carveout < 0 ? 0u : (unsigned)carveout;
+    cfg.attrs = at;
+    cfg.numAttrs = carveout < 0 ? 1 : 2;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // ---- launchers (defined in the .cu files) ----
 struct Dims {
     int L, d, H, Hkv, hd, F, V, max_seq;

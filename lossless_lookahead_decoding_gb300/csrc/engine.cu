@@ -693,6 +693,12 @@ extern "C" int la_create_batch(const la_model_desc* desc, int W, int N, int G, i
                                                (long long)desc->n_layers * kRows, desc->n_heads, desc->n_kv_heads,
                                                desc->head_dim, desc->max_seq, tb.T, items);
             ctx->use_attn_tc = arc == LA_OK;
+            // the pair prefers the largest shared-memory carveout; the GEMMs, their
+            // epilogues and the residual norms then ask for it too, so that no SM
+            // of the layer chain has to be reconfigured between kernels (with the
+            // mma.sync attention the same setting was slower, so it is kept to
+            // this path)
+            if (ctx->use_attn_tc) ctx->tc.carveout = 100;
             if (arc == LA_ERR_ARG) {
                 ctx->err = "max_seq must be <= 4096 on the bf16 tensor-core path";
                 rc = LA_ERR_ARG;

@@ -883,7 +883,7 @@ void launch_gemm(const TcPlan& p, const GemmCfg& g, cudaStream_t s, int rows, in
     const Impl& im = *(const Impl*)p.impl;
     GemmArgs a{g.tiles, g.KB, g.ctas, rows, im.wpack + g.unit0 * kStageA, im.partial, im.err};
     if (p.prof) p.prof->begin(s);
-    launch_pdl(k_gemm_tc, dim3(g.ctas), dim3(kThreads), kSmemBytes, s, g.b, a);
+    launch_pdl_carve(k_gemm_tc, dim3(g.ctas), dim3(kThreads), kSmemBytes, s, p.carveout, g.b, a);
     if (p.prof) {
         // algorithmic: every weight once, the rows' inputs once, the rows' outputs once
         const double K = (double)g.KB * kBK, Nw = (double)g.tiles * kBM;
@@ -1054,9 +1054,9 @@ void tc_qkv_rope(const TcPlan& p, cudaStream_t s, int layer, int rows, const int
     e.VS = (__nv_bfloat16*)VS;
     launch_epi(p, s, [&] {
         if (rows <= 16)
-            launch_pdl(k_epi_qkv<8>, dim3(g.tiles, (rows + 15) / 16), dim3(128), 0, s, e);
+            launch_pdl_carve(k_epi_qkv<8>, dim3(g.tiles, (rows + 15) / 16), dim3(128), 0, s, p.carveout, e);
         else
-            launch_pdl(k_epi_qkv<11>, dim3(g.tiles, (rows + 21) / 22), dim3(128), 0, s, e);
+            launch_pdl_carve(k_epi_qkv<11>, dim3(g.tiles, (rows + 21) / 22), dim3(128), 0, s, p.carveout, e);
     });
 }
 
@@ -1082,11 +1082,11 @@ void tc_resid_rmsnorm(const TcPlan& p, cudaStream_t s, const TcResid& pend, floa
     ResidArgs a{pend.tiles, pend.KB, pend.ctas, pend.rows, pend.partial};
     if (p.prof) p.prof->begin(s);
     if (d <= 4 * kRnThreads)
-        launch_pdl(k_resid_rmsnorm, dim3(pend.rows), dim3(kRnThreads), 0, s, a, X, (const __nv_bfloat16*)w,
-                   (__nv_bfloat16*)XN, d, eps);
+        launch_pdl_carve(k_resid_rmsnorm, dim3(pend.rows), dim3(kRnThreads), 0, s, p.carveout, a, X,
+                         (const __nv_bfloat16*)w, (__nv_bfloat16*)XN, d, eps);
     else
-        launch_pdl(k_resid_rmsnorm_wide, dim3(pend.rows), dim3(kRnThreads), 0, s, a, X, (const __nv_bfloat16*)w,
-                   (__nv_bfloat16*)XN, d, eps);
+        launch_pdl_carve(k_resid_rmsnorm_wide, dim3(pend.rows), dim3(kRnThreads), 0, s, p.carveout, a, X,
+                         (const __nv_bfloat16*)w, (__nv_bfloat16*)XN, d, eps);
     if (p.prof) p.prof->end(s, P_NORM, 0, 0);
 }
 
@@ -1099,9 +1099,10 @@ void tc_gateup_swiglu(const TcPlan& p, cudaStream_t s, int layer, int rows)
     e.H = (__nv_bfloat16*)im.HID;
     launch_epi(p, s, [&] {
         if (rows <= 16)
-            launch_pdl(k_epi_swiglu<8, 2>, dim3(g.tiles / 2, (rows + 7) / 8), dim3(128), 0, s, e);
+            launch_pdl_carve(k_epi_swiglu<8, 2>, dim3(g.tiles / 2, (rows + 7) / 8), dim3(128), 0, s, p.carveout, e);
         else
-            launch_pdl(k_epi_swiglu<16, 1>, dim3(g.tiles / 2, (rows + 15) / 16), dim3(128), 0, s, e);
+            launch_pdl_carve(k_epi_swiglu<16, 1>, dim3(g.tiles / 2, (rows + 15) / 16), dim3(128), 0, s, p.carveout,
+                             e);
     });
 }
 
@@ -1114,8 +1115,8 @@ void tc_lmhead_argmax(const TcPlan& p, cudaStream_t s, int rows, float* logits, 
     e.logits = logits;
     e.amaxp = amaxp;
     launch_epi(p, s, [&] {
-        launch_pdl(k_gemm_epi<EPI_LOGITS>, epi_grid(g, rows), dim3(128), 0, s, e);
-        launch_pdl(k_argmax_unpack, dim3(1), dim3(kRows), 0, s, amaxp, amax, rows);
+        launch_pdl_carve(k_gemm_epi<EPI_LOGITS>, epi_grid(g, rows), dim3(128), 0, s, p.carveout, e);
+        launch_pdl_carve(k_argmax_unpack, dim3(1), dim3(kRows), 0, s, p.carveout, amaxp, amax, rows);
     });
 }
 

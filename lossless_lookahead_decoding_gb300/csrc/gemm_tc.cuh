@@ -13,6 +13,7 @@ struct TcPlan {
     bool ok = false;
     void* impl = nullptr;        // owned state (tensor maps, split-K scratch)
     Profiler* prof = nullptr;    // optional kernel timing
+    int carveout = -1;           // >= 0: preferred shared-memory carveout (%) of every launch
 };
 
 // 0 = plan made, 1 = shape not supported (caller falls back to SIMT), < 0 error.
