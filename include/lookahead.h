@@ -240,6 +240,18 @@ LA_API int la_prefill_seq(la_ctx* ctx, int seq, const int32_t* prompt, int len);
  * seed + b. */
 LA_API int la_step_batch(la_ctx* ctx, int32_t* out, int cap, int* n_out);
 
+/* Pages: "Summary" (output equal to greedy decoding) and "Key points" (main
+ * limitation: batches).
+ * Batched la_generate: prefill every sequence (prompts: HOST int32, the
+ * sequences' prompts back to back, lens: HOST int32[batch], each >= 1), then
+ * step the batch until every sequence has max_new tokens.  out: HOST
+ * int32[batch][max_new]; n_out: HOST int32[batch], each min(max_new,
+ * emitted).  A sequence that has its tokens keeps stepping with the others;
+ * its further tokens are dropped.  Errors as la_prefill_seq and
+ * la_step_batch (LA_ERR_CAPACITY when a sequence's cache fills first). */
+LA_API int la_generate_batch(la_ctx* ctx, const int32_t* prompts, const int* lens, int max_new, int32_t* out,
+                             int* n_out);
+
 /* Pages: "Key points" (steps taken against tokens emitted: the step count
  * the scaling law is about).  Counters since the last la_prefill (batched:
  * since sequence 0's; emitted and accept_hist count every sequence, steps

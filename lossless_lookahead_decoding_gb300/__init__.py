@@ -26,6 +26,7 @@ LA_PRESEED_PROMPT, LA_DEBUG_LOGITS, LA_NO_GRAPH, LA_SIMT, LA_PROFILE, LA_ATTN_TC
 
 EXPORTS = ("la_workspace_bytes", "la_create", "la_prefill", "la_step", "la_generate", "la_set_sampling", "la_get_stats",
            "la_get_profile", "la_workspace_bytes_batch", "la_create_batch", "la_prefill_seq", "la_step_batch",
+           "la_generate_batch",
            "la_debug_logits", "la_debug_argmax", "la_debug_rows", "la_debug_pool", "la_debug_window",
            "la_debug_set_argmax_override", "la_debug_select",
            "la_last_error", "la_destroy", "la_attention", "la_attention_noalloc", "la_pool_create", "la_pool_insert", "la_pool_lookup", "la_pool_size",
@@ -79,6 +80,7 @@ def lib():
             "la_create_batch": (i32, [vp, i32, i32, i32, i32, vp, sz, u64, i32, vp]),
             "la_prefill_seq": (i32, [vp, i32, vp, i32]),
             "la_step_batch": (i32, [vp, vp, i32, vp]),
+            "la_generate_batch": (i32, [vp, vp, vp, i32, vp, vp]),
             "la_debug_select": (i32, [vp, i32]),
             "la_set_sampling": (i32, [vp, C.c_float, u64]),
             "la_get_stats": (i32, [vp, vp]),
@@ -168,6 +170,18 @@ def la_step_batch(ctx, batch: int, N: int = 8) -> list:
     n = np.zeros(batch, np.int32)
     _check(ctx, lib().la_step_batch(ctx, _p(out), cap, _p(n)))
     return [out[b, : n[b]].copy() for b in range(batch)]
+
+
+def la_generate_batch(ctx, prompts, max_new: int) -> list:
+    """Prefill every sequence with its prompt and step until each has max_new
+    tokens: a list of token arrays, one per sequence."""
+    ps = [np.ascontiguousarray(p, dtype=np.int32) for p in prompts]
+    flat = np.ascontiguousarray(np.concatenate(ps), dtype=np.int32)
+    lens = np.array([len(p) for p in ps], np.int32)
+    out = np.zeros((len(ps), max(max_new, 1)), np.int32)
+    n = np.zeros(len(ps), np.int32)
+    _check(ctx, lib().la_generate_batch(ctx, _p(flat), _p(lens), max_new, _p(out), _p(n)))
+    return [out[b, : n[b]].copy() for b in range(len(ps))]
 
 
 def la_debug_select(ctx, seq: int) -> None:
@@ -366,6 +380,9 @@ class Decoder:
 
     def step_batch(self):
         return la_step_batch(self.ctx, self.batch, self.N)
+
+    def generate_batch(self, prompts, max_new: int):
+        return la_generate_batch(self.ctx, prompts, max_new)
 
     def select(self, seq: int):
         """Point the debug accessors at sequence seq."""

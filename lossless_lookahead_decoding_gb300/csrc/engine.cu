@@ -974,6 +974,42 @@ extern "C" int la_generate(la_ctx* ctx, const int32_t* prompt, int len, int max_
     return rc;
 }
 
+extern "C" int la_generate_batch(la_ctx* ctx, const int32_t* prompts, const int* lens, int max_new, int32_t* out,
+                                 int* n_out)
+{
+    if (!ctx) return LA_ERR_ARG;
+    if (!prompts || !lens || !n_out || max_new < 0 || (max_new > 0 && !out))
+        return fail(ctx, LA_ERR_ARG, "bad prompt or output buffer");
+    const int B = ctx->B;
+    size_t off = 0;
+    for (int b = 0; b < B; b++) {
+        if (lens[b] < 1) return fail(ctx, LA_ERR_ARG, "prompt must hold at least one token");
+        const int rc = prefill_seq(ctx, b, prompts + off, lens[b]);
+        if (rc) return rc;
+        off += (size_t)lens[b];
+    }
+    for (int b = 0; b < B; b++) n_out[b] = 0;
+    std::vector<int32_t> buf((size_t)B * kMaxN);
+    std::vector<int> n(B);
+    int rc = LA_OK;
+    auto done = [&]() {
+        for (int b = 0; b < B; b++)
+            if (n_out[b] < max_new) return false;
+        return true;
+    };
+    // the batch steps every sequence together; a sequence that has its
+    // tokens keeps stepping with the others and its further tokens are dropped
+    while (!done()) {
+        rc = run_step(ctx);
+        if (rc) break;
+        for (int b = 0; b < B; b++) {
+            const DState& h = ctx->h_st[b];
+            for (int i = 0; i < h.n_emit && n_out[b] < max_new; i++) out[(size_t)b * max_new + n_out[b]++] = h.emit[i];
+        }
+    }
+    return rc;
+}
+
 extern "C" int la_get_profile(la_ctx* ctx, la_prof_entry* out, int cap, int* n_out)
 {
     static const char* names[P_NCLS] = {"gemm_qkv", "gemm_o",    "gemm_gateup", "gemm_down", "gemm_lmhead",

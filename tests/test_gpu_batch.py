@@ -247,3 +247,27 @@ def test_batch_fills_the_128_row_pass(WNG, B):
             assert np.array_equal(batched.logits().view(np.uint32), d.logits().view(np.uint32)), b
     for d in [batched] + list(singles.values()):
         d.close()
+
+
+@pytest.mark.parametrize("mode", ["fp32", "bf16"])
+def test_generate_batch_equals_batch1_generate(mode):
+    """la_generate_batch: every sequence's max_new tokens equal la_generate of
+    a batch-1 context on its prompt (bit for bit); a cache that fills first
+    returns LA_ERR_CAPACITY."""
+    import lossless_lookahead_decoding_gb300 as LA
+    dtype, mflags = MODES[mode]
+    cfg = I.MODELS["tiny"]
+    w = I.make_weights(cfg, 0, bf16=dtype == 1)
+    dw = LA.device_weights(cfg, w, dtype)
+    prompts = _prompts("tiny", 3, cut=7)
+    dec = LA.Decoder(cfg, dw, dtype, 4, 3, 4, 256, flags=mflags, batch=3)
+    got = dec.generate_batch(prompts, 40)
+    one = LA.Decoder(cfg, dw, dtype, 4, 3, 4, 256, flags=mflags)
+    for b, p in enumerate(prompts):
+        assert len(got[b]) == 40
+        assert np.array_equal(got[b], one.generate(p, 40)), b
+    assert dec.stats()["emitted"] >= 3 * 40
+    small = LA.Decoder(cfg, dw, dtype, 4, 3, 4, 64, flags=mflags, batch=3)
+    with pytest.raises(LA.LAError) as e:
+        small.generate_batch(prompts, 60)
+    assert e.value.code == LA.LA_ERR_CAPACITY
