@@ -438,8 +438,9 @@ BATCH_SWEEP = [(0, 2, 0, 1), (0, 2, 0, 2), (0, 2, 0, 4), (0, 2, 0, 8), (0, 2, 0,
 def run_batch_sweep(args, rank, world):
     """Batched decoding: per (W, N, G, batch), the step latency and the
     tokens/s of all sequences together (prompts of the workload's recipe,
-    seeds 1..batch), and whether sequence 0's tokens equal a batch-1 greedy
-    context's on the same prompt."""
+    seeds 1..batch), the same end to end through la_generate_batch (host
+    prompts in, prefill included, host tokens out), and whether sequence 0's
+    tokens equal a batch-1 greedy context's on the same prompt."""
     import torch
     import lossless_lookahead_decoding_gb300 as LA
     from lossless_lookahead_decoding_gb300 import build as B
@@ -472,6 +473,12 @@ def run_batch_sweep(args, rank, world):
                 tok += sum(len(t) for t in got)
             out0.extend(got[0].tolist())
         torch.cuda.synchronize()
+        # end to end through la_generate_batch: host prompts in (prefill
+        # included), host tokens out, n_steps tokens per sequence
+        t0 = time.perf_counter()
+        outs = dec.generate_batch(prompts[:bsz], n_steps)
+        torch.cuda.synchronize()
+        e2e_s = time.perf_counter() - t0
         dec.close()
         ms = [a.elapsed_time(b) for a, b in ev]
         T = 1 + (W + G) * (N - 1)
@@ -480,6 +487,7 @@ def run_batch_sweep(args, rank, world):
                       "tokens_per_step": round(tok / args.steps, 4),
                       "tokens_per_s": round(tok / (sum(ms) / 1e3), 2),
                       "tokens_per_s_per_sequence": round(tok / bsz / (sum(ms) / 1e3), 2),
+                      "e2e_tokens_per_s": round(sum(len(o) for o in outs) / e2e_s, 2),
                       "seq0_equals_batch1_greedy": bool(np.array_equal(np.array(out0[:len(want)], np.int32),
                                                                        want[:len(out0)])),
                       "steps": args.steps, "warmup": args.warmup, "data": "synthetic prompts, random-init weights"})
