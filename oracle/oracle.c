@@ -55,6 +55,10 @@
  *     token is then distributed exactly as p of its row (the acceptance
  *     probabilities telescope), so the emitted sequence has the distribution
  *     of plain ancestral sampling.  The lookahead branch keeps using argmaxes.
+ *     Top-k (optional, another of the sampling schemes the summary says are
+ *     supported): p is first restricted to the top_k tokens by weight (ties
+ *     to the lower index) and renormalised; the rule is unchanged, so each
+ *     emitted token then follows the restricted p (keep_top_k).
  *
  * Model (M1-M3): h = x + Wo*Attn(RMSNorm(x)); y = h + Wd*(silu(Wg n) . Wu n),
  * n = RMSNorm(h); RMSNorm(x) = x / sqrt(mean(x^2) + eps) * w (Zhang and
@@ -703,16 +707,39 @@ OM_EXPORT uint64_t om_sample_weight(float z, float mx, float tau, int V)
     return (uint64_t)ldexpf(e, sample_bits(V));
 }
 
-static uint64_t weights_tau(const float* z, int V, float tau, uint64_t* E)
+/* Top-k restriction (top_k in 1..V-1; 0 or >= V keeps every token): the
+ * distribution is renormalised over the top_k tokens by weight, ties to the
+ * lower token index, i.e. the top_k largest keys E(v) V + (V - 1 - v) (all
+ * distinct, < 2^63 since E(v) <= 2^B); the others get weight 0. */
+static int cmp_desc_u64(const void* a, const void* b)
+{
+    const uint64_t x = *(const uint64_t*)a, y = *(const uint64_t*)b;
+    return x < y ? 1 : (x > y ? -1 : 0);
+}
+
+OM_EXPORT uint64_t om_top_k_key(uint64_t E, int v, int V) { return E * (uint64_t)V + (uint64_t)(V - 1 - v); }
+
+static void keep_top_k(uint64_t* E, int V, int top_k)
+{
+    if (top_k <= 0 || top_k >= V) return;
+    uint64_t* key = (uint64_t*)malloc(sizeof(uint64_t) * V);
+    for (int v = 0; v < V; v++) key[v] = om_top_k_key(E[v], v, V);
+    qsort(key, (size_t)V, sizeof(uint64_t), cmp_desc_u64);
+    const uint64_t K = key[top_k - 1];  /* the top_k-th largest key */
+    for (int v = 0; v < V; v++)
+        if (om_top_k_key(E[v], v, V) < K) E[v] = 0;
+    free(key);
+}
+
+static uint64_t weights_tau(const float* z, int V, float tau, int top_k, uint64_t* E)
 {
     float mx = z[0];
     for (int v = 1; v < V; v++)
         if (z[v] > mx) mx = z[v];
+    for (int v = 0; v < V; v++) E[v] = om_sample_weight(z[v], mx, tau, V);
+    keep_top_k(E, V, top_k);
     uint64_t S = 0;
-    for (int v = 0; v < V; v++) {
-        E[v] = om_sample_weight(z[v], mx, tau, V);
-        S += E[v];
-    }
+    for (int v = 0; v < V; v++) S += E[v];
     return S;
 }
 
@@ -747,12 +774,12 @@ static int draw_excluding(const uint64_t* E, int V, uint64_t S, const int* excl,
     return last >= 0 ? last : 0;
 }
 
-/* n plain draws from softmax(z / tau) (the primitive every sampled token
- * goes through). */
-OM_EXPORT void om_sample_logits(const float* z, int V, float tau, uint64_t* rng, int n, int* out)
+/* n plain draws from softmax(z / tau), restricted to the top_k tokens when
+ * top_k is in 1..V-1 (the primitive every sampled token goes through). */
+OM_EXPORT void om_sample_logits(const float* z, int V, float tau, int top_k, uint64_t* rng, int n, int* out)
 {
     uint64_t* E = (uint64_t*)malloc(sizeof(uint64_t) * V);
-    const uint64_t S = weights_tau(z, V, tau, E);
+    const uint64_t S = weights_tau(z, V, tau, top_k, E);
     for (int i = 0; i < n; i++) out[i] = draw_excluding(E, V, S, NULL, 0, 0, uniform24(rng));
     free(E);
 }
@@ -764,8 +791,8 @@ OM_EXPORT void om_sample_logits(const float* z, int V, float tau, uint64_t* rng,
  * lookahead branch's harvest and shift use the rows' argmaxes as in R6/R7.
  * Writes the emitted tokens and the rows whose KV is committed; returns m+1.
  */
-OM_EXPORT int om_ctrl_advance_sample(om_ctrl* k, const float* logits, float tau, uint64_t* rng, int* emit,
-                                     int* rows, int* gstar)
+OM_EXPORT int om_ctrl_advance_sample(om_ctrl* k, const float* logits, float tau, int top_k, uint64_t* rng,
+                                     int* emit, int* rows, int* gstar)
 {
     const int V = k->V, n1 = k->N - 1, Gp = k->Gp;
     uint64_t* E = (uint64_t*)malloc(sizeof(uint64_t) * V);
@@ -777,7 +804,7 @@ OM_EXPORT int om_ctrl_advance_sample(om_ctrl* k, const float* logits, float tau,
     int row = 0, m = 0, g_best = -1, done = 0;
     rows[0] = 0;
     for (int i = 0; i < n1 && !done; i++) {
-        const uint64_t S = weights_tau(logits + (size_t)row * V, V, tau, E);
+        const uint64_t S = weights_tau(logits + (size_t)row * V, V, tau, top_k, E);
         int nrej = 0, acc_g = -1;
         uint64_t R = 0;
         for (int g = 0; g < Gp && acc_g < 0; g++) {
@@ -810,7 +837,7 @@ OM_EXPORT int om_ctrl_advance_sample(om_ctrl* k, const float* logits, float tau,
     for (int i = 0; i < m; i++) rows[i + 1] = row_vf(k, g_best, i);
     if (!done) {
         /* every level accepted: the bonus token from the last accepted row */
-        const uint64_t S = weights_tau(logits + (size_t)row * V, V, tau, E);
+        const uint64_t S = weights_tau(logits + (size_t)row * V, V, tau, top_k, E);
         emit[m] = draw_excluding(E, V, S, NULL, 0, 0, uniform24(rng));
     }
     if (gstar) *gstar = g_best;
@@ -872,7 +899,7 @@ OM_EXPORT int om_lookahead(const om_model* m, const int* prompt, int len, int W,
  * softmax(logits / tau) by om_sample_logits' rule, one uniform per token from
  * the splitmix64 stream seeded with rng_seed. */
 OM_EXPORT int om_sample_decode(const om_model* m, const int* prompt, int len, int max_new, int max_seq, float tau,
-                               uint64_t rng_seed, int* out)
+                               int top_k, uint64_t rng_seed, int* out)
 {
     if (len < 1 || max_new < 0 || len - 1 + max_new > max_seq || !(tau > 0.0f)) return -1;
     om_seq* s = om_seq_new(m, max_seq);
@@ -887,7 +914,7 @@ OM_EXPORT int om_sample_decode(const om_model* m, const int* prompt, int len, in
         if (rc) break;
         const int row0 = 0;
         rc = om_commit(s, P, 1, &row0);
-        om_sample_logits(z, m->vocab, tau, &rng, 1, &out[t]);
+        om_sample_logits(z, m->vocab, tau, top_k, &rng, 1, &out[t]);
         c = out[t];
         P++;
     }
@@ -900,8 +927,8 @@ OM_EXPORT int om_sample_decode(const om_model* m, const int* prompt, int len, in
  * verification drawing from softmax(logits / tau) with the splitmix64 stream
  * seeded with rng_seed. */
 OM_EXPORT int om_lookahead_sample(const om_model* m, const int* prompt, int len, int W, int N, int G, uint64_t seed,
-                                  int preseed, int variant, float tau, uint64_t rng_seed, int max_new, int max_seq,
-                                  int* out, int* steps_out, int* accept_hist)
+                                  int preseed, int variant, float tau, int top_k, uint64_t rng_seed, int max_new,
+                                  int max_seq, int* out, int* steps_out, int* accept_hist)
 {
     if (len < 1 || max_new < 0 || !(tau > 0.0f)) return -1;
     if (len - 1 + max_new + W + N > max_seq) return -1;
@@ -924,7 +951,7 @@ OM_EXPORT int om_lookahead_sample(const om_model* m, const int* prompt, int len,
         int T = om_ctrl_rows(k, c, P, tok, pos, vis);
         rc = om_step_forward(s, P, T, tok, pos, vis, logits, amax);
         if (rc) break;
-        int ne = om_ctrl_advance_sample(k, logits, tau, &rng, emit, rows, NULL);
+        int ne = om_ctrl_advance_sample(k, logits, tau, top_k, &rng, emit, rows, NULL);
         rc = om_commit(s, P, ne, rows);
         for (int i = 0; i < ne && n < max_new; i++) out[n++] = emit[i];
         if (accept_hist) accept_hist[ne]++;

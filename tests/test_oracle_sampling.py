@@ -13,6 +13,11 @@ here (see the oracle's header).  What fixes it, independently of the oracle:
 * structural facts of one verification step: a candidate value is emitted
   only by being accepted, and then the step continues to the next level;
 * tau -> 0 reduces sampled decoding and sampled lookahead to greedy decoding;
+* top-k (another sampling scheme the summary page says is supported): draws
+  stay inside the top-k tokens by weight (computed here from the per-token
+  weights, ties to the lower index), follow the softmax renormalised over
+  them, and the sampled lookahead with top-k matches top-k ancestral sampling
+  on the Markov model; top_k >= V is plain sampling, top_k = 1 deterministic;
 * the fp32 exponential the probabilities are built from is within 3 ulp of
   the library exponential over its whole range (2 ulp; measured 1.24), exact at 0 and at integer
   multiples of ln 2 where the polynomial sees t = 0, and flushes to 0 below
@@ -231,3 +236,96 @@ def test_integer_weights_are_the_softmax(V):
         x = np.abs((z.astype(np.float64) - mx) / tau)
         tol = 2 * (2 * x[big].max() + 4) * 2.0 ** -24
         assert np.abs(p[big] / ref[big] - 1).max() <= tol
+
+
+# ------------------------------------------------------------------ top-k
+
+def _top_k_set(z, tau, k):
+    """The top-k tokens by the integer weights (ties to the lower index),
+    computed here from the per-token weights, apart from the oracle's own
+    restriction."""
+    V = len(z)
+    mx = float(np.max(z))
+    E = [O.sample_weight(float(x), mx, tau, V) for x in z]
+    order = sorted(range(V), key=lambda v: (-E[v], v))
+    return set(order[:k]), E
+
+
+@pytest.mark.parametrize("k", [1, 2, 5, 7])
+def test_top_k_draws_follow_the_restricted_softmax(k):
+    """Draws with top_k = k only ever pick the k tokens of largest weight and
+    follow the softmax renormalised over them; k = 1 is deterministic."""
+    V, tau, n = 8, 0.9, 120_000
+    z = np.random.default_rng(7).normal(0, 1.3, V).astype(np.float32)
+    keep, E = _top_k_set(z, tau, k)
+    x = O.sample_logits(z, tau, O.Rng(13), n, top_k=k)
+    assert set(np.unique(x).tolist()) <= keep
+    p = np.zeros(V)
+    sm = _softmax(z, tau)
+    for v in keep:
+        p[v] = sm[v]
+    p /= p.sum()
+    freq = np.bincount(x, minlength=V) / n
+    assert _close(freq, p, n), (freq, p)
+    if k == 1:
+        assert len(np.unique(x)) == 1
+
+
+def test_top_k_of_the_whole_vocabulary_is_plain_sampling():
+    """top_k = 0, = V and > V draw exactly what plain sampling draws from the
+    same uniform stream; the key order puts equal weights lower index first."""
+    V = 9
+    z = np.random.default_rng(8).normal(0, 1.0, V).astype(np.float32)
+    ref = O.sample_logits(z, 1.3, O.Rng(21), 500)
+    for k in (0, V, V + 5):
+        assert np.array_equal(O.sample_logits(z, 1.3, O.Rng(21), 500, top_k=k), ref)
+    assert O.top_k_key(7, 2, 10) > O.top_k_key(7, 3, 10) > O.top_k_key(6, 0, 10)
+
+
+def test_top_k_ties_go_to_the_lower_index():
+    """Equal logits give equal weights; top_k keeps the lowest indices among
+    them."""
+    z = np.array([0.5, 1.0, 1.0, 1.0, -2.0], np.float32)
+    x = O.sample_logits(z, 1.0, O.Rng(5), 20_000, top_k=2)
+    assert set(np.unique(x).tolist()) == {1, 2}
+
+
+@pytest.mark.parametrize("W,N,G,k", [(2, 3, 3, 2), (0, 4, 2, 3)])
+def test_sampled_lookahead_with_top_k_matches_ancestral_top_k_sampling(W, N, G, k):
+    """As the Markov-model test above, with every row restricted to its top_k
+    tokens: the lookahead process's token sequences against the exact
+    probabilities of top-k ancestral sampling."""
+    V, K, tau = 5, 3, 1.0
+    Z = (np.random.default_rng(4).normal(0, 1.6, (V, V))).astype(np.float32)
+    P1 = np.zeros((V, V))
+    for a in range(V):
+        keep, _ = _top_k_set(Z[a], tau, k)
+        sm = _softmax(Z[a], tau)
+        for v in keep:
+            P1[a, v] = sm[v]
+        P1[a] /= P1[a].sum()
+    prompt = np.array([0, 1, 2, 1, 0, 3, 1, 2, 4, 1], np.int32)
+    c0 = int(prompt[-1])
+    ctrl = O.Controller(W, N, G, V)
+    ctrl.init(prompt, seed=5, preseed=True)
+    r = O.Rng(9)
+    n = 40_000
+    counts = np.zeros((V,) * K)
+    for _ in range(n):
+        c, P, out = c0, 9, []
+        while len(out) < K:
+            tok, pos, vis = ctrl.rows(c, P)
+            emit, rows, g = ctrl.advance_sample(Z[tok], tau, r, top_k=k)
+            out.extend(emit.tolist())
+            c, P = int(emit[-1]), P + len(emit)
+        counts[tuple(out[:K])] += 1
+    exact = np.zeros((V,) * K)
+    for seq in itertools.product(range(V), repeat=K):
+        pr, prev = 1.0, c0
+        for t in seq:
+            pr *= P1[prev, t]
+            prev = t
+        exact[seq] = pr
+    assert counts.ravel()[exact.ravel() == 0].sum() == 0  # nothing outside the top-k sets
+    freq = counts / n
+    assert _close(freq.ravel(), exact.ravel(), n)
