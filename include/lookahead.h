@@ -194,6 +194,19 @@ LA_API int la_step(la_ctx* ctx, int32_t* out, int cap, int* n_out);
  * written. */
 LA_API int la_set_sampling(la_ctx* ctx, float temperature, uint64_t seed);
 
+/* Pages: "Summary" (several sampling schemes are supported; the pages give
+ * none of them, so this restriction is this library's).
+ * Top-k for sampling verification: with top_k in 1..vocab-1, every row's
+ * distribution (the temperature softmax of la_set_sampling, as integer
+ * weights) is restricted to its top_k tokens by weight, equal weights lower
+ * token index first, and renormalised; the verification rule is unchanged,
+ * so each emitted token follows the restricted distribution of its row.
+ * 0 (the default) or >= vocab keeps every token; no effect under greedy
+ * verification.  Takes effect at the next step (the step is captured
+ * again).  Costs a radix select over each sampled row's vocabulary per step.
+ * LA_ERR_ARG for top_k < 0. */
+LA_API int la_set_top_k(la_ctx* ctx, int top_k);
+
 /* Pages: "Summary" (decoding that emits what plain greedy decoding emits,
  * several tokens per step).
  * la_prefill, then la_step until max_new tokens; out: HOST int32[max_new]

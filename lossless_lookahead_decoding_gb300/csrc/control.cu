@@ -334,6 +334,90 @@ __device__ __forceinline__ unsigned long long weight_of(float z, float mx, float
     return __float2ull_rz(ldexpf(e, B));
 }
 
+// Top-k order: token v of weight E ranks by the key E V + (V - 1 - v) (larger
+// weight first, equal weights lower index first; distinct, < 2^63).  The
+// top_k tokens are those whose key is at least the top_k-th largest key K
+// (K = 0 keeps every token).
+__device__ __forceinline__ unsigned long long top_key(unsigned long long E, int v, int V)
+{
+    return E * (unsigned long long)V + (unsigned long long)(V - 1 - v);
+}
+
+// The weight of token v in the restricted distribution.
+__device__ __forceinline__ unsigned long long kept_weight(float z, int v, float mx, float tau, int B, int V,
+                                                          unsigned long long K)
+{
+    const unsigned long long E = weight_of(z, mx, tau, B);
+    return top_key(E, v, V) >= K ? E : 0ull;
+}
+
+// The top_k-th largest key of a row (all threads of the block): a radix
+// select over the 64-bit keys, 8 bits per pass from the top; the keys are
+// distinct, so after the last pass the prefix is that key.  Most keys share
+// their high digits (most tokens have a tiny weight), so each warp counts
+// equal digits once (one shared-memory atomic per distinct digit), and warp
+// 0 finds the digit holding the wanted rank with a suffix scan over the 256
+// buckets (8 per lane).  blockDim.x is a multiple of 32.
+__device__ unsigned long long top_k_threshold(const float* __restrict__ z, int V, float mx, float tau, int B, int k)
+{
+    __shared__ unsigned int hist[256];
+    __shared__ unsigned long long s_prefix;
+    __shared__ unsigned int s_rank;
+    const int lane = threadIdx.x & 31, iters = (V + blockDim.x - 1) / blockDim.x;
+    unsigned long long prefix = 0, mask = 0;
+    if (threadIdx.x == 0) s_rank = (unsigned int)k;  // rank among the keys that match the prefix (1 = largest)
+    for (int shift = 56; shift >= 0; shift -= 8) {
+        for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+        __syncthreads();
+        for (int it = 0; it < iters; it++) {
+            const int v = it * blockDim.x + threadIdx.x;
+            unsigned int d = 0xffffffffu;  // no bucket
+            if (v < V) {
+                const unsigned long long key = top_key(weight_of(z[v], mx, tau, B), v, V);
+                if ((key & mask) == prefix) d = (unsigned int)(key >> shift) & 255u;
+            }
+            const unsigned int peers = __match_any_sync(0xffffffffu, d);
+            if (d != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&hist[d], (unsigned int)__popc(peers));
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            // lane l holds buckets 255-8l .. 248-8l (descending digit order)
+            unsigned int c[8], part = 0;
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                c[j] = hist[255 - 8 * lane - j];
+                part += c[j];
+            }
+            unsigned int incl = part;  // inclusive scan over lanes (higher digits first)
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const unsigned int rank = s_rank, before = incl - part;
+            // the first lane whose buckets reach the rank picks the digit
+            const unsigned int hit = __ballot_sync(0xffffffffu, incl >= rank);
+            if (lane == __ffs(hit) - 1) {
+                unsigned int cum = before;
+                int d = 255 - 8 * lane - 7;  // the lowest digit of this lane, if the scan runs through
+                for (int j = 0; j < 8; j++) {
+                    if (cum + c[j] >= rank) {
+                        d = 255 - 8 * lane - j;
+                        break;
+                    }
+                    cum += c[j];
+                }
+                s_rank = rank - cum;
+                s_prefix = prefix | ((unsigned long long)d << shift);
+            }
+        }
+        __syncthreads();
+        prefix = s_prefix;
+        mask |= 255ull << shift;
+        __syncthreads();
+    }
+    return prefix;
+}
+
 // a * b as 128 bits (hi, lo)
 struct U128 {
     unsigned long long hi, lo;
@@ -345,19 +429,21 @@ __device__ __forceinline__ bool lt128(U128 a, U128 b) { return a.hi < b.hi || (a
 // Uniform U: the top 24 bits of the next output (u = U / 2^24).
 __device__ __forceinline__ unsigned long long uniform_u24(unsigned long long* x) { return smix64(x) >> 40; }
 
-// Row max and total weight S (weight_of) for row 0 (block 0) and the
-// verification rows vbase.. (blocks 1..): the rows whose softmax sampling
-// verification reads.  stats[2r] = the max's float bits, stats[2r+1] = S.
+// Row max, top-k threshold key K and total kept weight S for row 0 (block 0)
+// and the verification rows vbase.. (blocks 1..): the rows whose softmax
+// sampling verification reads.  stats[3r] = the max's float bits,
+// stats[3r+1] = S, stats[3r+2] = K (0 without a top-k restriction).
 constexpr int kStatThreads = 256;
 
 __global__ void __launch_bounds__(kStatThreads) k_row_stats(const float* __restrict__ logits, int V, float tau,
-                                                           int vbase, int T, unsigned long long* __restrict__ stats)
+                                                           int vbase, int T, int top_k,
+                                                           unsigned long long* __restrict__ stats)
 {
     pdl_wait();
     pdl_trigger();
     // sequence blockIdx.y of a batch: its rows are T rows further on
     logits += (size_t)blockIdx.y * T * V;
-    stats += (size_t)blockIdx.y * T * 2;
+    stats += (size_t)blockIdx.y * T * 3;
     const int r = blockIdx.x == 0 ? 0 : vbase + blockIdx.x - 1;
     const float* z = logits + (size_t)r * V;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, B = sample_bits(V);
@@ -370,23 +456,26 @@ __global__ void __launch_bounds__(kStatThreads) k_row_stats(const float* __restr
     __syncthreads();
     mx = s_m[0];
     for (int w = 1; w < kStatThreads / 32; w++) mx = fmaxf(mx, s_m[w]);
+    const unsigned long long K = (top_k > 0 && top_k < V) ? top_k_threshold(z, V, mx, tau, B, top_k) : 0ull;
     unsigned long long sum = 0;
-    for (int v = threadIdx.x; v < V; v += kStatThreads) sum += weight_of(z[v], mx, tau, B);
+    for (int v = threadIdx.x; v < V; v += kStatThreads) sum += kept_weight(z[v], v, mx, tau, B, V, K);
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     if (lane == 0) s_s[warp] = sum;
     __syncthreads();
     if (threadIdx.x == 0) {
         unsigned long long t = 0;
         for (int w = 0; w < kStatThreads / 32; w++) t += s_s[w];
-        stats[2 * r] = __float_as_uint(mx);
-        stats[2 * r + 1] = t;
+        stats[3 * r] = __float_as_uint(mx);
+        stats[3 * r + 1] = t;
+        stats[3 * r + 2] = K;
     }
 }
 
 void launch_row_stats(cudaStream_t s, const float* logits, int V, float tau, int vbase, int T,
-                      unsigned long long* stats, int B)
+                      unsigned long long* stats, int B, int top_k)
 {
-    launch_pdl(k_row_stats, dim3(1 + T - vbase, B), dim3(kStatThreads), 0, s, logits, V, tau, vbase, T, stats);
+    launch_pdl(k_row_stats, dim3(1 + T - vbase, B), dim3(kStatThreads), 0, s, logits, V, tau, vbase, T, top_k,
+               stats);
 }
 
 // ------------------------------------------------- verify + harvest + shift ---
@@ -398,8 +487,8 @@ constexpr int kVerifyWarps = 32;  // window columns harvested at once (W <= kMax
 // whose running weight A has A 2^24 > U (S - R); the last admissible token of
 // nonzero weight if none.  Every thread of the block takes part (a
 // contiguous chunk of tokens each; chunk totals by a block scan, exact).
-__device__ int block_draw(const float* z, int V, float tau, float mx, unsigned long long S, const int* rej, int nrej,
-                          unsigned long long R, unsigned long long U)
+__device__ int block_draw(const float* z, int V, float tau, float mx, unsigned long long S, unsigned long long K,
+                          const int* rej, int nrej, unsigned long long R, unsigned long long U)
 {
     __shared__ unsigned long long s_part[kVerifyWarps];
     __shared__ int s_pick, s_last;
@@ -409,7 +498,7 @@ __device__ int block_draw(const float* z, int V, float tau, float mx, unsigned l
     auto weight = [&](int v) -> unsigned long long {
         for (int k = 0; k < nrej; k++)
             if (rej[k] == v) return 0ull;
-        return weight_of(z[v], mx, tau, B);
+        return kept_weight(z[v], v, mx, tau, B, V, K);
     };
     unsigned long long loc = 0;
     int last = -1;
@@ -481,8 +570,8 @@ __device__ void sample_verify(DState* st, const int* tok, const float* logits, i
         if (tid == 0) {
             const int row = s_row, B = sample_bits(V);
             const float* z = logits + (size_t)row * V;
-            const float mx = __uint_as_float((unsigned)stats[2 * row]);
-            const unsigned long long S = stats[2 * row + 1];
+            const float mx = __uint_as_float((unsigned)stats[3 * row]);
+            const unsigned long long S = stats[3 * row + 1], K = stats[3 * row + 2];
             int nrej = 0, acc = -1;
             unsigned long long R = 0;
             for (int g = 0; g < ncand && acc < 0; g++) {
@@ -491,7 +580,7 @@ __device__ void sample_verify(DState* st, const int* tok, const float* logits, i
                 bool seen = false;
                 for (int k = 0; k < nrej; k++) seen = seen || s_rej[k] == v;
                 if (seen) continue;  // a value already tried at this level
-                const unsigned long long U = uniform_u24(&s_rng), E = weight_of(z[v], mx, tau, B);
+                const unsigned long long U = uniform_u24(&s_rng), E = kept_weight(z[v], v, mx, tau, B, V, K);
                 if (lt128(mul128(U, S - R), shl24(E))) {  // u (1 - R/S) < E/S
                     acc = g;
                 } else {
@@ -507,8 +596,8 @@ __device__ void sample_verify(DState* st, const int* tok, const float* logits, i
         __syncthreads();
         if (s_acc < 0) {
             const int row = s_row;
-            const int v = block_draw(logits + (size_t)row * V, V, tau, __uint_as_float((unsigned)stats[2 * row]),
-                                     stats[2 * row + 1], s_rej, s_nrej, s_R, s_u);
+            const int v = block_draw(logits + (size_t)row * V, V, tau, __uint_as_float((unsigned)stats[3 * row]),
+                                     stats[3 * row + 1], stats[3 * row + 2], s_rej, s_nrej, s_R, s_u);
             if (tid == 0) {
                 s_emit[s_m] = v;
                 s_done = 1;
@@ -531,8 +620,8 @@ __device__ void sample_verify(DState* st, const int* tok, const float* logits, i
         if (tid == 0) s_u = uniform_u24(&s_rng);
         __syncthreads();
         const int row = s_row;
-        const int v = block_draw(logits + (size_t)row * V, V, tau, __uint_as_float((unsigned)stats[2 * row]),
-                                 stats[2 * row + 1], nullptr, 0, 0ull, s_u);
+        const int v = block_draw(logits + (size_t)row * V, V, tau, __uint_as_float((unsigned)stats[3 * row]),
+                                 stats[3 * row + 1], stats[3 * row + 2], nullptr, 0, 0ull, s_u);
         if (tid == 0) s_emit[s_m] = v;
         __syncthreads();
     }
@@ -588,7 +677,7 @@ __global__ void __launch_bounds__(kVerifyWarps * 32)
         tok += b * T;
         amax += b * T;
         logits += b * T * V;
-        stats += b * T * 2;
+        stats += b * T * 3;
     }
     if (ovr[0]) amax = ovr + 1;  // debug: the rows' argmaxes set from the host
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;

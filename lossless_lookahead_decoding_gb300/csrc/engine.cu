@@ -66,6 +66,7 @@ struct la_ctx {
     int dseq = 0;  // the sequence the debug accessors read
     uint64_t seed = 0;
     float tau = 0.f;              // > 0: sampling verification at this temperature
+    int top_k = 0;                // > 0: ... from the top_k tokens of each row only
     unsigned long long* SSTAT = nullptr;  // per-row softmax max (float bits) / integer weight total for sampling
     int* AOVR = nullptr;                  // debug argmax override: [0] on, [1..T] the rows' argmaxes
     cudaStream_t s = nullptr;
@@ -242,7 +243,7 @@ static Layout make_layout(const la_model_desc* d, int W, int N, int G, int B, in
     const size_t pa = attn_mma_partial_bytes(d->n_heads, d->head_dim, d->max_seq);
     const size_t pt = attn_tc_partial_bytes(d->n_heads, d->head_dim, d->max_seq);
     ly.add(pa > pt ? pa : pt);                           // L_ATTN_PART split partials
-    ly.add(kRows * 16);                                  // L_SSTAT sampling row statistics
+    ly.add(kRows * 24);                                  // L_SSTAT sampling row statistics (max, S, K)
     return ly;
 }
 
@@ -441,7 +442,7 @@ static void enqueue_step(la_ctx* c)
     run_forward(c, c->B * c->T, c->rs_step, true, 0, c->B);
     c->prof.begin(c->s);
     const int vbase = 1 + c->W * (c->N - 1);
-    if (c->tau > 0.f) launch_row_stats(c->s, c->LOGITS, c->d.vocab, c->tau, vbase, c->T, c->SSTAT, c->B);
+    if (c->tau > 0.f) launch_row_stats(c->s, c->LOGITS, c->d.vocab, c->tau, vbase, c->T, c->SSTAT, c->B, c->top_k);
     launch_verify_update(c->s, c->st, c->tok, c->AMAX, c->win, c->pool, c->W, c->N, c->G, c->LOGITS, c->d.vocab,
                          c->tau, c->SSTAT, (c->flags & LA_MASK_DIAG) != 0, c->AOVR, c->B, c->sb);
     launch_commit(c->s, c->st, false, 0, c->N, c->KS, c->VS, c->KC, c->VC, c->d.n_layers, c->d.n_kv_heads,
@@ -953,6 +954,20 @@ extern "C" int la_set_sampling(la_ctx* ctx, float temperature, uint64_t seed)
         cudaGraphDestroy(ctx->graph);
         ctx->graph = nullptr;
     }
+    return LA_OK;
+}
+
+extern "C" int la_set_top_k(la_ctx* ctx, int top_k)
+{
+    if (!ctx) return LA_ERR_ARG;
+    if (top_k < 0) return fail(ctx, LA_ERR_ARG, "top_k must be >= 0");
+    if (top_k != ctx->top_k && ctx->gexec) {  // the step's launches change: capture it again
+        cudaGraphExecDestroy(ctx->gexec);
+        ctx->gexec = nullptr;
+        cudaGraphDestroy(ctx->graph);
+        ctx->graph = nullptr;
+    }
+    ctx->top_k = top_k;
     return LA_OK;
 }
 

@@ -33,14 +33,19 @@ def _setup(dtype):
     return cfg, w, I.make_prompt("tiny"), I.LOOKAHEAD["tiny"]
 
 
-@pytest.mark.parametrize("dtype,flags", [(0, 0), (1, 0), (1, 64), (1, 32)],
-                         ids=["fp32", "bf16", "bf16-diagonal", "bf16-attntc"])
-def test_sampled_steps_replay_the_oracle_rule(dtype, flags):
+@pytest.mark.parametrize("dtype,flags,top_k,tau", [(0, 0, 0, 0.05), (1, 0, 0, 0.05), (1, 64, 0, 0.05),
+                                                   (1, 32, 0, 0.05), (0, 0, 5, 0.8), (1, 0, 40, 1.0),
+                                                   (1, 32, 2, 0.7), (1, 0, 1, 1.0), (1, 0, 1024, 0.05)],
+                         ids=["fp32", "bf16", "bf16-diagonal", "bf16-attntc", "fp32-top5", "bf16-top40",
+                              "bf16-attntc-top2", "bf16-top1", "bf16-topV"])
+def test_sampled_steps_replay_the_oracle_rule(dtype, flags, top_k, tau):
+    """(top_k > 0: each row restricted to its top_k tokens by weight, on both
+    sides; top_k = vocab keeps every token.)"""
     import lossless_lookahead_decoding_gb300 as LA
     cfg, w, prompt, (W, N, G) = _setup(dtype)
-    tau, seed = 0.05, 77
+    seed = 77
     dec = gpu_decoder(cfg, w, dtype, W, N, G, 256, flags=flags | LA.LA_DEBUG_LOGITS)
-    dec.set_sampling(tau, seed)
+    dec.set_sampling(tau, seed, top_k=top_k)
     ctrl = O.Controller(W, N, G, cfg.vocab, variant=O.DIAGONAL if flags & LA.LA_MASK_DIAG else 0)
     ctrl.init(prompt, seed=2)
     rng = O.Rng(seed)
@@ -53,7 +58,7 @@ def test_sampled_steps_replay_the_oracle_rule(dtype, flags):
         tok, pos, _ = ctrl.rows(c, P)
         T = len(tok)
         assert np.array_equal(tok_g[:T], tok) and np.array_equal(pos_g[:T], pos)
-        emit_o, _, _ = ctrl.advance_sample(dec.logits()[:T], tau, rng)
+        emit_o, _, _ = ctrl.advance_sample(dec.logits()[:T], tau, rng, top_k=top_k)
         assert np.array_equal(emit, emit_o), (emit, emit_o)
         assert np.array_equal(dec.window(), ctrl.window())
         for key in set(int(x) for x in tok):
@@ -61,7 +66,8 @@ def test_sampled_steps_replay_the_oracle_rule(dtype, flags):
         multi += len(emit) > 1
         P += len(emit)
         c = int(emit[-1])
-    assert multi > 0  # candidates were accepted under sampling
+    if tau <= 0.1 or top_k in (1, 2):
+        assert multi > 0  # candidates were accepted under sampling
 
 
 @pytest.mark.parametrize("dtype", [0, 1], ids=["fp32", "bf16"])
@@ -78,3 +84,20 @@ def test_temperature_to_zero_and_back_is_greedy(dtype):
     assert np.array_equal(dec.generate(prompt, 48), g)
     with pytest.raises(LA.LAError):
         dec.set_sampling(math.nan, 1)
+
+
+def test_top_k_one_emits_the_largest_weight_token():
+    """top_k = 1 leaves one token per row: the sampled decode is
+    deterministic, the same for any uniform stream, and equals the oracle's
+    top-1 ancestral decode."""
+    import lossless_lookahead_decoding_gb300 as LA
+    cfg, w, prompt, (W, N, G) = _setup(0)
+    a = gpu_decoder(cfg, w, 0, W, N, G, 256)
+    a.set_sampling(0.9, 1, top_k=1)
+    b = gpu_decoder(cfg, w, 0, W, N, G, 256)
+    b.set_sampling(0.9, 12345, top_k=1)
+    ta, tb = a.generate(prompt, 40), b.generate(prompt, 40)
+    assert np.array_equal(ta, tb)
+    assert np.array_equal(ta, O.sample_decode(O.Model(cfg, w), prompt, 40, 0.9, 3, top_k=1))
+    with pytest.raises(LA.LAError):
+        LA.la_set_top_k(a.ctx, -1)
