@@ -357,24 +357,35 @@ __device__ __forceinline__ unsigned long long kept_weight(float z, int v, float 
 // their high digits (most tokens have a tiny weight), so each warp counts
 // equal digits once (one shared-memory atomic per distinct digit), and warp
 // 0 finds the digit holding the wanted rank with a suffix scan over the 256
-// buckets (8 per lane).  blockDim.x is a multiple of 32.
+// buckets (8 per lane).  Once the keys still matching the prefix fit
+// kTopCap, the next pass also gathers them into shared memory and the passes
+// after it read only those.  blockDim.x is a multiple of 32.
+constexpr int kTopCap = 4096;
+
 __device__ unsigned long long top_k_threshold(const float* __restrict__ z, int V, float mx, float tau, int B, int k)
 {
     __shared__ unsigned int hist[256];
+    __shared__ unsigned long long s_keys[kTopCap];
     __shared__ unsigned long long s_prefix;
-    __shared__ unsigned int s_rank;
-    const int lane = threadIdx.x & 31, iters = (V + blockDim.x - 1) / blockDim.x;
+    __shared__ unsigned int s_rank, s_sel, s_n;
+    const int lane = threadIdx.x & 31;
     unsigned long long prefix = 0, mask = 0;
+    int mode = 0;  // 0: every token; 1: every token, gathering the matching keys; 2: the gathered keys
     if (threadIdx.x == 0) s_rank = (unsigned int)k;  // rank among the keys that match the prefix (1 = largest)
     for (int shift = 56; shift >= 0; shift -= 8) {
         for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+        if (threadIdx.x == 0 && mode == 1) s_n = 0;
         __syncthreads();
+        const int n = mode == 2 ? (int)s_n : V, iters = (n + blockDim.x - 1) / blockDim.x;
         for (int it = 0; it < iters; it++) {
-            const int v = it * blockDim.x + threadIdx.x;
+            const int i = it * blockDim.x + threadIdx.x;
             unsigned int d = 0xffffffffu;  // no bucket
-            if (v < V) {
-                const unsigned long long key = top_key(weight_of(z[v], mx, tau, B), v, V);
-                if ((key & mask) == prefix) d = (unsigned int)(key >> shift) & 255u;
+            if (i < n) {
+                const unsigned long long key = mode == 2 ? s_keys[i] : top_key(weight_of(z[i], mx, tau, B), i, V);
+                if ((key & mask) == prefix) {
+                    d = (unsigned int)(key >> shift) & 255u;
+                    if (mode == 1) s_keys[atomicAdd(&s_n, 1u)] = key;
+                }
             }
             const unsigned int peers = __match_any_sync(0xffffffffu, d);
             if (d != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&hist[d], (unsigned int)__popc(peers));
@@ -407,12 +418,14 @@ __device__ unsigned long long top_k_threshold(const float* __restrict__ z, int V
                     cum += c[j];
                 }
                 s_rank = rank - cum;
+                s_sel = hist[d];  // keys matching the extended prefix
                 s_prefix = prefix | ((unsigned long long)d << shift);
             }
         }
         __syncthreads();
         prefix = s_prefix;
         mask |= 255ull << shift;
+        mode = mode == 1 ? 2 : (mode == 0 && s_sel <= (unsigned int)kTopCap ? 1 : mode);
         __syncthreads();
     }
     return prefix;
