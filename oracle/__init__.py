@@ -90,12 +90,12 @@ def lib():
             "om_attention": (i32, [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]),
             "om_uniform": (f64, [vp]), "om_exp_neg": (f32, [f32]),
             "om_sample_weight": (C.c_uint64, [f32, f32, f32, i32]),
-            "om_sample_logits": (None, [vp, i32, f32, i32, vp, i32, vp]),
-            "om_ctrl_advance_sample": (i32, [vp, vp, f32, i32, vp, vp, vp, vp]),
-            "om_sample_decode": (i32, [vp, vp, i32, i32, i32, f32, i32, u64, vp]),
-            "om_top_k_key": (u64, [u64, i32, i32]),
-            "om_lookahead_sample": (i32, [vp, vp, i32, i32, i32, i32, u64, i32, i32, f32, i32, u64, i32, i32, vp, vp,
-                                          vp]),
+            "om_sample_logits": (None, [vp, i32, f32, i32, f32, vp, i32, vp]),
+            "om_ctrl_advance_sample": (i32, [vp, vp, f32, i32, f32, vp, vp, vp, vp]),
+            "om_sample_decode": (i32, [vp, vp, i32, i32, i32, f32, i32, f32, u64, vp]),
+            "om_top_k_key": (u64, [u64, i32, i32]), "om_top_p24": (C.c_uint32, [f32]),
+            "om_lookahead_sample": (i32, [vp, vp, i32, i32, i32, i32, u64, i32, i32, f32, i32, f32, u64, i32, i32, vp,
+                                          vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -221,20 +221,21 @@ def lookahead(model: Model, prompt, W: int, N: int, G: int, max_new: int, seed: 
 
 
 def sample_decode(model: Model, prompt, max_new: int, tau: float, rng_seed: int, max_seq: int | None = None,
-                  top_k: int = 0):
+                  top_k: int = 0, top_p: float = 1.0):
     """Plain ancestral sampling at temperature tau (top_k > 0: from the top_k
-    tokens by weight)."""
+    tokens by weight; top_p < 1: then from the smallest leading set of those
+    holding top_p of their weight)."""
     p = _i32(prompt)
     max_seq = max_seq or (len(p) + max_new + 8)
     out = np.zeros(max_new, np.int32)
-    if lib().om_sample_decode(model.ptr, _p(p), len(p), max_new, max_seq, tau, top_k, rng_seed, _p(out)):
+    if lib().om_sample_decode(model.ptr, _p(p), len(p), max_new, max_seq, tau, top_k, top_p, rng_seed, _p(out)):
         raise ValueError("om_sample_decode failed")
     return out
 
 
 def lookahead_sample(model: Model, prompt, W: int, N: int, G: int, max_new: int, tau: float, rng_seed: int,
                      seed: int = 2, preseed: bool = False, max_seq: int | None = None, variant: int = 0,
-                     top_k: int = 0):
+                     top_k: int = 0, top_p: float = 1.0):
     """Lookahead decoding with sampling verification; (tokens, steps, accept_hist)."""
     p = _i32(prompt)
     max_seq = max_seq or (len(p) + max_new + W + N + 8)
@@ -242,7 +243,7 @@ def lookahead_sample(model: Model, prompt, W: int, N: int, G: int, max_new: int,
     steps = np.zeros(1, np.int32)
     hist = np.zeros(N + 1, np.int32)
     rc = lib().om_lookahead_sample(model.ptr, _p(p), len(p), W, N, G, seed, int(preseed), variant, tau, top_k,
-                                   rng_seed, max_new, max_seq, _p(out), _p(steps), _p(hist))
+                                   top_p, rng_seed, max_new, max_seq, _p(out), _p(steps), _p(hist))
     if rc:
         raise ValueError("om_lookahead_sample failed")
     return out, int(steps[0]), hist
@@ -273,13 +274,20 @@ def sample_weight(z: float, mx: float, tau: float, V: int) -> int:
     return int(lib().om_sample_weight(float(z), float(mx), float(tau), int(V)))
 
 
-def sample_logits(z, tau: float, rng: Rng, n: int, top_k: int = 0):
+def sample_logits(z, tau: float, rng: Rng, n: int, top_k: int = 0, top_p: float = 1.0):
     """n draws from softmax(z / tau) (one uniform each); top_k > 0: from the
-    top_k tokens by weight, ties to the lower index."""
+    top_k tokens by weight, ties to the lower index; top_p < 1: then from the
+    smallest leading set of those, in the same order, holding at least top_p
+    of their weight."""
     z = np.ascontiguousarray(z, dtype=np.float32)
     out = np.zeros(n, np.int32)
-    lib().om_sample_logits(_p(z), len(z), tau, top_k, rng.ptr, n, _p(out))
+    lib().om_sample_logits(_p(z), len(z), tau, top_k, top_p, rng.ptr, n, _p(out))
     return out
+
+
+def top_p24(top_p: float) -> int:
+    """The top-p bound as floor(top_p 2^24) in 1..2^24 (2^24: no restriction)."""
+    return int(lib().om_top_p24(float(top_p)))
 
 
 def top_k_key(E: int, v: int, V: int) -> int:
@@ -330,15 +338,16 @@ class Controller:
         n = lib().om_ctrl_advance(self.h, _p(a), _p(emit), _p(rows), C.cast(g, C.c_void_p))
         return emit[:n].copy(), rows[:n].copy(), int(g[0])
 
-    def advance_sample(self, logits, tau: float, rng: Rng, top_k: int = 0):
+    def advance_sample(self, logits, tau: float, rng: Rng, top_k: int = 0, top_p: float = 1.0):
         """R10 verification by sampling from the rows' logits [T][V] (top_k >
-        0: each row restricted to its top_k tokens), then the R6/R7 harvest
+        0: each row restricted to its top_k tokens; top_p < 1: then to the
+        leading set holding top_p of their weight), then the R6/R7 harvest
         and shift with the rows' argmaxes."""
         lg = np.ascontiguousarray(logits, dtype=np.float32)
         emit = np.zeros(self.N + 1, np.int32)
         rows = np.zeros(self.N + 1, np.int32)
         g = (C.c_int * 1)()
-        n = lib().om_ctrl_advance_sample(self.h, _p(lg), tau, top_k, rng.ptr, _p(emit), _p(rows),
+        n = lib().om_ctrl_advance_sample(self.h, _p(lg), tau, top_k, top_p, rng.ptr, _p(emit), _p(rows),
                                          C.cast(g, C.c_void_p))
         return emit[:n].copy(), rows[:n].copy(), int(g[0])
 

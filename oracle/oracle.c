@@ -55,10 +55,12 @@
  *     token is then distributed exactly as p of its row (the acceptance
  *     probabilities telescope), so the emitted sequence has the distribution
  *     of plain ancestral sampling.  The lookahead branch keeps using argmaxes.
- *     Top-k (optional, another of the sampling schemes the summary says are
- *     supported): p is first restricted to the top_k tokens by weight (ties
- *     to the lower index) and renormalised; the rule is unchanged, so each
- *     emitted token then follows the restricted p (keep_top_k).
+ *     Top-k and top-p (optional; the summary says several sampling schemes
+ *     are supported): p is first restricted to the top_k tokens by weight
+ *     (ties to the lower index), then to the smallest leading set of those,
+ *     in the same order, holding at least top_p of their weight, and
+ *     renormalised; the rule is unchanged, so each emitted token then
+ *     follows the restricted p (keep_top_k, keep_top_p).
  *
  * Model (M1-M3): h = x + Wo*Attn(RMSNorm(x)); y = h + Wd*(silu(Wg n) . Wu n),
  * n = RMSNorm(h); RMSNorm(x) = x / sqrt(mean(x^2) + eps) * w (Zhang and
@@ -731,13 +733,59 @@ static void keep_top_k(uint64_t* E, int V, int top_k)
     free(key);
 }
 
-static uint64_t weights_tau(const float* z, int V, float tau, int top_k, uint64_t* E)
+/* Top-p (nucleus) restriction after top-k: p24 = floor(top_p 2^24) in
+ * 1..2^24 (2^24 keeps every token of nonzero weight).  In descending key
+ * order, the smallest leading set whose weight A has A 2^24 >= p24 S (S the
+ * total kept so far) is kept; the rest gets weight 0. */
+OM_EXPORT uint32_t om_top_p24(float top_p)
+{
+    if (!(top_p < 1.0f)) return 1u << 24;
+    const double x = (double)top_p * 16777216.0;
+    return x < 1.0 ? 1u : (uint32_t)x;
+}
+
+typedef struct {
+    uint64_t key;
+    int v;
+} keyed;
+
+static int cmp_keyed_desc(const void* a, const void* b)
+{
+    const uint64_t x = ((const keyed*)a)->key, y = ((const keyed*)b)->key;
+    return x < y ? 1 : (x > y ? -1 : 0);
+}
+
+static void keep_top_p(uint64_t* E, int V, uint32_t p24)
+{
+    if (p24 >= (1u << 24)) return;
+    uint64_t S = 0;
+    for (int v = 0; v < V; v++) S += E[v];
+    if (S == 0) return;
+    keyed* o = (keyed*)malloc(sizeof(keyed) * V);
+    for (int v = 0; v < V; v++) {
+        o[v].key = om_top_k_key(E[v], v, V);
+        o[v].v = v;
+    }
+    qsort(o, (size_t)V, sizeof(keyed), cmp_keyed_desc);
+    const unsigned __int128 target = (unsigned __int128)p24 * S;
+    uint64_t A = 0;
+    int i = 0;
+    for (; i < V; i++) {
+        A += E[o[i].v];
+        if (((unsigned __int128)A << 24) >= target) break;
+    }
+    for (int j = i + 1; j < V; j++) E[o[j].v] = 0;
+    free(o);
+}
+
+static uint64_t weights_tau(const float* z, int V, float tau, int top_k, uint32_t p24, uint64_t* E)
 {
     float mx = z[0];
     for (int v = 1; v < V; v++)
         if (z[v] > mx) mx = z[v];
     for (int v = 0; v < V; v++) E[v] = om_sample_weight(z[v], mx, tau, V);
     keep_top_k(E, V, top_k);
+    keep_top_p(E, V, p24);
     uint64_t S = 0;
     for (int v = 0; v < V; v++) S += E[v];
     return S;
@@ -776,10 +824,11 @@ static int draw_excluding(const uint64_t* E, int V, uint64_t S, const int* excl,
 
 /* n plain draws from softmax(z / tau), restricted to the top_k tokens when
  * top_k is in 1..V-1 (the primitive every sampled token goes through). */
-OM_EXPORT void om_sample_logits(const float* z, int V, float tau, int top_k, uint64_t* rng, int n, int* out)
+OM_EXPORT void om_sample_logits(const float* z, int V, float tau, int top_k, float top_p, uint64_t* rng, int n,
+                                int* out)
 {
     uint64_t* E = (uint64_t*)malloc(sizeof(uint64_t) * V);
-    const uint64_t S = weights_tau(z, V, tau, top_k, E);
+    const uint64_t S = weights_tau(z, V, tau, top_k, om_top_p24(top_p), E);
     for (int i = 0; i < n; i++) out[i] = draw_excluding(E, V, S, NULL, 0, 0, uniform24(rng));
     free(E);
 }
@@ -791,8 +840,8 @@ OM_EXPORT void om_sample_logits(const float* z, int V, float tau, int top_k, uin
  * lookahead branch's harvest and shift use the rows' argmaxes as in R6/R7.
  * Writes the emitted tokens and the rows whose KV is committed; returns m+1.
  */
-OM_EXPORT int om_ctrl_advance_sample(om_ctrl* k, const float* logits, float tau, int top_k, uint64_t* rng,
-                                     int* emit, int* rows, int* gstar)
+OM_EXPORT int om_ctrl_advance_sample(om_ctrl* k, const float* logits, float tau, int top_k, float top_p,
+                                     uint64_t* rng, int* emit, int* rows, int* gstar)
 {
     const int V = k->V, n1 = k->N - 1, Gp = k->Gp;
     uint64_t* E = (uint64_t*)malloc(sizeof(uint64_t) * V);
@@ -804,7 +853,7 @@ OM_EXPORT int om_ctrl_advance_sample(om_ctrl* k, const float* logits, float tau,
     int row = 0, m = 0, g_best = -1, done = 0;
     rows[0] = 0;
     for (int i = 0; i < n1 && !done; i++) {
-        const uint64_t S = weights_tau(logits + (size_t)row * V, V, tau, top_k, E);
+        const uint64_t S = weights_tau(logits + (size_t)row * V, V, tau, top_k, om_top_p24(top_p), E);
         int nrej = 0, acc_g = -1;
         uint64_t R = 0;
         for (int g = 0; g < Gp && acc_g < 0; g++) {
@@ -837,7 +886,7 @@ OM_EXPORT int om_ctrl_advance_sample(om_ctrl* k, const float* logits, float tau,
     for (int i = 0; i < m; i++) rows[i + 1] = row_vf(k, g_best, i);
     if (!done) {
         /* every level accepted: the bonus token from the last accepted row */
-        const uint64_t S = weights_tau(logits + (size_t)row * V, V, tau, top_k, E);
+        const uint64_t S = weights_tau(logits + (size_t)row * V, V, tau, top_k, om_top_p24(top_p), E);
         emit[m] = draw_excluding(E, V, S, NULL, 0, 0, uniform24(rng));
     }
     if (gstar) *gstar = g_best;
@@ -899,7 +948,7 @@ OM_EXPORT int om_lookahead(const om_model* m, const int* prompt, int len, int W,
  * softmax(logits / tau) by om_sample_logits' rule, one uniform per token from
  * the splitmix64 stream seeded with rng_seed. */
 OM_EXPORT int om_sample_decode(const om_model* m, const int* prompt, int len, int max_new, int max_seq, float tau,
-                               int top_k, uint64_t rng_seed, int* out)
+                               int top_k, float top_p, uint64_t rng_seed, int* out)
 {
     if (len < 1 || max_new < 0 || len - 1 + max_new > max_seq || !(tau > 0.0f)) return -1;
     om_seq* s = om_seq_new(m, max_seq);
@@ -914,7 +963,7 @@ OM_EXPORT int om_sample_decode(const om_model* m, const int* prompt, int len, in
         if (rc) break;
         const int row0 = 0;
         rc = om_commit(s, P, 1, &row0);
-        om_sample_logits(z, m->vocab, tau, top_k, &rng, 1, &out[t]);
+        om_sample_logits(z, m->vocab, tau, top_k, top_p, &rng, 1, &out[t]);
         c = out[t];
         P++;
     }
@@ -927,8 +976,8 @@ OM_EXPORT int om_sample_decode(const om_model* m, const int* prompt, int len, in
  * verification drawing from softmax(logits / tau) with the splitmix64 stream
  * seeded with rng_seed. */
 OM_EXPORT int om_lookahead_sample(const om_model* m, const int* prompt, int len, int W, int N, int G, uint64_t seed,
-                                  int preseed, int variant, float tau, int top_k, uint64_t rng_seed, int max_new,
-                                  int max_seq, int* out, int* steps_out, int* accept_hist)
+                                  int preseed, int variant, float tau, int top_k, float top_p, uint64_t rng_seed,
+                                  int max_new, int max_seq, int* out, int* steps_out, int* accept_hist)
 {
     if (len < 1 || max_new < 0 || !(tau > 0.0f)) return -1;
     if (len - 1 + max_new + W + N > max_seq) return -1;
@@ -951,7 +1000,7 @@ OM_EXPORT int om_lookahead_sample(const om_model* m, const int* prompt, int len,
         int T = om_ctrl_rows(k, c, P, tok, pos, vis);
         rc = om_step_forward(s, P, T, tok, pos, vis, logits, amax);
         if (rc) break;
-        int ne = om_ctrl_advance_sample(k, logits, tau, top_k, &rng, emit, rows, NULL);
+        int ne = om_ctrl_advance_sample(k, logits, tau, top_k, top_p, &rng, emit, rows, NULL);
         rc = om_commit(s, P, ne, rows);
         for (int i = 0; i < ne && n < max_new; i++) out[n++] = emit[i];
         if (accept_hist) accept_hist[ne]++;

@@ -18,6 +18,13 @@ here (see the oracle's header).  What fixes it, independently of the oracle:
   weights, ties to the lower index), follow the softmax renormalised over
   them, and the sampled lookahead with top-k matches top-k ancestral sampling
   on the Markov model; top_k >= V is plain sampling, top_k = 1 deterministic;
+* top-p (nucleus sampling, Holtzman et al. 2020): on a distribution printed
+  here (0.5, 0.3, 0.15, 0.05) the kept sets for p = 0.45, 0.75, 0.9 are {0},
+  {0, 1}, {0, 1, 2}, and draws follow the renormalised probabilities; after
+  top_k = 2 the bound applies to the renormalised pair (0.625, 0.375); equal
+  weights are kept lower index first; top_p = 1 is plain sampling and a tiny
+  top_p is greedy; the sampled lookahead with top-p matches top-p ancestral
+  sampling on the Markov model;
 * the fp32 exponential the probabilities are built from is within 3 ulp of
   the library exponential over its whole range (2 ulp; measured 1.24), exact at 0 and at integer
   multiples of ln 2 where the polynomial sees t = 0, and flushes to 0 below
@@ -327,5 +334,119 @@ def test_sampled_lookahead_with_top_k_matches_ancestral_top_k_sampling(W, N, G, 
             prev = t
         exact[seq] = pr
     assert counts.ravel()[exact.ravel() == 0].sum() == 0  # nothing outside the top-k sets
+    freq = counts / n
+    assert _close(freq.ravel(), exact.ravel(), n)
+
+
+# ------------------------------------------------------------------ top-p
+
+_P4 = np.array([0.5, 0.3, 0.15, 0.05])
+
+
+def _draw_freq(z, tau, n, seed, **kw):
+    x = O.sample_logits(z, tau, O.Rng(seed), n, **kw)
+    return x, np.bincount(x, minlength=len(z)) / n
+
+
+@pytest.mark.parametrize("top_p,keep", [(0.45, [0]), (0.75, [0, 1]), (0.9, [0, 1, 2]), (0.99, [0, 1, 2, 3])])
+def test_top_p_keeps_the_nucleus_of_a_printed_distribution(top_p, keep):
+    """p = (0.5, 0.3, 0.15, 0.05) as logits log p at tau = 1: the smallest
+    leading set holding top_p of the mass, and draws from it renormalised."""
+    z = np.log(_P4).astype(np.float32)
+    n = 100_000
+    x, freq = _draw_freq(z, 1.0, n, 31, top_p=top_p)
+    assert sorted(np.unique(x).tolist()) == keep
+    q = np.zeros(4)
+    q[keep] = _P4[keep]
+    q /= q.sum()
+    assert _close(freq, q, n), (freq, q)
+
+
+@pytest.mark.parametrize("top_p,keep", [(0.6, [0]), (0.7, [0, 1]), (0.99, [0, 1])])
+def test_top_p_applies_to_the_top_k_renormalised(top_p, keep):
+    """top_k = 2 leaves (0.5, 0.3) renormalised to (0.625, 0.375): top_p 0.6
+    keeps token 0 alone, 0.7 both; token 2 never appears."""
+    z = np.log(_P4).astype(np.float32)
+    x, _ = _draw_freq(z, 1.0, 40_000, 32, top_k=2, top_p=top_p)
+    assert sorted(np.unique(x).tolist()) == keep
+
+
+def test_top_p_ties_go_to_the_lower_index():
+    """Equal logits: (1, 1, 1, 0) has weights w, w, w, w/e; half the mass
+    (1.68 w) needs two of the equal tokens, the lower two."""
+    z = np.array([1.0, 1.0, 1.0, 0.0], np.float32)
+    x, _ = _draw_freq(z, 1.0, 20_000, 33, top_p=0.5)
+    assert sorted(np.unique(x).tolist()) == [0, 1]
+
+
+def test_top_p_one_is_plain_sampling_and_tiny_top_p_is_greedy():
+    """top_p = 1 draws exactly what plain sampling draws from the same
+    stream; top_p -> 0 leaves the argmax alone (greedy decoding)."""
+    z = np.random.default_rng(12).normal(0, 1.0, 11).astype(np.float32)
+    ref = O.sample_logits(z, 0.8, O.Rng(41), 600)
+    assert np.array_equal(O.sample_logits(z, 0.8, O.Rng(41), 600, top_p=1.0), ref)
+    x = O.sample_logits(z, 0.8, O.Rng(41), 600, top_p=1e-6)
+    assert np.all(x == int(np.argmax(z)))
+    assert O.top_p24(1.0) == 1 << 24 and O.top_p24(0.5) == 1 << 23 and O.top_p24(1e-12) == 1
+    assert O.top_p24(0.9) == int(np.floor(np.float64(np.float32(0.9)) * 2.0**24))
+
+
+def test_top_p_mass_boundary_is_inclusive():
+    """Weights (w, w): top_p = 0.5 is reached exactly by the first token, so
+    only token 0 is kept; just above 0.5 both are."""
+    z = np.array([0.0, 0.0], np.float32)
+    x, _ = _draw_freq(z, 1.0, 4_000, 34, top_p=0.5)
+    assert np.all(x == 0)
+    x, _ = _draw_freq(z, 1.0, 4_000, 34, top_p=0.5 + 2.0**-20)
+    assert sorted(np.unique(x).tolist()) == [0, 1]
+
+
+@pytest.mark.parametrize("W,N,G,k,top_p", [(2, 3, 3, 0, 0.8), (0, 4, 2, 4, 0.7)])
+def test_sampled_lookahead_with_top_p_matches_ancestral_top_p_sampling(W, N, G, k, top_p):
+    """The Markov-model test with every row restricted by top-k (k > 0) and
+    then top-p: the lookahead process's token sequences against the exact
+    probabilities of that ancestral sampling, the kept sets computed here
+    from the probabilities in float64 (no kept set of this model has mass
+    within 1e-6 of the bound)."""
+    V, K, tau = 5, 3, 1.0
+    Z = (np.random.default_rng(4).normal(0, 1.6, (V, V))).astype(np.float32)
+    P1 = np.zeros((V, V))
+    for a in range(V):
+        sm = _softmax(Z[a], tau)
+        order = sorted(range(V), key=lambda v: (-sm[v], v))
+        if k:
+            order = order[:k]
+        tot = sum(sm[v] for v in order)
+        acc = 0.0
+        for v in order:
+            assert abs(acc / tot - top_p) > 1e-6
+            P1[a, v] = sm[v]
+            acc += sm[v]
+            if acc / tot >= top_p:
+                break
+        P1[a] /= P1[a].sum()
+    prompt = np.array([0, 1, 2, 1, 0, 3, 1, 2, 4, 1], np.int32)
+    c0 = int(prompt[-1])
+    ctrl = O.Controller(W, N, G, V)
+    ctrl.init(prompt, seed=5, preseed=True)
+    r = O.Rng(19)
+    n = 40_000
+    counts = np.zeros((V,) * K)
+    for _ in range(n):
+        c, P, out = c0, 9, []
+        while len(out) < K:
+            tok, pos, vis = ctrl.rows(c, P)
+            emit, rows, g = ctrl.advance_sample(Z[tok], tau, r, top_k=k, top_p=top_p)
+            out.extend(emit.tolist())
+            c, P = int(emit[-1]), P + len(emit)
+        counts[tuple(out[:K])] += 1
+    exact = np.zeros((V,) * K)
+    for seq in itertools.product(range(V), repeat=K):
+        pr, prev = 1.0, c0
+        for t in seq:
+            pr *= P1[prev, t]
+            prev = t
+        exact[seq] = pr
+    assert counts.ravel()[exact.ravel() == 0].sum() == 0  # nothing outside the kept sets
     freq = counts / n
     assert _close(freq.ravel(), exact.ravel(), n)
