@@ -78,6 +78,8 @@ def parse():
                          "instead of token for token")
     ap.add_argument("--top-k", type=int, default=0,
                     help="with --sample: restrict each row's distribution to its top-k tokens (0: all)")
+    ap.add_argument("--top-p", type=float, default=1.0,
+                    help="with --sample: then to the leading tokens holding this share of their weight (1: all)")
     ap.add_argument("--batch-sweep", action="store_true",
                     help="instead of the benchmark line: one JSON line per (W,N,G,batch) of batched decoding "
                          "(several sequences in one forward pass per step, batch x T <= 128 rows)")
@@ -268,7 +270,7 @@ def run_ours(args, rank, world):
     sample = getattr(args, "sample", 0.0)
     if sample > 0:
         for d in (la, gr):
-            d.set_sampling(sample, SAMPLE_SEED, top_k=getattr(args, "top_k", 0))
+            d.set_sampling(sample, SAMPLE_SEED, top_k=getattr(args, "top_k", 0), top_p=getattr(args, "top_p", 1.0))
     clocks = Clocks(local)
     clocks.start()
     tok, step_ms_l, wall, acc = timed_steps(la, prompt, gen, args.warmup, args.steps)
@@ -306,7 +308,8 @@ def run_ours(args, rank, world):
     # per-kernel-class timing (separate profiled pass: events around launches)
     prof_dec = LA.Decoder(cfg, dw, LA.LA_BF16, W, N, G, max_seq, flags=flags | LA.LA_PROFILE | LA.LA_NO_GRAPH)
     if sample > 0:
-        prof_dec.set_sampling(sample, SAMPLE_SEED, top_k=getattr(args, "top_k", 0))
+        prof_dec.set_sampling(sample, SAMPLE_SEED, top_k=getattr(args, "top_k", 0),
+                              top_p=getattr(args, "top_p", 1.0))
     prof_warm, prof_steps = 2, min(args.steps, 64)
     timed_steps(prof_dec, prompt, gen, prof_warm, prof_steps)
     prof = prof_dec.profile()
@@ -360,7 +363,8 @@ def run_ours(args, rank, world):
         # same library's greedy step time over the same prompt and steps
         "lookahead_premium_ms": round(step_ms - g_step_ms, 4),
         "lossless_vs_greedy": lossless, "full_generation_steps": full_steps,
-        "verification": ({"mode": "sampling", "temperature": sample, "top_k": getattr(args, "top_k", 0)}
+        "verification": ({"mode": "sampling", "temperature": sample, "top_k": getattr(args, "top_k", 0),
+                          "top_p": getattr(args, "top_p", 1.0)}
                          if sample > 0 else {"mode": "greedy"}),
         "step_roofline": {"t_roof_ms": round(t_roof * 1e3, 4), "frac": round(t_roof * 1e3 / step_ms, 4),
                           "bytes": sbytes, "flops": sflops, "P": P_mid, "peak_src": peaks["src"]},

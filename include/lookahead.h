@@ -207,6 +207,21 @@ LA_API int la_set_sampling(la_ctx* ctx, float temperature, uint64_t seed);
  * LA_ERR_ARG for top_k < 0. */
 LA_API int la_set_top_k(la_ctx* ctx, int top_k);
 
+/* Pages: "Summary" (several sampling schemes are supported; the pages give
+ * none of them, so this restriction is this library's).
+ * Top-p (nucleus) for sampling verification: after the top-k restriction,
+ * every row's distribution is restricted to the smallest leading set of its
+ * tokens, in the top-k order (larger weight first, equal weights lower token
+ * index first), whose weight A reaches A 2^24 >= floor(top_p 2^24) S (S the
+ * weight left by top-k), and renormalised; the verification rule is
+ * unchanged, so each emitted token follows the restricted distribution of
+ * its row.  1 (the default) keeps every token; no effect under greedy
+ * verification.  Takes effect at the next step (the step is captured
+ * again).  Costs a weighted radix select over each sampled row's
+ * vocabulary per step.  LA_ERR_ARG for a NULL context or top_p outside
+ * (0, 1] (NaN included). */
+LA_API int la_set_top_p(la_ctx* ctx, float top_p);
+
 /* Pages: "Summary" (decoding that emits what plain greedy decoding emits,
  * several tokens per step).
  * la_prefill, then la_step until max_new tokens; out: HOST int32[max_new]

@@ -25,7 +25,7 @@ LA_FP32, LA_BF16 = 0, 1
 LA_PRESEED_PROMPT, LA_DEBUG_LOGITS, LA_NO_GRAPH, LA_SIMT, LA_PROFILE, LA_ATTN_TC, LA_MASK_DIAG = 1, 2, 4, 8, 16, 32, 64
 
 EXPORTS = ("la_workspace_bytes", "la_create", "la_prefill", "la_step", "la_generate", "la_set_sampling", "la_get_stats",
-           "la_get_profile", "la_set_top_k", "la_workspace_bytes_batch", "la_create_batch", "la_prefill_seq", "la_step_batch",
+           "la_get_profile", "la_set_top_k", "la_set_top_p", "la_workspace_bytes_batch", "la_create_batch", "la_prefill_seq", "la_step_batch",
            "la_generate_batch",
            "la_debug_logits", "la_debug_argmax", "la_debug_rows", "la_debug_pool", "la_debug_window",
            "la_debug_set_argmax_override", "la_debug_select",
@@ -83,7 +83,7 @@ def lib():
             "la_generate_batch": (i32, [vp, vp, vp, i32, vp, vp]),
             "la_debug_select": (i32, [vp, i32]),
             "la_set_sampling": (i32, [vp, C.c_float, u64]),
-            "la_set_top_k": (i32, [vp, i32]),
+            "la_set_top_k": (i32, [vp, i32]), "la_set_top_p": (i32, [vp, C.c_float]),
             "la_get_stats": (i32, [vp, vp]),
             "la_get_profile": (i32, [vp, vp, i32, vp]),
             "la_debug_logits": (i32, [vp, vp, sz]),
@@ -195,6 +195,10 @@ def la_set_sampling(ctx, temperature: float, seed: int) -> None:
 
 def la_set_top_k(ctx, top_k: int) -> None:
     _check(ctx, lib().la_set_top_k(ctx, int(top_k)))
+
+
+def la_set_top_p(ctx, top_p: float) -> None:
+    _check(ctx, lib().la_set_top_p(ctx, float(top_p)))
 
 
 def la_generate(ctx, prompt, max_new: int) -> np.ndarray:
@@ -393,11 +397,13 @@ class Decoder:
         """Point the debug accessors at sequence seq."""
         la_debug_select(self.ctx, seq)
 
-    def set_sampling(self, temperature: float, seed: int, top_k: int = 0):
+    def set_sampling(self, temperature: float, seed: int, top_k: int = 0, top_p: float = 1.0):
         """Sampling verification at this temperature (<= 0: greedy), from each
-        row's top_k tokens when top_k > 0."""
+        row's top_k tokens when top_k > 0, then from the leading ones holding
+        top_p of their weight when top_p < 1."""
         la_set_sampling(self.ctx, temperature, seed)
         la_set_top_k(self.ctx, top_k)
+        la_set_top_p(self.ctx, top_p)
 
     def generate(self, prompt, max_new: int):
         return la_generate(self.ctx, prompt, max_new)

@@ -163,7 +163,7 @@ void launch_verify_update(cudaStream_t s, DState* st, const int* tok, const int*
                           PoolView pool, int W, int N, int G, const float* logits, int V, float tau,
                           const unsigned long long* stats, bool diag, const int* ovr, int B = 1, size_t sb = 0);
 void launch_row_stats(cudaStream_t s, const float* logits, int V, float tau, int vbase, int T,
-                      unsigned long long* stats, int B = 1, int top_k = 0);
+                      unsigned long long* stats, int B = 1, int top_k = 0, unsigned int p24 = 1u << 24);
 void launch_commit(cudaStream_t s, const DState* st, bool prefill, int n_prefill, int n_max, const void* KS,
                    const void* VS, void* KC, void* VC, int L, int Hkv, int hd, int max_seq, int esz, int B = 1,
                    int T = 0, size_t sb = 0);

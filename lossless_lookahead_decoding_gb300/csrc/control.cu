@@ -358,14 +358,15 @@ __device__ __forceinline__ unsigned long long kept_weight(float z, int v, float 
 // equal digits once (one shared-memory atomic per distinct digit), and warp
 // 0 finds the digit holding the wanted rank with a suffix scan over the 256
 // buckets (8 per lane).  Once the keys still matching the prefix fit
-// kTopCap, the next pass also gathers them into shared memory and the passes
-// after it read only those.  blockDim.x is a multiple of 32.
+// kTopCap, the next pass also gathers them into shared memory (s_keys, the
+// caller's) and the passes after it read only those.  blockDim.x is a
+// multiple of 32.
 constexpr int kTopCap = 4096;
 
-__device__ unsigned long long top_k_threshold(const float* __restrict__ z, int V, float mx, float tau, int B, int k)
+__device__ unsigned long long top_k_threshold(const float* __restrict__ z, int V, float mx, float tau, int B, int k,
+                                              unsigned long long* s_keys)
 {
     __shared__ unsigned int hist[256];
-    __shared__ unsigned long long s_keys[kTopCap];
     __shared__ unsigned long long s_prefix;
     __shared__ unsigned int s_rank, s_sel, s_n;
     const int lane = threadIdx.x & 31;
@@ -439,19 +440,145 @@ __device__ __forceinline__ U128 mul128(unsigned long long a, unsigned long long 
 __device__ __forceinline__ U128 shl24(unsigned long long a) { return {a >> 40, a << 24}; }
 __device__ __forceinline__ bool lt128(U128 a, U128 b) { return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo); }
 
+// Top-p bound after top-k (all threads of the block): among the tokens of
+// key >= Kk (total weight Sk), in descending key order, the key of the first
+// token whose running weight A reaches A 2^24 >= p24 Sk; *S_out = A.  The
+// restriction keeps the keys >= the result, which is >= Kk.  A radix select
+// like top_k_threshold's with each digit's weight in place of its count.
+// When the active lanes of a warp share one digit (the first pass: most
+// tokens have tiny weights), they add their weights with shuffles and one
+// lane adds the total; otherwise each lane adds its own.  The buckets are
+// 64-bit sums kept as two 32-bit words (the carry out of the low word goes
+// to the high one), as 32-bit shared-memory atomics are native and 64-bit
+// ones are not.  Only tokens of nonzero weight take part; the token found
+// has nonzero weight.  Each pass keeps A_above (the weight of the keys above
+// the prefix) with A_above 2^24 < p24 Sk <= (A_above + the prefix's weight)
+// 2^24, so a digit reaching the bound always exists.
+__device__ __forceinline__ void add_weight(unsigned int* lo, unsigned int* hi, unsigned long long w)
+{
+    const unsigned int l = (unsigned int)w, old = atomicAdd(lo, l);
+    atomicAdd(hi, (unsigned int)(w >> 32) + (old + l < old ? 1u : 0u));
+}
+
+__device__ unsigned long long top_p_threshold(const float* __restrict__ z, int V, float mx, float tau, int B,
+                                              unsigned long long Kk, unsigned long long Sk, unsigned int p24,
+                                              unsigned long long* s_keys, unsigned long long* S_out)
+{
+    __shared__ unsigned int hlo[256], hhi[256], hc[256];
+    __shared__ unsigned long long s_prefix, s_above, s_last;
+    __shared__ unsigned int s_sel, s_n;
+    const int lane = threadIdx.x & 31;
+    const U128 target = mul128(p24, Sk);
+    unsigned long long prefix = 0, mask = 0;
+    int mode = 0;  // as in top_k_threshold
+    if (threadIdx.x == 0) {
+        s_above = 0;
+        s_last = 0;
+    }
+    for (int shift = 56; shift >= 0; shift -= 8) {
+        for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+            hlo[i] = 0;
+            hhi[i] = 0;
+            hc[i] = 0;
+        }
+        if (threadIdx.x == 0 && mode == 1) s_n = 0;
+        __syncthreads();
+        const int n = mode == 2 ? (int)s_n : V, iters = (n + blockDim.x - 1) / blockDim.x;
+        for (int it = 0; it < iters; it++) {
+            const int i = it * blockDim.x + threadIdx.x;
+            unsigned int d = 0xffffffffu;  // no bucket
+            unsigned long long w = 0;
+            if (i < n) {
+                unsigned long long key;
+                if (mode == 2) {
+                    key = s_keys[i];
+                    w = key / (unsigned long long)V;
+                } else {
+                    w = weight_of(z[i], mx, tau, B);
+                    key = top_key(w, i, V);
+                }
+                if (w != 0 && key >= Kk && (key & mask) == prefix) {
+                    d = (unsigned int)(key >> shift) & 255u;
+                    if (mode == 1) s_keys[atomicAdd(&s_n, 1u)] = key;
+                } else {
+                    w = 0;
+                }
+            }
+            const unsigned int act = __ballot_sync(0xffffffffu, d != 0xffffffffu);
+            if (act) {
+                const unsigned int d0 = __shfl_sync(0xffffffffu, d, __ffs(act) - 1);
+                if (__all_sync(0xffffffffu, d == d0 || d == 0xffffffffu)) {
+                    unsigned long long t = w;  // the warp's total (< 2^63: part of one row's weight)
+                    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                    if (lane == 0) {
+                        add_weight(&hlo[d0], &hhi[d0], t);
+                        atomicAdd(&hc[d0], (unsigned int)__popc(act));
+                    }
+                } else if (d != 0xffffffffu) {
+                    add_weight(&hlo[d], &hhi[d], w);
+                    atomicAdd(&hc[d], 1u);
+                }
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            // lane l holds buckets 255-8l .. 248-8l (descending digit order)
+            unsigned long long c[8], part = 0;
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const int b = 255 - 8 * lane - j;
+                c[j] = ((unsigned long long)hhi[b] << 32) | hlo[b];
+                part += c[j];
+            }
+            unsigned long long incl = part;
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const unsigned long long above = s_above;
+            const unsigned int hit = __ballot_sync(0xffffffffu, !lt128(shl24(above + incl), target));
+            if (lane == (hit ? __ffs(hit) - 1 : 31)) {
+                unsigned long long cum = above + incl - part;
+                int d = 255 - 8 * lane - 7;
+                for (int j = 0; j < 8; j++) {
+                    if (!lt128(shl24(cum + c[j]), target)) {
+                        d = 255 - 8 * lane - j;
+                        break;
+                    }
+                    cum += c[j];
+                }
+                s_above = cum;
+                s_last = ((unsigned long long)hhi[d] << 32) | hlo[d];
+                s_sel = hc[d];
+                s_prefix = prefix | ((unsigned long long)d << shift);
+            }
+        }
+        __syncthreads();
+        prefix = s_prefix;
+        mask |= 255ull << shift;
+        mode = mode == 1 ? 2 : (mode == 0 && s_sel <= (unsigned int)kTopCap ? 1 : mode);
+        __syncthreads();
+    }
+    *S_out = s_above + s_last;
+    return prefix;
+}
+
 // Uniform U: the top 24 bits of the next output (u = U / 2^24).
 __device__ __forceinline__ unsigned long long uniform_u24(unsigned long long* x) { return smix64(x) >> 40; }
 
-// Row max, top-k threshold key K and total kept weight S for row 0 (block 0)
-// and the verification rows vbase.. (blocks 1..): the rows whose softmax
+// Row max, threshold key K and total kept weight S for row 0 (block 0) and
+// the verification rows vbase.. (blocks 1..): the rows whose softmax
 // sampling verification reads.  stats[3r] = the max's float bits,
-// stats[3r+1] = S, stats[3r+2] = K (0 without a top-k restriction).
-constexpr int kStatThreads = 256;
+// stats[3r+1] = S, stats[3r+2] = K (0 without a top-k or top-p restriction;
+// the kept tokens are those of key >= K).  p24 = floor(top_p 2^24), 2^24 for
+// no top-p restriction.
+constexpr int kStatThreads = 1024;  // one row per block: the selects' passes want every warp of an SM
 
 __global__ void __launch_bounds__(kStatThreads) k_row_stats(const float* __restrict__ logits, int V, float tau,
-                                                           int vbase, int T, int top_k,
+                                                           int vbase, int T, int top_k, unsigned int p24,
                                                            unsigned long long* __restrict__ stats)
 {
+    __shared__ unsigned long long s_keys[kTopCap];  // the radix selects' gathered keys
     pdl_wait();
     pdl_trigger();
     // sequence blockIdx.y of a batch: its rows are T rows further on
@@ -469,15 +596,16 @@ __global__ void __launch_bounds__(kStatThreads) k_row_stats(const float* __restr
     __syncthreads();
     mx = s_m[0];
     for (int w = 1; w < kStatThreads / 32; w++) mx = fmaxf(mx, s_m[w]);
-    const unsigned long long K = (top_k > 0 && top_k < V) ? top_k_threshold(z, V, mx, tau, B, top_k) : 0ull;
+    unsigned long long K = (top_k > 0 && top_k < V) ? top_k_threshold(z, V, mx, tau, B, top_k, s_keys) : 0ull;
     unsigned long long sum = 0;
     for (int v = threadIdx.x; v < V; v += kStatThreads) sum += kept_weight(z[v], v, mx, tau, B, V, K);
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     if (lane == 0) s_s[warp] = sum;
     __syncthreads();
+    unsigned long long t = 0;
+    for (int w = 0; w < kStatThreads / 32; w++) t += s_s[w];
+    if (p24 < (1u << 24)) K = top_p_threshold(z, V, mx, tau, B, K, t, p24, s_keys, &t);
     if (threadIdx.x == 0) {
-        unsigned long long t = 0;
-        for (int w = 0; w < kStatThreads / 32; w++) t += s_s[w];
         stats[3 * r] = __float_as_uint(mx);
         stats[3 * r + 1] = t;
         stats[3 * r + 2] = K;
@@ -485,10 +613,10 @@ __global__ void __launch_bounds__(kStatThreads) k_row_stats(const float* __restr
 }
 
 void launch_row_stats(cudaStream_t s, const float* logits, int V, float tau, int vbase, int T,
-                      unsigned long long* stats, int B, int top_k)
+                      unsigned long long* stats, int B, int top_k, unsigned int p24)
 {
     launch_pdl(k_row_stats, dim3(1 + T - vbase, B), dim3(kStatThreads), 0, s, logits, V, tau, vbase, T, top_k,
-               stats);
+               p24, stats);
 }
 
 // ------------------------------------------------- verify + harvest + shift ---

@@ -67,6 +67,7 @@ struct la_ctx {
     uint64_t seed = 0;
     float tau = 0.f;              // > 0: sampling verification at this temperature
     int top_k = 0;                // > 0: ... from the top_k tokens of each row only
+    unsigned int top_p24 = 1u << 24;  // < 2^24: ... then from the leading tokens holding top_p of their weight
     unsigned long long* SSTAT = nullptr;  // per-row softmax max (float bits) / integer weight total for sampling
     int* AOVR = nullptr;                  // debug argmax override: [0] on, [1..T] the rows' argmaxes
     cudaStream_t s = nullptr;
@@ -442,7 +443,8 @@ static void enqueue_step(la_ctx* c)
     run_forward(c, c->B * c->T, c->rs_step, true, 0, c->B);
     c->prof.begin(c->s);
     const int vbase = 1 + c->W * (c->N - 1);
-    if (c->tau > 0.f) launch_row_stats(c->s, c->LOGITS, c->d.vocab, c->tau, vbase, c->T, c->SSTAT, c->B, c->top_k);
+    if (c->tau > 0.f) launch_row_stats(c->s, c->LOGITS, c->d.vocab, c->tau, vbase, c->T, c->SSTAT, c->B, c->top_k,
+                                       c->top_p24);
     launch_verify_update(c->s, c->st, c->tok, c->AMAX, c->win, c->pool, c->W, c->N, c->G, c->LOGITS, c->d.vocab,
                          c->tau, c->SSTAT, (c->flags & LA_MASK_DIAG) != 0, c->AOVR, c->B, c->sb);
     launch_commit(c->s, c->st, false, 0, c->N, c->KS, c->VS, c->KC, c->VC, c->d.n_layers, c->d.n_kv_heads,
@@ -968,6 +970,23 @@ extern "C" int la_set_top_k(la_ctx* ctx, int top_k)
         ctx->graph = nullptr;
     }
     ctx->top_k = top_k;
+    return LA_OK;
+}
+
+extern "C" int la_set_top_p(la_ctx* ctx, float top_p)
+{
+    if (!ctx) return LA_ERR_ARG;
+    if (!(top_p > 0.f && top_p <= 1.f)) return fail(ctx, LA_ERR_ARG, "top_p must be in (0, 1]");
+    // floor(top_p 2^24), at least 1 (exact: a float times 2^24 in double)
+    const double x = (double)top_p * 16777216.0;
+    const unsigned int p24 = top_p >= 1.f ? 1u << 24 : (x < 1.0 ? 1u : (unsigned int)x);
+    if (p24 != ctx->top_p24 && ctx->gexec) {  // the step's launches change: capture it again
+        cudaGraphExecDestroy(ctx->gexec);
+        ctx->gexec = nullptr;
+        cudaGraphDestroy(ctx->graph);
+        ctx->graph = nullptr;
+    }
+    ctx->top_p24 = p24;
     return LA_OK;
 }
 

@@ -120,17 +120,18 @@ def test_batch_fp32_equals_oracle_greedy():
         assert np.array_equal(np.array(outs[b][:n], np.int32), O.greedy(om, p, n)), b
 
 
-def test_batch_sampling_streams():
+@pytest.mark.parametrize("top_k,top_p", [(0, 1.0), (20, 0.7)], ids=["plain", "top20-p0.7"])
+def test_batch_sampling_streams(top_k, top_p):
     """Sampling verification: sequence b of a batch draws what a batch-1
-    context seeded with seed + b draws."""
+    context seeded with seed + b draws (with and without top-k / top-p)."""
     import lossless_lookahead_decoding_gb300 as LA
     cfg = I.MODELS["tiny"]
     w = I.make_weights(cfg, 0, bf16=True)
     B = 3
     batched, singles = _pair(cfg, w, 1, (4, 3, 4), B, LA.LA_DEBUG_LOGITS, 256)
-    batched.set_sampling(0.9, 11)
+    batched.set_sampling(0.9, 11, top_k=top_k, top_p=top_p)
     for b, s in enumerate(singles):
-        s.set_sampling(0.9, 11 + b)
+        s.set_sampling(0.9, 11 + b, top_k=top_k, top_p=top_p)
     _run(batched, singles, _prompts("tiny", B, cut=3), 16)
 
 
