@@ -23,6 +23,13 @@
 // The split that holds the first tail chunk is run by kRep CTAs: each
 // repeats the split's shared chunks and then takes a share of the row
 // groups, so the per-group work is spread over more SMs.
+//
+// Batched decoding with at most 16 rows per sequence (greedy batches: one)
+// runs a narrow instance instead: a 16-row tile, 4 warps, no replicas and
+// 108 KB of shared memory, so that two CTAs share an SM.  There one warp
+// computes per CTA, so the SM's number of resident CTAs sets how many
+// (sequence, head, split) items progress at once; every row's arithmetic is
+// the wide instance's (the same chunks, instructions and order).
 #include <type_traits>
 
 #include "common.cuh"
@@ -207,39 +214,43 @@ struct AttnArgs {
 // Shared memory: the Q tile, kBufs chunk buffers (K then V of one chunk; up
 // to kBufs chunk loads in flight), the step rows' K and V, and the state
 // hand-off (o in buffers 1..2 once the cached chunks are done, m and l apart).
+// R: rows of the tile (kRows, or 16 for the narrow instance).
 constexpr int kBufs = 3;
+constexpr int kNarrowRows = 16, kNarrowWarps = 4;
 
-template <int HD>
+template <int HD, int R = kRows>
 struct AttnSmem {
     static constexpr int RB = HD * 2, PS = HD + 4;  // global partial state: o[HD], m, l, 2 pad
-    static constexpr int kQ = 0;                                  // Q tile [kRows][HD]
-    static constexpr int kBuf0 = kQ + kRows * RB;                 // chunk buffers
+    static constexpr int kQ = 0;                                  // Q tile [R][HD]
+    static constexpr int kBuf0 = kQ + R * RB;                     // chunk buffers
     static constexpr int kBufBytes = 2 * kChunk * RB;             // K [kChunk][HD] then V
-    static constexpr int kDumpO = kBuf0 + kBufBytes;              // o [kRows][HD] fp32 (buffers 1, 2)
-    static_assert(kRows * HD * 4 <= (kBufs - 1) * kBufBytes, "hand-off fits two chunk buffers");
-    static constexpr int kKS = kBuf0 + kBufs * kBufBytes;         // step K [kRows][HD]
-    static constexpr int kVS = kKS + kRows * RB;                  // step V
-    static constexpr int kML = kVS + kRows * RB;                  // m, l [kRows][2] fp32
-    static constexpr int kZero = kML + kRows * 8;                 // one zero row
+    static constexpr int kDumpO = kBuf0 + kBufBytes;              // o [R][HD] fp32 (buffers 1, 2)
+    static_assert(R * HD * 4 <= (kBufs - 1) * kBufBytes, "hand-off fits two chunk buffers");
+    static constexpr int kKS = kBuf0 + kBufs * kBufBytes;         // step K [R][HD]
+    static constexpr int kVS = kKS + R * RB;                      // step V
+    static constexpr int kML = kVS + R * RB;                      // m, l [R][2] fp32
+    static constexpr int kZero = kML + R * 8;                     // one zero row
     static constexpr int kInts = kZero + RB;                      // group bookkeeping
-    static constexpr int kBytes = kInts + (2 * kRows + 2) * 4;
+    static constexpr int kBytes = kInts + (2 * R + 2) * 4;
 };
 
 // kBatch: grid z is the sequence of a batched step (one sequence: z = 0 and
-// none of the per-sequence offsets is computed).
-template <int HD, bool kBatch>
-__global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
+// none of the per-sequence offsets is computed).  R rows per tile, W warps,
+// NR CTAs for the split with the first tail chunk (the wide instance: kRows,
+// kWarps, kRep; the narrow one: kNarrowRows, kNarrowWarps, 1).
+template <int HD, bool kBatch, int R = kRows, int W = kWarps, int NR = kRep>
+__global__ void __launch_bounds__(W * 32, R == kRows ? 1 : 2) k_attn_mma(AttnArgs a)
 {
     pdl_wait();
     pdl_trigger();
-    using L = AttnSmem<HD>;
+    using L = AttnSmem<HD, R>;
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int RB = HD * 2, NCH = HD / 8, PS = L::PS;
     const uint32_t sb = su32(smem);
     float* dump_o = (float*)(smem + L::kDumpO);
     float* dump_ml = (float*)(smem + L::kML);
-    int* gcnt = (int*)(smem + L::kInts);  // [kRows + 1] rows of each group (< a.rows)
-    int* gslab = gcnt + kRows + 1;        // [kRows + 1] slab prefix over groups
+    int* gcnt = (int*)(smem + L::kInts);  // [R + 1] rows of each group (< a.rows)
+    int* gslab = gcnt + R + 1;            // [R + 1] slab prefix over groups
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int dq = a.H * HD, dkv = a.Hkv * HD;
@@ -257,7 +268,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
     const int tail_split = (P / kChunk) * kChunk / kSplit;
     const int sp = blockIdx.y < a.nsplit ? blockIdx.y : tail_split;
     const int rep = blockIdx.y < a.nsplit ? 0 : blockIdx.y - a.nsplit + 1;
-    const int n_rep = sp == tail_split ? kRep : 1;
+    const int n_rep = sp == tail_split ? NR : 1;
     const int p0 = sp * kSplit;
     if (p0 > maxpos) return;
     const int c_begin = p0 / kChunk;
@@ -279,7 +290,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
     };
 
     // Q tile: virtual rows of the CTA's heads (beyond vrows zero)
-    for (int i = tid; i < kRows * NCH; i += blockDim.x) {
+    for (int i = tid; i < R * NCH; i += blockDim.x) {
         const int v = i / NCH, c = i % NCH;
         const bool ok = v < vrows;
         const int hl = ok ? v / a.rows : 0, r = ok ? v - hl * a.rows : 0;
@@ -297,7 +308,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
     auto buf = [&](int i) { return L::kBuf0 + (i % kBufs) * L::kBufBytes; };
     // group 0: Q, and the step rows' K/V of this KV head when the CTA has tail work
     if (has_tail) {
-        for (int i = tid; i < kRows * NCH; i += blockDim.x) {
+        for (int i = tid; i < R * NCH; i += blockDim.x) {
             const int r = i / NCH, c = i % NCH;
             const bool ok = r < a.rows;
             const size_t off = (row0 + (ok ? r : 0)) * dkv + kvh * HD + c * 8;
@@ -389,7 +400,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attn_mma(AttnArgs a)
     __syncthreads();
     const int n_group_items = gslab[ng], n_items = a.hpc * n_group_items;
     const int g4 = lane >> 2;
-    for (int it_all = rep * kWarps + warp; it_all < n_items; it_all += n_rep * kWarps) {
+    for (int it_all = rep * W + warp; it_all < n_items; it_all += n_rep * W) {
         // item = (head of the CTA, slab of a row group); rows r, virtual rows hl * rows + r
         const int hl = it_all / n_group_items, it = it_all - hl * n_group_items, vofs = hl * a.rows;
         int g = 0;
@@ -555,16 +566,15 @@ size_t attn_mma_partial_bytes(int H, int hd, int max_seq)
 
 bool attn_mma_init(int hd)
 {
+    auto set = [](auto kern, int bytes) {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
+    };
     if (hd == 128)
-        return cudaFuncSetAttribute(k_attn_mma<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    AttnSmem<128>::kBytes) == cudaSuccess &&
-               cudaFuncSetAttribute(k_attn_mma<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    AttnSmem<128>::kBytes) == cudaSuccess;
+        return set(k_attn_mma<128, false>, AttnSmem<128>::kBytes) && set(k_attn_mma<128, true>, AttnSmem<128>::kBytes) &&
+               set(k_attn_mma<128, true, kNarrowRows, kNarrowWarps, 1>, AttnSmem<128, kNarrowRows>::kBytes);
     if (hd == 64)
-        return cudaFuncSetAttribute(k_attn_mma<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    AttnSmem<64>::kBytes) == cudaSuccess &&
-               cudaFuncSetAttribute(k_attn_mma<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    AttnSmem<64>::kBytes) == cudaSuccess;
+        return set(k_attn_mma<64, false>, AttnSmem<64>::kBytes) && set(k_attn_mma<64, true>, AttnSmem<64>::kBytes) &&
+               set(k_attn_mma<64, true, kNarrowRows, kNarrowWarps, 1>, AttnSmem<64, kNarrowRows>::kBytes);
     return false;
 }
 
@@ -591,21 +601,30 @@ void launch_attn_mma(cudaStream_t s, const DState* st, RowSet rs, int max_rel, c
     a.nsplit = (max_seq + kSplit - 1) / kSplit;
     a.max_rel = max_rel;
     a.sl2 = 1.4426950408889634f / sqrtf((float)hd);
+    // the narrow instance: batches of at most 16 rows (and row groups) per sequence
+    const bool narrow = B > 1 && rows <= kNarrowRows && rs.ngrp <= kNarrowRows;
+    const int tile = narrow ? kNarrowRows : kRows;
     // query heads per CTA: the largest power of two dividing the GQA group
-    // whose stacked rows still fit the 128-row tile (1 without GQA)
+    // whose stacked rows still fit the tile (1 without GQA)
     const int group = H / Hkv;
     a.hpc = 1;
-    while (group % (2 * a.hpc) == 0 && 2 * a.hpc * rows <= kRows) a.hpc *= 2;
-    dim3 grid(H / a.hpc, a.nsplit + kRep - 1, B);
+    while (group % (2 * a.hpc) == 0 && 2 * a.hpc * rows <= tile) a.hpc *= 2;
+    dim3 grid(H / a.hpc, a.nsplit + (narrow ? 0 : kRep - 1), B);
     dim3 cgrid((rows * H + kCombWarps - 1) / kCombWarps, B);
-    auto go = [&](auto mma, auto comb, int smem) {
-        launch_pdl(mma, grid, dim3(kWarps * 32), smem, s, a);
+    auto go = [&](auto mma, auto comb, int smem, int warps) {
+        launch_pdl(mma, grid, dim3(warps * 32), smem, s, a);
         launch_pdl(comb, cgrid, dim3(kCombWarps * 32), 0, s, a);
     };
-    if (hd == 128 && B == 1) go(k_attn_mma<128, false>, k_attn_combine<128, false>, AttnSmem<128>::kBytes);
-    else if (hd == 128) go(k_attn_mma<128, true>, k_attn_combine<128, true>, AttnSmem<128>::kBytes);
-    else if (B == 1) go(k_attn_mma<64, false>, k_attn_combine<64, false>, AttnSmem<64>::kBytes);
-    else go(k_attn_mma<64, true>, k_attn_combine<64, true>, AttnSmem<64>::kBytes);
+    if (hd == 128 && narrow)
+        go(k_attn_mma<128, true, kNarrowRows, kNarrowWarps, 1>, k_attn_combine<128, true>,
+           AttnSmem<128, kNarrowRows>::kBytes, kNarrowWarps);
+    else if (hd == 128 && B == 1) go(k_attn_mma<128, false>, k_attn_combine<128, false>, AttnSmem<128>::kBytes, kWarps);
+    else if (hd == 128) go(k_attn_mma<128, true>, k_attn_combine<128, true>, AttnSmem<128>::kBytes, kWarps);
+    else if (narrow)
+        go(k_attn_mma<64, true, kNarrowRows, kNarrowWarps, 1>, k_attn_combine<64, true>,
+           AttnSmem<64, kNarrowRows>::kBytes, kNarrowWarps);
+    else if (B == 1) go(k_attn_mma<64, false>, k_attn_combine<64, false>, AttnSmem<64>::kBytes, kWarps);
+    else go(k_attn_mma<64, true>, k_attn_combine<64, true>, AttnSmem<64>::kBytes, kWarps);
 }
 
 }  // namespace la
