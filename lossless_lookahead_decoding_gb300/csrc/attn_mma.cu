@@ -25,11 +25,12 @@
 // groups, so the per-group work is spread over more SMs.
 //
 // Batched decoding with at most 16 rows per sequence (greedy batches: one)
-// runs a narrow instance instead: a 16-row tile, 4 warps, no replicas and
-// 108 KB of shared memory, so that two CTAs share an SM.  There one warp
-// computes per CTA, so the SM's number of resident CTAs sets how many
-// (sequence, head, split) items progress at once; every row's arithmetic is
-// the wide instance's (the same chunks, instructions and order).
+// runs a narrow instance instead: a 16-row tile, no replicas, 4 warps and
+// 108 KB of shared memory (two CTAs per SM), or for at most 8 rows 2 warps,
+// two chunk buffers, 8 step rows and 72 KB (three per SM).  There one warp computes per
+// CTA, so the SM's number of resident CTAs sets how many (sequence, head,
+// split) items progress at once; every row's arithmetic is the wide
+// instance's (the same chunks, instructions and order).
 #include <type_traits>
 
 #include "common.cuh"
@@ -214,21 +215,22 @@ struct AttnArgs {
 // Shared memory: the Q tile, kBufs chunk buffers (K then V of one chunk; up
 // to kBufs chunk loads in flight), the step rows' K and V, and the state
 // hand-off (o in buffers 1..2 once the cached chunks are done, m and l apart).
-// R: rows of the tile (kRows, or 16 for the narrow instance).
+// R: rows of the tile (kRows, or 16 for the narrow instances); NB chunk
+// buffers; RS step rows.
 constexpr int kBufs = 3;
-constexpr int kNarrowRows = 16, kNarrowWarps = 4;
+constexpr int kNarrowRows = 16, kNarrowWarps = 4, kNarrow8Warps = 2;
 
-template <int HD, int R = kRows>
+template <int HD, int R = kRows, int NB = kBufs, int RS = R>
 struct AttnSmem {
     static constexpr int RB = HD * 2, PS = HD + 4;  // global partial state: o[HD], m, l, 2 pad
     static constexpr int kQ = 0;                                  // Q tile [R][HD]
     static constexpr int kBuf0 = kQ + R * RB;                     // chunk buffers
     static constexpr int kBufBytes = 2 * kChunk * RB;             // K [kChunk][HD] then V
-    static constexpr int kDumpO = kBuf0 + kBufBytes;              // o [R][HD] fp32 (buffers 1, 2)
-    static_assert(R * HD * 4 <= (kBufs - 1) * kBufBytes, "hand-off fits two chunk buffers");
-    static constexpr int kKS = kBuf0 + kBufs * kBufBytes;         // step K [R][HD]
-    static constexpr int kVS = kKS + R * RB;                      // step V
-    static constexpr int kML = kVS + R * RB;                      // m, l [R][2] fp32
+    static constexpr int kDumpO = kBuf0 + kBufBytes;              // o [R][HD] fp32 (buffers 1..)
+    static_assert(R * HD * 4 <= (NB - 1) * kBufBytes, "hand-off fits the chunk buffers after the first");
+    static constexpr int kKS = kBuf0 + NB * kBufBytes;            // step K [RS][HD]
+    static constexpr int kVS = kKS + RS * RB;                     // step V
+    static constexpr int kML = kVS + RS * RB;                     // m, l [R][2] fp32
     static constexpr int kZero = kML + R * 8;                     // one zero row
     static constexpr int kInts = kZero + RB;                      // group bookkeeping
     static constexpr int kBytes = kInts + (2 * R + 2) * 4;
@@ -236,14 +238,15 @@ struct AttnSmem {
 
 // kBatch: grid z is the sequence of a batched step (one sequence: z = 0 and
 // none of the per-sequence offsets is computed).  R rows per tile, W warps,
-// NR CTAs for the split with the first tail chunk (the wide instance: kRows,
-// kWarps, kRep; the narrow one: kNarrowRows, kNarrowWarps, 1).
-template <int HD, bool kBatch, int R = kRows, int W = kWarps, int NR = kRep>
-__global__ void __launch_bounds__(W * 32, R == kRows ? 1 : 2) k_attn_mma(AttnArgs a)
+// NR CTAs for the split with the first tail chunk, NB chunk buffers, RS step
+// rows, MB CTAs per SM (the wide instance: kRows, kWarps, kRep, kBufs, kRows,
+// 1).
+template <int HD, bool kBatch, int R = kRows, int W = kWarps, int NR = kRep, int NB = kBufs, int RS = R, int MB = 1>
+__global__ void __launch_bounds__(W * 32, MB) k_attn_mma(AttnArgs a)
 {
     pdl_wait();
     pdl_trigger();
-    using L = AttnSmem<HD, R>;
+    using L = AttnSmem<HD, R, NB, RS>;
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int RB = HD * 2, NCH = HD / 8, PS = L::PS;
     const uint32_t sb = su32(smem);
@@ -305,10 +308,10 @@ __global__ void __launch_bounds__(W * 32, R == kRows ? 1 : 2) k_attn_mma(AttnArg
             cp_async16(swz<HD>(sb + vofs, r, c), vc + off, ok);
         }
     };
-    auto buf = [&](int i) { return L::kBuf0 + (i % kBufs) * L::kBufBytes; };
+    auto buf = [&](int i) { return L::kBuf0 + (i % NB) * L::kBufBytes; };
     // group 0: Q, and the step rows' K/V of this KV head when the CTA has tail work
     if (has_tail) {
-        for (int i = tid; i < R * NCH; i += blockDim.x) {
+        for (int i = tid; i < RS * NCH; i += blockDim.x) {
             const int r = i / NCH, c = i % NCH;
             const bool ok = r < a.rows;
             const size_t off = (row0 + (ok ? r : 0)) * dkv + kvh * HD + c * 8;
@@ -317,10 +320,10 @@ __global__ void __launch_bounds__(W * 32, R == kRows ? 1 : 2) k_attn_mma(AttnArg
         }
     }
     cp_commit();
-    // groups 1..kBufs: the first cached chunks (empty groups keep the count uniform)
+    // groups 1..NB: the first cached chunks (empty groups keep the count uniform)
     const int n_shared = c_shared_end - c_begin;
 #pragma unroll
-    for (int j = 0; j < kBufs; j++) {
+    for (int j = 0; j < NB; j++) {
         if (j < n_shared) load_chunk(c_begin + j, buf(j), buf(j) + kChunk * RB, P);
         cp_commit();
     }
@@ -333,7 +336,7 @@ __global__ void __launch_bounds__(W * 32, R == kRows ? 1 : 2) k_attn_mma(AttnArg
 
     uint32_t qf[HD / 16][4];
     for (int i = 0; i < n_shared; i++) {
-        cp_wait<kBufs - 1>();  // chunk i (and everything before it) has landed
+        cp_wait<NB - 1>();  // chunk i (and everything before it) has landed
         __syncthreads();
         if (warp * 16 < vrows) {  // slabs of padding rows only are skipped
             if (i == 0) {
@@ -354,7 +357,7 @@ __global__ void __launch_bounds__(W * 32, R == kRows ? 1 : 2) k_attn_mma(AttnArg
             chunk_update<HD, false>(qf, st, kr, [](int, int) { return true; }, a.sl2);
         }
         __syncthreads();  // buffer i is free again
-        if (i + kBufs < n_shared) load_chunk(c_begin + i + kBufs, buf(i), buf(i) + kChunk * RB, P);
+        if (i + NB < n_shared) load_chunk(c_begin + i + NB, buf(i), buf(i) + kChunk * RB, P);
         cp_commit();
     }
     // state after the shared chunks: final partial, or hand-off to the tail
@@ -569,12 +572,20 @@ bool attn_mma_init(int hd)
     auto set = [](auto kern, int bytes) {
         return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
     };
-    if (hd == 128)
-        return set(k_attn_mma<128, false>, AttnSmem<128>::kBytes) && set(k_attn_mma<128, true>, AttnSmem<128>::kBytes) &&
-               set(k_attn_mma<128, true, kNarrowRows, kNarrowWarps, 1>, AttnSmem<128, kNarrowRows>::kBytes);
-    if (hd == 64)
-        return set(k_attn_mma<64, false>, AttnSmem<64>::kBytes) && set(k_attn_mma<64, true>, AttnSmem<64>::kBytes) &&
-               set(k_attn_mma<64, true, kNarrowRows, kNarrowWarps, 1>, AttnSmem<64, kNarrowRows>::kBytes);
+    // the narrow instances also ask for the largest shared-memory carveout (two or three CTAs per SM)
+    auto set_narrow = [&](auto kern, int bytes) {
+        return set(kern, bytes) &&
+               cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess;
+    };
+    auto all = [&](auto hdc) {
+        constexpr int HD = decltype(hdc)::value;
+        return set(k_attn_mma<HD, false>, AttnSmem<HD>::kBytes) && set(k_attn_mma<HD, true>, AttnSmem<HD>::kBytes) &&
+               set_narrow(k_attn_mma<HD, true, kNarrowRows, kNarrowWarps, 1>, AttnSmem<HD, kNarrowRows>::kBytes) &&
+               set_narrow(k_attn_mma<HD, true, kNarrowRows, kNarrow8Warps, 1, 2, 8, 3>,
+                          AttnSmem<HD, kNarrowRows, 2, 8>::kBytes);
+    };
+    if (hd == 128) return all(std::integral_constant<int, 128>());
+    if (hd == 64) return all(std::integral_constant<int, 64>());
     return false;
 }
 
@@ -601,7 +612,7 @@ void launch_attn_mma(cudaStream_t s, const DState* st, RowSet rs, int max_rel, c
     a.nsplit = (max_seq + kSplit - 1) / kSplit;
     a.max_rel = max_rel;
     a.sl2 = 1.4426950408889634f / sqrtf((float)hd);
-    // the narrow instance: batches of at most 16 rows (and row groups) per sequence
+    // the narrow instances: batches of at most 16 rows, and 16 row groups, per sequence
     const bool narrow = B > 1 && rows <= kNarrowRows && rs.ngrp <= kNarrowRows;
     const int tile = narrow ? kNarrowRows : kRows;
     // query heads per CTA: the largest power of two dividing the GQA group
@@ -609,22 +620,34 @@ void launch_attn_mma(cudaStream_t s, const DState* st, RowSet rs, int max_rel, c
     const int group = H / Hkv;
     a.hpc = 1;
     while (group % (2 * a.hpc) == 0 && 2 * a.hpc * rows <= tile) a.hpc *= 2;
+    // the 2-warp instance (three CTAs per SM) for at most 8 rows once the CTAs
+    // of one split outnumber the SMs; below that each CTA's own latency
+    // counts and 4 warps load a chunk faster
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const bool narrow8 = narrow && rows <= 8 && B * (H / a.hpc) > sms;
     dim3 grid(H / a.hpc, a.nsplit + (narrow ? 0 : kRep - 1), B);
     dim3 cgrid((rows * H + kCombWarps - 1) / kCombWarps, B);
     auto go = [&](auto mma, auto comb, int smem, int warps) {
         launch_pdl(mma, grid, dim3(warps * 32), smem, s, a);
         launch_pdl(comb, cgrid, dim3(kCombWarps * 32), 0, s, a);
     };
-    if (hd == 128 && narrow)
-        go(k_attn_mma<128, true, kNarrowRows, kNarrowWarps, 1>, k_attn_combine<128, true>,
-           AttnSmem<128, kNarrowRows>::kBytes, kNarrowWarps);
-    else if (hd == 128 && B == 1) go(k_attn_mma<128, false>, k_attn_combine<128, false>, AttnSmem<128>::kBytes, kWarps);
-    else if (hd == 128) go(k_attn_mma<128, true>, k_attn_combine<128, true>, AttnSmem<128>::kBytes, kWarps);
-    else if (narrow)
-        go(k_attn_mma<64, true, kNarrowRows, kNarrowWarps, 1>, k_attn_combine<64, true>,
-           AttnSmem<64, kNarrowRows>::kBytes, kNarrowWarps);
-    else if (B == 1) go(k_attn_mma<64, false>, k_attn_combine<64, false>, AttnSmem<64>::kBytes, kWarps);
-    else go(k_attn_mma<64, true>, k_attn_combine<64, true>, AttnSmem<64>::kBytes, kWarps);
+    auto pick = [&](auto hdc) {
+        constexpr int HD = decltype(hdc)::value;
+        if (narrow8)
+            go(k_attn_mma<HD, true, kNarrowRows, kNarrow8Warps, 1, 2, 8, 3>, k_attn_combine<HD, true>,
+               AttnSmem<HD, kNarrowRows, 2, 8>::kBytes, kNarrow8Warps);
+        else if (narrow)
+            go(k_attn_mma<HD, true, kNarrowRows, kNarrowWarps, 1>, k_attn_combine<HD, true>,
+               AttnSmem<HD, kNarrowRows>::kBytes, kNarrowWarps);
+        else if (B == 1)
+            go(k_attn_mma<HD, false>, k_attn_combine<HD, false>, AttnSmem<HD>::kBytes, kWarps);
+        else
+            go(k_attn_mma<HD, true>, k_attn_combine<HD, true>, AttnSmem<HD>::kBytes, kWarps);
+    };
+    if (hd == 128) pick(std::integral_constant<int, 128>());
+    else pick(std::integral_constant<int, 64>());
 }
 
 }  // namespace la

@@ -76,8 +76,9 @@ def _run(batched, singles, prompts, steps, logits=True):
 
 @pytest.mark.parametrize("mode", list(MODES))
 @pytest.mark.parametrize("WNG,B", [((4, 3, 4), 3), ((0, 2, 0), 8), ((5, 4, 3), 4), ((0, 3, 3), 4), ((3, 3, 0), 2),
-                                   ((4, 3, 4), 7)],
-                         ids=["la-b3", "greedy-b8", "la-b4", "promptlookup-b4", "noverify-b2", "la-b7-full"])
+                                   ((4, 3, 4), 7), ((3, 3, 3), 3), ((0, 2, 0), 40)],
+                         ids=["la-b3", "greedy-b8", "la-b4", "promptlookup-b4", "noverify-b2", "la-b7-full",
+                              "la-b3-13rows", "greedy-b40"])
 def test_batch_equals_batch1_contexts(mode, WNG, B):
     import lossless_lookahead_decoding_gb300 as LA
     dtype, mflags = MODES[mode]
@@ -85,7 +86,7 @@ def test_batch_equals_batch1_contexts(mode, WNG, B):
     w = I.make_weights(cfg, 0, bf16=dtype == 1)
     flags = mflags | LA.LA_DEBUG_LOGITS | LA.LA_PRESEED_PROMPT
     batched, singles = _pair(cfg, w, dtype, WNG, B, flags, 256)
-    outs = _run(batched, singles, _prompts("tiny", B, cut=3), 12)
+    outs = _run(batched, singles, _prompts("tiny", B, cut=3 if B <= 8 else 0), 12)
     st = batched.stats()
     assert st["steps"] == 12 and st["emitted"] == sum(len(o) for o in outs)
     assert st["rows"] == B * (1 + (WNG[0] + WNG[2]) * (WNG[1] - 1))
@@ -145,6 +146,53 @@ def test_batch_7b_widths_two_layer_slice():
     w = {k: (v[:2] if isinstance(v, list) else v) for k, v in full.items()}
     batched, singles = _pair(cfg, w, 1, (7, 5, 7), 2, LA.LA_DEBUG_LOGITS, 640)
     _run(batched, singles, _prompts("7b", 2, cut=16), 4)
+
+
+@pytest.mark.parametrize("WNG,B", [((0, 2, 0), 8), ((0, 2, 0), 3), ((3, 3, 3), 2)],
+                         ids=["greedy-b8", "greedy-b3", "la-13rows-b2"])
+def test_batch_narrow_attention_7b_widths(WNG, B):
+    """Batches of at most 16 rows per sequence run the attention's narrow
+    instances (at most 8 rows and more CTAs than SMs: 2 warps, three CTAs
+    per SM; otherwise 4 warps, two per SM) at head_dim 128: 470-512-token
+    prompts (two 256-position splits and a tail), every sequence against its
+    batch-1 context (wide instance), bit for bit."""
+    import lossless_lookahead_decoding_gb300 as LA
+    cfg = I.MODELS["7b"].sliced(2)
+    full = I.make_weights(I.MODELS["7b"], 0, bf16=True, layers=[0, 1])
+    w = {k: (v[:2] if isinstance(v, list) else v) for k, v in full.items()}
+    batched, singles = _pair(cfg, w, 1, WNG, B, LA.LA_DEBUG_LOGITS, 640)
+    _run(batched, singles, _prompts("7b", B, cut=16), 3)
+
+
+@pytest.mark.parametrize("B", [3, 24])
+def test_batch_narrow_attention_34b_gqa_greedy(B):
+    """Greedy batches at 34B widths: the narrow instances stack the 8 query
+    heads of a KV head as rows of the 16-row tile (3 sequences: 24 CTAs a
+    split, the 4-warp instance; 24 sequences: 192, the 2-warp one); the
+    first, a middle and the last sequence against batch-1 contexts, bit for
+    bit."""
+    import lossless_lookahead_decoding_gb300 as LA
+    cfg = I.MODELS["34b"].sliced(1)
+    full = I.make_weights(I.MODELS["34b"], 0, bf16=True, layers=[0])
+    w = {k: (v[:1] if isinstance(v, list) else v) for k, v in full.items()}
+    dw = LA.device_weights(cfg, w, LA.LA_BF16)
+    flags = LA.LA_DEBUG_LOGITS
+    prompts = [I.plant_spans(I.zipf_tokens(300 - 7 * b, 4000, 1.2, 21 + b), 16, 6, 22 + b) for b in range(B)]
+    batched = LA.Decoder(cfg, dw, LA.LA_BF16, 0, 2, 0, 384, flags=flags, batch=B)
+    for b, p in enumerate(prompts):
+        batched.prefill_seq(b, p)
+    picks = sorted({0, B // 2, B - 1})
+    singles = {b: LA.Decoder(cfg, dw, LA.LA_BF16, 0, 2, 0, 384, flags=flags) for b in picks}
+    for b, d in singles.items():
+        d.prefill(prompts[b])
+    for _ in range(3):
+        got = batched.step_batch()
+        for b, d in singles.items():
+            assert np.array_equal(got[b], d.step()), b
+            batched.select(b)
+            assert np.array_equal(batched.logits().view(np.uint32), d.logits().view(np.uint32)), b
+    for d in [batched] + list(singles.values()):
+        d.close()
 
 
 def test_batch_34b_widths_gqa_one_layer_slice():
