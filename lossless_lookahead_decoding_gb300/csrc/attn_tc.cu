@@ -412,7 +412,7 @@ struct BSmem {
     // the staged K/V; after the tiles, the same bytes hold the merge's
     // per-slot region-B outputs [128 slots][HD + 4] and split weights [128][kMaxSp]
     static constexpr int kStageBytes = 2 * kStep + 2 * kWin;
-    static constexpr int kMergeBytes = kRows * (HD + 4) * 4 + kRows * kMaxSp * 4;
+    static constexpr int kMergeBytes = kRows * (HD + 4) * 4;  // the slots' region-B outputs
     static constexpr int kArea = kStageBytes > kMergeBytes ? kStageBytes : kMergeBytes;
     static constexpr int kKS = 0;
     static constexpr int kVS = kKS + kStep;
@@ -422,7 +422,7 @@ struct BSmem {
     static constexpr int kBar = kZero + 256;
     static constexpr int kInts = kBar + 64;             // rows per group, slab prefix
     static constexpr int kSlot = kInts + ((2 * kRows + 2) * 4 + 15) / 16 * 16;  // per-slot merge state
-    static constexpr int kBytes = kSlot + 7 * kRows * 4 + 16;
+    static constexpr int kBytes = kSlot + 5 * kRows * 4 + 16;  // row, splits, max, sum; slot list + count
 };
 
 // at most 112 registers a thread: a window CTA (8 warps) then fits on an SM
@@ -667,14 +667,11 @@ __global__ void __maxnreg__(112)
     // every warp is past its tiles: their bytes take the slots' region-B
     // outputs and region A's split weights.
     float* sO = (float*)(sm + L::kKS);            // [slot][HD + 4]
-    float* sW = sO + kRows * (HD + 4);            // [slot][kMaxSp]
     int* sRow = (int*)(sm + L::kSlot);            // row of the slot, -1 if none
     int* sNA = sRow + kRows;                      // region-A splits of the row
     float* sMB = (float*)(sNA + kRows);           // region B's max, sum and weight
     float* sLB = sMB + kRows;
-    float* sWB = sLB + kRows;
-    float* sLs = sWB + kRows;                     // the row's softmax sum over all parts
-    int* sList = (int*)(sLs + kRows);             // slots holding a row, then their count
+    int* sList = (int*)(sLB + kRows);             // slots holding a row, then their count
     __syncthreads();
     if (busy && staged) {
 #pragma unroll
@@ -696,80 +693,117 @@ __global__ void __maxnreg__(112)
         sRow[warp * 16 + lane] = -1;
     }
     if (tid == 0) sList[kRows] = 0;
+    __syncthreads();
+    // the slots holding a row (any order: it only assigns items to threads)
+    if (tid < kRows && sRow[tid] >= 0) sList[atomicAdd(&sList[kRows], 1)] = tid;
     pdl_wait();  // the cache kernel is complete: its split partials are visible
     pdl_trigger();
     __syncthreads();
-    // per slot: the max over the parts, the parts' weights 2^(m - max) and the
-    // softmax sum over region A's splits in ascending order, then region B
+    // Per item (slot, 4 output dims; kIB per thread at a time): the max over
+    // region B and every split, the splits' weights 2^(m - max) and the
+    // softmax sum in ascending split order then region B, and O = sum over
+    // splits (ascending) of w O_split + wB O_B; out = O / sum.  The (max,
+    // sum) pairs of the first kMB splits and the outputs of the first kSB
+    // splits are loaded together, so one round trip to L2 serves most rows;
+    // the weights of later splits are read again where they are used.
     const size_t pstride = (size_t)kRows * (HD + 4);  // from one split's partial to the next
-    if (tid < kRows) {
-        const int slot = tid, r = sRow[slot];
-        if (r >= 0) {
-            const int nA = sNA[slot];
-            const float* pr = part_row<HD>(a, h, 0, r) + HD;
-            // every split's (max, sum) in flight together, then max, weights
-            // and the sum in ascending split order from registers
-            float2 ml[kMaxSp];
-#pragma unroll
-            for (int sp = 0; sp < kMaxSp; sp++)
-                ml[sp] = sp < nA ? __ldcg((const float2*)(pr + sp * pstride)) : make_float2(-INFINITY, 0.f);
-            float M = sMB[slot];
-#pragma unroll
-            for (int sp = 0; sp < kMaxSp; sp++) M = fmaxf(M, ml[sp].x);
-            float Ls = 0.f;
-#pragma unroll
-            for (int sp = 0; sp < kMaxSp; sp++) {
-                if (sp < nA) {
-                    const float w = ex2(ml[sp].x - M);
-                    sW[slot * kMaxSp + sp] = w;
-                    Ls += ml[sp].y * w;
-                }
-            }
-            const float wB = ex2(sMB[slot] - M);
-            sWB[slot] = wB;
-            sLs[slot] = Ls + sLB[slot] * wB;
-            sList[atomicAdd(&sList[kRows], 1)] = slot;
-        }
-    }
-    __syncthreads();
-    // O = sum over splits (ascending) of w O_split, + wB O_B; out = O / sum
-    // Items (slot, 4 output dims), kIB per thread at a time, the loads of
-    // kSB splits of all of them in flight together; each item's sum runs in
-    // ascending split order.
-    constexpr int C4 = HD / 4, kIB = 2, kSB = 4;
+    constexpr int C4 = HD / 4, kIB = 2, kSB = 4, kMB = 8;
     const int n_items = sList[kRows] * C4;
     for (int i0 = tid; i0 < n_items; i0 += kIB * blockDim.x) {
         int slot[kIB], nA[kIB];
-        const float* pr[kIB];
-        float4 acc[kIB];
+        const float *pr[kIB], *pm[kIB];
         int nmax = 0;
 #pragma unroll
         for (int k = 0; k < kIB; k++) {
             const int i = i0 + k * blockDim.x;
-            slot[k] = i < n_items ? sList[i / C4] : 0;
-            nA[k] = i < n_items ? sNA[slot[k]] : 0;
-            pr[k] = part_row<HD>(a, h, 0, i < n_items ? sRow[slot[k]] : 0) + (i % C4) * 4;
-            acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            const bool ok = i < n_items;
+            slot[k] = ok ? sList[i / C4] : 0;
+            nA[k] = ok ? sNA[slot[k]] : 0;
+            pm[k] = part_row<HD>(a, h, 0, ok ? sRow[slot[k]] : 0) + HD;
+            pr[k] = pm[k] - HD + (i % C4) * 4;
             nmax = max(nmax, nA[k]);
         }
-        for (int s0 = 0; s0 < nmax; s0 += kSB) {
-            float4 x[kIB][kSB];
+        float2 ml[kIB][kMB];
+        float4 x[kIB][kSB];
+#pragma unroll
+        for (int k = 0; k < kIB; k++) {
+#pragma unroll
+            for (int j = 0; j < kMB; j++)
+                ml[k][j] = j < nA[k] ? __ldcg((const float2*)(pm[k] + j * pstride)) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+            for (int j = 0; j < kSB; j++)
+                x[k][j] = j < nA[k] ? __ldcg((const float4*)(pr[k] + j * pstride)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float M[kIB], wB[kIB], inv[kIB], w[kIB][kMB];
+        float4 acc[kIB];
+#pragma unroll
+        for (int k = 0; k < kIB; k++) {
+            const bool ok = i0 + k * blockDim.x < n_items;
+            float mx = ok ? sMB[slot[k]] : 0.f;
+#pragma unroll
+            for (int j = 0; j < kMB; j++) mx = fmaxf(mx, ml[k][j].x);
+            for (int sp = kMB; sp < nA[k]; sp++) mx = fmaxf(mx, __ldcg((const float2*)(pm[k] + sp * pstride)).x);
+            M[k] = mx;
+            float Ls = 0.f;
+#pragma unroll
+            for (int j = 0; j < kMB; j++) {
+                w[k][j] = j < nA[k] ? ex2(ml[k][j].x - mx) : 0.f;
+                if (j < nA[k]) Ls += ml[k][j].y * w[k][j];
+            }
+            for (int sp = kMB; sp < nA[k]; sp++) {
+                const float2 v = __ldcg((const float2*)(pm[k] + sp * pstride));
+                Ls += v.y * ex2(v.x - mx);
+            }
+            wB[k] = ok ? ex2(sMB[slot[k]] - mx) : 0.f;
+            inv[k] = ok ? Ls + sLB[slot[k]] * wB[k] : 1.f;
+            acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        // splits 0 .. kMB-1: weights held in registers
+#pragma unroll
+        for (int c = 0; c < kMB / kSB; c++) {
+            if (c * kSB >= nmax) break;
+            if (c > 0) {
+#pragma unroll
+                for (int k = 0; k < kIB; k++)
+#pragma unroll
+                    for (int j = 0; j < kSB; j++)
+                        x[k][j] = c * kSB + j < nA[k] ? __ldcg((const float4*)(pr[k] + (c * kSB + j) * pstride))
+                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
 #pragma unroll
             for (int k = 0; k < kIB; k++)
 #pragma unroll
-                for (int j = 0; j < kSB; j++)
-                    x[k][j] = s0 + j < nA[k] ? __ldcg((const float4*)(pr[k] + (s0 + j) * pstride))
-                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int j = 0; j < kSB; j++) {
+                    if (c * kSB + j < nA[k]) {
+                        const float ww = w[k][c * kSB + j];
+                        acc[k].x += x[k][j].x * ww;
+                        acc[k].y += x[k][j].y * ww;
+                        acc[k].z += x[k][j].z * ww;
+                        acc[k].w += x[k][j].w * ww;
+                    }
+                }
+        }
+        // later splits (long contexts): each weight from its (max, sum) again
+        for (int s0 = kMB; s0 < nmax; s0 += kSB) {
+            float xm[kIB][kSB];
+#pragma unroll
+            for (int k = 0; k < kIB; k++)
+#pragma unroll
+                for (int j = 0; j < kSB; j++) {
+                    const bool in = s0 + j < nA[k];
+                    x[k][j] = in ? __ldcg((const float4*)(pr[k] + (s0 + j) * pstride)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    xm[k][j] = in ? __ldcg(pm[k] + (s0 + j) * pstride) : 0.f;
+                }
 #pragma unroll
             for (int k = 0; k < kIB; k++)
 #pragma unroll
                 for (int j = 0; j < kSB; j++) {
                     if (s0 + j < nA[k]) {
-                        const float w = sW[slot[k] * kMaxSp + s0 + j];
-                        acc[k].x += x[k][j].x * w;
-                        acc[k].y += x[k][j].y * w;
-                        acc[k].z += x[k][j].z * w;
-                        acc[k].w += x[k][j].w * w;
+                        const float ww = ex2(xm[k][j] - M[k]);
+                        acc[k].x += x[k][j].x * ww;
+                        acc[k].y += x[k][j].y * ww;
+                        acc[k].z += x[k][j].z * ww;
+                        acc[k].w += x[k][j].w * ww;
                     }
                 }
         }
@@ -778,10 +812,11 @@ __global__ void __maxnreg__(112)
             const int i = i0 + k * blockDim.x;
             if (i >= n_items) continue;
             const int sl = slot[k], c4 = i % C4, r = sRow[sl];
-            const float wB = sWB[sl], inv = sLs[sl];
             const float4 ob = *(const float4*)(sO + sl * (HD + 4) + c4 * 4);
-            __nv_bfloat162 lo2 = __floats2bfloat162_rn((acc[k].x + ob.x * wB) / inv, (acc[k].y + ob.y * wB) / inv);
-            __nv_bfloat162 hi2 = __floats2bfloat162_rn((acc[k].z + ob.z * wB) / inv, (acc[k].w + ob.w * wB) / inv);
+            __nv_bfloat162 lo2 =
+                __floats2bfloat162_rn((acc[k].x + ob.x * wB[k]) / inv[k], (acc[k].y + ob.y * wB[k]) / inv[k]);
+            __nv_bfloat162 hi2 =
+                __floats2bfloat162_rn((acc[k].z + ob.z * wB[k]) / inv[k], (acc[k].w + ob.w * wB[k]) / inv[k]);
             uint2 u;
             u.x = *reinterpret_cast<uint32_t*>(&lo2);
             u.y = *reinterpret_cast<uint32_t*>(&hi2);
