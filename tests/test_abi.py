@@ -110,3 +110,16 @@ def test_batched_workspace_grows_by_one_sequence_block_per_sequence():
     g1, g2 = LA.la_workspace_bytes_batch(d, 0, 2, 0, 1), LA.la_workspace_bytes_batch(d, 0, 2, 0, 2)
     assert LA.la_workspace_bytes_batch(d, 0, 2, 0, 128) == g1 + 127 * (g2 - g1)
     assert LA.la_workspace_bytes_batch(d, 0, 2, 0, 129) == 0
+
+
+def test_sampling_setters_refuse_a_null_context_on_the_host():
+    """la_set_sampling, la_set_top_k and la_set_top_p check their context
+    before anything else: a NULL context is LA_ERR_ARG with no GPU call."""
+    import lossless_lookahead_decoding_gb300 as LA
+    from helpers import build_lib
+    build_lib()
+    L = LA.lib()
+    assert L.la_set_sampling(None, 0.7, 1) == LA.LA_ERR_ARG
+    assert L.la_set_top_k(None, 5) == LA.LA_ERR_ARG
+    for p in (0.5, 1.0, 0.0, float("nan")):
+        assert L.la_set_top_p(None, p) == LA.LA_ERR_ARG
