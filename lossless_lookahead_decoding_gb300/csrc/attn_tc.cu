@@ -412,7 +412,7 @@ struct BSmem {
     // the staged K/V; after the tiles, the same bytes hold the merge's
     // per-slot region-B outputs [128 slots][HD + 4] and split weights [128][kMaxSp]
     static constexpr int kStageBytes = 2 * kStep + 2 * kWin;
-    static constexpr int kMergeBytes = kRows * (HD + 4) * 4;  // the slots' region-B outputs
+    static constexpr int kMergeBytes = kRows * (HD + 4) * 4 + kRows * kMaxSp * 4;  // region-B outputs, split weights
     static constexpr int kArea = kStageBytes > kMergeBytes ? kStageBytes : kMergeBytes;
     static constexpr int kKS = 0;
     static constexpr int kVS = kKS + kStep;
@@ -422,8 +422,109 @@ struct BSmem {
     static constexpr int kBar = kZero + 256;
     static constexpr int kInts = kBar + 64;             // rows per group, slab prefix
     static constexpr int kSlot = kInts + ((2 * kRows + 2) * 4 + 15) / 16 * 16;  // per-slot merge state
-    static constexpr int kBytes = kSlot + 5 * kRows * 4 + 16;  // row, splits, max, sum; slot list + count
+    static constexpr int kBytes = kSlot + 7 * kRows * 4 + 16;
 };
+
+// The merge's arithmetic, spelled out as IEEE operations so that both merge
+// paths below give a row the same bits: acc += x w per split in ascending
+// order, and out = (acc + wB O_B) / sum, rounded to bf16.
+__device__ __forceinline__ float4 fma4(float4 x, float w, float4 acc)
+{
+    return make_float4(__fmaf_rn(x.x, w, acc.x), __fmaf_rn(x.y, w, acc.y), __fmaf_rn(x.z, w, acc.z),
+                       __fmaf_rn(x.w, w, acc.w));
+}
+
+__device__ __forceinline__ uint2 merge_out(float4 acc, float4 ob, float wB, float inv)
+{
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(__fdiv_rn(__fmaf_rn(ob.x, wB, acc.x), inv),
+                                                    __fdiv_rn(__fmaf_rn(ob.y, wB, acc.y), inv));
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(__fdiv_rn(__fmaf_rn(ob.z, wB, acc.z), inv),
+                                                    __fdiv_rn(__fmaf_rn(ob.w, wB, acc.w), inv));
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&lo);
+    u.y = *reinterpret_cast<const uint32_t*>(&hi);
+    return u;
+}
+
+// The merge for CTAs holding a row with more than 8 region-A splits (long
+// contexts): one thread per slot loads every split's (max, sum) together and
+// puts the max, the splits' weights 2^(m - max) and the softmax sum (ascending
+// split order, then region B) in shared memory; after a barrier the items
+// (slot, 4 output dims; kIB per thread) load kSB splits' outputs at a time
+// and sum them in ascending split order.  out = (O + wB O_B) / sum.
+template <int HD>
+__device__ void merge_long(const TcAttnArgs& a, int h, const float* sO, float* sW, const int* sRow, const int* sNA,
+                           const float* sMB, const float* sLB, float* sWB, float* sLs, const int* sList,
+                           int n_items, size_t pstride)
+{
+    constexpr int C4 = HD / 4, kIB = 2, kSB = 4;
+    const int tid = threadIdx.x, dq = a.H * HD;
+    if (tid < kRows && sRow[tid] >= 0) {
+        const int slot = tid, nA = sNA[slot];
+        const float* pr = part_row<HD>(a, h, 0, sRow[slot]) + HD;
+        float2 ml[kMaxSp];
+#pragma unroll
+        for (int sp = 0; sp < kMaxSp; sp++)
+            ml[sp] = sp < nA ? __ldcg((const float2*)(pr + sp * pstride)) : make_float2(-INFINITY, 0.f);
+        float M = sMB[slot];
+#pragma unroll
+        for (int sp = 0; sp < kMaxSp; sp++) M = fmaxf(M, ml[sp].x);
+        float Ls = 0.f;
+#pragma unroll
+        for (int sp = 0; sp < kMaxSp; sp++) {
+            if (sp < nA) {
+                const float w = ex2(ml[sp].x - M);
+                sW[slot * kMaxSp + sp] = w;
+                Ls = __fmaf_rn(ml[sp].y, w, Ls);
+            }
+        }
+        const float wB = ex2(sMB[slot] - M);
+        sWB[slot] = wB;
+        sLs[slot] = __fmaf_rn(sLB[slot], wB, Ls);
+    }
+    __syncthreads();
+    for (int i0 = tid; i0 < n_items; i0 += kIB * blockDim.x) {
+        int slot[kIB], nA[kIB];
+        const float* pr[kIB];
+        float4 acc[kIB];
+        int nmax = 0;
+#pragma unroll
+        for (int k = 0; k < kIB; k++) {
+            const int i = i0 + k * blockDim.x;
+            slot[k] = i < n_items ? sList[i / C4] : 0;
+            nA[k] = i < n_items ? sNA[slot[k]] : 0;
+            pr[k] = part_row<HD>(a, h, 0, i < n_items ? sRow[slot[k]] : 0) + (i % C4) * 4;
+            acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            nmax = max(nmax, nA[k]);
+        }
+        for (int s0 = 0; s0 < nmax; s0 += kSB) {
+            float4 x[kIB][kSB];
+#pragma unroll
+            for (int k = 0; k < kIB; k++)
+#pragma unroll
+                for (int j = 0; j < kSB; j++)
+                    x[k][j] = s0 + j < nA[k] ? __ldcg((const float4*)(pr[k] + (s0 + j) * pstride))
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < kIB; k++)
+#pragma unroll
+                for (int j = 0; j < kSB; j++) {
+                    if (s0 + j < nA[k]) {
+                        const float w = sW[slot[k] * kMaxSp + s0 + j];
+                        acc[k] = fma4(x[k][j], w, acc[k]);
+                    }
+                }
+        }
+#pragma unroll
+        for (int k = 0; k < kIB; k++) {
+            const int i = i0 + k * blockDim.x;
+            if (i >= n_items) continue;
+            const int sl = slot[k], c4 = i % C4, r = sRow[sl];
+            const float4 ob = *(const float4*)(sO + sl * (HD + 4) + c4 * 4);
+            *(uint2*)(a.out + (size_t)r * dq + h * HD + c4 * 4) = merge_out(acc[k], ob, sWB[sl], sLs[sl]);
+        }
+    }
+}
 
 // at most 112 registers a thread: a window CTA (8 warps) then fits on an SM
 // beside a cache CTA (10 warps at 96 registers) -- each of the SM's four
@@ -671,7 +772,10 @@ __global__ void __maxnreg__(112)
     int* sNA = sRow + kRows;                      // region-A splits of the row
     float* sMB = (float*)(sNA + kRows);           // region B's max, sum and weight
     float* sLB = sMB + kRows;
-    int* sList = (int*)(sLB + kRows);             // slots holding a row, then their count
+    float* sWB = sLB + kRows;                     // long contexts: region B's weight and
+    float* sLs = sWB + kRows;                     // the row's softmax sum over all parts
+    float* sW = sO + kRows * (HD + 4);            // ... and the splits' weights [slot][kMaxSp]
+    int* sList = (int*)(sLs + kRows);             // slots holding a row, their count, a long-context flag
     __syncthreads();
     if (busy && staged) {
 #pragma unroll
@@ -692,23 +796,32 @@ __global__ void __maxnreg__(112)
     } else if (lane < 16) {
         sRow[warp * 16 + lane] = -1;
     }
-    if (tid == 0) sList[kRows] = 0;
+    constexpr int C4 = HD / 4, kIB = 2, kSB = 4, kMB = 8;
+    if (tid == 0) {
+        sList[kRows] = 0;
+        sList[kRows + 1] = 0;
+    }
     __syncthreads();
     // the slots holding a row (any order: it only assigns items to threads)
-    if (tid < kRows && sRow[tid] >= 0) sList[atomicAdd(&sList[kRows], 1)] = tid;
+    if (tid < kRows && sRow[tid] >= 0) {
+        sList[atomicAdd(&sList[kRows], 1)] = tid;
+        if (sNA[tid] > kMB) sList[kRows + 1] = 1;
+    }
     pdl_wait();  // the cache kernel is complete: its split partials are visible
     pdl_trigger();
     __syncthreads();
-    // Per item (slot, 4 output dims; kIB per thread at a time): the max over
-    // region B and every split, the splits' weights 2^(m - max) and the
-    // softmax sum in ascending split order then region B, and O = sum over
-    // splits (ascending) of w O_split + wB O_B; out = O / sum.  The (max,
-    // sum) pairs of the first kMB splits and the outputs of the first kSB
-    // splits are loaded together, so one round trip to L2 serves most rows;
-    // the weights of later splits are read again where they are used.
     const size_t pstride = (size_t)kRows * (HD + 4);  // from one split's partial to the next
-    constexpr int C4 = HD / 4, kIB = 2, kSB = 4, kMB = 8;
     const int n_items = sList[kRows] * C4;
+    if (sList[kRows + 1]) {
+        merge_long<HD>(a, h, sO, sW, sRow, sNA, sMB, sLB, sWB, sLs, sList, n_items, pstride);
+        return;
+    }
+    // Rows of at most kMB splits: per item (slot, 4 output dims; kIB per
+    // thread at a time) the max over region B and every split, the splits'
+    // weights 2^(m - max) and the softmax sum in ascending split order then
+    // region B, and O = sum over splits (ascending) of w O_split + wB O_B;
+    // out = O / sum.  Every split's (max, sum) and the first kSB splits'
+    // outputs are loaded together: one round trip to L2 and no barrier.
     for (int i0 = tid; i0 < n_items; i0 += kIB * blockDim.x) {
         int slot[kIB], nA[kIB];
         const float *pr[kIB], *pm[kIB];
@@ -734,7 +847,7 @@ __global__ void __maxnreg__(112)
             for (int j = 0; j < kSB; j++)
                 x[k][j] = j < nA[k] ? __ldcg((const float4*)(pr[k] + j * pstride)) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        float M[kIB], wB[kIB], inv[kIB], w[kIB][kMB];
+        float wB[kIB], inv[kIB], w[kIB][kMB];
         float4 acc[kIB];
 #pragma unroll
         for (int k = 0; k < kIB; k++) {
@@ -742,20 +855,14 @@ __global__ void __maxnreg__(112)
             float mx = ok ? sMB[slot[k]] : 0.f;
 #pragma unroll
             for (int j = 0; j < kMB; j++) mx = fmaxf(mx, ml[k][j].x);
-            for (int sp = kMB; sp < nA[k]; sp++) mx = fmaxf(mx, __ldcg((const float2*)(pm[k] + sp * pstride)).x);
-            M[k] = mx;
             float Ls = 0.f;
 #pragma unroll
             for (int j = 0; j < kMB; j++) {
                 w[k][j] = j < nA[k] ? ex2(ml[k][j].x - mx) : 0.f;
-                if (j < nA[k]) Ls += ml[k][j].y * w[k][j];
-            }
-            for (int sp = kMB; sp < nA[k]; sp++) {
-                const float2 v = __ldcg((const float2*)(pm[k] + sp * pstride));
-                Ls += v.y * ex2(v.x - mx);
+                if (j < nA[k]) Ls = __fmaf_rn(ml[k][j].y, w[k][j], Ls);
             }
             wB[k] = ok ? ex2(sMB[slot[k]] - mx) : 0.f;
-            inv[k] = ok ? Ls + sLB[slot[k]] * wB[k] : 1.f;
+            inv[k] = ok ? __fmaf_rn(sLB[slot[k]], wB[k], Ls) : 1.f;
             acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         // splits 0 .. kMB-1: weights held in registers
@@ -775,35 +882,7 @@ __global__ void __maxnreg__(112)
 #pragma unroll
                 for (int j = 0; j < kSB; j++) {
                     if (c * kSB + j < nA[k]) {
-                        const float ww = w[k][c * kSB + j];
-                        acc[k].x += x[k][j].x * ww;
-                        acc[k].y += x[k][j].y * ww;
-                        acc[k].z += x[k][j].z * ww;
-                        acc[k].w += x[k][j].w * ww;
-                    }
-                }
-        }
-        // later splits (long contexts): each weight from its (max, sum) again
-        for (int s0 = kMB; s0 < nmax; s0 += kSB) {
-            float xm[kIB][kSB];
-#pragma unroll
-            for (int k = 0; k < kIB; k++)
-#pragma unroll
-                for (int j = 0; j < kSB; j++) {
-                    const bool in = s0 + j < nA[k];
-                    x[k][j] = in ? __ldcg((const float4*)(pr[k] + (s0 + j) * pstride)) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    xm[k][j] = in ? __ldcg(pm[k] + (s0 + j) * pstride) : 0.f;
-                }
-#pragma unroll
-            for (int k = 0; k < kIB; k++)
-#pragma unroll
-                for (int j = 0; j < kSB; j++) {
-                    if (s0 + j < nA[k]) {
-                        const float ww = ex2(xm[k][j] - M[k]);
-                        acc[k].x += x[k][j].x * ww;
-                        acc[k].y += x[k][j].y * ww;
-                        acc[k].z += x[k][j].z * ww;
-                        acc[k].w += x[k][j].w * ww;
+                        acc[k] = fma4(x[k][j], w[k][c * kSB + j], acc[k]);
                     }
                 }
         }
@@ -813,14 +892,7 @@ __global__ void __maxnreg__(112)
             if (i >= n_items) continue;
             const int sl = slot[k], c4 = i % C4, r = sRow[sl];
             const float4 ob = *(const float4*)(sO + sl * (HD + 4) + c4 * 4);
-            __nv_bfloat162 lo2 =
-                __floats2bfloat162_rn((acc[k].x + ob.x * wB[k]) / inv[k], (acc[k].y + ob.y * wB[k]) / inv[k]);
-            __nv_bfloat162 hi2 =
-                __floats2bfloat162_rn((acc[k].z + ob.z * wB[k]) / inv[k], (acc[k].w + ob.w * wB[k]) / inv[k]);
-            uint2 u;
-            u.x = *reinterpret_cast<uint32_t*>(&lo2);
-            u.y = *reinterpret_cast<uint32_t*>(&hi2);
-            *(uint2*)(a.out + (size_t)r * dq + h * HD + c4 * 4) = u;
+            *(uint2*)(a.out + (size_t)r * dq + h * HD + c4 * 4) = merge_out(acc[k], ob, wB[k], inv[k]);
         }
     }
 }

@@ -238,3 +238,39 @@ def test_argmax_override_drives_every_acceptance_length(WNG, flags):
     w = _weights(cfg, True)
     seen = _override_replay(cfg, w, *WNG, 40, seed=sum(WNG) + flags, flags=flags)
     assert seen == set(range(1, WNG[1] + 1)), seen  # 1..N tokens per step all occurred
+
+
+@pytest.mark.parametrize("mode", ["bf16", "bf16attntc"])
+def test_row0_logits_equal_greedy_across_the_merge_paths(mode):
+    """Row 0 of every lookahead step (the current token at P) has, bit for
+    bit, the logits the greedy decoder computes at P: here at P = 1049..1120,
+    where the tcgen05 attention's merge takes its long-context path (rows
+    with more than 8 region-A splits of 128 positions, position >= 1071) for
+    CTAs that also hold rows of 8 splits, while greedy decoding of those
+    rows takes the short path; and the default attention across its
+    256-position split boundary at 1024."""
+    import lossless_lookahead_decoding_gb300 as LA
+    dtype, mflags = MODES[mode]
+    cfg = I.MODELS["tiny"]
+    w = _weights(cfg, True)
+    prompt = I.random_prompt(1050, cfg.vocab, 77)
+    la = gpu_decoder(cfg, w, dtype, 15, 5, 15, 1300, flags=mflags | LA.LA_DEBUG_LOGITS)
+    g = gpu_decoder(cfg, w, dtype, 0, 2, 0, 1300, flags=mflags | LA.LA_DEBUG_LOGITS)
+    la.prefill(prompt)
+    g.prefill(prompt)
+    P, row0, toks = len(prompt) - 1, {}, []
+    while P < 1120:
+        emit = la.step()
+        row0[P] = la.logits()[0].copy()
+        toks.extend(emit.tolist())
+        P += len(emit)
+    Pg, gt, checked = len(prompt) - 1, [], 0
+    while Pg < P:
+        e = g.step()
+        if Pg in row0:
+            assert np.array_equal(g.logits()[0].view(np.uint32), row0[Pg].view(np.uint32)), Pg
+            checked += 1
+        gt.extend(e.tolist())
+        Pg += 1
+    assert gt[: len(toks)] == toks[: len(gt)]
+    assert checked >= 20 and any(1053 <= p <= 1070 for p in row0)
