@@ -83,6 +83,8 @@ def parse():
     ap.add_argument("--batch-sweep", action="store_true",
                     help="instead of the benchmark line: one JSON line per (W,N,G,batch) of batched decoding "
                          "(several sequences in one forward pass per step, batch x T <= 128 rows)")
+    ap.add_argument("--batch-only", type=int, default=0,
+                    help="with --batch-sweep: only the points of this many sequences (0: every point)")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the benchmark line: one JSON line per (W,N,G) of a sweep, plus "
                          "the prompt-lookup mode (W=0, G>0, pool seeded from the prompt) and greedy")
@@ -442,6 +444,11 @@ BATCH_SWEEP = [(0, 2, 0, 1), (0, 2, 0, 2), (0, 2, 0, 4), (0, 2, 0, 8), (0, 2, 0,
                (15, 5, 15, 1), (7, 5, 7, 1), (7, 5, 7, 2), (5, 5, 5, 3), (3, 5, 3, 5), (3, 4, 3, 6)]
 
 
+def batch_points(only: int = 0):
+    """The --batch-sweep points, or those of `only` sequences."""
+    return [p for p in BATCH_SWEEP if not only or p[3] == only]
+
+
 def run_batch_sweep(args, rank, world):
     """Batched decoding: per (W, N, G, batch), the step latency and the
     tokens/s of all sequences together (prompts of the workload's recipe,
@@ -457,14 +464,17 @@ def run_batch_sweep(args, rank, world):
     if args.layers:
         cfg = cfg.sliced(args.layers)
     n_steps = args.warmup + args.steps
-    prompts = [I.make_prompt(args.workload, seed=1 + b) for b in range(max(b for *_, b in BATCH_SWEEP))]
+    points = batch_points(getattr(args, "batch_only", 0))
+    if not points:
+        raise SystemExit(f"no --batch-sweep point has {args.batch_only} sequences")
+    prompts = [I.make_prompt(args.workload, seed=1 + b) for b in range(max(b for *_, b in points))]
     max_seq = len(prompts[0]) + n_steps * 8 + 32
     dw = build_model(cfg, LA.LA_BF16)
     ref = LA.Decoder(cfg, dw, LA.LA_BF16, 0, 2, 0, max_seq)
     want = ref.generate(prompts[0], n_steps)  # one token per greedy step: enough for every point
     ref.close()
     lines = []
-    for W, N, G, bsz in BATCH_SWEEP:
+    for W, N, G, bsz in points:
         dec = LA.Decoder(cfg, dw, LA.LA_BF16, W, N, G, max_seq, batch=bsz)
         for b in range(bsz):
             dec.prefill_seq(b, prompts[b])

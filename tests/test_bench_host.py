@@ -88,6 +88,8 @@ def test_batch_sweep_points_fit_one_pass():
     greedy = sorted(b for W, N, G, b in bench.BATCH_SWEEP if W == 0 and G == 0)
     assert greedy[0] == 1 and greedy[-1] == 128
     assert (15, 5, 15, 1) in bench.BATCH_SWEEP
+    assert bench.batch_points(128) == [(0, 2, 0, 128)] and bench.batch_points() == bench.BATCH_SWEEP
+    assert bench.batch_points(2) == [(0, 2, 0, 2), (7, 5, 7, 2)] and bench.batch_points(7) == []
 
 
 def test_attention_choice_of_the_benchmark():
